@@ -1,0 +1,165 @@
+"""Seeded synthetic inputs for chunked gated linear attention.
+
+This module holds no arithmetic of the method itself: it only draws the
+random inputs (numpy ``Generator(PCG64(seed))`` in fp32), rounds them to bf16
+where a workload says so, and lays them out in the token-major buffers of the
+FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths on
+Ascend NPUs" (section "Core design": fixed-capacity buffers of T_max tokens and
+N_max + 1 cu_seqlens entries).  The same arrays feed the CPU oracle and the
+CUDA library, so both see identical rounded values.
+
+Input recipe (one draw per tensor, in this order):
+  q, k   ~ N(0, 1), then L2-normalised over d_k
+  v      ~ N(0, 1)
+  beta   = sigmoid(N(0, 1))                  per token and head
+  g      = -softplus(N(0, 1))                per token and head (GDN) or per key channel (KDA)
+  h0     ~ N(0, 0.1^2) fp32, or zeros
+  do     ~ N(0, 1), dht ~ N(0, 0.1^2)        (backward workloads)
+bf16 tensors (q, k, v, beta, do) are rounded to nearest-even after drawing;
+g, h0 and dht stay fp32.  Rows of the fixed-capacity buffers past the last
+live token are filled with NaN so that any read of them shows up.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+GDN, KDA = 0, 1
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest bf16 (ties to even); NaN stays NaN.
+
+    Returns float32 values that are exactly representable in bf16."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    out = r.view(np.float32).copy()
+    nan = np.isnan(x)
+    out[nan] = np.float32("nan")
+    return out
+
+
+@dataclass
+class Workload:
+    """A named synthetic workload.  Sizes follow the method's own notation."""
+    name: str
+    variant: int                 # GDN or KDA
+    dtype: str                   # "f32" or "bf16": type of q, k, v, beta (and o)
+    H: int
+    K: int
+    V: int
+    lengths: list                # live sequence lengths (may contain zeros)
+    n_max: int                   # cu_seqlens capacity - 1
+    t_max: int                   # token capacity
+    bt: int = 64
+    h0: bool = True
+    backward: bool = False
+    seed: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lengths))
+
+    @property
+    def scale(self) -> float:
+        return float(self.K) ** -0.5
+
+
+def dense(name, variant, dtype, B, T, H, K, V, h0=True, backward=False, seed=0, bt=64):
+    """B equal-length sequences of T tokens (a dense batch is varlen with equal lengths)."""
+    return Workload(name, variant, dtype, H, K, V, [T] * B, B, B * T, bt, h0, backward, seed)
+
+
+def varlen(name, variant, dtype, lengths, n_max, t_max, H, K, V, h0=True, backward=False,
+           seed=0, bt=64):
+    return Workload(name, variant, dtype, H, K, V, list(lengths), n_max, t_max, bt, h0,
+                    backward, seed)
+
+
+def random_lengths(n: int, lo: int, hi: int, seed: int) -> list:
+    """n lengths uniform in [lo, hi] from a seeded PCG64 stream."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return [int(x) for x in rng.integers(lo, hi + 1, size=n)]
+
+
+# The five standard workloads.  Index = seed.
+def standard_workloads():
+    return [
+        dense("gdn_fwd_fp32_T256_H2_d64", GDN, "f32", 1, 256, 2, 64, 64, h0=False, seed=0),
+        dense("gdn_fwd_bf16_T4096_H16_d128", GDN, "bf16", 1, 4096, 16, 128, 128, seed=1),
+        dense("kda_fwd_bf16_T2048_H10_d128", KDA, "bf16", 1, 2048, 10, 128, 128, seed=2),
+        varlen("gdn_varlen_bf16_N32_Nmax64_Tmax65536_H16_d128", GDN, "bf16",
+               random_lengths(32, 1, 2048, 30), 64, 65536, 16, 128, 128, seed=3),
+        dense("gdn_fwdbwd_bf16_B4_T8192_H16_d128", GDN, "bf16", 4, 8192, 16, 128, 128,
+              backward=True, seed=4),
+    ]
+
+
+def workload_by_name(name: str) -> Workload:
+    for w in standard_workloads():
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def cu_seqlens_of(w: Workload) -> np.ndarray:
+    """cu_seqlens of shape [n_max + 1]; slots past the live sequences are zero-length."""
+    lens = list(w.lengths) + [0] * (w.n_max - len(w.lengths))
+    cu = np.zeros(w.n_max + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    return cu
+
+
+def make_inputs(w: Workload, seed: int | None = None, pad_value: float = float("nan")):
+    """Draw the inputs of workload ``w``.
+
+    Returns a dict of float32 numpy arrays (bf16-representable where w.dtype is
+    bf16) in fixed-capacity layout: q, k [T_max,H,K]; v [T_max,H,V]; beta [T_max,H];
+    g [T_max,H] or [T_max,H,K]; h0 [N_max,H,K,V] or None; cu_seqlens int32
+    [N_max+1]; and, for backward workloads, do [T_max,H,V] and dht [N_max,H,K,V]."""
+    seed = w.seed if seed is None else seed
+    rng = np.random.Generator(np.random.PCG64(seed))
+    T, Tm, H, K, V = w.total_tokens, w.t_max, w.H, w.K, w.V
+    assert T <= Tm
+
+    def pad(a):
+        out = np.full((Tm,) + a.shape[1:], pad_value, dtype=np.float32)
+        out[:T] = a
+        return out
+
+    def rnd(a):
+        return bf16_round(a) if w.dtype == "bf16" else a.astype(np.float32)
+
+    q = rng.standard_normal((T, H, K), dtype=np.float32)
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((T, H, K), dtype=np.float32)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, V), dtype=np.float32)
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H), dtype=np.float32)))
+    gshape = (T, H, K) if w.variant == KDA else (T, H)
+    g = -np.logaddexp(0.0, rng.standard_normal(gshape, dtype=np.float32)).astype(np.float32)
+    out = dict(q=pad(rnd(q)), k=pad(rnd(k)), v=pad(rnd(v)), beta=pad(rnd(beta)),
+               g=pad(g.astype(np.float32)), cu_seqlens=cu_seqlens_of(w))
+    out["h0"] = ((0.1 * rng.standard_normal((w.n_max, H, K, V), dtype=np.float32))
+                 if w.h0 else None)
+    if w.backward:
+        out["do"] = pad(rnd(rng.standard_normal((T, H, V), dtype=np.float32)))
+        out["dht"] = 0.1 * rng.standard_normal((w.n_max, H, K, V), dtype=np.float32)
+    return out
+
+
+def layout_seeds(w: Workload):
+    """Seeds of the replay layouts of a varlen workload: capture layout, then three replays."""
+    return [w.seed * 10, w.seed * 10 + 1, w.seed * 10 + 2, w.seed * 10 + 3]
+
+
+def varlen_layout(w: Workload, layout_seed: int) -> Workload:
+    """A fresh varlen layout with the same capacities: same sequence count, new lengths."""
+    n = len(w.lengths)
+    hi = w.extra.get("max_len", 2048)
+    lens = random_lengths(n, 1, hi, layout_seed)
+    return varlen(w.name, w.variant, w.dtype, lens, w.n_max, w.t_max, w.H, w.K, w.V, w.h0,
+                  w.backward, seed=layout_seed, bt=w.bt)
