@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""GDN/KDA chunk prefill throughput on GB300: tokens/s and fraction of roofline.
+
+One step = the whole hot path over one batch: chunk_meta_build (device
+metadata from cu_seqlens) followed by the fused chunk forward (and, for the
+forward+backward workload, the backward).  Inputs are seeded synthetic data
+already resident in HBM.  Several input sets are rotated so that the bytes one
+step touches were evicted from L2 by the steps in between (total footprint
+> 3x L2); no explicit flush is needed.
+
+Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (weak scaling: the (sequence, head) units
+are independent, there is no exchange step), timings are max-reduced.
+
+--impl reference times the fp64 CPU oracle instead (rank 0 only) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_gated_linear_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "gdn_fwd_bf16_T4096_H16_d128"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gcl", choices=["gcl", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[w.name for w in synth.standard_workloads()])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- accounting
+def bytes_per_step(w) -> int:
+    """Algorithmic HBM bytes of one forward launch: every input read once, o written once,
+    h0 read and ht written once per (sequence, head)."""
+    b = 2 if w.dtype == "bf16" else 4
+    th = w.total_tokens * w.H
+    per_th = (2 * w.K + 2 * w.V + 1) * b + 4 * (w.K if w.variant == synth.KDA else 1)
+    units = w.n_max * w.H          # ht is written for every sequence slot (ht = h0 if empty)
+    state = w.K * w.V * 4 * ((1 if w.h0 else 0) + 1) * units
+    return th * per_th + state
+
+
+def flops_per_step(w) -> float:
+    """Tensor-core FLOPs of one forward launch (chunk size 64, per token-head):
+    KK^T and QK^T (2 x 2CK), W (2CK), U and L.E (2 x 2CV), WS, QS and the state update
+    (3 x 2KV), solve (2C^2/3)."""
+    C = 64
+    per = 6 * C * w.K + 4 * C * w.V + 6 * w.K * w.V + 2 * C * C / 3
+    return per * w.total_tokens * w.H
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record():
+    """DRAM bytes per launch from the committed ncu summary of the forward kernel, if it was
+    taken on the current kernel source (checked by hash), else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            a, b = line.split(":", 1)
+            kv[a.strip()] = b.strip()
+    src = kv.get("kernel_source")
+    if not src or not os.path.exists(os.path.join(ROOT, src)):
+        return None
+    sha = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+    if sha != kv.get("kernel_source_sha256_16"):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_scaled"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.marks = [None, None]
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def start(self):
+        self.marks[0] = time.time()
+
+    def stop(self):
+        self.marks[1] = time.time()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        t0, t1 = self.marks
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1 + 0.1]
+        if not inside:   # region shorter than the sampling period: nearest samples
+            inside = [s for (t, s) in sorted(self.samples, key=lambda ts: abs(ts[0] - t1))[:2]]
+        if not inside:
+            return None
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class Runner:
+    """Static device buffers for one input set plus prebuilt C-ABI argument structs."""
+
+    def __init__(self, gcl, w, x, dev):
+        import torch
+        self.gcl, self.w = gcl, w
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.t = {}
+        for n in ("q", "k", "v", "beta", "do"):
+            if x.get(n) is not None:
+                self.t[n] = torch.from_numpy(x[n]).to(dev).to(dt).contiguous()
+        for n in ("g", "h0", "dht"):
+            if x.get(n) is not None:
+                self.t[n] = torch.from_numpy(x[n]).to(dev).contiguous()
+        self.t["cu"] = torch.from_numpy(x["cu_seqlens"]).to(dev)
+        ntm = gcl.nt_max(w.t_max, w.n_max, w.bt)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.t["idx"] = torch.empty((ntm, 2), **i32)
+        self.t["off"] = torch.empty((w.n_max + 1,), **i32)
+        self.t["order"] = torch.empty((w.n_max,), **i32)
+        self.t["status"] = torch.zeros((1,), **i32)
+        self.t["o"] = torch.empty((w.t_max, w.H, w.V), dtype=dt, device=dev)
+        self.t["ht"] = torch.empty((w.n_max, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+        if w.backward:
+            self.t["hs"] = torch.empty((ntm, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+            f32 = dict(dtype=torch.float32, device=dev)
+            for n, shp in (("dq", (w.t_max, w.H, w.K)), ("dk", (w.t_max, w.H, w.K)),
+                           ("dv", (w.t_max, w.H, w.V)), ("dg", tuple(x["g"].shape)),
+                           ("dbeta", (w.t_max, w.H)), ("dh0", (w.n_max, w.H, w.K, w.V))):
+                self.t[n] = torch.empty(shp, **f32)
+        t = self.t
+        self.meta_args = (t["cu"].data_ptr(), w.n_max, w.t_max, w.bt, ntm, t["idx"].data_ptr(),
+                          t["off"].data_ptr(), t["order"].data_ptr(), t["status"].data_ptr())
+        self.fwd_args = gcl.fwd_args(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], t["o"],
+                                     h0=t.get("h0"), ht=t["ht"], h_save=t.get("hs"),
+                                     chunk_offsets=t["off"], seq_order=t["order"],
+                                     dev_status=t["status"], scale=w.scale)
+        self.fwd = gcl.lib().kda_chunk_fwd if w.variant == synth.KDA else gcl.lib().gdn_chunk_fwd
+        if w.backward:
+            args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], t["cu"], t["idx"],
+                    t["off"], t["dq"], t["dk"], t["dv"], t["dg"], t["dbeta"])
+            kw = dict(h0=t.get("h0"), dht=t.get("dht"), dh0=t["dh0"], h_save=t["hs"],
+                      dev_status=t["status"], scale=w.scale)
+            nb = gcl.bwd_workspace_bytes(*args, **kw)
+            t["ws"] = torch.empty(nb, dtype=torch.uint8, device=dev)
+            self.bwd_args = gcl.bwd_args(*args, workspace=t["ws"], **kw)
+
+    def footprint(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.t.values())
+
+    def meta(self, s):
+        st = self.gcl.lib().chunk_meta_build(*self.meta_args, s)
+        if st:
+            raise RuntimeError(self.gcl.lib().gcl_last_error().decode())
+
+    def forward(self, s):
+        st = self.fwd(ctypes.byref(self.fwd_args), s)
+        if st:
+            raise RuntimeError(self.gcl.lib().gcl_last_error().decode())
+
+    def backward(self, s):
+        st = self.gcl.lib().gdn_chunk_bwd(ctypes.byref(self.bwd_args), s)
+        if st:
+            raise RuntimeError(self.gcl.lib().gcl_last_error().decode())
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    import chunked_gated_linear_gb300 as gcl
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w = synth.workload_by_name(args.workload)
+    x = synth.make_inputs(w, seed=w.seed + 1000 * rank)
+    first = Runner(gcl, w, x, dev)
+    n_sets = max(2, -(-3 * L2_BYTES // max(first.footprint(), 1)))
+    sets = [first] + [Runner(gcl, w, synth.make_inputs(w, seed=w.seed + 1000 * rank + i), dev)
+                      for i in range(1, n_sets)]
+    stream = torch.cuda.current_stream()
+    s = ctypes.c_void_p(stream.cuda_stream)
+
+    def step(r, ev=None):
+        r.meta(s)
+        if ev is not None:
+            ev[0].record(stream)
+        r.forward(s)
+        if ev is not None:
+            ev[1].record(stream)
+        if w.backward:
+            r.backward(s)
+
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize()
+    for r in sets:
+        assert int(r.t["status"].item()) == 0
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        r = sets[i % n_sets]
+        ev_s[i].record(stream)
+        step(r, ev_k[i])
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
+    kern_ms = [a.elapsed_time(b) for a, b in ev_k]
+    region_ms = ev_s[0].elapsed_time(ev_e[-1])
+    tot = torch.tensor([sum(step_ms), sum(kern_ms), region_ms], dtype=torch.float64,
+                       device=dev)
+    if dist is not None:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+    ms_step = float(tot[0]) / K
+    ms_kern = float(tot[1]) / K
+    value = w.total_tokens * world / (ms_step * 1e-3)
+
+    # end-to-end through the C ABI with host buffers: H2D inputs, step, D2H outputs
+    e2e = run_e2e(gcl, w, x, first, stream, s, args.e2e_steps, world, dist)
+    clk = clocks.summary()
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    ab = bytes_per_step(w)
+    achieved = ab / (ms_kern * 1e-3) / 1e9
+    traffic = traffic_record()
+    line = {
+        "metric": "GDN/KDA chunk prefill tokens/s on 1 GB300 and % of roofline (HBM/TC)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded PCG64; q,k L2-normalised N(0,1), v N(0,1), "
+                "beta=sigmoid(N), g=-softplus(N), h0 N(0,0.1^2))",
+        "config": {"workload": w.name, "tokens_per_step": w.total_tokens, "heads": w.H,
+                   "d_k": w.K, "d_v": w.V, "chunk": w.bt, "n_max": w.n_max,
+                   "t_max": w.t_max, "parallelism": f"replicas x{world}",
+                   "l2": f"rotating {n_sets} input sets, {n_sets * first.footprint() / 2**20:.0f} "
+                         f"MiB total (> 3x L2); no flush",
+                   "timed_region_ms": region_ms, "host_wall_ms": wall * 1e3},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "gdn_chunk_fwd" if w.variant == synth.GDN else "kda_chunk_fwd",
+                     "kernel_ms": ms_kern, "algorithmic_bytes_per_launch": ab,
+                     "tensor_flops_per_launch": flops_per_step(w), "peak_source": peak_kind},
+        "e2e": e2e,
+        "gpu_launches": K * (2 + (2 if w.backward else 0)),
+        "clocks": clk,
+    }
+    return line
+
+
+def run_e2e(gcl, w, x, r, stream, s, steps, world, dist):
+    """Same metric through the public C-ABI calls with pinned host buffers: per step the H2D
+    copy of every input, meta + forward, and the D2H copy of o and ht."""
+    import torch
+    names = [n for n in ("q", "k", "v", "g", "beta", "h0", "cu") if n in r.t]
+    host = {n: torch.empty_like(r.t[n], device="cpu").pin_memory() for n in names}
+    for n in names:
+        host[n].copy_(r.t[n])
+    out_h = {n: torch.empty_like(r.t[n], device="cpu").pin_memory() for n in ("o", "ht")}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = sum(out_h[n].numel() * out_h[n].element_size() for n in out_h)
+    times = []
+    for i in range(steps + 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for n in names:
+            r.t[n].copy_(host[n], non_blocking=True)
+        r.meta(s)
+        r.forward(s)
+        if w.backward:
+            r.backward(s)
+        for n in out_h:
+            out_h[n].copy_(r.t[n], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    ms = float(np.mean(times))
+    t = torch.tensor([ms], dtype=torch.float64, device=r.t["q"].device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t[0])
+    return {"value": w.total_tokens * world / (ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, x, heads, tokens):
+    """The oracle on the first `tokens` tokens of every sequence and the first `heads`
+    heads; returns (seconds, token-heads processed)."""
+    import oracle
+    cu = x["cu_seqlens"].astype(np.int64)
+    rows = []
+    new_cu = [0]
+    for n in range(len(cu) - 1):
+        s, e = int(cu[n]), int(min(cu[n + 1], cu[n] + tokens))
+        rows.append(np.arange(s, e))
+        new_cu.append(new_cu[-1] + (e - s))
+    rows = np.concatenate(rows) if rows else np.zeros(0, dtype=np.int64)
+    sl = {n: x[n][rows][:, :heads] for n in ("q", "k", "v", "g", "beta")}
+    h0 = None if x["h0"] is None else x["h0"][:, :heads]
+    t0 = time.perf_counter()
+    oracle.fwd(w.variant, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], h0, new_cu, w.scale)
+    return time.perf_counter() - t0, len(rows) * heads
+
+
+def cpu_baseline(w, x, budget_s=12.0):
+    import oracle
+    heads = w.H
+    dt, th = oracle_sample(w, x, heads, 64)          # calibration
+    rate = th / max(dt, 1e-6)
+    tokens = int(min(max(64, budget_s * rate / max(heads * len(w.lengths), 1)),
+                     max(w.lengths)))
+    dt, th = oracle_sample(w, x, heads, tokens)
+    return {"value": th / w.H / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 token recurrence, first {tokens} tokens of every sequence, all "
+                      f"{heads} heads ({th} token-heads, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    import oracle
+    oracle.build()
+    w = synth.workload_by_name(args.workload)
+    x = synth.make_inputs(w)
+    heads = 1
+    dt, th = oracle_sample(w, x, heads, 64)
+    per_th = dt / max(th, 1)
+    budget = 120.0 / max(args.steps + args.warmup, 1)    # whole run within ~2 minutes
+    tokens = int(min(max(1, budget / per_th / max(len(w.lengths), 1)), max(w.lengths)))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, heads, tokens)
+    times = []
+    th = 0
+    for _ in range(args.steps):
+        dt, th = oracle_sample(w, x, heads, tokens)
+        times.append(dt)
+    sec = float(np.mean(times))
+    value = th / heads / sec / w.H       # tokens/s of the full-head workload
+    sample = (f"fp64 token recurrence on host cores, per step the first {tokens} tokens of "
+              f"every sequence for {heads} of {w.H} heads, scaled to all heads")
+    return {
+        "impl": "reference",
+        "metric": "GDN/KDA chunk prefill tokens/s on 1 GB300 and % of roofline (HBM/TC)",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_step": w.total_tokens, "heads": w.H},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist_
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist_.init_process_group("nccl")
+        dist = dist_
+    line = run_gpu(args, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            w = synth.workload_by_name(args.workload)
+            line["cpu_baseline"] = cpu_baseline(w, synth.make_inputs(w))
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

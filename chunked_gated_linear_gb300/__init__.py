@@ -1,0 +1,179 @@
+"""Python binding of libgcl, the GB300 chunked gated linear attention library.
+
+Argument marshalling only: every entry point forwards torch tensors' device
+pointers and the current CUDA stream to the C ABI declared in
+``include/gcl.h``; all computation happens in the library's CUDA kernels.  The
+library must have been built (``python -m chunked_gated_linear_gb300._build``
+or ``__graft_entry__.build()``); importing this package fails loudly otherwise,
+and there is no other implementation to fall back on.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgcl.so")
+
+GCL_F32, GCL_BF16 = 0, 1
+DEV_STATUS = {0: "ok", 1: "cu_seqlens decreasing", 2: "cu_seqlens[0] != 0",
+              3: "cu_seqlens[N_max] > T_max", 4: "invalid sequence range"}
+CHUNK = 64
+
+
+class GclError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+        self.status = status
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
+                ("cu_seqlens", ctypes.c_void_p), ("chunk_offsets", ctypes.c_void_p),
+                ("seq_order", ctypes.c_void_p), ("o", ctypes.c_void_p), ("ht", ctypes.c_void_p),
+                ("h_save", ctypes.c_void_p), ("dev_status", ctypes.c_void_p),
+                ("t_max", ctypes.c_int64), ("n_max", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("bt", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
+                ("d_o", ctypes.c_void_p), ("dht", ctypes.c_void_p),
+                ("cu_seqlens", ctypes.c_void_p), ("chunk_indices", ctypes.c_void_p),
+                ("chunk_offsets", ctypes.c_void_p), ("h_save", ctypes.c_void_p),
+                ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+                ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p), ("dh0", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("dev_status", ctypes.c_void_p), ("t_max", ctypes.c_int64),
+                ("n_max", ctypes.c_int32), ("H", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("V", ctypes.c_int32), ("bt", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("dtype", ctypes.c_int32)]
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libgcl.so and declare its C signatures."""
+    if not os.path.exists(path):
+        raise ImportError(f"libgcl.so not built at {path}; run chunked_gated_linear_gb300._build")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.gcl_last_error.restype = ctypes.c_char_p
+    lib.gcl_status_string.restype = ctypes.c_char_p
+    lib.gcl_status_string.argtypes = [i32]
+    lib.gcl_nt_max.restype = i64
+    lib.gcl_nt_max.argtypes = [i64, i64, i32]
+    lib.chunk_meta_build.restype = ctypes.c_int
+    lib.chunk_meta_build.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp]
+    for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
+        getattr(lib, fn).restype = ctypes.c_int
+        getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs), vp]
+    lib.gdn_chunk_bwd.restype = ctypes.c_int
+    lib.gdn_chunk_bwd.argtypes = [ctypes.POINTER(BwdArgs), vp]
+    lib.gcl_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.gcl_bwd_workspace_bytes.argtypes = [ctypes.POINTER(BwdArgs)]
+    return lib
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = load_library()
+    return _lib
+
+
+def _p(t):
+    """Device pointer of a tensor (or None)."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libgcl must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return ctypes.c_void_p(stream if isinstance(stream, int) else stream.cuda_stream)
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(fn, st):
+    if st != 0:
+        raise GclError(fn, st, lib().gcl_last_error().decode())
+
+
+def _dtype_of(t):
+    import torch
+    if t.dtype == torch.float32:
+        return GCL_F32
+    if t.dtype == torch.bfloat16:
+        return GCL_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def nt_max(t_max: int, n_max: int, bt: int = CHUNK) -> int:
+    return int(lib().gcl_nt_max(t_max, n_max, bt))
+
+
+def chunk_meta_build(cu_seqlens, t_max, chunk_indices, chunk_offsets, dev_status,
+                     seq_order=None, bt: int = CHUNK, stream=None):
+    n_max = cu_seqlens.shape[0] - 1
+    _check("chunk_meta_build",
+           lib().chunk_meta_build(_p(cu_seqlens), n_max, t_max, bt, chunk_indices.shape[0],
+                                  _p(chunk_indices), _p(chunk_offsets), _p(seq_order),
+                                  _p(dev_status), _stream(stream)))
+
+
+def fwd_args(q, k, v, g, beta, cu_seqlens, o, h0=None, ht=None, h_save=None,
+             chunk_offsets=None, seq_order=None, dev_status=None, scale=None, bt=CHUNK):
+    T, H, K = q.shape
+    V = v.shape[-1]
+    a = FwdArgs(q=_p(q), k=_p(k), v=_p(v), g=_p(g), beta=_p(beta), h0=_p(h0),
+                cu_seqlens=_p(cu_seqlens), chunk_offsets=_p(chunk_offsets),
+                seq_order=_p(seq_order), o=_p(o), ht=_p(ht), h_save=_p(h_save),
+                dev_status=_p(dev_status), t_max=T, n_max=cu_seqlens.shape[0] - 1, H=H, K=K,
+                V=V, bt=bt, scale=float(K ** -0.5 if scale is None else scale),
+                dtype=_dtype_of(q))
+    return a
+
+
+def gdn_chunk_fwd(*args, stream=None, **kw):
+    a = fwd_args(*args, **kw)
+    _check("gdn_chunk_fwd", lib().gdn_chunk_fwd(ctypes.byref(a), _stream(stream)))
+
+
+def kda_chunk_fwd(*args, stream=None, **kw):
+    a = fwd_args(*args, **kw)
+    _check("kda_chunk_fwd", lib().kda_chunk_fwd(ctypes.byref(a), _stream(stream)))
+
+
+def bwd_args(q, k, v, g, beta, d_o, cu_seqlens, chunk_indices, chunk_offsets, dq, dk, dv, dg,
+             dbeta, h0=None, dht=None, dh0=None, h_save=None, workspace=None,
+             dev_status=None, scale=None, bt=CHUNK):
+    T, H, K = q.shape
+    V = v.shape[-1]
+    return BwdArgs(q=_p(q), k=_p(k), v=_p(v), g=_p(g), beta=_p(beta), h0=_p(h0), d_o=_p(d_o),
+                   dht=_p(dht), cu_seqlens=_p(cu_seqlens), chunk_indices=_p(chunk_indices),
+                   chunk_offsets=_p(chunk_offsets), h_save=_p(h_save), dq=_p(dq), dk=_p(dk),
+                   dv=_p(dv), dg=_p(dg), dbeta=_p(dbeta), dh0=_p(dh0),
+                   workspace=_p(workspace),
+                   workspace_bytes=0 if workspace is None else workspace.numel()
+                   * workspace.element_size(),
+                   dev_status=_p(dev_status), t_max=T, n_max=cu_seqlens.shape[0] - 1, H=H, K=K,
+                   V=V, bt=bt, scale=float(K ** -0.5 if scale is None else scale),
+                   dtype=_dtype_of(q))
+
+
+def bwd_workspace_bytes(*args, **kw) -> int:
+    a = bwd_args(*args, **kw)
+    return int(lib().gcl_bwd_workspace_bytes(ctypes.byref(a)))
+
+
+def gdn_chunk_bwd(*args, stream=None, **kw):
+    a = bwd_args(*args, **kw)
+    _check("gdn_chunk_bwd", lib().gdn_chunk_bwd(ctypes.byref(a), _stream(stream)))

@@ -1,0 +1,430 @@
+// bwd_simt.cu -- GDN chunk backward on the CUDA cores (fp32 arithmetic).
+//
+// FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths
+// on Ascend NPUs", section "Step 3": the backward path covers recomputation,
+// state, WY, gate and gradient kernels.  Here that is three launches:
+//
+//  1. (only without saved states) the forward kernel recomputes the state
+//     before every chunk, S_n, into the workspace;
+//  2. dstate sweep: per (sequence, head, value-column slice), in reverse chunk
+//     order, the gradient w.r.t. the state after chunk n, dS'_n, is saved and
+//     carried back through the chunk:
+//        dE = L^T dO + Ktil dS'
+//        dS = Gamma_c dS' + Qhat^T dO - W^T dE        (dS'_{n-1} = dS)
+//     with Qhat = scale diag(Gamma) Q, Ktil = diag(exp(gamma_c - gamma)) K;
+//     the last dS is dh0.  It needs no forward state.
+//  3. chunk gradients, one CTA per row of chunk_indices (sentinel rows exit):
+//     with S = S_n, dS' = dS'_n, R = diag(beta)(V - diag(Gamma) K S), E = T R,
+//        dVb = T^T dE,  dv = diag(beta) dVb,   dT = dE R^T,   dL = dO E^T,
+//        dA  = -T^T dT T^T (strictly lower),
+//        dq  = scale diag(Gamma) dO S^T + P K,            P = scale e^{g_r-g_i} dL
+//        dk  = diag(e^{g_c-g}) E dS'^T - diag(beta Gamma) dVb S^T
+//              + P^T Q + M K + M^T K,                      M = dA beta_r e^{g_r-g_i}
+//        dbeta, dgamma from every beta, Gamma, Gamma_c and exp(gamma_r - gamma_i)
+//        factor, dg = reverse cumsum of dgamma inside the chunk.
+//     The value dimension is walked in slices of VS columns; products that sum
+//     over it accumulate in registers (dq, dk partials) and shared memory
+//     (dT, dL, row sums), always in a fixed order, so results are bitwise
+//     reproducible (no atomics).
+#include "simt_map.cuh"
+
+namespace gcl {
+namespace {
+
+constexpr int C = kChunk;
+
+// ---------------------------------------------------------------- dstate sweep
+constexpr int kSweepThreads = 256;
+
+template <int K, int VS, int VAR>
+struct SweepLayout {
+    static constexpr int LK = K + 1, LV = VS + 1;
+    static constexpr int oQ = 0, oK = oQ + C * LK, oW = oK + C * LK;
+    static constexpr int oDO = oW + C * LK, oDE = oDO + C * LV, oDS = oDE + C * LV;
+    static constexpr int oA = oDS + K * LV, oT = oA + C * kLC, oL = oT + C * kLC;
+    static constexpr int oB = oL + C * kLC, oG = oB + C;
+    static constexpr int total = oG + (VAR == kKDA ? C * LK : C);
+    static constexpr size_t bytes = sizeof(float) * total;
+};
+
+template <int VAR, typename Tin, int K, int VS>
+__global__ void __launch_bounds__(kSweepThreads)
+dstate_sweep_kernel(BwdParams p) {
+    using Lay = SweepLayout<K, VS, VAR>;
+    extern __shared__ float sm[];
+    float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sW = sm + Lay::oW;
+    float *sDO = sm + Lay::oDO, *sDE = sm + Lay::oDE, *sDS = sm + Lay::oDS;
+    float *sA = sm + Lay::oA, *sT = sm + Lay::oT, *sL = sm + Lay::oL;
+    float *sB = sm + Lay::oB, *sG = sm + Lay::oG;
+    constexpr int LK = Lay::LK, LV = Lay::LV;
+
+    if (status_blocks(p.dev_status)) return;
+    const int tid = threadIdx.x;
+    const int v0 = blockIdx.x * VS, h = blockIdx.y, n = blockIdx.z;
+    const int H = p.H, V = p.V;
+    const int64_t bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+    if (bos < 0 || eos < bos || eos > p.t_max) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *beta = static_cast<const Tin *>(p.beta);
+    const Tin *d_o = static_cast<const Tin *>(p.d_o);
+    const int64_t KV = (int64_t)K * V;
+    const int64_t state_base = ((int64_t)n * H + h) * KV;
+
+    for (int e = tid; e < K * VS; e += kSweepThreads) {
+        const int c = e / VS, j = e % VS;
+        sDS[c * LV + j] = p.dht ? p.dht[state_base + (int64_t)c * V + v0 + j] : 0.f;
+    }
+    const int nchunks = (int)((eos - bos + C - 1) / C);
+    for (int ic = nchunks - 1; ic >= 0; --ic) {
+        const int64_t t0 = bos + (int64_t)ic * C;
+        const int len = (int)(eos - t0 < C ? eos - t0 : C);
+        __syncthreads();
+        {   // dS' of this chunk: gradient w.r.t. the state after it
+            const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+            float *dst = p.dh + (row * H + h) * KV;
+            for (int e = tid; e < K * VS; e += kSweepThreads) {
+                const int c = e / VS, j = e % VS;
+                dst[(int64_t)c * V + v0 + j] = sDS[c * LV + j];
+            }
+        }
+        simt_load_chunk<VAR, Tin, K, kSweepThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG,
+                                                    sB);
+        for (int e = tid; e < C * VS; e += kSweepThreads) {
+            const int r = e / VS, j = e % VS;
+            sDO[r * LV + j] = r < len ? ld_in(d_o, ((t0 + r) * H + h) * (int64_t)V + v0 + j) : 0.f;
+        }
+        __syncthreads();
+        simt_gate_cumsum<VAR, K, kSweepThreads>(sG);
+        __syncthreads();
+        simt_intra<VAR, K, kSweepThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+        __syncthreads();
+        simt_solve<kSweepThreads>(sA, sT);
+        simt_w<VAR, K, kSweepThreads>(sT, sB, sG, sK, sW);
+        // dE = L^T dO + Ktil dS'
+        for (int e = tid; e < C * VS; e += kSweepThreads) {
+            const int i = e / VS, j = e % VS;
+            float acc = 0.f;
+            for (int r = i; r < C; ++r) acc = fmaf(sL[r * kLC + i], sDO[r * LV + j], acc);
+            for (int c = 0; c < K; ++c) {
+                const float kt = expf(gam<VAR, K>(sG, C - 1, c) - gam<VAR, K>(sG, i, c)) *
+                                 sK[i * LK + c];
+                acc = fmaf(kt, sDS[c * LV + j], acc);
+            }
+            sDE[i * LV + j] = acc;
+        }
+        for (int e = tid; e < C * K; e += kSweepThreads) {
+            const int r = e / K, c = e % K;
+            sQ[r * LK + c] *= p.scale * expf(gam<VAR, K>(sG, r, c));
+        }
+        __syncthreads();
+        // dS = Gamma_c dS' + Qhat^T dO - W^T dE   (in place: each element reads only itself)
+        for (int e = tid; e < K * VS; e += kSweepThreads) {
+            const int c = e / VS, j = e % VS;
+            float acc = expf(gam<VAR, K>(sG, C - 1, c)) * sDS[c * LV + j];
+            for (int r = 0; r < C; ++r) {
+                acc = fmaf(sQ[r * LK + c], sDO[r * LV + j], acc);
+                acc = fmaf(-sW[r * LK + c], sDE[r * LV + j], acc);
+            }
+            sDS[c * LV + j] = acc;
+        }
+    }
+    __syncthreads();
+    if (p.dh0) {
+        for (int e = tid; e < K * VS; e += kSweepThreads) {
+            const int c = e / VS, j = e % VS;
+            p.dh0[state_base + (int64_t)c * V + v0 + j] = sDS[c * LV + j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- chunk gradients (GDN)
+constexpr int kGradThreads = 512;
+constexpr int kVS = 16;   // value columns per slice
+
+template <int K>
+struct GradLayout {
+    static constexpr int LK = K + 1, LV = kVS + 1;
+    static constexpr int oQ = 0, oK = oQ + C * LK;
+    static constexpr int oT = oK + C * LK, oL = oT + C * kLC;
+    static constexpr int oDL = oL + C * kLC, oDT = oDL + C * kLC;
+    static constexpr int oB = oDT + C * kLC, oG = oB + C;
+    static constexpr int oRA = oG + C, oRB = oRA + C, oRC = oRB + C, oRD = oRC + C;
+    static constexpr int oDG = oRD + C;                // dgamma per row
+    static constexpr int oRED = oDG + C;               // 32 floats for a block reduction
+    static constexpr int oFree = oRED + 32;            // slice region
+    // slice buffers
+    static constexpr int oS = oFree, oDS = oS + K * LV;
+    static constexpr int oV = oDS + K * LV, oDO = oV + C * LV, oKS = oDO + C * LV;
+    static constexpr int oR = oKS + C * LV, oE = oR + C * LV, oDE = oE + C * LV;
+    static constexpr int oDVB = oDE + C * LV, oX1 = oDVB + C * LV, oX2 = oX1 + C * LV;
+    static constexpr int oFreeEnd = oX2 + C * LV;
+    static_assert(oFreeEnd - oFree >= 2 * C * kLC, "slice region reused for two C x C tiles");
+    static constexpr size_t bytes = sizeof(float) * oFreeEnd;
+};
+
+template <typename Tin, int K>
+__global__ void __launch_bounds__(kGradThreads)
+chunk_grad_kernel(BwdParams p) {
+    using Lay = GradLayout<K>;
+    extern __shared__ float sm[];
+    constexpr int LK = Lay::LK, LV = Lay::LV;
+    constexpr int CPT = K / 8;   // dq/dk columns owned per thread
+    float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sT = sm + Lay::oT, *sL = sm + Lay::oL;
+    float *sDL = sm + Lay::oDL, *sDT = sm + Lay::oDT, *sB = sm + Lay::oB, *sG = sm + Lay::oG;
+    float *sRA = sm + Lay::oRA, *sRB = sm + Lay::oRB, *sRC = sm + Lay::oRC, *sRD = sm + Lay::oRD;
+    float *sDG = sm + Lay::oDG, *sRed = sm + Lay::oRED;
+    float *sS = sm + Lay::oS, *sDS = sm + Lay::oDS, *sV = sm + Lay::oV, *sDO = sm + Lay::oDO;
+    float *sKS = sm + Lay::oKS, *sR = sm + Lay::oR, *sE = sm + Lay::oE, *sDE = sm + Lay::oDE;
+    float *sDVB = sm + Lay::oDVB, *sX1 = sm + Lay::oX1, *sX2 = sm + Lay::oX2;
+    float *sA = sm + Lay::oFree;              // A during the Map; later dT T^T
+    float *sAp = sm + Lay::oFree + C * kLC;   // A' at the end
+
+    if (status_blocks(p.dev_status)) return;
+    const int n = p.chunk_indices[2 * blockIdx.x];
+    if (n < 0) return;                         // sentinel row: nothing to do
+    const int ic = p.chunk_indices[2 * blockIdx.x + 1];
+    const int tid = threadIdx.x, h = blockIdx.y;
+    const int H = p.H, V = p.V;
+    const int64_t bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+    const int64_t t0 = bos + (int64_t)ic * C;
+    if (bos < 0 || eos < bos || eos > p.t_max || t0 >= eos) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int len = (int)(eos - t0 < C ? eos - t0 : C);
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    const Tin *beta = static_cast<const Tin *>(p.beta);
+    const Tin *d_o = static_cast<const Tin *>(p.d_o);
+    const int64_t KV = (int64_t)K * V;
+    const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+    const float *Sg = p.h + (row * H + h) * KV;
+    const float *dSg = p.dh + (row * H + h) * KV;
+
+    // ---- Map recompute
+    simt_load_chunk<kGDN, Tin, K, kGradThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    __syncthreads();
+    simt_gate_cumsum<kGDN, K, kGradThreads>(sG);
+    __syncthreads();
+    simt_intra<kGDN, K, kGradThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    for (int e = tid; e < C * kLC; e += kGradThreads) { sDL[e] = 0.f; sDT[e] = 0.f; }
+    for (int r = tid; r < C; r += kGradThreads) { sRA[r] = sRB[r] = sRC[r] = sRD[r] = 0.f; }
+    __syncthreads();
+    simt_solve<kGradThreads>(sA, sT);
+
+    const float gC = sG[C - 1];
+    const int my_r = tid / 8, my_c0 = tid % 8;    // owner of dq/dk partials
+    float dq_p[CPT], dk_p[CPT];
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) { dq_p[m] = 0.f; dk_p[m] = 0.f; }
+    float dgc_part = 0.f;
+
+    for (int s0 = 0; s0 < V; s0 += kVS) {
+        __syncthreads();
+        for (int e = tid; e < K * kVS; e += kGradThreads) {
+            const int c = e / kVS, j = e % kVS;
+            const float sv = Sg[(int64_t)c * V + s0 + j], dsv = dSg[(int64_t)c * V + s0 + j];
+            sS[c * LV + j] = sv;
+            sDS[c * LV + j] = dsv;
+            dgc_part = fmaf(sv, dsv, dgc_part);
+        }
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int r = e / kVS, j = e % kVS;
+            const int64_t gi = ((t0 + r) * H + h) * (int64_t)V + s0 + j;
+            sV[r * LV + j] = r < len ? ld_in(v, gi) : 0.f;
+            sDO[r * LV + j] = r < len ? ld_in(d_o, gi) : 0.f;
+        }
+        __syncthreads();
+        // KS, R = diag(beta)(V - diag(Gamma) KS), X1 = dO * (Q S), X2 = K dS'
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int r = e / kVS, j = e % kVS;
+            float ks = 0.f, qs = 0.f, kd = 0.f;
+            for (int c = 0; c < K; ++c) {
+                ks = fmaf(sK[r * LK + c], sS[c * LV + j], ks);
+                qs = fmaf(sQ[r * LK + c], sS[c * LV + j], qs);
+                kd = fmaf(sK[r * LK + c], sDS[c * LV + j], kd);
+            }
+            sKS[r * LV + j] = ks;
+            sR[r * LV + j] = sB[r] * (sV[r * LV + j] - expf(sG[r]) * ks);
+            sX1[r * LV + j] = sDO[r * LV + j] * qs;
+            sX2[r * LV + j] = kd;
+        }
+        __syncthreads();
+        // E = T R;  dE = L^T dO + exp(gamma_c - gamma) X2
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int r = e / kVS, j = e % kVS;
+            float ev = 0.f, de = expf(gC - sG[r]) * sX2[r * LV + j];
+            for (int i = 0; i <= r; ++i) ev = fmaf(sT[r * kLC + i], sR[i * LV + j], ev);
+            for (int r2 = r; r2 < C; ++r2) de = fmaf(sL[r2 * kLC + r], sDO[r2 * LV + j], de);
+            sE[r * LV + j] = ev;
+            sDE[r * LV + j] = de;
+        }
+        __syncthreads();
+        // dVb = T^T dE; dv = beta dVb
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int i = e / kVS, j = e % kVS;
+            float acc = 0.f;
+            for (int r = i; r < C; ++r) acc = fmaf(sT[r * kLC + i], sDE[r * LV + j], acc);
+            sDVB[i * LV + j] = acc;
+            if (i < len) p.dv[((t0 + i) * H + h) * (int64_t)V + s0 + j] = sB[i] * acc;
+        }
+        // dL += dO E^T (i <= r);  dT += dE R^T (i <= r)
+        for (int e = tid; e < C * C; e += kGradThreads) {
+            const int r = e / C, i = e % C;
+            if (i <= r) {
+                float dl = 0.f, dt = 0.f;
+                for (int j = 0; j < kVS; ++j) {
+                    dl = fmaf(sDO[r * LV + j], sE[i * LV + j], dl);
+                    dt = fmaf(sDE[r * LV + j], sR[i * LV + j], dt);
+                }
+                sDL[r * kLC + i] += dl;
+                sDT[r * kLC + i] += dt;
+            }
+        }
+        __syncthreads();
+        // register partials: dq_p += dO S^T;  dk_p += e^{g_c-g} E dS'^T - beta Gamma dVb S^T
+        {
+            const float fe = expf(gC - sG[my_r]);
+            const float fb = sB[my_r] * expf(sG[my_r]);
+#pragma unroll
+            for (int m = 0; m < CPT; ++m) {
+                const int c = my_c0 + 8 * m;
+                float aq = dq_p[m], ak = dk_p[m];
+                for (int j = 0; j < kVS; ++j) {
+                    aq = fmaf(sDO[my_r * LV + j], sS[c * LV + j], aq);
+                    ak = fmaf(fe * sE[my_r * LV + j], sDS[c * LV + j], ak);
+                    ak = fmaf(-fb * sDVB[my_r * LV + j], sS[c * LV + j], ak);
+                }
+                dq_p[m] = aq;
+                dk_p[m] = ak;
+            }
+        }
+        // row sums (one thread per row, fixed order)
+        for (int r = tid; r < C; r += kGradThreads) {
+            float a = 0.f, b = 0.f, cc = 0.f, d = 0.f;
+            for (int j = 0; j < kVS; ++j) {
+                a += sX1[r * LV + j];
+                b = fmaf(sDVB[r * LV + j], sV[r * LV + j], b);
+                cc = fmaf(sDVB[r * LV + j], sKS[r * LV + j], cc);
+                d = fmaf(sE[r * LV + j], sX2[r * LV + j], d);
+            }
+            sRA[r] += a; sRB[r] += b; sRC[r] += cc; sRD[r] += d;
+        }
+    }
+    // <dS', S> over the whole state: fixed-order block reduction
+    {
+        float x = dgc_part;
+        for (int d = 16; d > 0; d >>= 1) x += __shfl_xor_sync(0xffffffffu, x, d);
+        if ((tid & 31) == 0) sRed[tid >> 5] = x;
+    }
+    __syncthreads();
+    // dA = -T^T (dT T^T), strictly lower.  X = dT T^T into sA (dT is lower incl. diag).
+    for (int e = tid; e < C * C; e += kGradThreads) {
+        const int r = e / C, m = e % C;
+        float acc = 0.f;
+        for (int i = 0; i <= min(r, m); ++i) acc = fmaf(sDT[r * kLC + i], sT[m * kLC + i], acc);
+        sA[r * kLC + m] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < C * C; e += kGradThreads) {
+        const int r = e / C, i = e % C;
+        float acc = 0.f;
+        if (i < r)
+            for (int m = r; m < C; ++m) acc = fmaf(-sT[m * kLC + r], sA[m * kLC + i], acc);
+        sDT[r * kLC + i] = acc;      // sDT now holds dA
+    }
+    __syncthreads();
+    simt_intra<kGDN, K, kGradThreads>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
+    __syncthreads();
+    const float* sDA = sDT;
+    // dgamma and dbeta, one thread per row
+    for (int r = tid; r < C; r += kGradThreads) {
+        const float gr = sG[r], Gr = expf(gr);
+        float dg = p.scale * Gr * sRA[r];
+        for (int i = 0; i <= r; ++i) dg = fmaf(sDL[r * kLC + i], sL[r * kLC + i], dg);
+        for (int r2 = r; r2 < C; ++r2) dg = fmaf(-sDL[r2 * kLC + r], sL[r2 * kLC + r], dg);
+        float da_row = 0.f;
+        for (int i = 0; i < r; ++i) da_row = fmaf(sDA[r * kLC + i], sAp[r * kLC + i], da_row);
+        dg = fmaf(sB[r], da_row, dg);
+        for (int r2 = r + 1; r2 < C; ++r2)
+            dg = fmaf(-sDA[r2 * kLC + r] * sB[r2], sAp[r2 * kLC + r], dg);
+        dg -= sB[r] * Gr * sRC[r];
+        dg -= expf(gC - gr) * sRD[r];
+        sDG[r] = dg;
+        if (r < len) p.dbeta[(t0 + r) * H + h] = sRB[r] - Gr * sRC[r] + da_row;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // dgamma_c: the Ktil factors and Gamma_c; gamma_c is the last row's gamma
+        float dgc = 0.f;
+        for (int w = 0; w < kGradThreads / 32; ++w) dgc += sRed[w];
+        dgc *= expf(gC);
+        for (int i = 0; i < C; ++i) dgc = fmaf(expf(gC - sG[i]), sRD[i], dgc);
+        sDG[C - 1] += dgc;
+        // dg = reverse cumsum of dgamma
+        float acc = 0.f;
+        for (int r = C - 1; r >= 0; --r) {
+            acc += sDG[r];
+            if (r < len) p.dg[(t0 + r) * H + h] = acc;
+        }
+    }
+    // dq, dk
+    {
+        const int r = my_r;
+        if (r < len) {
+            const float gr = sG[r];
+#pragma unroll
+            for (int m = 0; m < CPT; ++m) {
+                const int c = my_c0 + 8 * m;
+                float aq = p.scale * expf(gr) * dq_p[m];
+                for (int i = 0; i <= r; ++i)
+                    aq = fmaf(p.scale * expf(gr - sG[i]) * sDL[r * kLC + i], sK[i * LK + c], aq);
+                float ak = dk_p[m];
+                for (int r2 = r; r2 < C; ++r2)
+                    ak = fmaf(p.scale * expf(sG[r2] - gr) * sDL[r2 * kLC + r], sQ[r2 * LK + c], ak);
+                for (int i = 0; i < r; ++i)
+                    ak = fmaf(sDA[r * kLC + i] * sB[r] * expf(gr - sG[i]), sK[i * LK + c], ak);
+                for (int r2 = r + 1; r2 < C; ++r2)
+                    ak = fmaf(sDA[r2 * kLC + r] * sB[r2] * expf(sG[r2] - gr), sK[r2 * LK + c], ak);
+                p.dq[((t0 + r) * H + h) * (int64_t)K + c] = aq;
+                p.dk[((t0 + r) * H + h) * (int64_t)K + c] = ak;
+            }
+        }
+    }
+}
+
+template <typename Kern>
+cudaError_t prep(Kern kern, size_t bytes) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename Tin, int K, int VS>
+cudaError_t launch_k(const BwdParams &p, cudaStream_t s) {
+    auto sweep = dstate_sweep_kernel<kGDN, Tin, K, VS>;
+    const size_t sb = SweepLayout<K, VS, kGDN>::bytes;
+    cudaError_t e = prep(sweep, sb);
+    if (e != cudaSuccess) return e;
+    sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto grad = chunk_grad_kernel<Tin, K>;
+    const size_t gb = GradLayout<K>::bytes;
+    if ((e = prep(grad, gb)) != cudaSuccess) return e;
+    grad<<<dim3((unsigned)p.nt_max, p.H), kGradThreads, gb, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, cudaStream_t s) {
+    if (dtype == GCL_BF16)
+        return p.K == 64 ? launch_k<__nv_bfloat16, 64, 64>(p, s)
+                         : launch_k<__nv_bfloat16, 128, 32>(p, s);
+    return p.K == 64 ? launch_k<float, 64, 64>(p, s) : launch_k<float, 128, 32>(p, s);
+}
+
+}  // namespace gcl

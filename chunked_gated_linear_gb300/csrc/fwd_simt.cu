@@ -1,0 +1,183 @@
+// fwd_simt.cu -- fused chunkwise forward on the CUDA cores, all arithmetic in fp32.
+//
+// This kernel serves fp32 inputs (where a 1e-5 relative bound leaves no room
+// for reduced-precision tensor-core operands) and every size the tensor-core
+// kernel does not take.  One CTA owns one (sequence, head, value-column slice):
+// it walks the chunks of its sequence in order and keeps its slice of the
+// state S [K x VS] in shared memory for the whole sequence (HA-NPU paper
+// "Empowering Hybrid Attention Models on NPUs", section 4: head-level mapping
+// with the Map-Reduce-Map pipeline fused on one core; column-wise split of the
+// value dimension, which needs no cross-CTA reduction because column j of S
+// depends only on column j of v and h0).
+//
+// Per chunk of c <= 64 tokens (Map phase in simt_map.cuh):
+//   Map     A, L, T = (I + A)^-1, W = T diag(beta Gamma) K, U = T diag(beta) V
+//   Reduce  E = U - W S                                          (state read)
+//   Map     O = scale diag(Gamma) Q S + L E                      (chunk output)
+//   Reduce  S <- Gamma_c S + (diag(exp(gamma_c - gamma)) K)^T E (in-place update)
+// with the per-key-channel gate of KDA in place of the scalar one.  The output
+// is computed from the old state before the update overwrites it (HA-NPU
+// section 5, chunk-first order).  Rows past the end of the sequence are loaded
+// as k = q = v = 0, beta = 0, g = 0, which leaves S unchanged.
+#include "simt_map.cuh"
+
+namespace gcl {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int C = kChunk;
+
+template <int K, int VS, int VAR>
+struct FwdLayout {
+    static constexpr int LK = K + 1;
+    static constexpr int LV = VS + 1;
+    static constexpr int oQ = 0;                     // Q, later scale*Gamma*Q   [C][LK]
+    static constexpr int oK = oQ + C * LK;           // K                        [C][LK]
+    static constexpr int oW = oK + C * LK;           // W                        [C][LK]
+    static constexpr int oV = oW + C * LK;           // V slice                  [C][LV]
+    static constexpr int oE = oV + C * LV;           // E                        [C][LV]
+    static constexpr int oS = oE + C * LV;           // state slice              [K][LV]
+    static constexpr int oA = oS + K * LV;           // A                        [C][kLC]
+    static constexpr int oT = oA + C * kLC;          // T = (I + A)^-1           [C][kLC]
+    static constexpr int oL = oT + C * kLC;          // L                        [C][kLC]
+    static constexpr int oB = oL + C * kLC;          // beta                     [C]
+    static constexpr int oG = oB + C;                // gamma [C] or [C][LK]
+    static constexpr int total = oG + (VAR == kKDA ? C * LK : C);
+    static constexpr size_t bytes = sizeof(float) * total;
+};
+
+template <int VAR, typename Tin, int K, int VS>
+__global__ void __launch_bounds__(kThreads)
+fwd_simt_kernel(FwdParams p) {
+    using Lay = FwdLayout<K, VS, VAR>;
+    extern __shared__ float sm[];
+    float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sW = sm + Lay::oW;
+    float *sV = sm + Lay::oV, *sE = sm + Lay::oE, *sS = sm + Lay::oS;
+    float *sA = sm + Lay::oA, *sT = sm + Lay::oT, *sL = sm + Lay::oL;
+    float *sB = sm + Lay::oB, *sG = sm + Lay::oG;
+    constexpr int LK = Lay::LK, LV = Lay::LV;
+
+    if (status_blocks(p.dev_status)) return;
+    const int tid = threadIdx.x;
+    const int split = blockIdx.x, h = blockIdx.y;
+    const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
+    const int H = p.H, V = p.V;
+    const int v0 = split * VS;
+    const int64_t bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+    if (bos < 0 || eos < bos || eos > p.t_max) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    const Tin *beta = static_cast<const Tin *>(p.beta);
+    Tin *o = static_cast<Tin *>(p.o);
+    const int64_t KV = (int64_t)K * V;
+    const int64_t state_base = ((int64_t)n * H + h) * KV;
+
+    for (int e = tid; e < K * VS; e += kThreads) {
+        const int c = e / VS, j = e % VS;
+        sS[c * LV + j] = p.h0 ? p.h0[state_base + (int64_t)c * V + v0 + j] : 0.f;
+    }
+    const int nchunks = (int)((eos - bos + C - 1) / C);
+    for (int ic = 0; ic < nchunks; ++ic) {
+        const int64_t t0 = bos + (int64_t)ic * C;
+        const int len = (int)(eos - t0 < C ? eos - t0 : C);
+        __syncthreads();   // previous chunk finished with every buffer
+        if (p.h_save) {
+            const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+            float *dst = p.h_save + (row * H + h) * KV;
+            for (int e = tid; e < K * VS; e += kThreads) {
+                const int c = e / VS, j = e % VS;
+                dst[(int64_t)c * V + v0 + j] = sS[c * LV + j];
+            }
+        }
+        simt_load_chunk<VAR, Tin, K, kThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+        for (int e = tid; e < C * VS; e += kThreads) {
+            const int r = e / VS, j = e % VS;
+            sV[r * LV + j] = r < len ? ld_in(v, ((t0 + r) * H + h) * (int64_t)V + v0 + j) : 0.f;
+        }
+        __syncthreads();
+        simt_gate_cumsum<VAR, K, kThreads>(sG);
+        __syncthreads();
+        simt_intra<VAR, K, kThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+        __syncthreads();
+        simt_solve<kThreads>(sA, sT);
+        simt_w<VAR, K, kThreads>(sT, sB, sG, sK, sW);
+        __syncthreads();
+        // E = T diag(beta) V - W S
+        for (int e = tid; e < C * VS; e += kThreads) {
+            const int r = e / VS, j = e % VS;
+            float acc = 0.f;
+            for (int i = 0; i <= r; ++i) acc = fmaf(sT[r * kLC + i] * sB[i], sV[i * LV + j], acc);
+            for (int c = 0; c < K; ++c) acc = fmaf(-sW[r * LK + c], sS[c * LV + j], acc);
+            sE[r * LV + j] = acc;
+        }
+        // Q <- scale Gamma Q (in place; A and L no longer need Q)
+        for (int e = tid; e < C * K; e += kThreads) {
+            const int r = e / K, c = e % K;
+            sQ[r * LK + c] *= p.scale * expf(gam<VAR, K>(sG, r, c));
+        }
+        __syncthreads();
+        // O = (scale Gamma Q) S + L E   (old state: read before the update)
+        if (o != nullptr) {
+            for (int e = tid; e < C * VS; e += kThreads) {
+                const int r = e / VS, j = e % VS;
+                if (r < len) {
+                    float acc = 0.f;
+                    for (int c = 0; c < K; ++c) acc = fmaf(sQ[r * LK + c], sS[c * LV + j], acc);
+                    for (int i = 0; i <= r; ++i) acc = fmaf(sL[r * kLC + i], sE[i * LV + j], acc);
+                    st_out(o, ((t0 + r) * H + h) * (int64_t)V + v0 + j, acc);
+                }
+            }
+        }
+        __syncthreads();
+        // S <- Gamma_c S + (K * exp(gamma_c - gamma))^T E   (in place)
+        for (int e = tid; e < K * VS; e += kThreads) {
+            const int c = e / VS, j = e % VS;
+            const float gC = gam<VAR, K>(sG, C - 1, c);
+            float acc = expf(gC) * sS[c * LV + j];
+            for (int i = 0; i < C; ++i)
+                acc = fmaf(expf(gC - gam<VAR, K>(sG, i, c)) * sK[i * LK + c], sE[i * LV + j], acc);
+            sS[c * LV + j] = acc;
+        }
+    }
+    __syncthreads();
+    if (p.ht) {
+        for (int e = tid; e < K * VS; e += kThreads) {
+            const int c = e / VS, j = e % VS;
+            p.ht[state_base + (int64_t)c * V + v0 + j] = sS[c * LV + j];
+        }
+    }
+}
+
+template <int VAR, typename Tin, int K, int VS>
+cudaError_t launch_one(const FwdParams &p, cudaStream_t s) {
+    using Lay = FwdLayout<K, VS, VAR>;
+    auto kern = fwd_simt_kernel<VAR, Tin, K, VS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay::bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.V / VS, p.H, p.n_max);
+    kern<<<grid, kThreads, Lay::bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int VAR, typename Tin>
+cudaError_t launch_dtype(const FwdParams &p, cudaStream_t s) {
+    if (p.K == 64) return launch_one<VAR, Tin, 64, 64>(p, s);
+    return launch_one<VAR, Tin, 128, 32>(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s) {
+    if (variant == kGDN)
+        return dtype == GCL_BF16 ? launch_dtype<kGDN, __nv_bfloat16>(p, s)
+                                 : launch_dtype<kGDN, float>(p, s);
+    return dtype == GCL_BF16 ? launch_dtype<kKDA, __nv_bfloat16>(p, s)
+                             : launch_dtype<kKDA, float>(p, s);
+}
+
+}  // namespace gcl

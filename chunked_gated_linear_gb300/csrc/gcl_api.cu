@@ -1,0 +1,212 @@
+// gcl_api.cu -- the C ABI: argument checks, launch plans, error reporting.
+//
+// FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths
+// on Ascend NPUs", section "API proposal": externally supplied metadata must
+// match the expected shape and layout, and an unsupported request must fail
+// clearly instead of falling back.  Every check here runs on the host before
+// anything is enqueued; launch shapes depend only on the sizes, never on
+// device data, so each call can be captured in a CUDA graph.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "gcl_internal.cuh"
+
+namespace gcl {
+
+static thread_local char g_err[512];
+
+gcl_status_t fail(gcl_status_t st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+gcl_status_t cuda_check(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return GCL_OK;
+    return fail(GCL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static gcl_status_t check_common(const char *fn, const void *q, const void *k, const void *v,
+                                 const float *g, const void *beta, const int32_t *cu,
+                                 int64_t t_max, int32_t n_max, int32_t H, int32_t K, int32_t V,
+                                 int32_t bt, int32_t dtype) {
+    if (!q || !k || !v || !g || !beta || !cu)
+        return fail(GCL_ERR_INVALID_ARG, "%s: q, k, v, g, beta and cu_seqlens are required", fn);
+    if (t_max < 1 || t_max >= (int64_t(1) << 31) || n_max < 1 || H < 1)
+        return fail(GCL_ERR_INVALID_ARG, "%s: need 1 <= t_max < 2^31, n_max >= 1, H >= 1", fn);
+    if (bt != kChunk)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (this build implements 64)", fn, bt);
+    if ((K != 64 && K != 128) || (V != 64 && V != 128))
+        return fail(GCL_ERR_UNSUPPORTED, "%s: K=%d V=%d (supported: 64 or 128 each)", fn, K, V);
+    if (dtype != GCL_F32 && dtype != GCL_BF16)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: dtype %d (supported: GCL_F32, GCL_BF16)", fn, dtype);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(cu))
+        return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
+    return GCL_OK;
+}
+
+static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int variant) {
+    const char *fn = variant == kGDN ? "gdn_chunk_fwd" : "kda_chunk_fwd";
+    if (!a) return fail(GCL_ERR_INVALID_ARG, "%s: args is NULL", fn);
+    gcl_status_t st = check_common(fn, a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->t_max,
+                                   a->n_max, a->H, a->K, a->V, a->bt, a->dtype);
+    if (st != GCL_OK) return st;
+    if (a->h_save && !a->chunk_offsets)
+        return fail(GCL_ERR_INVALID_ARG, "%s: h_save needs chunk_offsets", fn);
+    if ((a->o && !aligned16(a->o)) || (a->ht && !aligned16(a->ht)) ||
+        (a->h0 && !aligned16(a->h0)) || (a->h_save && !aligned16(a->h_save)))
+        return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
+    FwdParams p{};
+    p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.h0 = a->h0;
+    p.cu_seqlens = a->cu_seqlens; p.chunk_offsets = a->chunk_offsets; p.seq_order = a->seq_order;
+    p.o = a->o; p.ht = a->ht; p.h_save = a->h_save; p.dev_status = a->dev_status;
+    p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V;
+    p.scale = a->scale;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = fwd_tc_supported(variant, a->dtype, a->K, a->V)
+                        ? launch_fwd_tc(p, variant, s)
+                        : launch_fwd_simt(p, variant, a->dtype, s);
+    return cuda_check(e, fn);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static size_t bwd_ws(const gcl_bwd_args *a) {
+    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
+    if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
+    const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
+    return per * (a->h_save ? 1 : 2);
+}
+
+}  // namespace gcl
+
+using namespace gcl;
+
+extern "C" {
+
+const char *gcl_last_error(void) { return g_err; }
+
+const char *gcl_status_string(int32_t s) {
+    switch (s) {
+        case GCL_OK: return "GCL_OK";
+        case GCL_ERR_INVALID_ARG: return "GCL_ERR_INVALID_ARG";
+        case GCL_ERR_UNSUPPORTED: return "GCL_ERR_UNSUPPORTED";
+        case GCL_ERR_CAPACITY: return "GCL_ERR_CAPACITY";
+        case GCL_ERR_CUDA: return "GCL_ERR_CUDA";
+        default: return "unknown";
+    }
+}
+
+int64_t gcl_nt_max(int64_t t_max, int64_t n_max, int32_t bt) {
+    if (t_max <= 0 || n_max <= 0 || bt <= 0) return -1;
+    return (t_max + bt - 1) / bt + n_max - 1;
+}
+
+gcl_status_t chunk_meta_build(const int32_t *cu_seqlens, int32_t n_max, int64_t t_max,
+                              int32_t bt, int64_t nt_max, int32_t *chunk_indices,
+                              int32_t *chunk_offsets, int32_t *seq_order, int32_t *dev_status,
+                              gcl_stream_t stream) {
+    g_err[0] = 0;
+    if (!cu_seqlens || !chunk_indices || !chunk_offsets || !dev_status)
+        return fail(GCL_ERR_INVALID_ARG,
+                    "chunk_meta_build: cu_seqlens, chunk_indices, chunk_offsets, dev_status "
+                    "are required");
+    if (n_max < 1 || t_max < 1 || t_max >= (int64_t(1) << 31) || bt < 1)
+        return fail(GCL_ERR_INVALID_ARG,
+                    "chunk_meta_build: need n_max >= 1, 1 <= t_max < 2^31, bt >= 1");
+    if (nt_max != gcl_nt_max(t_max, n_max, bt))
+        return fail(GCL_ERR_INVALID_ARG, "chunk_meta_build: nt_max=%lld, expected %lld",
+                    (long long)nt_max, (long long)gcl_nt_max(t_max, n_max, bt));
+    return cuda_check(launch_chunk_meta(cu_seqlens, n_max, t_max, bt, nt_max, chunk_indices,
+                                        chunk_offsets, seq_order, dev_status,
+                                        static_cast<cudaStream_t>(stream)),
+                      "chunk_meta_build");
+}
+
+gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream) {
+    g_err[0] = 0;
+    return run_fwd(args, stream, kGDN);
+}
+
+gcl_status_t kda_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream) {
+    g_err[0] = 0;
+    return run_fwd(args, stream, kKDA);
+}
+
+size_t gcl_bwd_workspace_bytes(const gcl_bwd_args *a) {
+    if (!a) return 0;
+    return bwd_ws(a);
+}
+
+gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
+    g_err[0] = 0;
+    const char *fn = "gdn_chunk_bwd";
+    if (!a) return fail(GCL_ERR_INVALID_ARG, "%s: args is NULL", fn);
+    gcl_status_t st = check_common(fn, a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->t_max,
+                                   a->n_max, a->H, a->K, a->V, a->bt, a->dtype);
+    if (st != GCL_OK) return st;
+    if (!a->d_o || !a->chunk_indices || !a->chunk_offsets || !a->dq || !a->dk || !a->dv ||
+        !a->dg || !a->dbeta)
+        return fail(GCL_ERR_INVALID_ARG,
+                    "%s: d_o, chunk_indices, chunk_offsets, dq, dk, dv, dg, dbeta are required",
+                    fn);
+    const size_t need = bwd_ws(a);
+    if (!a->workspace || a->workspace_bytes < need)
+        return fail(GCL_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    if (!aligned16(a->workspace) || !aligned16(a->d_o) || !aligned16(a->dq) ||
+        !aligned16(a->dk) || !aligned16(a->dv) || !aligned16(a->dg) || !aligned16(a->dbeta))
+        return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
+    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
+    const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
+    char *ws = static_cast<char *>(a->workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    BwdParams p{};
+    p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.h0 = a->h0;
+    p.d_o = a->d_o; p.dht = a->dht; p.cu_seqlens = a->cu_seqlens;
+    p.chunk_indices = a->chunk_indices; p.chunk_offsets = a->chunk_offsets;
+    p.dh = reinterpret_cast<float *>(ws);
+    p.dq = a->dq; p.dk = a->dk; p.dv = a->dv; p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->dh0;
+    p.dev_status = a->dev_status;
+    p.t_max = a->t_max; p.nt_max = ntm; p.n_max = a->n_max;
+    p.H = a->H; p.K = a->K; p.V = a->V; p.scale = a->scale;
+    if (a->h_save) {
+        p.h = a->h_save;
+    } else {
+        float *h = reinterpret_cast<float *>(ws + per);
+        FwdParams f{};
+        f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
+        f.cu_seqlens = a->cu_seqlens; f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
+        f.o = nullptr; f.ht = nullptr; f.h_save = h; f.dev_status = a->dev_status;
+        f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
+        f.scale = a->scale;
+        cudaError_t e = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
+                            ? launch_fwd_tc(f, kGDN, s)
+                            : launch_fwd_simt(f, kGDN, a->dtype, s);
+        if ((st = cuda_check(e, "gdn_chunk_bwd (state recompute)")) != GCL_OK) return st;
+        p.h = h;
+    }
+    return cuda_check(launch_bwd_simt(p, a->dtype, s), fn);
+}
+
+}  // extern "C"

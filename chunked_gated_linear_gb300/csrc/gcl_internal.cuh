@@ -1,0 +1,79 @@
+// gcl_internal.cuh -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gcl.h"
+
+namespace gcl {
+
+enum Variant { kGDN = 0, kKDA = 1 };
+constexpr int kChunk = 64;   // BT: tokens per chunk
+
+// Host: record a one-line error for gcl_last_error() and return `st`.
+gcl_status_t fail(gcl_status_t st, const char *fmt, ...);
+gcl_status_t cuda_check(cudaError_t e, const char *what);
+int num_sms();   // SMs of the current device (cached per device)
+
+// Launch parameters of the forward kernels (a resolved copy of gcl_fwd_args).
+struct FwdParams {
+    const void *q, *k, *v;
+    const float *g;
+    const void *beta;
+    const float *h0;
+    const int32_t *cu_seqlens, *chunk_offsets, *seq_order;
+    void *o;
+    float *ht, *h_save;
+    int32_t *dev_status;
+    int64_t t_max;
+    int32_t n_max, H, K, V;
+    float scale;
+};
+
+struct BwdParams {
+    const void *q, *k, *v;
+    const float *g;
+    const void *beta;
+    const float *h0;
+    const void *d_o;
+    const float *dht;
+    const int32_t *cu_seqlens, *chunk_indices, *chunk_offsets;
+    const float *h;       // states before every chunk [nt_max, H, K, V]
+    float *dh;            // state gradients after every chunk [nt_max, H, K, V] (scratch)
+    float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+    int32_t *dev_status;
+    int64_t t_max, nt_max;
+    int32_t n_max, H, K, V;
+    float scale;
+};
+
+// Kernel launchers (return a CUDA error code; no host synchronisation).
+cudaError_t launch_chunk_meta(const int32_t *cu, int32_t n_max, int64_t t_max, int32_t bt,
+                              int64_t nt_max, int32_t *idx, int32_t *off, int32_t *order,
+                              int32_t *status, cudaStream_t s);
+cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s);
+cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s);
+bool fwd_tc_supported(int variant, int dtype, int K, int V);
+cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, cudaStream_t s);
+
+// ---- device helpers -------------------------------------------------------
+__device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_out(float *p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_out(__nv_bfloat16 *p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+// Reads the device status word (if any); true means "do no work".
+__device__ __forceinline__ bool status_blocks(const int32_t *st) {
+    return st != nullptr && *reinterpret_cast<const volatile int32_t *>(st) != 0;
+}
+__device__ __forceinline__ void status_set(int32_t *st, int32_t code) {
+    if (st != nullptr) atomicCAS(st, 0, code);
+}
+
+}  // namespace gcl

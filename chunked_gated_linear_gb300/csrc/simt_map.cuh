@@ -1,0 +1,140 @@
+// simt_map.cuh -- the chunk-local Map phase on the CUDA cores (fp32).
+//
+// Shared by the fp32 forward and the backward kernels.  For one chunk of one
+// (sequence, head) it loads q, k, g, beta (rows r >= len read as zero), forms
+// the in-chunk inclusive cumsum gamma of the log gate (FLA RFC "[RFC] Add
+// Graph Capture Support for FLA Prefill and Training Paths on Ascend NPUs",
+// section "Step 3": gate / chunk cumsum), the decay-weighted matrices
+//   A'[r,i] = exp(gamma_r - gamma_i) (k_r . k_i)            i < r   (A = beta_r A')
+//   L[r,i]  = scale exp(gamma_r - gamma_i) (q_r . k_i)     i <= r
+// ("forward intra": KK^T and QK^T; per key channel for KDA), and
+// T = (I + A)^-1 by row-wise forward substitution ("triangular solve").
+// All decay factors are exp of a non-positive number, so nothing overflows.
+#pragma once
+
+#include "gcl_internal.cuh"
+
+namespace gcl {
+
+constexpr int kC = kChunk;
+constexpr int kLC = kC + 1;
+
+// Shared-memory row strides: +1 float spreads rows over the banks.
+template <int K>
+struct SimtStrides {
+    static constexpr int LK = K + 1;
+};
+
+template <int VAR, typename Tin, int K, int NT>
+__device__ __forceinline__ void simt_load_chunk(const Tin *q, const Tin *k, const float *g,
+                                                const Tin *beta, int64_t t0, int len, int h,
+                                                int H, float *sQ, float *sK, float *sG,
+                                                float *sB) {
+    constexpr int LK = K + 1;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < kC * K; e += NT) {
+        const int r = e / K, c = e % K;
+        const int64_t gi = ((t0 + r) * H + h) * (int64_t)K + c;
+        sQ[r * LK + c] = r < len ? ld_in(q, gi) : 0.f;
+        sK[r * LK + c] = r < len ? ld_in(k, gi) : 0.f;
+        if (VAR == kKDA) sG[r * LK + c] = r < len ? g[gi] : 0.f;
+    }
+    for (int r = tid; r < kC; r += NT) {
+        sB[r] = r < len ? ld_in(beta, (t0 + r) * H + h) : 0.f;
+        if (VAR == kGDN) sG[r] = r < len ? g[(t0 + r) * H + h] : 0.f;
+    }
+}
+
+// gamma: inclusive cumsum of g down the chunk (per key channel for KDA).
+template <int VAR, int K, int NT>
+__device__ __forceinline__ void simt_gate_cumsum(float *sG) {
+    constexpr int LK = K + 1;
+    const int tid = threadIdx.x;
+    if (VAR == kGDN) {
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int r = 0; r < kC; ++r) { acc += sG[r]; sG[r] = acc; }
+        }
+    } else {
+        for (int c = tid; c < K; c += NT) {
+            float acc = 0.f;
+            for (int r = 0; r < kC; ++r) { acc += sG[r * LK + c]; sG[r * LK + c] = acc; }
+        }
+    }
+}
+
+template <int VAR, int K>
+__device__ __forceinline__ float gam(const float *sG, int r, int c) {
+    return VAR == kGDN ? sG[r] : sG[r * (K + 1) + c];
+}
+
+// A (= beta_r A', strictly lower) into sA and L into sL.  If sAp is not null it
+// also receives A' (without beta).
+template <int VAR, int K, int NT>
+__device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, const float *sG,
+                                           const float *sB, float scale, float *sA, float *sL,
+                                           float *sAp) {
+    constexpr int LK = K + 1;
+    for (int e = threadIdx.x; e < kC * kC; e += NT) {
+        const int r = e / kC, i = e % kC;
+        float ap = 0.f, l = 0.f;
+        if (i <= r) {
+            float kk = 0.f, qk = 0.f;
+            if (VAR == kGDN) {
+                for (int c = 0; c < K; ++c) {
+                    kk = fmaf(sK[r * LK + c], sK[i * LK + c], kk);
+                    qk = fmaf(sQ[r * LK + c], sK[i * LK + c], qk);
+                }
+                const float d = expf(sG[r] - sG[i]);
+                kk *= d;
+                qk *= d;
+            } else {
+                for (int c = 0; c < K; ++c) {
+                    const float d = expf(sG[r * LK + c] - sG[i * LK + c]);
+                    kk = fmaf(sK[r * LK + c] * d, sK[i * LK + c], kk);
+                    qk = fmaf(sQ[r * LK + c] * d, sK[i * LK + c], qk);
+                }
+            }
+            ap = (i < r) ? kk : 0.f;
+            l = scale * qk;
+        }
+        if (sA) sA[r * kLC + i] = sB[r] * ap;
+        if (sAp) sAp[r * kLC + i] = ap;
+        if (sL) sL[r * kLC + i] = l;
+    }
+}
+
+// T = (I + A)^-1 for unit lower-triangular I + A:
+//   T[r,r] = 1,  T[r,i] = -A[r,i] - sum_{i<m<r} A[r,m] T[m,i]  (i < r), row by row.
+template <int NT>
+__device__ __forceinline__ void simt_solve(const float *sA, float *sT) {
+    for (int e = threadIdx.x; e < kC * kC; e += NT) {
+        const int r = e / kC, i = e % kC;
+        sT[r * kLC + i] = (r == i) ? 1.f : 0.f;
+    }
+    __syncthreads();
+    for (int r = 1; r < kC; ++r) {
+        for (int i = threadIdx.x; i < r; i += NT) {
+            float acc = -sA[r * kLC + i];
+            for (int m = i + 1; m < r; ++m) acc = fmaf(-sA[r * kLC + m], sT[m * kLC + i], acc);
+            sT[r * kLC + i] = acc;
+        }
+        __syncthreads();
+    }
+}
+
+// W = T diag(beta Gamma) K (GDN) or T diag(beta) (K * Gamma) (KDA).
+template <int VAR, int K, int NT>
+__device__ __forceinline__ void simt_w(const float *sT, const float *sB, const float *sG,
+                                       const float *sK, float *sW) {
+    constexpr int LK = K + 1;
+    for (int e = threadIdx.x; e < kC * K; e += NT) {
+        const int r = e / K, c = e % K;
+        float acc = 0.f;
+        for (int i = 0; i <= r; ++i)
+            acc = fmaf(sT[r * kLC + i] * sB[i] * expf(gam<VAR, K>(sG, i, c)), sK[i * LK + c], acc);
+        sW[r * LK + c] = acc;
+    }
+}
+
+}  // namespace gcl

@@ -1,0 +1,211 @@
+/*
+ * gcl.h -- C ABI of the GB300 chunked gated linear attention library (libgcl).
+ *
+ * The library computes the chunkwise Map-Reduce-Map prefill of two recurrences
+ * over varlen batches addressed by cu_seqlens:
+ *
+ *   GDN  S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *   KDA  S_t = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T
+ *        o_t = S_t^T (scale q_t),  alpha_t = exp(g_t),  a_t = exp(g_t) (per key channel)
+ *
+ * Sources: HA-NPU paper "Empowering Hybrid Attention Models on NPUs"
+ * (section 2.1: fixed-size recurrent state per head, chunkwise Map-Reduce-Map;
+ * section 4: head-level mapping and column-wise split of tail heads;
+ * section 5: chunk-first in-place state update, W = A^-1 K and the grouped
+ * GEMMs KS, QS, KK^T, QK^T) and the FLA RFC "[RFC] Add Graph Capture Support
+ * for FLA Prefill and Training Paths on Ascend NPUs" (section "Core design":
+ * fixed capacity T_max / N_max / BT / NT_max, the [-1, 0] sentinel, device-side
+ * metadata, the static buffer contract; section "API proposal":
+ * max_num_seqs, chunk_indices, chunk_offsets, fail clearly, no silent fallback).
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer named "device" is a CUDA device pointer owned by the caller.
+ *    The library never allocates, frees, synchronises or creates graphs.
+ *  - `stream` is a cudaStream_t passed as an opaque pointer (NULL = legacy
+ *    default stream).  All work is enqueued on it; calls return before the GPU
+ *    finishes.  Launch configurations depend only on the sizes given here, never
+ *    on device data, so every call may be captured into a CUDA graph and
+ *    replayed after the caller updates its buffers in place.
+ *  - Host-checkable errors (NULL where a pointer is required, unsupported sizes
+ *    or dtypes, misaligned pointers) return a non-zero gcl_status_t before any
+ *    work is enqueued; nothing falls back to another implementation.
+ *    gcl_last_error() gives a one-line reason (per calling thread).
+ *  - Data-dependent errors are reported through `dev_status`, a device int32:
+ *    chunk_meta_build writes 0 (ok) or a GCL_DEV_* code; the compute entry
+ *    points read it first and do nothing when it is non-zero.  The caller reads
+ *    it after its own synchronisation.
+ *  - Layouts are token-major and row-major (contiguous):
+ *      q, k [T_max, H, K];  v, o [T_max, H, V];  beta [T_max, H];
+ *      g [T_max, H] (GDN) or [T_max, H, K] (KDA), fp32 log-space gate (<= 0);
+ *      states h0, ht, dht, dh0 [N_max, H, K, V] fp32.
+ *    Token rows at or past cu_seqlens[N_max] are never read or written.
+ */
+#ifndef GCL_H
+#define GCL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gcl_status {
+    GCL_OK = 0,
+    GCL_ERR_INVALID_ARG = 1,   /* NULL pointer, inconsistent or out-of-range size */
+    GCL_ERR_UNSUPPORTED = 2,   /* size, dtype or chunk size this build does not implement */
+    GCL_ERR_CAPACITY = 3,      /* a fixed capacity (workspace, scratch) is too small */
+    GCL_ERR_CUDA = 4           /* a CUDA call failed (message in gcl_last_error) */
+} gcl_status_t;
+
+/* Device status word values (written by chunk_meta_build). */
+#define GCL_DEV_OK 0
+#define GCL_DEV_CU_DECREASING 1    /* cu_seqlens[n+1] < cu_seqlens[n] for some n        */
+#define GCL_DEV_CU_NONZERO_START 2 /* cu_seqlens[0] != 0                                 */
+#define GCL_DEV_CU_OVER_CAPACITY 3 /* cu_seqlens[N_max] > T_max                          */
+#define GCL_DEV_BAD_RANGE 4        /* a compute kernel met an invalid sequence range      */
+
+typedef enum gcl_dtype {
+    GCL_F32 = 0,   /* q, k, v, beta, do, o in fp32; every internal product in fp32     */
+    GCL_BF16 = 1   /* q, k, v, beta, do, o in bf16; state and accumulation in fp32     */
+} gcl_dtype_t;
+
+typedef void *gcl_stream_t;
+
+/* One-line reason for the last non-OK status returned on this thread ("" if none). */
+const char *gcl_last_error(void);
+
+/* Name of a gcl_status_t or GCL_DEV_* value. */
+const char *gcl_status_string(int32_t status);
+
+/*
+ * NT_max = ceil(t_max / bt) + n_max - 1: the most chunks any layout of at most
+ * t_max tokens in at most n_max sequences can have (FLA RFC, "Core design /
+ * Fixed-capacity execution").  Returns -1 for non-positive arguments.
+ */
+int64_t gcl_nt_max(int64_t t_max, int64_t n_max, int32_t bt);
+
+/*
+ * chunk_meta_build -- device-side chunk metadata (FLA RFC, "Core design /
+ * Device-side metadata"; zero-length tail sequences from "Step 1").
+ *
+ *   cu_seqlens     device int32 [n_max + 1], non-decreasing, cu_seqlens[0] = 0,
+ *                  cu_seqlens[n_max] <= t_max; zero-length sequences allowed.
+ *   chunk_indices  device int32 [nt_max, 2] (out): row j = (n, i) for the i-th
+ *                  chunk of sequence n, rows in sequence-major order; rows at or
+ *                  past the live chunk count hold the sentinel [-1, 0].
+ *   chunk_offsets  device int32 [n_max + 1] (out): exclusive prefix sum of the
+ *                  per-sequence chunk counts ceil(len_n / bt); the last entry is
+ *                  the live chunk count.
+ *   seq_order      device int32 [n_max] (out, may be NULL): sequence indices
+ *                  sorted by length, longest first (ties by index); the compute
+ *                  kernels use it to start long sequences first.
+ *   dev_status     device int32 [1] (out): GCL_DEV_OK, or the first failing check
+ *                  in the order NONZERO_START, DECREASING, OVER_CAPACITY.  On
+ *                  failure every row is the sentinel, every offset is 0 and
+ *                  seq_order is the identity, so later kernels do no work.
+ *   nt_max         must equal gcl_nt_max(t_max, n_max, bt).
+ *
+ * One kernel launch; no host synchronisation; graph-capturable.
+ * Host errors: INVALID_ARG for NULL required pointers, n_max < 1, t_max < 1,
+ * t_max >= 2^31, bt < 1 or nt_max mismatch.
+ */
+gcl_status_t chunk_meta_build(const int32_t *cu_seqlens, int32_t n_max, int64_t t_max,
+                              int32_t bt, int64_t nt_max, int32_t *chunk_indices,
+                              int32_t *chunk_offsets, int32_t *seq_order,
+                              int32_t *dev_status, gcl_stream_t stream);
+
+/*
+ * Forward arguments (GDN and KDA).  All pointers are device pointers.
+ */
+typedef struct gcl_fwd_args {
+    const void *q;                 /* [t_max, H, K]  dtype                                   */
+    const void *k;                 /* [t_max, H, K]  dtype                                   */
+    const void *v;                 /* [t_max, H, V]  dtype                                   */
+    const float *g;                /* GDN [t_max, H]; KDA [t_max, H, K]; fp32 log gate <= 0  */
+    const void *beta;              /* [t_max, H]  dtype                                      */
+    const float *h0;               /* [n_max, H, K, V] fp32, or NULL for a zero state        */
+    const int32_t *cu_seqlens;     /* [n_max + 1] int32                                      */
+    const int32_t *chunk_offsets;  /* [n_max + 1] from chunk_meta_build; required iff h_save */
+    const int32_t *seq_order;      /* [n_max] from chunk_meta_build, or NULL (index order)   */
+    void *o;                       /* [t_max, H, V] dtype (out); live rows only; may be NULL */
+    float *ht;                     /* [n_max, H, K, V] fp32 (out) or NULL                    */
+    float *h_save;                 /* [nt_max, H, K, V] fp32 (out) or NULL: the state before */
+                                   /* chunk i of sequence n at row chunk_offsets[n] + i      */
+    int32_t *dev_status;           /* [1] or NULL: no work if non-zero on entry; set to      */
+                                   /* GCL_DEV_BAD_RANGE if a sequence range is invalid       */
+    int64_t t_max;                 /* token capacity of every [t_max, ...] buffer            */
+    int32_t n_max;                 /* sequence capacity (cu_seqlens has n_max + 1 entries)   */
+    int32_t H, K, V;               /* heads, key dim, value dim                              */
+    int32_t bt;                    /* chunk size; 64 in this build                           */
+    float scale;                   /* read-out scale, usually K^-1/2                         */
+    int32_t dtype;                 /* gcl_dtype_t of q, k, v, beta, o                        */
+} gcl_fwd_args;
+
+/*
+ * gdn_chunk_fwd -- gated delta rule prefill: o and ht from q, k, v, g, beta, h0.
+ * kda_chunk_fwd -- the same with the per-key-channel gate of KDA.
+ *
+ * Each (sequence, head) runs the chunkwise Map-Reduce-Map pipeline (HA-NPU
+ * sections 2.1 and 4; FLA RFC "Step 3": gate/chunk cumsum -> intra (KK^T and
+ * triangular solve) -> recompute_w_u -> h -> o) in one fused launch with the
+ * state held on chip; the value dimension of each head may be split across
+ * CTAs (HA-NPU section 4, column-wise split without cross-core reductions).
+ * Zero-length sequences write ht = h0 (or zeros).
+ *
+ * Supported: bt = 64; K, V in {64, 128}; dtype GCL_F32 or GCL_BF16.  bf16
+ * inputs with K = V = 128 run on the tensor cores (tcgen05); everything else
+ * runs the fp32 CUDA-core kernel.  Pointers must be 16-byte aligned.
+ */
+gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
+gcl_status_t kda_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
+
+/*
+ * Backward arguments (GDN).  All pointers are device pointers.
+ */
+typedef struct gcl_bwd_args {
+    const void *q, *k, *v;         /* as in gcl_fwd_args                                     */
+    const float *g;                /* [t_max, H] fp32                                        */
+    const void *beta;              /* [t_max, H] dtype                                       */
+    const float *h0;               /* [n_max, H, K, V] or NULL                               */
+    const void *d_o;               /* [t_max, H, V] dtype: gradient of the loss w.r.t. o     */
+    const float *dht;              /* [n_max, H, K, V] fp32 or NULL: gradient w.r.t. ht      */
+    const int32_t *cu_seqlens;     /* [n_max + 1]                                            */
+    const int32_t *chunk_indices;  /* [nt_max, 2] from chunk_meta_build                      */
+    const int32_t *chunk_offsets;  /* [n_max + 1] from chunk_meta_build                      */
+    const float *h_save;           /* [nt_max, H, K, V] from the forward, or NULL: then the  */
+                                   /* states are recomputed into the workspace              */
+    float *dq, *dk;                /* [t_max, H, K] fp32 (out), live rows                    */
+    float *dv;                     /* [t_max, H, V] fp32 (out)                               */
+    float *dg;                     /* [t_max, H] fp32 (out): w.r.t. the raw log gate g       */
+    float *dbeta;                  /* [t_max, H] fp32 (out)                                  */
+    float *dh0;                    /* [n_max, H, K, V] fp32 (out) or NULL                    */
+    void *workspace;               /* device scratch of gcl_bwd_workspace_bytes() bytes      */
+    size_t workspace_bytes;
+    int32_t *dev_status;           /* as in gcl_fwd_args                                     */
+    int64_t t_max;
+    int32_t n_max, H, K, V, bt;
+    float scale;
+    int32_t dtype;
+} gcl_bwd_args;
+
+/* Bytes of device workspace gdn_chunk_bwd needs for these sizes (depends on whether
+ * h_save is NULL).  Returns 0 for unsupported sizes. */
+size_t gcl_bwd_workspace_bytes(const gcl_bwd_args *args);
+
+/*
+ * gdn_chunk_bwd -- gradients dq, dk, dv, dg, dbeta, dh0 of
+ *   L(o, ht) with upstream gradients d_o and dht,
+ * through the GDN chunk forward (FLA RFC "Step 3": recomputation, state, WY,
+ * gate and gradient kernels).  A reverse sweep over the chunks of each
+ * (sequence, head) carries the state gradient; the per-chunk gradients are then
+ * computed in parallel over chunk_indices, whose sentinel rows exit at once.
+ * Supported sizes as for the forward.
+ */
+gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *args, gcl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCL_H */

@@ -1,0 +1,99 @@
+"""Helpers for the GPU parity tests: move synthetic inputs to the device, call the
+library through its C ABI, and compare against the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import chunked_gated_linear_gb300 as gcl
+import oracle
+from chunked_gated_linear_gb300 import synth
+
+DEV = "cuda:0"
+CANARY = 1536.0          # exact in bf16; written into output padding, must survive every call
+TOL = {"f32": 1e-5, "bf16": 5e-3}   # rel-Frobenius bounds (fp32 inputs / bf16 inputs)
+
+
+def relF(got, want) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    den = np.linalg.norm(want)
+    return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
+
+
+def tdtype(w):
+    return torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+
+def to_device(w, x):
+    """Device tensors for the library: q, k, v, beta, do in the workload dtype; g, h0, dht fp32."""
+    dt = tdtype(w)
+    d = {}
+    for name in ("q", "k", "v", "beta", "do"):
+        if name in x and x[name] is not None:
+            d[name] = torch.from_numpy(x[name]).to(DEV).to(dt).contiguous()
+    for name in ("g", "h0", "dht"):
+        if name in x and x[name] is not None:
+            d[name] = torch.from_numpy(x[name]).to(DEV).contiguous()
+    d["cu_seqlens"] = torch.from_numpy(x["cu_seqlens"].astype(np.int32)).to(DEV)
+    return d
+
+
+class Meta:
+    """Static metadata buffers of one capacity (T_max, N_max, BT)."""
+
+    def __init__(self, t_max, n_max, bt=64):
+        self.t_max, self.n_max, self.bt = t_max, n_max, bt
+        self.nt_max = gcl.nt_max(t_max, n_max, bt)
+        self.idx = torch.full((self.nt_max, 2), 77, dtype=torch.int32, device=DEV)
+        self.off = torch.full((n_max + 1,), 77, dtype=torch.int32, device=DEV)
+        self.order = torch.full((n_max,), 77, dtype=torch.int32, device=DEV)
+        self.status = torch.full((1,), 77, dtype=torch.int32, device=DEV)
+
+    def build(self, cu_dev, stream=None):
+        gcl.chunk_meta_build(cu_dev, self.t_max, self.idx, self.off, self.status,
+                             seq_order=self.order, bt=self.bt, stream=stream)
+
+
+def run_fwd(w, d, meta=None, h_save=False, o_fill=CANARY, use_order=True):
+    """Run chunk_meta_build + the forward for workload w on device inputs d.
+
+    Returns dict of device outputs: o, ht, h_save (if asked), plus meta."""
+    if meta is None:
+        meta = Meta(w.t_max, w.n_max, w.bt)
+        meta.build(d["cu_seqlens"])
+    o = torch.full((w.t_max, w.H, w.V), o_fill, dtype=tdtype(w), device=DEV)
+    ht = torch.full((w.n_max, w.H, w.K, w.V), o_fill, dtype=torch.float32, device=DEV)
+    hs = None
+    if h_save:
+        hs = torch.full((meta.nt_max, w.H, w.K, w.V), o_fill, dtype=torch.float32, device=DEV)
+    fn = gcl.kda_chunk_fwd if w.variant == synth.KDA else gcl.gdn_chunk_fwd
+    fn(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], o, h0=d.get("h0"), ht=ht,
+       h_save=hs, chunk_offsets=meta.off, seq_order=meta.order if use_order else None,
+       dev_status=meta.status, scale=w.scale, bt=w.bt)
+    return dict(o=o, ht=ht, h_save=hs, meta=meta)
+
+
+def oracle_fwd(w, x):
+    return oracle.fwd(w.variant, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                      x["cu_seqlens"], w.scale)
+
+
+def check_fwd(w, x, out, tol=None, label=""):
+    """Compare device outputs against the oracle; check padding canaries."""
+    tol = TOL[w.dtype] if tol is None else tol
+    torch.cuda.synchronize()
+    assert int(out["meta"].status.item()) == 0, "device status " + str(out["meta"].status.item())
+    o_ref, ht_ref = oracle_fwd(w, x)
+    T = w.total_tokens
+    o = out["o"].float().cpu().numpy()
+    ht = out["ht"].cpu().numpy()
+    assert np.isfinite(o[:T]).all(), label + " non-finite o"
+    e_o = relF(o[:T], o_ref[:T])
+    e_h = relF(ht, ht_ref)
+    assert e_o <= tol, f"{label} o rel-Frobenius {e_o:.3e} > {tol}"
+    assert e_h <= tol, f"{label} ht rel-Frobenius {e_h:.3e} > {tol}"
+    if T < w.t_max:
+        pad = o[T:]
+        assert (pad == np.float32(CANARY)).all(), label + " output padding was written"
+    return e_o, e_h

@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/gcl.h declares, and rejects bad arguments before it
+touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_gated_linear_gb300 import _build
+    _build.build()
+    import chunked_gated_linear_gb300 as gcl
+    return gcl.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gcl.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for fn in ("chunk_meta_build", "gdn_chunk_fwd", "kda_chunk_fwd", "gdn_chunk_bwd"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_nt_max_matches_oracle(lib):
+    for t in (1, 63, 64, 65, 4096, 65536):
+        for n in (1, 2, 64):
+            for bt in (16, 32, 64):
+                assert lib.gcl_nt_max(t, n, bt) == oracle.nt_max(t, n, bt)
+    assert lib.gcl_nt_max(0, 1, 64) == -1
+
+
+def test_host_errors_before_any_launch(lib):
+    import chunked_gated_linear_gb300 as gcl
+    INVALID, UNSUPPORTED, CAPACITY = 1, 2, 3
+    # NULL args struct
+    assert lib.gdn_chunk_fwd(None, None) == INVALID
+    assert lib.kda_chunk_fwd(None, None) == INVALID
+    assert lib.gdn_chunk_bwd(None, None) == INVALID
+    # missing required pointers
+    a = gcl.FwdArgs(t_max=128, n_max=1, H=1, K=128, V=128, bt=64, scale=1.0, dtype=1)
+    assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == INVALID
+    assert b"required" in lib.gcl_last_error()
+    fake = 1 << 20   # a 16-byte aligned non-null value; never dereferenced on these paths
+    full = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake, t_max=128,
+                n_max=1, H=1, K=128, V=128, bt=64, scale=1.0, dtype=1)
+    for bad, code in ((dict(bt=32), UNSUPPORTED), (dict(K=96), UNSUPPORTED),
+                      (dict(V=256), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED),
+                      (dict(t_max=0), INVALID), (dict(n_max=0), INVALID),
+                      (dict(q=fake + 4), INVALID), (dict(h_save=fake), INVALID)):
+        args = gcl.FwdArgs(**{**full, **bad})
+        assert lib.gdn_chunk_fwd(ctypes.byref(args), None) == code, bad
+        assert lib.kda_chunk_fwd(ctypes.byref(args), None) == code, bad
+        assert lib.gcl_last_error() != b""
+    # chunk_meta_build: nt_max must match, pointers required
+    assert lib.chunk_meta_build(fake, 4, 256, 64, 7, fake, fake, None, None, None) == INVALID
+    assert lib.chunk_meta_build(fake, 4, 256, 64, 8, fake, fake, None, fake, None) == INVALID
+    assert b"nt_max" in lib.gcl_last_error()
+    # backward: workspace capacity is checked on the host
+    b = gcl.BwdArgs(q=fake, k=fake, v=fake, g=fake, beta=fake, d_o=fake, cu_seqlens=fake,
+                    chunk_indices=fake, chunk_offsets=fake, dq=fake, dk=fake, dv=fake, dg=fake,
+                    dbeta=fake, workspace=fake, workspace_bytes=16, t_max=128, n_max=1, H=1,
+                    K=128, V=128, bt=64, scale=1.0, dtype=1)
+    need = lib.gcl_bwd_workspace_bytes(ctypes.byref(b))
+    assert need >= 2 * 4 * 2 * 128 * 128            # dh and recomputed h for NT_max = 2 chunks
+    assert lib.gdn_chunk_bwd(ctypes.byref(b), None) == CAPACITY
+    b.h_save = fake
+    assert lib.gcl_bwd_workspace_bytes(ctypes.byref(b)) < need
+
+
+def test_status_strings(lib):
+    assert lib.gcl_status_string(0) == b"GCL_OK"
+    assert lib.gcl_status_string(3) == b"GCL_ERR_CAPACITY"

@@ -1,0 +1,93 @@
+"""GDN backward parity against the fp64 reverse-mode oracle."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import oracle  # noqa: E402
+import chunked_gated_linear_gb300 as gcl  # noqa: E402
+from chunked_gated_linear_gb300 import synth  # noqa: E402
+from gpu_util import DEV, TOL, Meta, relF, run_fwd, to_device  # noqa: E402
+
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+def run_bwd(w, d, meta, h_save=None, with_dht=True):
+    T, H, K, V = w.t_max, w.H, w.K, w.V
+    f32 = dict(dtype=torch.float32, device=DEV)
+    out = dict(dq=torch.zeros((T, H, K), **f32), dk=torch.zeros((T, H, K), **f32),
+               dv=torch.zeros((T, H, V), **f32), dg=torch.zeros((T, H), **f32),
+               dbeta=torch.zeros((T, H), **f32), dh0=torch.zeros((w.n_max, H, K, V), **f32))
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["do"], d["cu_seqlens"], meta.idx,
+            meta.off, out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"])
+    kw = dict(h0=d.get("h0"), dht=d["dht"] if with_dht else None, dh0=out["dh0"],
+              h_save=h_save, dev_status=meta.status, scale=w.scale)
+    nbytes = gcl.bwd_workspace_bytes(*args, **kw)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    gcl.gdn_chunk_bwd(*args, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert int(meta.status.item()) == 0
+    return {k_: v_.cpu().numpy() for k_, v_ in out.items()}
+
+
+def oracle_bwd(w, x, with_dht=True):
+    return oracle.bwd(synth.GDN, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"],
+                      x["dht"] if with_dht else None, x["cu_seqlens"], w.scale)
+
+
+def compare(w, got, ref, tol):
+    T = w.total_tokens
+    for key in GRADS:
+        a, b = (got[key], ref[key]) if key == "dh0" else (got[key][:T], ref[key][:T])
+        e = relF(a, b)
+        assert e <= tol, f"{key}: rel-Frobenius {e:.3e} > {tol}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("KV", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("saved", [True, False])
+def test_small_varlen(dtype, KV, saved):
+    K, V = KV
+    lens = [1, 63, 0, 64, 65, 150]
+    w = synth.varlen("bwd", synth.GDN, dtype, lens, 7, sum(lens) + 20, 2, K, V, backward=True,
+                     seed=11)
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    fw = run_fwd(w, d, h_save=saved)
+    got = run_bwd(w, d, fw["meta"], h_save=fw["h_save"])
+    compare(w, got, oracle_bwd(w, x), TOL[dtype])
+
+
+def test_no_dht_no_h0():
+    w = synth.varlen("bwd0", synth.GDN, "bf16", [130, 7], 2, 200, 2, 128, 128, h0=False,
+                     backward=True, seed=12)
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    meta = Meta(w.t_max, w.n_max)
+    meta.build(d["cu_seqlens"])
+    got = run_bwd(w, d, meta, with_dht=False)
+    compare(w, got, oracle_bwd(w, x, with_dht=False), TOL["bf16"])
+
+
+def test_fwd_bwd_full_size_sampled_units():
+    """B=4, T=8192, H=16, d=128, bf16: forward + backward on the GPU at full size; the oracle
+    recomputes sampled (sequence, head) units one by one and every gradient of those units is
+    compared."""
+    w = synth.standard_workloads()[4]
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    fw = run_fwd(w, d, h_save=True)
+    got = run_bwd(w, d, fw["meta"], h_save=fw["h_save"])
+    T = w.lengths[0]
+    for (b, h) in ((0, 0), (2, 7), (3, 15)):
+        s, e = b * T, (b + 1) * T
+        sl = {m: x[m][s:e, h:h + 1] for m in ("q", "k", "v", "g", "beta", "do")}
+        ref = oracle.bwd(synth.GDN, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"],
+                         x["h0"][b:b + 1, h:h + 1], sl["do"], x["dht"][b:b + 1, h:h + 1],
+                         [0, T], w.scale)
+        for key in ("dq", "dk", "dv", "dg", "dbeta"):
+            e_ = relF(got[key][s:e, h:h + 1], ref[key])
+            assert e_ <= TOL["bf16"], f"unit ({b},{h}) {key}: {e_:.3e}"
+        e_ = relF(got["dh0"][b, h], ref["dh0"][0, 0])
+        assert e_ <= TOL["bf16"], f"unit ({b},{h}) dh0: {e_:.3e}"

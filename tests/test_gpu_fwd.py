@@ -1,0 +1,94 @@
+"""Forward parity (GDN and KDA) against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import oracle  # noqa: E402
+from chunked_gated_linear_gb300 import synth  # noqa: E402
+from gpu_util import CANARY, DEV, Meta, TOL, check_fwd, relF, run_fwd, to_device  # noqa: E402
+
+STD = synth.standard_workloads()
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2], ids=[w.name for w in STD[:3]])
+def test_standard_workload_full_size(idx):
+    w = STD[idx]
+    x = synth.make_inputs(w)
+    out = run_fwd(w, to_device(w, x))
+    e_o, e_h = check_fwd(w, x, out, label=w.name)
+    print(f"{w.name}: o {e_o:.2e} ht {e_h:.2e}")
+
+
+CASES = []
+for variant in (synth.GDN, synth.KDA):
+    for dtype in ("f32", "bf16"):
+        for KV in ((64, 64), (128, 128), (64, 128), (128, 64)):
+            CASES.append((variant, dtype, KV))
+
+
+@pytest.mark.parametrize("variant,dtype,KV", CASES,
+                         ids=[f"{'kda' if c[0] else 'gdn'}-{c[1]}-K{c[2][0]}V{c[2][1]}" for c in CASES])
+def test_varlen_ragged_shapes(variant, dtype, KV):
+    """Lengths 1, 63, 64, 65, 200, zero-length in the middle and at the tail, slack in T_max."""
+    K, V = KV
+    lens = [1, 63, 0, 64, 65, 200]
+    w = synth.varlen("ragged", variant, dtype, lens, 8, sum(lens) + 37, 3, K, V, seed=5)
+    x = synth.make_inputs(w)
+    out = run_fwd(w, to_device(w, x), h_save=True)
+    check_fwd(w, x, out, label="ragged")
+    # saved chunk states
+    meta = out["meta"]
+    off = meta.off.cpu().numpy()
+    _, _, hc = oracle.fwd(variant, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                          x["cu_seqlens"], w.scale, bt=64, chunk_offsets=off,
+                          nt_rows=meta.nt_max)
+    live = int(off[-1])
+    hs = out["h_save"].cpu().numpy()
+    assert relF(hs[:live], hc[:live]) <= TOL[dtype]
+    assert (hs[live:] == np.float32(CANARY)).all()      # unused rows untouched
+
+
+@pytest.mark.parametrize("variant", [synth.GDN, synth.KDA])
+def test_zero_initial_state_and_dense_batch(variant):
+    w = synth.dense("dense", variant, "bf16", 3, 300, 2, 128, 128, h0=False, seed=9)
+    x = synth.make_inputs(w)
+    check_fwd(w, x, run_fwd(w, to_device(w, x)), label="dense h0=None")
+
+
+def test_single_token_and_empty_batch():
+    w = synth.varlen("one", synth.GDN, "bf16", [1], 2, 64, 2, 128, 128, seed=4)
+    x = synth.make_inputs(w)
+    check_fwd(w, x, run_fwd(w, to_device(w, x)), label="T=1")
+    # every sequence empty: ht = h0, o untouched
+    w = synth.varlen("empty", synth.GDN, "bf16", [0, 0], 2, 64, 2, 128, 128, seed=4)
+    x = synth.make_inputs(w)
+    out = run_fwd(w, to_device(w, x))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out["ht"].cpu().numpy(), x["h0"])
+    assert (out["o"].float().cpu().numpy() == np.float32(CANARY)).all()
+
+
+def test_deterministic_and_order_independent():
+    w = synth.varlen("det", synth.GDN, "bf16", [300, 5, 700, 64], 6, 1200, 4, 128, 128, seed=6)
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    a = run_fwd(w, d)
+    b = run_fwd(w, d)
+    c = run_fwd(w, d, use_order=False)
+    torch.cuda.synchronize()
+    for key in ("o", "ht"):
+        assert torch.equal(a[key], b[key]) and torch.equal(a[key], c[key]), key
+
+
+def test_invalid_cu_seqlens_do_nothing():
+    w = synth.varlen("bad", synth.GDN, "bf16", [100, 50], 2, 256, 2, 128, 128, seed=7)
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    d["cu_seqlens"] = torch.tensor([0, 100, 60], dtype=torch.int32, device=DEV)   # decreasing
+    out = run_fwd(w, d)
+    torch.cuda.synchronize()
+    assert int(out["meta"].status.item()) == 1
+    assert (out["o"].float().cpu().numpy() == np.float32(CANARY)).all()
+    assert (out["ht"].cpu().numpy() == np.float32(CANARY)).all()
