@@ -85,6 +85,10 @@ dstate_sweep_kernel(BwdParams p) {
         __syncthreads();
         {   // dS' of this chunk: gradient w.r.t. the state after it
             const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+            if (row < 0 || row >= p.nt_max) {      // metadata inconsistent with cu_seqlens
+                if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+                return;
+            }
             float *dst = p.dh + (row * H + h) * KV;
             for (int e = tid; e < K * VS; e += kSweepThreads) {
                 const int c = e / VS, j = e % VS;
@@ -186,6 +190,10 @@ chunk_grad_kernel(BwdParams p) {
     if (status_blocks(p.dev_status)) return;
     const int n = p.chunk_indices[2 * blockIdx.x];
     if (n < 0) return;                         // sentinel row: nothing to do
+    if (n >= p.n_max) {
+        if (threadIdx.x == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
     const int ic = p.chunk_indices[2 * blockIdx.x + 1];
     const int tid = threadIdx.x, h = blockIdx.y;
     const int H = p.H, V = p.V;
@@ -203,6 +211,10 @@ chunk_grad_kernel(BwdParams p) {
     const Tin *d_o = static_cast<const Tin *>(p.d_o);
     const int64_t KV = (int64_t)K * V;
     const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+    if (row < 0 || row >= p.nt_max || ic < 0) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
     const float *Sg = p.h + (row * H + h) * KV;
     const float *dSg = p.dh + (row * H + h) * KV;
 

@@ -87,6 +87,10 @@ fwd_simt_kernel(FwdParams p) {
         __syncthreads();   // previous chunk finished with every buffer
         if (p.h_save) {
             const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+            if (row < 0 || row >= p.nt_max) {      // metadata inconsistent with cu_seqlens
+                if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+                return;
+            }
             float *dst = p.h_save + (row * H + h) * KV;
             for (int e = tid; e < K * VS; e += kThreads) {
                 const int c = e / VS, j = e % VS;

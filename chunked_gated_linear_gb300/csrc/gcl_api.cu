@@ -80,6 +80,7 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     p.cu_seqlens = a->cu_seqlens; p.chunk_offsets = a->chunk_offsets; p.seq_order = a->seq_order;
     p.o = a->o; p.ht = a->ht; p.h_save = a->h_save; p.dev_status = a->dev_status;
     p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V;
+    p.nt_max = gcl_nt_max(a->t_max, a->n_max, a->bt);
     p.scale = a->scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = fwd_tc_supported(variant, a->dtype, a->K, a->V)
@@ -199,6 +200,7 @@ gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
         f.cu_seqlens = a->cu_seqlens; f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
         f.o = nullptr; f.ht = nullptr; f.h_save = h; f.dev_status = a->dev_status;
         f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
+        f.nt_max = ntm;
         f.scale = a->scale;
         cudaError_t e = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
                             ? launch_fwd_tc(f, kGDN, s)

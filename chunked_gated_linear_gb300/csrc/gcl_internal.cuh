@@ -27,7 +27,7 @@ struct FwdParams {
     void *o;
     float *ht, *h_save;
     int32_t *dev_status;
-    int64_t t_max;
+    int64_t t_max, nt_max;
     int32_t n_max, H, K, V;
     float scale;
 };
