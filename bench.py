@@ -191,10 +191,13 @@ class Runner:
         t = self.t
         self.meta_args = (t["cu"].data_ptr(), w.n_max, w.t_max, w.bt, ntm, t["idx"].data_ptr(),
                           t["off"].data_ptr(), t["order"].data_ptr(), t["status"].data_ptr())
-        self.fwd_args = gcl.fwd_args(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], t["o"],
-                                     h0=t.get("h0"), ht=t["ht"], h_save=t.get("hs"),
-                                     chunk_offsets=t["off"], seq_order=t["order"],
-                                     dev_status=t["status"], scale=w.scale)
+        fargs = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], t["o"])
+        fkw = dict(h0=t.get("h0"), ht=t["ht"], h_save=t.get("hs"), chunk_indices=t["idx"],
+                   chunk_offsets=t["off"], seq_order=t["order"], dev_status=t["status"],
+                   scale=w.scale)
+        t["fws"] = torch.empty(max(gcl.fwd_workspace_bytes(*fargs, **fkw), 16),
+                               dtype=torch.uint8, device=dev)
+        self.fwd_args = gcl.fwd_args(*fargs, workspace=t["fws"], **fkw)
         self.fwd = gcl.lib().kda_chunk_fwd if w.variant == synth.KDA else gcl.lib().gdn_chunk_fwd
         if w.backward:
             args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], t["cu"], t["idx"],

@@ -30,9 +30,11 @@ class GclError(RuntimeError):
 class FwdArgs(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
-                ("cu_seqlens", ctypes.c_void_p), ("chunk_offsets", ctypes.c_void_p),
+                ("cu_seqlens", ctypes.c_void_p), ("chunk_indices", ctypes.c_void_p),
+                ("chunk_offsets", ctypes.c_void_p),
                 ("seq_order", ctypes.c_void_p), ("o", ctypes.c_void_p), ("ht", ctypes.c_void_p),
                 ("h_save", ctypes.c_void_p), ("dev_status", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("t_max", ctypes.c_int64), ("n_max", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("bt", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
@@ -69,6 +71,8 @@ def load_library(path: str = LIB_PATH):
     for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
         getattr(lib, fn).restype = ctypes.c_int
         getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs), vp]
+    lib.gcl_fwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.gcl_fwd_workspace_bytes.argtypes = [ctypes.POINTER(FwdArgs)]
     lib.gdn_chunk_bwd.restype = ctypes.c_int
     lib.gdn_chunk_bwd.argtypes = [ctypes.POINTER(BwdArgs), vp]
     lib.gcl_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -129,17 +133,28 @@ def chunk_meta_build(cu_seqlens, t_max, chunk_indices, chunk_offsets, dev_status
                                   _p(dev_status), _stream(stream)))
 
 
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
 def fwd_args(q, k, v, g, beta, cu_seqlens, o, h0=None, ht=None, h_save=None,
-             chunk_offsets=None, seq_order=None, dev_status=None, scale=None, bt=CHUNK):
+             chunk_indices=None, chunk_offsets=None, seq_order=None, dev_status=None,
+             workspace=None, scale=None, bt=CHUNK):
     T, H, K = q.shape
     V = v.shape[-1]
     a = FwdArgs(q=_p(q), k=_p(k), v=_p(v), g=_p(g), beta=_p(beta), h0=_p(h0),
-                cu_seqlens=_p(cu_seqlens), chunk_offsets=_p(chunk_offsets),
-                seq_order=_p(seq_order), o=_p(o), ht=_p(ht), h_save=_p(h_save),
-                dev_status=_p(dev_status), t_max=T, n_max=cu_seqlens.shape[0] - 1, H=H, K=K,
-                V=V, bt=bt, scale=float(K ** -0.5 if scale is None else scale),
+                cu_seqlens=_p(cu_seqlens), chunk_indices=_p(chunk_indices),
+                chunk_offsets=_p(chunk_offsets), seq_order=_p(seq_order), o=_p(o), ht=_p(ht),
+                h_save=_p(h_save), dev_status=_p(dev_status), workspace=_p(workspace),
+                workspace_bytes=_nbytes(workspace), t_max=T, n_max=cu_seqlens.shape[0] - 1,
+                H=H, K=K, V=V, bt=bt, scale=float(K ** -0.5 if scale is None else scale),
                 dtype=_dtype_of(q))
     return a
+
+
+def fwd_workspace_bytes(*args, **kw) -> int:
+    a = fwd_args(*args, **kw)
+    return int(lib().gcl_fwd_workspace_bytes(ctypes.byref(a)))
 
 
 def gdn_chunk_fwd(*args, stream=None, **kw):
@@ -161,9 +176,7 @@ def bwd_args(q, k, v, g, beta, d_o, cu_seqlens, chunk_indices, chunk_offsets, dq
                    dht=_p(dht), cu_seqlens=_p(cu_seqlens), chunk_indices=_p(chunk_indices),
                    chunk_offsets=_p(chunk_offsets), h_save=_p(h_save), dq=_p(dq), dk=_p(dk),
                    dv=_p(dv), dg=_p(dg), dbeta=_p(dbeta), dh0=_p(dh0),
-                   workspace=_p(workspace),
-                   workspace_bytes=0 if workspace is None else workspace.numel()
-                   * workspace.element_size(),
+                   workspace=_p(workspace), workspace_bytes=_nbytes(workspace),
                    dev_status=_p(dev_status), t_max=T, n_max=cu_seqlens.shape[0] - 1, H=H, K=K,
                    V=V, bt=bt, scale=float(K ** -0.5 if scale is None else scale),
                    dtype=_dtype_of(q))

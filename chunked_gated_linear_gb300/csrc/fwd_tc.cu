@@ -1,12 +1,674 @@
-// fwd_tc.cu -- tensor-core (tcgen05) fused chunk forward for bf16 inputs.
+// fwd_tc.cu -- tensor-core (tcgen05 + TMA) chunk forward of the gated delta rule,
+// bf16 inputs, d_k = d_v = 128, chunk 64.
+//
+// HA-NPU paper "Empowering Hybrid Attention Models on NPUs": section 2.1
+// (Map-Reduce-Map: the Map phases are independent across chunks, only the
+// Reduce is serial), section 4 (one (head, column slice) per core, tail heads
+// split along the value columns), section 5 (chunk-first in-place state update;
+// grouped GEMMs KK^T, QK^T, KS, QS; W = A^-1 K with the inversion decoupled from
+// the GEMMs).  FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and
+// Training Paths on Ascend NPUs", "Core design": fixed grids over NT_max chunk
+// rows with the [-1, 0] sentinel checked before any pointer arithmetic.
+//
+// Two launches:
+//
+//  prep   one CTA per row of chunk_indices and head (chunk-parallel Map):
+//         D1 = [K; Q] K^T on the tensor cores (M = 128: KK^T and QK^T stacked),
+//         then on the CUDA cores
+//           A[r,i] = beta_r exp(g_r - g_i) (k_r . k_i)       i < r
+//           L[r,i] = scale exp(g_r - g_i) (q_r . k_i)        i <= r
+//         and T = (I + A)^-1 by blocked forward substitution (16 x 16 diagonal
+//         blocks, then three levels of off-diagonal blocks).  [T; L] goes to the
+//         workspace as bf16 (128 x 64 per chunk and head).
+//
+//  chain  one CTA per (sequence, head, column slice of width VS) walks the
+//         chunks in order with its state slice S [128 x VS] in fp32 registers
+//         (thread c owns key row c) and a bf16 copy in shared memory:
+//           P1  W^T   = (diag(beta Gamma) K)^T T^T          -> TMEM, stored as -W
+//           P2  D2    = [T; L] (diag(beta) V)               =  [U; L diag(beta) V]
+//           C1  D2   += [-W; scale diag(Gamma) Q] S         =  [E; L beta V + Qhat S]
+//           C2  D3    = (diag(exp(g_c - g)) K)^T E          (state increment)
+//           C3  D2   += [T; L] E                            -> bottom: L beta V + O
+//         S <- Gamma_c S + D3 (fp32), O = bottom - L beta V.  E = U - W S comes
+//         out of the accumulator directly; every operand is either loaded by TMA
+//         or a row-scaled copy of a TMA tile (the transposed views use MN-major
+//         shared-memory descriptors), so no operand is transposed by hand except
+//         the small E and S slices.
+//
+// Rows past the end of a sequence are zeroed (selected, not multiplied) in every
+// operand the CUDA cores build, so NaN padding never reaches an MMA.
+#include <cudaTypedefs.h>
+
 #include "gcl_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gcl {
+namespace {
 
-bool fwd_tc_supported(int, int, int, int) { return false; }
+using namespace tc;
+constexpr int C = 64;
+constexpr int KD = 128;
+constexpr int VD = 128;
+constexpr int kThreads = 128;
+constexpr int kTLRows = 128;   // [T; L] rows per chunk and head
 
-cudaError_t launch_fwd_tc(const FwdParams &, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ uint4 scale8(uint4 v, float f) {
+    __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 x = __bfloat1622float2(p[i]);
+        p[i] = __floats2bfloat162_rn(x.x * f, x.y * f);
+    }
+    return v;
+}
+
+__device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
+}
+
+// ============================================================================ prep
+struct PrepParams {
+    const int32_t *chunk_indices, *cu;
+    const float *g;
+    const __nv_bfloat16 *beta;
+    __nv_bfloat16 *tl;          // [nt_max, H, 128, 64]
+    int32_t *status;
+    int64_t t_max;
+    int32_t n_max, H;
+    float scale;
+};
+
+constexpr int kPrepSmem = 1024 + 32768 + 2 * (C * (C + 1) * 4) + 3 * 16 * 17 * 4;
+
+__global__ void __launch_bounds__(kThreads)
+tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               PrepParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t *sKQ = smem;                                         // [2 cb][128 rows][128 B]
+    float *sA = reinterpret_cast<float *>(smem + 32768);         // [64][65]
+    float *sT = sA + C * (C + 1);                                // [64][65]
+    float *sX = sT + C * (C + 1);                                // [3][16][17]
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+    __shared__ float sG[C], sB[C];
+
+    if (status_blocks(p.status)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, j = blockIdx.x, h = blockIdx.y;
+    const int n = p.chunk_indices[2 * j];
+    if (n < 0) return;                              // sentinel: unused chunk slot
+    const int ic = p.chunk_indices[2 * j + 1];
+    if (n >= p.n_max || ic < 0) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t bos = p.cu[n], eos = p.cu[n + 1], t0 = bos + (int64_t)ic * C;
+    if (bos < 0 || eos < bos || eos > p.t_max || t0 >= eos) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int len = (int)(eos - t0 < C ? eos - t0 : C);
+    const int H = p.H;
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        s_err = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, 64);
+        tmem_relinquish();
+    }
+    if (tid < C) {
+        sG[tid] = tid < len ? p.g[(t0 + tid) * H + h] : 0.f;
+        sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
+    }
+    for (int e = tid; e < C * (C + 1); e += kThreads) sT[e] = 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar_tma, 32768);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(sKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
+            tma_load_3d(sKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
+        }
+        if (mbar_wait(&bar_tma, 0, &s_err, 1)) {
+            tc_fence_after();
+            const uint32_t base = smem_u32(sKQ);
+            constexpr uint32_t idesc = idesc_bf16(128, 64);
+            for (int s = 0; s < KD / 16; ++s) {
+                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                mma_bf16(tmem, smem_desc(base + off, 16, 1024, kSwizzle128B),
+                         smem_desc(base + off, 16, 1024, kSwizzle128B), idesc, s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+    }
+    if (tid == 32) {                                  // gate cumsum while the MMA runs
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) { acc += sG[r]; sG[r] = acc; }
+    }
+    __syncthreads();
+    mbar_wait(&bar_mma, 0, &s_err, 2);
+    tc_fence_after();
+    __syncthreads();
+    if (s_err == 0) {
+        float v[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + q * 16, v + q * 16);
+        tmem_ld_wait();
+        __nv_bfloat16 *tl = p.tl + ((size_t)j * H + h) * kTLRows * C;
+        if (tid < C) {
+            const int r = tid;
+            const float gr = sG[r], br = sB[r];
+#pragma unroll
+            for (int i = 0; i < C; ++i)
+                sA[r * (C + 1) + i] = (i < r && r < len) ? br * __expf(gr - sG[i]) * v[i] : 0.f;
+        } else {
+            const int r = tid - C;
+            const float gr = sG[r];
+            uint4 *dst = reinterpret_cast<uint4 *>(tl + (size_t)(C + r) * C);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint4 pk;
+                __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i0 = q * 8 + 2 * e, i1 = i0 + 1;
+                    const float l0 = (i0 <= r && r < len) ? p.scale * __expf(gr - sG[i0]) * v[i0] : 0.f;
+                    const float l1 = (i1 <= r && r < len) ? p.scale * __expf(gr - sG[i1]) * v[i1] : 0.f;
+                    pp[e] = __floats2bfloat162_rn(l0, l1);
+                }
+                dst[q] = pk;
+            }
+        }
+        __syncthreads();
+        // ---- T = (I + A)^-1.  Diagonal 16x16 blocks: thread (b, jj) owns column jj of block b.
+        if (tid < C) {
+            const int b = tid >> 4, jj = tid & 15, o = b * 16;
+            float tc[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) tc[r] = (r == jj) ? 1.f : 0.f;
+#pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                if (r > jj) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        if (m >= jj && m < r) acc = fmaf(sA[(o + r) * (C + 1) + o + m], tc[m], acc);
+                    tc[r] = -acc;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(o + r) * (C + 1) + o + jj] = tc[r];
+        }
+        __syncthreads();
+        // ---- off-diagonal blocks, level d: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, i - j = d
+        for (int d = 1; d < 4; ++d) {
+            const int nblk = 4 - d;
+            for (int e = tid; e < nblk * 256; e += kThreads) {
+                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
+                float acc = 0.f;
+                for (int m = bj * 16; m < bi * 16; ++m)
+                    acc = fmaf(sA[(bi * 16 + rr) * (C + 1) + m], sT[m * (C + 1) + bj * 16 + cc], acc);
+                sX[blk * 272 + rr * 17 + cc] = acc;
+            }
+            __syncthreads();
+            for (int e = tid; e < nblk * 256; e += kThreads) {
+                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    acc = fmaf(sT[(bi * 16 + rr) * (C + 1) + bi * 16 + m], sX[blk * 272 + m * 17 + cc], acc);
+                sT[(bi * 16 + rr) * (C + 1) + bj * 16 + cc] = -acc;
+            }
+            __syncthreads();
+        }
+        // ---- T (bf16) -> rows 0..63 of the [T; L] block: thread pair per row
+        {
+            const int r = tid >> 1, half = tid & 1;
+            uint4 *dst = reinterpret_cast<uint4 *>(tl + (size_t)r * C + half * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 pk;
+                __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i0 = half * 32 + q * 8 + 2 * e;
+                    pp[e] = __floats2bfloat162_rn(sT[r * (C + 1) + i0], sT[r * (C + 1) + i0 + 1]);
+                }
+                dst[q] = pk;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+// ============================================================================ chain
+struct ChainParams {
+    const int32_t *cu, *chunk_offsets, *seq_order;
+    const float *g;
+    const __nv_bfloat16 *beta;
+    const float *h0;
+    __nv_bfloat16 *o;
+    float *ht, *h_save;
+    int32_t *status;
+    int64_t t_max, nt_max;
+    int32_t n_max, H;
+    float scale;
+};
+
+template <int VS>
+struct ChainLayout {
+    static constexpr uint32_t oK = 0;                       // K tiles, 2 stages x 16 KB
+    static constexpr uint32_t oWQ = 32768;                  // [-W; Qhat], 2 stages x 32 KB
+    static constexpr uint32_t oTL = oWQ + 65536;            // [T; L], 2 stages x 16 KB
+    static constexpr uint32_t oKB = oTL + 32768;            // beta Gamma K (MN-major), 16 KB
+    static constexpr uint32_t oKT = oKB + 16384;            // exp(g_c - g) K (MN-major), 16 KB
+    static constexpr uint32_t oSB = oKT + 16384;            // S^T bf16, K-major [2][VS][128 B]
+    static constexpr uint32_t oET = oSB + VS * 256;         // E^T bf16, K-major [VS][128 B]
+    static constexpr uint32_t oVB = oET + VS * 128;         // (beta V)^T bf16, K-major
+    static constexpr uint32_t oV = oVB + VS * 128;          // V tiles [64][VS], 2 stages
+    static constexpr uint32_t kVTile = C * VS * 2;
+    static constexpr uint32_t total = oV + 2 * kVTile;
+    static constexpr uint32_t bytes = total + 1024;         // + alignment slack
+    static constexpr uint32_t tmem_cols = VS <= 32 ? 128 : 256;
+    static constexpr uint32_t kStageBytes = 16384 + 16384 + 16384 + kVTile;   // per chunk TMA
+};
+
+template <int VS>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_tl,
+                ChainParams p) {
+    using Lay = ChainLayout<VS>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t bar_tma[2], bar_mma;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+    __shared__ float sG[C], sB[C];
+
+    if (status_blocks(p.status)) return;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int split = blockIdx.x, h = blockIdx.y;
+    const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
+    const int H = p.H, v0 = split * VS;
+    const int64_t bos = p.cu[n], eos = p.cu[n + 1];
+    if (n < 0 || n >= p.n_max || bos < 0 || eos < bos || eos > p.t_max) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int nch = (int)((eos - bos + C - 1) / C);
+    const int64_t row0 = p.chunk_offsets[n];
+    if (nch > 0 && (row0 < 0 || row0 + nch > p.nt_max)) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const uint32_t sbase = smem_u32(smem);
+    const int64_t KV = (int64_t)KD * VD;
+    const int64_t state_base = ((int64_t)n * H + h) * KV;
+
+    if (tid == 0) {
+        mbar_init(&bar_tma[0], 1);
+        mbar_init(&bar_tma[1], 1);
+        mbar_init(&bar_mma, 1);
+        s_err = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, Lay::tmem_cols);
+        tmem_relinquish();
+    }
+    // state slice: thread c owns key row c
+    const int c = tid;
+    float S[VS];
+    {
+        const float *src = p.h0 ? p.h0 + state_base + (int64_t)c * VD + v0 : nullptr;
+#pragma unroll
+        for (int jj = 0; jj < VS; ++jj) S[jj] = src ? src[jj] : 0.f;
+#pragma unroll
+        for (int jj = 0; jj < VS; ++jj) st_bf16(smem, Lay::oSB + sw128_offset(VS, jj, c), S[jj]);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t tD_W = tmem, tD2 = tmem + 64, tD3 = tmem + 64 + VS;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+
+    auto issue_tma = [&](int ic, int stage) {
+        const int t0 = (int)(bos + (int64_t)ic * C);
+        const int tl_y = (int)(((row0 + ic) * H + h) * kTLRows);
+        uint64_t *bar = &bar_tma[stage];
+        mbar_arrive_expect_tx(bar, Lay::kStageBytes);
+        uint8_t *kt = smem + Lay::oK + stage * 16384;
+        uint8_t *wq = smem + Lay::oWQ + stage * 32768;
+        tma_load_3d(kt, &tm_k, 0, h, t0, bar);
+        tma_load_3d(kt + 8192, &tm_k, 64, h, t0, bar);
+        tma_load_3d(wq + 8192, &tm_q, 0, h, t0, bar);            // Q rows 64..127 of [-W; Qhat]
+        tma_load_3d(wq + 16384 + 8192, &tm_q, 64, h, t0, bar);
+        tma_load_2d(smem + Lay::oTL + stage * 16384, &tm_tl, 0, tl_y, bar);
+        tma_load_3d(smem + Lay::oV + stage * Lay::kVTile, &tm_v, v0, h, t0, bar);
+    };
+    if (tid == 0 && nch > 0) issue_tma(0, 0);
+
+    uint32_t mma_phase = 0;
+    bool failed = false;
+    for (int ic = 0; ic < nch; ++ic) {
+        const int stage = ic & 1;
+        const int64_t t0 = bos + (int64_t)ic * C;
+        const int len = (int)(eos - t0 < C ? eos - t0 : C);
+        if (tid == 0 && ic + 1 < nch) issue_tma(ic + 1, stage ^ 1);
+        if (p.h_save) {
+            float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)c * VD + v0;
+#pragma unroll
+            for (int jj = 0; jj < VS; jj += 4)
+                *reinterpret_cast<float4 *>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+        }
+        if (tid < C) {
+            sG[tid] = tid < len ? p.g[(t0 + tid) * H + h] : 0.f;
+            sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int r = 0; r < C; ++r) { acc += sG[r]; sG[r] = acc; }
+        }
+        mbar_wait(&bar_tma[stage], (ic >> 1) & 1, &s_err, 3);
+        __syncthreads();
+        if (s_err) { failed = true; break; }
+        const float gC = sG[C - 1];
+        uint8_t *ktile = smem + Lay::oK + stage * 16384;
+        uint8_t *wq = smem + Lay::oWQ + stage * 32768;
+        // ---- operands: beta Gamma K, exp(g_c - g) K, scale Gamma Q (in place), (beta V)^T
+        {
+            const int r = tid >> 1, cb = tid & 1;
+            const bool live = r < len;
+            const float gr = sG[r];
+            const float f_kb = live ? sB[r] * __expf(gr) : 0.f;
+            const float f_kt = live ? __expf(gC - gr) : 0.f;
+            const float f_q = live ? p.scale * __expf(gr) : 0.f;
+            const uint32_t roff = cb * 8192 + r * 128;
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 kv = *reinterpret_cast<const uint4 *>(ktile + roff + q * 16);
+                *reinterpret_cast<uint4 *>(smem + Lay::oKB + roff + q * 16) = live ? scale8(kv, f_kb) : zero;
+                *reinterpret_cast<uint4 *>(smem + Lay::oKT + roff + q * 16) = live ? scale8(kv, f_kt) : zero;
+                uint4 *qp = reinterpret_cast<uint4 *>(wq + cb * 16384 + 8192 + r * 128 + q * 16);
+                *qp = live ? scale8(*qp, f_q) : zero;
+            }
+            const __nv_bfloat16 *vt =
+                reinterpret_cast<const __nv_bfloat16 *>(smem + Lay::oV + stage * Lay::kVTile);
+            for (int e = tid; e < C * VS; e += kThreads) {
+                const int rr = e / VS, jj = e % VS;
+                const float x = rr < len ? sB[rr] * bf2f(vt[rr * VS + jj]) : 0.f;
+                st_bf16(smem, Lay::oVB + sw128_offset(VS, jj, rr), x);
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+        const uint32_t tl_addr = sbase + Lay::oTL + stage * 16384;
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
+            constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 0);
+            for (int s = 0; s < 4; ++s)      // W^T = (beta Gamma K)^T T^T
+                mma_bf16(tD_W, smem_desc(sbase + Lay::oKB + s * 2048, 8192, 1024, kSwizzle128B),
+                         smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B), id_w, s > 0);
+            for (int s = 0; s < 4; ++s)      // D2 = [T; L] (beta V)
+                mma_bf16(tD2, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oVB + s * 32, 16, 1024, kSwizzle128B), id_v, s > 0);
+            mma_commit(&bar_mma);
+        }
+        mbar_wait(&bar_mma, mma_phase, &s_err, 4);
+        mma_phase ^= 1;
+        tc_fence_after();
+        // ---- -W into rows 0..63 of [-W; Qhat]; bottom rows keep L (beta V) for the output
+        float lvb[VS];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float w[16];
+            tmem_ld16(tD_W + lane_off + q * 16, w);
+            tmem_ld_wait();
+#pragma unroll
+            for (int r = 0; r < 16; ++r) st_bf16(wq, sw128_offset(128, q * 16 + r, c), -w[r]);
+        }
+        if (tid >= C) {
+#pragma unroll
+            for (int q = 0; q < VS / 16; ++q) tmem_ld16(tD2 + lane_off + q * 16, lvb + q * 16);
+            tmem_ld_wait();
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (s_err) { failed = true; break; }
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(128, VS, 0, 0);
+            const uint32_t wq_addr = sbase + Lay::oWQ + stage * 32768;
+            for (int s = 0; s < 8; ++s)      // D2 += [-W; Qhat] S
+                mma_bf16(tD2, smem_desc(wq_addr + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oSB + (s >> 2) * (VS * 128) + (s & 3) * 32, 16, 1024,
+                                   kSwizzle128B),
+                         id, 1);
+            mma_commit(&bar_mma);
+        }
+        mbar_wait(&bar_mma, mma_phase, &s_err, 5);
+        mma_phase ^= 1;
+        tc_fence_after();
+        // ---- E (rows 0..63 of D2) -> E^T bf16
+        if (tid < C) {
+#pragma unroll
+            for (int q = 0; q < VS / 16; ++q) {
+                float e[16];
+                tmem_ld16(tD2 + lane_off + q * 16, e);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    st_bf16(smem, Lay::oET + sw128_offset(VS, q * 16 + jj, tid), e[jj]);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (s_err) { failed = true; break; }
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_s = idesc_bf16(128, VS, 1, 0);
+            constexpr uint32_t id_o = idesc_bf16(128, VS, 0, 0);
+            for (int s = 0; s < 4; ++s)      // D3 = Ktil^T E
+                mma_bf16(tD3, smem_desc(sbase + Lay::oKT + s * 2048, 8192, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oET + s * 32, 16, 1024, kSwizzle128B), id_s, s > 0);
+            for (int s = 0; s < 4; ++s)      // D2 += [T; L] E
+                mma_bf16(tD2, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oET + s * 32, 16, 1024, kSwizzle128B), id_o, 1);
+            mma_commit(&bar_mma);
+        }
+        mbar_wait(&bar_mma, mma_phase, &s_err, 6);
+        mma_phase ^= 1;
+        tc_fence_after();
+        // ---- state update (all rows) and output (rows 64..127 of D2)
+        {
+            const float GC = __expf(gC);
+            const int r = tid - C;
+            const bool store = tid >= C && r < len && p.o != nullptr;
+            __nv_bfloat16 *dst = store ? p.o + ((t0 + r) * H + h) * (int64_t)VD + v0 : nullptr;
+#pragma unroll
+            for (int q = 0; q < VS / 16; ++q) {
+                float d3[16];
+                tmem_ld16(tD3 + lane_off + q * 16, d3);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    S[q * 16 + jj] = fmaf(GC, S[q * 16 + jj], d3[jj]);
+                    st_bf16(smem, Lay::oSB + sw128_offset(VS, q * 16 + jj, c), S[q * 16 + jj]);
+                }
+                if (tid >= C) {                       // warp-uniform: warps 2 and 3
+                    float d2[16];
+                    tmem_ld16(tD2 + lane_off + q * 16, d2);
+                    tmem_ld_wait();
+                    if (store) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 8) {
+                            uint4 pk;
+                            __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const int a = jj + 2 * e2;
+                                pp[e2] = __floats2bfloat162_rn(d2[a] - lvb[q * 16 + a],
+                                                               d2[a + 1] - lvb[q * 16 + a + 1]);
+                            }
+                            *reinterpret_cast<uint4 *>(dst + q * 16 + jj) = pk;
+                        }
+                    }
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (s_err) { failed = true; break; }
+    }
+    if (!failed && p.ht) {
+        float *dst = p.ht + state_base + (int64_t)c * VD + v0;
+#pragma unroll
+        for (int jj = 0; jj < VS; jj += 4)
+            *reinterpret_cast<float4 *>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, Lay::tmem_cols);
+    if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+// ============================================================================ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+              const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int VS>
+cudaError_t launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                         const CUtensorMap &mtl, const ChainParams &cp, int n_split, int H,
+                         int n_max, cudaStream_t s) {
+    using Lay = ChainLayout<VS>;
+    auto kern = tc_chain_kernel<VS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay::bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(n_split, H, n_max), kThreads, Lay::bytes, s>>>(mq, mk, mv, mtl, cp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fwd_tc_supported(int variant, int dtype, int K, int V) {
+    return variant == kGDN && dtype == GCL_BF16 && K == KD && V == VD;
+}
+
+size_t fwd_tc_workspace_bytes(int64_t nt_max, int H) {
+    return (size_t)nt_max * H * kTLRows * C * sizeof(__nv_bfloat16);
+}
+
+// Value-column split: the most CTAs per head that still fit one wave on the GPU,
+// between 2 (VS = 64, the shared-memory limit) and 8 (VS = 16).
+int fwd_tc_split(int n_max, int H) {
+    const int sms = num_sms();
+    int split = 2;
+    for (int cand : {4, 8})
+        if ((int64_t)n_max * H * cand <= sms) split = cand;
+    return split;
+}
+
+cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
+    (void)variant;
+    const int H = p.H;
+    CUtensorMap mq, mk, mv, mtl;
+    const cuuint64_t dqk[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sqk[2] = {(cuuint64_t)KD * 2, (cuuint64_t)H * KD * 2};
+    const cuuint32_t bqk[3] = {64, 1, 64};
+    const int split = fwd_tc_split(p.n_max, H);
+    const int VS = VD / split;
+    const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
+    const cuuint32_t bv[3] = {(cuuint32_t)VS, 1, 64};
+    const cuuint64_t dtl[2] = {(cuuint64_t)C, (cuuint64_t)p.nt_max * H * kTLRows};
+    const cuuint64_t stl[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t btl[2] = {64, (cuuint32_t)kTLRows};
+    if (!make_map(&mq, p.q, 3, dqk, sqk, bqk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mk, p.k, 3, dqk, sqk, bqk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mv, p.v, 3, dv, sv, bv, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&mtl, p.workspace, 2, dtl, stl, btl, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+
+    PrepParams pp{};
+    pp.chunk_indices = p.chunk_indices;
+    pp.cu = p.cu_seqlens;
+    pp.g = p.g;
+    pp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
+    pp.tl = static_cast<__nv_bfloat16 *>(p.workspace);
+    pp.status = p.dev_status;
+    pp.t_max = p.t_max;
+    pp.n_max = p.n_max;
+    pp.H = H;
+    pp.scale = p.scale;
+    cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPrepSmem);
+    if (e != cudaSuccess) return e;
+    tc_prep_kernel<<<dim3((unsigned)p.nt_max, H), kThreads, kPrepSmem, s>>>(mq, mk, pp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    ChainParams cp{};
+    cp.cu = p.cu_seqlens;
+    cp.chunk_offsets = p.chunk_offsets;
+    cp.seq_order = p.seq_order;
+    cp.g = p.g;
+    cp.beta = pp.beta;
+    cp.h0 = p.h0;
+    cp.o = static_cast<__nv_bfloat16 *>(p.o);
+    cp.ht = p.ht;
+    cp.h_save = p.h_save;
+    cp.status = p.dev_status;
+    cp.t_max = p.t_max;
+    cp.nt_max = p.nt_max;
+    cp.n_max = p.n_max;
+    cp.H = H;
+    cp.scale = p.scale;
+    switch (VS) {
+        case 16: return launch_chain<16>(mq, mk, mv, mtl, cp, split, H, p.n_max, s);
+        case 32: return launch_chain<32>(mq, mk, mv, mtl, cp, split, H, p.n_max, s);
+        default: return launch_chain<64>(mq, mk, mv, mtl, cp, split, H, p.n_max, s);
+    }
 }
 
 }  // namespace gcl

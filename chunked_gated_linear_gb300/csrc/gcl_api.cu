@@ -72,30 +72,55 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     if (st != GCL_OK) return st;
     if (a->h_save && !a->chunk_offsets)
         return fail(GCL_ERR_INVALID_ARG, "%s: h_save needs chunk_offsets", fn);
+    const bool tc = fwd_tc_supported(variant, a->dtype, a->K, a->V);
+    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
+    if (tc) {
+        if (!a->chunk_indices || !a->chunk_offsets)
+            return fail(GCL_ERR_INVALID_ARG,
+                        "%s: chunk_indices and chunk_offsets are required for bf16 K=V=128", fn);
+        const size_t need = fwd_tc_workspace_bytes(ntm, a->H);
+        if (!a->workspace || a->workspace_bytes < need)
+            return fail(GCL_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn,
+                        need, a->workspace ? a->workspace_bytes : (size_t)0);
+        if (!aligned16(a->workspace))
+            return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
+    }
     if ((a->o && !aligned16(a->o)) || (a->ht && !aligned16(a->ht)) ||
         (a->h0 && !aligned16(a->h0)) || (a->h_save && !aligned16(a->h_save)))
         return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
     FwdParams p{};
     p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.h0 = a->h0;
-    p.cu_seqlens = a->cu_seqlens; p.chunk_offsets = a->chunk_offsets; p.seq_order = a->seq_order;
+    p.cu_seqlens = a->cu_seqlens; p.chunk_indices = a->chunk_indices;
+    p.chunk_offsets = a->chunk_offsets; p.seq_order = a->seq_order;
     p.o = a->o; p.ht = a->ht; p.h_save = a->h_save; p.dev_status = a->dev_status;
+    p.workspace = a->workspace;
     p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V;
-    p.nt_max = gcl_nt_max(a->t_max, a->n_max, a->bt);
+    p.nt_max = ntm;
     p.scale = a->scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = fwd_tc_supported(variant, a->dtype, a->K, a->V)
-                        ? launch_fwd_tc(p, variant, s)
-                        : launch_fwd_simt(p, variant, a->dtype, s);
+    cudaError_t e = tc ? launch_fwd_tc(p, variant, s) : launch_fwd_simt(p, variant, a->dtype, s);
     return cuda_check(e, fn);
+}
+
+static size_t fwd_ws(const gcl_fwd_args *a, int variant) {
+    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V)) return 0;
+    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
+    if (ntm <= 0 || a->H <= 0) return 0;
+    return fwd_tc_workspace_bytes(ntm, a->H);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Backward workspace: dS' per chunk [nt_max, H, K, V] fp32; without saved states also
+// the recomputed states (same shape) and the forward's own workspace.
 static size_t bwd_ws(const gcl_bwd_args *a) {
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
-    return per * (a->h_save ? 1 : 2);
+    if (a->h_save) return per;
+    const size_t fw = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
+                          ? align256(fwd_tc_workspace_bytes(ntm, a->H)) : 0;
+    return 2 * per + fw;
 }
 
 }  // namespace gcl
@@ -141,6 +166,11 @@ gcl_status_t chunk_meta_build(const int32_t *cu_seqlens, int32_t n_max, int64_t 
                                         chunk_offsets, seq_order, dev_status,
                                         static_cast<cudaStream_t>(stream)),
                       "chunk_meta_build");
+}
+
+size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args) {
+    if (!args) return 0;
+    return fwd_ws(args, kGDN);
 }
 
 gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream) {
@@ -197,8 +227,10 @@ gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
         float *h = reinterpret_cast<float *>(ws + per);
         FwdParams f{};
         f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
-        f.cu_seqlens = a->cu_seqlens; f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
+        f.cu_seqlens = a->cu_seqlens; f.chunk_indices = a->chunk_indices;
+        f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
         f.o = nullptr; f.ht = nullptr; f.h_save = h; f.dev_status = a->dev_status;
+        f.workspace = ws + 2 * per;
         f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
         f.nt_max = ntm;
         f.scale = a->scale;

@@ -23,10 +23,11 @@ struct FwdParams {
     const float *g;
     const void *beta;
     const float *h0;
-    const int32_t *cu_seqlens, *chunk_offsets, *seq_order;
+    const int32_t *cu_seqlens, *chunk_indices, *chunk_offsets, *seq_order;
     void *o;
     float *ht, *h_save;
     int32_t *dev_status;
+    void *workspace;
     int64_t t_max, nt_max;
     int32_t n_max, H, K, V;
     float scale;
@@ -56,6 +57,7 @@ cudaError_t launch_chunk_meta(const int32_t *cu, int32_t n_max, int64_t t_max, i
 cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s);
 bool fwd_tc_supported(int variant, int dtype, int K, int V);
+size_t fwd_tc_workspace_bytes(int64_t nt_max, int H);
 cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, cudaStream_t s);
 
 // ---- device helpers -------------------------------------------------------

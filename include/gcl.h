@@ -64,6 +64,7 @@ typedef enum gcl_status {
 #define GCL_DEV_CU_NONZERO_START 2 /* cu_seqlens[0] != 0                                 */
 #define GCL_DEV_CU_OVER_CAPACITY 3 /* cu_seqlens[N_max] > T_max                          */
 #define GCL_DEV_BAD_RANGE 4        /* a compute kernel met an invalid sequence range      */
+#define GCL_DEV_WAIT_TIMEOUT 5     /* a kernel gave up waiting on an async copy or MMA    */
 
 typedef enum gcl_dtype {
     GCL_F32 = 0,   /* q, k, v, beta, do, o in fp32; every internal product in fp32     */
@@ -126,7 +127,8 @@ typedef struct gcl_fwd_args {
     const void *beta;              /* [t_max, H]  dtype                                      */
     const float *h0;               /* [n_max, H, K, V] fp32, or NULL for a zero state        */
     const int32_t *cu_seqlens;     /* [n_max + 1] int32                                      */
-    const int32_t *chunk_offsets;  /* [n_max + 1] from chunk_meta_build; required iff h_save */
+    const int32_t *chunk_indices;  /* [nt_max, 2] from chunk_meta_build (tensor-core path)   */
+    const int32_t *chunk_offsets;  /* [n_max + 1] from chunk_meta_build                      */
     const int32_t *seq_order;      /* [n_max] from chunk_meta_build, or NULL (index order)   */
     void *o;                       /* [t_max, H, V] dtype (out); live rows only; may be NULL */
     float *ht;                     /* [n_max, H, K, V] fp32 (out) or NULL                    */
@@ -134,6 +136,8 @@ typedef struct gcl_fwd_args {
                                    /* chunk i of sequence n at row chunk_offsets[n] + i      */
     int32_t *dev_status;           /* [1] or NULL: no work if non-zero on entry; set to      */
                                    /* GCL_DEV_BAD_RANGE if a sequence range is invalid       */
+    void *workspace;               /* device scratch of gcl_fwd_workspace_bytes() bytes      */
+    size_t workspace_bytes;
     int64_t t_max;                 /* token capacity of every [t_max, ...] buffer            */
     int32_t n_max;                 /* sequence capacity (cu_seqlens has n_max + 1 entries)   */
     int32_t H, K, V;               /* heads, key dim, value dim                              */
@@ -141,6 +145,11 @@ typedef struct gcl_fwd_args {
     float scale;                   /* read-out scale, usually K^-1/2                         */
     int32_t dtype;                 /* gcl_dtype_t of q, k, v, beta, o                        */
 } gcl_fwd_args;
+
+/* Bytes of device workspace the forward needs for these sizes (0 when the fp32
+ * CUDA-core kernel serves them).  The tensor-core path keeps, per chunk and
+ * head, the inverted intra-chunk matrix T and the masked decayed QK^T (bf16). */
+size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
 
 /*
  * gdn_chunk_fwd -- gated delta rule prefill: o and ht from q, k, v, g, beta, h0.
@@ -153,9 +162,12 @@ typedef struct gcl_fwd_args {
  * CTAs (HA-NPU section 4, column-wise split without cross-core reductions).
  * Zero-length sequences write ht = h0 (or zeros).
  *
- * Supported: bt = 64; K, V in {64, 128}; dtype GCL_F32 or GCL_BF16.  bf16
- * inputs with K = V = 128 run on the tensor cores (tcgen05); everything else
- * runs the fp32 CUDA-core kernel.  Pointers must be 16-byte aligned.
+ * Supported: bt = 64; K, V in {64, 128}; dtype GCL_F32 or GCL_BF16.  GDN with
+ * bf16 inputs and K = V = 128 runs on the tensor cores (tcgen05): a
+ * chunk-parallel launch over chunk_indices forms T = (I + A)^-1 and L per chunk
+ * into the workspace, then the per-(sequence, head, column slice) launch runs
+ * the state recurrence.  Everything else runs the fp32 CUDA-core kernel.
+ * Pointers must be 16-byte aligned.
  */
 gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
 gcl_status_t kda_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);

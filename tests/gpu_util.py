@@ -68,10 +68,14 @@ def run_fwd(w, d, meta=None, h_save=False, o_fill=CANARY, use_order=True):
     if h_save:
         hs = torch.full((meta.nt_max, w.H, w.K, w.V), o_fill, dtype=torch.float32, device=DEV)
     fn = gcl.kda_chunk_fwd if w.variant == synth.KDA else gcl.gdn_chunk_fwd
-    fn(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], o, h0=d.get("h0"), ht=ht,
-       h_save=hs, chunk_offsets=meta.off, seq_order=meta.order if use_order else None,
-       dev_status=meta.status, scale=w.scale, bt=w.bt)
-    return dict(o=o, ht=ht, h_save=hs, meta=meta)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], o)
+    kw = dict(h0=d.get("h0"), ht=ht, h_save=hs, chunk_indices=meta.idx, chunk_offsets=meta.off,
+              seq_order=meta.order if use_order else None, dev_status=meta.status,
+              scale=w.scale, bt=w.bt)
+    nb = gcl.fwd_workspace_bytes(*args, **kw)
+    ws = torch.full((max(nb, 16),), 0xFF, dtype=torch.uint8, device=DEV)   # stale contents
+    fn(*args, workspace=ws, **kw)
+    return dict(o=o, ht=ht, h_save=hs, meta=meta, ws=ws)
 
 
 def oracle_fwd(w, x):

@@ -22,12 +22,16 @@ def test_capture_once_replay_three_layouts():
     o = torch.full((base.t_max, base.H, base.V), CANARY, dtype=tdtype(base), device=DEV)
     ht = torch.zeros((base.n_max, base.H, base.K, base.V), dtype=torch.float32, device=DEV)
 
+    args = (static["q"], static["k"], static["v"], static["g"], static["beta"],
+            static["cu_seqlens"], o)
+    kw = dict(h0=static["h0"], ht=ht, chunk_indices=meta.idx, chunk_offsets=meta.off,
+              seq_order=meta.order, dev_status=meta.status, scale=base.scale)
+    ws = torch.empty(max(gcl.fwd_workspace_bytes(*args, **kw), 16), dtype=torch.uint8,
+                     device=DEV)
+
     def step(stream=None):
         meta.build(static["cu_seqlens"], stream=stream)
-        gcl.gdn_chunk_fwd(static["q"], static["k"], static["v"], static["g"], static["beta"],
-                          static["cu_seqlens"], o, h0=static["h0"], ht=ht,
-                          chunk_offsets=meta.off, seq_order=meta.order,
-                          dev_status=meta.status, scale=base.scale, stream=stream)
+        gcl.gdn_chunk_fwd(*args, workspace=ws, stream=stream, **kw)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
