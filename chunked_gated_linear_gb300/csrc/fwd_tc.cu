@@ -64,6 +64,30 @@ __device__ __forceinline__ uint4 scale8(uint4 v, float f) {
     return v;
 }
 
+// Inclusive scan of one float per lane across a warp.
+__device__ __forceinline__ float warp_incl_scan(float x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    return x;
+}
+
+// gamma = inclusive cumsum of the 64 gate values of a chunk, by warps 0 and 1 (threads
+// 0..63 each hold g of their row); the total of warp 0 is handed over through shared
+// memory.  All threads of the block must call it (it contains a block barrier).
+__device__ __forceinline__ float chunk_cumsum(float g, float *s_carry) {
+    const int tid = threadIdx.x;
+    float x = 0.f;
+    if (tid < 64) x = warp_incl_scan(g);
+    if (tid == 31) *s_carry = x;
+    __syncthreads();
+    if (tid >= 32 && tid < 64) x += *s_carry;
+    return x;
+}
+
 __device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
 }
@@ -123,9 +147,14 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_alloc(&s_tmem, 64);
         tmem_relinquish();
     }
-    if (tid < C) {
-        sG[tid] = tid < len ? p.g[(t0 + tid) * H + h] : 0.f;
-        sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
+    __shared__ float s_carry;
+    {
+        const float gv = (tid < len) ? p.g[(t0 + tid) * H + h] : 0.f;
+        const float gam = chunk_cumsum(gv, &s_carry);
+        if (tid < C) {
+            sG[tid] = gam;
+            sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
+        }
     }
     for (int e = tid; e < C * (C + 1); e += kThreads) sT[e] = 0.f;
     tc_fence_before();
@@ -149,10 +178,6 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             mma_commit(&bar_mma);
         }
-    }
-    if (tid == 32) {                                  // gate cumsum while the MMA runs
-        float acc = 0.f;
-        for (int r = 0; r < C; ++r) { acc += sG[r]; sG[r] = acc; }
     }
     __syncthreads();
     mbar_wait(&bar_mma, 0, &s_err, 2);
@@ -297,6 +322,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
     __shared__ float sG[C], sB[C];
+    __shared__ float s_carry;
 
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -376,14 +402,13 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int jj = 0; jj < VS; jj += 4)
                 *reinterpret_cast<float4 *>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
         }
-        if (tid < C) {
-            sG[tid] = tid < len ? p.g[(t0 + tid) * H + h] : 0.f;
-            sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            float acc = 0.f;
-            for (int r = 0; r < C; ++r) { acc += sG[r]; sG[r] = acc; }
+        {
+            const float gv = (tid < len) ? p.g[(t0 + tid) * H + h] : 0.f;
+            const float gam = chunk_cumsum(gv, &s_carry);
+            if (tid < C) {
+                sG[tid] = gam;
+                sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
+            }
         }
         mbar_wait(&bar_tma[stage], (ic >> 1) & 1, &s_err, 3);
         __syncthreads();
