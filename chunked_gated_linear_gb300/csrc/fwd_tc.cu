@@ -104,7 +104,8 @@ struct PrepParams {
     float scale;
 };
 
-constexpr int kPrepSmem = 1024 + 32768 + 2 * (C * (C + 1) * 4) + 3 * 16 * 17 * 4;
+// The fp32 solve buffers reuse the K/Q tile once the MMA has consumed it.
+constexpr int kPrepSmem = 1024 + 2 * (C * (C + 1) * 4) + 3 * 16 * 17 * 4;
 
 __global__ void __launch_bounds__(kThreads)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -112,8 +113,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *sKQ = smem;                                         // [2 cb][128 rows][128 B]
-    float *sA = reinterpret_cast<float *>(smem + 32768);         // [64][65]
-    float *sT = sA + C * (C + 1);                                // [64][65]
+    float *sA = reinterpret_cast<float *>(smem);                 // [64][65], after the MMA
+    float *sT = sA + C * (C + 1);                                // [64][65], after the MMA
     float *sX = sT + C * (C + 1);                                // [3][16][17]
     __shared__ uint64_t bar_tma, bar_mma;
     __shared__ uint32_t s_tmem;
@@ -156,7 +157,6 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
         }
     }
-    for (int e = tid; e < C * (C + 1); e += kThreads) sT[e] = 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -188,6 +188,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + q * 16, v + q * 16);
         tmem_ld_wait();
+        for (int e = tid; e < C * (C + 1); e += kThreads) sT[e] = 0.f;   // K/Q tile is dead now
         __nv_bfloat16 *tl = p.tl + ((size_t)j * H + h) * kTLRows * C;
         if (tid < C) {
             const int r = tid;
@@ -306,7 +307,7 @@ struct ChainLayout {
     static constexpr uint32_t kVTile = C * VS * 2;
     static constexpr uint32_t total = oV + 2 * kVTile;
     static constexpr uint32_t bytes = total + 1024;         // + alignment slack
-    static constexpr uint32_t tmem_cols = VS <= 32 ? 128 : 256;
+    static constexpr uint32_t tmem_cols = 256;              // D_W 128 + D2 VS + D3 VS
     static constexpr uint32_t kStageBytes = 16384 + 16384 + 16384 + kVTile;   // per chunk TMA
 };
 
@@ -323,6 +324,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __shared__ int s_err;
     __shared__ float sG[C], sB[C];
     __shared__ float s_carry;
+    __shared__ float sF[3][C];       // per-row scale factors: beta Gamma, exp(g_c - g), scale Gamma
 
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -370,7 +372,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tD_W = tmem, tD2 = tmem + 64, tD3 = tmem + 64 + VS;
+    const uint32_t tD_W = tmem, tD2 = tmem + 128, tD3 = tmem + 128 + VS;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
     auto issue_tma = [&](int ic, int stage) {
@@ -391,6 +393,15 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     uint32_t mma_phase = 0;
     bool failed = false;
+    // gate and beta of the next chunk are loaded one chunk ahead (registers of threads 0..63)
+    float g_next = 0.f, b_next = 0.f;
+    if (nch > 0 && tid < C) {
+        const int len0 = (int)(eos - bos < C ? eos - bos : C);
+        if (tid < len0) {
+            g_next = p.g[(bos + tid) * H + h];
+            b_next = bf2f(p.beta[(bos + tid) * H + h]);
+        }
+    }
     for (int ic = 0; ic < nch; ++ic) {
         const int stage = ic & 1;
         const int64_t t0 = bos + (int64_t)ic * C;
@@ -403,11 +414,25 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 *reinterpret_cast<float4 *>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
         }
         {
-            const float gv = (tid < len) ? p.g[(t0 + tid) * H + h] : 0.f;
-            const float gam = chunk_cumsum(gv, &s_carry);
+            const float gam = chunk_cumsum(g_next, &s_carry);
+            const float bcur = b_next;
+            if (tid < C && ic + 1 < nch) {          // prefetch the next chunk's gate and beta
+                const int64_t t1 = t0 + C;
+                const int len1 = (int)(eos - t1 < C ? eos - t1 : C);
+                g_next = tid < len1 ? p.g[(t1 + tid) * H + h] : 0.f;
+                b_next = tid < len1 ? bf2f(p.beta[(t1 + tid) * H + h]) : 0.f;
+            }
             if (tid < C) {
                 sG[tid] = gam;
-                sB[tid] = tid < len ? bf2f(p.beta[(t0 + tid) * H + h]) : 0.f;
+                sB[tid] = bcur;
+            }
+            __syncthreads();
+            if (tid < C) {
+                const bool live = tid < len;
+                const float gc = sG[C - 1];
+                sF[0][tid] = live ? bcur * __expf(gam) : 0.f;
+                sF[1][tid] = live ? __expf(gc - gam) : 0.f;
+                sF[2][tid] = live ? p.scale * __expf(gam) : 0.f;
             }
         }
         mbar_wait(&bar_tma[stage], (ic >> 1) & 1, &s_err, 3);
@@ -416,28 +441,29 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float gC = sG[C - 1];
         uint8_t *ktile = smem + Lay::oK + stage * 16384;
         uint8_t *wq = smem + Lay::oWQ + stage * 32768;
-        // ---- operands: beta Gamma K, exp(g_c - g) K, scale Gamma Q (in place), (beta V)^T
+        // ---- operands: beta Gamma K, exp(g_c - g) K, scale Gamma Q (in place), (beta V)^T.
+        // Task t = 16-byte chunk (t & 7) of row (t >> 3) & 63 in column block t >> 9:
+        // a warp touches 512 contiguous bytes, so the accesses are bank-conflict free.
         {
-            const int r = tid >> 1, cb = tid & 1;
-            const bool live = r < len;
-            const float gr = sG[r];
-            const float f_kb = live ? sB[r] * __expf(gr) : 0.f;
-            const float f_kt = live ? __expf(gC - gr) : 0.f;
-            const float f_q = live ? p.scale * __expf(gr) : 0.f;
-            const uint32_t roff = cb * 8192 + r * 128;
             const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 kv = *reinterpret_cast<const uint4 *>(ktile + roff + q * 16);
-                *reinterpret_cast<uint4 *>(smem + Lay::oKB + roff + q * 16) = live ? scale8(kv, f_kb) : zero;
-                *reinterpret_cast<uint4 *>(smem + Lay::oKT + roff + q * 16) = live ? scale8(kv, f_kt) : zero;
-                uint4 *qp = reinterpret_cast<uint4 *>(wq + cb * 16384 + 8192 + r * 128 + q * 16);
-                *qp = live ? scale8(*qp, f_q) : zero;
+            for (int i = 0; i < 8; ++i) {
+                const int t = i * kThreads + tid;
+                const int r = (t >> 3) & 63;
+                const uint32_t off = (t >> 9) * 8192 + r * 128 + (t & 7) * 16;
+                const bool live = r < len;
+                const uint4 kv = *reinterpret_cast<const uint4 *>(ktile + off);
+                *reinterpret_cast<uint4 *>(smem + Lay::oKB + off) = live ? scale8(kv, sF[0][r]) : zero;
+                *reinterpret_cast<uint4 *>(smem + Lay::oKT + off) = live ? scale8(kv, sF[1][r]) : zero;
+                uint4 *qp = reinterpret_cast<uint4 *>(wq + (t >> 9) * 16384 + 8192 + r * 128 + (t & 7) * 16);
+                *qp = live ? scale8(*qp, sF[2][r]) : zero;
             }
             const __nv_bfloat16 *vt =
                 reinterpret_cast<const __nv_bfloat16 *>(smem + Lay::oV + stage * Lay::kVTile);
-            for (int e = tid; e < C * VS; e += kThreads) {
-                const int rr = e / VS, jj = e % VS;
+#pragma unroll
+            for (int i = 0; i < C * VS / kThreads; ++i) {
+                const int e = i * kThreads + tid;
+                const int rr = e & 63, jj = e >> 6;
                 const float x = rr < len ? sB[rr] * bf2f(vt[rr * VS + jj]) : 0.f;
                 st_bf16(smem, Lay::oVB + sw128_offset(VS, jj, rr), x);
             }
@@ -447,11 +473,11 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t tl_addr = sbase + Lay::oTL + stage * 16384;
         if (tid == 0) {
             tc_fence_after();
-            constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
+            constexpr uint32_t id_w = idesc_bf16(128, 128, 0, 1);
             constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 0);
-            for (int s = 0; s < 4; ++s)      // W^T = (beta Gamma K)^T T^T
-                mma_bf16(tD_W, smem_desc(sbase + Lay::oKB + s * 2048, 8192, 1024, kSwizzle128B),
-                         smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B), id_w, s > 0);
+            for (int s = 0; s < 4; ++s)      // [W; L beta Gamma K] = [T; L] (beta Gamma K)
+                mma_bf16(tD_W, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oKB + s * 2048, 8192, 1024, kSwizzle128B), id_w, s > 0);
             for (int s = 0; s < 4; ++s)      // D2 = [T; L] (beta V)
                 mma_bf16(tD2, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
                          smem_desc(sbase + Lay::oVB + s * 32, 16, 1024, kSwizzle128B), id_v, s > 0);
@@ -460,17 +486,30 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_wait(&bar_mma, mma_phase, &s_err, 4);
         mma_phase ^= 1;
         tc_fence_after();
-        // ---- -W into rows 0..63 of [-W; Qhat]; bottom rows keep L (beta V) for the output
+        // ---- -W (lanes 0..63 of D_W: token rows) into rows 0..63 of [-W; Qhat] with
+        // 16-byte stores; lanes 64..127 keep L (beta V) (rows 64.. of D2) for the output.
         float lvb[VS];
+        if (tid < C) {
+            const int r = tid;
+            const uint32_t rbase = (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float w[16];
-            tmem_ld16(tD_W + lane_off + q * 16, w);
-            tmem_ld_wait();
+            for (int q = 0; q < 8; ++q) {            // 16 keys per TMEM load = two 16-byte chunks
+                float w[16];
+                tmem_ld16(tD_W + lane_off + q * 16, w);
+                tmem_ld_wait();
 #pragma unroll
-            for (int r = 0; r < 16; ++r) st_bf16(wq, sw128_offset(128, q * 16 + r, c), -w[r]);
-        }
-        if (tid >= C) {
+                for (int hc = 0; hc < 2; ++hc) {
+                    const int key0 = q * 16 + hc * 8;          // first key of this 16-byte chunk
+                    uint4 pk;
+                    __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2)
+                        pp[e2] = __floats2bfloat162_rn(-w[hc * 8 + 2 * e2], -w[hc * 8 + 2 * e2 + 1]);
+                    const int cb = key0 >> 6, ch = (key0 & 63) >> 3;
+                    *reinterpret_cast<uint4 *>(wq + cb * 16384 + rbase + ((ch ^ (r & 7)) << 4)) = pk;
+                }
+            }
+        } else {
 #pragma unroll
             for (int q = 0; q < VS / 16; ++q) tmem_ld16(tD2 + lane_off + q * 16, lvb + q * 16);
             tmem_ld_wait();
