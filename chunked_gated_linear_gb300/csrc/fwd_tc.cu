@@ -50,7 +50,7 @@ constexpr int C = 64;
 constexpr int KD = 128;
 constexpr int VD = 128;
 constexpr int kThreads = 128;
-constexpr int kTLRows = 128;   // [T; L] rows per chunk and head
+constexpr int kTLRows = 192;   // [T diag(beta Gamma); T; L] rows per chunk and head
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
@@ -199,7 +199,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         } else {
             const int r = tid - C;
             const float gr = sG[r];
-            uint4 *dst = reinterpret_cast<uint4 *>(tl + (size_t)(C + r) * C);
+            uint4 *dst = reinterpret_cast<uint4 *>(tl + (size_t)(2 * C + r) * C);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 uint4 pk;
@@ -256,20 +256,26 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             __syncthreads();
         }
-        // ---- T (bf16) -> rows 0..63 of the [T; L] block: thread pair per row
+        // ---- T diag(beta Gamma) -> rows 0..63, T -> rows 64..127 (bf16): thread pair per row
         {
             const int r = tid >> 1, half = tid & 1;
-            uint4 *dst = reinterpret_cast<uint4 *>(tl + (size_t)r * C + half * 32);
+            uint4 *dst_s = reinterpret_cast<uint4 *>(tl + (size_t)r * C + half * 32);
+            uint4 *dst_t = reinterpret_cast<uint4 *>(tl + (size_t)(C + r) * C + half * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint4 pk;
-                __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+                uint4 pt, ps;
+                __nv_bfloat162 *ppt = reinterpret_cast<__nv_bfloat162 *>(&pt);
+                __nv_bfloat162 *pps = reinterpret_cast<__nv_bfloat162 *>(&ps);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i0 = half * 32 + q * 8 + 2 * e;
-                    pp[e] = __floats2bfloat162_rn(sT[r * (C + 1) + i0], sT[r * (C + 1) + i0 + 1]);
+                    const float t0v = sT[r * (C + 1) + i0], t1v = sT[r * (C + 1) + i0 + 1];
+                    ppt[e] = __floats2bfloat162_rn(t0v, t1v);
+                    pps[e] = __floats2bfloat162_rn(t0v * sB[i0] * __expf(sG[i0]),
+                                                   t1v * sB[i0 + 1] * __expf(sG[i0 + 1]));
                 }
-                dst[q] = pk;
+                dst_t[q] = pt;
+                dst_s[q] = ps;
             }
         }
     }
@@ -296,19 +302,18 @@ struct ChainParams {
 template <int VS>
 struct ChainLayout {
     static constexpr uint32_t oK = 0;                       // K tiles, 2 stages x 16 KB
-    static constexpr uint32_t oWQ = 32768;                  // [-W; Qhat], 2 stages x 32 KB
-    static constexpr uint32_t oTL = oWQ + 65536;            // [T; L], 2 stages x 16 KB
-    static constexpr uint32_t oKB = oTL + 32768;            // beta Gamma K (MN-major), 16 KB
-    static constexpr uint32_t oKT = oKB + 16384;            // exp(g_c - g) K (MN-major), 16 KB
-    static constexpr uint32_t oSB = oKT + 16384;            // S^T bf16, K-major [2][VS][128 B]
+    static constexpr uint32_t oWQ = 32768;                  // [-W; Q], 2 stages x 32 KB
+    static constexpr uint32_t oTL = oWQ + 65536;            // [T diag(bG); T; L], 2 x 24 KB
+    static constexpr uint32_t oSB = oTL + 49152;            // S^T bf16, K-major [2][VS][128 B]
     static constexpr uint32_t oET = oSB + VS * 256;         // E^T bf16, K-major [VS][128 B]
-    static constexpr uint32_t oVB = oET + VS * 128;         // (beta V)^T bf16, K-major
+    static constexpr uint32_t oFT = oET + VS * 128;         // (exp(g_c - g) E)^T bf16
+    static constexpr uint32_t oVB = oFT + VS * 128;         // (beta V)^T bf16, K-major
     static constexpr uint32_t oV = oVB + VS * 128;          // V tiles [64][VS], 2 stages
     static constexpr uint32_t kVTile = C * VS * 2;
     static constexpr uint32_t total = oV + 2 * kVTile;
     static constexpr uint32_t bytes = total + 1024;         // + alignment slack
-    static constexpr uint32_t tmem_cols = 256;              // D_W 128 + D2 VS + D3 VS
-    static constexpr uint32_t kStageBytes = 16384 + 16384 + 16384 + kVTile;   // per chunk TMA
+    static constexpr uint32_t tmem_cols = 128 + 3 * VS <= 256 ? 256 : 512;
+    static constexpr uint32_t kStageBytes = 16384 + 16384 + 24576 + kVTile;   // per chunk TMA
 };
 
 template <int VS>
@@ -372,7 +377,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tD_W = tmem, tD2 = tmem + 128, tD3 = tmem + 128 + VS;
+    const uint32_t tD_W = tmem, tD2 = tmem + 128, tD3 = tmem + 128 + VS, tD4 = tmem + 128 + 2 * VS;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
     auto issue_tma = [&](int ic, int stage) {
@@ -384,9 +389,9 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint8_t *wq = smem + Lay::oWQ + stage * 32768;
         tma_load_3d(kt, &tm_k, 0, h, t0, bar);
         tma_load_3d(kt + 8192, &tm_k, 64, h, t0, bar);
-        tma_load_3d(wq + 8192, &tm_q, 0, h, t0, bar);            // Q rows 64..127 of [-W; Qhat]
+        tma_load_3d(wq + 8192, &tm_q, 0, h, t0, bar);            // Q rows 64..127 of [-W; Q]
         tma_load_3d(wq + 16384 + 8192, &tm_q, 64, h, t0, bar);
-        tma_load_2d(smem + Lay::oTL + stage * 16384, &tm_tl, 0, tl_y, bar);
+        tma_load_2d(smem + Lay::oTL + stage * 24576, &tm_tl, 0, tl_y, bar);
         tma_load_3d(smem + Lay::oV + stage * Lay::kVTile, &tm_v, v0, h, t0, bar);
     };
     if (tid == 0 && nch > 0) issue_tma(0, 0);
@@ -430,7 +435,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (tid < C) {
                 const bool live = tid < len;
                 const float gc = sG[C - 1];
-                sF[0][tid] = live ? bcur * __expf(gam) : 0.f;
                 sF[1][tid] = live ? __expf(gc - gam) : 0.f;
                 sF[2][tid] = live ? p.scale * __expf(gam) : 0.f;
             }
@@ -441,22 +445,16 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float gC = sG[C - 1];
         uint8_t *ktile = smem + Lay::oK + stage * 16384;
         uint8_t *wq = smem + Lay::oWQ + stage * 32768;
-        // ---- operands: beta Gamma K, exp(g_c - g) K, scale Gamma Q (in place), (beta V)^T.
-        // Task t = 16-byte chunk (t & 7) of row (t >> 3) & 63 in column block t >> 9:
-        // a warp touches 512 contiguous bytes, so the accesses are bank-conflict free.
+        // ---- operands: (beta V)^T slice; K rows past the end of a partial chunk are zeroed
+        // (they may hold the next sequence or NaN padding and K enters the MMAs raw).
         {
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = i * kThreads + tid;
-                const int r = (t >> 3) & 63;
-                const uint32_t off = (t >> 9) * 8192 + r * 128 + (t & 7) * 16;
-                const bool live = r < len;
-                const uint4 kv = *reinterpret_cast<const uint4 *>(ktile + off);
-                *reinterpret_cast<uint4 *>(smem + Lay::oKB + off) = live ? scale8(kv, sF[0][r]) : zero;
-                *reinterpret_cast<uint4 *>(smem + Lay::oKT + off) = live ? scale8(kv, sF[1][r]) : zero;
-                uint4 *qp = reinterpret_cast<uint4 *>(wq + (t >> 9) * 16384 + 8192 + r * 128 + (t & 7) * 16);
-                *qp = live ? scale8(*qp, sF[2][r]) : zero;
+            if (len < C) {
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                for (int t = tid; t < 2 * C * 8; t += kThreads) {
+                    const int r = (t >> 3) & 63;
+                    if (r >= len)
+                        *reinterpret_cast<uint4 *>(ktile + (t >> 9) * 8192 + r * 128 + (t & 7) * 16) = zero;
+                }
             }
             const __nv_bfloat16 *vt =
                 reinterpret_cast<const __nv_bfloat16 *>(smem + Lay::oV + stage * Lay::kVTile);
@@ -470,16 +468,18 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         fence_async_smem();
         __syncthreads();
-        const uint32_t tl_addr = sbase + Lay::oTL + stage * 16384;
+        const uint32_t tl_addr = sbase + Lay::oTL + stage * 24576;     // [T bG; T] window
+        const uint32_t tl2_addr = tl_addr + 8192;                        // [T; L] window
+        const uint32_t k_addr = sbase + Lay::oK + stage * 16384;
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id_w = idesc_bf16(128, 128, 0, 1);
             constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 0);
-            for (int s = 0; s < 4; ++s)      // [W; L beta Gamma K] = [T; L] (beta Gamma K)
+            for (int s = 0; s < 4; ++s)      // [W; T K] = [T diag(beta Gamma); T] K
                 mma_bf16(tD_W, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oKB + s * 2048, 8192, 1024, kSwizzle128B), id_w, s > 0);
-            for (int s = 0; s < 4; ++s)      // D2 = [T; L] (beta V)
-                mma_bf16(tD2, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B), id_w, s > 0);
+            for (int s = 0; s < 4; ++s)      // D2 = [T; L] (beta V) = [U; L beta V]
+                mma_bf16(tD2, smem_desc(tl2_addr + s * 32, 16, 1024, kSwizzle128B),
                          smem_desc(sbase + Lay::oVB + s * 32, 16, 1024, kSwizzle128B), id_v, s > 0);
             mma_commit(&bar_mma);
         }
@@ -532,16 +532,20 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_wait(&bar_mma, mma_phase, &s_err, 5);
         mma_phase ^= 1;
         tc_fence_after();
-        // ---- E (rows 0..63 of D2) -> E^T bf16
+        // ---- E (rows 0..63 of D2) -> E^T and (exp(g_c - g) E)^T, bf16
         if (tid < C) {
+            const float f = sF[1][tid];
 #pragma unroll
             for (int q = 0; q < VS / 16; ++q) {
                 float e[16];
                 tmem_ld16(tD2 + lane_off + q * 16, e);
                 tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    st_bf16(smem, Lay::oET + sw128_offset(VS, q * 16 + jj, tid), e[jj]);
+                for (int jj = 0; jj < 16; ++jj) {
+                    const uint32_t off = sw128_offset(VS, q * 16 + jj, tid);
+                    st_bf16(smem, Lay::oET + off, e[jj]);
+                    st_bf16(smem, Lay::oFT + off, f * e[jj]);
+                }
             }
         }
         fence_async_smem();
@@ -552,12 +556,12 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_after();
             constexpr uint32_t id_s = idesc_bf16(128, VS, 1, 0);
             constexpr uint32_t id_o = idesc_bf16(128, VS, 0, 0);
-            for (int s = 0; s < 4; ++s)      // D3 = Ktil^T E
-                mma_bf16(tD3, smem_desc(sbase + Lay::oKT + s * 2048, 8192, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oET + s * 32, 16, 1024, kSwizzle128B), id_s, s > 0);
-            for (int s = 0; s < 4; ++s)      // D2 += [T; L] E
-                mma_bf16(tD2, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oET + s * 32, 16, 1024, kSwizzle128B), id_o, 1);
+            for (int s = 0; s < 4; ++s)      // D3 = K^T (exp(g_c - g) E)
+                mma_bf16(tD3, smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oFT + s * 32, 16, 1024, kSwizzle128B), id_s, s > 0);
+            for (int s = 0; s < 4; ++s)      // D4 = [T; L] E
+                mma_bf16(tD4, smem_desc(tl2_addr + s * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oET + s * 32, 16, 1024, kSwizzle128B), id_o, s > 0);
             mma_commit(&bar_mma);
         }
         mbar_wait(&bar_mma, mma_phase, &s_err, 6);
@@ -580,10 +584,12 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     st_bf16(smem, Lay::oSB + sw128_offset(VS, q * 16 + jj, c), S[q * 16 + jj]);
                 }
                 if (tid >= C) {                       // warp-uniform: warps 2 and 3
-                    float d2[16];
+                    float d2[16], d4[16];
                     tmem_ld16(tD2 + lane_off + q * 16, d2);
+                    tmem_ld16(tD4 + lane_off + q * 16, d4);
                     tmem_ld_wait();
                     if (store) {
+                        const float fq = sF[2][r];
 #pragma unroll
                         for (int jj = 0; jj < 16; jj += 8) {
                             uint4 pk;
@@ -591,8 +597,9 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                             for (int e2 = 0; e2 < 4; ++e2) {
                                 const int a = jj + 2 * e2;
-                                pp[e2] = __floats2bfloat162_rn(d2[a] - lvb[q * 16 + a],
-                                                               d2[a + 1] - lvb[q * 16 + a + 1]);
+                                pp[e2] = __floats2bfloat162_rn(
+                                    fmaf(fq, d2[a] - lvb[q * 16 + a], d4[a]),
+                                    fmaf(fq, d2[a + 1] - lvb[q * 16 + a + 1], d4[a + 1]));
                             }
                             *reinterpret_cast<uint4 *>(dst + q * 16 + jj) = pk;
                         }
