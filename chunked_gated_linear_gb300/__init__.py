@@ -71,6 +71,10 @@ def load_library(path: str = LIB_PATH):
     for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
         getattr(lib, fn).restype = ctypes.c_int
         getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs), vp]
+    lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.gdn_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(FwdArgs), vp]
+    lib.gcl_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    lib.gcl_noalloc_scratch_bytes.argtypes = []
     lib.gcl_fwd_workspace_bytes.restype = ctypes.c_size_t
     lib.gcl_fwd_workspace_bytes.argtypes = [ctypes.POINTER(FwdArgs)]
     lib.gdn_chunk_bwd.restype = ctypes.c_int
@@ -160,6 +164,18 @@ def fwd_workspace_bytes(*args, **kw) -> int:
 def gdn_chunk_fwd(*args, stream=None, **kw):
     a = fwd_args(*args, **kw)
     _check("gdn_chunk_fwd", lib().gdn_chunk_fwd(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_chunk_fwd_noalloc(*args, stream=None, **kw):
+    """gdn_chunk_fwd without a workspace argument: the library's static scratch is used
+    (for callers that cannot allocate device memory; see include/gcl.h)."""
+    kw.pop("workspace", None)
+    a = fwd_args(*args, **kw)
+    _check("gdn_chunk_fwd_noalloc", lib().gdn_chunk_fwd_noalloc(ctypes.byref(a), _stream(stream)))
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(lib().gcl_noalloc_scratch_bytes())
 
 
 def kda_chunk_fwd(*args, stream=None, **kw):

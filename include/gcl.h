@@ -173,6 +173,35 @@ gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
 gcl_status_t kda_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
 
 /*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate device
+ * memory.  The paper has no counterpart; this is a convenience of this library.
+ *
+ * Some callers cannot hand the forward a workspace: code running inside a CUDA
+ * graph capture whose allocator is not capture-aware, runtimes that fix their
+ * memory budget at start-up and forbid later cudaMalloc calls, and plugin hosts
+ * that pass tensors in but offer no allocator.  This entry point takes the same
+ * arguments as gdn_chunk_fwd but ignores args->workspace / workspace_bytes: the
+ * scratch lives in a static device array of gcl_noalloc_scratch_bytes() bytes
+ * (32 MiB) inside the library, which every GPU that loads the library holds
+ * until the process exits.  It allocates and frees nothing.
+ *
+ *  - Sizes whose scratch (gcl_fwd_workspace_bytes) exceeds that limit return
+ *    GCL_ERR_CAPACITY before any work is enqueued.  The bf16 K = V = 128 path
+ *    needs 24 KiB per chunk and head, i.e. up to 1365 chunk-heads (for example
+ *    T = 4096 tokens with 16 heads).
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current) and caches it; make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the array and leave their contents in it;
+ *    calls whose GPU executions overlap (unordered streams, concurrent graph
+ *    replays) race on it and give wrong results.
+ */
+gcl_status_t gdn_chunk_fwd_noalloc(const gcl_fwd_args *args, gcl_stream_t stream);
+
+/* Size in bytes of the static scratch array used by gdn_chunk_fwd_noalloc. */
+size_t gcl_noalloc_scratch_bytes(void);
+
+/*
  * Backward arguments (GDN).  All pointers are device pointers.
  */
 typedef struct gcl_bwd_args {
