@@ -54,16 +54,6 @@ constexpr int kTLRows = 192;   // [T diag(beta Gamma); T; L] rows per chunk and 
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-__device__ __forceinline__ uint4 scale8(uint4 v, float f) {
-    __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 x = __bfloat1622float2(p[i]);
-        p[i] = __floats2bfloat162_rn(x.x * f, x.y * f);
-    }
-    return v;
-}
-
 // Inclusive scan of one float per lane across a warp.
 __device__ __forceinline__ float warp_incl_scan(float x) {
     const int lane = threadIdx.x & 31;
@@ -299,6 +289,8 @@ struct ChainParams {
     float scale;
 };
 
+constexpr int kChainThreads = 256;
+
 template <int VS>
 struct ChainLayout {
     static constexpr uint32_t oK = 0;                       // K tiles, 2 stages x 16 KB
@@ -312,27 +304,39 @@ struct ChainLayout {
     static constexpr uint32_t kVTile = C * VS * 2;
     static constexpr uint32_t total = oV + 2 * kVTile;
     static constexpr uint32_t bytes = total + 1024;         // + alignment slack
-    static constexpr uint32_t tmem_cols = 128 + 3 * VS <= 256 ? 256 : 512;
+    // TMEM: D_W 128 | U (2 stages) | [-W S; Q S] | K^T (f E) | [T; L] E
+    static constexpr uint32_t tD2p = 128, tD2c = 128 + 2 * VS, tD3 = 128 + 3 * VS,
+                              tD4 = 128 + 4 * VS;
+    static constexpr uint32_t tmem_cols = 128 + 5 * VS <= 256 ? 256 : 512;
     static constexpr uint32_t kStageBytes = 16384 + 16384 + 24576 + kVTile;   // per chunk TMA
 };
 
+// Per-(sequence, head, column slice) state recurrence.  256 threads; thread t
+// owns TMEM lane / state row 32 (w & 3) + (t & 31) of warp w and the column half
+// (w >> 2) of the slice, so every per-column step is split over two warpgroups.
+// Software pipeline per chunk n (one thread issues every TMA and MMA):
+//   C1(n) | map(n+1): gates, (beta V)^T, P1/P2(n+1) | E(n) | C2,C3(n) | W(n+1) | S,O(n) | TMA(n+2)
+// so the state-independent work of chunk n+1 runs while chunk n's MMAs execute.
 template <int VS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_tl,
                 ChainParams p) {
     using Lay = ChainLayout<VS>;
+    constexpr int HV = VS / 2;                              // columns per thread
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t bar_tma[2], bar_mma;
+    __shared__ uint64_t bar_tma[2], bar_c1, bar_c23, bar_p;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
-    __shared__ float sG[C], sB[C];
-    __shared__ float s_carry;
-    __shared__ float sF[3][C];       // per-row scale factors: beta Gamma, exp(g_c - g), scale Gamma
+    __shared__ float s_carry, s_gc;
+    __shared__ float sFE[2][C], sFQ[2][C], sB[2][C], sGC[2];
 
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + (tid & 31);              // TMEM lane owned by this thread
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int split = blockIdx.x, h = blockIdx.y;
     const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
     const int H = p.H, v0 = split * VS;
@@ -350,11 +354,14 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sbase = smem_u32(smem);
     const int64_t KV = (int64_t)KD * VD;
     const int64_t state_base = ((int64_t)n * H + h) * KV;
+    const int c0 = half * HV;                               // first column of this thread
 
     if (tid == 0) {
         mbar_init(&bar_tma[0], 1);
         mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_c1, 1);
+        mbar_init(&bar_c23, 1);
+        mbar_init(&bar_p, 1);
         s_err = 0;
         fence_barrier_init();
     }
@@ -362,25 +369,26 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_alloc(&s_tmem, Lay::tmem_cols);
         tmem_relinquish();
     }
-    // state slice: thread c owns key row c
-    const int c = tid;
-    float S[VS];
+    float S[HV];
     {
-        const float *src = p.h0 ? p.h0 + state_base + (int64_t)c * VD + v0 : nullptr;
+        const float *src = p.h0 ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
 #pragma unroll
-        for (int jj = 0; jj < VS; ++jj) S[jj] = src ? src[jj] : 0.f;
+        for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
 #pragma unroll
-        for (int jj = 0; jj < VS; ++jj) st_bf16(smem, Lay::oSB + sw128_offset(VS, jj, c), S[jj]);
+        for (int j = 0; j < HV; ++j) st_bf16(smem, Lay::oSB + sw128_offset(VS, c0 + j, row), S[j]);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tD_W = tmem, tD2 = tmem + 128, tD3 = tmem + 128 + VS, tD4 = tmem + 128 + 2 * VS;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-    auto issue_tma = [&](int ic, int stage) {
+    auto chunk_len = [&](int ic) -> int {
+        const int64_t t0 = bos + (int64_t)ic * C;
+        return (int)(eos - t0 < C ? eos - t0 : C);
+    };
+    auto issue_tma = [&](int ic) {
+        const int stage = ic & 1;
         const int t0 = (int)(bos + (int64_t)ic * C);
         const int tl_y = (int)(((row0 + ic) * H + h) * kTLRows);
         uint64_t *bar = &bar_tma[stage];
@@ -394,229 +402,236 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_2d(smem + Lay::oTL + stage * 24576, &tm_tl, 0, tl_y, bar);
         tma_load_3d(smem + Lay::oV + stage * Lay::kVTile, &tm_v, v0, h, t0, bar);
     };
-    if (tid == 0 && nch > 0) issue_tma(0, 0);
-
-    uint32_t mma_phase = 0;
-    bool failed = false;
-    // gate and beta of the next chunk are loaded one chunk ahead (registers of threads 0..63)
-    float g_next = 0.f, b_next = 0.f;
-    if (nch > 0 && tid < C) {
-        const int len0 = (int)(eos - bos < C ? eos - bos : C);
-        if (tid < len0) {
-            g_next = p.g[(bos + tid) * H + h];
-            b_next = bf2f(p.beta[(bos + tid) * H + h]);
-        }
-    }
-    for (int ic = 0; ic < nch; ++ic) {
-        const int stage = ic & 1;
-        const int64_t t0 = bos + (int64_t)ic * C;
-        const int len = (int)(eos - t0 < C ? eos - t0 : C);
-        if (tid == 0 && ic + 1 < nch) issue_tma(ic + 1, stage ^ 1);
-        if (p.h_save) {
-            float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)c * VD + v0;
-#pragma unroll
-            for (int jj = 0; jj < VS; jj += 4)
-                *reinterpret_cast<float4 *>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
-        }
-        {
-            const float gam = chunk_cumsum(g_next, &s_carry);
-            const float bcur = b_next;
-            if (tid < C && ic + 1 < nch) {          // prefetch the next chunk's gate and beta
-                const int64_t t1 = t0 + C;
-                const int len1 = (int)(eos - t1 < C ? eos - t1 : C);
-                g_next = tid < len1 ? p.g[(t1 + tid) * H + h] : 0.f;
-                b_next = tid < len1 ? bf2f(p.beta[(t1 + tid) * H + h]) : 0.f;
-            }
-            if (tid < C) {
-                sG[tid] = gam;
-                sB[tid] = bcur;
-            }
-            __syncthreads();
-            if (tid < C) {
-                const bool live = tid < len;
-                const float gc = sG[C - 1];
-                sF[1][tid] = live ? __expf(gc - gam) : 0.f;
-                sF[2][tid] = live ? p.scale * __expf(gam) : 0.f;
-            }
-        }
-        mbar_wait(&bar_tma[stage], (ic >> 1) & 1, &s_err, 3);
+    auto sync_all = [&]() {
+        tc_fence_before();
         __syncthreads();
-        if (s_err) { failed = true; break; }
-        const float gC = sG[C - 1];
-        uint8_t *ktile = smem + Lay::oK + stage * 16384;
-        uint8_t *wq = smem + Lay::oWQ + stage * 32768;
-        // ---- operands: (beta V)^T slice; K rows past the end of a partial chunk are zeroed
-        // (they may hold the next sequence or NaN padding and K enters the MMAs raw).
-        {
-            if (len < C) {
-                const uint4 zero = make_uint4(0, 0, 0, 0);
-                for (int t = tid; t < 2 * C * 8; t += kThreads) {
-                    const int r = (t >> 3) & 63;
-                    if (r >= len)
-                        *reinterpret_cast<uint4 *>(ktile + (t >> 9) * 8192 + r * 128 + (t & 7) * 16) = zero;
-                }
+        tc_fence_after();
+    };
+
+    // gate and beta of the chunk being prepared, loaded one chunk ahead (threads 0..63)
+    float g_next = 0.f, b_next = 0.f;
+    auto load_gate = [&](int ic) {
+        g_next = 0.f;
+        b_next = 0.f;
+        if (ic < nch && tid < C && tid < chunk_len(ic)) {
+            const int64_t t = bos + (int64_t)ic * C + tid;
+            g_next = p.g[t * H + h];
+            b_next = bf2f(p.beta[t * H + h]);
+        }
+    };
+
+    // State-independent work of chunk ic: gate cumsum and factors, zeroing of K
+    // rows past the end of a partial chunk, the (beta V)^T slice.
+    auto map_chunk = [&](int ic) {
+        const int st = ic & 1, len = chunk_len(ic);
+        const float gam = chunk_cumsum(g_next, &s_carry);   // contains a block barrier
+        // gamma_c is the last row's gamma (rows past the end of the sequence have g = 0)
+        if (tid == C - 1) s_gc = gam;
+        __syncthreads();    // also orders the cumsum's reads of s_carry before its next use
+        if (tid < C) {
+            const bool live = tid < len;
+            sB[st][tid] = b_next;
+            sFE[st][tid] = live ? __expf(s_gc - gam) : 0.f;
+            sFQ[st][tid] = live ? p.scale * __expf(gam) : 0.f;
+            if (tid == C - 1) sGC[st] = __expf(gam);
+        }
+        load_gate(ic + 1);
+        mbar_wait(&bar_tma[st], (ic >> 1) & 1, &s_err, 3);
+        __syncthreads();
+        uint8_t *ktile = smem + Lay::oK + st * 16384;
+        if (len < C) {
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            for (int t = tid; t < 2 * C * 8; t += kChainThreads) {
+                const int r = (t >> 3) & 63;
+                if (r >= len)
+                    *reinterpret_cast<uint4 *>(ktile + (t >> 9) * 8192 + r * 128 + (t & 7) * 16) = zero;
             }
-            const __nv_bfloat16 *vt =
-                reinterpret_cast<const __nv_bfloat16 *>(smem + Lay::oV + stage * Lay::kVTile);
+        }
+        const __nv_bfloat16 *vt =
+            reinterpret_cast<const __nv_bfloat16 *>(smem + Lay::oV + st * Lay::kVTile);
 #pragma unroll
-            for (int i = 0; i < C * VS / kThreads; ++i) {
-                const int e = i * kThreads + tid;
-                const int rr = e & 63, jj = e >> 6;
-                const float x = rr < len ? sB[rr] * bf2f(vt[rr * VS + jj]) : 0.f;
-                st_bf16(smem, Lay::oVB + sw128_offset(VS, jj, rr), x);
-            }
+        for (int i = 0; i < C * VS / kChainThreads; ++i) {
+            const int e = i * kChainThreads + tid;
+            const int rr = e & 63, jj = e >> 6;
+            const float x = rr < len ? sB[st][rr] * bf2f(vt[rr * VS + jj]) : 0.f;
+            st_bf16(smem, Lay::oVB + sw128_offset(VS, jj, rr), x);
         }
         fence_async_smem();
-        __syncthreads();
-        const uint32_t tl_addr = sbase + Lay::oTL + stage * 24576;     // [T bG; T] window
-        const uint32_t tl2_addr = tl_addr + 8192;                        // [T; L] window
-        const uint32_t k_addr = sbase + Lay::oK + stage * 16384;
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_w = idesc_bf16(128, 128, 0, 1);
-            constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 0);
-            for (int s = 0; s < 4; ++s)      // [W; T K] = [T diag(beta Gamma); T] K
-                mma_bf16(tD_W, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B), id_w, s > 0);
-            for (int s = 0; s < 4; ++s)      // D2 = [T; L] (beta V) = [U; L beta V]
-                mma_bf16(tD2, smem_desc(tl2_addr + s * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oVB + s * 32, 16, 1024, kSwizzle128B), id_v, s > 0);
-            mma_commit(&bar_mma);
-        }
-        mbar_wait(&bar_mma, mma_phase, &s_err, 4);
-        mma_phase ^= 1;
+        sync_all();
+    };
+    // P1: [W; T K] = [T diag(beta Gamma); T] K;  P2: U-stage = [T; L] (beta V)^T
+    auto issue_p = [&](int ic) {
+        const int st = ic & 1;
+        const uint32_t tl_addr = sbase + Lay::oTL + st * 24576;
+        const uint32_t k_addr = sbase + Lay::oK + st * 16384;
+        constexpr uint32_t id_w = idesc_bf16(128, 128, 0, 1);
+        constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 0);
+        for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
+                     smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B), id_w, s > 0);
+        for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem + Lay::tD2p + st * VS, smem_desc(tl_addr + 8192 + s * 32, 16, 1024, kSwizzle128B),
+                     smem_desc(sbase + Lay::oVB + s * 32, 16, 1024, kSwizzle128B), id_v, s > 0);
+        mma_commit(&bar_p);
+    };
+    // -W (D_W lanes 0..63) into rows 0..63 of [-W; Q] of the chunk's stage.
+    auto write_w = [&](int ic) {
+        mbar_wait(&bar_p, ic & 1, &s_err, 4);
         tc_fence_after();
-        // ---- -W (lanes 0..63 of D_W: token rows) into rows 0..63 of [-W; Qhat] with
-        // 16-byte stores; lanes 64..127 keep L (beta V) (rows 64.. of D2) for the output.
-        float lvb[VS];
-        if (tid < C) {
-            const int r = tid;
-            const uint32_t rbase = (r >> 3) * 1024 + (r & 7) * 128;
+        if (quarter < 2) {
+            uint8_t *wq = smem + Lay::oWQ + (ic & 1) * 32768;
+            const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {            // 16 keys per TMEM load = two 16-byte chunks
+            for (int q = 0; q < 4; ++q) {
                 float w[16];
-                tmem_ld16(tD_W + lane_off + q * 16, w);
+                tmem_ld16(tmem + lane_off + half * 64 + q * 16, w);
                 tmem_ld_wait();
 #pragma unroll
                 for (int hc = 0; hc < 2; ++hc) {
-                    const int key0 = q * 16 + hc * 8;          // first key of this 16-byte chunk
+                    const int key0 = half * 64 + q * 16 + hc * 8;
                     uint4 pk;
                     __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2)
                         pp[e2] = __floats2bfloat162_rn(-w[hc * 8 + 2 * e2], -w[hc * 8 + 2 * e2 + 1]);
                     const int cb = key0 >> 6, ch = (key0 & 63) >> 3;
-                    *reinterpret_cast<uint4 *>(wq + cb * 16384 + rbase + ((ch ^ (r & 7)) << 4)) = pk;
+                    *reinterpret_cast<uint4 *>(wq + cb * 16384 + rbase + ((ch ^ (row & 7)) << 4)) = pk;
+                }
+            }
+        }
+        fence_async_smem();
+        sync_all();
+    };
+
+    // ---- prologue: chunks 0 and 1 in flight, operands of chunk 0 ready
+    if (tid == 0 && nch > 0) issue_tma(0);
+    if (tid == 0 && nch > 1) issue_tma(1);
+    load_gate(0);
+    if (nch > 0) {
+        map_chunk(0);
+        if (tid == 0) issue_p(0);
+        write_w(0);
+    }
+
+    bool failed = false;
+    for (int ic = 0; ic < nch; ++ic) {
+        const int st = ic & 1, len = chunk_len(ic);
+        const int64_t t0 = bos + (int64_t)ic * C;
+        if (p.h_save) {
+            float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
+#pragma unroll
+            for (int j = 0; j < HV; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+        // C1: [-W S; Q S] = [-W; Q] S
+        if (tid == 0) {
+            constexpr uint32_t id = idesc_bf16(128, VS, 0, 0);
+            const uint32_t wq_addr = sbase + Lay::oWQ + st * 32768;
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tmem + Lay::tD2c,
+                         smem_desc(wq_addr + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(sbase + Lay::oSB + (s >> 2) * (VS * 128) + (s & 3) * 32, 16, 1024,
+                                   kSwizzle128B),
+                         id, s > 0);
+            mma_commit(&bar_c1);
+        }
+        // map of the next chunk while C1 runs
+        if (ic + 1 < nch) {
+            map_chunk(ic + 1);
+            if (tid == 0) issue_p(ic + 1);
+        }
+        // E = U - W S (rows 0..63) -> E^T and (exp(g_c - g) E)^T; Q S (rows 64..127) kept
+        mbar_wait(&bar_c1, ic & 1, &s_err, 5);
+        tc_fence_after();
+        float qs[HV];
+        if (quarter < 2) {
+            const float f = sFE[st][row];
+#pragma unroll
+            for (int q = 0; q < HV / 8; ++q) {
+                float u[8], ws[8];
+                tmem_ld8(tmem + lane_off + Lay::tD2p + st * VS + c0 + q * 8, u);
+                tmem_ld8(tmem + lane_off + Lay::tD2c + c0 + q * 8, ws);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float e = u[j] + ws[j];
+                    const uint32_t off = sw128_offset(VS, c0 + q * 8 + j, row);
+                    st_bf16(smem, Lay::oET + off, e);
+                    st_bf16(smem, Lay::oFT + off, f * e);
                 }
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < VS / 16; ++q) tmem_ld16(tD2 + lane_off + q * 16, lvb + q * 16);
+            for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + Lay::tD2c + c0 + q * 8, qs + q * 8);
             tmem_ld_wait();
         }
         fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (s_err) { failed = true; break; }
+        sync_all();
+        // C2: K^T (f E);  C3: [T; L] E
         if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(128, VS, 0, 0);
-            const uint32_t wq_addr = sbase + Lay::oWQ + stage * 32768;
-            for (int s = 0; s < 8; ++s)      // D2 += [-W; Qhat] S
-                mma_bf16(tD2, smem_desc(wq_addr + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oSB + (s >> 2) * (VS * 128) + (s & 3) * 32, 16, 1024,
-                                   kSwizzle128B),
-                         id, 1);
-            mma_commit(&bar_mma);
-        }
-        mbar_wait(&bar_mma, mma_phase, &s_err, 5);
-        mma_phase ^= 1;
-        tc_fence_after();
-        // ---- E (rows 0..63 of D2) -> E^T and (exp(g_c - g) E)^T, bf16
-        if (tid < C) {
-            const float f = sF[1][tid];
-#pragma unroll
-            for (int q = 0; q < VS / 16; ++q) {
-                float e[16];
-                tmem_ld16(tD2 + lane_off + q * 16, e);
-                tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const uint32_t off = sw128_offset(VS, q * 16 + jj, tid);
-                    st_bf16(smem, Lay::oET + off, e[jj]);
-                    st_bf16(smem, Lay::oFT + off, f * e[jj]);
-                }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (s_err) { failed = true; break; }
-        if (tid == 0) {
-            tc_fence_after();
             constexpr uint32_t id_s = idesc_bf16(128, VS, 1, 0);
             constexpr uint32_t id_o = idesc_bf16(128, VS, 0, 0);
-            for (int s = 0; s < 4; ++s)      // D3 = K^T (exp(g_c - g) E)
-                mma_bf16(tD3, smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B),
+            const uint32_t k_addr = sbase + Lay::oK + st * 16384;
+            const uint32_t tl2_addr = sbase + Lay::oTL + st * 24576 + 8192;
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + Lay::tD3, smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B),
                          smem_desc(sbase + Lay::oFT + s * 32, 16, 1024, kSwizzle128B), id_s, s > 0);
-            for (int s = 0; s < 4; ++s)      // D4 = [T; L] E
-                mma_bf16(tD4, smem_desc(tl2_addr + s * 32, 16, 1024, kSwizzle128B),
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + Lay::tD4, smem_desc(tl2_addr + s * 32, 16, 1024, kSwizzle128B),
                          smem_desc(sbase + Lay::oET + s * 32, 16, 1024, kSwizzle128B), id_o, s > 0);
-            mma_commit(&bar_mma);
+            mma_commit(&bar_c23);
         }
-        mbar_wait(&bar_mma, mma_phase, &s_err, 6);
-        mma_phase ^= 1;
+        // -W of the next chunk while C2/C3 run
+        if (ic + 1 < nch) write_w(ic + 1);
+        // S <- Gamma_c S + K^T (f E);  O = scale Gamma Q S + L E
+        mbar_wait(&bar_c23, ic & 1, &s_err, 6);
         tc_fence_after();
-        // ---- state update (all rows) and output (rows 64..127 of D2)
         {
-            const float GC = __expf(gC);
-            const int r = tid - C;
-            const bool store = tid >= C && r < len && p.o != nullptr;
-            __nv_bfloat16 *dst = store ? p.o + ((t0 + r) * H + h) * (int64_t)VD + v0 : nullptr;
+            const float GC = sGC[st];
 #pragma unroll
-            for (int q = 0; q < VS / 16; ++q) {
-                float d3[16];
-                tmem_ld16(tD3 + lane_off + q * 16, d3);
+            for (int q = 0; q < HV / 8; ++q) {
+                float d3[8];
+                tmem_ld8(tmem + lane_off + Lay::tD3 + c0 + q * 8, d3);
                 tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    S[q * 16 + jj] = fmaf(GC, S[q * 16 + jj], d3[jj]);
-                    st_bf16(smem, Lay::oSB + sw128_offset(VS, q * 16 + jj, c), S[q * 16 + jj]);
+                for (int j = 0; j < 8; ++j) {
+                    S[q * 8 + j] = fmaf(GC, S[q * 8 + j], d3[j]);
+                    st_bf16(smem, Lay::oSB + sw128_offset(VS, c0 + q * 8 + j, row), S[q * 8 + j]);
                 }
-                if (tid >= C) {                       // warp-uniform: warps 2 and 3
-                    float d2[16], d4[16];
-                    tmem_ld16(tD2 + lane_off + q * 16, d2);
-                    tmem_ld16(tD4 + lane_off + q * 16, d4);
-                    tmem_ld_wait();
-                    if (store) {
-                        const float fq = sF[2][r];
+            }
+            if (quarter >= 2) {
+                const int r = row - C;
+                float d4[HV];
 #pragma unroll
-                        for (int jj = 0; jj < 16; jj += 8) {
-                            uint4 pk;
-                            __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+                for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + Lay::tD4 + c0 + q * 8, d4 + q * 8);
+                tmem_ld_wait();
+                if (r < len && p.o != nullptr) {
+                    const float fq = sFQ[st][r];
+                    __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * (int64_t)VD + v0 + c0;
 #pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                const int a = jj + 2 * e2;
-                                pp[e2] = __floats2bfloat162_rn(
-                                    fmaf(fq, d2[a] - lvb[q * 16 + a], d4[a]),
-                                    fmaf(fq, d2[a + 1] - lvb[q * 16 + a + 1], d4[a + 1]));
-                            }
-                            *reinterpret_cast<uint4 *>(dst + q * 16 + jj) = pk;
-                        }
+                    for (int j = 0; j < HV; j += 8) {
+                        uint4 pk;
+                        __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2)
+                            pp[e2] = __floats2bfloat162_rn(fmaf(fq, qs[j + 2 * e2], d4[j + 2 * e2]),
+                                                           fmaf(fq, qs[j + 2 * e2 + 1], d4[j + 2 * e2 + 1]));
+                        *reinterpret_cast<uint4 *>(dst + j) = pk;
                     }
                 }
             }
         }
         fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        sync_all();
         if (s_err) { failed = true; break; }
+        // stage st is free: fetch chunk ic + 2 into it
+        if (tid == 0 && ic + 2 < nch) issue_tma(ic + 2);
     }
     if (!failed && p.ht) {
-        float *dst = p.ht + state_base + (int64_t)c * VD + v0;
+        float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
 #pragma unroll
-        for (int jj = 0; jj < VS; jj += 4)
-            *reinterpret_cast<float4 *>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+        for (int j = 0; j < HV; j += 4)
+            *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     tc_fence_before();
     __syncthreads();
@@ -657,7 +672,7 @@ cudaError_t launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(n_split, H, n_max), kThreads, Lay::bytes, s>>>(mq, mk, mv, mtl, cp);
+    kern<<<dim3(n_split, H, n_max), kChainThreads, Lay::bytes, s>>>(mq, mk, mv, mtl, cp);
     return cudaGetLastError();
 }
 
