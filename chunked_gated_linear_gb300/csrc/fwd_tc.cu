@@ -50,7 +50,9 @@ constexpr int C = 64;
 constexpr int KD = 128;
 constexpr int VD = 128;
 constexpr int kThreads = 128;
-constexpr int kTLRows = 192;   // [T diag(beta Gamma); T; L] rows per chunk and head
+constexpr int kTLRows = 192;   // [T diag(beta Gamma); T diag(beta); L] rows per chunk and head
+constexpr int kFRows = 4;      // per-chunk factors (fp32 rows of 64): exp(g_c - g), scale exp(g),
+                               // exp(g_c) (broadcast), unused
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
@@ -78,16 +80,14 @@ __device__ __forceinline__ float chunk_cumsum(float g, float *s_carry) {
     return x;
 }
 
-__device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
-}
 
 // ============================================================================ prep
 struct PrepParams {
     const int32_t *chunk_indices, *cu;
     const float *g;
     const __nv_bfloat16 *beta;
-    __nv_bfloat16 *tl;          // [nt_max, H, 128, 64]
+    __nv_bfloat16 *tl;          // [nt_max, H, 192, 64]
+    float *fac;                 // [nt_max, H, 4, 64]
     int32_t *status;
     int64_t t_max;
     int32_t n_max, H;
@@ -182,7 +182,12 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         __nv_bfloat16 *tl = p.tl + ((size_t)j * H + h) * kTLRows * C;
         if (tid < C) {
             const int r = tid;
-            const float gr = sG[r], br = sB[r];
+            const float gr = sG[r], br = sB[r], gc = sG[C - 1];
+            const bool live = r < len;
+            float *fac = p.fac + ((size_t)j * H + h) * kFRows * C;
+            fac[r] = live ? __expf(gc - gr) : 0.f;               // state-update decay of row r
+            fac[C + r] = live ? p.scale * __expf(gr) : 0.f;     // read-out factor of row r
+            fac[2 * C + r] = __expf(gc);                         // chunk decay Gamma_c
 #pragma unroll
             for (int i = 0; i < C; ++i)
                 sA[r * (C + 1) + i] = (i < r && r < len) ? br * __expf(gr - sG[i]) * v[i] : 0.f;
@@ -246,7 +251,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             __syncthreads();
         }
-        // ---- T diag(beta Gamma) -> rows 0..63, T -> rows 64..127 (bf16): thread pair per row
+        // ---- T diag(beta Gamma) -> rows 0..63, T diag(beta) -> rows 64..127 (bf16)
         {
             const int r = tid >> 1, half = tid & 1;
             uint4 *dst_s = reinterpret_cast<uint4 *>(tl + (size_t)r * C + half * 32);
@@ -260,7 +265,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int e = 0; e < 4; ++e) {
                     const int i0 = half * 32 + q * 8 + 2 * e;
                     const float t0v = sT[r * (C + 1) + i0], t1v = sT[r * (C + 1) + i0 + 1];
-                    ppt[e] = __floats2bfloat162_rn(t0v, t1v);
+                    ppt[e] = __floats2bfloat162_rn(t0v * sB[i0], t1v * sB[i0 + 1]);
                     pps[e] = __floats2bfloat162_rn(t0v * sB[i0] * __expf(sG[i0]),
                                                    t1v * sB[i0 + 1] * __expf(sG[i0 + 1]));
                 }
@@ -278,64 +283,62 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // ============================================================================ chain
 struct ChainParams {
     const int32_t *cu, *chunk_offsets, *seq_order;
-    const float *g;
-    const __nv_bfloat16 *beta;
     const float *h0;
     __nv_bfloat16 *o;
     float *ht, *h_save;
     int32_t *status;
     int64_t t_max, nt_max;
     int32_t n_max, H;
-    float scale;
 };
 
 constexpr int kChainThreads = 256;
 
-template <int VS>
+// Shared memory of the chain kernel.  Per stage (two stages, chunk n in stage n & 1):
+// K tile, [-W; Q], [T diag(bG); T diag(b); L], the 64-column V tile holding this
+// slice, and the chunk's factors.  Then the MN-major B operands S, E and f E
+// (VS used columns of 64-element swizzle atoms).
 struct ChainLayout {
-    static constexpr uint32_t oK = 0;                       // K tiles, 2 stages x 16 KB
-    static constexpr uint32_t oWQ = 32768;                  // [-W; Q], 2 stages x 32 KB
-    static constexpr uint32_t oTL = oWQ + 65536;            // [T diag(bG); T; L], 2 x 24 KB
-    static constexpr uint32_t oSB = oTL + 49152;            // S^T bf16, K-major [2][VS][128 B]
-    static constexpr uint32_t oET = oSB + VS * 256;         // E^T bf16, K-major [VS][128 B]
-    static constexpr uint32_t oFT = oET + VS * 128;         // (exp(g_c - g) E)^T bf16
-    static constexpr uint32_t oVB = oFT + VS * 128;         // (beta V)^T bf16, K-major
-    static constexpr uint32_t oV = oVB + VS * 128;          // V tiles [64][VS], 2 stages
-    static constexpr uint32_t kVTile = C * VS * 2;
-    static constexpr uint32_t total = oV + 2 * kVTile;
-    static constexpr uint32_t bytes = total + 1024;         // + alignment slack
-    // TMEM: D_W 128 | U (2 stages) | [-W S; Q S] | K^T (f E) | [T; L] E
-    static constexpr uint32_t tD2p = 128, tD2c = 128 + 2 * VS, tD3 = 128 + 3 * VS,
-                              tD4 = 128 + 4 * VS;
-    static constexpr uint32_t tmem_cols = 128 + 5 * VS <= 256 ? 256 : 512;
-    static constexpr uint32_t kStageBytes = 16384 + 16384 + 24576 + kVTile;   // per chunk TMA
+    static constexpr uint32_t kK = 16384, kWQ = 32768, kTL = 24576, kV = 8192, kF = 1024;
+    static constexpr uint32_t kStage = kK + kWQ + kTL + kV + kF;          // 82944 (1024-aligned)
+    static constexpr uint32_t oK = 0, oWQ = kK, oTL = oWQ + kWQ, oV = oTL + kTL, oF = oV + kV;
+    static constexpr uint32_t oSB = 2 * kStage;                          // S, 16 k-groups
+    static constexpr uint32_t oET = oSB + 16384;                         // E, 8 k-groups
+    static constexpr uint32_t oFT = oET + 8192;                          // exp(g_c - g) E
+    static constexpr uint32_t total = oFT + 8192;
+    static constexpr uint32_t bytes = total + 1024;                      // + alignment slack
+    static constexpr uint32_t kTmaBytes = kStage;
 };
 
-// Per-(sequence, head, column slice) state recurrence.  256 threads; thread t
-// owns TMEM lane / state row 32 (w & 3) + (t & 31) of warp w and the column half
-// (w >> 2) of the slice, so every per-column step is split over two warpgroups.
-// Software pipeline per chunk n (one thread issues every TMA and MMA):
-//   C1(n) | map(n+1): gates, (beta V)^T, P1/P2(n+1) | E(n) | C2,C3(n) | W(n+1) | S,O(n) | TMA(n+2)
-// so the state-independent work of chunk n+1 runs while chunk n's MMAs execute.
+// Offset of element (k, n) of an MN-major bf16 operand with the 128-byte swizzle and
+// n < 64: 8-row k-groups of 1024 B, 16-byte chunk index XOR (k % 8).
+__device__ __forceinline__ uint32_t mn_sw128(int k, int n) {
+    return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((n >> 3) ^ (k & 7))) << 4) + (n & 7) * 2);
+}
+
+// Per-(sequence, head, column slice) state recurrence.  256 threads; thread t owns
+// TMEM lane / row 32 (w & 3) + (t & 31) of warp w and the column half (w >> 2) of the
+// slice.  Software pipeline per chunk n (thread 0 issues every TMA and MMA):
+//   C1(n) | P1/P2(n+1) | E(n) | C2,C3(n) | W(n+1) | S,O(n) | TMA(n+2)
 template <int VS>
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_tl,
-                ChainParams p) {
-    using Lay = ChainLayout<VS>;
+                const __grid_constant__ CUtensorMap tm_f, ChainParams p) {
+    using Lay = ChainLayout;
     constexpr int HV = VS / 2;                              // columns per thread
+    // TMEM: D_W 128 | U (2 stages) | [-W S; Q S] | K^T (f E) | [. ; L E]
+    constexpr uint32_t tD2p = 128, tD2c = 128 + 2 * VS, tD3 = 128 + 3 * VS, tD4 = 128 + 4 * VS;
+    constexpr uint32_t kTmemCols = 128 + 5 * VS <= 256 ? 256 : 512;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     __shared__ uint64_t bar_tma[2], bar_c1, bar_c23, bar_p;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
-    __shared__ float s_carry, s_gc;
-    __shared__ float sFE[2][C], sFQ[2][C], sB[2][C], sGC[2];
 
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + (tid & 31);              // TMEM lane owned by this thread
+    const int row = quarter * 32 + (tid & 31);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int split = blockIdx.x, h = blockIdx.y;
     const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
@@ -354,7 +357,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sbase = smem_u32(smem);
     const int64_t KV = (int64_t)KD * VD;
     const int64_t state_base = ((int64_t)n * H + h) * KV;
-    const int c0 = half * HV;                               // first column of this thread
+    const int c0 = half * HV;
 
     if (tid == 0) {
         mbar_init(&bar_tma[0], 1);
@@ -366,16 +369,24 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_barrier_init();
     }
     if (warp == 0) {
-        tmem_alloc(&s_tmem, Lay::tmem_cols);
+        tmem_alloc(&s_tmem, kTmemCols);
         tmem_relinquish();
     }
+    // 8 consecutive bf16 of row `k` of an MN-major operand, columns [n0, n0 + 8)
+    auto st_mn8 = [&](uint32_t base, int k, int n0, const float *x) {
+        uint4 pk;
+        __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        *reinterpret_cast<uint4 *>(smem + base + mn_sw128(k, n0)) = pk;
+    };
     float S[HV];
     {
         const float *src = p.h0 ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
 #pragma unroll
         for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
 #pragma unroll
-        for (int j = 0; j < HV; ++j) st_bf16(smem, Lay::oSB + sw128_offset(VS, c0 + j, row), S[j]);
+        for (int j = 0; j < HV; j += 8) st_mn8(Lay::oSB, row, c0 + j, S + j);
     }
     fence_async_smem();
     tc_fence_before();
@@ -383,120 +394,90 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
+    // descriptors (start address field advanced by adding offset >> 4)
+    const uint64_t dSB = smem_desc(sbase + Lay::oSB, 8192, 1024, kSwizzle128B);
+    const uint64_t dET = smem_desc(sbase + Lay::oET, 8192, 1024, kSwizzle128B);
+    const uint64_t dFT = smem_desc(sbase + Lay::oFT, 8192, 1024, kSwizzle128B);
+    auto dK = [&](int st) { return smem_desc(sbase + st * Lay::kStage + Lay::oK, 8192, 1024, kSwizzle128B); };
+    auto dKmaj = [&](uint32_t off) { return smem_desc(sbase + off, 16, 1024, kSwizzle128B); };
+
     auto chunk_len = [&](int ic) -> int {
         const int64_t t0 = bos + (int64_t)ic * C;
         return (int)(eos - t0 < C ? eos - t0 : C);
     };
     auto issue_tma = [&](int ic) {
-        const int stage = ic & 1;
+        const int st = ic & 1;
         const int t0 = (int)(bos + (int64_t)ic * C);
-        const int tl_y = (int)(((row0 + ic) * H + h) * kTLRows);
-        uint64_t *bar = &bar_tma[stage];
-        mbar_arrive_expect_tx(bar, Lay::kStageBytes);
-        uint8_t *kt = smem + Lay::oK + stage * 16384;
-        uint8_t *wq = smem + Lay::oWQ + stage * 32768;
-        tma_load_3d(kt, &tm_k, 0, h, t0, bar);
-        tma_load_3d(kt + 8192, &tm_k, 64, h, t0, bar);
-        tma_load_3d(wq + 8192, &tm_q, 0, h, t0, bar);            // Q rows 64..127 of [-W; Q]
-        tma_load_3d(wq + 16384 + 8192, &tm_q, 64, h, t0, bar);
-        tma_load_2d(smem + Lay::oTL + stage * 24576, &tm_tl, 0, tl_y, bar);
-        tma_load_3d(smem + Lay::oV + stage * Lay::kVTile, &tm_v, v0, h, t0, bar);
+        const int unit = (int)((row0 + ic) * H + h);
+        uint64_t *bar = &bar_tma[st];
+        uint8_t *b = smem + st * Lay::kStage;
+        mbar_arrive_expect_tx(bar, Lay::kTmaBytes);
+        tma_load_3d(b + Lay::oK, &tm_k, 0, h, t0, bar);
+        tma_load_3d(b + Lay::oK + 8192, &tm_k, 64, h, t0, bar);
+        tma_load_3d(b + Lay::oWQ + 8192, &tm_q, 0, h, t0, bar);          // Q rows of [-W; Q]
+        tma_load_3d(b + Lay::oWQ + 16384 + 8192, &tm_q, 64, h, t0, bar);
+        tma_load_2d(b + Lay::oTL, &tm_tl, 0, unit * kTLRows, bar);
+        tma_load_3d(b + Lay::oV, &tm_v, v0 & ~63, h, t0, bar);
+        tma_load_2d(b + Lay::oF, &tm_f, 0, unit * kFRows, bar);
     };
     auto sync_all = [&]() {
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
     };
-
-    // gate and beta of the chunk being prepared, loaded one chunk ahead (threads 0..63)
-    float g_next = 0.f, b_next = 0.f;
-    auto load_gate = [&](int ic) {
-        g_next = 0.f;
-        b_next = 0.f;
-        if (ic < nch && tid < C && tid < chunk_len(ic)) {
-            const int64_t t = bos + (int64_t)ic * C + tid;
-            g_next = p.g[t * H + h];
-            b_next = bf2f(p.beta[t * H + h]);
-        }
-    };
-
-    // State-independent work of chunk ic: gate cumsum and factors, zeroing of K
-    // rows past the end of a partial chunk, the (beta V)^T slice.
-    auto map_chunk = [&](int ic) {
+    // chunk ic's tiles have landed; K rows past the end of a partial chunk are zeroed
+    // (they may hold the next sequence or NaN padding and K enters the MMAs raw)
+    auto land_chunk = [&](int ic) {
         const int st = ic & 1, len = chunk_len(ic);
-        const float gam = chunk_cumsum(g_next, &s_carry);   // contains a block barrier
-        // gamma_c is the last row's gamma (rows past the end of the sequence have g = 0)
-        if (tid == C - 1) s_gc = gam;
-        __syncthreads();    // also orders the cumsum's reads of s_carry before its next use
-        if (tid < C) {
-            const bool live = tid < len;
-            sB[st][tid] = b_next;
-            sFE[st][tid] = live ? __expf(s_gc - gam) : 0.f;
-            sFQ[st][tid] = live ? p.scale * __expf(gam) : 0.f;
-            if (tid == C - 1) sGC[st] = __expf(gam);
-        }
-        load_gate(ic + 1);
         mbar_wait(&bar_tma[st], (ic >> 1) & 1, &s_err, 3);
         __syncthreads();
-        uint8_t *ktile = smem + Lay::oK + st * 16384;
         if (len < C) {
+            uint8_t *kt = smem + st * Lay::kStage + Lay::oK;
             const uint4 zero = make_uint4(0, 0, 0, 0);
             for (int t = tid; t < 2 * C * 8; t += kChainThreads) {
                 const int r = (t >> 3) & 63;
-                if (r >= len)
-                    *reinterpret_cast<uint4 *>(ktile + (t >> 9) * 8192 + r * 128 + (t & 7) * 16) = zero;
+                if (r >= len) *reinterpret_cast<uint4 *>(kt + (t >> 9) * 8192 + r * 128 + (t & 7) * 16) = zero;
             }
+            fence_async_smem();
         }
-        const __nv_bfloat16 *vt =
-            reinterpret_cast<const __nv_bfloat16 *>(smem + Lay::oV + st * Lay::kVTile);
-#pragma unroll
-        for (int i = 0; i < C * VS / kChainThreads; ++i) {
-            const int e = i * kChainThreads + tid;
-            const int rr = e & 63, jj = e >> 6;
-            const float x = rr < len ? sB[st][rr] * bf2f(vt[rr * VS + jj]) : 0.f;
-            st_bf16(smem, Lay::oVB + sw128_offset(VS, jj, rr), x);
-        }
-        fence_async_smem();
         sync_all();
     };
-    // P1: [W; T K] = [T diag(beta Gamma); T] K;  P2: U-stage = [T; L] (beta V)^T
+    // P1: [W; .] = [T diag(beta Gamma); T diag(beta)] K;  P2: [U; .] = [T diag(beta); L] V
     auto issue_p = [&](int ic) {
         const int st = ic & 1;
-        const uint32_t tl_addr = sbase + Lay::oTL + st * 24576;
-        const uint32_t k_addr = sbase + Lay::oK + st * 16384;
+        const uint32_t b = st * Lay::kStage;
         constexpr uint32_t id_w = idesc_bf16(128, 128, 0, 1);
-        constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 0);
-        for (int s = 0; s < 4; ++s)
-            mma_bf16(tmem, smem_desc(tl_addr + s * 32, 16, 1024, kSwizzle128B),
-                     smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B), id_w, s > 0);
-        for (int s = 0; s < 4; ++s)
-            mma_bf16(tmem + Lay::tD2p + st * VS, smem_desc(tl_addr + 8192 + s * 32, 16, 1024, kSwizzle128B),
-                     smem_desc(sbase + Lay::oVB + s * 32, 16, 1024, kSwizzle128B), id_v, s > 0);
+        constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 1);
+        const uint64_t a1 = dKmaj(b + Lay::oTL), b1 = dK(st);
+        const uint64_t a2 = dKmaj(b + Lay::oTL + 8192);
+        const uint64_t b2 = smem_desc(sbase + b + Lay::oV + (v0 & 63) * 2, 8192, 1024, kSwizzle128B);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) mma_bf16(tmem, a1 + s * 2, b1 + s * 128, id_w, s > 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD2p + st * VS, a2 + s * 2, b2 + s * 128, id_v, s > 0);
         mma_commit(&bar_p);
     };
-    // -W (D_W lanes 0..63) into rows 0..63 of [-W; Q] of the chunk's stage.
+    // -W (D_W lanes 0..63) into rows 0..63 of [-W; Q] of the chunk's stage
     auto write_w = [&](int ic) {
         mbar_wait(&bar_p, ic & 1, &s_err, 4);
         tc_fence_after();
         if (quarter < 2) {
-            uint8_t *wq = smem + Lay::oWQ + (ic & 1) * 32768;
+            uint8_t *wq = smem + (ic & 1) * Lay::kStage + Lay::oWQ;
             const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
+            float w[64];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float w[16];
-                tmem_ld16(tmem + lane_off + half * 64 + q * 16, w);
-                tmem_ld_wait();
+            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, w + q * 16);
+            tmem_ld_wait();
 #pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
-                    const int key0 = half * 64 + q * 16 + hc * 8;
-                    uint4 pk;
-                    __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+            for (int q = 0; q < 8; ++q) {
+                const int key0 = half * 64 + q * 8;
+                uint4 pk;
+                __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2)
-                        pp[e2] = __floats2bfloat162_rn(-w[hc * 8 + 2 * e2], -w[hc * 8 + 2 * e2 + 1]);
-                    const int cb = key0 >> 6, ch = (key0 & 63) >> 3;
-                    *reinterpret_cast<uint4 *>(wq + cb * 16384 + rbase + ((ch ^ (row & 7)) << 4)) = pk;
-                }
+                for (int e2 = 0; e2 < 4; ++e2)
+                    pp[e2] = __floats2bfloat162_rn(-w[q * 8 + 2 * e2], -w[q * 8 + 2 * e2 + 1]);
+                const int cb = key0 >> 6, ch = (key0 & 63) >> 3;
+                *reinterpret_cast<uint4 *>(wq + cb * 16384 + rbase + ((ch ^ (row & 7)) << 4)) = pk;
             }
         }
         fence_async_smem();
@@ -506,9 +487,8 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- prologue: chunks 0 and 1 in flight, operands of chunk 0 ready
     if (tid == 0 && nch > 0) issue_tma(0);
     if (tid == 0 && nch > 1) issue_tma(1);
-    load_gate(0);
     if (nch > 0) {
-        map_chunk(0);
+        land_chunk(0);
         if (tid == 0) issue_p(0);
         write_w(0);
     }
@@ -517,6 +497,8 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int ic = 0; ic < nch; ++ic) {
         const int st = ic & 1, len = chunk_len(ic);
         const int64_t t0 = bos + (int64_t)ic * C;
+        const uint32_t sb = st * Lay::kStage;
+        const float *fac = reinterpret_cast<const float *>(smem + sb + Lay::oF);
         if (p.h_save) {
             float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
 #pragma unroll
@@ -525,60 +507,54 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // C1: [-W S; Q S] = [-W; Q] S
         if (tid == 0) {
-            constexpr uint32_t id = idesc_bf16(128, VS, 0, 0);
-            const uint32_t wq_addr = sbase + Lay::oWQ + st * 32768;
+            constexpr uint32_t id = idesc_bf16(128, VS, 0, 1);
+            const uint64_t a = dKmaj(sb + Lay::oWQ);
+#pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_bf16(tmem + Lay::tD2c,
-                         smem_desc(wq_addr + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oSB + (s >> 2) * (VS * 128) + (s & 3) * 32, 16, 1024,
-                                   kSwizzle128B),
-                         id, s > 0);
+                mma_bf16(tmem + tD2c, a + (s >> 2) * 1024 + (s & 3) * 2, dSB + s * 128, id, s > 0);
             mma_commit(&bar_c1);
         }
-        // map of the next chunk while C1 runs
+        // operands of the next chunk while C1 runs
         if (ic + 1 < nch) {
-            map_chunk(ic + 1);
+            land_chunk(ic + 1);
             if (tid == 0) issue_p(ic + 1);
         }
-        // E = U - W S (rows 0..63) -> E^T and (exp(g_c - g) E)^T; Q S (rows 64..127) kept
+        // E = U - W S (rows 0..63) -> E and exp(g_c - g) E;  Q S (rows 64..127) kept
         mbar_wait(&bar_c1, ic & 1, &s_err, 5);
         tc_fence_after();
         float qs[HV];
         if (quarter < 2) {
-            const float f = sFE[st][row];
+            const float f = fac[row];
 #pragma unroll
             for (int q = 0; q < HV / 8; ++q) {
-                float u[8], ws[8];
-                tmem_ld8(tmem + lane_off + Lay::tD2p + st * VS + c0 + q * 8, u);
-                tmem_ld8(tmem + lane_off + Lay::tD2c + c0 + q * 8, ws);
+                float u[8], ws[8], e[8], fe[8];
+                tmem_ld8(tmem + lane_off + tD2p + st * VS + c0 + q * 8, u);
+                tmem_ld8(tmem + lane_off + tD2c + c0 + q * 8, ws);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float e = u[j] + ws[j];
-                    const uint32_t off = sw128_offset(VS, c0 + q * 8 + j, row);
-                    st_bf16(smem, Lay::oET + off, e);
-                    st_bf16(smem, Lay::oFT + off, f * e);
+                    e[j] = u[j] + ws[j];
+                    fe[j] = f * e[j];
                 }
+                st_mn8(Lay::oET, row, c0 + q * 8, e);
+                st_mn8(Lay::oFT, row, c0 + q * 8, fe);
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + Lay::tD2c + c0 + q * 8, qs + q * 8);
+            for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + tD2c + c0 + q * 8, qs + q * 8);
             tmem_ld_wait();
         }
         fence_async_smem();
         sync_all();
-        // C2: K^T (f E);  C3: [T; L] E
+        // C2: K^T (f E);  C3: [T diag(beta); L] E
         if (tid == 0) {
-            constexpr uint32_t id_s = idesc_bf16(128, VS, 1, 0);
-            constexpr uint32_t id_o = idesc_bf16(128, VS, 0, 0);
-            const uint32_t k_addr = sbase + Lay::oK + st * 16384;
-            const uint32_t tl2_addr = sbase + Lay::oTL + st * 24576 + 8192;
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + Lay::tD3, smem_desc(k_addr + s * 2048, 8192, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oFT + s * 32, 16, 1024, kSwizzle128B), id_s, s > 0);
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + Lay::tD4, smem_desc(tl2_addr + s * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(sbase + Lay::oET + s * 32, 16, 1024, kSwizzle128B), id_o, s > 0);
+            constexpr uint32_t id_s = idesc_bf16(128, VS, 1, 1);
+            constexpr uint32_t id_o = idesc_bf16(128, VS, 0, 1);
+            const uint64_t a2 = dK(st), a3 = dKmaj(sb + Lay::oTL + 8192);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD3, a2 + s * 128, dFT + s * 128, id_s, s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD4, a3 + s * 2, dET + s * 128, id_o, s > 0);
             mma_commit(&bar_c23);
         }
         // -W of the next chunk while C2/C3 run
@@ -587,26 +563,24 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_wait(&bar_c23, ic & 1, &s_err, 6);
         tc_fence_after();
         {
-            const float GC = sGC[st];
+            const float GC = fac[2 * C];
 #pragma unroll
             for (int q = 0; q < HV / 8; ++q) {
                 float d3[8];
-                tmem_ld8(tmem + lane_off + Lay::tD3 + c0 + q * 8, d3);
+                tmem_ld8(tmem + lane_off + tD3 + c0 + q * 8, d3);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    S[q * 8 + j] = fmaf(GC, S[q * 8 + j], d3[j]);
-                    st_bf16(smem, Lay::oSB + sw128_offset(VS, c0 + q * 8 + j, row), S[q * 8 + j]);
-                }
+                for (int j = 0; j < 8; ++j) S[q * 8 + j] = fmaf(GC, S[q * 8 + j], d3[j]);
+                st_mn8(Lay::oSB, row, c0 + q * 8, S + q * 8);
             }
             if (quarter >= 2) {
                 const int r = row - C;
                 float d4[HV];
 #pragma unroll
-                for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + Lay::tD4 + c0 + q * 8, d4 + q * 8);
+                for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + tD4 + c0 + q * 8, d4 + q * 8);
                 tmem_ld_wait();
                 if (r < len && p.o != nullptr) {
-                    const float fq = sFQ[st][r];
+                    const float fq = fac[C + r];
                     __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * (int64_t)VD + v0 + c0;
 #pragma unroll
                     for (int j = 0; j < HV; j += 8) {
@@ -624,8 +598,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_async_smem();
         sync_all();
         if (s_err) { failed = true; break; }
-        // stage st is free: fetch chunk ic + 2 into it
-        if (tid == 0 && ic + 2 < nch) issue_tma(ic + 2);
+        if (tid == 0 && ic + 2 < nch) issue_tma(ic + 2);    // stage st is free
     }
     if (!failed && p.ht) {
         float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
@@ -635,7 +608,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, Lay::tmem_cols);
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
     if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
 }
 
@@ -654,25 +627,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
-              const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw) {
+              const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, dt, rank, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int VS>
 cudaError_t launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                         const CUtensorMap &mtl, const ChainParams &cp, int n_split, int H,
-                         int n_max, cudaStream_t s) {
-    using Lay = ChainLayout<VS>;
+                         const CUtensorMap &mtl, const CUtensorMap &mf, const ChainParams &cp,
+                         int n_split, int H, int n_max, cudaStream_t s) {
     auto kern = tc_chain_kernel<VS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Lay::bytes);
+                                         (int)ChainLayout::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(n_split, H, n_max), kChainThreads, Lay::bytes, s>>>(mq, mk, mv, mtl, cp);
+    kern<<<dim3(n_split, H, n_max), kChainThreads, ChainLayout::bytes, s>>>(mq, mk, mv, mtl, mf, cp);
     return cudaGetLastError();
 }
 
@@ -683,7 +656,7 @@ bool fwd_tc_supported(int variant, int dtype, int K, int V) {
 }
 
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H) {
-    return (size_t)nt_max * H * kTLRows * C * sizeof(__nv_bfloat16);
+    return (size_t)nt_max * H * (kTLRows * C * sizeof(__nv_bfloat16) + kFRows * C * sizeof(float));
 }
 
 // Value-column split: the most CTAs per head that still fit one wave on the GPU,
@@ -699,22 +672,27 @@ int fwd_tc_split(int n_max, int H) {
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     (void)variant;
     const int H = p.H;
-    CUtensorMap mq, mk, mv, mtl;
+    const int64_t units = p.nt_max * H;              // chunk-head slots of the workspace
+    __nv_bfloat16 *tl = static_cast<__nv_bfloat16 *>(p.workspace);
+    float *fac = reinterpret_cast<float *>(tl + (size_t)units * kTLRows * C);
+    CUtensorMap mq, mk, mv, mtl, mf;
     const cuuint64_t dqk[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)p.t_max};
     const cuuint64_t sqk[2] = {(cuuint64_t)KD * 2, (cuuint64_t)H * KD * 2};
-    const cuuint32_t bqk[3] = {64, 1, 64};
-    const int split = fwd_tc_split(p.n_max, H);
-    const int VS = VD / split;
+    const cuuint32_t b64[3] = {64, 1, 64};
     const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
     const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
-    const cuuint32_t bv[3] = {(cuuint32_t)VS, 1, 64};
-    const cuuint64_t dtl[2] = {(cuuint64_t)C, (cuuint64_t)p.nt_max * H * kTLRows};
+    const cuuint64_t dtl[2] = {(cuuint64_t)C, (cuuint64_t)units * kTLRows};
     const cuuint64_t stl[1] = {(cuuint64_t)C * 2};
     const cuuint32_t btl[2] = {64, (cuuint32_t)kTLRows};
-    if (!make_map(&mq, p.q, 3, dqk, sqk, bqk, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mk, p.k, 3, dqk, sqk, bqk, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, p.v, 3, dv, sv, bv, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&mtl, p.workspace, 2, dtl, stl, btl, CU_TENSOR_MAP_SWIZZLE_128B))
+    const cuuint64_t df[2] = {(cuuint64_t)C, (cuuint64_t)units * kFRows};
+    const cuuint64_t sf[1] = {(cuuint64_t)C * 4};
+    const cuuint32_t bf[2] = {64, (cuuint32_t)kFRows};
+    if (!make_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mtl, tl, 2, dtl, stl, btl, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mf, fac, 2, df, sf, bf, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
 
     PrepParams pp{};
@@ -722,7 +700,8 @@ cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     pp.cu = p.cu_seqlens;
     pp.g = p.g;
     pp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
-    pp.tl = static_cast<__nv_bfloat16 *>(p.workspace);
+    pp.tl = tl;
+    pp.fac = fac;
     pp.status = p.dev_status;
     pp.t_max = p.t_max;
     pp.n_max = p.n_max;
@@ -738,8 +717,6 @@ cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     cp.cu = p.cu_seqlens;
     cp.chunk_offsets = p.chunk_offsets;
     cp.seq_order = p.seq_order;
-    cp.g = p.g;
-    cp.beta = pp.beta;
     cp.h0 = p.h0;
     cp.o = static_cast<__nv_bfloat16 *>(p.o);
     cp.ht = p.ht;
@@ -749,11 +726,11 @@ cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     cp.nt_max = p.nt_max;
     cp.n_max = p.n_max;
     cp.H = H;
-    cp.scale = p.scale;
-    switch (VS) {
-        case 16: return launch_chain<16>(mq, mk, mv, mtl, cp, split, H, p.n_max, s);
-        case 32: return launch_chain<32>(mq, mk, mv, mtl, cp, split, H, p.n_max, s);
-        default: return launch_chain<64>(mq, mk, mv, mtl, cp, split, H, p.n_max, s);
+    const int split = fwd_tc_split(p.n_max, H);
+    switch (VD / split) {
+        case 16: return launch_chain<16>(mq, mk, mv, mtl, mf, cp, split, H, p.n_max, s);
+        case 32: return launch_chain<32>(mq, mk, mv, mtl, mf, cp, split, H, p.n_max, s);
+        default: return launch_chain<64>(mq, mk, mv, mtl, mf, cp, split, H, p.n_max, s);
     }
 }
 

@@ -187,7 +187,7 @@ gcl_status_t kda_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
  *
  *  - Sizes whose scratch (gcl_fwd_workspace_bytes) exceeds that limit return
  *    GCL_ERR_CAPACITY before any work is enqueued.  The bf16 K = V = 128 path
- *    needs 24 KiB per chunk and head, i.e. up to 1365 chunk-heads (for example
+ *    needs 25 KiB per chunk and head, i.e. up to 1310 chunk-heads (for example
  *    T = 4096 tokens with 16 heads).
  *  - The first call on a device looks up the array's device address (with that
  *    device current) and caches it; make that first call before any stream
