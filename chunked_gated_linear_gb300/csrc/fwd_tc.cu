@@ -306,7 +306,9 @@ struct ChainLayout {
     static constexpr uint32_t oFT = oET + 8192;                          // exp(g_c - g) E
     static constexpr uint32_t total = oFT + 8192;
     static constexpr uint32_t bytes = total + 1024;                      // + alignment slack
-    static constexpr uint32_t kTmaBytes = kStage;
+    // bytes TMA delivers per stage: K, the Q half of [-W; Q], [T..; L], V, factors
+    // (the -W half is written by the threads)
+    static constexpr uint32_t kTmaBytes = kK + kWQ / 2 + kTL + kV + kF;
 };
 
 // Offset of element (k, n) of an MN-major bf16 operand with the 128-byte swizzle and
