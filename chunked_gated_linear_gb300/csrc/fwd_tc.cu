@@ -427,18 +427,23 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncthreads();
         tc_fence_after();
     };
-    // chunk ic's tiles have landed; K rows past the end of a partial chunk are zeroed
-    // (they may hold the next sequence or NaN padding and K enters the MMAs raw)
+    // chunk ic's tiles have landed; K and V rows past the end of a partial chunk are
+    // zeroed (they may hold the next sequence or NaN padding, and K and V enter the MMAs
+    // raw, where 0 * NaN would poison the products)
     auto land_chunk = [&](int ic) {
         const int st = ic & 1, len = chunk_len(ic);
         mbar_wait(&bar_tma[st], (ic >> 1) & 1, &s_err, 3);
         __syncthreads();
         if (len < C) {
             uint8_t *kt = smem + st * Lay::kStage + Lay::oK;
+            uint8_t *vt = smem + st * Lay::kStage + Lay::oV;
             const uint4 zero = make_uint4(0, 0, 0, 0);
-            for (int t = tid; t < 2 * C * 8; t += kChainThreads) {
-                const int r = (t >> 3) & 63;
-                if (r >= len) *reinterpret_cast<uint4 *>(kt + (t >> 9) * 8192 + r * 128 + (t & 7) * 16) = zero;
+            for (int t = tid; t < 3 * C * 8; t += kChainThreads) {      // 2 K blocks + V tile
+                const int r = (t >> 3) & 63, blk = t >> 9;
+                if (r >= len) {
+                    uint8_t *base = blk < 2 ? kt + blk * 8192 : vt;
+                    *reinterpret_cast<uint4 *>(base + r * 128 + (t & 7) * 16) = zero;
+                }
             }
             fence_async_smem();
         }
