@@ -291,8 +291,6 @@ struct ChainParams {
     int32_t n_max, H;
 };
 
-constexpr int kChainThreads = 256;
-
 // Shared memory of the chain kernel.  Per stage (two stages, chunk n in stage n & 1):
 // K tile, [-W; Q], [T diag(bG); T diag(b); L], the 64-column V tile holding this
 // slice, and the chunk's factors.  Then the MN-major B operands S, E and f E
@@ -317,29 +315,56 @@ __device__ __forceinline__ uint32_t mn_sw128(int k, int n) {
     return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((n >> 3) ^ (k & 7))) << 4) + (n & 7) * 2);
 }
 
-// Per-(sequence, head, column slice) state recurrence.  256 threads; thread t owns
-// TMEM lane / row 32 (w & 3) + (t & 31) of warp w and the column half (w >> 2) of the
-// slice.  Software pipeline per chunk n (thread 0 issues every TMA and MMA):
-//   C1(n) | P1/P2(n+1) | E(n) | C2,C3(n) | W(n+1) | S,O(n) | TMA(n+2)
+constexpr int kComputeThreads = 256;                  // warps 0..7
+constexpr int kChainThreads = kComputeThreads + 32;   // + warp 8: TMA and MMA issue
+
+__device__ __forceinline__ void compute_barrier() {   // named barrier over warps 0..7
+    asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
+}
+
+// Named barrier over warps 0..7 that returns the OR of every thread's flag, so all
+// compute threads take the same branch on it.
+__device__ __forceinline__ bool compute_barrier_or(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "n"(kComputeThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Per-(sequence, head, column slice) state recurrence, warp-specialised.
+// Warps 0..7 compute: thread t owns TMEM lane / row 32 (w & 3) + (t & 31) of warp w and
+// the column half (w >> 2) of the slice.  Warp 8 (one lane) issues every TMA and MMA.
+// Per chunk n, with stage n & 1 holding its tiles:
+//   issuer:  C1(n) = [-W; Q] S  |  P(n+1)  |  C2(n) = K^T (f E), C3(n) = [T diag(b); L] E  |  TMA(n+2)
+//   compute: land(n+1)  |  E(n)  |  -W(n+1)  |  S, O(n)
+// Hand-offs use mbarriers; the compute side arrives from one thread after a named
+// barrier over its 256 threads (each of which fenced its shared writes first).
 template <int VS>
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_tl,
                 const __grid_constant__ CUtensorMap tm_f, ChainParams p) {
     using Lay = ChainLayout;
-    constexpr int HV = VS / 2;                              // columns per thread
+    constexpr int HV = VS / 2;                              // columns per compute thread
     // TMEM: D_W 128 | U (2 stages) | [-W S; Q S] | K^T (f E) | [. ; L E]
     constexpr uint32_t tD2p = 128, tD2c = 128 + 2 * VS, tD3 = 128 + 3 * VS, tD4 = 128 + 4 * VS;
     constexpr uint32_t kTmemCols = 128 + 5 * VS <= 256 ? 256 : 512;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t bar_tma[2], bar_c1, bar_c23, bar_p;
+    __shared__ uint64_t bar_tma[2], bar_ops[2], bar_c1, bar_c23, bar_p, bar_sb, bar_w, bar_e;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int quarter = warp & 3, half = warp >> 2;
+    const bool compute = warp < 8;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + (tid & 31);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int split = blockIdx.x, h = blockIdx.y;
@@ -362,260 +387,283 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int c0 = half * HV;
 
     if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_tma[i], 1);
+            mbar_init(&bar_ops[i], 1);
+        }
         mbar_init(&bar_c1, 1);
         mbar_init(&bar_c23, 1);
         mbar_init(&bar_p, 1);
+        mbar_init(&bar_sb, 1);
+        mbar_init(&bar_w, 1);
+        mbar_init(&bar_e, 1);
         s_err = 0;
         fence_barrier_init();
     }
-    if (warp == 0) {
+    if (warp == 8) {
         tmem_alloc(&s_tmem, kTmemCols);
         tmem_relinquish();
     }
-    // 8 consecutive bf16 of row `k` of an MN-major operand, columns [n0, n0 + 8)
-    auto st_mn8 = [&](uint32_t base, int k, int n0, const float *x) {
-        uint4 pk;
-        __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-        *reinterpret_cast<uint4 *>(smem + base + mn_sw128(k, n0)) = pk;
-    };
-    float S[HV];
-    {
-        const float *src = p.h0 ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
-#pragma unroll
-        for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
-#pragma unroll
-        for (int j = 0; j < HV; j += 8) st_mn8(Lay::oSB, row, c0 + j, S + j);
-    }
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    // descriptors (start address field advanced by adding offset >> 4)
-    const uint64_t dSB = smem_desc(sbase + Lay::oSB, 8192, 1024, kSwizzle128B);
-    const uint64_t dET = smem_desc(sbase + Lay::oET, 8192, 1024, kSwizzle128B);
-    const uint64_t dFT = smem_desc(sbase + Lay::oFT, 8192, 1024, kSwizzle128B);
-    auto dK = [&](int st) { return smem_desc(sbase + st * Lay::kStage + Lay::oK, 8192, 1024, kSwizzle128B); };
-    auto dKmaj = [&](uint32_t off) { return smem_desc(sbase + off, 16, 1024, kSwizzle128B); };
-
     auto chunk_len = [&](int ic) -> int {
         const int64_t t0 = bos + (int64_t)ic * C;
         return (int)(eos - t0 < C ? eos - t0 : C);
     };
-    auto issue_tma = [&](int ic) {
-        const int st = ic & 1;
-        const int t0 = (int)(bos + (int64_t)ic * C);
-        const int unit = (int)((row0 + ic) * H + h);
-        uint64_t *bar = &bar_tma[st];
-        uint8_t *b = smem + st * Lay::kStage;
-        mbar_arrive_expect_tx(bar, Lay::kTmaBytes);
-        tma_load_3d(b + Lay::oK, &tm_k, 0, h, t0, bar);
-        tma_load_3d(b + Lay::oK + 8192, &tm_k, 64, h, t0, bar);
-        tma_load_3d(b + Lay::oWQ + 8192, &tm_q, 0, h, t0, bar);          // Q rows of [-W; Q]
-        tma_load_3d(b + Lay::oWQ + 16384 + 8192, &tm_q, 64, h, t0, bar);
-        tma_load_2d(b + Lay::oTL, &tm_tl, 0, unit * kTLRows, bar);
-        tma_load_3d(b + Lay::oV, &tm_v, v0 & ~63, h, t0, bar);
-        tma_load_2d(b + Lay::oF, &tm_f, 0, unit * kFRows, bar);
-    };
-    auto sync_all = [&]() {
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    };
-    // chunk ic's tiles have landed; K and V rows past the end of a partial chunk are
-    // zeroed (they may hold the next sequence or NaN padding, and K and V enter the MMAs
-    // raw, where 0 * NaN would poison the products)
-    auto land_chunk = [&](int ic) {
-        const int st = ic & 1, len = chunk_len(ic);
-        mbar_wait(&bar_tma[st], (ic >> 1) & 1, &s_err, 3);
-        __syncthreads();
-        if (len < C) {
-            uint8_t *kt = smem + st * Lay::kStage + Lay::oK;
-            uint8_t *vt = smem + st * Lay::kStage + Lay::oV;
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            for (int t = tid; t < 3 * C * 8; t += kChainThreads) {      // 2 K blocks + V tile
-                const int r = (t >> 3) & 63, blk = t >> 9;
-                if (r >= len) {
-                    uint8_t *base = blk < 2 ? kt + blk * 8192 : vt;
-                    *reinterpret_cast<uint4 *>(base + r * 128 + (t & 7) * 16) = zero;
+
+    if (!compute) {
+        // ======================================================= issuer (warp 8, lane 0)
+        if ((tid & 31) == 0) {
+            const uint64_t dSB = smem_desc(sbase + Lay::oSB, 8192, 1024, kSwizzle128B);
+            const uint64_t dET = smem_desc(sbase + Lay::oET, 8192, 1024, kSwizzle128B);
+            const uint64_t dFT = smem_desc(sbase + Lay::oFT, 8192, 1024, kSwizzle128B);
+            auto dK = [&](int st) {
+                return smem_desc(sbase + st * Lay::kStage + Lay::oK, 8192, 1024, kSwizzle128B);
+            };
+            auto dKmaj = [&](uint32_t off) { return smem_desc(sbase + off, 16, 1024, kSwizzle128B); };
+            auto issue_tma = [&](int ic) {
+                const int st = ic & 1;
+                const int t0 = (int)(bos + (int64_t)ic * C);
+                const int unit = (int)((row0 + ic) * H + h);
+                uint64_t *bar = &bar_tma[st];
+                uint8_t *b = smem + st * Lay::kStage;
+                mbar_arrive_expect_tx(bar, Lay::kTmaBytes);
+                tma_load_3d(b + Lay::oK, &tm_k, 0, h, t0, bar);
+                tma_load_3d(b + Lay::oK + 8192, &tm_k, 64, h, t0, bar);
+                tma_load_3d(b + Lay::oWQ + 8192, &tm_q, 0, h, t0, bar);      // Q rows of [-W; Q]
+                tma_load_3d(b + Lay::oWQ + 16384 + 8192, &tm_q, 64, h, t0, bar);
+                tma_load_2d(b + Lay::oTL, &tm_tl, 0, unit * kTLRows, bar);
+                tma_load_3d(b + Lay::oV, &tm_v, v0 & ~63, h, t0, bar);
+                tma_load_2d(b + Lay::oF, &tm_f, 0, unit * kFRows, bar);
+            };
+            // P1: [W; .] = [T diag(bG); T diag(b)] K;  P2: [U; .] = [T diag(b); L] V
+            auto issue_p = [&](int ic) {
+                const int st = ic & 1;
+                const uint32_t b = st * Lay::kStage;
+                constexpr uint32_t id_w = idesc_bf16(128, 128, 0, 1);
+                constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 1);
+                const uint64_t a1 = dKmaj(b + Lay::oTL), b1 = dK(st);
+                const uint64_t a2 = dKmaj(b + Lay::oTL + 8192);
+                const uint64_t b2 =
+                    smem_desc(sbase + b + Lay::oV + (v0 & 63) * 2, 8192, 1024, kSwizzle128B);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_bf16(tmem, a1 + s * 2, b1 + s * 128, id_w, s > 0);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tmem + tD2p + st * VS, a2 + s * 2, b2 + s * 128, id_v, s > 0);
+                mma_commit(&bar_p);
+            };
+            if (nch > 0) issue_tma(0);
+            if (nch > 1) issue_tma(1);
+            if (nch > 0 && mbar_wait(&bar_ops[0], 0, &s_err, 7)) {
+                tc_fence_after();
+                issue_p(0);
+            }
+            for (int ic = 0; ic < nch && !s_err; ++ic) {
+                const int st = ic & 1;
+                const uint32_t sb = st * Lay::kStage;
+                if (!mbar_wait(&bar_sb, ic & 1, &s_err, 8) || !mbar_wait(&bar_w, ic & 1, &s_err, 9)) break;
+                tc_fence_after();
+                {   // C1: [-W S; Q S] = [-W; Q] S
+                    constexpr uint32_t id = idesc_bf16(128, VS, 0, 1);
+                    const uint64_t a = dKmaj(sb + Lay::oWQ);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        mma_bf16(tmem + tD2c, a + (s >> 2) * 1024 + (s & 3) * 2, dSB + s * 128, id, s > 0);
+                    mma_commit(&bar_c1);
+                }
+                if (ic + 1 < nch) {
+                    if (!mbar_wait(&bar_ops[(ic + 1) & 1], ((ic + 1) >> 1) & 1, &s_err, 10)) break;
+                    tc_fence_after();
+                    issue_p(ic + 1);
+                }
+                if (!mbar_wait(&bar_e, ic & 1, &s_err, 11)) break;
+                tc_fence_after();
+                {   // C2: K^T (f E);  C3: [T diag(b); L] E
+                    constexpr uint32_t id_s = idesc_bf16(128, VS, 1, 1);
+                    constexpr uint32_t id_o = idesc_bf16(128, VS, 0, 1);
+                    const uint64_t a2 = dK(st), a3 = dKmaj(sb + Lay::oTL + 8192);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD3, a2 + s * 128, dFT + s * 128, id_s, s > 0);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD4, a3 + s * 2, dET + s * 128, id_o, s > 0);
+                    mma_commit(&bar_c23);
+                }
+                if (ic + 2 < nch) {          // stage st is free once S, O(ic) are done
+                    if (!mbar_wait(&bar_sb, (ic + 1) & 1, &s_err, 12)) break;
+                    issue_tma(ic + 2);
                 }
             }
-            fence_async_smem();
         }
-        sync_all();
-    };
-    // P1: [W; .] = [T diag(beta Gamma); T diag(beta)] K;  P2: [U; .] = [T diag(beta); L] V
-    auto issue_p = [&](int ic) {
-        const int st = ic & 1;
-        const uint32_t b = st * Lay::kStage;
-        constexpr uint32_t id_w = idesc_bf16(128, 128, 0, 1);
-        constexpr uint32_t id_v = idesc_bf16(128, VS, 0, 1);
-        const uint64_t a1 = dKmaj(b + Lay::oTL), b1 = dK(st);
-        const uint64_t a2 = dKmaj(b + Lay::oTL + 8192);
-        const uint64_t b2 = smem_desc(sbase + b + Lay::oV + (v0 & 63) * 2, 8192, 1024, kSwizzle128B);
+    } else {
+        // ======================================================= compute (warps 0..7)
+        auto st_mn8 = [&](uint32_t base, int k, int n0, const float *x) {
+            uint4 pk;
+            __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
-        for (int s = 0; s < 4; ++s) mma_bf16(tmem, a1 + s * 2, b1 + s * 128, id_w, s > 0);
+            for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+            *reinterpret_cast<uint4 *>(smem + base + mn_sw128(k, n0)) = pk;
+        };
+        // hand-off to the issuer: every compute thread has fenced its writes
+        auto handoff = [&](uint64_t *bar) {
+            fence_async_smem();
+            tc_fence_before();
+            compute_barrier();
+            if (tid == 0) mbar_arrive(bar);
+        };
+        // chunk ic's tiles have landed; K and V rows past the end of a partial chunk are
+        // zeroed (they may hold the next sequence or NaN padding and enter the MMAs raw)
+        auto land_chunk = [&](int ic) {
+            const int st = ic & 1, len = chunk_len(ic);
+            mbar_wait(&bar_tma[st], (ic >> 1) & 1, &s_err, 3);
+            if (len < C) {
+                uint8_t *kt = smem + st * Lay::kStage + Lay::oK;
+                uint8_t *vt = smem + st * Lay::kStage + Lay::oV;
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                for (int t = tid; t < 3 * C * 8; t += kComputeThreads) {
+                    const int r = (t >> 3) & 63, blk = t >> 9;
+                    if (r >= len) {
+                        uint8_t *base = blk < 2 ? kt + blk * 8192 : vt;
+                        *reinterpret_cast<uint4 *>(base + r * 128 + (t & 7) * 16) = zero;
+                    }
+                }
+            }
+            handoff(&bar_ops[st]);
+        };
+        // -W (D_W lanes 0..63) into rows 0..63 of [-W; Q] of the chunk's stage
+        auto write_w = [&](int ic) {
+            mbar_wait(&bar_p, ic & 1, &s_err, 4);
+            tc_fence_after();
+            if (quarter < 2) {
+                uint8_t *wq = smem + (ic & 1) * Lay::kStage + Lay::oWQ;
+                const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
+                float w[64];
 #pragma unroll
-        for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD2p + st * VS, a2 + s * 2, b2 + s * 128, id_v, s > 0);
-        mma_commit(&bar_p);
-    };
-    // -W (D_W lanes 0..63) into rows 0..63 of [-W; Q] of the chunk's stage
-    auto write_w = [&](int ic) {
-        mbar_wait(&bar_p, ic & 1, &s_err, 4);
-        tc_fence_after();
-        if (quarter < 2) {
-            uint8_t *wq = smem + (ic & 1) * Lay::kStage + Lay::oWQ;
-            const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
-            float w[64];
+                for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, w + q * 16);
+                tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, w + q * 16);
-            tmem_ld_wait();
+                for (int q = 0; q < 8; ++q) {
+                    const int key0 = half * 64 + q * 8;
+                    uint4 pk;
+                    __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int key0 = half * 64 + q * 8;
-                uint4 pk;
-                __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+                    for (int e2 = 0; e2 < 4; ++e2)
+                        pp[e2] = __floats2bfloat162_rn(-w[q * 8 + 2 * e2], -w[q * 8 + 2 * e2 + 1]);
+                    const int cb = key0 >> 6, ch = (key0 & 63) >> 3;
+                    *reinterpret_cast<uint4 *>(wq + cb * 16384 + rbase + ((ch ^ (row & 7)) << 4)) = pk;
+                }
+            }
+            handoff(&bar_w);
+        };
+
+        float S[HV];
+        {
+            const float *src = p.h0 ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
 #pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2)
-                    pp[e2] = __floats2bfloat162_rn(-w[q * 8 + 2 * e2], -w[q * 8 + 2 * e2 + 1]);
-                const int cb = key0 >> 6, ch = (key0 & 63) >> 3;
-                *reinterpret_cast<uint4 *>(wq + cb * 16384 + rbase + ((ch ^ (row & 7)) << 4)) = pk;
+            for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
+#pragma unroll
+            for (int j = 0; j < HV; j += 8) st_mn8(Lay::oSB, row, c0 + j, S + j);
+        }
+        handoff(&bar_sb);
+        if (nch > 0) {
+            land_chunk(0);
+            write_w(0);
+        }
+        bool failed = false;
+        for (int ic = 0; ic < nch; ++ic) {
+            const int st = ic & 1, len = chunk_len(ic);
+            const int64_t t0 = bos + (int64_t)ic * C;
+            const float *fac = reinterpret_cast<const float *>(smem + st * Lay::kStage + Lay::oF);
+            if (p.h_save) {
+                float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
+#pragma unroll
+                for (int j = 0; j < HV; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            }
+            if (ic + 1 < nch) land_chunk(ic + 1);          // while C1 runs
+            // E = U - W S (rows 0..63) -> E and exp(g_c - g) E;  Q S (rows 64..127) kept
+            mbar_wait(&bar_c1, ic & 1, &s_err, 5);
+            tc_fence_after();
+            float qs[HV];
+            if (quarter < 2) {
+                const float f = fac[row];
+#pragma unroll
+                for (int q = 0; q < HV / 8; ++q) {
+                    float u[8], ws[8], e[8], fe[8];
+                    tmem_ld8(tmem + lane_off + tD2p + st * VS + c0 + q * 8, u);
+                    tmem_ld8(tmem + lane_off + tD2c + c0 + q * 8, ws);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        e[j] = u[j] + ws[j];
+                        fe[j] = f * e[j];
+                    }
+                    st_mn8(Lay::oET, row, c0 + q * 8, e);
+                    st_mn8(Lay::oFT, row, c0 + q * 8, fe);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + tD2c + c0 + q * 8, qs + q * 8);
+                tmem_ld_wait();
+            }
+            handoff(&bar_e);
+            if (ic + 1 < nch) write_w(ic + 1);             // while C2/C3 run
+            // S <- Gamma_c S + K^T (f E);  O = scale Gamma Q S + L E
+            mbar_wait(&bar_c23, ic & 1, &s_err, 6);
+            tc_fence_after();
+            {
+                const float GC = fac[2 * C];
+#pragma unroll
+                for (int q = 0; q < HV / 8; ++q) {
+                    float d3[8];
+                    tmem_ld8(tmem + lane_off + tD3 + c0 + q * 8, d3);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) S[q * 8 + j] = fmaf(GC, S[q * 8 + j], d3[j]);
+                    st_mn8(Lay::oSB, row, c0 + q * 8, S + q * 8);
+                }
+                if (quarter >= 2) {
+                    const int r = row - C;
+                    float d4[HV];
+#pragma unroll
+                    for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + tD4 + c0 + q * 8, d4 + q * 8);
+                    tmem_ld_wait();
+                    if (r < len && p.o != nullptr) {
+                        const float fq = fac[C + r];
+                        __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * (int64_t)VD + v0 + c0;
+#pragma unroll
+                        for (int j = 0; j < HV; j += 8) {
+                            uint4 pk;
+                            __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2)
+                                pp[e2] = __floats2bfloat162_rn(fmaf(fq, qs[j + 2 * e2], d4[j + 2 * e2]),
+                                                               fmaf(fq, qs[j + 2 * e2 + 1], d4[j + 2 * e2 + 1]));
+                            *reinterpret_cast<uint4 *>(dst + j) = pk;
+                        }
+                    }
+                }
+            }
+            handoff(&bar_sb);
+            // the issuer may record a timeout at any moment: decide on it uniformly
+            if (compute_barrier_or(*reinterpret_cast<volatile int *>(&s_err) != 0)) {
+                failed = true;
+                break;
             }
         }
-        fence_async_smem();
-        sync_all();
-    };
-
-    // ---- prologue: chunks 0 and 1 in flight, operands of chunk 0 ready
-    if (tid == 0 && nch > 0) issue_tma(0);
-    if (tid == 0 && nch > 1) issue_tma(1);
-    if (nch > 0) {
-        land_chunk(0);
-        if (tid == 0) issue_p(0);
-        write_w(0);
-    }
-
-    bool failed = false;
-    for (int ic = 0; ic < nch; ++ic) {
-        const int st = ic & 1, len = chunk_len(ic);
-        const int64_t t0 = bos + (int64_t)ic * C;
-        const uint32_t sb = st * Lay::kStage;
-        const float *fac = reinterpret_cast<const float *>(smem + sb + Lay::oF);
-        if (p.h_save) {
-            float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
+        if (!failed && p.ht) {
+            float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
 #pragma unroll
             for (int j = 0; j < HV; j += 4)
                 *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
-        // C1: [-W S; Q S] = [-W; Q] S
-        if (tid == 0) {
-            constexpr uint32_t id = idesc_bf16(128, VS, 0, 1);
-            const uint64_t a = dKmaj(sb + Lay::oWQ);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16(tmem + tD2c, a + (s >> 2) * 1024 + (s & 3) * 2, dSB + s * 128, id, s > 0);
-            mma_commit(&bar_c1);
-        }
-        // operands of the next chunk while C1 runs
-        if (ic + 1 < nch) {
-            land_chunk(ic + 1);
-            if (tid == 0) issue_p(ic + 1);
-        }
-        // E = U - W S (rows 0..63) -> E and exp(g_c - g) E;  Q S (rows 64..127) kept
-        mbar_wait(&bar_c1, ic & 1, &s_err, 5);
-        tc_fence_after();
-        float qs[HV];
-        if (quarter < 2) {
-            const float f = fac[row];
-#pragma unroll
-            for (int q = 0; q < HV / 8; ++q) {
-                float u[8], ws[8], e[8], fe[8];
-                tmem_ld8(tmem + lane_off + tD2p + st * VS + c0 + q * 8, u);
-                tmem_ld8(tmem + lane_off + tD2c + c0 + q * 8, ws);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    e[j] = u[j] + ws[j];
-                    fe[j] = f * e[j];
-                }
-                st_mn8(Lay::oET, row, c0 + q * 8, e);
-                st_mn8(Lay::oFT, row, c0 + q * 8, fe);
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + tD2c + c0 + q * 8, qs + q * 8);
-            tmem_ld_wait();
-        }
-        fence_async_smem();
-        sync_all();
-        // C2: K^T (f E);  C3: [T diag(beta); L] E
-        if (tid == 0) {
-            constexpr uint32_t id_s = idesc_bf16(128, VS, 1, 1);
-            constexpr uint32_t id_o = idesc_bf16(128, VS, 0, 1);
-            const uint64_t a2 = dK(st), a3 = dKmaj(sb + Lay::oTL + 8192);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD3, a2 + s * 128, dFT + s * 128, id_s, s > 0);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tmem + tD4, a3 + s * 2, dET + s * 128, id_o, s > 0);
-            mma_commit(&bar_c23);
-        }
-        // -W of the next chunk while C2/C3 run
-        if (ic + 1 < nch) write_w(ic + 1);
-        // S <- Gamma_c S + K^T (f E);  O = scale Gamma Q S + L E
-        mbar_wait(&bar_c23, ic & 1, &s_err, 6);
-        tc_fence_after();
-        {
-            const float GC = fac[2 * C];
-#pragma unroll
-            for (int q = 0; q < HV / 8; ++q) {
-                float d3[8];
-                tmem_ld8(tmem + lane_off + tD3 + c0 + q * 8, d3);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) S[q * 8 + j] = fmaf(GC, S[q * 8 + j], d3[j]);
-                st_mn8(Lay::oSB, row, c0 + q * 8, S + q * 8);
-            }
-            if (quarter >= 2) {
-                const int r = row - C;
-                float d4[HV];
-#pragma unroll
-                for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + tD4 + c0 + q * 8, d4 + q * 8);
-                tmem_ld_wait();
-                if (r < len && p.o != nullptr) {
-                    const float fq = fac[C + r];
-                    __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * (int64_t)VD + v0 + c0;
-#pragma unroll
-                    for (int j = 0; j < HV; j += 8) {
-                        uint4 pk;
-                        __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2)
-                            pp[e2] = __floats2bfloat162_rn(fmaf(fq, qs[j + 2 * e2], d4[j + 2 * e2]),
-                                                           fmaf(fq, qs[j + 2 * e2 + 1], d4[j + 2 * e2 + 1]));
-                        *reinterpret_cast<uint4 *>(dst + j) = pk;
-                    }
-                }
-            }
-        }
-        fence_async_smem();
-        sync_all();
-        if (s_err) { failed = true; break; }
-        if (tid == 0 && ic + 2 < nch) issue_tma(ic + 2);    // stage st is free
-    }
-    if (!failed && p.ht) {
-        float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
-#pragma unroll
-        for (int j = 0; j < HV; j += 4)
-            *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 8) tmem_dealloc(tmem, kTmemCols);
     if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
 }
 
