@@ -75,8 +75,9 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(FwdArgs), vp]
     lib.gcl_noalloc_scratch_bytes.restype = ctypes.c_size_t
     lib.gcl_noalloc_scratch_bytes.argtypes = []
-    lib.gcl_fwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.gcl_fwd_workspace_bytes.argtypes = [ctypes.POINTER(FwdArgs)]
+    for fn in ("gcl_fwd_workspace_bytes", "gcl_fwd_workspace_min_bytes"):
+        getattr(lib, fn).restype = ctypes.c_size_t
+        getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs)]
     lib.gdn_chunk_bwd.restype = ctypes.c_int
     lib.gdn_chunk_bwd.argtypes = [ctypes.POINTER(BwdArgs), vp]
     lib.gcl_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -157,8 +158,15 @@ def fwd_args(q, k, v, g, beta, cu_seqlens, o, h0=None, ht=None, h_save=None,
 
 
 def fwd_workspace_bytes(*args, **kw) -> int:
+    """Workspace of the fastest launch plan for these sizes."""
     a = fwd_args(*args, **kw)
     return int(lib().gcl_fwd_workspace_bytes(ctypes.byref(a)))
+
+
+def fwd_workspace_min_bytes(*args, **kw) -> int:
+    """Least workspace the forward accepts (it then runs the W-form plan)."""
+    a = fwd_args(*args, **kw)
+    return int(lib().gcl_fwd_workspace_min_bytes(ctypes.byref(a)))
 
 
 def gdn_chunk_fwd(*args, stream=None, **kw):

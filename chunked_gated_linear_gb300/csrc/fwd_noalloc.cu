@@ -8,7 +8,8 @@
 // no allocator.  For them this entry point keeps the forward's scratch (the
 // per-chunk [T diag(beta Gamma); T; L] matrices of the tensor-core path) in a
 // fixed file-scope device array instead of the `workspace` field of
-// gcl_fwd_args.  The array is part of the library image: every GPU that loads
+// gcl_fwd_args.  The launch plan is the fastest one whose scratch fits in the array
+// (problems with few units whose transition-form records do not fit run the W form).  The array is part of the library image: every GPU that loads
 // the library holds kNoallocScratchBytes of device memory until the process
 // exits.  Problems whose scratch would not fit are rejected on the host.
 //
@@ -65,7 +66,7 @@ extern "C" size_t gcl_noalloc_scratch_bytes(void) { return kNoallocScratchBytes;
 
 extern "C" gcl_status_t gdn_chunk_fwd_noalloc(const gcl_fwd_args *args, gcl_stream_t stream) {
     if (!args) return fail(GCL_ERR_INVALID_ARG, "gdn_chunk_fwd_noalloc: args is NULL");
-    const size_t need = gcl_fwd_workspace_bytes(args);
+    const size_t need = gcl_fwd_workspace_min_bytes(args);
     if (need > kNoallocScratchBytes)
         return fail(GCL_ERR_CAPACITY,
                     "gdn_chunk_fwd_noalloc: these sizes need %zu bytes of scratch; the "

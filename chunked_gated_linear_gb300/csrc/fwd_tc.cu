@@ -668,30 +668,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ============================================================================ host
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
-              const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw,
-              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, dt, rank, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int VS>
 cudaError_t launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                          const CUtensorMap &mtl, const CUtensorMap &mf, const ChainParams &cp,
@@ -705,6 +681,30 @@ cudaError_t launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUt
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+                     const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw,
+                     CUtensorMapDataType dt) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, rank, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool fwd_tc_supported(int variant, int dtype, int K, int V) {
     return variant == kGDN && dtype == GCL_BF16 && K == KD && V == VD;
@@ -724,9 +724,14 @@ int fwd_tc_split(int n_max, int H) {
     return split;
 }
 
+bool fwd_tc_prefers_transition(int n_max, int H) { return fwd_tc_split(n_max, H) >= 4; }
+
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     (void)variant;
     const int H = p.H;
+    if (fwd_tc_prefers_transition(p.n_max, H) &&
+        p.workspace_bytes >= fwd_tc_t_workspace_bytes(p.nt_max, H))
+        return launch_fwd_tc_t(p, fwd_tc_split(p.n_max, H), s);
     const int64_t units = p.nt_max * H;              // chunk-head slots of the workspace
     __nv_bfloat16 *tl = static_cast<__nv_bfloat16 *>(p.workspace);
     float *fac = reinterpret_cast<float *>(tl + (size_t)units * kTLRows * C);
@@ -742,12 +747,12 @@ cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     const cuuint64_t df[2] = {(cuuint64_t)C, (cuuint64_t)units * kFRows};
     const cuuint64_t sf[1] = {(cuuint64_t)C * 4};
     const cuuint32_t bf[2] = {64, (cuuint32_t)kFRows};
-    if (!make_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mtl, tl, 2, dtl, stl, btl, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mf, fac, 2, df, sf, bf, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+    if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mtl, tl, 2, dtl, stl, btl, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mf, fac, 2, df, sf, bf, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
 
     PrepParams pp{};

@@ -1,0 +1,797 @@
+// fwd_tc_transition.cu -- GDN chunk forward in transition form (bf16, d_k = d_v = 128,
+// chunk 64), for launches whose serial chain dominates: few (sequence, head) units,
+// each split over 4 or 8 value-column slices.
+//
+// HA-NPU paper "Empowering Hybrid Attention Models on NPUs", section 2.1: the Map
+// phases are chunk-parallel, only the Reduce is serial; section 5: the
+// state-independent GEMMs are grouped and decoupled from the state read.  Here the
+// chunk-parallel Map goes one step further and folds everything the state update and
+// the output need into per-chunk matrices, so the serial Reduce is one small GEMM per
+// chunk.  From E = U - W S, S' = Gamma_c S + Ktil^T E and O = scale diag(Gamma) Q S + L E:
+//
+//   S' = Gamma_c S + N S + B,          O = Y S + Z,          with
+//   N = -Ktil^T W   (128 x 128),       B = Ktil^T U   (128 x V),
+//   Y = scale diag(Gamma) Q - L W  (64 x 128),   Z = L U   (64 x V),
+//   Ktil = diag(exp(g_c - g)) K,  W = T diag(beta Gamma) K,  U = T diag(beta) V.
+//
+// The per-chunk affine map (Gamma_c I + N, B) is the chunk-level form of the state
+// transition the same paper's Map-Reduce-Map decomposition composes across segments.
+// The state stays in fp32; N, B, Y, Z are bf16 MMA operands.
+//
+// prep_t   one CTA per row of chunk_indices and head, 256 threads, two CTAs per SM:
+//            MMA1  [K; Q] K^T                   -> A, L (CUDA cores: decay, mask)
+//            solve T = (I + A)^-1               (blocked forward substitution)
+//            MMA2  [T bG; T b] K, [T bG; T b] V -> W, U
+//            MMA4  [T b; L] [W | U]             -> L W, L U  -> Y, Z
+//            MMA3  Ktil^T [W | U]               -> -N, B
+//          and writes [Y; N] (192 x 128), B (128 x 128), Z (64 x 128) as bf16 and
+//          Gamma_c into one 96 KiB record per chunk and head.
+// chain_t  one CTA per (sequence, head, column slice): per chunk the serial step
+//          G1 = N S and the output G2 = [Y; .] S, with TMA several chunks ahead.
+#include <cudaTypedefs.h>
+
+#include "gcl_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace gcl {
+namespace {
+
+using namespace tc;
+constexpr int C = 64;
+constexpr int KD = 128;
+constexpr int VD = 128;
+
+// record per chunk and head in the workspace
+constexpr size_t kYNRows = 192;                      // [Y; N], bf16, 128 columns
+constexpr size_t kYNBytes = kYNRows * KD * 2;        // 48 KiB
+constexpr size_t kBBytes = (size_t)KD * VD * 2;      // 32 KiB
+constexpr size_t kZBytes = (size_t)C * VD * 2;       // 16 KiB
+constexpr size_t kGBytes = 16;                       // Gamma_c, padded to 16 bytes
+constexpr size_t kUnitBytes = kYNBytes + kBBytes + kZBytes + kGBytes;
+static_assert(kUnitBytes % 16 == 0, "TMA strides are multiples of 16 bytes");
+
+__device__ __forceinline__ float warp_scan(float x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    return x;
+}
+
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    uint4 pk;
+    __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    return pk;
+}
+
+// K-major 128-byte-swizzled bf16 tile of `rows` rows per 64-column block: byte offset
+// of the 16-byte chunk that holds columns [col, col + 8) of `row`.
+__device__ __forceinline__ uint32_t kmaj16(int rows, int row, int col) {
+    return (uint32_t)((col >> 6) * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
+                      ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+// MN-major 128-byte-swizzled bf16 operand (8-row k-groups of 1024 B, 64-element atoms
+// `atom_bytes` apart): byte offset of the 16-byte chunk holding elements [n, n + 8) of k.
+__device__ __forceinline__ uint32_t mnmaj16(uint32_t atom_bytes, int k, int n) {
+    return (uint32_t)((n >> 6) * atom_bytes + (k >> 3) * 1024 + (k & 7) * 128 +
+                      ((((n & 63) >> 3) ^ (k & 7)) << 4));
+}
+
+// ============================================================================ prep_t
+struct PrepTParams {
+    const int32_t *chunk_indices, *cu;
+    const float *g;
+    const __nv_bfloat16 *beta;
+    uint8_t *ws;                 // nt_max * H records of kUnitBytes
+    int32_t *status;
+    int64_t t_max;
+    int32_t n_max, H;
+    float scale;
+};
+
+constexpr int kPrepThreads = 256;
+// dynamic shared memory, offsets from the 1024-aligned base
+constexpr uint32_t pKQ = 0;        // [2 col blocks][K rows 0..63 | Q rows 0..63][128 B]  32 KiB
+constexpr uint32_t pV = 32768;     // [2 col blocks][64 rows][128 B]                      16 KiB
+constexpr uint32_t pTL = 49152;    // [T diag(bG); T diag(b); L], 192 rows of 64 tokens   24 KiB
+constexpr uint32_t pA = 73728;     // fp32 A, T [64][65], X [3][16][17]; later [W | U]
+constexpr uint32_t pEnd = pA + 2 * C * (C + 1) * 4 + 3 * 16 * 17 * 4;
+constexpr int kPrepTSmem = pEnd + 1024;
+static_assert(pEnd - pA >= 4 * 8192, "[W | U] (4 atoms of 8 KiB) reuses the solve buffers");
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, PrepTParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    float *sA = reinterpret_cast<float *>(smem + pA);
+    float *sT = sA + C * (C + 1);
+    float *sX = sT + C * (C + 1);
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+    __shared__ float sG[C], sB[C], sF[C], sFQ[C], s_carry;
+
+    if (status_blocks(p.status)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, j = blockIdx.x, h = blockIdx.y;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int lrow = quarter * 32 + (tid & 31);           // TMEM lane read by this thread
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int n = p.chunk_indices[2 * j];
+    if (n < 0) return;                                     // sentinel: unused slot
+    const int ic = p.chunk_indices[2 * j + 1];
+    if (n >= p.n_max || ic < 0) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t bos = p.cu[n], eos = p.cu[n + 1], t0 = bos + (int64_t)ic * C;
+    if (bos < 0 || eos < bos || eos > p.t_max || t0 >= eos) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int len = (int)(eos - t0 < C ? eos - t0 : C);
+    const int H = p.H;
+    uint8_t *rec = p.ws + ((size_t)j * H + h) * kUnitBytes;
+    __nv_bfloat16 *gYN = reinterpret_cast<__nv_bfloat16 *>(rec);
+    __nv_bfloat16 *gB = reinterpret_cast<__nv_bfloat16 *>(rec + kYNBytes);
+    __nv_bfloat16 *gZ = reinterpret_cast<__nv_bfloat16 *>(rec + kYNBytes + kBBytes);
+    float *gGC = reinterpret_cast<float *>(rec + kYNBytes + kBBytes + kZBytes);
+    const uint32_t sbase = smem_u32(smem);
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        s_err = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, 256);
+        tmem_relinquish();
+    }
+    {   // gamma = inclusive cumsum of g over the chunk (warps 0 and 1), beta
+        const float gv = (tid < len) ? p.g[(t0 + tid) * H + h] : 0.f;
+        float x = tid < C ? warp_scan(gv) : 0.f;
+        if (tid == 31) s_carry = x;
+        __syncthreads();
+        if (tid >= 32 && tid < C) x += s_carry;
+        if (tid < C) {
+            sG[tid] = x;
+            sB[tid] = tid < len ? __bfloat162float(p.beta[(t0 + tid) * H + h]) : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    if (tid < C) {
+        const bool live = tid < len;
+        sF[tid] = live ? __expf(sG[C - 1] - sG[tid]) : 0.f;   // row factor of Ktil
+        sFQ[tid] = live ? p.scale * __expf(sG[tid]) : 0.f;    // read-out factor
+    }
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar_tma, 49152);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(smem + pKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
+            tma_load_3d(smem + pKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
+            tma_load_3d(smem + pV + cb * 8192, &tm_v, cb * 64, h, (int)t0, &bar_tma);
+        }
+    }
+    uint32_t phase = 0;
+    // every thread waits for the tensor-core group just committed; the block then agrees
+    // on whether any wait gave up
+    auto mma_done = [&](int code) -> bool {
+        const bool ok = mbar_wait(&bar_mma, phase, &s_err, code);
+        phase ^= 1;
+        tc_fence_after();
+        return !__syncthreads_or(!ok);
+    };
+    auto to_async = [&]() {      // shared writes and TMEM reads -> next tensor-core group
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+    do {
+        const bool landed = mbar_wait(&bar_tma, 0, &s_err, 1);
+        if (__syncthreads_or(!landed)) break;
+        // rows past the end of a partial chunk: zero K, Q and V (they may hold the next
+        // sequence or NaN padding and every one of them enters an MMA raw)
+        if (len < C) {
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            for (int t = tid; t < 6 * C * 8; t += kPrepThreads) {
+                const int r = (t >> 3) & 63, blk = t >> 9;       // K0 K1 Q0 Q1 V0 V1
+                if (r >= len) {
+                    const uint32_t base = blk < 4 ? pKQ + (blk & 1) * 16384 + (blk >> 1) * 8192
+                                                  : pV + (blk - 4) * 8192;
+                    *reinterpret_cast<uint4 *>(smem + base + r * 128 + (t & 7) * 16) = zero;
+                }
+            }
+        }
+        to_async();
+        // ---- MMA1: [K; Q] K^T -> lanes 0..63: K K^T, lanes 64..127: Q K^T  (N = 64)
+        if (tid == 0) {
+            const uint64_t d = smem_desc(sbase + pKQ, 16, 1024, kSwizzle128B);
+            constexpr uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t o = (s >> 2) * 1024 + (s & 3) * 2;
+                mma_bf16(tmem, d + o, d + o, id, s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(2)) break;
+        {   // A (fp32) from lanes 0..63, L (bf16, rows 128.. of [..; L]) from lanes 64..127
+            float v[32];
+            tmem_ld16(tmem + lane_off + half * 32, v);
+            tmem_ld16(tmem + lane_off + half * 32 + 16, v + 16);
+            tmem_ld_wait();
+            if (lrow < C) {
+                const int r = lrow;
+                const float gr = sG[r], br = sB[r];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = half * 32 + i;
+                    sA[r * (C + 1) + col] =
+                        (col < r && r < len) ? br * __expf(gr - sG[col]) * v[i] : 0.f;
+                }
+            } else {
+                const int r = lrow - C;
+                const float gr = sG[r];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float l[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int col = half * 32 + q * 8 + e;
+                        l[e] = (col <= r && r < len) ? p.scale * __expf(gr - sG[col]) * v[q * 8 + e]
+                                                     : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, 2 * C + r, half * 32 + q * 8)) =
+                        pack8(l);
+                }
+            }
+            for (int e = tid; e < C * (C + 1); e += kPrepThreads) sT[e] = 0.f;
+        }
+        __syncthreads();
+        // ---- T = (I + A)^-1: 16 x 16 diagonal blocks (one thread per column), then three
+        // levels of off-diagonal blocks  T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+        if (tid < C) {
+            const int b = tid >> 4, jj = tid & 15, o = b * 16;
+            float tc[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) tc[r] = (r == jj) ? 1.f : 0.f;
+#pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                if (r > jj) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        if (m >= jj && m < r) acc = fmaf(sA[(o + r) * (C + 1) + o + m], tc[m], acc);
+                    tc[r] = -acc;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(o + r) * (C + 1) + o + jj] = tc[r];
+        }
+        __syncthreads();
+        for (int d = 1; d < 4; ++d) {
+            const int nblk = 4 - d;
+            for (int e = tid; e < nblk * 256; e += kPrepThreads) {
+                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
+                float acc = 0.f;
+                for (int m = bj * 16; m < bi * 16; ++m)
+                    acc = fmaf(sA[(bi * 16 + rr) * (C + 1) + m], sT[m * (C + 1) + bj * 16 + cc], acc);
+                sX[blk * 272 + rr * 17 + cc] = acc;
+            }
+            __syncthreads();
+            for (int e = tid; e < nblk * 256; e += kPrepThreads) {
+                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    acc = fmaf(sT[(bi * 16 + rr) * (C + 1) + bi * 16 + m], sX[blk * 272 + m * 17 + cc], acc);
+                sT[(bi * 16 + rr) * (C + 1) + bj * 16 + cc] = -acc;
+            }
+            __syncthreads();
+        }
+        // ---- T diag(beta Gamma) -> rows 0..63, T diag(beta) -> rows 64..127 (bf16, K-major)
+        {
+            const int r = tid >> 2;
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+                const int c0 = ((tid & 3) * 2 + qq) * 8;
+                float tb[8], tg[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    tb[e] = sT[r * (C + 1) + c0 + e] * sB[c0 + e];
+                    tg[e] = tb[e] * __expf(sG[c0 + e]);
+                }
+                *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, r, c0)) = pack8(tg);
+                *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, C + r, c0)) = pack8(tb);
+            }
+        }
+        to_async();
+        // ---- MMA2: [T bG; T b] K -> cols 0..127 (W in lanes 0..63);
+        //            [T bG; T b] V -> cols 128..255 (U in lanes 64..127).
+        // K and V are MN-major B operands (64-element atoms 16 KiB and 8 KiB apart).
+        if (tid == 0) {
+            const uint64_t a = smem_desc(sbase + pTL, 16, 1024, kSwizzle128B);
+            const uint64_t bk = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
+            const uint64_t bv = smem_desc(sbase + pV, 8192, 1024, kSwizzle128B);
+            constexpr uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, bk + s * 128, id, s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tmem + 128, a + s * 2, bv + s * 128, id, s > 0);
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(3)) break;
+        {   // [W | U] as one MN-major operand (N = 256: keys then values) in the solve buffers
+            const int tok = lrow & 63;
+            const int n0 = (lrow < C ? 0 : 128) + half * 64;
+            float wu[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + n0 + q * 16, wu + q * 16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(smem + pA + mnmaj16(8192, tok, n0 + q * 8)) = pack8(wu + q * 8);
+            // Ktil = diag(exp(g_c - g)) K, in place (MMA2 has consumed K)
+            for (int t = tid; t < 2 * C * 8; t += kPrepThreads) {
+                const int r = (t >> 3) & 63, cb = t >> 9;
+                uint4 *pk = reinterpret_cast<uint4 *>(smem + pKQ + cb * 16384 + r * 128 + (t & 7) * 16);
+                uint4 x = *pk;
+                __nv_bfloat162 *xx = reinterpret_cast<__nv_bfloat162 *>(&x);
+                const float f = sF[r];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 y = __bfloat1622float2(xx[e]);
+                    xx[e] = __floats2bfloat162_rn(f * y.x, f * y.y);
+                }
+                *pk = x;
+            }
+        }
+        to_async();
+        // ---- MMA4: [T b; L] [W | U] -> lanes 64..127: L W (cols 0..127), L U (cols 128..255)
+        if (tid == 0) {
+            const uint64_t a = smem_desc(sbase + pTL + 8192, 16, 1024, kSwizzle128B);
+            const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
+            constexpr uint32_t id = idesc_bf16(128, 256, 0, 1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, b + s * 128, id, s > 0);
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(4)) break;
+        if (lrow >= C) {   // Y = scale diag(Gamma) Q - L W and Z = L U, row r, columns half*64..
+            const int r = lrow - C;
+            const float fq = sFQ[r];
+            const bool live = r < len;
+            float x[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, x + q * 16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int c = half * 64 + q * 8;
+                const uint4 qv = *reinterpret_cast<const uint4 *>(smem + pKQ + kmaj16(128, C + r, c));
+                const __nv_bfloat162 *qq = reinterpret_cast<const __nv_bfloat162 *>(&qv);
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f2 = __bfloat1622float2(qq[e]);
+                    y[2 * e] = live ? fmaf(fq, f2.x, -x[q * 8 + 2 * e]) : 0.f;
+                    y[2 * e + 1] = live ? fmaf(fq, f2.y, -x[q * 8 + 2 * e + 1]) : 0.f;
+                }
+                *reinterpret_cast<uint4 *>(gYN + (size_t)r * KD + c) = pack8(y);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, x + q * 16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float z[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) z[e] = live ? x[q * 8 + e] : 0.f;
+                *reinterpret_cast<uint4 *>(gZ + (size_t)r * VD + half * 64 + q * 8) = pack8(z);
+            }
+        }
+        if (tid == 0) {
+            const float gc = __expf(sG[C - 1]);
+            *reinterpret_cast<float4 *>(gGC) = make_float4(gc, 0.f, 0.f, 0.f);
+        }
+        to_async();
+        // ---- MMA3: Ktil^T [W | U] -> cols 0..127: Ktil^T W = -N, cols 128..255: B
+        if (tid == 0) {
+            const uint64_t a = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
+            const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
+            constexpr uint32_t id = idesc_bf16(128, 256, 1, 1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 128, b + s * 128, id, s > 0);
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(5)) break;
+        {   // key row m = lrow: half 0 -> N row (rows 64.. of [Y; N]), half 1 -> B row
+            const int m = lrow;
+            const float sg = half == 0 ? -1.f : 1.f;
+            __nv_bfloat16 *dst = half == 0 ? gYN + (size_t)(C + m) * KD : gB + (size_t)m * VD;
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+                float x[64];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld16(tmem + lane_off + half * 128 + pass * 64 + q * 16, x + q * 16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = sg * x[q * 8 + e];
+                    *reinterpret_cast<uint4 *>(dst + pass * 64 + q * 8) = pack8(y);
+                }
+            }
+        }
+    } while (0);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+// ============================================================================ chain_t
+struct ChainTParams {
+    const int32_t *cu, *chunk_offsets, *seq_order;
+    const float *h0;
+    const uint8_t *ws;
+    __nv_bfloat16 *o;
+    float *ht, *h_save;
+    int32_t *status;
+    int64_t t_max, nt_max;
+    int32_t n_max, H;
+};
+
+// Shared memory: NS stages of {[Y; N] (two 64-column blocks of 192 rows, 128-byte
+// swizzle), B slice [128][VS], Z slice [64][VS], Gamma_c}, then two bf16 copies of the
+// state slice S as MN-major B operands (VS used columns of a 64-element atom).
+template <int VS, int NS>
+struct ChainTLayout {
+    static constexpr uint32_t kYN = 49152, kB = VS * 256, kZ = VS * 128, kG = 16;
+    static constexpr uint32_t oYN = 0, oB = kYN, oZ = oB + kB, oG = oZ + kZ;
+    static constexpr uint32_t kStage = (oG + kG + 1023) / 1024 * 1024;
+    static constexpr uint32_t oSB = NS * kStage;                 // two 16 KiB buffers
+    static constexpr uint32_t total = oSB + 2 * 16384;
+    static constexpr uint32_t bytes = total + 1024;              // + alignment slack
+    static constexpr uint32_t kTmaBytes = kYN + kB + kZ + kG;
+};
+
+__device__ __forceinline__ uint32_t mn_sw128(int k, int n) {
+    return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((n >> 3) ^ (k & 7))) << 4) + (n & 7) * 2);
+}
+
+constexpr int kComputeThreads = 256;                  // warps 0..7
+constexpr int kChainThreads = kComputeThreads + 32;   // + warp 8: TMA and MMA issue
+
+__device__ __forceinline__ void compute_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
+}
+__device__ __forceinline__ bool compute_barrier_or(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "n"(kComputeThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Per-(sequence, head, column slice) recurrence.  Warps 0..7 compute: thread t owns key
+// row 32 (w & 3) + (t & 31) of the state slice and the column half (w >> 2).  Warp 8
+// (one lane) issues every TMA and MMA.  Per chunk n (stage n % NS):
+//   issuer:  wait S(n) | G1(n) = N S(n) -> D1 | G2(n) = [Y; N_top] S(n) -> D2[n & 1] |
+//            refill the stage of chunk n - 1 with chunk n - 1 + NS
+//   compute: S(n+1) = Gamma_c S(n) + D1 + B -> Sb[(n+1) & 1] | O(n) = D2 + Z | free stage
+// Each barrier that is waited on by parity is only re-armed after its waiter has passed,
+// so no waiter can fall two phases behind.
+template <int VS, int NS>
+__global__ void __launch_bounds__(kChainThreads, 1)
+tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_constant__ CUtensorMap tm_b,
+                  const __grid_constant__ CUtensorMap tm_z, ChainTParams p) {
+    using Lay = ChainTLayout<VS, NS>;
+    constexpr int HV = VS / 2;                          // columns per compute thread
+    constexpr uint32_t tD1 = 0, tD2 = VS;               // D1 | D2 (two buffers)
+    constexpr uint32_t kTmemCols = 3 * VS <= 32 ? 32 : 3 * VS <= 64 ? 64 : 3 * VS <= 128 ? 128 : 256;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb, bar_g1, bar_g2[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+
+    if (status_blocks(p.status)) return;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const bool compute = warp < 8;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
+    const int row = quarter * 32 + (tid & 31);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int split = blockIdx.x, h = blockIdx.y;
+    const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
+    const int H = p.H, v0 = split * VS;
+    if (n < 0 || n >= p.n_max) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t bos = p.cu[n], eos = p.cu[n + 1];
+    if (bos < 0 || eos < bos || eos > p.t_max) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int nch = (int)((eos - bos + C - 1) / C);
+    const int64_t row0 = p.chunk_offsets[n];
+    if (nch > 0 && (row0 < 0 || row0 + nch > p.nt_max)) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const uint32_t sbase = smem_u32(smem);
+    const int64_t KV = (int64_t)KD * VD;
+    const int64_t state_base = ((int64_t)n * H + h) * KV;
+    const int c0 = half * HV;
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&bar_tma[i], 1);
+            mbar_init(&bar_free[i], 1);
+        }
+        mbar_init(&bar_sb, 1);
+        mbar_init(&bar_g1, 1);
+        mbar_init(&bar_g2[0], 1);
+        mbar_init(&bar_g2[1], 1);
+        s_err = 0;
+        fence_barrier_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(&s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (!compute) {
+        // ======================================================= issuer (warp 8, lane 0)
+        if ((tid & 31) == 0) {
+            auto issue_tma = [&](int ic) {
+                const int st = ic % NS;
+                const int unit = (int)((row0 + ic) * H + h);
+                uint64_t *bar = &bar_tma[st];
+                uint8_t *b = smem + st * Lay::kStage;
+                mbar_arrive_expect_tx(bar, Lay::kTmaBytes);
+                tma_load_3d(b + Lay::oYN, &tm_yn, 0, 0, unit, bar);
+                tma_load_3d(b + Lay::oYN + 24576, &tm_yn, 64, 0, unit, bar);
+                tma_load_3d(b + Lay::oB, &tm_b, v0, 0, unit, bar);
+                tma_load_3d(b + Lay::oZ, &tm_z, v0, 0, unit, bar);
+                bulk_load(b + Lay::oG, p.ws + (size_t)unit * kUnitBytes + kYNBytes + kBBytes + kZBytes,
+                          16, bar);
+            };
+            constexpr uint32_t id = idesc_bf16(128, VS, 0, 1);
+            for (int i = 0; i < NS && i < nch; ++i) issue_tma(i);
+            for (int ic = 0; ic < nch; ++ic) {
+                const int st = ic % NS;
+                if (!mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 7)) break;
+                if (!mbar_wait(&bar_sb, ic & 1, &s_err, 8)) break;
+                tc_fence_after();
+                const uint64_t dS = smem_desc(sbase + Lay::oSB + (ic & 1) * 16384, 8192, 1024, kSwizzle128B);
+                const uint64_t dA = smem_desc(sbase + st * Lay::kStage + Lay::oYN, 16, 1024, kSwizzle128B);
+                // G1: D1 = N S  (rows 64..191 of [Y; N]; key blocks 24 KiB apart)
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16(tmem + tD1, dA + (8192 >> 4) + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
+                             dS + s * 128, id, s > 0);
+                mma_commit(&bar_g1);
+                // G2: D2 = [Y; N_top] S  (rows 0..127)
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16(tmem + tD2 + (ic & 1) * VS, dA + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
+                             dS + s * 128, id, s > 0);
+                mma_commit(&bar_g2[ic & 1]);
+                const int nx = ic - 1 + NS;                 // refill the stage of chunk ic - 1
+                if (ic >= 1 && nx < nch) {
+                    if (!mbar_wait(&bar_free[(ic - 1) % NS], ((ic - 1) / NS) & 1, &s_err, 9)) break;
+                    issue_tma(nx);
+                }
+            }
+        }
+    } else {
+        // ======================================================= compute (warps 0..7)
+        auto st_sb = [&](int buf, const float *x) {       // bf16 copy of this thread's S values
+#pragma unroll
+            for (int j = 0; j < HV; j += 8) {
+                uint4 pk;
+                __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[j + 2 * e], x[j + 2 * e + 1]);
+                *reinterpret_cast<uint4 *>(smem + Lay::oSB + buf * 16384 + mn_sw128(row, c0 + j)) = pk;
+            }
+        };
+        float S[HV];
+        {
+            const float *src = p.h0 ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
+#pragma unroll
+            for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
+        }
+        st_sb(0, S);
+        fence_async_smem();
+        compute_barrier();
+        if (tid == 0) mbar_arrive(&bar_sb);
+        bool failed = false;
+        for (int ic = 0; ic < nch; ++ic) {
+            const int st = ic % NS, len = (int)(eos - bos - (int64_t)ic * C < C ? eos - bos - (int64_t)ic * C : C);
+            const int64_t t0 = bos + (int64_t)ic * C;
+            const uint8_t *stage = smem + st * Lay::kStage;
+            if (p.h_save) {
+                float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
+#pragma unroll
+                for (int j = 0; j < HV; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            }
+            mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 3);
+            mbar_wait(&bar_g1, ic & 1, &s_err, 4);
+            tc_fence_after();
+            {   // S(n+1) = Gamma_c S(n) + N S(n) + B
+                const float gc = *reinterpret_cast<const float *>(stage + Lay::oG);
+                const uint8_t *brow = stage + Lay::oB + row * (VS * 2) + c0 * 2;
+#pragma unroll
+                for (int j = 0; j < HV; j += 8) {
+                    float d1[8];
+                    tmem_ld8(tmem + lane_off + tD1 + c0 + j, d1);
+                    tmem_ld_wait();
+                    const uint4 bv = *reinterpret_cast<const uint4 *>(brow + j * 2);
+                    const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&bv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 b2 = __bfloat1622float2(bb[e]);
+                        S[j + 2 * e] = fmaf(gc, S[j + 2 * e], d1[2 * e] + b2.x);
+                        S[j + 2 * e + 1] = fmaf(gc, S[j + 2 * e + 1], d1[2 * e + 1] + b2.y);
+                    }
+                }
+            }
+            st_sb((ic + 1) & 1, S);
+            fence_async_smem();
+            tc_fence_before();
+            compute_barrier();
+            if (tid == 0) mbar_arrive(&bar_sb);
+            // O(n) = Y S(n) + Z  (token rows = TMEM lanes 0..63)
+            mbar_wait(&bar_g2[ic & 1], (ic >> 1) & 1, &s_err, 6);
+            tc_fence_after();
+            if (quarter < 2) {        // warp-uniform: every lane takes part in the TMEM load
+                float d2[HV];
+#pragma unroll
+                for (int j = 0; j < HV; j += 8)
+                    tmem_ld8(tmem + lane_off + tD2 + (ic & 1) * VS + c0 + j, d2 + j);
+                tmem_ld_wait();
+                if (row < len && p.o != nullptr) {
+                    const uint8_t *zrow = stage + Lay::oZ + row * (VS * 2) + c0 * 2;
+                    __nv_bfloat16 *dst = p.o + ((t0 + row) * H + h) * (int64_t)VD + v0 + c0;
+#pragma unroll
+                    for (int j = 0; j < HV; j += 8) {
+                        const uint4 zv = *reinterpret_cast<const uint4 *>(zrow + j * 2);
+                        const __nv_bfloat162 *zz = reinterpret_cast<const __nv_bfloat162 *>(&zv);
+                        float ov[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 z2 = __bfloat1622float2(zz[e]);
+                            ov[2 * e] = d2[j + 2 * e] + z2.x;
+                            ov[2 * e + 1] = d2[j + 2 * e + 1] + z2.y;
+                        }
+                        *reinterpret_cast<uint4 *>(dst + j) = pack8(ov);
+                    }
+                }
+            }
+            tc_fence_before();
+            // stage st is free; decide uniformly on a failure the issuer may have recorded
+            failed = compute_barrier_or(*reinterpret_cast<volatile int *>(&s_err) != 0);
+            if (tid == 0) mbar_arrive(&bar_free[st]);
+            if (failed) break;
+        }
+        if (!failed && p.ht) {
+            float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
+#pragma unroll
+            for (int j = 0; j < HV; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) tmem_dealloc(tmem, kTmemCols);
+    if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+// ============================================================================ host
+template <int VS, int NS>
+cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const ChainTParams &cp,
+                           int n_split, int H, int n_max, cudaStream_t s) {
+    using Lay = ChainTLayout<VS, NS>;
+    static_assert(Lay::bytes <= 232448, "chain_t shared memory");
+    const int64_t units = cp.nt_max * H;
+    CUtensorMap mb, mz;
+    const cuuint64_t db[3] = {(cuuint64_t)VD, (cuuint64_t)KD, (cuuint64_t)units};
+    const cuuint64_t sb[2] = {(cuuint64_t)VD * 2, (cuuint64_t)kUnitBytes};
+    const cuuint32_t bb[3] = {(cuuint32_t)VS, (cuuint32_t)KD, 1};
+    const cuuint64_t dz[3] = {(cuuint64_t)VD, (cuuint64_t)C, (cuuint64_t)units};
+    const cuuint32_t bz[3] = {(cuuint32_t)VS, (cuuint32_t)C, 1};
+    if (!make_tensor_map(&mb, ws + kYNBytes, 3, db, sb, bb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map(&mz, ws + kYNBytes + kBBytes, 3, dz, sb, bz, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kern = tc_chain_t_kernel<VS, NS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay::bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(n_split, H, n_max), kChainThreads, Lay::bytes, s>>>(myn, mb, mz, cp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H) { return (size_t)nt_max * H * kUnitBytes; }
+
+cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
+    const int H = p.H;
+    const int64_t units = p.nt_max * H;
+    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
+    CUtensorMap mq, mk, mv, myn;
+    const cuuint64_t dqk[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sqk[2] = {(cuuint64_t)KD * 2, (cuuint64_t)H * KD * 2};
+    const cuuint32_t b64[3] = {64, 1, 64};
+    const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
+    const cuuint64_t dyn[3] = {(cuuint64_t)KD, (cuuint64_t)kYNRows, (cuuint64_t)units};
+    const cuuint64_t syn[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
+    const cuuint32_t byn[3] = {64, (cuuint32_t)kYNRows, 1};
+    if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&myn, ws, 3, dyn, syn, byn, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+
+    PrepTParams pp{};
+    pp.chunk_indices = p.chunk_indices;
+    pp.cu = p.cu_seqlens;
+    pp.g = p.g;
+    pp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
+    pp.ws = ws;
+    pp.status = p.dev_status;
+    pp.t_max = p.t_max;
+    pp.n_max = p.n_max;
+    pp.H = H;
+    pp.scale = p.scale;
+    cudaError_t e = cudaFuncSetAttribute(tc_prep_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPrepTSmem);
+    if (e != cudaSuccess) return e;
+    tc_prep_t_kernel<<<dim3((unsigned)p.nt_max, H), kPrepThreads, kPrepTSmem, s>>>(mq, mk, mv, pp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    ChainTParams cp{};
+    cp.cu = p.cu_seqlens;
+    cp.chunk_offsets = p.chunk_offsets;
+    cp.seq_order = p.seq_order;
+    cp.h0 = p.h0;
+    cp.ws = ws;
+    cp.o = static_cast<__nv_bfloat16 *>(p.o);
+    cp.ht = p.ht;
+    cp.h_save = p.h_save;
+    cp.status = p.dev_status;
+    cp.t_max = p.t_max;
+    cp.nt_max = p.nt_max;
+    cp.n_max = p.n_max;
+    cp.H = H;
+    if (split == 8) return launch_chain_t<16, 3>(myn, ws, cp, split, H, p.n_max, s);
+    if (split == 4) return launch_chain_t<32, 3>(myn, ws, cp, split, H, p.n_max, s);
+    return cudaErrorInvalidValue;                   // the plan is only taken at splits 4 and 8
+}
+
+}  // namespace gcl

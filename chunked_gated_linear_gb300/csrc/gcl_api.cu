@@ -64,6 +64,16 @@ static gcl_status_t check_common(const char *fn, const void *q, const void *k, c
     return GCL_OK;
 }
 
+// Forward workspace: the minimum (W form) or what the fastest launch plan uses.
+static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
+    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V)) return 0;
+    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
+    if (ntm <= 0 || a->H <= 0 || a->n_max <= 0) return 0;
+    if (fastest && fwd_tc_prefers_transition(a->n_max, a->H))
+        return fwd_tc_t_workspace_bytes(ntm, a->H);
+    return fwd_tc_workspace_bytes(ntm, a->H);
+}
+
 static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int variant) {
     const char *fn = variant == kGDN ? "gdn_chunk_fwd" : "kda_chunk_fwd";
     if (!a) return fail(GCL_ERR_INVALID_ARG, "%s: args is NULL", fn);
@@ -80,8 +90,11 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
                         "%s: chunk_indices and chunk_offsets are required for bf16 K=V=128", fn);
         const size_t need = fwd_tc_workspace_bytes(ntm, a->H);
         if (!a->workspace || a->workspace_bytes < need)
-            return fail(GCL_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn,
-                        need, a->workspace ? a->workspace_bytes : (size_t)0);
+            return fail(GCL_ERR_CAPACITY,
+                        "%s: workspace of at least %zu bytes needed (%zu for the fastest "
+                        "plan), %zu given",
+                        fn, need, fwd_ws(a, variant, true),
+                        a->workspace ? a->workspace_bytes : (size_t)0);
         if (!aligned16(a->workspace))
             return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
     }
@@ -94,6 +107,7 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     p.chunk_offsets = a->chunk_offsets; p.seq_order = a->seq_order;
     p.o = a->o; p.ht = a->ht; p.h_save = a->h_save; p.dev_status = a->dev_status;
     p.workspace = a->workspace;
+    p.workspace_bytes = a->workspace ? a->workspace_bytes : 0;
     p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V;
     p.nt_max = ntm;
     p.scale = a->scale;
@@ -102,12 +116,6 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     return cuda_check(e, fn);
 }
 
-static size_t fwd_ws(const gcl_fwd_args *a, int variant) {
-    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V)) return 0;
-    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
-    if (ntm <= 0 || a->H <= 0) return 0;
-    return fwd_tc_workspace_bytes(ntm, a->H);
-}
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -170,7 +178,12 @@ gcl_status_t chunk_meta_build(const int32_t *cu_seqlens, int32_t n_max, int64_t 
 
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args) {
     if (!args) return 0;
-    return fwd_ws(args, kGDN);
+    return fwd_ws(args, kGDN, true);
+}
+
+size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args) {
+    if (!args) return 0;
+    return fwd_ws(args, kGDN, false);
 }
 
 gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream) {
@@ -231,6 +244,8 @@ gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
         f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
         f.o = nullptr; f.ht = nullptr; f.h_save = h; f.dev_status = a->dev_status;
         f.workspace = ws + 2 * per;
+        f.workspace_bytes = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
+                                ? fwd_tc_workspace_bytes(ntm, a->H) : 0;
         f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
         f.nt_max = ntm;
         f.scale = a->scale;

@@ -1,6 +1,7 @@
 // gcl_internal.cuh -- declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,6 +29,7 @@ struct FwdParams {
     float *ht, *h_save;
     int32_t *dev_status;
     void *workspace;
+    size_t workspace_bytes;
     int64_t t_max, nt_max;
     int32_t n_max, H, K, V;
     float scale;
@@ -55,9 +57,22 @@ cudaError_t launch_chunk_meta(const int32_t *cu, int32_t n_max, int64_t t_max, i
                               int64_t nt_max, int32_t *idx, int32_t *off, int32_t *order,
                               int32_t *status, cudaStream_t s);
 cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s);
+// Tensor-core forward (GDN, bf16, K = V = 128).  Two launch plans: the W form
+// (prep + chain, 25 KiB of workspace per chunk and head) and the transition form
+// (96 KiB per chunk and head, a shorter serial step), which is taken when the column
+// split is 4 or more and the workspace holds it.
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s);
+cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s);
 bool fwd_tc_supported(int variant, int dtype, int K, int V);
-size_t fwd_tc_workspace_bytes(int64_t nt_max, int H);
+size_t fwd_tc_workspace_bytes(int64_t nt_max, int H);     // W form (the minimum)
+size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H);   // transition form
+int fwd_tc_split(int n_max, int H);                        // value-column slices per head
+bool fwd_tc_prefers_transition(int n_max, int H);
+
+// Encodes a TMA tensor map (cuTensorMapEncodeTiled, looked up once through the runtime).
+bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+                     const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw,
+                     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, cudaStream_t s);
 
 // ---- device helpers -------------------------------------------------------

@@ -136,8 +136,8 @@ typedef struct gcl_fwd_args {
                                    /* chunk i of sequence n at row chunk_offsets[n] + i      */
     int32_t *dev_status;           /* [1] or NULL: no work if non-zero on entry; set to      */
                                    /* GCL_DEV_BAD_RANGE if a sequence range is invalid       */
-    void *workspace;               /* device scratch of gcl_fwd_workspace_bytes() bytes      */
-    size_t workspace_bytes;
+    void *workspace;               /* device scratch, at least                               */
+    size_t workspace_bytes;        /* gcl_fwd_workspace_min_bytes() bytes                    */
     int64_t t_max;                 /* token capacity of every [t_max, ...] buffer            */
     int32_t n_max;                 /* sequence capacity (cu_seqlens has n_max + 1 entries)   */
     int32_t H, K, V;               /* heads, key dim, value dim                              */
@@ -146,10 +146,19 @@ typedef struct gcl_fwd_args {
     int32_t dtype;                 /* gcl_dtype_t of q, k, v, beta, o                        */
 } gcl_fwd_args;
 
-/* Bytes of device workspace the forward needs for these sizes (0 when the fp32
- * CUDA-core kernel serves them).  The tensor-core path keeps, per chunk and
- * head, the inverted intra-chunk matrix T and the masked decayed QK^T (bf16). */
+/* Bytes of device workspace the forward's fastest launch plan uses for these sizes
+ * (0 when the fp32 CUDA-core kernel serves them), and the least it accepts.
+ *
+ * The tensor-core path has two plans.  The W form keeps per chunk and head the
+ * inverted intra-chunk matrix T and the masked decayed QK^T, 25 KiB (bf16); it is
+ * the minimum.  The transition form keeps per chunk and head the chunk's affine
+ * state map and output map (N, B, Y, Z below, bf16), 96 KiB; it shortens the serial
+ * step per chunk and is the fastest plan when each head is split over 4 or more
+ * value-column slices (few sequence-head units).  The forward runs the fastest plan
+ * whose scratch fits in workspace_bytes, so any workspace of at least the minimum
+ * works; a given size always selects the same plan. */
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
+size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
 
 /*
  * gdn_chunk_fwd -- gated delta rule prefill: o and ht from q, k, v, g, beta, h0.
@@ -164,9 +173,11 @@ size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
  *
  * Supported: bt = 64; K, V in {64, 128}; dtype GCL_F32 or GCL_BF16.  GDN with
  * bf16 inputs and K = V = 128 runs on the tensor cores (tcgen05): a
- * chunk-parallel launch over chunk_indices forms T = (I + A)^-1 and L per chunk
- * into the workspace, then the per-(sequence, head, column slice) launch runs
- * the state recurrence.  Everything else runs the fp32 CUDA-core kernel.
+ * chunk-parallel launch over chunk_indices forms per chunk either T = (I + A)^-1
+ * and L (W form) or the chunk's transition S' = Gamma_c S + N S + B and output
+ * O = Y S + Z (transition form) into the workspace, then the per-(sequence, head,
+ * column slice) launch runs the state recurrence.  Everything else runs the fp32
+ * CUDA-core kernel.
  * Pointers must be 16-byte aligned.
  */
 gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
@@ -185,10 +196,11 @@ gcl_status_t kda_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);
  * (32 MiB) inside the library, which every GPU that loads the library holds
  * until the process exits.  It allocates and frees nothing.
  *
- *  - Sizes whose scratch (gcl_fwd_workspace_bytes) exceeds that limit return
- *    GCL_ERR_CAPACITY before any work is enqueued.  The bf16 K = V = 128 path
- *    needs 25 KiB per chunk and head, i.e. up to 1310 chunk-heads (for example
- *    T = 4096 tokens with 16 heads).
+ *  - Sizes whose minimum scratch (gcl_fwd_workspace_min_bytes) exceeds that limit
+ *    return GCL_ERR_CAPACITY before any work is enqueued.  The bf16 K = V = 128
+ *    path needs at least 25 KiB per chunk and head, i.e. up to 1310 chunk-heads
+ *    (for example T = 4096 tokens with 16 heads).  The plan is the fastest one
+ *    whose scratch fits in the array.
  *  - The first call on a device looks up the array's device address (with that
  *    device current) and caches it; make that first call before any stream
  *    capture.

@@ -55,9 +55,11 @@ class Meta:
                              seq_order=self.order, bt=self.bt, stream=stream)
 
 
-def run_fwd(w, d, meta=None, h_save=False, o_fill=CANARY, use_order=True):
+def run_fwd(w, d, meta=None, h_save=False, o_fill=CANARY, use_order=True, plan="fastest"):
     """Run chunk_meta_build + the forward for workload w on device inputs d.
 
+    plan "fastest" hands the forward the workspace of its fastest launch plan, "min" the
+    least it accepts (the W-form plan of the tensor-core path).
     Returns dict of device outputs: o, ht, h_save (if asked), plus meta."""
     if meta is None:
         meta = Meta(w.t_max, w.n_max, w.bt)
@@ -72,7 +74,7 @@ def run_fwd(w, d, meta=None, h_save=False, o_fill=CANARY, use_order=True):
     kw = dict(h0=d.get("h0"), ht=ht, h_save=hs, chunk_indices=meta.idx, chunk_offsets=meta.off,
               seq_order=meta.order if use_order else None, dev_status=meta.status,
               scale=w.scale, bt=w.bt)
-    nb = gcl.fwd_workspace_bytes(*args, **kw)
+    nb = (gcl.fwd_workspace_bytes if plan == "fastest" else gcl.fwd_workspace_min_bytes)(*args, **kw)
     ws = torch.full((max(nb, 16),), 0xFF, dtype=torch.uint8, device=DEV)   # stale contents
     fn(*args, workspace=ws, **kw)
     return dict(o=o, ht=ht, h_save=hs, meta=meta, ws=ws)

@@ -12,13 +12,37 @@ from gpu_util import CANARY, DEV, Meta, TOL, check_fwd, relF, run_fwd, to_device
 STD = synth.standard_workloads()
 
 
-@pytest.mark.parametrize("idx", [0, 1, 2], ids=[w.name for w in STD[:3]])
-def test_standard_workload_full_size(idx):
+@pytest.mark.parametrize("idx,plan", [(0, "fastest"), (1, "fastest"), (1, "min"), (2, "fastest")],
+                         ids=[STD[0].name, STD[1].name + "-transition", STD[1].name + "-wform",
+                              STD[2].name])
+def test_standard_workload_full_size(idx, plan):
+    """The 4096-token, 16-head GDN workload runs both tensor-core plans: the transition
+    form (its fastest plan, 8 column slices per head) and the W form (least workspace)."""
     w = STD[idx]
     x = synth.make_inputs(w)
-    out = run_fwd(w, to_device(w, x))
+    out = run_fwd(w, to_device(w, x), plan=plan)
     e_o, e_h = check_fwd(w, x, out, label=w.name)
-    print(f"{w.name}: o {e_o:.2e} ht {e_h:.2e}")
+    print(f"{w.name} ({plan}): o {e_o:.2e} ht {e_h:.2e}")
+
+
+@pytest.mark.parametrize("H", [3, 1], ids=["split4", "split8"])
+@pytest.mark.parametrize("plan", ["fastest", "min"], ids=["transition", "wform"])
+def test_gdn_bf16_plans_ragged(plan, H):
+    """Both tensor-core plans on ragged lengths (1, 63, 64, 65, 200, empty), with h0 and
+    saved chunk states, at column splits 4 (H=3: 24 units) and 8 (H=1: 8 units)."""
+    lens = [1, 63, 0, 64, 65, 200, 130, 0]
+    w = synth.varlen("plans", synth.GDN, "bf16", lens, 8, sum(lens) + 40, H, 128, 128, seed=15)
+    x = synth.make_inputs(w)
+    out = run_fwd(w, to_device(w, x), h_save=True, plan=plan)
+    check_fwd(w, x, out, label=f"plans {plan}")
+    meta = out["meta"]
+    off = meta.off.cpu().numpy()
+    _, _, hc = oracle.fwd(synth.GDN, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                          x["cu_seqlens"], w.scale, bt=64, chunk_offsets=off, nt_rows=meta.nt_max)
+    live = int(off[-1])
+    hs = out["h_save"].cpu().numpy()
+    assert relF(hs[:live], hc[:live]) <= TOL["bf16"]
+    assert (hs[live:] == np.float32(CANARY)).all()
 
 
 CASES = []

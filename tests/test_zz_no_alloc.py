@@ -1,8 +1,9 @@
 """gdn_chunk_fwd_noalloc: the forward for callers that cannot allocate device memory.
 
 It must give the same results as gdn_chunk_fwd with a caller workspace, call after
-call (the static scratch keeps the previous call's contents), and refuse sizes whose
-scratch does not fit.  This file is collected last so that a run stopping at the first
+call (the static scratch keeps the previous call's contents), fall back to the W-form
+plan when the transition form's records do not fit its scratch, and refuse sizes whose
+minimum scratch does not fit.  This file is collected last so that a run stopping at the first
 failure has already run every other test."""
 import ctypes
 
@@ -35,8 +36,9 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         kw = dict(h0=d["h0"], chunk_indices=meta.idx, chunk_offsets=meta.off,
                   seq_order=meta.order, dev_status=meta.status, scale=w.scale)
         o_ref, ht_ref = _outputs(w)
-        need = gcl.fwd_workspace_bytes(*args, o_ref, ht=ht_ref, **kw)
+        need = gcl.fwd_workspace_min_bytes(*args, o_ref, ht=ht_ref, **kw)
         assert 0 < need <= gcl.noalloc_scratch_bytes()
+        assert gcl.fwd_workspace_bytes(*args, o_ref, ht=ht_ref, **kw) > gcl.noalloc_scratch_bytes()
         ws = torch.empty(need, dtype=torch.uint8, device=DEV)
         gcl.gdn_chunk_fwd(*args, o_ref, ht=ht_ref, workspace=ws, **kw)
         o_na, ht_na = _outputs(w)
@@ -58,7 +60,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     a = gcl.fwd_args(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], o, ht=ht,
                      chunk_indices=meta.idx, chunk_offsets=meta.off, dev_status=meta.status,
                      scale=w.scale)
-    assert gcl.lib().gcl_fwd_workspace_bytes(ctypes.byref(a)) > gcl.noalloc_scratch_bytes()
+    assert gcl.lib().gcl_fwd_workspace_min_bytes(ctypes.byref(a)) > gcl.noalloc_scratch_bytes()
     st = gcl.lib().gdn_chunk_fwd_noalloc(ctypes.byref(a), None)
     assert st == 3                                   # GCL_ERR_CAPACITY, nothing enqueued
     assert b"static scratch" in gcl.lib().gcl_last_error()
