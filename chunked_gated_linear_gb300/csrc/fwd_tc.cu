@@ -41,6 +41,7 @@
 
 #include "gcl_internal.cuh"
 #include "tc_ptx.cuh"
+#include "tc_solve.cuh"
 
 namespace gcl {
 namespace {
@@ -95,7 +96,8 @@ struct PrepParams {
 };
 
 // The fp32 solve buffers reuse the K/Q tile once the MMA has consumed it.
-constexpr int kPrepSmem = 1024 + 2 * (C * (C + 1) * 4) + 3 * 16 * 17 * 4;
+constexpr int kPrepSmem = 1024 + (kSolveFloats + C * kSolveLD) * 4;   // + decay table
+static_assert(kSolveFloats * 4 >= 32768, "the K/Q tile fits under the solve buffers");
 
 __global__ void __launch_bounds__(kThreads)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -103,13 +105,14 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *sKQ = smem;                                         // [2 cb][128 rows][128 B]
-    float *sA = reinterpret_cast<float *>(smem);                 // [64][65], after the MMA
-    float *sT = sA + C * (C + 1);                                // [64][65], after the MMA
-    float *sX = sT + C * (C + 1);                                // [3][16][17]
+    float *sA = reinterpret_cast<float *>(smem);                 // [64][kSolveLD], after the MMA
+    float *sT = sA + C * kSolveLD;                               // [64][kSolveLD], after the MMA
+    float *sX = sT + C * kSolveLD;                               // solve scratch
+    float *sD = sA + kSolveFloats;                               // [64][kSolveLD] decay table
     __shared__ uint64_t bar_tma, bar_mma;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
-    __shared__ float sG[C], sB[C];
+    __shared__ float sG[C], sB[C], sEG[C];
 
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, j = blockIdx.x, h = blockIdx.y;
@@ -157,6 +160,19 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tma_load_3d(sKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
             tma_load_3d(sKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
         }
+    }
+    // while the tiles load: Gamma per column and the decay table D[r][c] = exp(g_r - g_c) for
+    // c <= r (1 above the diagonal; the exponent is selected, so no lane branches around the
+    // exponential)
+    if (tid < C) sEG[tid] = __expf(sG[tid]);
+    for (int e = tid; e < C * C / 4; e += kThreads) {
+        const int r = e >> 4, c = (e & 15) * 4;
+        const float gr = sG[r];
+        *reinterpret_cast<float4 *>(sD + r * kSolveLD + c) =
+            make_float4(__expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
+                        __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
+    }
+    if (tid == 0) {
         if (mbar_wait(&bar_tma, 0, &s_err, 1)) {
             tc_fence_after();
             const uint32_t base = smem_u32(sKQ);
@@ -178,7 +194,6 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + q * 16, v + q * 16);
         tmem_ld_wait();
-        for (int e = tid; e < C * (C + 1); e += kThreads) sT[e] = 0.f;   // K/Q tile is dead now
         __nv_bfloat16 *tl = p.tl + ((size_t)j * H + h) * kTLRows * C;
         if (tid < C) {
             const int r = tid;
@@ -189,68 +204,36 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             fac[C + r] = live ? p.scale * __expf(gr) : 0.f;     // read-out factor of row r
             fac[2 * C + r] = __expf(gc);                         // chunk decay Gamma_c
 #pragma unroll
-            for (int i = 0; i < C; ++i)
-                sA[r * (C + 1) + i] = (i < r && r < len) ? br * __expf(gr - sG[i]) * v[i] : 0.f;
+            for (int i = 0; i < C; i += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(sD + r * kSolveLD + i);
+                const float dec[4] = {d4.x, d4.y, d4.z, d4.w};
+                float a[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a[e] = (i + e < r && r < len) ? br * dec[e] * v[i + e] : 0.f;
+                *reinterpret_cast<float4 *>(sA + r * kSolveLD + i) = make_float4(a[0], a[1], a[2], a[3]);
+            }
         } else {
             const int r = tid - C;
-            const float gr = sG[r];
             uint4 *dst = reinterpret_cast<uint4 *>(tl + (size_t)(2 * C + r) * C);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
+                const float4 da = *reinterpret_cast<const float4 *>(sD + r * kSolveLD + q * 8);
+                const float4 db = *reinterpret_cast<const float4 *>(sD + r * kSolveLD + q * 8 + 4);
+                const float dec[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
                 uint4 pk;
                 __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i0 = q * 8 + 2 * e, i1 = i0 + 1;
-                    const float l0 = (i0 <= r && r < len) ? p.scale * __expf(gr - sG[i0]) * v[i0] : 0.f;
-                    const float l1 = (i1 <= r && r < len) ? p.scale * __expf(gr - sG[i1]) * v[i1] : 0.f;
+                    const float l0 = (i0 <= r && r < len) ? p.scale * dec[2 * e] * v[i0] : 0.f;
+                    const float l1 = (i1 <= r && r < len) ? p.scale * dec[2 * e + 1] * v[i1] : 0.f;
                     pp[e] = __floats2bfloat162_rn(l0, l1);
                 }
                 dst[q] = pk;
             }
         }
         __syncthreads();
-        // ---- T = (I + A)^-1.  Diagonal 16x16 blocks: thread (b, jj) owns column jj of block b.
-        if (tid < C) {
-            const int b = tid >> 4, jj = tid & 15, o = b * 16;
-            float tc[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) tc[r] = (r == jj) ? 1.f : 0.f;
-#pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                if (r > jj) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        if (m >= jj && m < r) acc = fmaf(sA[(o + r) * (C + 1) + o + m], tc[m], acc);
-                    tc[r] = -acc;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(o + r) * (C + 1) + o + jj] = tc[r];
-        }
-        __syncthreads();
-        // ---- off-diagonal blocks, level d: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, i - j = d
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
-                float acc = 0.f;
-                for (int m = bj * 16; m < bi * 16; ++m)
-                    acc = fmaf(sA[(bi * 16 + rr) * (C + 1) + m], sT[m * (C + 1) + bj * 16 + cc], acc);
-                sX[blk * 272 + rr * 17 + cc] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc = fmaf(sT[(bi * 16 + rr) * (C + 1) + bi * 16 + m], sX[blk * 272 + m * 17 + cc], acc);
-                sT[(bi * 16 + rr) * (C + 1) + bj * 16 + cc] = -acc;
-            }
-            __syncthreads();
-        }
+        solve_unit_lower64<kThreads>(sA, sT, sX);   // T = (I + A)^-1
         // ---- T diag(beta Gamma) -> rows 0..63, T diag(beta) -> rows 64..127 (bf16)
         {
             const int r = tid >> 1, half = tid & 1;
@@ -264,10 +247,10 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i0 = half * 32 + q * 8 + 2 * e;
-                    const float t0v = sT[r * (C + 1) + i0], t1v = sT[r * (C + 1) + i0 + 1];
+                    const float t0v = i0 <= r ? sT[r * kSolveLD + i0] : 0.f;
+                    const float t1v = i0 + 1 <= r ? sT[r * kSolveLD + i0 + 1] : 0.f;
                     ppt[e] = __floats2bfloat162_rn(t0v * sB[i0], t1v * sB[i0 + 1]);
-                    pps[e] = __floats2bfloat162_rn(t0v * sB[i0] * __expf(sG[i0]),
-                                                   t1v * sB[i0 + 1] * __expf(sG[i0 + 1]));
+                    pps[e] = __floats2bfloat162_rn(t0v * sB[i0] * sEG[i0], t1v * sB[i0 + 1] * sEG[i0 + 1]);
                 }
                 dst_t[q] = pt;
                 dst_s[q] = ps;

@@ -32,6 +32,7 @@
 
 #include "gcl_internal.cuh"
 #include "tc_ptx.cuh"
+#include "tc_solve.cuh"
 
 namespace gcl {
 namespace {
@@ -98,23 +99,24 @@ constexpr int kPrepThreads = 256;
 constexpr uint32_t pKQ = 0;        // [2 col blocks][K rows 0..63 | Q rows 0..63][128 B]  32 KiB
 constexpr uint32_t pV = 32768;     // [2 col blocks][64 rows][128 B]                      16 KiB
 constexpr uint32_t pTL = 49152;    // [T diag(bG); T diag(b); L], 192 rows of 64 tokens   24 KiB
-constexpr uint32_t pA = 73728;     // fp32 A, T [64][65], X [3][16][17]; later [W | U]
-constexpr uint32_t pEnd = pA + 2 * C * (C + 1) * 4 + 3 * 16 * 17 * 4;
+constexpr uint32_t pA = 73728;     // fp32 A, T [64][kSolveLD], X; later [W | U]
+constexpr uint32_t pEnd = pA + kSolveFloats * 4;
 constexpr int kPrepTSmem = pEnd + 1024;
 static_assert(pEnd - pA >= 4 * 8192, "[W | U] (4 atoms of 8 KiB) reuses the solve buffers");
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, PrepTParams p) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rec,
+                 PrepTParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     float *sA = reinterpret_cast<float *>(smem + pA);
-    float *sT = sA + C * (C + 1);
-    float *sX = sT + C * (C + 1);
+    float *sT = sA + C * kSolveLD;
+    float *sX = sT + C * kSolveLD;
     __shared__ uint64_t bar_tma, bar_mma;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
-    __shared__ float sG[C], sB[C], sF[C], sFQ[C], s_carry;
+    __shared__ float sG[C], sB[C], sF[C], sFQ[C], sEG[C], s_carry;
 
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, j = blockIdx.x, h = blockIdx.y;
@@ -135,11 +137,8 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     const int len = (int)(eos - t0 < C ? eos - t0 : C);
     const int H = p.H;
-    uint8_t *rec = p.ws + ((size_t)j * H + h) * kUnitBytes;
-    __nv_bfloat16 *gYN = reinterpret_cast<__nv_bfloat16 *>(rec);
-    __nv_bfloat16 *gB = reinterpret_cast<__nv_bfloat16 *>(rec + kYNBytes);
-    __nv_bfloat16 *gZ = reinterpret_cast<__nv_bfloat16 *>(rec + kYNBytes + kBBytes);
-    float *gGC = reinterpret_cast<float *>(rec + kYNBytes + kBBytes + kZBytes);
+    const int unit = j * H + h;
+    float *gGC = reinterpret_cast<float *>(p.ws + (size_t)unit * kUnitBytes + kYNBytes + kBBytes + kZBytes);
     const uint32_t sbase = smem_u32(smem);
 
     if (tid == 0) {
@@ -167,11 +166,6 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    if (tid < C) {
-        const bool live = tid < len;
-        sF[tid] = live ? __expf(sG[C - 1] - sG[tid]) : 0.f;   // row factor of Ktil
-        sFQ[tid] = live ? p.scale * __expf(sG[tid]) : 0.f;    // read-out factor
-    }
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar_tma, 49152);
         for (int cb = 0; cb < 2; ++cb) {
@@ -179,6 +173,22 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_load_3d(smem + pKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
             tma_load_3d(smem + pV + cb * 8192, &tm_v, cb * 64, h, (int)t0, &bar_tma);
         }
+    }
+    // while the tiles load: per-row factors and the decay table D[r][c] = exp(g_r - g_c) for
+    // c <= r (1 above the diagonal: the exponent is selected, so no lane branches around the
+    // exponential) in the T buffer, which the solve only writes later
+    if (tid < C) {
+        const bool live = tid < len;
+        sF[tid] = live ? __expf(sG[C - 1] - sG[tid]) : 0.f;   // row factor of Ktil
+        sFQ[tid] = live ? p.scale * __expf(sG[tid]) : 0.f;    // read-out factor
+        sEG[tid] = __expf(sG[tid]);                            // Gamma of column tid
+    }
+    for (int e = tid; e < C * C / 4; e += kPrepThreads) {
+        const int r = e >> 4, c = (e & 15) * 4;
+        const float gr = sG[r];
+        *reinterpret_cast<float4 *>(sT + r * kSolveLD + c) =
+            make_float4(__expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
+                        __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
     }
     uint32_t phase = 0;
     // every thread waits for the tensor-core group just committed; the block then agrees
@@ -229,75 +239,42 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tmem_ld16(tmem + lane_off + half * 32, v);
             tmem_ld16(tmem + lane_off + half * 32 + 16, v + 16);
             tmem_ld_wait();
-            if (lrow < C) {
-                const int r = lrow;
-                const float gr = sG[r], br = sB[r];
+            const int r = lrow & 63;
+            float dec[32];                                   // D[r][half*32 ..]
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = half * 32 + i;
-                    sA[r * (C + 1) + col] =
-                        (col < r && r < len) ? br * __expf(gr - sG[col]) * v[i] : 0.f;
+            for (int i = 0; i < 32; i += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(sT + r * kSolveLD + half * 32 + i);
+                dec[i] = d4.x; dec[i + 1] = d4.y; dec[i + 2] = d4.z; dec[i + 3] = d4.w;
+            }
+            if (lrow < C) {
+                const float br = sB[r];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    float a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = half * 32 + i + e;
+                        a[e] = (col < r && r < len) ? br * dec[i + e] * v[i + e] : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(sA + r * kSolveLD + half * 32 + i) =
+                        make_float4(a[0], a[1], a[2], a[3]);
                 }
             } else {
-                const int r = lrow - C;
-                const float gr = sG[r];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float l[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int col = half * 32 + q * 8 + e;
-                        l[e] = (col <= r && r < len) ? p.scale * __expf(gr - sG[col]) * v[q * 8 + e]
-                                                     : 0.f;
+                        l[e] = (col <= r && r < len) ? p.scale * dec[q * 8 + e] * v[q * 8 + e] : 0.f;
                     }
                     *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, 2 * C + r, half * 32 + q * 8)) =
                         pack8(l);
                 }
             }
-            for (int e = tid; e < C * (C + 1); e += kPrepThreads) sT[e] = 0.f;
         }
         __syncthreads();
-        // ---- T = (I + A)^-1: 16 x 16 diagonal blocks (one thread per column), then three
-        // levels of off-diagonal blocks  T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
-        if (tid < C) {
-            const int b = tid >> 4, jj = tid & 15, o = b * 16;
-            float tc[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) tc[r] = (r == jj) ? 1.f : 0.f;
-#pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                if (r > jj) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        if (m >= jj && m < r) acc = fmaf(sA[(o + r) * (C + 1) + o + m], tc[m], acc);
-                    tc[r] = -acc;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(o + r) * (C + 1) + o + jj] = tc[r];
-        }
-        __syncthreads();
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
-                float acc = 0.f;
-                for (int m = bj * 16; m < bi * 16; ++m)
-                    acc = fmaf(sA[(bi * 16 + rr) * (C + 1) + m], sT[m * (C + 1) + bj * 16 + cc], acc);
-                sX[blk * 272 + rr * 17 + cc] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-                const int blk = e >> 8, bi = d + blk, bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc = fmaf(sT[(bi * 16 + rr) * (C + 1) + bi * 16 + m], sX[blk * 272 + m * 17 + cc], acc);
-                sT[(bi * 16 + rr) * (C + 1) + bj * 16 + cc] = -acc;
-            }
-            __syncthreads();
-        }
+        solve_unit_lower64<kPrepThreads>(sA, sT, sX);   // T = (I + A)^-1
         // ---- T diag(beta Gamma) -> rows 0..63, T diag(beta) -> rows 64..127 (bf16, K-major)
         {
             const int r = tid >> 2;
@@ -307,8 +284,8 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 float tb[8], tg[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    tb[e] = sT[r * (C + 1) + c0 + e] * sB[c0 + e];
-                    tg[e] = tb[e] * __expf(sG[c0 + e]);
+                    tb[e] = c0 + e <= r ? sT[r * kSolveLD + c0 + e] * sB[c0 + e] : 0.f;
+                    tg[e] = tb[e] * sEG[c0 + e];
                 }
                 *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, r, c0)) = pack8(tg);
                 *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, C + r, c0)) = pack8(tb);
@@ -366,6 +343,11 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mma_commit(&bar_mma);
         }
         if (!mma_done(4)) break;
+        // Outputs leave through shared memory in 64 x 64 boxes (128-byte swizzle) and TMA
+        // stores of the record rows: Y 0..63, N 64..191, B 192..319, Z 320..383.
+        auto box_chunk = [&](uint32_t box, int row, int q) {   // 16-byte chunk q of a box row
+            return smem + box + row * 128 + ((q ^ (row & 7)) << 4);
+        };
         if (lrow >= C) {   // Y = scale diag(Gamma) Q - L W and Z = L U, row r, columns half*64..
             const int r = lrow - C;
             const float fq = sFQ[r];
@@ -386,7 +368,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     y[2 * e] = live ? fmaf(fq, f2.x, -x[q * 8 + 2 * e]) : 0.f;
                     y[2 * e + 1] = live ? fmaf(fq, f2.y, -x[q * 8 + 2 * e + 1]) : 0.f;
                 }
-                *reinterpret_cast<uint4 *>(gYN + (size_t)r * KD + c) = pack8(y);
+                *reinterpret_cast<uint4 *>(box_chunk(pV + half * 8192, r, q)) = pack8(y);
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, x + q * 16);
@@ -396,7 +378,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 float z[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) z[e] = live ? x[q * 8 + e] : 0.f;
-                *reinterpret_cast<uint4 *>(gZ + (size_t)r * VD + half * 64 + q * 8) = pack8(z);
+                *reinterpret_cast<uint4 *>(box_chunk(pTL + half * 8192, r, q)) = pack8(z);
             }
         }
         if (tid == 0) {
@@ -404,6 +386,13 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             *reinterpret_cast<float4 *>(gGC) = make_float4(gc, 0.f, 0.f, 0.f);
         }
         to_async();
+        if (tid == 0) {   // Y and Z boxes
+            for (int cb = 0; cb < 2; ++cb) {
+                tma_store_3d(&tm_rec, smem + pV + cb * 8192, cb * 64, 0, unit);
+                tma_store_3d(&tm_rec, smem + pTL + cb * 8192, cb * 64, 320, unit);
+            }
+            bulk_commit();
+        }
         // ---- MMA3: Ktil^T [W | U] -> cols 0..127: Ktil^T W = -N, cols 128..255: B
         if (tid == 0) {
             const uint64_t a = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
@@ -414,10 +403,11 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mma_commit(&bar_mma);
         }
         if (!mma_done(5)) break;
-        {   // key row m = lrow: half 0 -> N row (rows 64.. of [Y; N]), half 1 -> B row
+        {   // key row m = lrow: half 0 -> N boxes (in the dead K/Q tiles), half 1 -> B boxes
+            // (in the dead [W | U] operand); box (m / 64, column block)
             const int m = lrow;
             const float sg = half == 0 ? -1.f : 1.f;
-            __nv_bfloat16 *dst = half == 0 ? gYN + (size_t)(C + m) * KD : gB + (size_t)m * VD;
+            const uint32_t base = (half == 0 ? pKQ : pA) + (m >> 6) * 2 * 8192;
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
                 float x[64];
@@ -430,11 +420,22 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     float y[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) y[e] = sg * x[q * 8 + e];
-                    *reinterpret_cast<uint4 *>(dst + pass * 64 + q * 8) = pack8(y);
+                    *reinterpret_cast<uint4 *>(box_chunk(base + pass * 8192, m & 63, q)) = pack8(y);
                 }
             }
         }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            for (int rb = 0; rb < 2; ++rb)
+                for (int cb = 0; cb < 2; ++cb) {
+                    tma_store_3d(&tm_rec, smem + pKQ + (rb * 2 + cb) * 8192, cb * 64, 64 + rb * 64, unit);
+                    tma_store_3d(&tm_rec, smem + pA + (rb * 2 + cb) * 8192, cb * 64, 192 + rb * 64, unit);
+                }
+            bulk_commit();
+        }
     } while (0);
+    if (tid == 0) bulk_wait_read();         // the stores' shared-memory reads are done
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
@@ -472,51 +473,45 @@ __device__ __forceinline__ uint32_t mn_sw128(int k, int n) {
 }
 
 constexpr int kComputeThreads = 256;                  // warps 0..7
-constexpr int kChainThreads = kComputeThreads + 32;   // + warp 8: TMA and MMA issue
+constexpr int kG1Parts = 2;                           // G1 issued from two threads, two accumulators
+constexpr int kChainThreads = kComputeThreads + 32 * (kG1Parts + 2);   // + G1, G2 and TMA warps
 
-__device__ __forceinline__ void compute_barrier() {
+__device__ __forceinline__ void compute_barrier() {   // named barrier over warps 0..7
     asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
 }
-__device__ __forceinline__ bool compute_barrier_or(bool flag) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)flag), "n"(kComputeThreads)
-        : "memory");
-    return r != 0;
-}
 
-// Per-(sequence, head, column slice) recurrence.  Warps 0..7 compute: thread t owns key
-// row 32 (w & 3) + (t & 31) of the state slice and the column half (w >> 2).  Warp 8
-// (one lane) issues every TMA and MMA.  Per chunk n (stage n % NS):
-//   issuer:  wait S(n) | G1(n) = N S(n) -> D1 | G2(n) = [Y; N_top] S(n) -> D2[n & 1] |
-//            refill the stage of chunk n - 1 with chunk n - 1 + NS
-//   compute: S(n+1) = Gamma_c S(n) + D1 + B -> Sb[(n+1) & 1] | O(n) = D2 + Z | free stage
-// Each barrier that is waited on by parity is only re-armed after its waiter has passed,
-// so no waiter can fall two phases behind.
+// Per-(sequence, head, column slice) recurrence, warp-specialised.  Warps 0..7 compute:
+// thread t owns key row 32 (w & 3) + (t & 31) of the state slice and the column half
+// (w >> 2).  One lane each of the next warps issues
+//   warps 8, 9:  G1(n) = N S(n), split over the key dimension into two accumulators
+//                (the serial step: it alone sits between S(n) and S(n+1)),
+//   warp 10:     G2(n) = [Y; N_top] S(n) (the output, off the serial path),
+//   warp 11:     the TMA loads of chunk n + NS once chunk n's stage is released.
+// Compute per chunk: S(n+1) = Gamma_c S(n) + B + D1a + D1b -> Sb[(n+1) & 1] | O(n) = D2 + Z.
+// Every mbarrier waited on by parity is re-armed only after its waiter has passed
+// (barriers that a faster party could lap come in pairs indexed by chunk parity), so no
+// waiter can fall two phases behind.  After a failed (timed-out) wait every further wait
+// returns at once, so all loops run to their ends without a uniform break.
 template <int VS, int NS>
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_constant__ CUtensorMap tm_b,
                   const __grid_constant__ CUtensorMap tm_z, ChainTParams p) {
     using Lay = ChainTLayout<VS, NS>;
     constexpr int HV = VS / 2;                          // columns per compute thread
-    constexpr uint32_t tD1 = 0, tD2 = VS;               // D1 | D2 (two buffers)
-    constexpr uint32_t kTmemCols = 3 * VS <= 32 ? 32 : 3 * VS <= 64 ? 64 : 3 * VS <= 128 ? 128 : 256;
+    constexpr int KS = 8 / kG1Parts;                    // K-steps (16 keys) per G1 part
+    constexpr uint32_t tD1 = 0, tD2 = kG1Parts * VS;    // D1 parts | D2 (two buffers)
+    constexpr uint32_t kCols = (kG1Parts + 2) * VS;
+    constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb, bar_g1, bar_g2[2];
+    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb1, bar_sb2[2], bar_g1[kG1Parts], bar_g2[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
     if (status_blocks(p.status)) return;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const bool compute = warp < 8;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = (warp >> 2) & 1;
-    const int row = quarter * 32 + (tid & 31);
+    const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int split = blockIdx.x, h = blockIdx.y;
     const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
@@ -544,12 +539,14 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bar_tma[i], 1);
-            mbar_init(&bar_free[i], 1);
+            mbar_init(&bar_free[i], kComputeThreads / 32);
         }
-        mbar_init(&bar_sb, 1);
-        mbar_init(&bar_g1, 1);
-        mbar_init(&bar_g2[0], 1);
-        mbar_init(&bar_g2[1], 1);
+        mbar_init(&bar_sb1, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_sb2[i], 1);
+            mbar_init(&bar_g2[i], 1);
+        }
+        for (int i = 0; i < kG1Parts; ++i) mbar_init(&bar_g1[i], 1);
         s_err = 0;
         fence_barrier_init();
     }
@@ -561,10 +558,52 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    constexpr uint32_t idm = idesc_bf16(128, VS, 0, 1);
+    auto dS = [&](int ic) {                          // S(ic) as the MN-major B operand
+        return smem_desc(sbase + Lay::oSB + (ic & 1) * 16384, 8192, 1024, kSwizzle128B);
+    };
+    auto dYN = [&](int st) {                         // [Y; N] of a stage, K-major
+        return smem_desc(sbase + st * Lay::kStage + Lay::oYN, 16, 1024, kSwizzle128B);
+    };
 
-    if (!compute) {
-        // ======================================================= issuer (warp 8, lane 0)
-        if ((tid & 31) == 0) {
+    if (warp >= 8 && warp < 8 + kG1Parts) {
+        // ============================================ G1 part (warps 8.., lane 0)
+        const int part = warp - 8;
+        if (lane == 0) {
+            for (int ic = 0; ic < nch; ++ic) {
+                const int st = ic % NS;
+                if (!mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 7)) break;
+                if (!mbar_wait(&bar_sb1, ic & 1, &s_err, 8)) break;
+                tc_fence_after();
+                const uint64_t a = dYN(st) + (8192 >> 4), b = dS(ic);   // N: rows 64..191
+#pragma unroll
+                for (int j = 0; j < KS; ++j) {
+                    const int s = part * KS + j;
+                    mma_bf16(tmem + tD1 + part * VS, a + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
+                             b + s * 128, idm, j > 0);
+                }
+                mma_commit(&bar_g1[part]);
+            }
+        }
+    } else if (warp == 8 + kG1Parts) {
+        // ============================================ G2 (lane 0)
+        if (lane == 0) {
+            for (int ic = 0; ic < nch; ++ic) {
+                const int st = ic % NS;
+                if (!mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 9)) break;
+                if (!mbar_wait(&bar_sb2[ic & 1], (ic >> 1) & 1, &s_err, 10)) break;
+                tc_fence_after();
+                const uint64_t a = dYN(st), b = dS(ic);                // [Y; N_top]: rows 0..127
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16(tmem + tD2 + (ic & 1) * VS, a + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
+                             b + s * 128, idm, s > 0);
+                mma_commit(&bar_g2[ic & 1]);
+            }
+        }
+    } else if (warp == 9 + kG1Parts) {
+        // ============================================ TMA producer (lane 0)
+        if (lane == 0) {
             auto issue_tma = [&](int ic) {
                 const int st = ic % NS;
                 const int unit = (int)((row0 + ic) * H + h);
@@ -578,44 +617,26 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 bulk_load(b + Lay::oG, p.ws + (size_t)unit * kUnitBytes + kYNBytes + kBBytes + kZBytes,
                           16, bar);
             };
-            constexpr uint32_t id = idesc_bf16(128, VS, 0, 1);
-            for (int i = 0; i < NS && i < nch; ++i) issue_tma(i);
             for (int ic = 0; ic < nch; ++ic) {
-                const int st = ic % NS;
-                if (!mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 7)) break;
-                if (!mbar_wait(&bar_sb, ic & 1, &s_err, 8)) break;
-                tc_fence_after();
-                const uint64_t dS = smem_desc(sbase + Lay::oSB + (ic & 1) * 16384, 8192, 1024, kSwizzle128B);
-                const uint64_t dA = smem_desc(sbase + st * Lay::kStage + Lay::oYN, 16, 1024, kSwizzle128B);
-                // G1: D1 = N S  (rows 64..191 of [Y; N]; key blocks 24 KiB apart)
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_bf16(tmem + tD1, dA + (8192 >> 4) + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
-                             dS + s * 128, id, s > 0);
-                mma_commit(&bar_g1);
-                // G2: D2 = [Y; N_top] S  (rows 0..127)
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_bf16(tmem + tD2 + (ic & 1) * VS, dA + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
-                             dS + s * 128, id, s > 0);
-                mma_commit(&bar_g2[ic & 1]);
-                const int nx = ic - 1 + NS;                 // refill the stage of chunk ic - 1
-                if (ic >= 1 && nx < nch) {
-                    if (!mbar_wait(&bar_free[(ic - 1) % NS], ((ic - 1) / NS) & 1, &s_err, 9)) break;
-                    issue_tma(nx);
-                }
+                if (ic >= NS && !mbar_wait(&bar_free[ic % NS], ((ic - NS) / NS) & 1, &s_err, 11)) break;
+                issue_tma(ic);
             }
         }
     } else {
-        // ======================================================= compute (warps 0..7)
+        // ============================================ compute (warps 0..7)
         auto st_sb = [&](int buf, const float *x) {       // bf16 copy of this thread's S values
 #pragma unroll
-            for (int j = 0; j < HV; j += 8) {
-                uint4 pk;
-                __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[j + 2 * e], x[j + 2 * e + 1]);
-                *reinterpret_cast<uint4 *>(smem + Lay::oSB + buf * 16384 + mn_sw128(row, c0 + j)) = pk;
+            for (int j = 0; j < HV; j += 8)
+                *reinterpret_cast<uint4 *>(smem + Lay::oSB + buf * 16384 + mn_sw128(row, c0 + j)) =
+                    pack8(x + j);
+        };
+        auto handoff = [&](int ic) {                      // S(ic) is in Sb[ic & 1]
+            fence_async_smem();
+            tc_fence_before();
+            compute_barrier();
+            if (tid == 0) {
+                mbar_arrive(&bar_sb1);
+                mbar_arrive(&bar_sb2[ic & 1]);
             }
         };
         float S[HV];
@@ -625,12 +646,11 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
         }
         st_sb(0, S);
-        fence_async_smem();
-        compute_barrier();
-        if (tid == 0) mbar_arrive(&bar_sb);
-        bool failed = false;
+        handoff(0);
         for (int ic = 0; ic < nch; ++ic) {
-            const int st = ic % NS, len = (int)(eos - bos - (int64_t)ic * C < C ? eos - bos - (int64_t)ic * C : C);
+            const int st = ic % NS;
+            const int64_t rem = eos - bos - (int64_t)ic * C;
+            const int len = (int)(rem < C ? rem : C);
             const int64_t t0 = bos + (int64_t)ic * C;
             const uint8_t *stage = smem + st * Lay::kStage;
             if (p.h_save) {
@@ -640,31 +660,40 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
             }
             mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 3);
-            mbar_wait(&bar_g1, ic & 1, &s_err, 4);
-            tc_fence_after();
-            {   // S(n+1) = Gamma_c S(n) + N S(n) + B
+            {   // Gamma_c S + B while G1 runs
                 const float gc = *reinterpret_cast<const float *>(stage + Lay::oG);
                 const uint8_t *brow = stage + Lay::oB + row * (VS * 2) + c0 * 2;
 #pragma unroll
                 for (int j = 0; j < HV; j += 8) {
-                    float d1[8];
-                    tmem_ld8(tmem + lane_off + tD1 + c0 + j, d1);
-                    tmem_ld_wait();
                     const uint4 bv = *reinterpret_cast<const uint4 *>(brow + j * 2);
                     const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&bv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 b2 = __bfloat1622float2(bb[e]);
-                        S[j + 2 * e] = fmaf(gc, S[j + 2 * e], d1[2 * e] + b2.x);
-                        S[j + 2 * e + 1] = fmaf(gc, S[j + 2 * e + 1], d1[2 * e + 1] + b2.y);
+                        S[j + 2 * e] = fmaf(gc, S[j + 2 * e], b2.x);
+                        S[j + 2 * e + 1] = fmaf(gc, S[j + 2 * e + 1], b2.y);
                     }
                 }
             }
+            {   // + N S(n): the G1 parts
+                float d1[kG1Parts][HV];
+#pragma unroll
+                for (int part = 0; part < kG1Parts; ++part) {
+                    mbar_wait(&bar_g1[part], ic & 1, &s_err, 4);
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < HV; j += 8)
+                        tmem_ld8(tmem + lane_off + tD1 + part * VS + c0 + j, d1[part] + j);
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < HV; ++j) {
+#pragma unroll
+                    for (int part = 0; part < kG1Parts; ++part) S[j] += d1[part][j];
+                }
+            }
             st_sb((ic + 1) & 1, S);
-            fence_async_smem();
-            tc_fence_before();
-            compute_barrier();
-            if (tid == 0) mbar_arrive(&bar_sb);
+            handoff(ic + 1);
             // O(n) = Y S(n) + Z  (token rows = TMEM lanes 0..63)
             mbar_wait(&bar_g2[ic & 1], (ic >> 1) & 1, &s_err, 6);
             tc_fence_after();
@@ -692,13 +721,12 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                     }
                 }
             }
+            // this warp is done with stage st and with D2[ic & 1]
             tc_fence_before();
-            // stage st is free; decide uniformly on a failure the issuer may have recorded
-            failed = compute_barrier_or(*reinterpret_cast<volatile int *>(&s_err) != 0);
-            if (tid == 0) mbar_arrive(&bar_free[st]);
-            if (failed) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_free[st]);
         }
-        if (!failed && p.ht) {
+        if (p.ht && *reinterpret_cast<volatile int *>(&s_err) == 0) {
             float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
 #pragma unroll
             for (int j = 0; j < HV; j += 4)
@@ -711,7 +739,6 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
 }
 
-// ============================================================================ host
 template <int VS, int NS>
 cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const ChainTParams &cp,
                            int n_split, int H, int n_max, cudaStream_t s) {
@@ -749,13 +776,17 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     const cuuint32_t b64[3] = {64, 1, 64};
     const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
     const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
+    CUtensorMap mrec;                                 // the record as 384 rows of 128 bf16
+    const cuuint64_t drec[3] = {(cuuint64_t)KD, (cuuint64_t)(kUnitBytes / (KD * 2)), (cuuint64_t)units};
+    const cuuint32_t brec[3] = {64, 64, 1};
     const cuuint64_t dyn[3] = {(cuuint64_t)KD, (cuuint64_t)kYNRows, (cuuint64_t)units};
     const cuuint64_t syn[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
     const cuuint32_t byn[3] = {64, (cuuint32_t)kYNRows, 1};
     if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&myn, ws, 3, dyn, syn, byn, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_tensor_map(&myn, ws, 3, dyn, syn, byn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mrec, ws, 3, drec, syn, brec, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
     PrepTParams pp{};
@@ -772,7 +803,7 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(tc_prep_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPrepTSmem);
     if (e != cudaSuccess) return e;
-    tc_prep_t_kernel<<<dim3((unsigned)p.nt_max, H), kPrepThreads, kPrepTSmem, s>>>(mq, mk, mv, pp);
+    tc_prep_t_kernel<<<dim3((unsigned)p.nt_max, H), kPrepThreads, kPrepTSmem, s>>>(mq, mk, mv, mrec, pp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     ChainTParams cp{};
