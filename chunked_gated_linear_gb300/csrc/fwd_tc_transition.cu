@@ -42,14 +42,16 @@ constexpr int C = 64;
 constexpr int KD = 128;
 constexpr int VD = 128;
 
-// record per chunk and head in the workspace
+// Workspace: one record per chunk and head, [Y; N | B | Z] as 384 rows of 128 bf16 (96 KiB,
+// so every record starts on a 1 KiB boundary and TMA rows never straddle extra sectors), then
+// Gamma_c of every record in 16-byte slots.
 constexpr size_t kYNRows = 192;                      // [Y; N], bf16, 128 columns
 constexpr size_t kYNBytes = kYNRows * KD * 2;        // 48 KiB
 constexpr size_t kBBytes = (size_t)KD * VD * 2;      // 32 KiB
 constexpr size_t kZBytes = (size_t)C * VD * 2;       // 16 KiB
-constexpr size_t kGBytes = 16;                       // Gamma_c, padded to 16 bytes
-constexpr size_t kUnitBytes = kYNBytes + kBBytes + kZBytes + kGBytes;
-static_assert(kUnitBytes % 16 == 0, "TMA strides are multiples of 16 bytes");
+constexpr size_t kUnitBytes = kYNBytes + kBBytes + kZBytes;
+constexpr size_t kGBytes = 16;                       // Gamma_c slot
+static_assert(kUnitBytes % 1024 == 0, "records start on 1 KiB boundaries");
 
 __device__ __forceinline__ float warp_scan(float x) {
     const int lane = threadIdx.x & 31;
@@ -87,9 +89,9 @@ struct PrepTParams {
     const int32_t *chunk_indices, *cu;
     const float *g;
     const __nv_bfloat16 *beta;
-    uint8_t *ws;                 // nt_max * H records of kUnitBytes
+    uint8_t *ws;                 // nt_max * H records of kUnitBytes, then the Gamma_c slots
     int32_t *status;
-    int64_t t_max;
+    int64_t t_max, nt_max;
     int32_t n_max, H;
     float scale;
 };
@@ -138,7 +140,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int len = (int)(eos - t0 < C ? eos - t0 : C);
     const int H = p.H;
     const int unit = j * H + h;
-    float *gGC = reinterpret_cast<float *>(p.ws + (size_t)unit * kUnitBytes + kYNBytes + kBBytes + kZBytes);
+    float *gGC = reinterpret_cast<float *>(p.ws + (size_t)p.nt_max * H * kUnitBytes + (size_t)unit * kGBytes);
     const uint32_t sbase = smem_u32(smem);
 
     if (tid == 0) {
@@ -614,8 +616,8 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 tma_load_3d(b + Lay::oYN + 24576, &tm_yn, 64, 0, unit, bar);
                 tma_load_3d(b + Lay::oB, &tm_b, v0, 0, unit, bar);
                 tma_load_3d(b + Lay::oZ, &tm_z, v0, 0, unit, bar);
-                bulk_load(b + Lay::oG, p.ws + (size_t)unit * kUnitBytes + kYNBytes + kBBytes + kZBytes,
-                          16, bar);
+                bulk_load(b + Lay::oG, p.ws + (size_t)p.nt_max * H * kUnitBytes + (size_t)unit * kGBytes,
+                          kGBytes, bar);
             };
             for (int ic = 0; ic < nch; ++ic) {
                 if (ic >= NS && !mbar_wait(&bar_free[ic % NS], ((ic - NS) / NS) & 1, &s_err, 11)) break;
@@ -764,7 +766,9 @@ cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const Chai
 
 }  // namespace
 
-size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H) { return (size_t)nt_max * H * kUnitBytes; }
+size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H) {
+    return (size_t)nt_max * H * (kUnitBytes + kGBytes);
+}
 
 cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     const int H = p.H;
@@ -778,6 +782,7 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
     CUtensorMap mrec;                                 // the record as 384 rows of 128 bf16
     const cuuint64_t drec[3] = {(cuuint64_t)KD, (cuuint64_t)(kUnitBytes / (KD * 2)), (cuuint64_t)units};
+    static_assert(kUnitBytes % (KD * 2) == 0, "a record is whole rows");
     const cuuint32_t brec[3] = {64, 64, 1};
     const cuuint64_t dyn[3] = {(cuuint64_t)KD, (cuuint64_t)kYNRows, (cuuint64_t)units};
     const cuuint64_t syn[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
@@ -797,6 +802,7 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     pp.ws = ws;
     pp.status = p.dev_status;
     pp.t_max = p.t_max;
+    pp.nt_max = p.nt_max;
     pp.n_max = p.n_max;
     pp.H = H;
     pp.scale = p.scale;

@@ -64,14 +64,25 @@ static gcl_status_t check_common(const char *fn, const void *q, const void *k, c
     return GCL_OK;
 }
 
+// The kernels' per-chunk records start on 1 KiB boundaries of the workspace (full cache lines
+// for every TMA row); the queried sizes include the slack for aligning the caller's pointer.
+constexpr size_t kWsAlign = 1024;
+
+static void align_ws(void *ws, size_t bytes, void **out, size_t *out_bytes) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
+    const uintptr_t a = (b + kWsAlign - 1) & ~(uintptr_t)(kWsAlign - 1);
+    *out = reinterpret_cast<void *>(a);
+    *out_bytes = bytes > a - b ? bytes - (a - b) : 0;
+}
+
 // Forward workspace: the minimum (W form) or what the fastest launch plan uses.
 static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
     if (!fwd_tc_supported(variant, a->dtype, a->K, a->V)) return 0;
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->n_max <= 0) return 0;
     if (fastest && fwd_tc_prefers_transition(a->n_max, a->H))
-        return fwd_tc_t_workspace_bytes(ntm, a->H);
-    return fwd_tc_workspace_bytes(ntm, a->H);
+        return fwd_tc_t_workspace_bytes(ntm, a->H) + kWsAlign;
+    return fwd_tc_workspace_bytes(ntm, a->H) + kWsAlign;
 }
 
 static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int variant) {
@@ -88,7 +99,7 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
         if (!a->chunk_indices || !a->chunk_offsets)
             return fail(GCL_ERR_INVALID_ARG,
                         "%s: chunk_indices and chunk_offsets are required for bf16 K=V=128", fn);
-        const size_t need = fwd_tc_workspace_bytes(ntm, a->H);
+        const size_t need = fwd_ws(a, variant, false);
         if (!a->workspace || a->workspace_bytes < need)
             return fail(GCL_ERR_CAPACITY,
                         "%s: workspace of at least %zu bytes needed (%zu for the fastest "
@@ -106,8 +117,9 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     p.cu_seqlens = a->cu_seqlens; p.chunk_indices = a->chunk_indices;
     p.chunk_offsets = a->chunk_offsets; p.seq_order = a->seq_order;
     p.o = a->o; p.ht = a->ht; p.h_save = a->h_save; p.dev_status = a->dev_status;
-    p.workspace = a->workspace;
-    p.workspace_bytes = a->workspace ? a->workspace_bytes : 0;
+    p.workspace = nullptr;
+    p.workspace_bytes = 0;
+    if (tc) align_ws(a->workspace, a->workspace_bytes, &p.workspace, &p.workspace_bytes);
     p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V;
     p.nt_max = ntm;
     p.scale = a->scale;
@@ -127,7 +139,7 @@ static size_t bwd_ws(const gcl_bwd_args *a) {
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
     if (a->h_save) return per;
     const size_t fw = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
-                          ? align256(fwd_tc_workspace_bytes(ntm, a->H)) : 0;
+                          ? align256(fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign : 0;
     return 2 * per + fw;
 }
 
@@ -243,9 +255,11 @@ gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
         f.cu_seqlens = a->cu_seqlens; f.chunk_indices = a->chunk_indices;
         f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
         f.o = nullptr; f.ht = nullptr; f.h_save = h; f.dev_status = a->dev_status;
-        f.workspace = ws + 2 * per;
-        f.workspace_bytes = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
-                                ? fwd_tc_workspace_bytes(ntm, a->H) : 0;
+        f.workspace = nullptr;
+        f.workspace_bytes = 0;
+        if (fwd_tc_supported(kGDN, a->dtype, a->K, a->V))     // room for the W form only
+            align_ws(ws + 2 * per, fwd_tc_workspace_bytes(ntm, a->H) + kWsAlign - 1, &f.workspace,
+                     &f.workspace_bytes);
         f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
         f.nt_max = ntm;
         f.scale = a->scale;
