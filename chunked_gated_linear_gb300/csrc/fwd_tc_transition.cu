@@ -474,39 +474,44 @@ __device__ __forceinline__ uint32_t mn_sw128(int k, int n) {
     return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((n >> 3) ^ (k & 7))) << 4) + (n & 7) * 2);
 }
 
-constexpr int kComputeThreads = 256;                  // warps 0..7
+constexpr int kComputeThreads = 256;                  // warps 0..7: the state
+constexpr int kOutWarps = 2;                          // warps 8, 9: the output rows 0..63
 constexpr int kG1Parts = 2;                           // G1 issued from two threads, two accumulators
-constexpr int kChainThreads = kComputeThreads + 32 * (kG1Parts + 2);   // + G1, G2 and TMA warps
+constexpr int kWarpG1 = 8 + kOutWarps;                // first G1 warp
+constexpr int kWarpG2 = kWarpG1 + kG1Parts;
+constexpr int kWarpTma = kWarpG2 + 1;
+constexpr int kChainThreads = 32 * (kWarpTma + 1);
 
 __device__ __forceinline__ void compute_barrier() {   // named barrier over warps 0..7
     asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
 }
 
-// Per-(sequence, head, column slice) recurrence, warp-specialised.  Warps 0..7 compute:
-// thread t owns key row 32 (w & 3) + (t & 31) of the state slice and the column half
-// (w >> 2).  One lane each of the next warps issues
-//   warps 8, 9:  G1(n) = N S(n), split over the key dimension into two accumulators
-//                (the serial step: it alone sits between S(n) and S(n+1)),
-//   warp 10:     G2(n) = [Y; N_top] S(n) (the output, off the serial path),
-//   warp 11:     the TMA loads of chunk n + NS once chunk n's stage is released.
-// Compute per chunk: S(n+1) = Gamma_c S(n) + B + D1a + D1b -> Sb[(n+1) & 1] | O(n) = D2 + Z.
-// Every mbarrier waited on by parity is re-armed only after its waiter has passed
-// (barriers that a faster party could lap come in pairs indexed by chunk parity), so no
-// waiter can fall two phases behind.  After a failed (timed-out) wait every further wait
-// returns at once, so all loops run to their ends without a uniform break.
+// Per-(sequence, head, column slice) recurrence, warp-specialised:
+//   warps 0..7   the state: thread t owns key row 32 (w & 3) + (t & 31) of the state slice and
+//                the column half (w >> 2); S(n+1) = Gamma_c S(n) + B + D1 -> Sb[(n+1) & 1];
+//   warps 8, 9   the output: token rows 32 (w - 8) + (t & 31); O(n) = D2 + Z;
+//   warps 10, 11 (one lane each) G1(n) = N S(n), split over the key dimension into two
+//                accumulators (the serial step: it alone sits between S(n) and S(n+1));
+//   warp 12      G2(n) = [Y; N_top] S(n) -> D2[n & 1] (the output, off the serial path);
+//   warp 13      the TMA loads of chunk n + NS once chunk n's stage is released.
+// Every mbarrier waited on by parity is re-armed only after its waiter has passed (barriers
+// that a faster party could lap come in pairs indexed by chunk parity), so no waiter can fall
+// two phases behind.  After a failed (timed-out) wait every further wait returns at once, so
+// all loops run to their ends without a uniform break.
 template <int VS, int NS>
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_constant__ CUtensorMap tm_b,
                   const __grid_constant__ CUtensorMap tm_z, ChainTParams p) {
     using Lay = ChainTLayout<VS, NS>;
-    constexpr int HV = VS / 2;                          // columns per compute thread
+    constexpr int HV = VS / 2;                          // columns per state thread
     constexpr int KS = 8 / kG1Parts;                    // K-steps (16 keys) per G1 part
     constexpr uint32_t tD1 = 0, tD2 = kG1Parts * VS;    // D1 parts | D2 (two buffers)
     constexpr uint32_t kCols = (kG1Parts + 2) * VS;
     constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb1, bar_sb2[2], bar_g1[kG1Parts], bar_g2[2];
+    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb1, bar_sb2[2], bar_g1[kG1Parts], bar_g2[2],
+        bar_d2free[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
@@ -536,23 +541,23 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     const uint32_t sbase = smem_u32(smem);
     const int64_t KV = (int64_t)KD * VD;
     const int64_t state_base = ((int64_t)n * H + h) * KV;
-    const int c0 = half * HV;
 
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bar_tma[i], 1);
-            mbar_init(&bar_free[i], kComputeThreads / 32);
+            mbar_init(&bar_free[i], kComputeThreads / 32 + kOutWarps);
         }
         mbar_init(&bar_sb1, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_sb2[i], 1);
             mbar_init(&bar_g2[i], 1);
+            mbar_init(&bar_d2free[i], kOutWarps);
         }
         for (int i = 0; i < kG1Parts; ++i) mbar_init(&bar_g1[i], 1);
         s_err = 0;
         fence_barrier_init();
     }
-    if (warp == 8) {
+    if (warp == kWarpG1) {
         tmem_alloc(&s_tmem, kTmemCols);
         tmem_relinquish();
     }
@@ -568,9 +573,9 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
         return smem_desc(sbase + st * Lay::kStage + Lay::oYN, 16, 1024, kSwizzle128B);
     };
 
-    if (warp >= 8 && warp < 8 + kG1Parts) {
-        // ============================================ G1 part (warps 8.., lane 0)
-        const int part = warp - 8;
+    if (warp >= kWarpG1 && warp < kWarpG1 + kG1Parts) {
+        // ============================================ G1 part (lane 0)
+        const int part = warp - kWarpG1;
         if (lane == 0) {
             for (int ic = 0; ic < nch; ++ic) {
                 const int st = ic % NS;
@@ -587,13 +592,15 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 mma_commit(&bar_g1[part]);
             }
         }
-    } else if (warp == 8 + kG1Parts) {
+    } else if (warp == kWarpG2) {
         // ============================================ G2 (lane 0)
         if (lane == 0) {
             for (int ic = 0; ic < nch; ++ic) {
                 const int st = ic % NS;
                 if (!mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 9)) break;
                 if (!mbar_wait(&bar_sb2[ic & 1], (ic >> 1) & 1, &s_err, 10)) break;
+                // D2[ic & 1] has been read for chunk ic - 2
+                if (ic >= 2 && !mbar_wait(&bar_d2free[ic & 1], ((ic - 2) >> 1) & 1, &s_err, 12)) break;
                 tc_fence_after();
                 const uint64_t a = dYN(st), b = dS(ic);                // [Y; N_top]: rows 0..127
 #pragma unroll
@@ -603,7 +610,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 mma_commit(&bar_g2[ic & 1]);
             }
         }
-    } else if (warp == 9 + kG1Parts) {
+    } else if (warp == kWarpTma) {
         // ============================================ TMA producer (lane 0)
         if (lane == 0) {
             auto issue_tma = [&](int ic) {
@@ -624,8 +631,49 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 issue_tma(ic);
             }
         }
+    } else if (warp >= 8) {
+        // ============================================ output (warps 8, 9): O(n) = Y S(n) + Z
+        const int orow = (warp - 8) * 32 + lane;               // token row = TMEM lane
+        const uint32_t olane = (uint32_t)((warp - 8) * 32) << 16;
+        for (int ic = 0; ic < nch; ++ic) {
+            const int st = ic % NS;
+            const int64_t rem = eos - bos - (int64_t)ic * C;
+            const int len = (int)(rem < C ? rem : C);
+            const int64_t t0 = bos + (int64_t)ic * C;
+            const uint8_t *stage = smem + st * Lay::kStage;
+            mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 5);
+            mbar_wait(&bar_g2[ic & 1], (ic >> 1) & 1, &s_err, 6);
+            tc_fence_after();
+            float d2[VS];
+#pragma unroll
+            for (int j = 0; j < VS; j += 8) tmem_ld8(tmem + olane + tD2 + (ic & 1) * VS + j, d2 + j);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_d2free[ic & 1]);
+            if (orow < len && p.o != nullptr) {
+                const uint8_t *zrow = stage + Lay::oZ + orow * (VS * 2);
+                __nv_bfloat16 *dst = p.o + ((t0 + orow) * H + h) * (int64_t)VD + v0;
+#pragma unroll
+                for (int j = 0; j < VS; j += 8) {
+                    const uint4 zv = *reinterpret_cast<const uint4 *>(zrow + j * 2);
+                    const __nv_bfloat162 *zz = reinterpret_cast<const __nv_bfloat162 *>(&zv);
+                    float ov[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 z2 = __bfloat1622float2(zz[e]);
+                        ov[2 * e] = d2[j + 2 * e] + z2.x;
+                        ov[2 * e + 1] = d2[j + 2 * e + 1] + z2.y;
+                    }
+                    *reinterpret_cast<uint4 *>(dst + j) = pack8(ov);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_free[st]);        // done with Z of stage st
+        }
     } else {
-        // ============================================ compute (warps 0..7)
+        // ============================================ state (warps 0..7)
+        const int c0 = half * HV;
         auto st_sb = [&](int buf, const float *x) {       // bf16 copy of this thread's S values
 #pragma unroll
             for (int j = 0; j < HV; j += 8)
@@ -651,9 +699,6 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
         handoff(0);
         for (int ic = 0; ic < nch; ++ic) {
             const int st = ic % NS;
-            const int64_t rem = eos - bos - (int64_t)ic * C;
-            const int len = (int)(rem < C ? rem : C);
-            const int64_t t0 = bos + (int64_t)ic * C;
             const uint8_t *stage = smem + st * Lay::kStage;
             if (p.h_save) {
                 float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
@@ -694,39 +739,12 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                     for (int part = 0; part < kG1Parts; ++part) S[j] += d1[part][j];
                 }
             }
+            // Sb[(ic + 1) & 1] was last read by G2(ic - 1)
+            if (ic >= 1) mbar_wait(&bar_g2[(ic - 1) & 1], ((ic - 1) >> 1) & 1, &s_err, 13);
             st_sb((ic + 1) & 1, S);
             handoff(ic + 1);
-            // O(n) = Y S(n) + Z  (token rows = TMEM lanes 0..63)
-            mbar_wait(&bar_g2[ic & 1], (ic >> 1) & 1, &s_err, 6);
-            tc_fence_after();
-            if (quarter < 2) {        // warp-uniform: every lane takes part in the TMEM load
-                float d2[HV];
-#pragma unroll
-                for (int j = 0; j < HV; j += 8)
-                    tmem_ld8(tmem + lane_off + tD2 + (ic & 1) * VS + c0 + j, d2 + j);
-                tmem_ld_wait();
-                if (row < len && p.o != nullptr) {
-                    const uint8_t *zrow = stage + Lay::oZ + row * (VS * 2) + c0 * 2;
-                    __nv_bfloat16 *dst = p.o + ((t0 + row) * H + h) * (int64_t)VD + v0 + c0;
-#pragma unroll
-                    for (int j = 0; j < HV; j += 8) {
-                        const uint4 zv = *reinterpret_cast<const uint4 *>(zrow + j * 2);
-                        const __nv_bfloat162 *zz = reinterpret_cast<const __nv_bfloat162 *>(&zv);
-                        float ov[8];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 z2 = __bfloat1622float2(zz[e]);
-                            ov[2 * e] = d2[j + 2 * e] + z2.x;
-                            ov[2 * e + 1] = d2[j + 2 * e + 1] + z2.y;
-                        }
-                        *reinterpret_cast<uint4 *>(dst + j) = pack8(ov);
-                    }
-                }
-            }
-            // this warp is done with stage st and with D2[ic & 1]
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_free[st]);
+            if (lane == 0) mbar_arrive(&bar_free[st]);        // done with B of stage st
         }
         if (p.ht && *reinterpret_cast<volatile int *>(&s_err) == 0) {
             float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
@@ -737,7 +755,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kWarpG1) tmem_dealloc(tmem, kTmemCols);
     if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
 }
 
