@@ -106,6 +106,40 @@ constexpr uint32_t pEnd = pA + kSolveFloats * 4;
 constexpr int kPrepTSmem = pEnd + 1024;
 static_assert(pEnd - pA >= 4 * 8192, "[W | U] (4 atoms of 8 KiB) reuses the solve buffers");
 
+// One work item per row j of chunk_indices and head h, numbered i = j H + h (the record
+// index).  Rows past the live chunks hold the [-1, 0] sentinel, so a CTA that walks its items
+// in increasing order stops at the first sentinel.
+struct PrepItem {
+    int64_t t0;
+    int h, len;
+};
+
+// Next live item at or after i in steps of `stride` (-1 when there is none); invalid rows set
+// the status word and are skipped.  Every thread of the block computes the same answer.
+__device__ __forceinline__ int next_item(const PrepTParams &p, int i, int stride, PrepItem *it) {
+    const int total = (int)(p.nt_max * p.H);
+    for (; i < total; i += stride) {
+        const int j = i / p.H;
+        const int n = p.chunk_indices[2 * j];
+        if (n < 0) return -1;                                  // sentinel: no more live rows
+        const int ic = p.chunk_indices[2 * j + 1];
+        if (n < p.n_max && ic >= 0) {
+            const int64_t bos = p.cu[n], eos = p.cu[n + 1], t0 = bos + (int64_t)ic * C;
+            if (bos >= 0 && eos >= bos && eos <= p.t_max && t0 < eos) {
+                it->t0 = t0;
+                it->h = i - j * p.H;
+                it->len = (int)(eos - t0 < C ? eos - t0 : C);
+                return i;
+            }
+        }
+        if (threadIdx.x == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+    }
+    return -1;
+}
+
+// Persistent: gridDim.x CTAs (two per SM) walk the items with stride gridDim.x.  The next
+// item's K and Q tiles are requested as soon as MMA3 has consumed the current ones, its V tile
+// once the output stores have read their staging buffers, and its gates during MMA3.
 __global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rec,
@@ -115,36 +149,26 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     float *sA = reinterpret_cast<float *>(smem + pA);
     float *sT = sA + C * kSolveLD;
     float *sX = sT + C * kSolveLD;
-    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint64_t bar_kq, bar_v, bar_mma;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
     __shared__ float sG[C], sB[C], sF[C], sFQ[C], sEG[C], s_carry;
 
     if (status_blocks(p.status)) return;
-    const int tid = threadIdx.x, warp = tid >> 5, j = blockIdx.x, h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int quarter = warp & 3, half = warp >> 2;
     const int lrow = quarter * 32 + (tid & 31);           // TMEM lane read by this thread
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int n = p.chunk_indices[2 * j];
-    if (n < 0) return;                                     // sentinel: unused slot
-    const int ic = p.chunk_indices[2 * j + 1];
-    if (n >= p.n_max || ic < 0) {
-        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
-        return;
-    }
-    const int64_t bos = p.cu[n], eos = p.cu[n + 1], t0 = bos + (int64_t)ic * C;
-    if (bos < 0 || eos < bos || eos > p.t_max || t0 >= eos) {
-        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
-        return;
-    }
-    const int len = (int)(eos - t0 < C ? eos - t0 : C);
-    const int H = p.H;
-    const int unit = j * H + h;
-    float *gGC = reinterpret_cast<float *>(p.ws + (size_t)p.nt_max * H * kUnitBytes + (size_t)unit * kGBytes);
+    const int H = p.H, stride = gridDim.x;
     const uint32_t sbase = smem_u32(smem);
 
+    PrepItem cur, nxt;
+    int icur = next_item(p, blockIdx.x, stride, &cur);
+    if (icur < 0) return;
+
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_kq, 1);
+        mbar_init(&bar_v, 1);
         mbar_init(&bar_mma, 1);
         s_err = 0;
         fence_barrier_init();
@@ -153,46 +177,38 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tmem_alloc(&s_tmem, 256);
         tmem_relinquish();
     }
-    {   // gamma = inclusive cumsum of g over the chunk (warps 0 and 1), beta
-        const float gv = (tid < len) ? p.g[(t0 + tid) * H + h] : 0.f;
-        float x = tid < C ? warp_scan(gv) : 0.f;
-        if (tid == 31) s_carry = x;
-        __syncthreads();
-        if (tid >= 32 && tid < C) x += s_carry;
-        if (tid < C) {
-            sG[tid] = x;
-            sB[tid] = tid < len ? __bfloat162float(p.beta[(t0 + tid) * H + h]) : 0.f;
+    auto load_kq = [&](const PrepItem &it) {
+        mbar_arrive_expect_tx(&bar_kq, 32768);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(smem + pKQ + cb * 16384, &tm_k, cb * 64, it.h, (int)it.t0, &bar_kq);
+            tma_load_3d(smem + pKQ + cb * 16384 + 8192, &tm_q, cb * 64, it.h, (int)it.t0, &bar_kq);
         }
+    };
+    auto load_v = [&](const PrepItem &it) {
+        mbar_arrive_expect_tx(&bar_v, 16384);
+        for (int cb = 0; cb < 2; ++cb) tma_load_3d(smem + pV + cb * 8192, &tm_v, cb * 64, it.h, (int)it.t0, &bar_v);
+    };
+    // gates of an item for threads 0..63 (row tid): raw g and beta (0 past the end)
+    auto load_gates = [&](const PrepItem &it, float &gv, float &bv) {
+        gv = 0.f;
+        bv = 0.f;
+        if (tid < it.len) {
+            gv = p.g[(it.t0 + tid) * H + it.h];
+            bv = __bfloat162float(p.beta[(it.t0 + tid) * H + it.h]);
+        }
+    };
+    float g_raw, b_raw;
+    load_gates(cur, g_raw, b_raw);
+    if (tid == 0) {
+        load_kq(cur);
+        load_v(cur);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_tma, 49152);
-        for (int cb = 0; cb < 2; ++cb) {
-            tma_load_3d(smem + pKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
-            tma_load_3d(smem + pKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
-            tma_load_3d(smem + pV + cb * 8192, &tm_v, cb * 64, h, (int)t0, &bar_tma);
-        }
-    }
-    // while the tiles load: per-row factors and the decay table D[r][c] = exp(g_r - g_c) for
-    // c <= r (1 above the diagonal: the exponent is selected, so no lane branches around the
-    // exponential) in the T buffer, which the solve only writes later
-    if (tid < C) {
-        const bool live = tid < len;
-        sF[tid] = live ? __expf(sG[C - 1] - sG[tid]) : 0.f;   // row factor of Ktil
-        sFQ[tid] = live ? p.scale * __expf(sG[tid]) : 0.f;    // read-out factor
-        sEG[tid] = __expf(sG[tid]);                            // Gamma of column tid
-    }
-    for (int e = tid; e < C * C / 4; e += kPrepThreads) {
-        const int r = e >> 4, c = (e & 15) * 4;
-        const float gr = sG[r];
-        *reinterpret_cast<float4 *>(sT + r * kSolveLD + c) =
-            make_float4(__expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
-                        __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
-    }
-    uint32_t phase = 0;
+
+    uint32_t phase = 0, ph_in = 0;
     // every thread waits for the tensor-core group just committed; the block then agrees
     // on whether any wait gave up
     auto mma_done = [&](int code) -> bool {
@@ -207,237 +223,300 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         __syncthreads();
         tc_fence_after();
     };
-    do {
-        const bool landed = mbar_wait(&bar_tma, 0, &s_err, 1);
-        if (__syncthreads_or(!landed)) break;
-        // rows past the end of a partial chunk: zero K, Q and V (they may hold the next
-        // sequence or NaN padding and every one of them enters an MMA raw)
-        if (len < C) {
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            for (int t = tid; t < 6 * C * 8; t += kPrepThreads) {
-                const int r = (t >> 3) & 63, blk = t >> 9;       // K0 K1 Q0 Q1 V0 V1
-                if (r >= len) {
-                    const uint32_t base = blk < 4 ? pKQ + (blk & 1) * 16384 + (blk >> 1) * 8192
-                                                  : pV + (blk - 4) * 8192;
-                    *reinterpret_cast<uint4 *>(smem + base + r * 128 + (t & 7) * 16) = zero;
-                }
-            }
-        }
-        to_async();
-        // ---- MMA1: [K; Q] K^T -> lanes 0..63: K K^T, lanes 64..127: Q K^T  (N = 64)
-        if (tid == 0) {
-            const uint64_t d = smem_desc(sbase + pKQ, 16, 1024, kSwizzle128B);
-            constexpr uint32_t id = idesc_bf16(128, 64);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t o = (s >> 2) * 1024 + (s & 3) * 2;
-                mma_bf16(tmem, d + o, d + o, id, s > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        if (!mma_done(2)) break;
-        {   // A (fp32) from lanes 0..63, L (bf16, rows 128.. of [..; L]) from lanes 64..127
-            float v[32];
-            tmem_ld16(tmem + lane_off + half * 32, v);
-            tmem_ld16(tmem + lane_off + half * 32 + 16, v + 16);
-            tmem_ld_wait();
-            const int r = lrow & 63;
-            float dec[32];                                   // D[r][half*32 ..]
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(sT + r * kSolveLD + half * 32 + i);
-                dec[i] = d4.x; dec[i + 1] = d4.y; dec[i + 2] = d4.z; dec[i + 3] = d4.w;
-            }
-            if (lrow < C) {
-                const float br = sB[r];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    float a[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int col = half * 32 + i + e;
-                        a[e] = (col < r && r < len) ? br * dec[i + e] * v[i + e] : 0.f;
-                    }
-                    *reinterpret_cast<float4 *>(sA + r * kSolveLD + half * 32 + i) =
-                        make_float4(a[0], a[1], a[2], a[3]);
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float l[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int col = half * 32 + q * 8 + e;
-                        l[e] = (col <= r && r < len) ? p.scale * dec[q * 8 + e] * v[q * 8 + e] : 0.f;
-                    }
-                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, 2 * C + r, half * 32 + q * 8)) =
-                        pack8(l);
-                }
+    // 16-byte chunk q of row `row` of a 64 x 64 output box (128-byte swizzle)
+    auto box_chunk = [&](uint32_t box, int row, int q) {
+        return smem + box + row * 128 + ((q ^ (row & 7)) << 4);
+    };
+    while (icur >= 0) {
+        bool item_done = false;
+        const int len = cur.len;
+        const int unit = icur;
+        float *gGC = reinterpret_cast<float *>(p.ws + (size_t)p.nt_max * H * kUnitBytes + (size_t)unit * kGBytes);
+        {   // gamma = inclusive cumsum of g over the chunk (warps 0 and 1), beta
+            float x = tid < C ? warp_scan(g_raw) : 0.f;
+            if (tid == 31) s_carry = x;
+            __syncthreads();                      // (also: the previous item's buffers are free)
+            if (tid >= 32 && tid < C) x += s_carry;
+            if (tid < C) {
+                sG[tid] = x;
+                sB[tid] = b_raw;
             }
         }
         __syncthreads();
-        solve_unit_lower64<kPrepThreads>(sA, sT, sX);   // T = (I + A)^-1
-        // ---- T diag(beta Gamma) -> rows 0..63, T diag(beta) -> rows 64..127 (bf16, K-major)
-        {
-            const int r = tid >> 2;
-#pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-                const int c0 = ((tid & 3) * 2 + qq) * 8;
-                float tb[8], tg[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    tb[e] = c0 + e <= r ? sT[r * kSolveLD + c0 + e] * sB[c0 + e] : 0.f;
-                    tg[e] = tb[e] * sEG[c0 + e];
+        // factors and the decay table D[r][c] = exp(g_r - g_c) for c <= r (1 above the
+        // diagonal: the exponent is selected, so no lane branches around the exponential) in
+        // the T buffer, which the solve only writes later
+        if (tid < C) {
+            const bool live = tid < len;
+            sF[tid] = live ? __expf(sG[C - 1] - sG[tid]) : 0.f;   // row factor of Ktil
+            sFQ[tid] = live ? p.scale * __expf(sG[tid]) : 0.f;    // read-out factor
+            sEG[tid] = __expf(sG[tid]);                            // Gamma of column tid
+        }
+        for (int e = tid; e < C * C / 4; e += kPrepThreads) {
+            const int r = e >> 4, c = (e & 15) * 4;
+            const float gr = sG[r];
+            *reinterpret_cast<float4 *>(sT + r * kSolveLD + c) =
+                make_float4(__expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
+                            __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
+        }
+        do {
+            const bool landed = mbar_wait(&bar_kq, ph_in, &s_err, 1);
+            if (__syncthreads_or(!landed)) break;
+            // rows past the end of a partial chunk: zero K and Q (they may hold the next
+            // sequence or NaN padding and enter the MMAs raw); V likewise once it lands
+            if (len < C) {
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                for (int t = tid; t < 4 * C * 8; t += kPrepThreads) {
+                    const int r = (t >> 3) & 63, blk = t >> 9;       // K0 K1 Q0 Q1
+                    if (r >= len)
+                        *reinterpret_cast<uint4 *>(smem + pKQ + (blk & 1) * 16384 + (blk >> 1) * 8192 +
+                                                   r * 128 + (t & 7) * 16) = zero;
                 }
-                *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, r, c0)) = pack8(tg);
-                *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, C + r, c0)) = pack8(tb);
             }
-        }
-        to_async();
-        // ---- MMA2: [T bG; T b] K -> cols 0..127 (W in lanes 0..63);
-        //            [T bG; T b] V -> cols 128..255 (U in lanes 64..127).
-        // K and V are MN-major B operands (64-element atoms 16 KiB and 8 KiB apart).
-        if (tid == 0) {
-            const uint64_t a = smem_desc(sbase + pTL, 16, 1024, kSwizzle128B);
-            const uint64_t bk = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
-            const uint64_t bv = smem_desc(sbase + pV, 8192, 1024, kSwizzle128B);
-            constexpr uint32_t id = idesc_bf16(128, 128, 0, 1);
+            to_async();
+            // ---- MMA1: [K; Q] K^T -> lanes 0..63: K K^T, lanes 64..127: Q K^T  (N = 64)
+            if (tid == 0) {
+                const uint64_t d = smem_desc(sbase + pKQ, 16, 1024, kSwizzle128B);
+                constexpr uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, bk + s * 128, id, s > 0);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tmem + 128, a + s * 2, bv + s * 128, id, s > 0);
-            mma_commit(&bar_mma);
-        }
-        if (!mma_done(3)) break;
-        {   // [W | U] as one MN-major operand (N = 256: keys then values) in the solve buffers
-            const int tok = lrow & 63;
-            const int n0 = (lrow < C ? 0 : 128) + half * 64;
-            float wu[64];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + n0 + q * 16, wu + q * 16);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4 *>(smem + pA + mnmaj16(8192, tok, n0 + q * 8)) = pack8(wu + q * 8);
-            // Ktil = diag(exp(g_c - g)) K, in place (MMA2 has consumed K)
-            for (int t = tid; t < 2 * C * 8; t += kPrepThreads) {
-                const int r = (t >> 3) & 63, cb = t >> 9;
-                uint4 *pk = reinterpret_cast<uint4 *>(smem + pKQ + cb * 16384 + r * 128 + (t & 7) * 16);
-                uint4 x = *pk;
-                __nv_bfloat162 *xx = reinterpret_cast<__nv_bfloat162 *>(&x);
-                const float f = sF[r];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 y = __bfloat1622float2(xx[e]);
-                    xx[e] = __floats2bfloat162_rn(f * y.x, f * y.y);
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t o = (s >> 2) * 1024 + (s & 3) * 2;
+                    mma_bf16(tmem, d + o, d + o, id, s > 0);
                 }
-                *pk = x;
+                mma_commit(&bar_mma);
             }
-        }
-        to_async();
-        // ---- MMA4: [T b; L] [W | U] -> lanes 64..127: L W (cols 0..127), L U (cols 128..255)
-        if (tid == 0) {
-            const uint64_t a = smem_desc(sbase + pTL + 8192, 16, 1024, kSwizzle128B);
-            const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
-            constexpr uint32_t id = idesc_bf16(128, 256, 0, 1);
+            if (!mma_done(2)) break;
+            {   // A (fp32) from lanes 0..63, L (bf16, rows 128.. of [..; L]) from lanes 64..127
+                float v[32];
+                tmem_ld16(tmem + lane_off + half * 32, v);
+                tmem_ld16(tmem + lane_off + half * 32 + 16, v + 16);
+                tmem_ld_wait();
+                const int r = lrow & 63;
+                float dec[32];                                   // D[r][half*32 ..]
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, b + s * 128, id, s > 0);
-            mma_commit(&bar_mma);
-        }
-        if (!mma_done(4)) break;
-        // Outputs leave through shared memory in 64 x 64 boxes (128-byte swizzle) and TMA
-        // stores of the record rows: Y 0..63, N 64..191, B 192..319, Z 320..383.
-        auto box_chunk = [&](uint32_t box, int row, int q) {   // 16-byte chunk q of a box row
-            return smem + box + row * 128 + ((q ^ (row & 7)) << 4);
-        };
-        if (lrow >= C) {   // Y = scale diag(Gamma) Q - L W and Z = L U, row r, columns half*64..
-            const int r = lrow - C;
-            const float fq = sFQ[r];
-            const bool live = r < len;
-            float x[64];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, x + q * 16);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int c = half * 64 + q * 8;
-                const uint4 qv = *reinterpret_cast<const uint4 *>(smem + pKQ + kmaj16(128, C + r, c));
-                const __nv_bfloat162 *qq = reinterpret_cast<const __nv_bfloat162 *>(&qv);
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f2 = __bfloat1622float2(qq[e]);
-                    y[2 * e] = live ? fmaf(fq, f2.x, -x[q * 8 + 2 * e]) : 0.f;
-                    y[2 * e + 1] = live ? fmaf(fq, f2.y, -x[q * 8 + 2 * e + 1]) : 0.f;
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(sT + r * kSolveLD + half * 32 + i);
+                    dec[i] = d4.x; dec[i + 1] = d4.y; dec[i + 2] = d4.z; dec[i + 3] = d4.w;
                 }
-                *reinterpret_cast<uint4 *>(box_chunk(pV + half * 8192, r, q)) = pack8(y);
+                if (lrow < C) {
+                    const float br = sB[r];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        float a[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int col = half * 32 + i + e;
+                            a[e] = (col < r && r < len) ? br * dec[i + e] * v[i + e] : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(sA + r * kSolveLD + half * 32 + i) =
+                            make_float4(a[0], a[1], a[2], a[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float l[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int col = half * 32 + q * 8 + e;
+                            l[e] = (col <= r && r < len) ? p.scale * dec[q * 8 + e] * v[q * 8 + e] : 0.f;
+                        }
+                        *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, 2 * C + r, half * 32 + q * 8)) =
+                            pack8(l);
+                    }
+                }
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, x + q * 16);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float z[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) z[e] = live ? x[q * 8 + e] : 0.f;
-                *reinterpret_cast<uint4 *>(box_chunk(pTL + half * 8192, r, q)) = pack8(z);
+            __syncthreads();
+            solve_unit_lower64<kPrepThreads>(sA, sT, sX);   // T = (I + A)^-1
+            {
+                const bool vl = mbar_wait(&bar_v, ph_in, &s_err, 6);
+                if (__syncthreads_or(!vl)) break;
             }
-        }
-        if (tid == 0) {
-            const float gc = __expf(sG[C - 1]);
-            *reinterpret_cast<float4 *>(gGC) = make_float4(gc, 0.f, 0.f, 0.f);
-        }
-        to_async();
-        if (tid == 0) {   // Y and Z boxes
-            for (int cb = 0; cb < 2; ++cb) {
-                tma_store_3d(&tm_rec, smem + pV + cb * 8192, cb * 64, 0, unit);
-                tma_store_3d(&tm_rec, smem + pTL + cb * 8192, cb * 64, 320, unit);
+            if (len < C) {
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                for (int t = tid; t < 2 * C * 8; t += kPrepThreads) {
+                    const int r = (t >> 3) & 63, cb = t >> 9;
+                    if (r >= len) *reinterpret_cast<uint4 *>(smem + pV + cb * 8192 + r * 128 + (t & 7) * 16) = zero;
+                }
             }
-            bulk_commit();
-        }
-        // ---- MMA3: Ktil^T [W | U] -> cols 0..127: Ktil^T W = -N, cols 128..255: B
-        if (tid == 0) {
-            const uint64_t a = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
-            const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
-            constexpr uint32_t id = idesc_bf16(128, 256, 1, 1);
+            // ---- T diag(beta Gamma) -> rows 0..63, T diag(beta) -> rows 64..127 (bf16, K-major)
+            {
+                const int r = tid >> 2;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 128, b + s * 128, id, s > 0);
-            mma_commit(&bar_mma);
-        }
-        if (!mma_done(5)) break;
-        {   // key row m = lrow: half 0 -> N boxes (in the dead K/Q tiles), half 1 -> B boxes
-            // (in the dead [W | U] operand); box (m / 64, column block)
-            const int m = lrow;
-            const float sg = half == 0 ? -1.f : 1.f;
-            const uint32_t base = (half == 0 ? pKQ : pA) + (m >> 6) * 2 * 8192;
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int c0 = ((tid & 3) * 2 + qq) * 8;
+                    float tb[8], tg[8];
 #pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
+                    for (int e = 0; e < 8; ++e) {
+                        tb[e] = c0 + e <= r ? sT[r * kSolveLD + c0 + e] * sB[c0 + e] : 0.f;
+                        tg[e] = tb[e] * sEG[c0 + e];
+                    }
+                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, r, c0)) = pack8(tg);
+                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, C + r, c0)) = pack8(tb);
+                }
+            }
+            to_async();
+            // ---- MMA2: [T bG; T b] K -> cols 0..127 (W in lanes 0..63);
+            //            [T bG; T b] V -> cols 128..255 (U in lanes 64..127).
+            // K and V are MN-major B operands (64-element atoms 16 KiB and 8 KiB apart).
+            if (tid == 0) {
+                const uint64_t a = smem_desc(sbase + pTL, 16, 1024, kSwizzle128B);
+                const uint64_t bk = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
+                const uint64_t bv = smem_desc(sbase + pV, 8192, 1024, kSwizzle128B);
+                constexpr uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, bk + s * 128, id, s > 0);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_bf16(tmem + 128, a + s * 2, bv + s * 128, id, s > 0);
+                mma_commit(&bar_mma);
+            }
+            if (!mma_done(3)) break;
+            {   // [W | U] as one MN-major operand (N = 256: keys then values) in the solve buffers
+                const int tok = lrow & 63;
+                const int n0 = (lrow < C ? 0 : 128) + half * 64;
+                float wu[64];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + n0 + q * 16, wu + q * 16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<uint4 *>(smem + pA + mnmaj16(8192, tok, n0 + q * 8)) = pack8(wu + q * 8);
+                // Ktil = diag(exp(g_c - g)) K, in place (MMA2 has consumed K)
+                for (int t = tid; t < 2 * C * 8; t += kPrepThreads) {
+                    const int r = (t >> 3) & 63, cb = t >> 9;
+                    uint4 *pk = reinterpret_cast<uint4 *>(smem + pKQ + cb * 16384 + r * 128 + (t & 7) * 16);
+                    uint4 x = *pk;
+                    __nv_bfloat162 *xx = reinterpret_cast<__nv_bfloat162 *>(&x);
+                    const float f = sF[r];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 y = __bfloat1622float2(xx[e]);
+                        xx[e] = __floats2bfloat162_rn(f * y.x, f * y.y);
+                    }
+                    *pk = x;
+                }
+            }
+            to_async();
+            // ---- MMA4: [T b; L] [W | U] -> lanes 64..127: L W (cols 0..127), L U (cols 128..255)
+            if (tid == 0) {
+                const uint64_t a = smem_desc(sbase + pTL + 8192, 16, 1024, kSwizzle128B);
+                const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
+                constexpr uint32_t id = idesc_bf16(128, 256, 0, 1);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, b + s * 128, id, s > 0);
+                mma_commit(&bar_mma);
+            }
+            if (!mma_done(4)) break;
+            // Outputs leave through shared memory in 64 x 64 boxes (128-byte swizzle) and TMA
+            // stores of the record rows: Y 0..63, N 64..191, B 192..319, Z 320..383.
+            if (lrow >= C) {   // Y = scale diag(Gamma) Q - L W and Z = L U, row r, columns half*64..
+                const int r = lrow - C;
+                const float fq = sFQ[r];
+                const bool live = r < len;
                 float x[64];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    tmem_ld16(tmem + lane_off + half * 128 + pass * 64 + q * 16, x + q * 16);
+                for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, x + q * 16);
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
+                    const int c = half * 64 + q * 8;
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(smem + pKQ + kmaj16(128, C + r, c));
+                    const __nv_bfloat162 *qq = reinterpret_cast<const __nv_bfloat162 *>(&qv);
                     float y[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = sg * x[q * 8 + e];
-                    *reinterpret_cast<uint4 *>(box_chunk(base + pass * 8192, m & 63, q)) = pack8(y);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f2 = __bfloat1622float2(qq[e]);
+                        y[2 * e] = live ? fmaf(fq, f2.x, -x[q * 8 + 2 * e]) : 0.f;
+                        y[2 * e + 1] = live ? fmaf(fq, f2.y, -x[q * 8 + 2 * e + 1]) : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(box_chunk(pV + half * 8192, r, q)) = pack8(y);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, x + q * 16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float z[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) z[e] = live ? x[q * 8 + e] : 0.f;
+                    *reinterpret_cast<uint4 *>(box_chunk(pTL + half * 8192, r, q)) = pack8(z);
                 }
             }
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            for (int rb = 0; rb < 2; ++rb)
+            if (tid == 0) {
+                const float gc = __expf(sG[C - 1]);
+                *reinterpret_cast<float4 *>(gGC) = make_float4(gc, 0.f, 0.f, 0.f);
+            }
+            to_async();
+            if (tid == 0) {   // Y and Z boxes
                 for (int cb = 0; cb < 2; ++cb) {
-                    tma_store_3d(&tm_rec, smem + pKQ + (rb * 2 + cb) * 8192, cb * 64, 64 + rb * 64, unit);
-                    tma_store_3d(&tm_rec, smem + pA + (rb * 2 + cb) * 8192, cb * 64, 192 + rb * 64, unit);
+                    tma_store_3d(&tm_rec, smem + pV + cb * 8192, cb * 64, 0, unit);
+                    tma_store_3d(&tm_rec, smem + pTL + cb * 8192, cb * 64, 320, unit);
                 }
-            bulk_commit();
-        }
-    } while (0);
-    if (tid == 0) bulk_wait_read();         // the stores' shared-memory reads are done
+                bulk_commit();
+            }
+            // ---- MMA3: Ktil^T [W | U] -> cols 0..127: Ktil^T W = -N, cols 128..255: B
+            if (tid == 0) {
+                const uint64_t a = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
+                const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
+                constexpr uint32_t id = idesc_bf16(128, 256, 1, 1);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 128, b + s * 128, id, s > 0);
+                mma_commit(&bar_mma);
+            }
+            // the next item and its gates, while MMA3 runs
+            const int inext = next_item(p, icur + stride, stride, &nxt);
+            if (inext >= 0) load_gates(nxt, g_raw, b_raw);
+            if (!mma_done(5)) break;
+            if (tid == 0) {
+                if (inext >= 0) load_kq(nxt);          // K and Q of this item are consumed
+                bulk_wait_read();                      // the Y and Z stores have read pV, pTL
+            }
+            __syncthreads();
+            {   // key row m = lrow: half 0 -> N boxes in the [W | U] buffer, half 1 -> B boxes
+                // (0, 0), (0, 1), (1, 0) in the [..; L] buffer and (1, 1) in the V buffer
+                const int m = lrow;
+                const float sg = half == 0 ? -1.f : 1.f;
+#pragma unroll
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int bidx = (m >> 6) * 2 + pass;
+                    const uint32_t box = half == 0 ? pA + bidx * 8192 : (bidx < 3 ? pTL + bidx * 8192 : pV);
+                    float x[64];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(tmem + lane_off + half * 128 + pass * 64 + q * 16, x + q * 16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) y[e] = sg * x[q * 8 + e];
+                        *reinterpret_cast<uint4 *>(box_chunk(box, m & 63, q)) = pack8(y);
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                for (int rb = 0; rb < 2; ++rb)
+                    for (int cb = 0; cb < 2; ++cb) {
+                        const int bidx = rb * 2 + cb;
+                        tma_store_3d(&tm_rec, smem + pA + bidx * 8192, cb * 64, 64 + rb * 64, unit);
+                        tma_store_3d(&tm_rec, smem + (bidx < 3 ? pTL + bidx * 8192 : pV), cb * 64,
+                                     192 + rb * 64, unit);
+                    }
+                bulk_commit();
+                bulk_wait_read();                      // staging buffers are free again
+                if (inext >= 0) load_v(nxt);
+            }
+            tc_fence_after();
+            icur = inext;
+            cur = nxt;
+            ph_in ^= 1;
+            item_done = true;
+        } while (0);
+        if (!item_done) break;                         // a wait gave up (uniformly decided)
+    }
+    if (tid == 0) bulk_wait_read();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
@@ -827,7 +906,9 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(tc_prep_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPrepTSmem);
     if (e != cudaSuccess) return e;
-    tc_prep_t_kernel<<<dim3((unsigned)p.nt_max, H), kPrepThreads, kPrepTSmem, s>>>(mq, mk, mv, mrec, pp);
+    const int64_t items = p.nt_max * H;
+    const int grid = (int)(items < 2 * (int64_t)num_sms() ? items : 2 * (int64_t)num_sms());
+    tc_prep_t_kernel<<<grid, kPrepThreads, kPrepTSmem, s>>>(mq, mk, mv, mrec, pp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     ChainTParams cp{};
