@@ -227,6 +227,30 @@ class Runner:
             raise RuntimeError(self.gcl.lib().gcl_last_error().decode())
 
 
+def reduce_max(values, dist, device):
+    """Element-wise maximum over the ranks of a list of timings (the slowest replica sets the
+    job's time); identity without a process group."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own replica (weak scaling), the step time
+    is the slowest rank's."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
+def launches_per_step(w) -> int:
+    """Library kernels per step: chunk_meta_build, the forward (prep and chain on the tensor
+    cores for GDN bf16 d_k = d_v = 128, one fused CUDA-core kernel otherwise) and the
+    backward's sweep and chunk-gradient kernels."""
+    tc = w.variant == synth.GDN and w.dtype == "bf16" and w.K == 128 and w.V == 128
+    return 1 + (2 if tc else 1) + (2 if w.backward else 0)
+
+
 def run_gpu(args, rank, world, dist):
     import torch
     import chunked_gated_linear_gb300 as gcl
@@ -283,13 +307,10 @@ def run_gpu(args, rank, world, dist):
     step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
     kern_ms = [a.elapsed_time(b) for a, b in ev_k]
     region_ms = ev_s[0].elapsed_time(ev_e[-1])
-    tot = torch.tensor([sum(step_ms), sum(kern_ms), region_ms], dtype=torch.float64,
-                       device=dev)
-    if dist is not None:
-        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-    ms_step = float(tot[0]) / K
-    ms_kern = float(tot[1]) / K
-    value = w.total_tokens * world / (ms_step * 1e-3)
+    tot = reduce_max([sum(step_ms), sum(kern_ms), region_ms], dist, dev)
+    ms_step = tot[0] / K
+    ms_kern = tot[1] / K
+    value = job_throughput(w.total_tokens, world, ms_step)
 
     # end-to-end through the C ABI with host buffers: H2D inputs, step, D2H outputs
     e2e = run_e2e(gcl, w, x, first, stream, s, args.e2e_steps, world, dist)
@@ -319,7 +340,7 @@ def run_gpu(args, rank, world, dist):
                      "kernel_ms": ms_kern, "algorithmic_bytes_per_launch": ab,
                      "tensor_flops_per_launch": flops_per_step(w), "peak_source": peak_kind},
         "e2e": e2e,
-        "gpu_launches": K * (2 + (2 if w.backward else 0)),
+        "gpu_launches": K * launches_per_step(w),
         "clocks": clk,
     }
     return line
@@ -352,12 +373,8 @@ def run_e2e(gcl, w, x, r, stream, s, steps, world, dist):
         torch.cuda.synchronize()
         if i >= 3:
             times.append(e0.elapsed_time(e1))
-    ms = float(np.mean(times))
-    t = torch.tensor([ms], dtype=torch.float64, device=r.t["q"].device)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t[0])
-    return {"value": w.total_tokens * world / (ms * 1e-3), "unit": "tokens/s",
+    ms = reduce_max([float(np.mean(times))], dist, r.t["q"].device)[0]
+    return {"value": job_throughput(w.total_tokens, world, ms), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
