@@ -6,7 +6,8 @@
 //
 //  1. (only without saved states) the forward kernel recomputes the state
 //     before every chunk, S_n, into the workspace;
-//  2. dstate sweep: per (sequence, head, value-column slice), in reverse chunk
+//  2. dstate sweep (here unless the caller ran the tensor-core sweep of
+//     bwd_tc_transition.cu): per (sequence, head, value-column slice), in reverse chunk
 //     order, the gradient w.r.t. the state after chunk n, dS'_n, is saved and
 //     carried back through the chunk:
 //        dE = L^T dO + Ktil dS'
@@ -416,13 +417,15 @@ cudaError_t prep(Kern kern, size_t bytes) {
 }
 
 template <typename Tin, int K, int VS>
-cudaError_t launch_k(const BwdParams &p, cudaStream_t s) {
-    auto sweep = dstate_sweep_kernel<kGDN, Tin, K, VS>;
-    const size_t sb = SweepLayout<K, VS, kGDN>::bytes;
-    cudaError_t e = prep(sweep, sb);
-    if (e != cudaSuccess) return e;
-    sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+cudaError_t launch_k(const BwdParams &p, bool sweep_done, cudaStream_t s) {
+    cudaError_t e;
+    if (!sweep_done) {
+        auto sweep = dstate_sweep_kernel<kGDN, Tin, K, VS>;
+        const size_t sb = SweepLayout<K, VS, kGDN>::bytes;
+        if ((e = prep(sweep, sb)) != cudaSuccess) return e;
+        sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     auto grad = chunk_grad_kernel<Tin, K>;
     const size_t gb = GradLayout<K>::bytes;
     if ((e = prep(grad, gb)) != cudaSuccess) return e;
@@ -432,11 +435,12 @@ cudaError_t launch_k(const BwdParams &p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, cudaStream_t s) {
+cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s) {
     if (dtype == GCL_BF16)
-        return p.K == 64 ? launch_k<__nv_bfloat16, 64, 64>(p, s)
-                         : launch_k<__nv_bfloat16, 128, 32>(p, s);
-    return p.K == 64 ? launch_k<float, 64, 64>(p, s) : launch_k<float, 128, 32>(p, s);
+        return p.K == 64 ? launch_k<__nv_bfloat16, 64, 64>(p, sweep_done, s)
+                         : launch_k<__nv_bfloat16, 128, 32>(p, sweep_done, s);
+    return p.K == 64 ? launch_k<float, 64, 64>(p, sweep_done, s)
+                     : launch_k<float, 128, 32>(p, sweep_done, s);
 }
 
 }  // namespace gcl

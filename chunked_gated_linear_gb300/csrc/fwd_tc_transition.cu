@@ -33,25 +33,13 @@
 #include "gcl_internal.cuh"
 #include "tc_ptx.cuh"
 #include "tc_solve.cuh"
+#include "transition.cuh"
 
 namespace gcl {
 namespace {
 
 using namespace tc;
-constexpr int C = 64;
-constexpr int KD = 128;
-constexpr int VD = 128;
-
-// Workspace: one record per chunk and head, [Y; N | B | Z] as 384 rows of 128 bf16 (96 KiB,
-// so every record starts on a 1 KiB boundary and TMA rows never straddle extra sectors), then
-// Gamma_c of every record in 16-byte slots.
-constexpr size_t kYNRows = 192;                      // [Y; N], bf16, 128 columns
-constexpr size_t kYNBytes = kYNRows * KD * 2;        // 48 KiB
-constexpr size_t kBBytes = (size_t)KD * VD * 2;      // 32 KiB
-constexpr size_t kZBytes = (size_t)C * VD * 2;       // 16 KiB
-constexpr size_t kUnitBytes = kYNBytes + kBBytes + kZBytes;
-constexpr size_t kGBytes = 16;                       // Gamma_c slot
-static_assert(kUnitBytes % 1024 == 0, "records start on 1 KiB boundaries");
+using namespace tr;
 
 __device__ __forceinline__ float warp_scan(float x) {
     const int lane = threadIdx.x & 31;
@@ -61,14 +49,6 @@ __device__ __forceinline__ float warp_scan(float x) {
         if (lane >= d) x += y;
     }
     return x;
-}
-
-__device__ __forceinline__ uint4 pack8(const float *x) {
-    uint4 pk;
-    __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-    return pk;
 }
 
 // K-major 128-byte-swizzled bf16 tile of `rows` rows per 64-column block: byte offset
@@ -231,7 +211,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bool item_done = false;
         const int len = cur.len;
         const int unit = icur;
-        float *gGC = reinterpret_cast<float *>(p.ws + (size_t)p.nt_max * H * kUnitBytes + (size_t)unit * kGBytes);
+        float *gGC = reinterpret_cast<float *>(p.ws + gc_offset(p.nt_max, H, unit));
         {   // gamma = inclusive cumsum of g over the chunk (warps 0 and 1), beta
             float x = tid < C ? warp_scan(g_raw) : 0.f;
             if (tid == 31) s_carry = x;
@@ -549,10 +529,6 @@ struct ChainTLayout {
     static constexpr uint32_t kTmaBytes = kYN + kB + kZ + kG;
 };
 
-__device__ __forceinline__ uint32_t mn_sw128(int k, int n) {
-    return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((n >> 3) ^ (k & 7))) << 4) + (n & 7) * 2);
-}
-
 constexpr int kComputeThreads = 256;                  // warps 0..7: the state
 constexpr int kOutWarps = 2;                          // warps 8, 9: the output rows 0..63
 constexpr int kG1Parts = 2;                           // G1 issued from two threads, two accumulators
@@ -702,8 +678,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 tma_load_3d(b + Lay::oYN + 24576, &tm_yn, 64, 0, unit, bar);
                 tma_load_3d(b + Lay::oB, &tm_b, v0, 0, unit, bar);
                 tma_load_3d(b + Lay::oZ, &tm_z, v0, 0, unit, bar);
-                bulk_load(b + Lay::oG, p.ws + (size_t)p.nt_max * H * kUnitBytes + (size_t)unit * kGBytes,
-                          kGBytes, bar);
+                bulk_load(b + Lay::oG, p.ws + gc_offset(p.nt_max, H, unit), kGBytes, bar);
             };
             for (int ic = 0; ic < nch; ++ic) {
                 if (ic >= NS && !mbar_wait(&bar_free[ic % NS], ((ic - NS) / NS) & 1, &s_err, 11)) break;
@@ -867,30 +842,27 @@ size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H) {
     return (size_t)nt_max * H * (kUnitBytes + kGBytes);
 }
 
-cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
+size_t transition_record_bytes(int64_t nt_max, int H) { return fwd_tc_t_workspace_bytes(nt_max, H); }
+
+cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
     const int H = p.H;
     const int64_t units = p.nt_max * H;
-    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
-    CUtensorMap mq, mk, mv, myn;
+    CUtensorMap mq, mk, mv, mrec;
     const cuuint64_t dqk[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)p.t_max};
     const cuuint64_t sqk[2] = {(cuuint64_t)KD * 2, (cuuint64_t)H * KD * 2};
     const cuuint32_t b64[3] = {64, 1, 64};
     const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
     const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
-    CUtensorMap mrec;                                 // the record as 384 rows of 128 bf16
+    // the record as 384 rows of 128 bf16, 64 x 64 boxes
     const cuuint64_t drec[3] = {(cuuint64_t)KD, (cuuint64_t)(kUnitBytes / (KD * 2)), (cuuint64_t)units};
     static_assert(kUnitBytes % (KD * 2) == 0, "a record is whole rows");
+    const cuuint64_t srec[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
     const cuuint32_t brec[3] = {64, 64, 1};
-    const cuuint64_t dyn[3] = {(cuuint64_t)KD, (cuuint64_t)kYNRows, (cuuint64_t)units};
-    const cuuint64_t syn[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
-    const cuuint32_t byn[3] = {64, (cuuint32_t)kYNRows, 1};
     if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&myn, ws, 3, dyn, syn, byn, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&mrec, ws, 3, drec, syn, brec, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_tensor_map(&mrec, ws, 3, drec, srec, brec, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-
     PrepTParams pp{};
     pp.chunk_indices = p.chunk_indices;
     pp.cu = p.cu_seqlens;
@@ -906,10 +878,22 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(tc_prep_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPrepTSmem);
     if (e != cudaSuccess) return e;
-    const int64_t items = p.nt_max * H;
-    const int grid = (int)(items < 2 * (int64_t)num_sms() ? items : 2 * (int64_t)num_sms());
+    const int grid = (int)(units < 2 * (int64_t)num_sms() ? units : 2 * (int64_t)num_sms());
     tc_prep_t_kernel<<<grid, kPrepThreads, kPrepTSmem, s>>>(mq, mk, mv, mrec, pp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
+    const int H = p.H;
+    const int64_t units = p.nt_max * H;
+    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
+    cudaError_t e = launch_prep_t(p, ws, s);
+    if (e != cudaSuccess) return e;
+    CUtensorMap myn;
+    const cuuint64_t dyn[3] = {(cuuint64_t)KD, (cuuint64_t)kYNRows, (cuuint64_t)units};
+    const cuuint64_t syn[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
+    const cuuint32_t byn[3] = {64, (cuuint32_t)kYNRows, 1};
+    if (!make_tensor_map(&myn, ws, 3, dyn, syn, byn, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
 
     ChainTParams cp{};
     cp.cu = p.cu_seqlens;

@@ -11,6 +11,7 @@
 #include <cstring>
 
 #include "gcl_internal.cuh"
+#include "transition.cuh"
 
 namespace gcl {
 
@@ -132,15 +133,17 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Backward workspace: dS' per chunk [nt_max, H, K, V] fp32; without saved states also
-// the recomputed states (same shape) and the forward's own workspace.
+// the recomputed states (same shape) and the forward's own workspace; on the tensor-core
+// path also the transition-form records the state-gradient sweep reads.
 static size_t bwd_ws(const gcl_bwd_args *a) {
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
+    const bool tc = fwd_tc_supported(kGDN, a->dtype, a->K, a->V);
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
-    if (a->h_save) return per;
-    const size_t fw = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
-                          ? align256(fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign : 0;
-    return 2 * per + fw;
+    const size_t rec = tc ? align256(transition_record_bytes(ntm, a->H)) + kWsAlign : 0;
+    if (a->h_save) return per + rec;
+    const size_t fw = tc ? align256(fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign : 0;
+    return 2 * per + fw + rec;
 }
 
 }  // namespace gcl
@@ -246,30 +249,44 @@ gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
     p.dev_status = a->dev_status;
     p.t_max = a->t_max; p.nt_max = ntm; p.n_max = a->n_max;
     p.H = a->H; p.K = a->K; p.V = a->V; p.scale = a->scale;
+    const bool tc = fwd_tc_supported(kGDN, a->dtype, a->K, a->V);
+    FwdParams f{};
+    f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
+    f.cu_seqlens = a->cu_seqlens; f.chunk_indices = a->chunk_indices;
+    f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
+    f.o = nullptr; f.ht = nullptr; f.h_save = nullptr; f.dev_status = a->dev_status;
+    f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
+    f.nt_max = ntm;
+    f.scale = a->scale;
+    const size_t used = a->h_save ? per : 2 * per + (tc ? align256(fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign : 0);
     if (a->h_save) {
         p.h = a->h_save;
     } else {
         float *h = reinterpret_cast<float *>(ws + per);
-        FwdParams f{};
-        f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
-        f.cu_seqlens = a->cu_seqlens; f.chunk_indices = a->chunk_indices;
-        f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
-        f.o = nullptr; f.ht = nullptr; f.h_save = h; f.dev_status = a->dev_status;
+        f.h_save = h;
         f.workspace = nullptr;
         f.workspace_bytes = 0;
         if (fwd_tc_supported(kGDN, a->dtype, a->K, a->V))     // room for the W form only
             align_ws(ws + 2 * per, fwd_tc_workspace_bytes(ntm, a->H) + kWsAlign - 1, &f.workspace,
                      &f.workspace_bytes);
-        f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
-        f.nt_max = ntm;
-        f.scale = a->scale;
-        cudaError_t e = fwd_tc_supported(kGDN, a->dtype, a->K, a->V)
+        cudaError_t e = tc
                             ? launch_fwd_tc(f, kGDN, s)
                             : launch_fwd_simt(f, kGDN, a->dtype, s);
         if ((st = cuda_check(e, "gdn_chunk_bwd (state recompute)")) != GCL_OK) return st;
+        f.h_save = nullptr;
         p.h = h;
     }
-    return cuda_check(launch_bwd_simt(p, a->dtype, s), fn);
+    if (tc) {   // transition-form records, then the state-gradient sweep on the tensor cores
+        void *rec = nullptr;
+        size_t rec_bytes = 0;
+        align_ws(ws + used, a->workspace_bytes - used, &rec, &rec_bytes);
+        if (rec_bytes < transition_record_bytes(ntm, a->H))
+            return fail(GCL_ERR_CAPACITY, "%s: workspace too small for the sweep records", fn);
+        cudaError_t e = launch_prep_t(f, static_cast<uint8_t *>(rec), s);
+        if (e == cudaSuccess) e = launch_bwd_sweep_t(p, static_cast<const uint8_t *>(rec), s);
+        if ((st = cuda_check(e, "gdn_chunk_bwd (state-gradient sweep)")) != GCL_OK) return st;
+    }
+    return cuda_check(launch_bwd_simt(p, a->dtype, tc, s), fn);
 }
 
 }  // extern "C"

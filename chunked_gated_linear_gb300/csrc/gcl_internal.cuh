@@ -73,7 +73,11 @@ bool fwd_tc_prefers_transition(int n_max, int H);
 bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
                      const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw,
                      CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, cudaStream_t s);
+// CUDA-core backward: the state-gradient sweep (unless sweep_done: dh already holds dS'
+// per chunk and dh0 is written) and the chunk gradients.
+cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s);
+// Tensor-core state-gradient sweep from transition-form records (GDN, bf16, K = V = 128).
+cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *records, cudaStream_t s);
 
 // ---- device helpers -------------------------------------------------------
 __device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }

@@ -1,0 +1,59 @@
+// transition.cuh -- the per-chunk record of the transition form, shared by its forward
+// (fwd_tc_transition.cu) and backward (bwd_tc_transition.cu) kernels.
+//
+// For chunk n of a sequence (HA-NPU paper "Empowering Hybrid Attention Models on NPUs",
+// section 2.1, Map-Reduce-Map) the state update and the output are affine in the state
+// entering the chunk:
+//   S' = Gamma_c S + N S + B,      O = Y S + Z,
+//   N = -Ktil^T W,  B = Ktil^T U,  Y = scale diag(Gamma) Q - L W,  Z = L U.
+// The record holds [Y; N | B | Z] as 384 rows of 128 bf16 (Y rows 0..63, N 64..191,
+// B 192..319, Z 320..383; 96 KiB so every record starts on a 1 KiB boundary).  The workspace
+// is nt_max * H records, then (forward only) the bf16 state entering every chunk, then
+// Gamma_c of every record in 16-byte slots.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gcl_internal.cuh"
+
+namespace gcl {
+namespace tr {
+
+constexpr int C = 64;
+constexpr int KD = 128;
+constexpr int VD = 128;
+constexpr size_t kYNRows = 192;                      // [Y; N], bf16, 128 columns
+constexpr size_t kYNBytes = kYNRows * KD * 2;        // 48 KiB
+constexpr size_t kBBytes = (size_t)KD * VD * 2;      // 32 KiB
+constexpr size_t kZBytes = (size_t)C * VD * 2;       // 16 KiB
+constexpr size_t kUnitBytes = kYNBytes + kBBytes + kZBytes;
+constexpr size_t kGBytes = 16;                       // Gamma_c slot
+static_assert(kUnitBytes % 1024 == 0, "records start on 1 KiB boundaries");
+
+// Address of the Gamma_c slot of record `unit` in a workspace of nt_max * H records.
+__host__ __device__ inline size_t gc_offset(int64_t nt_max, int H, int64_t unit) {
+    return (size_t)nt_max * H * kUnitBytes + (size_t)unit * kGBytes;
+}
+
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    uint4 pk;
+    __nv_bfloat162 *pp = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pp[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    return pk;
+}
+
+// Offset of element (k, n) (n < 64) of an MN-major bf16 operand with the 128-byte swizzle:
+// 8-row k-groups of 1024 B, 16-byte chunk index XOR (k % 8).
+__device__ __forceinline__ uint32_t mn_sw128(int k, int n) {
+    return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((n >> 3) ^ (k & 7))) << 4) + (n & 7) * 2);
+}
+
+}  // namespace tr
+
+// Records of every live chunk and head into ws (nt_max * H records + Gamma_c slots).
+cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s);
+size_t transition_record_bytes(int64_t nt_max, int H);
+
+}  // namespace gcl
