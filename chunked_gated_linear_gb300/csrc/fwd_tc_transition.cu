@@ -134,6 +134,9 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __shared__ int s_err;
     __shared__ float sG[C], sB[C], sF[C], sFQ[C], sEG[C], s_carry;
 
+    // the chain kernel may be scheduled on SMs this grid leaves; it reads the records only
+    // after waiting for this grid's completion
+    launch_dependents();
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quarter = warp & 3, half = warp >> 2;
@@ -516,15 +519,17 @@ struct ChainTParams {
 };
 
 // Shared memory: NS stages of {[Y; N] (two 64-column blocks of 192 rows, 128-byte
-// swizzle), B slice [128][VS], Z slice [64][VS], Gamma_c}, then two bf16 copies of the
-// state slice S as MN-major B operands (VS used columns of a 64-element atom).
+// swizzle), B slice [128][VS], Z slice [64][VS], Gamma_c}, then three bf16 copies of the
+// state slice S as MN-major B operands (VS used columns of a 64-element atom): S(n) in
+// buffer n % 3, so the copy of S(n+1) overwrites the one G2 read two chunks earlier.
 template <int VS, int NS>
 struct ChainTLayout {
     static constexpr uint32_t kYN = 49152, kB = VS * 256, kZ = VS * 128, kG = 16;
     static constexpr uint32_t oYN = 0, oB = kYN, oZ = oB + kB, oG = oZ + kZ;
     static constexpr uint32_t kStage = (oG + kG + 1023) / 1024 * 1024;
-    static constexpr uint32_t oSB = NS * kStage;                 // two 16 KiB buffers
-    static constexpr uint32_t total = oSB + 2 * 16384;
+    static constexpr int kSB = 3;                                // bf16 copies of S
+    static constexpr uint32_t oSB = NS * kStage;                 // kSB buffers of 16 KiB
+    static constexpr uint32_t total = oSB + kSB * 16384;
     static constexpr uint32_t bytes = total + 1024;              // + alignment slack
     static constexpr uint32_t kTmaBytes = kYN + kB + kZ + kG;
 };
@@ -537,13 +542,11 @@ constexpr int kWarpG2 = kWarpG1 + kG1Parts;
 constexpr int kWarpTma = kWarpG2 + 1;
 constexpr int kChainThreads = 32 * (kWarpTma + 1);
 
-__device__ __forceinline__ void compute_barrier() {   // named barrier over warps 0..7
-    asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
-}
 
 // Per-(sequence, head, column slice) recurrence, warp-specialised:
 //   warps 0..7   the state: thread t owns key row 32 (w & 3) + (t & 31) of the state slice and
-//                the column half (w >> 2); S(n+1) = Gamma_c S(n) + B + D1 -> Sb[(n+1) & 1];
+//                the column half (w >> 2); S(n+1) = Gamma_c S(n) + B + D1 -> Sb[(n+1) % 3];
+//                each warp hands its part over with its own mbarrier arrival;
 //   warps 8, 9   the output: token rows 32 (w - 8) + (t & 31); O(n) = D2 + Z;
 //   warps 10, 11 (one lane each) G1(n) = N S(n), split over the key dimension into two
 //                accumulators (the serial step: it alone sits between S(n) and S(n+1));
@@ -565,7 +568,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb1, bar_sb2[2], bar_g1[kG1Parts], bar_g2[2],
+    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb1, bar_sb2[2], bar_g1[kG1Parts], bar_g2[3],
         bar_d2free[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
@@ -602,12 +605,12 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             mbar_init(&bar_tma[i], 1);
             mbar_init(&bar_free[i], kComputeThreads / 32 + kOutWarps);
         }
-        mbar_init(&bar_sb1, 1);
+        mbar_init(&bar_sb1, kComputeThreads / 32);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_sb2[i], 1);
-            mbar_init(&bar_g2[i], 1);
+            mbar_init(&bar_sb2[i], kComputeThreads / 32);
             mbar_init(&bar_d2free[i], kOutWarps);
         }
+        for (int i = 0; i < 3; ++i) mbar_init(&bar_g2[i], 1);
         for (int i = 0; i < kG1Parts; ++i) mbar_init(&bar_g1[i], 1);
         s_err = 0;
         fence_barrier_init();
@@ -622,7 +625,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     const uint32_t tmem = s_tmem;
     constexpr uint32_t idm = idesc_bf16(128, VS, 0, 1);
     auto dS = [&](int ic) {                          // S(ic) as the MN-major B operand
-        return smem_desc(sbase + Lay::oSB + (ic & 1) * 16384, 8192, 1024, kSwizzle128B);
+        return smem_desc(sbase + Lay::oSB + (ic % Lay::kSB) * 16384, 8192, 1024, kSwizzle128B);
     };
     auto dYN = [&](int st) {                         // [Y; N] of a stage, K-major
         return smem_desc(sbase + st * Lay::kStage + Lay::oYN, 16, 1024, kSwizzle128B);
@@ -662,7 +665,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 for (int s = 0; s < 8; ++s)
                     mma_bf16(tmem + tD2 + (ic & 1) * VS, a + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
                              b + s * 128, idm, s > 0);
-                mma_commit(&bar_g2[ic & 1]);
+                mma_commit(&bar_g2[ic % 3]);
             }
         }
     } else if (warp == kWarpTma) {
@@ -680,6 +683,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 tma_load_3d(b + Lay::oZ, &tm_z, v0, 0, unit, bar);
                 bulk_load(b + Lay::oG, p.ws + gc_offset(p.nt_max, H, unit), kGBytes, bar);
             };
+            grid_dependency_wait();      // the records are complete (launched as a dependent)
             for (int ic = 0; ic < nch; ++ic) {
                 if (ic >= NS && !mbar_wait(&bar_free[ic % NS], ((ic - NS) / NS) & 1, &s_err, 11)) break;
                 issue_tma(ic);
@@ -696,7 +700,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             const int64_t t0 = bos + (int64_t)ic * C;
             const uint8_t *stage = smem + st * Lay::kStage;
             mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 5);
-            mbar_wait(&bar_g2[ic & 1], (ic >> 1) & 1, &s_err, 6);
+            mbar_wait(&bar_g2[ic % 3], (ic / 3) & 1, &s_err, 6);
             tc_fence_after();
             float d2[VS];
 #pragma unroll
@@ -734,11 +738,11 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 *reinterpret_cast<uint4 *>(smem + Lay::oSB + buf * 16384 + mn_sw128(row, c0 + j)) =
                     pack8(x + j);
         };
-        auto handoff = [&](int ic) {                      // S(ic) is in Sb[ic & 1]
+        auto handoff = [&](int ic) {                      // this warp's part of S(ic) is in its buffer
             fence_async_smem();
             tc_fence_before();
-            compute_barrier();
-            if (tid == 0) {
+            __syncwarp();
+            if (lane == 0) {
                 mbar_arrive(&bar_sb1);
                 mbar_arrive(&bar_sb2[ic & 1]);
             }
@@ -793,9 +797,9 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                     for (int part = 0; part < kG1Parts; ++part) S[j] += d1[part][j];
                 }
             }
-            // Sb[(ic + 1) & 1] was last read by G2(ic - 1)
-            if (ic >= 1) mbar_wait(&bar_g2[(ic - 1) & 1], ((ic - 1) >> 1) & 1, &s_err, 13);
-            st_sb((ic + 1) & 1, S);
+            // Sb[(ic + 1) % 3] was last read by G1 and G2 of chunk ic - 2 (long complete)
+            if (ic >= 2) mbar_wait(&bar_g2[(ic - 2) % 3], ((ic - 2) / 3) & 1, &s_err, 13);
+            st_sb((ic + 1) % Lay::kSB, S);
             handoff(ic + 1);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_free[st]);        // done with B of stage st
@@ -832,7 +836,19 @@ cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const Chai
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(n_split, H, n_max), kChainThreads, Lay::bytes, s>>>(myn, mb, mz, cp);
+    // launched as a programmatic dependent of the prep: its prologue overlaps the prep's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_split, H, n_max);
+    cfg.blockDim = dim3(kChainThreads);
+    cfg.dynamicSmemBytes = Lay::bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, myn, mb, mz, cp);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -910,7 +926,7 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     cp.n_max = p.n_max;
     cp.H = H;
     if (split == 8) return launch_chain_t<16, 3>(myn, ws, cp, split, H, p.n_max, s);
-    if (split == 4) return launch_chain_t<32, 3>(myn, ws, cp, split, H, p.n_max, s);
+    if (split == 4) return launch_chain_t<32, 2>(myn, ws, cp, split, H, p.n_max, s);
     return cudaErrorInvalidValue;                   // the plan is only taken at splits 4 and 8
 }
 

@@ -47,10 +47,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  On timeout sets
-// *err (if it is still 0) to `code` and returns false.
+// *err (if it is still 0) to `code` and returns false.  A completed phase is seen by the
+// non-blocking probe; otherwise the thread suspends in try_wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -130,6 +144,18 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA).
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- dependent launches
+// Programmatic dependent launch: the next kernel on the stream may start (its CTAs run
+// their prologue) once every CTA of this grid has called launch_dependents or exited;
+// grid_dependency_wait blocks until the previous grid has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMEM
