@@ -52,6 +52,7 @@ chunk_meta_kernel(const int32_t *__restrict__ cu, int32_t n_max, int64_t t_max, 
     __shared__ int s_warp[32];
     __shared__ int s_total;
     __shared__ int s_carry;
+    launch_dependents();          // the forward's first kernel waits for this grid's completion
     if (threadIdx.x == 0) {
         s_flags = 0;
         s_carry = 0;

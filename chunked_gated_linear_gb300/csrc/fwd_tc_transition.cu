@@ -134,6 +134,9 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __shared__ int s_err;
     __shared__ float sG[C], sB[C], sF[C], sFQ[C], sEG[C], s_carry;
 
+    // launched as a dependent of the metadata (or any earlier) kernel: nothing written by
+    // earlier kernels is read before this wait
+    grid_dependency_wait();
     // the chain kernel may be scheduled on SMs this grid leaves; it reads the records only
     // after waiting for this grid's completion
     launch_dependents();
@@ -837,19 +840,8 @@ cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const Chai
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
     // launched as a programmatic dependent of the prep: its prologue overlaps the prep's tail
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_split, H, n_max);
-    cfg.blockDim = dim3(kChainThreads);
-    cfg.dynamicSmemBytes = Lay::bytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, myn, mb, mz, cp);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(n_split, H, n_max), dim3(kChainThreads), Lay::bytes, s, myn, mb,
+                            mz, cp);
 }
 
 }  // namespace
@@ -895,8 +887,8 @@ cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
                                          kPrepTSmem);
     if (e != cudaSuccess) return e;
     const int grid = (int)(units < 2 * (int64_t)num_sms() ? units : 2 * (int64_t)num_sms());
-    tc_prep_t_kernel<<<grid, kPrepThreads, kPrepTSmem, s>>>(mq, mk, mv, mrec, pp);
-    return cudaGetLastError();
+    return launch_dependent(tc_prep_t_kernel, dim3(grid), dim3(kPrepThreads), kPrepTSmem, s, mq, mk, mv,
+                            mrec, pp);
 }
 
 cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "gcl.h"
 
 namespace gcl {
@@ -87,6 +89,37 @@ __device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) {
 __device__ __forceinline__ void st_out(float *p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, int64_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
+}
+
+// Programmatic dependent launch: the next kernel on the stream, if launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization, may start once every CTA of this grid
+// has called launch_dependents or exited; grid_dependency_wait blocks until the previous
+// grid on the stream has completed and its memory operations are visible (a no-op for a
+// kernel launched without the attribute).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launches kern<<<grid, block, smem, s>>>(args...) as a programmatic dependent of the
+// previous kernel on the stream.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Reads the device status word (if any); true means "do no work".

@@ -146,18 +146,6 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- dependent launches
-// Programmatic dependent launch: the next kernel on the stream may start (its CTAs run
-// their prologue) once every CTA of this grid has called launch_dependents or exited;
-// grid_dependency_wait blocks until the previous grid has completed and its memory
-// operations are visible.
-__device__ __forceinline__ void launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- TMEM
 // Allocation: one full warp; the base address is written to *dst (shared memory).
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
