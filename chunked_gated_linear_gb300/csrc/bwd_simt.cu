@@ -160,7 +160,9 @@ struct GradLayout {
     static constexpr int oRA = oG + C, oRB = oRA + C, oRC = oRB + C, oRD = oRC + C;
     static constexpr int oDG = oRD + C;                // dgamma per row
     static constexpr int oRED = oDG + C;               // 32 floats for a block reduction
-    static constexpr int oFree = oRED + 32;            // slice region
+    static constexpr int oEG = oRED + 32;              // exp(gamma) per row
+    static constexpr int oFR = oEG + C;                // exp(gamma_c - gamma) per row
+    static constexpr int oFree = oFR + C;              // slice region
     // slice buffers
     static constexpr int oS = oFree, oDS = oS + K * LV;
     static constexpr int oV = oDS + K * LV, oDO = oV + C * LV, oKS = oDO + C * LV;
@@ -182,6 +184,7 @@ chunk_grad_kernel(BwdParams p) {
     float *sDL = sm + Lay::oDL, *sDT = sm + Lay::oDT, *sB = sm + Lay::oB, *sG = sm + Lay::oG;
     float *sRA = sm + Lay::oRA, *sRB = sm + Lay::oRB, *sRC = sm + Lay::oRC, *sRD = sm + Lay::oRD;
     float *sDG = sm + Lay::oDG, *sRed = sm + Lay::oRED;
+    float *sEG = sm + Lay::oEG, *sFR = sm + Lay::oFR;
     float *sS = sm + Lay::oS, *sDS = sm + Lay::oDS, *sV = sm + Lay::oV, *sDO = sm + Lay::oDO;
     float *sKS = sm + Lay::oKS, *sR = sm + Lay::oR, *sE = sm + Lay::oE, *sDE = sm + Lay::oDE;
     float *sDVB = sm + Lay::oDVB, *sX1 = sm + Lay::oX1, *sX2 = sm + Lay::oX2;
@@ -231,6 +234,12 @@ chunk_grad_kernel(BwdParams p) {
     simt_solve<kGradThreads>(sA, sT);
 
     const float gC = sG[C - 1];
+    // per-row exponentials, once (the loops below only multiply)
+    for (int r = tid; r < C; r += kGradThreads) {
+        sEG[r] = expf(sG[r]);
+        sFR[r] = expf(gC - sG[r]);
+    }
+    __syncthreads();
     const int my_r = tid / 8, my_c0 = tid % 8;    // owner of dq/dk partials
     float dq_p[CPT], dk_p[CPT];
 #pragma unroll
@@ -263,7 +272,7 @@ chunk_grad_kernel(BwdParams p) {
                 kd = fmaf(sK[r * LK + c], sDS[c * LV + j], kd);
             }
             sKS[r * LV + j] = ks;
-            sR[r * LV + j] = sB[r] * (sV[r * LV + j] - expf(sG[r]) * ks);
+            sR[r * LV + j] = sB[r] * (sV[r * LV + j] - sEG[r] * ks);
             sX1[r * LV + j] = sDO[r * LV + j] * qs;
             sX2[r * LV + j] = kd;
         }
@@ -271,7 +280,7 @@ chunk_grad_kernel(BwdParams p) {
         // E = T R;  dE = L^T dO + exp(gamma_c - gamma) X2
         for (int e = tid; e < C * kVS; e += kGradThreads) {
             const int r = e / kVS, j = e % kVS;
-            float ev = 0.f, de = expf(gC - sG[r]) * sX2[r * LV + j];
+            float ev = 0.f, de = sFR[r] * sX2[r * LV + j];
             for (int i = 0; i <= r; ++i) ev = fmaf(sT[r * kLC + i], sR[i * LV + j], ev);
             for (int r2 = r; r2 < C; ++r2) de = fmaf(sL[r2 * kLC + r], sDO[r2 * LV + j], de);
             sE[r * LV + j] = ev;
@@ -302,8 +311,8 @@ chunk_grad_kernel(BwdParams p) {
         __syncthreads();
         // register partials: dq_p += dO S^T;  dk_p += e^{g_c-g} E dS'^T - beta Gamma dVb S^T
         {
-            const float fe = expf(gC - sG[my_r]);
-            const float fb = sB[my_r] * expf(sG[my_r]);
+            const float fe = sFR[my_r];
+            const float fb = sB[my_r] * sEG[my_r];
 #pragma unroll
             for (int m = 0; m < CPT; ++m) {
                 const int c = my_c0 + 8 * m;
@@ -386,24 +395,30 @@ chunk_grad_kernel(BwdParams p) {
             if (r < len) p.dg[(t0 + r) * H + h] = acc;
         }
     }
-    // dq, dk
+    // P = scale e^{g_r - g_i} dL (i <= r) and M = dA beta_r e^{g_r - g_i} (i < r), in place of
+    // dL and dA (the gate gradient above has read them), zero elsewhere
+    __syncthreads();
+    for (int e = tid; e < C * C; e += kGradThreads) {
+        const int r = e / C, i = e % C;
+        const float dec = i <= r ? expf(sG[r] - sG[i]) : 0.f;
+        sDL[r * kLC + i] = i <= r ? p.scale * dec * sDL[r * kLC + i] : 0.f;
+        sDT[r * kLC + i] = i < r ? sDT[r * kLC + i] * sB[r] * dec : 0.f;
+    }
+    __syncthreads();
+    // dq = scale Gamma dO S^T + P K;  dk = partials + P^T Q + M K + M^T K
     {
+        const float *sP = sDL, *sM = sDT;
         const int r = my_r;
         if (r < len) {
-            const float gr = sG[r];
 #pragma unroll
             for (int m = 0; m < CPT; ++m) {
                 const int c = my_c0 + 8 * m;
-                float aq = p.scale * expf(gr) * dq_p[m];
-                for (int i = 0; i <= r; ++i)
-                    aq = fmaf(p.scale * expf(gr - sG[i]) * sDL[r * kLC + i], sK[i * LK + c], aq);
+                float aq = p.scale * sEG[r] * dq_p[m];
+                for (int i = 0; i <= r; ++i) aq = fmaf(sP[r * kLC + i], sK[i * LK + c], aq);
                 float ak = dk_p[m];
-                for (int r2 = r; r2 < C; ++r2)
-                    ak = fmaf(p.scale * expf(sG[r2] - gr) * sDL[r2 * kLC + r], sQ[r2 * LK + c], ak);
-                for (int i = 0; i < r; ++i)
-                    ak = fmaf(sDA[r * kLC + i] * sB[r] * expf(gr - sG[i]), sK[i * LK + c], ak);
-                for (int r2 = r + 1; r2 < C; ++r2)
-                    ak = fmaf(sDA[r2 * kLC + r] * sB[r2] * expf(sG[r2] - gr), sK[r2 * LK + c], ak);
+                for (int r2 = r; r2 < C; ++r2) ak = fmaf(sP[r2 * kLC + r], sQ[r2 * LK + c], ak);
+                for (int i = 0; i < r; ++i) ak = fmaf(sM[r * kLC + i], sK[i * LK + c], ak);
+                for (int r2 = r + 1; r2 < C; ++r2) ak = fmaf(sM[r2 * kLC + r], sK[r2 * LK + c], ak);
                 p.dq[((t0 + r) * H + h) * (int64_t)K + c] = aq;
                 p.dk[((t0 + r) * H + h) * (int64_t)K + c] = ak;
             }
