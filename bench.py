@@ -246,9 +246,10 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
 def launches_per_step(w) -> int:
     """Library kernels per step: chunk_meta_build, the forward (prep and chain on the tensor
     cores for GDN bf16 d_k = d_v = 128, one fused CUDA-core kernel otherwise) and the
-    backward's sweep and chunk-gradient kernels."""
+    backward (on the tensor cores: transition records, state-gradient sweep and two
+    chunk-gradient kernels; otherwise the sweep and one chunk-gradient kernel)."""
     tc = w.variant == synth.GDN and w.dtype == "bf16" and w.K == 128 and w.V == 128
-    return 1 + (2 if tc else 1) + (2 if w.backward else 0)
+    return 1 + (2 if tc else 1) + ((4 if tc else 2) if w.backward else 0)
 
 
 def run_gpu(args, rank, world, dist):

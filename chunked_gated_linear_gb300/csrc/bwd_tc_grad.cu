@@ -1,0 +1,812 @@
+// bwd_tc_grad.cu -- chunk gradients of the GDN backward on the tensor cores (bf16 inputs,
+// d_k = d_v = 128, chunk 64): dq, dk, dv, dbeta, dg from the state entering every chunk S
+// and the gradient of the state after it dS' (the sweep's output).
+//
+// FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths on Ascend
+// NPUs", section "Step 3": recomputation, WY, gate and gradient kernels.  With
+// R = diag(beta)(V - diag(Gamma) K S), E = T R, dE = L^T dO + Ktil dS':
+//   dv  = diag(beta) T^T dE,               dT = dE R^T (lower),   dL = dO E^T (lower),
+//   dq  = scale diag(Gamma) dO S^T + P K,   P = scale D o dL,
+//   dk  = diag(e^{g_c - g}) E dS'^T - diag(beta Gamma) (T^T dE) S^T + P^T Q + M K + M^T K,
+//   M   = beta_r D o dA,   dA = -T^T dT T^T (strictly lower),   D[r][i] = e^{g_r - g_i},
+// and the gate and beta gradients from row sums.  Two launches per chunk and head:
+//   grad1  (tensor cores) the recompute (K K^T, Q K^T, the triangular solve) and five MMA
+//          rounds: [K; Q][S | dS'], [T; L] R and L^T dO, then T^T dE, [E; dO][S | dS']^T,
+//          [E; dO] E^T, [dE; E] R^T, then (T^T dE) S^T.  It writes dv, the partial dq and dk,
+//          and T, D o K K^T, L, dL, dT and four row sums per chunk to a scratch record;
+//   grad2  dA on the CUDA cores (fp32), the gate and beta gradients, and one MMA round
+//          [M; P] K, M^T K + P^T Q that completes dq and dk.
+#include <cudaTypedefs.h>
+
+#include "gcl_internal.cuh"
+#include "tc_ptx.cuh"
+#include "tc_solve.cuh"
+#include "transition.cuh"
+
+namespace gcl {
+namespace {
+
+using namespace tc;
+using namespace tr;
+
+// scratch record per chunk and head (fp32): T, A' = D o K K^T (strict), L, dL, dT [64][64],
+// then rows: RA = sum_v dO o QS, RB = sum_v dVb o V, RC = sum_c (dVb S^T) o K,
+// RD = sum_v E o K dS', and <dS', S> in the first entry of row 4.
+constexpr int kScrT = 0, kScrAp = 4096, kScrL = 8192, kScrDL = 12288, kScrDT = 16384;
+constexpr int kScrRows = 20480;
+constexpr int kScrFloats = kScrRows + 8 * 64;
+
+struct GradParams {
+    const int32_t *chunk_indices, *cu;
+    const float *g;
+    const __nv_bfloat16 *beta, *v;
+    const float *h, *dh;
+    float *dq, *dk, *dv, *dg, *dbeta;
+    float *scratch;
+    int32_t *status;
+    int64_t t_max, nt_max;
+    int32_t n_max, H;
+    float scale;
+};
+
+constexpr int kThreads = 256;
+
+// metadata of row j of chunk_indices; false for sentinels and invalid rows (reported)
+__device__ __forceinline__ bool chunk_of_row(const GradParams &p, int j, int64_t &t0, int &len) {
+    const int n = p.chunk_indices[2 * j];
+    if (n < 0) return false;
+    const int ic = p.chunk_indices[2 * j + 1];
+    if (n >= p.n_max || ic < 0) {
+        if (threadIdx.x == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return false;
+    }
+    const int64_t bos = p.cu[n], eos = p.cu[n + 1];
+    t0 = bos + (int64_t)ic * C;
+    if (bos < 0 || eos < bos || eos > p.t_max || t0 >= eos) {
+        if (threadIdx.x == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return false;
+    }
+    len = (int)(eos - t0 < C ? eos - t0 : C);
+    return true;
+}
+
+// gamma (inclusive cumsum of g over the chunk) and beta, for rows 0..63; all threads call it
+__device__ __forceinline__ void chunk_gates(const GradParams &p, int64_t t0, int len, int h, float *sG,
+                                            float *sB, float *s_carry) {
+    const int tid = threadIdx.x;
+    const float gv = (tid < len) ? p.g[(t0 + tid) * p.H + h] : 0.f;
+    float x = tid < C ? warp_scan(gv) : 0.f;
+    if (tid == 31) *s_carry = x;
+    __syncthreads();
+    if (tid >= 32 && tid < C) x += *s_carry;
+    if (tid < C) {
+        sG[tid] = x;
+        sB[tid] = tid < len ? __bfloat162float(p.beta[(t0 + tid) * p.H + h]) : 0.f;
+    }
+    __syncthreads();
+}
+
+// ============================================================================ grad1
+// shared memory (offsets from the 1024-aligned base)
+constexpr uint32_t gKQ = 0;          // [K; Q]: 2 column blocks x 128 rows          32 KiB
+constexpr uint32_t gV = 32768;       // V, then R: 2 blocks x 64 rows                16 KiB
+constexpr uint32_t gS = 49152;       // S bf16: 2 blocks x 128 rows (key x value)    32 KiB
+constexpr uint32_t gDS = 81920;      // dS' bf16                                     32 KiB
+constexpr uint32_t gT3 = 114688;     // [dE; E; dO]: 2 blocks x 192 rows             48 KiB
+constexpr uint32_t gTL = 163840;     // [T; L]: 128 rows x 64 columns, then dVb      16 KiB
+constexpr uint32_t gF = 180224;      // fp32 A (-> dL), T (-> dT), solve scratch
+constexpr uint32_t g1End = gF + kSolveFloats * 4;
+constexpr int kGrad1Smem = g1End + 1024;
+static_assert(kGrad1Smem <= 232448, "grad1 shared memory");
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                GradParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    float *sA = reinterpret_cast<float *>(smem + gF);
+    float *sT = sA + C * kSolveLD;
+    float *sX = sT + C * kSolveLD;
+    float *sDL = sA, *sDT = sT;                 // after the solve
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+    __shared__ float sG[C], sB[C], sEG[C], sFR[C], sRow[4][C], sRed[kThreads / 32], s_carry;
+
+    if (status_blocks(p.status)) return;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int lrow = quarter * 32 + (tid & 31);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int j = blockIdx.x, h = blockIdx.y, H = p.H;
+    int64_t t0;
+    int len;
+    if (!chunk_of_row(p, j, t0, len)) return;
+    const int unit = j * H + h;
+    const uint32_t sbase = smem_u32(smem);
+    const int64_t KV = (int64_t)KD * VD;
+    float *scr = p.scratch + (size_t)unit * kScrFloats;
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        s_err = 0;
+        fence_barrier_init();
+        mbar_arrive_expect_tx(&bar_tma, 65536);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(smem + gKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
+            tma_load_3d(smem + gKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
+            tma_load_3d(smem + gV + cb * 8192, &tm_v, cb * 64, h, (int)t0, &bar_tma);
+            tma_load_3d(smem + gT3 + cb * 24576 + 16384, &tm_do, cb * 64, h, (int)t0, &bar_tma);
+        }
+    }
+    __syncwarp();
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    for (int e = tid; e < 4 * C; e += kThreads) (&sRow[0][0])[e] = 0.f;
+    chunk_gates(p, t0, len, h, sG, sB, &s_carry);
+    const float gC = sG[C - 1];
+    if (tid < C) {
+        sEG[tid] = __expf(sG[tid]);
+        sFR[tid] = tid < len ? __expf(gC - sG[tid]) : 0.f;
+    }
+    // decay table D[r][c] = exp(g_r - g_c) for c <= r (1 above the diagonal) in the T buffer
+    for (int e = tid; e < C * C / 4; e += kThreads) {
+        const int r = e >> 4, c = (e & 15) * 4;
+        const float gr = sG[r];
+        *reinterpret_cast<float4 *>(sT + r * kSolveLD + c) =
+            make_float4(__expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
+                        __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
+    }
+    // S and dS' (fp32) -> bf16 operand tiles; <dS', S>
+    float dgc = 0.f;
+    {
+        const float *Sg = p.h + (int64_t)unit * KV, *dSg = p.dh + (int64_t)unit * KV;
+        for (int e = tid; e < KD * VD / 8; e += kThreads) {
+            const int key = e >> 4, c0 = (e & 15) * 8;
+            const float4 a0 = *reinterpret_cast<const float4 *>(Sg + key * VD + c0);
+            const float4 a1 = *reinterpret_cast<const float4 *>(Sg + key * VD + c0 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(dSg + key * VD + c0);
+            const float4 b1 = *reinterpret_cast<const float4 *>(dSg + key * VD + c0 + 4);
+            const float sv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float dv8[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) dgc = fmaf(sv[q], dv8[q], dgc);
+            *reinterpret_cast<uint4 *>(smem + gS + kmaj16(128, key, c0)) = pack8(sv);
+            *reinterpret_cast<uint4 *>(smem + gDS + kmaj16(128, key, c0)) = pack8(dv8);
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) dgc += __shfl_xor_sync(0xffffffffu, dgc, d);
+        if ((tid & 31) == 0) sRed[warp] = dgc;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    uint32_t phase = 0;
+    auto mma_done = [&](int code) -> bool {
+        const bool ok = mbar_wait(&bar_mma, phase, &s_err, code);
+        phase ^= 1;
+        tc_fence_after();
+        return !__syncthreads_or(!ok);
+    };
+    auto to_async = [&]() {
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+    // 16-byte chunk of a K-major tile with `rows` rows per block of 64 columns
+    auto kchunk = [&](uint32_t base, int rows, int r, int c) {
+        return reinterpret_cast<uint4 *>(smem + base + kmaj16(rows, r, c));
+    };
+    auto ld64 = [&](uint32_t col, float *x) {        // 64 columns of this thread's TMEM lane
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + col + q * 16, x + q * 16);
+        tmem_ld_wait();
+    };
+    auto unpack8 = [](uint4 w, float *x) {
+        const __nv_bfloat162 *pp = reinterpret_cast<const __nv_bfloat162 *>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(pp[e]);
+            x[2 * e] = f.x;
+            x[2 * e + 1] = f.y;
+        }
+    };
+    do {
+        const bool landed = mbar_wait(&bar_tma, 0, &s_err, 1);
+        if (__syncthreads_or(!landed)) break;
+        if (len < C) {   // rows past the end: zero K, Q, V and dO (NaN padding enters MMAs raw)
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            for (int t = tid; t < 8 * C * 8; t += kThreads) {
+                const int r = (t >> 3) & 63, blk = t >> 9;     // K0 K1 Q0 Q1 V0 V1 dO0 dO1
+                if (r >= len) {
+                    uint32_t base;
+                    if (blk < 4) base = gKQ + (blk & 1) * 16384 + (blk >> 1) * 8192;
+                    else if (blk < 6) base = gV + (blk - 4) * 8192;
+                    else base = gT3 + (blk - 6) * 24576 + 16384;
+                    *reinterpret_cast<uint4 *>(smem + base + r * 128 + (t & 7) * 16) = zero;
+                }
+            }
+        }
+        to_async();
+        // ---- MMA1: [K; Q] K^T
+        if (tid == 0) {
+            const uint64_t d = smem_desc(sbase + gKQ, 16, 1024, kSwizzle128B);
+            constexpr uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t o = (s >> 2) * 1024 + (s & 3) * 2;
+                mma_bf16(tmem, d + o, d + o, id, s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(2)) break;
+        {   // lanes 0..63: A' = D o K K^T (strict) -> A = beta A' for the solve, A' -> scratch;
+            // lanes 64..127: L = scale D o Q K^T (lower) -> [T; L] rows 64.., L -> scratch
+            float v[32];
+            tmem_ld16(tmem + lane_off + half * 32, v);
+            tmem_ld16(tmem + lane_off + half * 32 + 16, v + 16);
+            tmem_ld_wait();
+            const int r = lrow & 63;
+            float dec[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(sT + r * kSolveLD + half * 32 + i);
+                dec[i] = d4.x; dec[i + 1] = d4.y; dec[i + 2] = d4.z; dec[i + 3] = d4.w;
+            }
+            if (lrow < C) {
+                const float br = sB[r];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    float ap[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = half * 32 + i + e;
+                        ap[e] = (col < r && r < len) ? dec[i + e] * v[i + e] : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(sA + r * kSolveLD + half * 32 + i) =
+                        make_float4(br * ap[0], br * ap[1], br * ap[2], br * ap[3]);
+                    *reinterpret_cast<float4 *>(scr + kScrAp + r * C + half * 32 + i) =
+                        make_float4(ap[0], ap[1], ap[2], ap[3]);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float l[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int col = half * 32 + q * 8 + e;
+                        l[e] = (col <= r && r < len) ? p.scale * dec[q * 8 + e] * v[q * 8 + e] : 0.f;
+                    }
+                    *kchunk(gTL, 128, C + r, half * 32 + q * 8) = pack8(l);
+                    *reinterpret_cast<float4 *>(scr + kScrL + r * C + half * 32 + q * 8) =
+                        make_float4(l[0], l[1], l[2], l[3]);
+                    *reinterpret_cast<float4 *>(scr + kScrL + r * C + half * 32 + q * 8 + 4) =
+                        make_float4(l[4], l[5], l[6], l[7]);
+                }
+            }
+        }
+        __syncthreads();
+        solve_unit_lower64<kThreads>(sA, sT, sX);   // T = (I + A)^-1
+        {   // T (lower, zero above) -> bf16 rows 0..63 of [T; L] and the scratch record
+            const int r = tid >> 2;
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+                const int c0 = ((tid & 3) * 2 + qq) * 8;
+                float t8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t8[e] = c0 + e <= r ? sT[r * kSolveLD + c0 + e] : 0.f;
+                *kchunk(gTL, 128, r, c0) = pack8(t8);
+                *reinterpret_cast<float4 *>(scr + kScrT + r * C + c0) = make_float4(t8[0], t8[1], t8[2], t8[3]);
+                *reinterpret_cast<float4 *>(scr + kScrT + r * C + c0 + 4) = make_float4(t8[4], t8[5], t8[6], t8[7]);
+            }
+        }
+        to_async();
+        // ---- R2: [K; Q] S -> cols 0..127, [K; Q] dS' -> cols 128..255 (S, dS' as MN-major B)
+        if (tid == 0) {
+            const uint64_t a = smem_desc(sbase + gKQ, 16, 1024, kSwizzle128B);
+            const uint64_t bs = smem_desc(sbase + gS, 16384, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(sbase + gDS, 16384, 1024, kSwizzle128B);
+            constexpr uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t o = (s >> 2) * 1024 + (s & 3) * 2;
+                mma_bf16(tmem, a + o, bs + s * 128, id, s > 0);
+            }
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t o = (s >> 2) * 1024 + (s & 3) * 2;
+                mma_bf16(tmem + 128, a + o, bd + s * 128, id, s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(3)) break;
+        {
+            float x[64];
+            ld64(half * 64, x);                      // K S (lanes 0..63) or Q S (lanes 64..127)
+            if (lrow < C) {                          // R = beta (V - Gamma K S), in place of V
+                const int r = lrow;
+                const float br = sB[r], gr = sEG[r];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c = half * 64 + q * 8;
+                    float vv[8], rr[8];
+                    unpack8(*kchunk(gV, 64, r, c), vv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) rr[e] = br * (vv[e] - gr * x[q * 8 + e]);
+                    *kchunk(gV, 64, r, c) = pack8(rr);
+                }
+            } else {                                  // RA = sum_v dO o Q S
+                const int r = lrow - C;
+                float ra = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float dd[8];
+                    unpack8(*kchunk(gT3, 192, 128 + r, half * 64 + q * 8), dd);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ra = fmaf(dd[e], x[q * 8 + e], ra);
+                }
+                atomicAdd(&sRow[0][r], ra);
+            }
+        }
+        to_async();
+        // ---- R3: [T; L] R -> cols 256..383 (E in lanes 0..63); L^T dO -> cols 384..511
+        if (tid == 0) {
+            const uint64_t a = smem_desc(sbase + gTL, 16, 1024, kSwizzle128B);
+            const uint64_t br = smem_desc(sbase + gV, 8192, 1024, kSwizzle128B);
+            const uint64_t al = smem_desc(sbase + gTL + 8192, 8192, 1024, kSwizzle128B);   // L^T
+            const uint64_t bo = smem_desc(sbase + gT3 + 16384, 24576, 1024, kSwizzle128B);  // dO
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + 256, a + s * 2, br + s * 128, idesc_bf16(128, 128, 0, 1), s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + 384, al + s * 128, bo + s * 128, idesc_bf16(128, 128, 1, 1), s > 0);
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(4)) break;
+        if (lrow < C) {   // dE = Ktil dS' + L^T dO -> [dE; ..] rows 0..63, E -> rows 64..127; RD
+            const int r = lrow;
+            const float fr = sFR[r];
+            float e64[64], x[64];
+            ld64(256 + half * 64, e64);
+            ld64(128 + half * 64, x);                // K dS'
+            float rd = 0.f;
+#pragma unroll
+            for (int q = 0; q < 64; ++q) rd = fmaf(e64[q], x[q], rd);
+            atomicAdd(&sRow[3][r], rd);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *kchunk(gT3, 192, C + r, half * 64 + q * 8) = pack8(e64 + q * 8);
+            ld64(384 + half * 64, e64);               // L^T dO
+#pragma unroll
+            for (int q = 0; q < 64; ++q) x[q] = fmaf(fr, x[q], e64[q]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *kchunk(gT3, 192, r, half * 64 + q * 8) = pack8(x + q * 8);
+        }
+        to_async();
+        // ---- R4: dVb = T^T dE -> cols 0..127; [E; dO] S^T -> 128..255 (dO S^T in lanes 64..);
+        // [E; dO] dS'^T -> 256..383 (E dS'^T in lanes 0..63); [E; dO] E^T -> 384..447 (dO E^T in
+        // lanes 64..); [dE; E] R^T -> 448..511 (dE R^T in lanes 0..63)
+        if (tid == 0) {
+            const uint64_t at = smem_desc(sbase + gTL, 8192, 1024, kSwizzle128B);          // T^T
+            const uint64_t bde = smem_desc(sbase + gT3, 24576, 1024, kSwizzle128B);        // dE
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem, at + s * 128, bde + s * 128, idesc_bf16(128, 128, 1, 1), s > 0);
+            const uint64_t aeo = smem_desc(sbase + gT3 + 8192, 16, 1024, kSwizzle128B);    // [E; dO]
+            const uint64_t ade = smem_desc(sbase + gT3, 16, 1024, kSwizzle128B);           // [dE; E]
+            const uint64_t bs = smem_desc(sbase + gS, 16, 1024, kSwizzle128B);             // S^T
+            const uint64_t bd = smem_desc(sbase + gDS, 16, 1024, kSwizzle128B);            // dS'^T
+            const uint64_t be = smem_desc(sbase + gT3 + 8192, 16, 1024, kSwizzle128B);     // E^T
+            const uint64_t brr = smem_desc(sbase + gV, 16, 1024, kSwizzle128B);            // R^T
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t oa = (s >> 2) * (24576 >> 4) + (s & 3) * 2;
+                const uint64_t os = (s >> 2) * (16384 >> 4) + (s & 3) * 2;
+                const uint64_t orr = (s >> 2) * (8192 >> 4) + (s & 3) * 2;
+                mma_bf16(tmem + 128, aeo + oa, bs + os, idesc_bf16(128, 128), s > 0);
+                mma_bf16(tmem + 256, aeo + oa, bd + os, idesc_bf16(128, 128), s > 0);
+                mma_bf16(tmem + 384, aeo + oa, be + oa, idesc_bf16(128, 64), s > 0);
+                mma_bf16(tmem + 448, ade + oa, brr + orr, idesc_bf16(128, 64), s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(5)) break;
+        if (lrow < C) {
+            const int r = lrow;
+            const bool live = r < len;
+            float x[64];
+            ld64(half * 64, x);                      // dVb
+            float rb = 0.f;
+            const __nv_bfloat16 *vrow = p.v + ((t0 + r) * H + h) * (int64_t)VD + half * 64;
+            float *dvrow = p.dv + ((t0 + r) * H + h) * (int64_t)VD + half * 64;
+            const float br = sB[r];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                *kchunk(gTL, 64, r, half * 64 + q * 8) = pack8(x + q * 8);   // dVb tile
+                if (live) {
+                    float vv[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(vrow + q * 8), vv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) rb = fmaf(x[q * 8 + e], vv[e], rb);
+                    *reinterpret_cast<float4 *>(dvrow + q * 8) =
+                        make_float4(br * x[q * 8], br * x[q * 8 + 1], br * x[q * 8 + 2], br * x[q * 8 + 3]);
+                    *reinterpret_cast<float4 *>(dvrow + q * 8 + 4) =
+                        make_float4(br * x[q * 8 + 4], br * x[q * 8 + 5], br * x[q * 8 + 6], br * x[q * 8 + 7]);
+                }
+            }
+            atomicAdd(&sRow[1][r], rb);
+            ld64(256 + half * 64, x);                // E dS'^T
+            if (live) {
+                float *dkrow = p.dk + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
+                const float fr = sFR[r];
+#pragma unroll
+                for (int q = 0; q < 64; q += 4)
+                    *reinterpret_cast<float4 *>(dkrow + q) =
+                        make_float4(fr * x[q], fr * x[q + 1], fr * x[q + 2], fr * x[q + 3]);
+            }
+            {   // dT = dE R^T (32 columns of this half)
+                float t32[32];
+                tmem_ld16(tmem + lane_off + 448 + half * 32, t32);
+                tmem_ld16(tmem + lane_off + 448 + half * 32 + 16, t32 + 16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 32; q += 4)
+                    *reinterpret_cast<float4 *>(sDT + r * kSolveLD + half * 32 + q) =
+                        make_float4(t32[q], t32[q + 1], t32[q + 2], t32[q + 3]);
+            }
+        } else {
+            const int r = lrow - C;
+            float x[64];
+            ld64(128 + half * 64, x);                // dO S^T
+            if (r < len) {
+                float *dqrow = p.dq + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
+                const float fq = p.scale * sEG[r];
+#pragma unroll
+                for (int q = 0; q < 64; q += 4)
+                    *reinterpret_cast<float4 *>(dqrow + q) =
+                        make_float4(fq * x[q], fq * x[q + 1], fq * x[q + 2], fq * x[q + 3]);
+            }
+            float t32[32];                           // dL = dO E^T (32 columns of this half)
+            tmem_ld16(tmem + lane_off + 384 + half * 32, t32);
+            tmem_ld16(tmem + lane_off + 384 + half * 32 + 16, t32 + 16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+                *reinterpret_cast<float4 *>(sDL + r * kSolveLD + half * 32 + q) =
+                    make_float4(t32[q], t32[q + 1], t32[q + 2], t32[q + 3]);
+        }
+        to_async();
+        // ---- R5: dVb S^T -> cols 0..127 (lanes 0..63)
+        if (tid == 0) {
+            const uint64_t a = smem_desc(sbase + gTL, 16, 1024, kSwizzle128B);
+            const uint64_t b = smem_desc(sbase + gS, 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tmem, a + (s >> 2) * (8192 >> 4) + (s & 3) * 2, b + (s >> 2) * (16384 >> 4) + (s & 3) * 2,
+                         idesc_bf16(128, 128), s > 0);
+            mma_commit(&bar_mma);
+        }
+        if (!mma_done(6)) break;
+        if (lrow < C) {   // dk -= beta Gamma dVb S^T;  RC = sum_c (dVb S^T) o K
+            const int r = lrow;
+            float x[64];
+            ld64(half * 64, x);
+            float rc = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float kk[8];
+                unpack8(*kchunk(gKQ, 128, r, half * 64 + q * 8), kk);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) rc = fmaf(x[q * 8 + e], kk[e], rc);
+            }
+            atomicAdd(&sRow[2][r], rc);
+            if (r < len) {
+                float *dkrow = p.dk + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
+                const float f = sB[r] * sEG[r];
+#pragma unroll
+                for (int q = 0; q < 64; q += 4) {
+                    float4 d = *reinterpret_cast<float4 *>(dkrow + q);
+                    d.x -= f * x[q]; d.y -= f * x[q + 1]; d.z -= f * x[q + 2]; d.w -= f * x[q + 3];
+                    *reinterpret_cast<float4 *>(dkrow + q) = d;
+                }
+            }
+        }
+        __syncthreads();
+        // scratch: dL, dT (as computed, full; the consumer masks them), row sums, <dS', S>
+        for (int e = tid; e < C * C / 4; e += kThreads) {
+            const int r = e >> 4, c = (e & 15) * 4;
+            *reinterpret_cast<float4 *>(scr + kScrDL + r * C + c) = *reinterpret_cast<const float4 *>(sDL + r * kSolveLD + c);
+            *reinterpret_cast<float4 *>(scr + kScrDT + r * C + c) = *reinterpret_cast<const float4 *>(sDT + r * kSolveLD + c);
+        }
+        for (int e = tid; e < 4 * C; e += kThreads) scr[kScrRows + e] = (&sRow[0][0])[e];
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < kThreads / 32; ++w) t += sRed[w];
+            scr[kScrRows + 4 * C] = t;
+        }
+    } while (0);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+// ============================================================================ grad2
+constexpr uint32_t hKQ = 0;          // [K; Q] tiles (TMA)                        32 KiB
+constexpr uint32_t hMP = 32768;      // [M; P] bf16: 128 rows x 64 columns         16 KiB
+constexpr uint32_t hPad = 49152;     // 8 KiB read as junk rows by the MN-major P^T view
+constexpr uint32_t hF = 57344;       // fp32 T, A', L, dL, dT (dA), X [64][kSolveLD]
+static_assert(hF == hPad + 8192, "the P^T view's second atom stays inside the allocation");
+constexpr uint32_t h2End = hF + 6 * C * kSolveLD * 4;
+constexpr int kGrad2Smem = h2End + 1024;
+static_assert(kGrad2Smem <= 232448, "grad2 shared memory");
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                GradParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    float *fT = reinterpret_cast<float *>(smem + hF);
+    float *fAp = fT + C * kSolveLD, *fL = fAp + C * kSolveLD, *fDL = fL + C * kSolveLD;
+    float *fDT = fDL + C * kSolveLD, *fX = fDT + C * kSolveLD;
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+    __shared__ float sG[C], sB[C], sDG[C], sRow[4][C], s_dgc, s_carry;
+
+    if (status_blocks(p.status)) return;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int lrow = quarter * 32 + (tid & 31);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int j = blockIdx.x, h = blockIdx.y, H = p.H;
+    int64_t t0;
+    int len;
+    if (!chunk_of_row(p, j, t0, len)) return;
+    const int unit = j * H + h;
+    const uint32_t sbase = smem_u32(smem);
+    const float *scr = p.scratch + (size_t)unit * kScrFloats;
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        s_err = 0;
+        fence_barrier_init();
+        mbar_arrive_expect_tx(&bar_tma, 32768);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(smem + hKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
+            tma_load_3d(smem + hKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
+        }
+    }
+    __syncwarp();
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, 256);
+        tmem_relinquish();
+    }
+    for (int e = tid; e < 5 * C * C / 4; e += kThreads) {       // T, A', L, dL, dT
+        const int m = e / (C * C / 4), w = e % (C * C / 4), r = w >> 4, c = (w & 15) * 4;
+        float *dst = fT + m * C * kSolveLD;
+        *reinterpret_cast<float4 *>(dst + r * kSolveLD + c) =
+            *reinterpret_cast<const float4 *>(scr + m * C * C + r * C + c);
+    }
+    for (int e = tid; e < 4 * C; e += kThreads) (&sRow[0][0])[e] = scr[kScrRows + e];
+    if (tid == 0) s_dgc = scr[kScrRows + 4 * C];
+    chunk_gates(p, t0, len, h, sG, sB, &s_carry);        // (its barriers also publish the loads)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    // ---- dA = -T^T (dT T^T), strictly lower; dT counts only on and below the diagonal.
+    // X = dT T^T: X[r][m] = sum_{i <= r} dT[r][i] T[m][i]  (T[m][i] = 0 for i > m; 1 x 4 strips)
+    for (int s = tid; s < C * 16; s += kThreads) {
+        const int r = s & 63, m0 = (s >> 6) * 4;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i <= r; ++i) {
+            const float dt = fDT[r * kSolveLD + i];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(dt, fT[(m0 + e) * kSolveLD + i], acc[e]);
+        }
+        *reinterpret_cast<float4 *>(fX + r * kSolveLD + m0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+    __syncthreads();
+    // dA[r][i] = -sum_{m >= r} T[m][r] X[m][i] for i < r, else 0  (over dT, which is consumed)
+    for (int s = tid; s < C * 16; s += kThreads) {
+        const int r = s & 63, i0 = (s >> 6) * 4;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (i0 < r) {
+            for (int m = r; m < C; ++m) {
+                const float t = fT[m * kSolveLD + r];
+                const float4 x = *reinterpret_cast<const float4 *>(fX + m * kSolveLD + i0);
+                acc[0] = fmaf(-t, x.x, acc[0]);
+                acc[1] = fmaf(-t, x.y, acc[1]);
+                acc[2] = fmaf(-t, x.z, acc[2]);
+                acc[3] = fmaf(-t, x.w, acc[3]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (i0 + e >= r) acc[e] = 0.f;
+        *reinterpret_cast<float4 *>(fDT + r * kSolveLD + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+    __syncthreads();
+    const float *fDA = fDT;
+    const float gC = sG[C - 1];
+    // ---- gate and beta gradients, one thread per row, fixed order
+    if (tid < C) {
+        const int r = tid;
+        const float gr = sG[r], Gr = __expf(gr), fr = r < len ? __expf(gC - gr) : 0.f;
+        float dgr = p.scale * Gr * sRow[0][r];
+        for (int i = 0; i <= r; ++i) dgr = fmaf(fDL[r * kSolveLD + i], fL[r * kSolveLD + i], dgr);
+        for (int r2 = r; r2 < C; ++r2) dgr = fmaf(-fDL[r2 * kSolveLD + r], fL[r2 * kSolveLD + r], dgr);
+        float da_row = 0.f;
+        for (int i = 0; i < r; ++i) da_row = fmaf(fDA[r * kSolveLD + i], fAp[r * kSolveLD + i], da_row);
+        dgr = fmaf(sB[r], da_row, dgr);
+        for (int r2 = r + 1; r2 < C; ++r2)
+            dgr = fmaf(-fDA[r2 * kSolveLD + r] * sB[r2], fAp[r2 * kSolveLD + r], dgr);
+        dgr -= sB[r] * Gr * sRow[2][r];
+        dgr -= fr * sRow[3][r];
+        sDG[r] = dgr;
+        if (r < len) p.dbeta[(t0 + r) * H + h] = sRow[1][r] - Gr * sRow[2][r] + da_row;
+    }
+    // ---- P = scale D o dL (i <= r) -> rows 64..127, M = beta_r D o dA (i < r) -> rows 0..63
+    // of the [M; P] operand (bf16, K-major over i)
+    {
+        const int r = tid >> 2;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+            const int c0 = ((tid & 3) * 2 + qq) * 8;
+            float m8[8], p8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = c0 + e;
+                const float dec = i <= r ? __expf(sG[r] - sG[i]) : 0.f;
+                p8[e] = i <= r ? p.scale * dec * fDL[r * kSolveLD + i] : 0.f;
+                m8[e] = i < r ? sB[r] * dec * fDA[r * kSolveLD + i] : 0.f;
+            }
+            *reinterpret_cast<uint4 *>(smem + hMP + kmaj16(128, r, c0)) = pack8(m8);
+            *reinterpret_cast<uint4 *>(smem + hMP + kmaj16(128, C + r, c0)) = pack8(p8);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {   // gamma_c: the Ktil factors and Gamma_c; dg = reverse cumsum of dgamma
+        float dgc = s_dgc * __expf(gC);
+        for (int i = 0; i < C; ++i) dgc = fmaf(i < len ? __expf(gC - sG[i]) : 0.f, sRow[3][i], dgc);
+        sDG[C - 1] += dgc;
+        float acc = 0.f;
+        for (int r = C - 1; r >= 0; --r) {
+            acc += sDG[r];
+            if (r < len) p.dg[(t0 + r) * H + h] = acc;
+        }
+    }
+    do {
+        const bool landed = mbar_wait(&bar_tma, 0, &s_err, 1);
+        if (__syncthreads_or(!landed)) break;
+        if (len < C) {   // K and Q rows past the end (NaN padding) enter the MMAs raw
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            for (int t = tid; t < 4 * C * 8; t += kThreads) {
+                const int r = (t >> 3) & 63, blk = t >> 9;
+                if (r >= len)
+                    *reinterpret_cast<uint4 *>(smem + hKQ + (blk & 1) * 16384 + (blk >> 1) * 8192 + r * 128 +
+                                               (t & 7) * 16) = zero;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- [M; P] K -> cols 0..127 (M K in lanes 0..63, P K in lanes 64..127);
+        //      M^T K + P^T Q -> cols 128..255 (lanes 0..63)
+        if (tid == 0) {
+            const uint64_t amp = smem_desc(sbase + hMP, 16, 1024, kSwizzle128B);
+            const uint64_t amt = smem_desc(sbase + hMP, 8192, 1024, kSwizzle128B);          // M^T
+            const uint64_t apt = smem_desc(sbase + hMP + 8192, 8192, 1024, kSwizzle128B);   // P^T
+            const uint64_t bk = smem_desc(sbase + hKQ, 16384, 1024, kSwizzle128B);
+            const uint64_t bq = smem_desc(sbase + hKQ + 8192, 16384, 1024, kSwizzle128B);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tmem, amp + s * 2, bk + s * 128, idesc_bf16(128, 128, 0, 1), s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + 128, amt + s * 128, bk + s * 128, idesc_bf16(128, 128, 1, 1), s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + 128, apt + s * 128, bq + s * 128, idesc_bf16(128, 128, 1, 1), 1);
+            mma_commit(&bar_mma);
+        }
+        const bool ok = mbar_wait(&bar_mma, 0, &s_err, 2);
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) break;
+        float x[64], y[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, x + q * 16);
+        tmem_ld_wait();
+        if (lrow < C) {   // dk += M K + M^T K + P^T Q
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, y + q * 16);
+            tmem_ld_wait();
+            const int r = lrow;
+            if (r < len) {
+                float *dkrow = p.dk + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
+#pragma unroll
+                for (int q = 0; q < 64; q += 4) {
+                    float4 d = *reinterpret_cast<float4 *>(dkrow + q);
+                    d.x += x[q] + y[q]; d.y += x[q + 1] + y[q + 1];
+                    d.z += x[q + 2] + y[q + 2]; d.w += x[q + 3] + y[q + 3];
+                    *reinterpret_cast<float4 *>(dkrow + q) = d;
+                }
+            }
+        } else {          // dq += P K
+            const int r = lrow - C;
+            if (r < len) {
+                float *dqrow = p.dq + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
+#pragma unroll
+                for (int q = 0; q < 64; q += 4) {
+                    float4 d = *reinterpret_cast<float4 *>(dqrow + q);
+                    d.x += x[q]; d.y += x[q + 1]; d.z += x[q + 2]; d.w += x[q + 3];
+                    *reinterpret_cast<float4 *>(dqrow + q) = d;
+                }
+            }
+        }
+    } while (0);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+}  // namespace
+
+size_t bwd_grad_tc_scratch_bytes(int64_t nt_max, int H) {
+    return (size_t)nt_max * H * kScrFloats * sizeof(float);
+}
+
+cudaError_t launch_bwd_grad_tc(const BwdParams &p, float *scratch, cudaStream_t s) {
+    const int H = p.H;
+    CUtensorMap mq, mk, mv, mdo;
+    const cuuint64_t dqk[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sqk[2] = {(cuuint64_t)KD * 2, (cuuint64_t)H * KD * 2};
+    const cuuint32_t b64[3] = {64, 1, 64};
+    const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
+    if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mdo, p.d_o, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    GradParams gp{};
+    gp.chunk_indices = p.chunk_indices;
+    gp.cu = p.cu_seqlens;
+    gp.g = p.g;
+    gp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
+    gp.v = static_cast<const __nv_bfloat16 *>(p.v);
+    gp.h = p.h;
+    gp.dh = p.dh;
+    gp.dq = p.dq;
+    gp.dk = p.dk;
+    gp.dv = p.dv;
+    gp.dg = p.dg;
+    gp.dbeta = p.dbeta;
+    gp.scratch = scratch;
+    gp.status = p.dev_status;
+    gp.t_max = p.t_max;
+    gp.nt_max = p.nt_max;
+    gp.n_max = p.n_max;
+    gp.H = H;
+    gp.scale = p.scale;
+    cudaError_t e = cudaFuncSetAttribute(tc_grad1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGrad1Smem);
+    if (e != cudaSuccess) return e;
+    tc_grad1_kernel<<<dim3((unsigned)p.nt_max, H), kThreads, kGrad1Smem, s>>>(mq, mk, mv, mdo, gp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(tc_grad2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGrad2Smem)) !=
+        cudaSuccess)
+        return e;
+    tc_grad2_kernel<<<dim3((unsigned)p.nt_max, H), kThreads, kGrad2Smem, s>>>(mq, mk, gp);
+    return cudaGetLastError();
+}
+
+}  // namespace gcl

@@ -41,29 +41,6 @@ namespace {
 using namespace tc;
 using namespace tr;
 
-__device__ __forceinline__ float warp_scan(float x) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, d);
-        if (lane >= d) x += y;
-    }
-    return x;
-}
-
-// K-major 128-byte-swizzled bf16 tile of `rows` rows per 64-column block: byte offset
-// of the 16-byte chunk that holds columns [col, col + 8) of `row`.
-__device__ __forceinline__ uint32_t kmaj16(int rows, int row, int col) {
-    return (uint32_t)((col >> 6) * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
-                      ((((col & 63) >> 3) ^ (row & 7)) << 4));
-}
-// MN-major 128-byte-swizzled bf16 operand (8-row k-groups of 1024 B, 64-element atoms
-// `atom_bytes` apart): byte offset of the 16-byte chunk holding elements [n, n + 8) of k.
-__device__ __forceinline__ uint32_t mnmaj16(uint32_t atom_bytes, int k, int n) {
-    return (uint32_t)((n >> 6) * atom_bytes + (k >> 3) * 1024 + (k & 7) * 128 +
-                      ((((n & 63) >> 3) ^ (k & 7)) << 4));
-}
-
 // ============================================================================ prep_t
 struct PrepTParams {
     const int32_t *chunk_indices, *cu;

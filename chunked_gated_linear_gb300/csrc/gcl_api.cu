@@ -140,7 +140,8 @@ static size_t bwd_ws(const gcl_bwd_args *a) {
     if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
     const bool tc = fwd_tc_supported(kGDN, a->dtype, a->K, a->V);
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
-    const size_t rec = tc ? align256(transition_record_bytes(ntm, a->H)) + kWsAlign : 0;
+    const size_t rec = tc ? align256(transition_record_bytes(ntm, a->H)) + kWsAlign +
+                                align256(bwd_grad_tc_scratch_bytes(ntm, a->H)) : 0;
     if (a->h_save) return per + rec;
     const size_t fw = tc ? align256(fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign : 0;
     return 2 * per + fw + rec;
@@ -280,13 +281,17 @@ gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
         void *rec = nullptr;
         size_t rec_bytes = 0;
         align_ws(ws + used, a->workspace_bytes - used, &rec, &rec_bytes);
-        if (rec_bytes < transition_record_bytes(ntm, a->H))
+        if (rec_bytes < align256(transition_record_bytes(ntm, a->H)) + bwd_grad_tc_scratch_bytes(ntm, a->H))
             return fail(GCL_ERR_CAPACITY, "%s: workspace too small for the sweep records", fn);
         cudaError_t e = launch_prep_t(f, static_cast<uint8_t *>(rec), s);
         if (e == cudaSuccess) e = launch_bwd_sweep_t(p, static_cast<const uint8_t *>(rec), s);
         if ((st = cuda_check(e, "gdn_chunk_bwd (state-gradient sweep)")) != GCL_OK) return st;
+        // chunk gradients on the tensor cores; their scratch follows the records
+        float *scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(rec) +
+                                                   align256(transition_record_bytes(ntm, a->H)));
+        return cuda_check(launch_bwd_grad_tc(p, scratch, s), fn);
     }
-    return cuda_check(launch_bwd_simt(p, a->dtype, tc, s), fn);
+    return cuda_check(launch_bwd_simt(p, a->dtype, false, s), fn);
 }
 
 }  // extern "C"

@@ -80,6 +80,10 @@ bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t
 cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s);
 // Tensor-core state-gradient sweep from transition-form records (GDN, bf16, K = V = 128).
 cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *records, cudaStream_t s);
+// Tensor-core chunk gradients (dq, dk, dv, dg, dbeta) from p.h and p.dh, with a scratch record
+// of bwd_grad_tc_scratch_bytes per launch (GDN, bf16, K = V = 128).
+cudaError_t launch_bwd_grad_tc(const BwdParams &p, float *scratch, cudaStream_t s);
+size_t bwd_grad_tc_scratch_bytes(int64_t nt_max, int H);
 
 // ---- device helpers -------------------------------------------------------
 __device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }
