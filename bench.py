@@ -195,8 +195,8 @@ class Runner:
         fkw = dict(h0=t.get("h0"), ht=t["ht"], h_save=t.get("hs"), chunk_indices=t["idx"],
                    chunk_offsets=t["off"], seq_order=t["order"], dev_status=t["status"],
                    scale=w.scale)
-        t["fws"] = torch.empty(max(gcl.fwd_workspace_bytes(*fargs, **fkw), 16),
-                               dtype=torch.uint8, device=dev)
+        wsq = gcl.kda_fwd_workspace_bytes if w.variant == synth.KDA else gcl.fwd_workspace_bytes
+        t["fws"] = torch.empty(max(wsq(*fargs, **fkw), 16), dtype=torch.uint8, device=dev)
         self.fwd_args = gcl.fwd_args(*fargs, workspace=t["fws"], **fkw)
         self.fwd = gcl.lib().kda_chunk_fwd if w.variant == synth.KDA else gcl.lib().gdn_chunk_fwd
         if w.backward:
@@ -245,10 +245,10 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
 
 def launches_per_step(w) -> int:
     """Library kernels per step: chunk_meta_build, the forward (prep and chain on the tensor
-    cores for GDN bf16 d_k = d_v = 128, one fused CUDA-core kernel otherwise) and the
-    backward (on the tensor cores: transition records, state-gradient sweep and two
+    cores for GDN and KDA bf16 d_k = d_v = 128, one fused CUDA-core kernel otherwise) and
+    the GDN backward (on the tensor cores: transition records, state-gradient sweep and two
     chunk-gradient kernels; otherwise the sweep and one chunk-gradient kernel)."""
-    tc = w.variant == synth.GDN and w.dtype == "bf16" and w.K == 128 and w.V == 128
+    tc = w.dtype == "bf16" and w.K == 128 and w.V == 128
     return 1 + (2 if tc else 1) + ((4 if tc else 2) if w.backward else 0)
 
 

@@ -75,7 +75,7 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(FwdArgs), vp]
     lib.gcl_noalloc_scratch_bytes.restype = ctypes.c_size_t
     lib.gcl_noalloc_scratch_bytes.argtypes = []
-    for fn in ("gcl_fwd_workspace_bytes", "gcl_fwd_workspace_min_bytes"):
+    for fn in ("gcl_fwd_workspace_bytes", "gcl_fwd_workspace_min_bytes", "gcl_kda_fwd_workspace_bytes"):
         getattr(lib, fn).restype = ctypes.c_size_t
         getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs)]
     lib.gdn_chunk_bwd.restype = ctypes.c_int
@@ -167,6 +167,12 @@ def fwd_workspace_min_bytes(*args, **kw) -> int:
     """Least workspace the forward accepts (it then runs the W-form plan)."""
     a = fwd_args(*args, **kw)
     return int(lib().gcl_fwd_workspace_min_bytes(ctypes.byref(a)))
+
+
+def kda_fwd_workspace_bytes(*args, **kw) -> int:
+    """Workspace kda_chunk_fwd needs (its one tensor-core plan; 0 on the CUDA-core path)."""
+    a = fwd_args(*args, **kw)
+    return int(lib().gcl_kda_fwd_workspace_bytes(ctypes.byref(a)))
 
 
 def gdn_chunk_fwd(*args, stream=None, **kw):

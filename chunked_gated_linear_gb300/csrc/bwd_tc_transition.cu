@@ -42,7 +42,7 @@ struct SweepTParams {
 // then two bf16 copies of dS' as MN-major B operands.
 template <int NS>
 struct SweepLayout {
-    static constexpr uint32_t kN = 32768, kY = 16384, kDO = 8192, kG = 16;
+    static constexpr uint32_t kN = 32768, kY = 16384, kDO = 8192, kG = kGBytes;
     static constexpr uint32_t oN = 0, oY = kN, oDO = oY + kY, oG = oDO + kDO;
     static constexpr uint32_t kStage = (oG + kG + 1023) / 1024 * 1024;
     static constexpr uint32_t oDS = NS * kStage;                 // two 16 KiB buffers

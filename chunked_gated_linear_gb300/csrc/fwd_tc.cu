@@ -690,7 +690,7 @@ bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t
 }
 
 bool fwd_tc_supported(int variant, int dtype, int K, int V) {
-    return variant == kGDN && dtype == GCL_BF16 && K == KD && V == VD;
+    return (variant == kGDN || variant == kKDA) && dtype == GCL_BF16 && K == KD && V == VD;
 }
 
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H) {
@@ -710,8 +710,11 @@ int fwd_tc_split(int n_max, int H) {
 bool fwd_tc_prefers_transition(int n_max, int H) { return fwd_tc_split(n_max, H) >= 4; }
 
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
-    (void)variant;
     const int H = p.H;
+    if (variant == kKDA) {   // KDA has the transition form only
+        if (p.workspace_bytes < fwd_tc_t_workspace_bytes(p.nt_max, H)) return cudaErrorInvalidValue;
+        return launch_fwd_tc_kda(p, fwd_tc_split(p.n_max, H), s);
+    }
     if (fwd_tc_prefers_transition(p.n_max, H) &&
         p.workspace_bytes >= fwd_tc_t_workspace_bytes(p.nt_max, H))
         return launch_fwd_tc_t(p, fwd_tc_split(p.n_max, H), s);

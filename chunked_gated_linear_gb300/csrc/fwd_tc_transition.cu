@@ -42,17 +42,6 @@ using namespace tc;
 using namespace tr;
 
 // ============================================================================ prep_t
-struct PrepTParams {
-    const int32_t *chunk_indices, *cu;
-    const float *g;
-    const __nv_bfloat16 *beta;
-    uint8_t *ws;                 // nt_max * H records of kUnitBytes, then the Gamma_c slots
-    int32_t *status;
-    int64_t t_max, nt_max;
-    int32_t n_max, H;
-    float scale;
-};
-
 constexpr int kPrepThreads = 256;
 // dynamic shared memory, offsets from the 1024-aligned base
 constexpr uint32_t pKQ = 0;        // [2 col blocks][K rows 0..63 | Q rows 0..63][128 B]  32 KiB
@@ -62,37 +51,6 @@ constexpr uint32_t pA = 73728;     // fp32 A, T [64][kSolveLD], X; later [W | U]
 constexpr uint32_t pEnd = pA + kSolveFloats * 4;
 constexpr int kPrepTSmem = pEnd + 1024;
 static_assert(pEnd - pA >= 4 * 8192, "[W | U] (4 atoms of 8 KiB) reuses the solve buffers");
-
-// One work item per row j of chunk_indices and head h, numbered i = j H + h (the record
-// index).  Rows past the live chunks hold the [-1, 0] sentinel, so a CTA that walks its items
-// in increasing order stops at the first sentinel.
-struct PrepItem {
-    int64_t t0;
-    int h, len;
-};
-
-// Next live item at or after i in steps of `stride` (-1 when there is none); invalid rows set
-// the status word and are skipped.  Every thread of the block computes the same answer.
-__device__ __forceinline__ int next_item(const PrepTParams &p, int i, int stride, PrepItem *it) {
-    const int total = (int)(p.nt_max * p.H);
-    for (; i < total; i += stride) {
-        const int j = i / p.H;
-        const int n = p.chunk_indices[2 * j];
-        if (n < 0) return -1;                                  // sentinel: no more live rows
-        const int ic = p.chunk_indices[2 * j + 1];
-        if (n < p.n_max && ic >= 0) {
-            const int64_t bos = p.cu[n], eos = p.cu[n + 1], t0 = bos + (int64_t)ic * C;
-            if (bos >= 0 && eos >= bos && eos <= p.t_max && t0 < eos) {
-                it->t0 = t0;
-                it->h = i - j * p.H;
-                it->len = (int)(eos - t0 < C ? eos - t0 : C);
-                return i;
-            }
-        }
-        if (threadIdx.x == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
-    }
-    return -1;
-}
 
 // Persistent: gridDim.x CTAs (two per SM) walk the items with stride gridDim.x.  The next
 // item's K and Q tiles are requested as soon as MMA3 has consumed the current ones, its V tile
@@ -499,12 +457,12 @@ struct ChainTParams {
 };
 
 // Shared memory: NS stages of {[Y; N] (two 64-column blocks of 192 rows, 128-byte
-// swizzle), B slice [128][VS], Z slice [64][VS], Gamma_c}, then three bf16 copies of the
+// swizzle), B slice [128][VS], Z slice [64][VS], the Gamma_c slot}, then three bf16 copies of the
 // state slice S as MN-major B operands (VS used columns of a 64-element atom): S(n) in
 // buffer n % 3, so the copy of S(n+1) overwrites the one G2 read two chunks earlier.
 template <int VS, int NS>
 struct ChainTLayout {
-    static constexpr uint32_t kYN = 49152, kB = VS * 256, kZ = VS * 128, kG = 16;
+    static constexpr uint32_t kYN = 49152, kB = VS * 256, kZ = VS * 128, kG = kGBytes;
     static constexpr uint32_t oYN = 0, oB = kYN, oZ = oB + kB, oG = oZ + kZ;
     static constexpr uint32_t kStage = (oG + kG + 1023) / 1024 * 1024;
     static constexpr int kSB = 3;                                // bf16 copies of S
@@ -536,7 +494,8 @@ constexpr int kChainThreads = 32 * (kWarpTma + 1);
 // that a faster party could lap come in pairs indexed by chunk parity), so no waiter can fall
 // two phases behind.  After a failed (timed-out) wait every further wait returns at once, so
 // all loops run to their ends without a uniform break.
-template <int VS, int NS>
+// KDA: Gamma_c is a per-key-channel vector (the state row of thread t decays by its own entry).
+template <int VS, int NS, bool KDA>
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_constant__ CUtensorMap tm_b,
                   const __grid_constant__ CUtensorMap tm_z, ChainTParams p) {
@@ -746,7 +705,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             }
             mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 3);
             {   // Gamma_c S + B while G1 runs
-                const float gc = *reinterpret_cast<const float *>(stage + Lay::oG);
+                const float gc = reinterpret_cast<const float *>(stage + Lay::oG)[KDA ? row : 0];
                 const uint8_t *brow = stage + Lay::oB + row * (VS * 2) + c0 * 2;
 #pragma unroll
                 for (int j = 0; j < HV; j += 8) {
@@ -797,7 +756,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
 }
 
-template <int VS, int NS>
+template <int VS, int NS, bool KDA>
 cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const ChainTParams &cp,
                            int n_split, int H, int n_max, cudaStream_t s) {
     using Lay = ChainTLayout<VS, NS>;
@@ -812,7 +771,7 @@ cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const Chai
     if (!make_tensor_map(&mb, ws + kYNBytes, 3, db, sb, bb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tensor_map(&mz, ws + kYNBytes + kBBytes, 3, dz, sb, bz, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kern = tc_chain_t_kernel<VS, NS>;
+    auto kern = tc_chain_t_kernel<VS, NS, KDA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
@@ -829,10 +788,10 @@ size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H) {
 
 size_t transition_record_bytes(int64_t nt_max, int H) { return fwd_tc_t_workspace_bytes(nt_max, H); }
 
-cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
+bool make_prep_maps(const FwdParams &p, uint8_t *ws, CUtensorMap *mq, CUtensorMap *mk, CUtensorMap *mv,
+                    CUtensorMap *mrec) {
     const int H = p.H;
     const int64_t units = p.nt_max * H;
-    CUtensorMap mq, mk, mv, mrec;
     const cuuint64_t dqk[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)p.t_max};
     const cuuint64_t sqk[2] = {(cuuint64_t)KD * 2, (cuuint64_t)H * KD * 2};
     const cuuint32_t b64[3] = {64, 1, 64};
@@ -843,12 +802,14 @@ cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
     static_assert(kUnitBytes % (KD * 2) == 0, "a record is whole rows");
     const cuuint64_t srec[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
     const cuuint32_t brec[3] = {64, 64, 1};
-    if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&mrec, ws, 3, drec, srec, brec, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    PrepTParams pp{};
+    return make_tensor_map(mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(mrec, ws, 3, drec, srec, brec, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+tr::PrepTParams make_prep_params(const FwdParams &p, uint8_t *ws) {
+    tr::PrepTParams pp{};
     pp.chunk_indices = p.chunk_indices;
     pp.cu = p.cu_seqlens;
     pp.g = p.g;
@@ -858,22 +819,28 @@ cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
     pp.t_max = p.t_max;
     pp.nt_max = p.nt_max;
     pp.n_max = p.n_max;
-    pp.H = H;
+    pp.H = p.H;
     pp.scale = p.scale;
+    return pp;
+}
+
+cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
+    CUtensorMap mq, mk, mv, mrec;
+    if (!make_prep_maps(p, ws, &mq, &mk, &mv, &mrec)) return cudaErrorInvalidValue;
+    const PrepTParams pp = make_prep_params(p, ws);
     cudaError_t e = cudaFuncSetAttribute(tc_prep_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPrepTSmem);
     if (e != cudaSuccess) return e;
+    const int64_t units = p.nt_max * p.H;
     const int grid = (int)(units < 2 * (int64_t)num_sms() ? units : 2 * (int64_t)num_sms());
     return launch_dependent(tc_prep_t_kernel, dim3(grid), dim3(kPrepThreads), kPrepTSmem, s, mq, mk, mv,
                             mrec, pp);
 }
 
-cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
+cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int split, bool kda,
+                                 cudaStream_t s) {
     const int H = p.H;
     const int64_t units = p.nt_max * H;
-    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
-    cudaError_t e = launch_prep_t(p, ws, s);
-    if (e != cudaSuccess) return e;
     CUtensorMap myn;
     const cuuint64_t dyn[3] = {(cuuint64_t)KD, (cuuint64_t)kYNRows, (cuuint64_t)units};
     const cuuint64_t syn[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
@@ -894,9 +861,22 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     cp.nt_max = p.nt_max;
     cp.n_max = p.n_max;
     cp.H = H;
-    if (split == 8) return launch_chain_t<16, 3>(myn, ws, cp, split, H, p.n_max, s);
-    if (split == 4) return launch_chain_t<32, 2>(myn, ws, cp, split, H, p.n_max, s);
-    return cudaErrorInvalidValue;                   // the plan is only taken at splits 4 and 8
+    if (kda) {
+        if (split == 8) return launch_chain_t<16, 3, true>(myn, ws, cp, split, H, p.n_max, s);
+        if (split == 4) return launch_chain_t<32, 2, true>(myn, ws, cp, split, H, p.n_max, s);
+        if (split == 2) return launch_chain_t<64, 2, true>(myn, ws, cp, split, H, p.n_max, s);
+        return cudaErrorInvalidValue;
+    }
+    if (split == 8) return launch_chain_t<16, 3, false>(myn, ws, cp, split, H, p.n_max, s);
+    if (split == 4) return launch_chain_t<32, 2, false>(myn, ws, cp, split, H, p.n_max, s);
+    return cudaErrorInvalidValue;                   // GDN takes this plan only at splits 4 and 8
+}
+
+cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
+    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
+    cudaError_t e = launch_prep_t(p, ws, s);
+    if (e != cudaSuccess) return e;
+    return launch_chain_records(p, ws, split, false, s);
 }
 
 }  // namespace gcl

@@ -65,6 +65,8 @@ cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStre
 // split is 4 or more and the workspace holds it.
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s);
 cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s);
+// KDA on the tensor cores: transition-form records with per-channel gates, then the chain.
+cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s);
 bool fwd_tc_supported(int variant, int dtype, int K, int V);
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H);     // W form (the minimum)
 size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H);   // transition form

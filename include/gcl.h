@@ -160,6 +160,14 @@ typedef struct gcl_fwd_args {
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
 size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
 
+/* Bytes of device workspace kda_chunk_fwd needs for these sizes (0 when the fp32
+ * CUDA-core kernel serves them).  KDA on the tensor cores has one plan, the
+ * transition form (96.5 KiB per chunk and head: the chunk's affine state map and
+ * output map, and the per-key-channel state decay of the chunk); a smaller
+ * workspace returns GCL_ERR_CAPACITY.  gcl_fwd_workspace_bytes and
+ * gcl_fwd_workspace_min_bytes describe gdn_chunk_fwd only. */
+size_t gcl_kda_fwd_workspace_bytes(const gcl_fwd_args *args);
+
 /*
  * gdn_chunk_fwd -- gated delta rule prefill: o and ht from q, k, v, g, beta, h0.
  * kda_chunk_fwd -- the same with the per-key-channel gate of KDA.
@@ -171,13 +179,14 @@ size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
  * CTAs (HA-NPU section 4, column-wise split without cross-core reductions).
  * Zero-length sequences write ht = h0 (or zeros).
  *
- * Supported: bt = 64; K, V in {64, 128}; dtype GCL_F32 or GCL_BF16.  GDN with
- * bf16 inputs and K = V = 128 runs on the tensor cores (tcgen05): a
+ * Supported: bt = 64; K, V in {64, 128}; dtype GCL_F32 or GCL_BF16.  GDN and
+ * KDA with bf16 inputs and K = V = 128 run on the tensor cores (tcgen05): a
  * chunk-parallel launch over chunk_indices forms per chunk either T = (I + A)^-1
- * and L (W form) or the chunk's transition S' = Gamma_c S + N S + B and output
- * O = Y S + Z (transition form) into the workspace, then the per-(sequence, head,
- * column slice) launch runs the state recurrence.  Everything else runs the fp32
- * CUDA-core kernel.
+ * and L (W form, GDN) or the chunk's transition S' = Gamma_c S + N S + B and
+ * output O = Y S + Z (transition form; for KDA Gamma_c is a per-key-channel
+ * diagonal) into the workspace, then the per-(sequence, head, column slice)
+ * launch runs the state recurrence.  Everything else runs the fp32 CUDA-core
+ * kernel.  The workspace of kda_chunk_fwd is sized by gcl_kda_fwd_workspace_bytes.
  * Pointers must be 16-byte aligned.
  */
 gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream);

@@ -74,7 +74,10 @@ def run_fwd(w, d, meta=None, h_save=False, o_fill=CANARY, use_order=True, plan="
     kw = dict(h0=d.get("h0"), ht=ht, h_save=hs, chunk_indices=meta.idx, chunk_offsets=meta.off,
               seq_order=meta.order if use_order else None, dev_status=meta.status,
               scale=w.scale, bt=w.bt)
-    nb = (gcl.fwd_workspace_bytes if plan == "fastest" else gcl.fwd_workspace_min_bytes)(*args, **kw)
+    if w.variant == synth.KDA:
+        nb = gcl.kda_fwd_workspace_bytes(*args, **kw)
+    else:
+        nb = (gcl.fwd_workspace_bytes if plan == "fastest" else gcl.fwd_workspace_min_bytes)(*args, **kw)
     ws = torch.full((max(nb, 16),), 0xFF, dtype=torch.uint8, device=DEV)   # stale contents
     fn(*args, workspace=ws, **kw)
     return dict(o=o, ht=ht, h_save=hs, meta=meta, ws=ws)

@@ -116,3 +116,41 @@ def test_invalid_cu_seqlens_do_nothing():
     assert int(out["meta"].status.item()) == 1
     assert (out["o"].float().cpu().numpy() == np.float32(CANARY)).all()
     assert (out["ht"].cpu().numpy() == np.float32(CANARY)).all()
+
+
+@pytest.mark.parametrize("H", [2, 4, 6], ids=["split8", "split4", "split2"])
+def test_kda_tensor_core_column_splits(H):
+    """KDA bf16 d=128 at 8, 4 and 2 value-column slices per head (16, 32 and 48
+    sequence-head units), ragged lengths, h0 and saved chunk states."""
+    lens = [1, 63, 0, 64, 65, 200, 130, 0]
+    w = synth.varlen("kda-split", synth.KDA, "bf16", lens, 8, sum(lens) + 40, H, 128, 128, seed=21)
+    x = synth.make_inputs(w)
+    out = run_fwd(w, to_device(w, x), h_save=True)
+    check_fwd(w, x, out, label=f"kda H={H}")
+    meta = out["meta"]
+    off = meta.off.cpu().numpy()
+    _, _, hc = oracle.fwd(synth.KDA, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                          x["cu_seqlens"], w.scale, bt=64, chunk_offsets=off, nt_rows=meta.nt_max)
+    live = int(off[-1])
+    assert relF(out["h_save"].cpu().numpy()[:live], hc[:live]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("regime", ["strong", "none", "mixed"])
+def test_kda_gate_extremes(regime):
+    """Per-channel gates far outside the generator's range: strong decay (log gates down to
+    -80 per token, so the decay over a 16-token block underflows fp32 when factored through
+    one reference), no decay (g = 0) and a mix of both across channels and tokens."""
+    lens = [300, 77]
+    w = synth.varlen("kda-gates", synth.KDA, "bf16", lens, 2, 400, 2, 128, 128, seed=23)
+    x = synth.make_inputs(w)
+    g = x["g"].copy()
+    rng = np.random.default_rng(5)
+    if regime == "strong":
+        g *= 20.0
+    elif regime == "none":
+        g[:] = 0.0
+    else:
+        g[rng.random(g.shape) < 0.1] *= 40.0       # scattered strong gates
+        g[:, :, :32] = 0.0                          # and undecayed channels
+    x["g"] = g.astype(np.float32)
+    check_fwd(w, x, run_fwd(w, to_device(w, x)), label=f"kda gates {regime}")
