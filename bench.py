@@ -82,23 +82,32 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record():
-    """DRAM bytes per launch from the committed ncu summary of the forward kernel, if it was
-    taken on the current kernel source (checked by hash), else None."""
+def traffic_record(workload: str):
+    """DRAM bytes per forward call of `workload` from the committed ncu summary
+    (profiles/traffic.txt, one [workload] section each), if it was taken on the current
+    kernel sources (checked by hash over the listed files), else None."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    kv = {}
+    sections, cur = {}, None
     for line in open(path):
-        if ":" in line and not line.startswith("#"):
-            a, b = line.split(":", 1)
-            kv[a.strip()] = b.strip()
-    src = kv.get("kernel_source")
-    if not src or not os.path.exists(os.path.join(ROOT, src)):
+        line = line.strip()
+        if line.startswith("[") and line.endswith("]"):
+            cur = sections.setdefault(line[1:-1], {})
+        elif cur is not None and ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            cur[k.strip()] = v.strip()
+    kv = sections.get(workload)
+    if not kv or not kv.get("kernel_sources"):
         return None
-    sha = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
-    if sha != kv.get("kernel_source_sha256_16"):
+    h = hashlib.sha256()
+    for src in kv["kernel_sources"].split():
+        f = os.path.join(ROOT, src)
+        if not os.path.exists(f):
+            return None
+        h.update(open(f, "rb").read())
+    if h.hexdigest()[:16] != kv.get("kernel_sources_sha256_16"):
         return None
     try:
         return float(kv["dram_bytes_per_launch_scaled"])
@@ -321,7 +330,7 @@ def run_gpu(args, rank, world, dist):
     peak, peak_kind = peaks()
     ab = bytes_per_step(w)
     achieved = ab / (ms_kern * 1e-3) / 1e9
-    traffic = traffic_record()
+    traffic = traffic_record(w.name)
     line = {
         "metric": "GDN/KDA chunk prefill tokens/s on 1 GB300 and % of roofline (HBM/TC)",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
