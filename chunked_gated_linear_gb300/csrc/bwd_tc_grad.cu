@@ -29,18 +29,23 @@ namespace {
 using namespace tc;
 using namespace tr;
 
-// scratch record per chunk and head (fp32): T, A' = D o K K^T (strict), L, dL, dT [64][64],
-// then rows: RA = sum_v dO o QS, RB = sum_v dVb o V, RC = sum_c (dVb S^T) o K,
-// RD = sum_v E o K dS', and <dS', S> in the first entry of row 4.
-constexpr int kScrT = 0, kScrAp = 4096, kScrL = 8192, kScrDL = 12288, kScrDT = 16384;
-constexpr int kScrRows = 20480;
-constexpr int kScrFloats = kScrRows + 8 * 64;
+// scratch record per chunk and head (fp32): T, A' = D o K K^T (strict), L, dL, dT as
+// [64][kSolveLD] (the shared-memory layout of the second kernel, so one bulk copy moves
+// them), then rows: RA = sum_v dO o QS, RB = sum_v dVb o V, RC = sum_c (dVb S^T) o K,
+// RD = sum_v E o K dS', and <dS', S> after them.
+constexpr int kScrMat = C * kSolveLD;
+constexpr int kScrT = 0, kScrAp = kScrMat, kScrL = 2 * kScrMat, kScrDL = 3 * kScrMat, kScrDT = 4 * kScrMat;
+constexpr int kScrRows = 5 * kScrMat;
+constexpr int kScrRowFloats = 4 * C + 8;             // a multiple of 4 floats (16 bytes)
+constexpr int kScrFloats = kScrRows + kScrRowFloats;
+static_assert((kScrFloats * 4) % 16 == 0 && (kScrRows * 4) % 16 == 0, "bulk copies of 16-byte multiples");
 
 struct GradParams {
     const int32_t *chunk_indices, *cu;
     const float *g;
     const __nv_bfloat16 *beta, *v;
-    const float *h, *dh;
+    const float *h;                 // the state entering every chunk, fp32 [unit][K][V]
+    const uint8_t *dh;              // dS' of every chunk, bf16 tiles of kDsTileBytes
     float *dq, *dk, *dv, *dg, *dbeta;
     float *scratch;
     int32_t *status;
@@ -95,6 +100,10 @@ constexpr uint32_t gDS = 81920;      // dS' bf16                                
 constexpr uint32_t gT3 = 114688;     // [dE; E; dO]: 2 blocks x 192 rows             48 KiB
 constexpr uint32_t gTL = 163840;     // [T; L]: 128 rows x 64 columns, then dVb      16 KiB
 constexpr uint32_t gF = 180224;      // fp32 A (-> dL), T (-> dT), solve scratch
+// At the start S arrives as fp32 (64 KiB) in staging: keys 0..31 in the [dE; E] rows of
+// column block 0 of gT3, keys 32..127 from gTL on (gTL and gF are contiguous).
+constexpr uint32_t gStage0 = gT3, gStage1 = gTL;
+static_assert(gTL + 16384 == gF && gStage1 + 3 * 16384 <= gF + kSolveFloats * 4, "S staging");
 constexpr uint32_t g1End = gF + kSolveFloats * 4;
 constexpr int kGrad1Smem = g1End + 1024;
 static_assert(kGrad1Smem <= 232448, "grad1 shared memory");
@@ -125,7 +134,6 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (!chunk_of_row(p, j, t0, len)) return;
     const int unit = j * H + h;
     const uint32_t sbase = smem_u32(smem);
-    const int64_t KV = (int64_t)KD * VD;
     float *scr = p.scratch + (size_t)unit * kScrFloats;
 
     if (tid == 0) {
@@ -133,13 +141,17 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&bar_mma, 1);
         s_err = 0;
         fence_barrier_init();
-        mbar_arrive_expect_tx(&bar_tma, 65536);
+        mbar_arrive_expect_tx(&bar_tma, 65536 + (uint32_t)kDsTileBytes + 65536);
         for (int cb = 0; cb < 2; ++cb) {
             tma_load_3d(smem + gKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
             tma_load_3d(smem + gKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
             tma_load_3d(smem + gV + cb * 8192, &tm_v, cb * 64, h, (int)t0, &bar_tma);
             tma_load_3d(smem + gT3 + cb * 24576 + 16384, &tm_do, cb * 64, h, (int)t0, &bar_tma);
         }
+        bulk_load(smem + gDS, p.dh + (size_t)unit * kDsTileBytes, (uint32_t)kDsTileBytes, &bar_tma);
+        const float *Sg = p.h + (int64_t)unit * KD * VD;
+        bulk_load(smem + gStage0, Sg, 16384, &bar_tma);
+        for (int q = 0; q < 3; ++q) bulk_load(smem + gStage1 + q * 16384, Sg + (q + 1) * 4096, 16384, &bar_tma);
     }
     __syncwarp();
     if (warp == 0) {
@@ -152,35 +164,6 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid < C) {
         sEG[tid] = __expf(sG[tid]);
         sFR[tid] = tid < len ? __expf(gC - sG[tid]) : 0.f;
-    }
-    // decay table D[r][c] = exp(g_r - g_c) for c <= r (1 above the diagonal) in the T buffer
-    for (int e = tid; e < C * C / 4; e += kThreads) {
-        const int r = e >> 4, c = (e & 15) * 4;
-        const float gr = sG[r];
-        *reinterpret_cast<float4 *>(sT + r * kSolveLD + c) =
-            make_float4(__expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
-                        __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
-    }
-    // S and dS' (fp32) -> bf16 operand tiles; <dS', S>
-    float dgc = 0.f;
-    {
-        const float *Sg = p.h + (int64_t)unit * KV, *dSg = p.dh + (int64_t)unit * KV;
-        for (int e = tid; e < KD * VD / 8; e += kThreads) {
-            const int key = e >> 4, c0 = (e & 15) * 8;
-            const float4 a0 = *reinterpret_cast<const float4 *>(Sg + key * VD + c0);
-            const float4 a1 = *reinterpret_cast<const float4 *>(Sg + key * VD + c0 + 4);
-            const float4 b0 = *reinterpret_cast<const float4 *>(dSg + key * VD + c0);
-            const float4 b1 = *reinterpret_cast<const float4 *>(dSg + key * VD + c0 + 4);
-            const float sv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float dv8[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) dgc = fmaf(sv[q], dv8[q], dgc);
-            *reinterpret_cast<uint4 *>(smem + gS + kmaj16(128, key, c0)) = pack8(sv);
-            *reinterpret_cast<uint4 *>(smem + gDS + kmaj16(128, key, c0)) = pack8(dv8);
-        }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) dgc += __shfl_xor_sync(0xffffffffu, dgc, d);
-        if ((tid & 31) == 0) sRed[warp] = dgc;
     }
     tc_fence_before();
     __syncthreads();
@@ -220,6 +203,34 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     do {
         const bool landed = mbar_wait(&bar_tma, 0, &s_err, 1);
         if (__syncthreads_or(!landed)) break;
+        {   // S (fp32 staging) -> bf16 operand tile; <dS', S> against the dS' tile
+            float dgc = 0.f;
+            for (int e = tid; e < KD * VD / 8; e += kThreads) {
+                const int key = e >> 4, c0 = (e & 15) * 8;
+                const float *src = reinterpret_cast<const float *>(
+                                       smem + (key < 32 ? gStage0 + key * 512 : gStage1 + (key - 32) * 512)) + c0;
+                const float4 a0 = *reinterpret_cast<const float4 *>(src);
+                const float4 a1 = *reinterpret_cast<const float4 *>(src + 4);
+                const float sv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                float dv8[8];
+                unpack8(*kchunk(gDS, 128, key, c0), dv8);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dgc = fmaf(sv[q], dv8[q], dgc);
+                *kchunk(gS, 128, key, c0) = pack8(sv);
+            }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) dgc += __shfl_xor_sync(0xffffffffu, dgc, d);
+            if ((tid & 31) == 0) sRed[warp] = dgc;
+        }
+        __syncthreads();                              // the staging (gT3, gTL, gF) is free
+        // decay table D[r][c] = exp(g_r - g_c) for c <= r (1 above the diagonal) in the T buffer
+        for (int e = tid; e < C * C / 4; e += kThreads) {
+            const int r = e >> 4, c = (e & 15) * 4;
+            const float gr = sG[r];
+            *reinterpret_cast<float4 *>(sT + r * kSolveLD + c) =
+                make_float4(__expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
+                            __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
+        }
         if (len < C) {   // rows past the end: zero K, Q, V and dO (NaN padding enters MMAs raw)
             const uint4 zero = make_uint4(0, 0, 0, 0);
             for (int t = tid; t < 8 * C * 8; t += kThreads) {
@@ -271,7 +282,7 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     *reinterpret_cast<float4 *>(sA + r * kSolveLD + half * 32 + i) =
                         make_float4(br * ap[0], br * ap[1], br * ap[2], br * ap[3]);
-                    *reinterpret_cast<float4 *>(scr + kScrAp + r * C + half * 32 + i) =
+                    *reinterpret_cast<float4 *>(scr + kScrAp + r * kSolveLD + half * 32 + i) =
                         make_float4(ap[0], ap[1], ap[2], ap[3]);
                 }
             } else {
@@ -284,9 +295,9 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         l[e] = (col <= r && r < len) ? p.scale * dec[q * 8 + e] * v[q * 8 + e] : 0.f;
                     }
                     *kchunk(gTL, 128, C + r, half * 32 + q * 8) = pack8(l);
-                    *reinterpret_cast<float4 *>(scr + kScrL + r * C + half * 32 + q * 8) =
+                    *reinterpret_cast<float4 *>(scr + kScrL + r * kSolveLD + half * 32 + q * 8) =
                         make_float4(l[0], l[1], l[2], l[3]);
-                    *reinterpret_cast<float4 *>(scr + kScrL + r * C + half * 32 + q * 8 + 4) =
+                    *reinterpret_cast<float4 *>(scr + kScrL + r * kSolveLD + half * 32 + q * 8 + 4) =
                         make_float4(l[4], l[5], l[6], l[7]);
                 }
             }
@@ -302,8 +313,8 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) t8[e] = c0 + e <= r ? sT[r * kSolveLD + c0 + e] : 0.f;
                 *kchunk(gTL, 128, r, c0) = pack8(t8);
-                *reinterpret_cast<float4 *>(scr + kScrT + r * C + c0) = make_float4(t8[0], t8[1], t8[2], t8[3]);
-                *reinterpret_cast<float4 *>(scr + kScrT + r * C + c0 + 4) = make_float4(t8[4], t8[5], t8[6], t8[7]);
+                *reinterpret_cast<float4 *>(scr + kScrT + r * kSolveLD + c0) = make_float4(t8[0], t8[1], t8[2], t8[3]);
+                *reinterpret_cast<float4 *>(scr + kScrT + r * kSolveLD + c0 + 4) = make_float4(t8[4], t8[5], t8[6], t8[7]);
             }
         }
         to_async();
@@ -521,8 +532,8 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // scratch: dL, dT (as computed, full; the consumer masks them), row sums, <dS', S>
         for (int e = tid; e < C * C / 4; e += kThreads) {
             const int r = e >> 4, c = (e & 15) * 4;
-            *reinterpret_cast<float4 *>(scr + kScrDL + r * C + c) = *reinterpret_cast<const float4 *>(sDL + r * kSolveLD + c);
-            *reinterpret_cast<float4 *>(scr + kScrDT + r * C + c) = *reinterpret_cast<const float4 *>(sDT + r * kSolveLD + c);
+            *reinterpret_cast<float4 *>(scr + kScrDL + r * kSolveLD + c) = *reinterpret_cast<const float4 *>(sDL + r * kSolveLD + c);
+            *reinterpret_cast<float4 *>(scr + kScrDT + r * kSolveLD + c) = *reinterpret_cast<const float4 *>(sDT + r * kSolveLD + c);
         }
         for (int e = tid; e < 4 * C; e += kThreads) scr[kScrRows + e] = (&sRow[0][0])[e];
         if (tid == 0) {
@@ -558,12 +569,14 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __shared__ uint64_t bar_tma, bar_mma;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
-    __shared__ float sG[C], sB[C], sDG[C], sRow[4][C], s_dgc, s_carry;
+    __shared__ __align__(16) float sRows[kScrRowFloats];   // RA, RB, RC, RD, <dS', S>
+    __shared__ float sG[C], sB[C], sDG[C], sPart[4][C], sRed2[2], s_carry;
+    const float *sRA = sRows, *sRB = sRows + C, *sRC = sRows + 2 * C, *sRD = sRows + 3 * C;
 
     if (status_blocks(p.status)) return;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
-    const int lrow = quarter * 32 + (tid & 31);
+    const int lrow = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int j = blockIdx.x, h = blockIdx.y, H = p.H;
     int64_t t0;
@@ -573,120 +586,130 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sbase = smem_u32(smem);
     const float *scr = p.scratch + (size_t)unit * kScrFloats;
 
-    if (tid == 0) {
+    if (tid == 0) {   // K and Q tiles, the five matrices and the row sums of the first kernel
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
         s_err = 0;
         fence_barrier_init();
-        mbar_arrive_expect_tx(&bar_tma, 32768);
+        mbar_arrive_expect_tx(&bar_tma, 32768 + kScrRows * 4 + kScrRowFloats * 4);
         for (int cb = 0; cb < 2; ++cb) {
             tma_load_3d(smem + hKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
             tma_load_3d(smem + hKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
         }
+        bulk_load(fT, scr, kScrRows * 4, &bar_tma);
+        bulk_load(sRows, scr + kScrRows, kScrRowFloats * 4, &bar_tma);
     }
     __syncwarp();
     if (warp == 0) {
         tmem_alloc(&s_tmem, 256);
         tmem_relinquish();
     }
-    for (int e = tid; e < 5 * C * C / 4; e += kThreads) {       // T, A', L, dL, dT
-        const int m = e / (C * C / 4), w = e % (C * C / 4), r = w >> 4, c = (w & 15) * 4;
-        float *dst = fT + m * C * kSolveLD;
-        *reinterpret_cast<float4 *>(dst + r * kSolveLD + c) =
-            *reinterpret_cast<const float4 *>(scr + m * C * C + r * C + c);
-    }
-    for (int e = tid; e < 4 * C; e += kThreads) (&sRow[0][0])[e] = scr[kScrRows + e];
-    if (tid == 0) s_dgc = scr[kScrRows + 4 * C];
-    chunk_gates(p, t0, len, h, sG, sB, &s_carry);        // (its barriers also publish the loads)
+    chunk_gates(p, t0, len, h, sG, sB, &s_carry);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    // ---- dA = -T^T (dT T^T), strictly lower; dT counts only on and below the diagonal.
-    // X = dT T^T: X[r][m] = sum_{i <= r} dT[r][i] T[m][i]  (T[m][i] = 0 for i > m; 1 x 4 strips)
-    for (int s = tid; s < C * 16; s += kThreads) {
-        const int r = s & 63, m0 = (s >> 6) * 4;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = 0; i <= r; ++i) {
-            const float dt = fDT[r * kSolveLD + i];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = fmaf(dt, fT[(m0 + e) * kSolveLD + i], acc[e]);
-        }
-        *reinterpret_cast<float4 *>(fX + r * kSolveLD + m0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    }
-    __syncthreads();
-    // dA[r][i] = -sum_{m >= r} T[m][r] X[m][i] for i < r, else 0  (over dT, which is consumed)
-    for (int s = tid; s < C * 16; s += kThreads) {
-        const int r = s & 63, i0 = (s >> 6) * 4;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (i0 < r) {
-            for (int m = r; m < C; ++m) {
-                const float t = fT[m * kSolveLD + r];
-                const float4 x = *reinterpret_cast<const float4 *>(fX + m * kSolveLD + i0);
-                acc[0] = fmaf(-t, x.x, acc[0]);
-                acc[1] = fmaf(-t, x.y, acc[1]);
-                acc[2] = fmaf(-t, x.z, acc[2]);
-                acc[3] = fmaf(-t, x.w, acc[3]);
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (i0 + e >= r) acc[e] = 0.f;
-        *reinterpret_cast<float4 *>(fDT + r * kSolveLD + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    }
-    __syncthreads();
-    const float *fDA = fDT;
-    const float gC = sG[C - 1];
-    // ---- gate and beta gradients, one thread per row, fixed order
-    if (tid < C) {
-        const int r = tid;
-        const float gr = sG[r], Gr = __expf(gr), fr = r < len ? __expf(gC - gr) : 0.f;
-        float dgr = p.scale * Gr * sRow[0][r];
-        for (int i = 0; i <= r; ++i) dgr = fmaf(fDL[r * kSolveLD + i], fL[r * kSolveLD + i], dgr);
-        for (int r2 = r; r2 < C; ++r2) dgr = fmaf(-fDL[r2 * kSolveLD + r], fL[r2 * kSolveLD + r], dgr);
-        float da_row = 0.f;
-        for (int i = 0; i < r; ++i) da_row = fmaf(fDA[r * kSolveLD + i], fAp[r * kSolveLD + i], da_row);
-        dgr = fmaf(sB[r], da_row, dgr);
-        for (int r2 = r + 1; r2 < C; ++r2)
-            dgr = fmaf(-fDA[r2 * kSolveLD + r] * sB[r2], fAp[r2 * kSolveLD + r], dgr);
-        dgr -= sB[r] * Gr * sRow[2][r];
-        dgr -= fr * sRow[3][r];
-        sDG[r] = dgr;
-        if (r < len) p.dbeta[(t0 + r) * H + h] = sRow[1][r] - Gr * sRow[2][r] + da_row;
-    }
-    // ---- P = scale D o dL (i <= r) -> rows 64..127, M = beta_r D o dA (i < r) -> rows 0..63
-    // of the [M; P] operand (bf16, K-major over i)
-    {
-        const int r = tid >> 2;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-            const int c0 = ((tid & 3) * 2 + qq) * 8;
-            float m8[8], p8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = c0 + e;
-                const float dec = i <= r ? __expf(sG[r] - sG[i]) : 0.f;
-                p8[e] = i <= r ? p.scale * dec * fDL[r * kSolveLD + i] : 0.f;
-                m8[e] = i < r ? sB[r] * dec * fDA[r * kSolveLD + i] : 0.f;
-            }
-            *reinterpret_cast<uint4 *>(smem + hMP + kmaj16(128, r, c0)) = pack8(m8);
-            *reinterpret_cast<uint4 *>(smem + hMP + kmaj16(128, C + r, c0)) = pack8(p8);
-        }
-    }
-    __syncthreads();
-    if (tid == 0) {   // gamma_c: the Ktil factors and Gamma_c; dg = reverse cumsum of dgamma
-        float dgc = s_dgc * __expf(gC);
-        for (int i = 0; i < C; ++i) dgc = fmaf(i < len ? __expf(gC - sG[i]) : 0.f, sRow[3][i], dgc);
-        sDG[C - 1] += dgc;
-        float acc = 0.f;
-        for (int r = C - 1; r >= 0; --r) {
-            acc += sDG[r];
-            if (r < len) p.dg[(t0 + r) * H + h] = acc;
-        }
-    }
     do {
         const bool landed = mbar_wait(&bar_tma, 0, &s_err, 1);
         if (__syncthreads_or(!landed)) break;
+        // ---- dA = -T^T (dT T^T), strictly lower; dT counts only on and below the diagonal.
+        // X = dT T^T: X[r][m] = sum_{i <= r} dT[r][i] T[m][i]  (T[m][i] = 0 for i > m; 1 x 4 strips)
+        for (int sidx = tid; sidx < C * 16; sidx += kThreads) {
+            const int r = sidx & 63, m0 = (sidx >> 6) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i <= r; ++i) {
+                const float dt = fDT[r * kSolveLD + i];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = fmaf(dt, fT[(m0 + e) * kSolveLD + i], acc[e]);
+            }
+            *reinterpret_cast<float4 *>(fX + r * kSolveLD + m0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        }
+        __syncthreads();
+        // dA[r][i] = -sum_{m >= r} T[m][r] X[m][i] for i < r, else 0  (over dT, which is consumed)
+        for (int sidx = tid; sidx < C * 16; sidx += kThreads) {
+            const int r = sidx & 63, i0 = (sidx >> 6) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (i0 < r) {
+                for (int m = r; m < C; ++m) {
+                    const float t = fT[m * kSolveLD + r];
+                    const float4 x = *reinterpret_cast<const float4 *>(fX + m * kSolveLD + i0);
+                    acc[0] = fmaf(-t, x.x, acc[0]);
+                    acc[1] = fmaf(-t, x.y, acc[1]);
+                    acc[2] = fmaf(-t, x.z, acc[2]);
+                    acc[3] = fmaf(-t, x.w, acc[3]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (i0 + e >= r) acc[e] = 0.f;
+            *reinterpret_cast<float4 *>(fDT + r * kSolveLD + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        }
+        __syncthreads();
+        const float *fDA = fDT;
+        const float gC = sG[C - 1];
+        // ---- gate and beta gradients.  Four sums per row, one warp pair each (rows
+        // 32 (w & 1) + lane): the row and column sums of dL o L and of dA o A' (beta-weighted
+        // columns); dL is zero-padded by L, dA and A' are strictly lower.
+        {
+            const int part = warp >> 1, r = (warp & 1) * 32 + lane;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (part == 0 || part == 2) {
+                const float *x = (part == 0 ? fDL : fDA) + r * kSolveLD;
+                const float *y = (part == 0 ? fL : fAp) + r * kSolveLD;
+#pragma unroll 4
+                for (int i = 0; i < C; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(x + i);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(y + i);
+                    acc[0] = fmaf(a4.x, b4.x, acc[0]);
+                    acc[1] = fmaf(a4.y, b4.y, acc[1]);
+                    acc[2] = fmaf(a4.z, b4.z, acc[2]);
+                    acc[3] = fmaf(a4.w, b4.w, acc[3]);
+                }
+            } else if (part == 1) {
+#pragma unroll 4
+                for (int r2 = 0; r2 < C; ++r2)
+                    acc[r2 & 3] = fmaf(fDL[r2 * kSolveLD + r], fL[r2 * kSolveLD + r], acc[r2 & 3]);
+            } else {
+#pragma unroll 4
+                for (int r2 = 0; r2 < C; ++r2)
+                    acc[r2 & 3] = fmaf(fDA[r2 * kSolveLD + r] * sB[r2], fAp[r2 * kSolveLD + r], acc[r2 & 3]);
+            }
+            sPart[part][r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        __syncthreads();
+        if (tid < C) {   // dgamma and dbeta of row tid
+            const int r = tid;
+            const float Gr = __expf(sG[r]);
+            const float fr = r < len ? __expf(gC - sG[r]) : 0.f;
+            const float da_row = sPart[2][r];
+            float frd = fr * sRD[r];
+            sDG[r] = p.scale * Gr * sRA[r] + (sPart[0][r] - sPart[1][r]) + sB[r] * da_row - sPart[3][r] -
+                     sB[r] * Gr * sRC[r] - frd;
+            if (r < len) p.dbeta[(t0 + r) * H + h] = sRB[r] - Gr * sRC[r] + da_row;
+            // the last row's gamma also carries the Ktil factors of every row: their sum
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) frd += __shfl_xor_sync(0xffffffffu, frd, d);
+            if (lane == 0) sRed2[warp] = frd;
+        }
+        // ---- P = scale D o dL (i <= r) -> rows 64..127, M = beta_r D o dA (i < r) -> rows 0..63
+        // of the [M; P] operand (bf16, K-major over i)
+        {
+            const int r = tid >> 2;
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+                const int c0 = ((tid & 3) * 2 + qq) * 8;
+                float m8[8], p8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = c0 + e;
+                    const float dec = i <= r ? __expf(sG[r] - sG[i]) : 0.f;
+                    p8[e] = i <= r ? p.scale * dec * fDL[r * kSolveLD + i] : 0.f;
+                    m8[e] = i < r ? sB[r] * dec * fDA[r * kSolveLD + i] : 0.f;
+                }
+                *reinterpret_cast<uint4 *>(smem + hMP + kmaj16(128, r, c0)) = pack8(m8);
+                *reinterpret_cast<uint4 *>(smem + hMP + kmaj16(128, C + r, c0)) = pack8(p8);
+            }
+        }
         if (len < C) {   // K and Q rows past the end (NaN padding) enter the MMAs raw
             const uint4 zero = make_uint4(0, 0, 0, 0);
             for (int t = tid; t < 4 * C * 8; t += kThreads) {
@@ -700,6 +723,19 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        {   // dg = reverse in-chunk cumsum of dgamma (thread t: row 63 - t), gamma_c at the last row
+            float x = 0.f;
+            if (tid < C) {
+                x = sDG[C - 1 - tid];
+                if (tid == 0) x += sRows[4 * C] * __expf(gC) + (sRed2[0] + sRed2[1]);
+                x = warp_scan(x);
+                if (tid == 31) s_carry = x;
+            }
+            __syncthreads();
+            if (tid >= 32 && tid < C) x += s_carry;
+            const int r = C - 1 - tid;
+            if (tid < C && r < len) p.dg[(t0 + r) * H + h] = x;
+        }
         // ---- [M; P] K -> cols 0..127 (M K in lanes 0..63, P K in lanes 64..127);
         //      M^T K + P^T Q -> cols 128..255 (lanes 0..63)
         if (tid == 0) {
@@ -785,7 +821,7 @@ cudaError_t launch_bwd_grad_tc(const BwdParams &p, float *scratch, cudaStream_t 
     gp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
     gp.v = static_cast<const __nv_bfloat16 *>(p.v);
     gp.h = p.h;
-    gp.dh = p.dh;
+    gp.dh = reinterpret_cast<const uint8_t *>(p.dh);
     gp.dq = p.dq;
     gp.dk = p.dk;
     gp.dv = p.dv;

@@ -31,7 +31,8 @@ struct SweepTParams {
     const int32_t *cu, *chunk_offsets;
     const float *dht;
     const uint8_t *ws;          // transition records + Gamma_c slots
-    float *dh, *dh0;            // dS' per chunk [nt_max, H, K, V]; dh0 [n_max, H, K, V]
+    uint8_t *dh;                // dS' per chunk: bf16 tiles of 32 KiB (see below)
+    float *dh0;                 // [n_max, H, K, V]
     int32_t *status;
     int64_t t_max, nt_max;
     int32_t n_max, H;
@@ -186,11 +187,12 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
             const int64_t rem = eos - bos - (int64_t)ic * C;
             const int len = (int)(rem < C ? rem : C);
             uint8_t *stage = smem + st * Lay::kStage;
-            {   // the gradient w.r.t. the state after chunk ic
-                float *dst = p.dh + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
+            {   // the gradient w.r.t. the state after chunk ic, as the chunk-gradient kernel's
+                // bf16 operand tile: key rows, two 64-column blocks, 128-byte swizzle
+                uint8_t *dst = p.dh + ((row0 + ic) * H + h) * (int64_t)kDsTileBytes;
 #pragma unroll
-                for (int j = 0; j < HV; j += 4)
-                    *reinterpret_cast<float4 *>(dst + j) = make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
+                for (int j = 0; j < HV; j += 8)
+                    *reinterpret_cast<uint4 *>(dst + kmaj16(128, row, v0 + c0 + j)) = pack8(dS + j);
             }
             mbar_wait(&bar_tma[st], (k / NS) & 1, &s_err, 3);
             if (len < C) {   // dO rows past the end may hold NaN padding; they enter the MMA raw
@@ -269,7 +271,7 @@ cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *ws, cudaStream
     sp.chunk_offsets = p.chunk_offsets;
     sp.dht = p.dht;
     sp.ws = ws;
-    sp.dh = p.dh;
+    sp.dh = reinterpret_cast<uint8_t *>(p.dh);
     sp.dh0 = p.dh0;
     sp.status = p.dev_status;
     sp.t_max = p.t_max;

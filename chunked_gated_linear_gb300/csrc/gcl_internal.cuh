@@ -46,7 +46,8 @@ struct BwdParams {
     const float *dht;
     const int32_t *cu_seqlens, *chunk_indices, *chunk_offsets;
     const float *h;       // states before every chunk [nt_max, H, K, V]
-    float *dh;            // state gradients after every chunk [nt_max, H, K, V] (scratch)
+    float *dh;            // state gradients after every chunk: fp32 [nt_max, H, K, V] on the
+                          // CUDA-core path, bf16 tiles of tr::kDsTileBytes on the tensor cores
     float *dq, *dk, *dv, *dg, *dbeta, *dh0;
     int32_t *dev_status;
     int64_t t_max, nt_max;

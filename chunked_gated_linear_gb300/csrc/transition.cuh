@@ -29,6 +29,9 @@ constexpr size_t kBBytes = (size_t)KD * VD * 2;      // 32 KiB
 constexpr size_t kZBytes = (size_t)C * VD * 2;       // 16 KiB
 constexpr size_t kUnitBytes = kYNBytes + kBBytes + kZBytes;
 constexpr size_t kGBytes = 512;                      // Gamma_c slot (128 floats)
+// The backward sweep hands dS' of every chunk to the chunk-gradient kernels as a bf16 tile:
+// 128 key rows x 128 value columns in two 64-column blocks, 128-byte swizzle (kmaj16 below).
+constexpr size_t kDsTileBytes = (size_t)KD * VD * 2;
 static_assert(kUnitBytes % 1024 == 0, "records start on 1 KiB boundaries");
 
 // Address of the Gamma_c slot of record `unit` in a workspace of nt_max * H records.
