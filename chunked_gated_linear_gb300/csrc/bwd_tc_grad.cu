@@ -549,24 +549,32 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ============================================================================ grad2
-constexpr uint32_t hKQ = 0;          // [K; Q] tiles (TMA)                        32 KiB
-constexpr uint32_t hMP = 32768;      // [M; P] bf16: 128 rows x 64 columns         16 KiB
-constexpr uint32_t hPad = 49152;     // 8 KiB read as junk rows by the MN-major P^T view
-constexpr uint32_t hF = 57344;       // fp32 T, A', L, dL, dT (dA), X [64][kSolveLD]
-static_assert(hF == hPad + 8192, "the P^T view's second atom stays inside the allocation");
-constexpr uint32_t h2End = hF + 6 * C * kSolveLD * 4;
+// Two CTAs per SM (104 KiB of shared memory each, at most 128 registers per thread), so one
+// CTA's copies overlap the other's arithmetic.  Shared memory, in the order of use:
+//   hMP  [M; P] bf16, 128 rows x 64 columns (the MN-major P^T view reads 8 KiB past it, into
+//        the T buffer: rows of junk that land in TMEM lanes nobody reads)
+//   hF   fp32 T, A', L (later X = dT T^T), dL, dT (later dA), [64][kSolveLD] each (one bulk
+//        copy of the scratch record); the K and Q tiles arrive late, over T and A'.
+constexpr uint32_t hMP = 0;
+constexpr uint32_t hF = 16384;
+constexpr uint32_t hKQ = hF;                  // [K; Q] tiles (TMA), once T and A' are consumed
+constexpr uint32_t h2End = hF + 5 * C * kSolveLD * 4;
 constexpr int kGrad2Smem = h2End + 1024;
-static_assert(kGrad2Smem <= 232448, "grad2 shared memory");
+static_assert(hF % 1024 == 0 && hKQ + 32768 <= hF + 3 * C * kSolveLD * 4, "K, Q over T, A', L");
+static_assert(hMP + 16384 + 8192 <= h2End, "the P^T view's second atom stays inside the allocation");
+static_assert(2 * (kGrad2Smem + 4096) <= 233472, "two CTAs per SM");
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 GradParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     float *fT = reinterpret_cast<float *>(smem + hF);
     float *fAp = fT + C * kSolveLD, *fL = fAp + C * kSolveLD, *fDL = fL + C * kSolveLD;
-    float *fDT = fDL + C * kSolveLD, *fX = fDT + C * kSolveLD;
-    __shared__ uint64_t bar_tma, bar_mma;
+    float *fDT = fDL + C * kSolveLD;
+    float *fX = fL;                           // X replaces L once the dL o L sums are taken
+    const float *fDA = fDT;                   // dA replaces dT
+    __shared__ uint64_t bar_in, bar_kq, bar_mma;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
     __shared__ __align__(16) float sRows[kScrRowFloats];   // RA, RB, RC, RD, <dS', S>
@@ -586,18 +594,15 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sbase = smem_u32(smem);
     const float *scr = p.scratch + (size_t)unit * kScrFloats;
 
-    if (tid == 0) {   // K and Q tiles, the five matrices and the row sums of the first kernel
-        mbar_init(&bar_tma, 1);
+    if (tid == 0) {   // the five matrices and the row sums of the first kernel
+        mbar_init(&bar_in, 1);
+        mbar_init(&bar_kq, 1);
         mbar_init(&bar_mma, 1);
         s_err = 0;
         fence_barrier_init();
-        mbar_arrive_expect_tx(&bar_tma, 32768 + kScrRows * 4 + kScrRowFloats * 4);
-        for (int cb = 0; cb < 2; ++cb) {
-            tma_load_3d(smem + hKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_tma);
-            tma_load_3d(smem + hKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_tma);
-        }
-        bulk_load(fT, scr, kScrRows * 4, &bar_tma);
-        bulk_load(sRows, scr + kScrRows, kScrRowFloats * 4, &bar_tma);
+        mbar_arrive_expect_tx(&bar_in, kScrRows * 4 + kScrRowFloats * 4);
+        bulk_load(fT, scr, kScrRows * 4, &bar_in);
+        bulk_load(sRows, scr + kScrRows, kScrRowFloats * 4, &bar_in);
     }
     __syncwarp();
     if (warp == 0) {
@@ -609,9 +614,40 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    const float gC = sG[C - 1];
+    // row (parts 0, 2) and column (parts 1, 3) sums over a [64][kSolveLD] pair, rows
+    // 32 (w & 1) + lane for the warp pair of the part; column sums weight row r2 by wc[r2]
+    auto row_sum = [&](const float *x, const float *y, int r) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int i = 0; i < C; i += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(x + r * kSolveLD + i);
+            const float4 b4 = *reinterpret_cast<const float4 *>(y + r * kSolveLD + i);
+            acc[0] = fmaf(a4.x, b4.x, acc[0]);
+            acc[1] = fmaf(a4.y, b4.y, acc[1]);
+            acc[2] = fmaf(a4.z, b4.z, acc[2]);
+            acc[3] = fmaf(a4.w, b4.w, acc[3]);
+        }
+        return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    };
+    auto col_sum = [&](const float *x, const float *y, const float *wc, int r) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int r2 = 0; r2 < C; ++r2)
+            acc[r2 & 3] = fmaf(x[r2 * kSolveLD + r] * (wc ? wc[r2] : 1.f), y[r2 * kSolveLD + r], acc[r2 & 3]);
+        return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    };
     do {
-        const bool landed = mbar_wait(&bar_tma, 0, &s_err, 1);
+        const bool landed = mbar_wait(&bar_in, 0, &s_err, 1);
         if (__syncthreads_or(!landed)) break;
+        // ---- gate sums of dL o L (L is zero above the diagonal and past the end):
+        // warps 0..3 the row sums, warps 4..7 the column sums
+        {
+            const int r = (warp & 1) * 32 + lane;
+            if (warp < 2) sPart[0][r] = row_sum(fDL, fL, r);
+            else if (warp < 4) sPart[1][r] = col_sum(fDL, fL, nullptr, r);
+        }
+        __syncthreads();
         // ---- dA = -T^T (dT T^T), strictly lower; dT counts only on and below the diagonal.
         // X = dT T^T: X[r][m] = sum_{i <= r} dT[r][i] T[m][i]  (T[m][i] = 0 for i > m; 1 x 4 strips)
         for (int sidx = tid; sidx < C * 16; sidx += kThreads) {
@@ -645,38 +681,21 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             *reinterpret_cast<float4 *>(fDT + r * kSolveLD + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         __syncthreads();
-        const float *fDA = fDT;
-        const float gC = sG[C - 1];
-        // ---- gate and beta gradients.  Four sums per row, one warp pair each (rows
-        // 32 (w & 1) + lane): the row and column sums of dL o L and of dA o A' (beta-weighted
-        // columns); dL is zero-padded by L, dA and A' are strictly lower.
+        // ---- gate sums of dA o A' (both strictly lower): row sums, beta-weighted column sums
         {
-            const int part = warp >> 1, r = (warp & 1) * 32 + lane;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (part == 0 || part == 2) {
-                const float *x = (part == 0 ? fDL : fDA) + r * kSolveLD;
-                const float *y = (part == 0 ? fL : fAp) + r * kSolveLD;
-#pragma unroll 4
-                for (int i = 0; i < C; i += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(x + i);
-                    const float4 b4 = *reinterpret_cast<const float4 *>(y + i);
-                    acc[0] = fmaf(a4.x, b4.x, acc[0]);
-                    acc[1] = fmaf(a4.y, b4.y, acc[1]);
-                    acc[2] = fmaf(a4.z, b4.z, acc[2]);
-                    acc[3] = fmaf(a4.w, b4.w, acc[3]);
-                }
-            } else if (part == 1) {
-#pragma unroll 4
-                for (int r2 = 0; r2 < C; ++r2)
-                    acc[r2 & 3] = fmaf(fDL[r2 * kSolveLD + r], fL[r2 * kSolveLD + r], acc[r2 & 3]);
-            } else {
-#pragma unroll 4
-                for (int r2 = 0; r2 < C; ++r2)
-                    acc[r2 & 3] = fmaf(fDA[r2 * kSolveLD + r] * sB[r2], fAp[r2 * kSolveLD + r], acc[r2 & 3]);
-            }
-            sPart[part][r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            const int r = (warp & 1) * 32 + lane;
+            if (warp < 2) sPart[2][r] = row_sum(fDA, fAp, r);
+            else if (warp < 4) sPart[3][r] = col_sum(fDA, fAp, sB, r);
         }
         __syncthreads();
+        if (tid == 0) {   // T, A' and L are consumed: the K and Q tiles of the last MMA round
+            fence_async_smem();
+            mbar_arrive_expect_tx(&bar_kq, 32768);
+            for (int cb = 0; cb < 2; ++cb) {
+                tma_load_3d(smem + hKQ + cb * 16384, &tm_k, cb * 64, h, (int)t0, &bar_kq);
+                tma_load_3d(smem + hKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, (int)t0, &bar_kq);
+            }
+        }
         if (tid < C) {   // dgamma and dbeta of row tid
             const int r = tid;
             const float Gr = __expf(sG[r]);
@@ -710,19 +729,7 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 *reinterpret_cast<uint4 *>(smem + hMP + kmaj16(128, C + r, c0)) = pack8(p8);
             }
         }
-        if (len < C) {   // K and Q rows past the end (NaN padding) enter the MMAs raw
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            for (int t = tid; t < 4 * C * 8; t += kThreads) {
-                const int r = (t >> 3) & 63, blk = t >> 9;
-                if (r >= len)
-                    *reinterpret_cast<uint4 *>(smem + hKQ + (blk & 1) * 16384 + (blk >> 1) * 8192 + r * 128 +
-                                               (t & 7) * 16) = zero;
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
         __syncthreads();
-        tc_fence_after();
         {   // dg = reverse in-chunk cumsum of dgamma (thread t: row 63 - t), gamma_c at the last row
             float x = 0.f;
             if (tid < C) {
@@ -736,6 +743,23 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int r = C - 1 - tid;
             if (tid < C && r < len) p.dg[(t0 + r) * H + h] = x;
         }
+        {
+            const bool kq = mbar_wait(&bar_kq, 0, &s_err, 3);
+            if (__syncthreads_or(!kq)) break;
+        }
+        if (len < C) {   // K and Q rows past the end (NaN padding) enter the MMAs raw
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            for (int t = tid; t < 4 * C * 8; t += kThreads) {
+                const int r = (t >> 3) & 63, blk = t >> 9;
+                if (r >= len)
+                    *reinterpret_cast<uint4 *>(smem + hKQ + (blk & 1) * 16384 + (blk >> 1) * 8192 + r * 128 +
+                                               (t & 7) * 16) = zero;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
         // ---- [M; P] K -> cols 0..127 (M K in lanes 0..63, P K in lanes 64..127);
         //      M^T K + P^T Q -> cols 128..255 (lanes 0..63)
         if (tid == 0) {
@@ -757,34 +781,25 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const bool ok = mbar_wait(&bar_mma, 0, &s_err, 2);
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
-        float x[64], y[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + half * 64 + q * 16, x + q * 16);
-        tmem_ld_wait();
-        if (lrow < C) {   // dk += M K + M^T K + P^T Q
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, y + q * 16);
+        // dk += M K + M^T K + P^T Q (lanes 0..63), dq += P K (lanes 64..127), 16 columns at a time
+        const bool isk = lrow < C;
+        const int r = isk ? lrow : lrow - C;
+        float *grow = (isk ? p.dk : p.dq) + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float x[16], y[16];
+            tmem_ld16(tmem + lane_off + half * 64 + q * 16, x);
+            if (isk) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, y);
             tmem_ld_wait();
-            const int r = lrow;
             if (r < len) {
-                float *dkrow = p.dk + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
 #pragma unroll
-                for (int q = 0; q < 64; q += 4) {
-                    float4 d = *reinterpret_cast<float4 *>(dkrow + q);
-                    d.x += x[q] + y[q]; d.y += x[q + 1] + y[q + 1];
-                    d.z += x[q + 2] + y[q + 2]; d.w += x[q + 3] + y[q + 3];
-                    *reinterpret_cast<float4 *>(dkrow + q) = d;
-                }
-            }
-        } else {          // dq += P K
-            const int r = lrow - C;
-            if (r < len) {
-                float *dqrow = p.dq + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
-#pragma unroll
-                for (int q = 0; q < 64; q += 4) {
-                    float4 d = *reinterpret_cast<float4 *>(dqrow + q);
-                    d.x += x[q]; d.y += x[q + 1]; d.z += x[q + 2]; d.w += x[q + 3];
-                    *reinterpret_cast<float4 *>(dqrow + q) = d;
+                for (int e = 0; e < 16; e += 4) {
+                    float4 d = *reinterpret_cast<float4 *>(grow + q * 16 + e);
+                    d.x += x[e] + (isk ? y[e] : 0.f);
+                    d.y += x[e + 1] + (isk ? y[e + 1] : 0.f);
+                    d.z += x[e + 2] + (isk ? y[e + 2] : 0.f);
+                    d.w += x[e + 3] + (isk ? y[e + 3] : 0.f);
+                    *reinterpret_cast<float4 *>(grow + q * 16 + e) = d;
                 }
             }
         }
