@@ -78,10 +78,12 @@ def load_library(path: str = LIB_PATH):
     for fn in ("gcl_fwd_workspace_bytes", "gcl_fwd_workspace_min_bytes", "gcl_kda_fwd_workspace_bytes"):
         getattr(lib, fn).restype = ctypes.c_size_t
         getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs)]
-    lib.gdn_chunk_bwd.restype = ctypes.c_int
-    lib.gdn_chunk_bwd.argtypes = [ctypes.POINTER(BwdArgs), vp]
-    lib.gcl_bwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.gcl_bwd_workspace_bytes.argtypes = [ctypes.POINTER(BwdArgs)]
+    for fn in ("gdn_chunk_bwd", "kda_chunk_bwd"):
+        getattr(lib, fn).restype = ctypes.c_int
+        getattr(lib, fn).argtypes = [ctypes.POINTER(BwdArgs), vp]
+    for fn in ("gcl_bwd_workspace_bytes", "gcl_kda_bwd_workspace_bytes"):
+        getattr(lib, fn).restype = ctypes.c_size_t
+        getattr(lib, fn).argtypes = [ctypes.POINTER(BwdArgs)]
     return lib
 
 
@@ -220,3 +222,14 @@ def bwd_workspace_bytes(*args, **kw) -> int:
 def gdn_chunk_bwd(*args, stream=None, **kw):
     a = bwd_args(*args, **kw)
     _check("gdn_chunk_bwd", lib().gdn_chunk_bwd(ctypes.byref(a), _stream(stream)))
+
+
+def kda_bwd_workspace_bytes(*args, **kw) -> int:
+    a = bwd_args(*args, **kw)
+    return int(lib().gcl_kda_bwd_workspace_bytes(ctypes.byref(a)))
+
+
+def kda_chunk_bwd(*args, stream=None, **kw):
+    """The KDA backward; dg has the shape of g, [T, H, K]."""
+    a = bwd_args(*args, **kw)
+    _check("kda_chunk_bwd", lib().kda_chunk_bwd(ctypes.byref(a), _stream(stream)))

@@ -1,4 +1,4 @@
-// bwd_simt.cu -- GDN chunk backward on the CUDA cores (fp32 arithmetic).
+// bwd_simt.cu -- GDN and KDA chunk backward on the CUDA cores (fp32 arithmetic).
 //
 // FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths
 // on Ascend NPUs", section "Step 3": the backward path covers recomputation,
@@ -426,6 +426,278 @@ chunk_grad_kernel(BwdParams p) {
     }
 }
 
+// ---------------------------------------------------------------- KDA chunk gradients
+// The decay is a vector over key channels, gamma[r][c].  With Kp = K o exp(gamma),
+// Kb = K o exp(gamma_c - gamma), R = diag(beta)(V - Kp S), E = T R:
+//   dE = L^T dO + Kb dS',   dR = T^T dE,   dv = diag(beta) dR,   dT = dE R^T,   dL = dO E^T,
+//   dA = -T^T dT T^T (strictly lower),   Y1 = dR S^T,   Y2 = dO S^T,   Y3 = E dS'^T,
+// and with D[r][i][c] = exp(gamma[r][c] - gamma[i][c]) the sums over the chunk
+//   PL[r][c] = sum_{i<=r} dL[r][i] k[i][c] D[r][i][c],   PA[r][c] = sum_{i<r} dA[r][i] k[i][c] D[r][i][c],
+//   QL[i][c] = sum_{r>=i} dL[r][i] q[r][c] D[r][i][c],   QA[i][c] = sum_{r>i} beta_r dA[r][i] k[r][c] D[r][i][c],
+// give
+//   dq = scale (exp(gamma) o Y2 + PL),
+//   dk = -beta exp(gamma) o Y1 + exp(gamma_c - gamma) o Y3 + beta PA + scale QL + QA,
+//   dgamma = q o dq + k o (-beta exp(gamma) o Y1 - exp(gamma_c - gamma) o Y3 + beta PA - scale QL - QA),
+//   dbeta = sum_v dR o (V - Kp S) + sum_i dA o A',
+// and the last row's gamma (gamma_c) adds exp(gamma_c) <dS', S> (per channel) and
+// sum_r k exp(gamma_c - gamma) o Y3 to every row of dg = reverse in-chunk cumsum of dgamma.
+// Exponentials of differences of gammas only, so nothing overflows for gates <= 0.
+template <int K>
+struct GradKdaLayout {
+    static constexpr int LK = K + 1, LV = kVS + 1;
+    static constexpr int oQ = 0, oK = oQ + C * LK, oG = oK + C * LK;
+    static constexpr int oT = oG + C * LK, oL = oT + C * kLC, oDL = oL + C * kLC, oDT = oDL + C * kLC;
+    static constexpr int oB = oDT + C * kLC, oGC = oB + C, oSS = oGC + K, oRB = oSS + K, oRC = oRB + C;
+    static constexpr int oFree = oRC + C;
+    static constexpr int oS = oFree, oDS = oS + K * LV;
+    static constexpr int oV = oDS + K * LV, oDO = oV + C * LV, oKS = oDO + C * LV, oR = oKS + C * LV;
+    static constexpr int oE = oR + C * LV, oDE = oE + C * LV, oDR = oDE + C * LV, oX2 = oDR + C * LV;
+    static constexpr int oFreeEnd = oX2 + C * LV;
+    static_assert(oFreeEnd - oFree >= 2 * C * kLC, "slice region reused for X and A'");
+    static_assert(oFree - oT >= 2 * C * LK, "T, L, dL, dT reused for dgamma and the gamma_c terms");
+    static constexpr size_t bytes = sizeof(float) * oFreeEnd;
+    static_assert(bytes <= 232448, "one CTA per SM");
+};
+
+template <typename Tin, int K>
+__global__ void __launch_bounds__(kGradThreads)
+chunk_grad_kda_kernel(BwdParams p) {
+    using Lay = GradKdaLayout<K>;
+    extern __shared__ float sm[];
+    constexpr int LK = Lay::LK, LV = Lay::LV;
+    constexpr int CPT = K / 8;   // (row, channel) pairs owned per thread
+    float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sG = sm + Lay::oG;
+    float *sT = sm + Lay::oT, *sL = sm + Lay::oL, *sDL = sm + Lay::oDL, *sDT = sm + Lay::oDT;
+    float *sB = sm + Lay::oB, *sGC = sm + Lay::oGC, *sSS = sm + Lay::oSS;
+    float *sRB = sm + Lay::oRB, *sRC = sm + Lay::oRC;
+    float *sS = sm + Lay::oS, *sDS = sm + Lay::oDS, *sV = sm + Lay::oV, *sDO = sm + Lay::oDO;
+    float *sKS = sm + Lay::oKS, *sR = sm + Lay::oR, *sE = sm + Lay::oE, *sDE = sm + Lay::oDE;
+    float *sDR = sm + Lay::oDR, *sX2 = sm + Lay::oX2;
+    float *sA = sm + Lay::oFree;              // A during the Map; later X = dT T^T
+    float *sAp = sm + Lay::oFree + C * kLC;   // A' at the end
+    float *sKp = sQ, *sKb = sG;               // in place of Q and gamma during the slice loop
+    float *sDGm = sT, *sW3 = sT + C * LK;     // dgamma and the gamma_c terms at the end
+
+    if (status_blocks(p.dev_status)) return;
+    const int n = p.chunk_indices[2 * blockIdx.x];
+    if (n < 0) return;                         // sentinel row: nothing to do
+    if (n >= p.n_max) {
+        if (threadIdx.x == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int ic = p.chunk_indices[2 * blockIdx.x + 1];
+    const int tid = threadIdx.x, h = blockIdx.y;
+    const int H = p.H, V = p.V;
+    const int64_t bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+    const int64_t t0 = bos + (int64_t)ic * C;
+    if (bos < 0 || eos < bos || eos > p.t_max || t0 >= eos) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int len = (int)(eos - t0 < C ? eos - t0 : C);
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    const Tin *beta = static_cast<const Tin *>(p.beta);
+    const Tin *d_o = static_cast<const Tin *>(p.d_o);
+    const int64_t KV = (int64_t)K * V;
+    const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+    if (row < 0 || row >= p.nt_max || ic < 0) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const float *Sg = p.h + (row * H + h) * KV;
+    const float *dSg = p.dh + (row * H + h) * KV;
+
+    // ---- Map recompute
+    simt_load_chunk<kKDA, Tin, K, kGradThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    __syncthreads();
+    simt_gate_cumsum<kKDA, K, kGradThreads>(sG);
+    __syncthreads();
+    simt_intra<kKDA, K, kGradThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    for (int e = tid; e < C * kLC; e += kGradThreads) { sDL[e] = 0.f; sDT[e] = 0.f; }
+    for (int r = tid; r < C; r += kGradThreads) { sRB[r] = 0.f; sRC[r] = 0.f; }
+    for (int c = tid; c < K; c += kGradThreads) { sSS[c] = 0.f; sGC[c] = sG[(C - 1) * LK + c]; }
+    __syncthreads();
+    simt_solve<kGradThreads>(sA, sT);
+    // Kp and Kb in place of Q and gamma (both are reloaded after the slice loop)
+    for (int e = tid; e < C * K; e += kGradThreads) {
+        const int r = e / K, c = e % K;
+        const float gm = sG[r * LK + c], kv = sK[r * LK + c];
+        sKp[r * LK + c] = kv * expf(gm);
+        sKb[r * LK + c] = kv * expf(sGC[c] - gm);
+    }
+    const int my_r = tid / 8, my_c0 = tid % 8;    // owner of (row, channel) partials
+    float y1[CPT], y2[CPT], y3[CPT];
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) { y1[m] = 0.f; y2[m] = 0.f; y3[m] = 0.f; }
+
+    for (int s0 = 0; s0 < V; s0 += kVS) {
+        __syncthreads();
+        for (int e = tid; e < K * kVS; e += kGradThreads) {
+            const int c = e / kVS, j = e % kVS;
+            sS[c * LV + j] = Sg[(int64_t)c * V + s0 + j];
+            sDS[c * LV + j] = dSg[(int64_t)c * V + s0 + j];
+        }
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int r = e / kVS, j = e % kVS;
+            const int64_t gi = ((t0 + r) * H + h) * (int64_t)V + s0 + j;
+            sV[r * LV + j] = r < len ? ld_in(v, gi) : 0.f;
+            sDO[r * LV + j] = r < len ? ld_in(d_o, gi) : 0.f;
+        }
+        __syncthreads();
+        for (int c = tid; c < K; c += kGradThreads) {   // <dS', S> per key channel
+            float a = sSS[c];
+            for (int j = 0; j < kVS; ++j) a = fmaf(sS[c * LV + j], sDS[c * LV + j], a);
+            sSS[c] = a;
+        }
+        // KS = Kp S, R = diag(beta)(V - KS), X2 = Kb dS'
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int r = e / kVS, j = e % kVS;
+            float ks = 0.f, kd = 0.f;
+            for (int c = 0; c < K; ++c) {
+                ks = fmaf(sKp[r * LK + c], sS[c * LV + j], ks);
+                kd = fmaf(sKb[r * LK + c], sDS[c * LV + j], kd);
+            }
+            sKS[r * LV + j] = ks;
+            sR[r * LV + j] = sB[r] * (sV[r * LV + j] - ks);
+            sX2[r * LV + j] = kd;
+        }
+        __syncthreads();
+        // E = T R;  dE = L^T dO + X2
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int r = e / kVS, j = e % kVS;
+            float ev = 0.f, de = sX2[r * LV + j];
+            for (int i = 0; i <= r; ++i) ev = fmaf(sT[r * kLC + i], sR[i * LV + j], ev);
+            for (int r2 = r; r2 < C; ++r2) de = fmaf(sL[r2 * kLC + r], sDO[r2 * LV + j], de);
+            sE[r * LV + j] = ev;
+            sDE[r * LV + j] = de;
+        }
+        __syncthreads();
+        // dR = T^T dE; dv = beta dR
+        for (int e = tid; e < C * kVS; e += kGradThreads) {
+            const int i = e / kVS, j = e % kVS;
+            float acc = 0.f;
+            for (int r = i; r < C; ++r) acc = fmaf(sT[r * kLC + i], sDE[r * LV + j], acc);
+            sDR[i * LV + j] = acc;
+            if (i < len) p.dv[((t0 + i) * H + h) * (int64_t)V + s0 + j] = sB[i] * acc;
+        }
+        // dL += dO E^T (i <= r);  dT += dE R^T (i <= r)
+        for (int e = tid; e < C * C; e += kGradThreads) {
+            const int r = e / C, i = e % C;
+            if (i <= r) {
+                float dl = 0.f, dt = 0.f;
+                for (int j = 0; j < kVS; ++j) {
+                    dl = fmaf(sDO[r * LV + j], sE[i * LV + j], dl);
+                    dt = fmaf(sDE[r * LV + j], sR[i * LV + j], dt);
+                }
+                sDL[r * kLC + i] += dl;
+                sDT[r * kLC + i] += dt;
+            }
+        }
+        __syncthreads();
+        // (row, channel) partials: Y1 += dR S^T, Y2 += dO S^T, Y3 += E dS'^T
+#pragma unroll
+        for (int m = 0; m < CPT; ++m) {
+            const int c = my_c0 + 8 * m;
+            float a1 = y1[m], a2 = y2[m], a3 = y3[m];
+            for (int j = 0; j < kVS; ++j) {
+                a1 = fmaf(sDR[my_r * LV + j], sS[c * LV + j], a1);
+                a2 = fmaf(sDO[my_r * LV + j], sS[c * LV + j], a2);
+                a3 = fmaf(sE[my_r * LV + j], sDS[c * LV + j], a3);
+            }
+            y1[m] = a1; y2[m] = a2; y3[m] = a3;
+        }
+        // row sums for dbeta (one thread per row, fixed order)
+        for (int r = tid; r < C; r += kGradThreads) {
+            float b = 0.f, cc = 0.f;
+            for (int j = 0; j < kVS; ++j) {
+                b = fmaf(sDR[r * LV + j], sV[r * LV + j], b);
+                cc = fmaf(sDR[r * LV + j], sKS[r * LV + j], cc);
+            }
+            sRB[r] += b;
+            sRC[r] += cc;
+        }
+    }
+    __syncthreads();
+    // q and gamma again (the slice loop held Kp and Kb in their buffers)
+    simt_load_chunk<kKDA, Tin, K, kGradThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    __syncthreads();
+    simt_gate_cumsum<kKDA, K, kGradThreads>(sG);
+    // dA = -T^T (dT T^T), strictly lower.  X = dT T^T into sA (dT is lower incl. diag).
+    for (int e = tid; e < C * C; e += kGradThreads) {
+        const int r = e / C, m = e % C;
+        float acc = 0.f;
+        for (int i = 0; i <= min(r, m); ++i) acc = fmaf(sDT[r * kLC + i], sT[m * kLC + i], acc);
+        sA[r * kLC + m] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < C * C; e += kGradThreads) {
+        const int r = e / C, i = e % C;
+        float acc = 0.f;
+        if (i < r)
+            for (int m = r; m < C; ++m) acc = fmaf(-sT[m * kLC + r], sA[m * kLC + i], acc);
+        sDT[r * kLC + i] = acc;      // sDT now holds dA
+    }
+    __syncthreads();
+    simt_intra<kKDA, K, kGradThreads>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
+    __syncthreads();
+    const float *sDA = sDT;
+    for (int r = tid; r < C; r += kGradThreads) {   // dbeta, one thread per row
+        float da_row = 0.f;
+        for (int i = 0; i < r; ++i) da_row = fmaf(sDA[r * kLC + i], sAp[r * kLC + i], da_row);
+        if (r < len) p.dbeta[(t0 + r) * H + h] = sRB[r] - sRC[r] + da_row;
+    }
+    // ---- dq, dk and dgamma of (my_r, channel)
+    float dgv[CPT], wv[CPT];
+    {
+        const int r = my_r;
+        const float br = sB[r];
+#pragma unroll
+        for (int m = 0; m < CPT; ++m) {
+            const int c = my_c0 + 8 * m;
+            const float gr = sG[r * LK + c], eg = expf(gr), ec = expf(sGC[c] - gr);
+            float pl = 0.f, pa = 0.f, ql = 0.f, qa = 0.f;
+            for (int i = 0; i <= r; ++i) {
+                const float kd = sK[i * LK + c] * expf(gr - sG[i * LK + c]);
+                pl = fmaf(sDL[r * kLC + i], kd, pl);
+                pa = fmaf(sDA[r * kLC + i], kd, pa);
+            }
+            for (int r2 = r; r2 < C; ++r2) {
+                const float d = expf(sG[r2 * LK + c] - gr);
+                ql = fmaf(sDL[r2 * kLC + r], sQ[r2 * LK + c] * d, ql);
+                qa = fmaf(sDA[r2 * kLC + r] * sB[r2], sK[r2 * LK + c] * d, qa);
+            }
+            const float qv = sQ[r * LK + c], kv = sK[r * LK + c];
+            const float dq = p.scale * (eg * y2[m] + pl);
+            const float dk = -br * eg * y1[m] + ec * y3[m] + br * pa + p.scale * ql + qa;
+            dgv[m] = qv * dq + kv * (-br * eg * y1[m] - ec * y3[m] + br * pa - p.scale * ql - qa);
+            wv[m] = kv * ec * y3[m];
+            if (r < len) {
+                p.dq[((t0 + r) * H + h) * (int64_t)K + c] = dq;
+                p.dk[((t0 + r) * H + h) * (int64_t)K + c] = dk;
+            }
+        }
+    }
+    __syncthreads();   // every read of T, L, dL, dA is done: reuse them for dgamma
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) {
+        const int c = my_c0 + 8 * m;
+        sDGm[my_r * LK + c] = dgv[m];
+        sW3[my_r * LK + c] = wv[m];
+    }
+    __syncthreads();
+    // dg = reverse cumsum of dgamma per channel; the gamma_c terms reach every row
+    for (int c = tid; c < K; c += kGradThreads) {
+        float acc = expf(sGC[c]) * sSS[c];
+        for (int r = 0; r < C; ++r) acc += sW3[r * LK + c];
+        for (int r = C - 1; r >= 0; --r) {
+            acc += sDGm[r * LK + c];
+            if (r < len) p.dg[((t0 + r) * H + h) * (int64_t)K + c] = acc;
+        }
+    }
+}
+
 template <typename Kern>
 cudaError_t prep(Kern kern, size_t bytes) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -448,7 +720,28 @@ cudaError_t launch_k(const BwdParams &p, bool sweep_done, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename Tin, int K, int VS>
+cudaError_t launch_kda(const BwdParams &p, cudaStream_t s) {
+    cudaError_t e;
+    auto sweep = dstate_sweep_kernel<kKDA, Tin, K, VS>;
+    const size_t sb = SweepLayout<K, VS, kKDA>::bytes;
+    if ((e = prep(sweep, sb)) != cudaSuccess) return e;
+    sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto grad = chunk_grad_kda_kernel<Tin, K>;
+    const size_t gb = GradKdaLayout<K>::bytes;
+    if ((e = prep(grad, gb)) != cudaSuccess) return e;
+    grad<<<dim3((unsigned)p.nt_max, p.H), kGradThreads, gb, s>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, cudaStream_t s) {
+    if (dtype == GCL_BF16)
+        return p.K == 64 ? launch_kda<__nv_bfloat16, 64, 64>(p, s) : launch_kda<__nv_bfloat16, 128, 32>(p, s);
+    return p.K == 64 ? launch_kda<float, 64, 64>(p, s) : launch_kda<float, 128, 32>(p, s);
+}
 
 cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s) {
     if (dtype == GCL_BF16)

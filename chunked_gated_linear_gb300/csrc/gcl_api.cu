@@ -136,21 +136,104 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Backward workspace: dS' per chunk [nt_max, H, K, V] fp32; without saved states also
 // the recomputed states (same shape) and the forward's own workspace; on the tensor-core
 // path also the transition-form records the state-gradient sweep reads.
-static size_t bwd_ws(const gcl_bwd_args *a) {
+// KDA runs the backward on the CUDA cores (its recompute forward may use the tensor cores).
+static size_t bwd_ws(const gcl_bwd_args *a, int variant) {
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
-    const bool tc = fwd_tc_supported(kGDN, a->dtype, a->K, a->V);
+    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V);
+    const bool tc = variant == kGDN && tc_fwd;
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
     const size_t rec = tc ? align256(transition_record_bytes(ntm, a->H)) + kWsAlign +
                                 align256(bwd_grad_tc_scratch_bytes(ntm, a->H)) : 0;
     if (a->h_save) return per + rec;
-    const size_t fw = tc ? align256(fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign : 0;
+    const size_t fw = !tc_fwd ? 0
+                      : align256(variant == kKDA ? fwd_tc_t_workspace_bytes(ntm, a->H)
+                                                 : fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign;
     return 2 * per + fw + rec;
 }
 
 }  // namespace gcl
 
 using namespace gcl;
+
+static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int variant) {
+    g_err[0] = 0;
+    const char *fn = variant == kGDN ? "gdn_chunk_bwd" : "kda_chunk_bwd";
+    if (!a) return fail(GCL_ERR_INVALID_ARG, "%s: args is NULL", fn);
+    gcl_status_t st = check_common(fn, a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->t_max,
+                                   a->n_max, a->H, a->K, a->V, a->bt, a->dtype);
+    if (st != GCL_OK) return st;
+    if (!a->d_o || !a->chunk_indices || !a->chunk_offsets || !a->dq || !a->dk || !a->dv ||
+        !a->dg || !a->dbeta)
+        return fail(GCL_ERR_INVALID_ARG,
+                    "%s: d_o, chunk_indices, chunk_offsets, dq, dk, dv, dg, dbeta are required",
+                    fn);
+    const size_t need = bwd_ws(a, variant);
+    if (!a->workspace || a->workspace_bytes < need)
+        return fail(GCL_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    if (!aligned16(a->workspace) || !aligned16(a->d_o) || !aligned16(a->dq) ||
+        !aligned16(a->dk) || !aligned16(a->dv) || !aligned16(a->dg) || !aligned16(a->dbeta))
+        return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
+    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
+    const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
+    char *ws = static_cast<char *>(a->workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    BwdParams p{};
+    p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.h0 = a->h0;
+    p.d_o = a->d_o; p.dht = a->dht; p.cu_seqlens = a->cu_seqlens;
+    p.chunk_indices = a->chunk_indices; p.chunk_offsets = a->chunk_offsets;
+    p.dh = reinterpret_cast<float *>(ws);
+    p.dq = a->dq; p.dk = a->dk; p.dv = a->dv; p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->dh0;
+    p.dev_status = a->dev_status;
+    p.t_max = a->t_max; p.nt_max = ntm; p.n_max = a->n_max;
+    p.H = a->H; p.K = a->K; p.V = a->V; p.scale = a->scale;
+    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V);
+    const bool tc = variant == kGDN && tc_fwd;        // tensor-core backward: GDN
+    FwdParams f{};
+    f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
+    f.cu_seqlens = a->cu_seqlens; f.chunk_indices = a->chunk_indices;
+    f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
+    f.o = nullptr; f.ht = nullptr; f.h_save = nullptr; f.dev_status = a->dev_status;
+    f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
+    f.nt_max = ntm;
+    f.scale = a->scale;
+    const size_t fw = !tc_fwd ? 0
+                      : align256(variant == kKDA ? fwd_tc_t_workspace_bytes(ntm, a->H)
+                                                 : fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign;
+    const size_t used = a->h_save ? per : 2 * per + fw;
+    if (a->h_save) {
+        p.h = a->h_save;
+    } else {
+        float *h = reinterpret_cast<float *>(ws + per);
+        f.h_save = h;
+        f.workspace = nullptr;
+        f.workspace_bytes = 0;
+        if (tc_fwd)     // GDN: room for the W form only; KDA: its transition form
+            align_ws(ws + 2 * per, fw - 1, &f.workspace, &f.workspace_bytes);
+        cudaError_t e = tc_fwd ? launch_fwd_tc(f, variant, s) : launch_fwd_simt(f, variant, a->dtype, s);
+        if ((st = cuda_check(e, "gdn_chunk_bwd (state recompute)")) != GCL_OK) return st;
+        f.h_save = nullptr;
+        p.h = h;
+    }
+    if (tc) {   // transition-form records, then the state-gradient sweep on the tensor cores
+        void *rec = nullptr;
+        size_t rec_bytes = 0;
+        align_ws(ws + used, a->workspace_bytes - used, &rec, &rec_bytes);
+        if (rec_bytes < align256(transition_record_bytes(ntm, a->H)) + bwd_grad_tc_scratch_bytes(ntm, a->H))
+            return fail(GCL_ERR_CAPACITY, "%s: workspace too small for the sweep records", fn);
+        cudaError_t e = launch_prep_t(f, static_cast<uint8_t *>(rec), s);
+        if (e == cudaSuccess) e = launch_bwd_sweep_t(p, static_cast<const uint8_t *>(rec), s);
+        if ((st = cuda_check(e, "gdn_chunk_bwd (state-gradient sweep)")) != GCL_OK) return st;
+        // chunk gradients on the tensor cores; their scratch follows the records
+        float *scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(rec) +
+                                                   align256(transition_record_bytes(ntm, a->H)));
+        return cuda_check(launch_bwd_grad_tc(p, scratch, s), fn);
+    }
+    if (variant == kKDA) return cuda_check(launch_bwd_simt_kda(p, a->dtype, s), fn);
+    return cuda_check(launch_bwd_simt(p, a->dtype, false, s), fn);
+}
 
 extern "C" {
 
@@ -217,86 +300,17 @@ gcl_status_t kda_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream) {
     return run_fwd(args, stream, kKDA);
 }
 
+size_t gcl_kda_bwd_workspace_bytes(const gcl_bwd_args *a) {
+    if (!a) return 0;
+    return bwd_ws(a, kKDA);
+}
+
 size_t gcl_bwd_workspace_bytes(const gcl_bwd_args *a) {
     if (!a) return 0;
-    return bwd_ws(a);
+    return bwd_ws(a, kGDN);
 }
 
-gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) {
-    g_err[0] = 0;
-    const char *fn = "gdn_chunk_bwd";
-    if (!a) return fail(GCL_ERR_INVALID_ARG, "%s: args is NULL", fn);
-    gcl_status_t st = check_common(fn, a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->t_max,
-                                   a->n_max, a->H, a->K, a->V, a->bt, a->dtype);
-    if (st != GCL_OK) return st;
-    if (!a->d_o || !a->chunk_indices || !a->chunk_offsets || !a->dq || !a->dk || !a->dv ||
-        !a->dg || !a->dbeta)
-        return fail(GCL_ERR_INVALID_ARG,
-                    "%s: d_o, chunk_indices, chunk_offsets, dq, dk, dv, dg, dbeta are required",
-                    fn);
-    const size_t need = bwd_ws(a);
-    if (!a->workspace || a->workspace_bytes < need)
-        return fail(GCL_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn, need,
-                    a->workspace ? a->workspace_bytes : (size_t)0);
-    if (!aligned16(a->workspace) || !aligned16(a->d_o) || !aligned16(a->dq) ||
-        !aligned16(a->dk) || !aligned16(a->dv) || !aligned16(a->dg) || !aligned16(a->dbeta))
-        return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
-    const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
-    const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
-    char *ws = static_cast<char *>(a->workspace);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    BwdParams p{};
-    p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.h0 = a->h0;
-    p.d_o = a->d_o; p.dht = a->dht; p.cu_seqlens = a->cu_seqlens;
-    p.chunk_indices = a->chunk_indices; p.chunk_offsets = a->chunk_offsets;
-    p.dh = reinterpret_cast<float *>(ws);
-    p.dq = a->dq; p.dk = a->dk; p.dv = a->dv; p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->dh0;
-    p.dev_status = a->dev_status;
-    p.t_max = a->t_max; p.nt_max = ntm; p.n_max = a->n_max;
-    p.H = a->H; p.K = a->K; p.V = a->V; p.scale = a->scale;
-    const bool tc = fwd_tc_supported(kGDN, a->dtype, a->K, a->V);
-    FwdParams f{};
-    f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
-    f.cu_seqlens = a->cu_seqlens; f.chunk_indices = a->chunk_indices;
-    f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
-    f.o = nullptr; f.ht = nullptr; f.h_save = nullptr; f.dev_status = a->dev_status;
-    f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
-    f.nt_max = ntm;
-    f.scale = a->scale;
-    const size_t used = a->h_save ? per : 2 * per + (tc ? align256(fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign : 0);
-    if (a->h_save) {
-        p.h = a->h_save;
-    } else {
-        float *h = reinterpret_cast<float *>(ws + per);
-        f.h_save = h;
-        f.workspace = nullptr;
-        f.workspace_bytes = 0;
-        if (fwd_tc_supported(kGDN, a->dtype, a->K, a->V))     // room for the W form only
-            align_ws(ws + 2 * per, fwd_tc_workspace_bytes(ntm, a->H) + kWsAlign - 1, &f.workspace,
-                     &f.workspace_bytes);
-        cudaError_t e = tc
-                            ? launch_fwd_tc(f, kGDN, s)
-                            : launch_fwd_simt(f, kGDN, a->dtype, s);
-        if ((st = cuda_check(e, "gdn_chunk_bwd (state recompute)")) != GCL_OK) return st;
-        f.h_save = nullptr;
-        p.h = h;
-    }
-    if (tc) {   // transition-form records, then the state-gradient sweep on the tensor cores
-        void *rec = nullptr;
-        size_t rec_bytes = 0;
-        align_ws(ws + used, a->workspace_bytes - used, &rec, &rec_bytes);
-        if (rec_bytes < align256(transition_record_bytes(ntm, a->H)) + bwd_grad_tc_scratch_bytes(ntm, a->H))
-            return fail(GCL_ERR_CAPACITY, "%s: workspace too small for the sweep records", fn);
-        cudaError_t e = launch_prep_t(f, static_cast<uint8_t *>(rec), s);
-        if (e == cudaSuccess) e = launch_bwd_sweep_t(p, static_cast<const uint8_t *>(rec), s);
-        if ((st = cuda_check(e, "gdn_chunk_bwd (state-gradient sweep)")) != GCL_OK) return st;
-        // chunk gradients on the tensor cores; their scratch follows the records
-        float *scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(rec) +
-                                                   align256(transition_record_bytes(ntm, a->H)));
-        return cuda_check(launch_bwd_grad_tc(p, scratch, s), fn);
-    }
-    return cuda_check(launch_bwd_simt(p, a->dtype, false, s), fn);
-}
+gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) { return run_bwd(a, stream, kGDN); }
+gcl_status_t kda_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) { return run_bwd(a, stream, kKDA); }
 
 }  // extern "C"

@@ -81,6 +81,9 @@ bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t
 // CUDA-core backward: the state-gradient sweep (unless sweep_done: dh already holds dS'
 // per chunk and dh0 is written) and the chunk gradients.
 cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s);
+// KDA backward on the CUDA cores: state-gradient sweep with per-channel decay, then the chunk
+// gradients (dg per key channel).
+cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, cudaStream_t s);
 // Tensor-core state-gradient sweep from transition-form records (GDN, bf16, K = V = 128).
 cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *records, cudaStream_t s);
 // Tensor-core chunk gradients (dq, dk, dv, dg, dbeta) from p.h and p.dh, with a scratch record

@@ -223,11 +223,11 @@ gcl_status_t gdn_chunk_fwd_noalloc(const gcl_fwd_args *args, gcl_stream_t stream
 size_t gcl_noalloc_scratch_bytes(void);
 
 /*
- * Backward arguments (GDN).  All pointers are device pointers.
+ * Backward arguments (GDN and KDA).  All pointers are device pointers.
  */
 typedef struct gcl_bwd_args {
     const void *q, *k, *v;         /* as in gcl_fwd_args                                     */
-    const float *g;                /* [t_max, H] fp32                                        */
+    const float *g;                /* GDN [t_max, H]; KDA [t_max, H, K]; fp32                */
     const void *beta;              /* [t_max, H] dtype                                       */
     const float *h0;               /* [n_max, H, K, V] or NULL                               */
     const void *d_o;               /* [t_max, H, V] dtype: gradient of the loss w.r.t. o     */
@@ -239,7 +239,7 @@ typedef struct gcl_bwd_args {
                                    /* states are recomputed into the workspace              */
     float *dq, *dk;                /* [t_max, H, K] fp32 (out), live rows                    */
     float *dv;                     /* [t_max, H, V] fp32 (out)                               */
-    float *dg;                     /* [t_max, H] fp32 (out): w.r.t. the raw log gate g       */
+    float *dg;                     /* shape of g, fp32 (out): w.r.t. the raw log gate g      */
     float *dbeta;                  /* [t_max, H] fp32 (out)                                  */
     float *dh0;                    /* [n_max, H, K, V] fp32 (out) or NULL                    */
     void *workspace;               /* device scratch of gcl_bwd_workspace_bytes() bytes      */
@@ -251,9 +251,11 @@ typedef struct gcl_bwd_args {
     int32_t dtype;
 } gcl_bwd_args;
 
-/* Bytes of device workspace gdn_chunk_bwd needs for these sizes (depends on whether
- * h_save is NULL).  Returns 0 for unsupported sizes. */
+/* Bytes of device workspace gdn_chunk_bwd (gcl_bwd_workspace_bytes) and
+ * kda_chunk_bwd (gcl_kda_bwd_workspace_bytes) need for these sizes (depends on
+ * whether h_save is NULL).  Returns 0 for unsupported sizes. */
 size_t gcl_bwd_workspace_bytes(const gcl_bwd_args *args);
+size_t gcl_kda_bwd_workspace_bytes(const gcl_bwd_args *args);
 
 /*
  * gdn_chunk_bwd -- gradients dq, dk, dv, dg, dbeta, dh0 of
@@ -262,9 +264,16 @@ size_t gcl_bwd_workspace_bytes(const gcl_bwd_args *args);
  * gate and gradient kernels).  A reverse sweep over the chunks of each
  * (sequence, head) carries the state gradient; the per-chunk gradients are then
  * computed in parallel over chunk_indices, whose sentinel rows exit at once.
- * Supported sizes as for the forward.
+ * Supported sizes as for the forward.  bf16 with K = V = 128 runs on the tensor
+ * cores (tcgen05), everything else on the CUDA cores in fp32.
+ *
+ * kda_chunk_bwd -- the same through the KDA chunk forward (per-key-channel gate;
+ * dg has the shape of g, [t_max, H, K]).  The sweep and the chunk gradients run on
+ * the CUDA cores in fp32 (the recompute of missing states uses the forward's own
+ * path, tensor cores for bf16 K = V = 128).  Errors as for gdn_chunk_bwd.
  */
 gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *args, gcl_stream_t stream);
+gcl_status_t kda_chunk_bwd(const gcl_bwd_args *args, gcl_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -16,23 +16,25 @@ GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 def run_bwd(w, d, meta, h_save=None, with_dht=True):
     T, H, K, V = w.t_max, w.H, w.K, w.V
     f32 = dict(dtype=torch.float32, device=DEV)
+    kda = w.variant == synth.KDA
     out = dict(dq=torch.zeros((T, H, K), **f32), dk=torch.zeros((T, H, K), **f32),
-               dv=torch.zeros((T, H, V), **f32), dg=torch.zeros((T, H), **f32),
+               dv=torch.zeros((T, H, V), **f32),
+               dg=torch.zeros((T, H, K) if kda else (T, H), **f32),
                dbeta=torch.zeros((T, H), **f32), dh0=torch.zeros((w.n_max, H, K, V), **f32))
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["do"], d["cu_seqlens"], meta.idx,
             meta.off, out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"])
     kw = dict(h0=d.get("h0"), dht=d["dht"] if with_dht else None, dh0=out["dh0"],
               h_save=h_save, dev_status=meta.status, scale=w.scale)
-    nbytes = gcl.bwd_workspace_bytes(*args, **kw)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
-    gcl.gdn_chunk_bwd(*args, workspace=ws, **kw)
+    nbytes = (gcl.kda_bwd_workspace_bytes if kda else gcl.bwd_workspace_bytes)(*args, **kw)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)      # stale contents
+    (gcl.kda_chunk_bwd if kda else gcl.gdn_chunk_bwd)(*args, workspace=ws, **kw)
     torch.cuda.synchronize()
     assert int(meta.status.item()) == 0
     return {k_: v_.cpu().numpy() for k_, v_ in out.items()}
 
 
 def oracle_bwd(w, x, with_dht=True):
-    return oracle.bwd(synth.GDN, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"],
+    return oracle.bwd(w.variant, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"],
                       x["dht"] if with_dht else None, x["cu_seqlens"], w.scale)
 
 
@@ -91,3 +93,35 @@ def test_fwd_bwd_full_size_sampled_units():
             assert e_ <= TOL["bf16"], f"unit ({b},{h}) {key}: {e_:.3e}"
         e_ = relF(got["dh0"][b, h], ref["dh0"][0, 0])
         assert e_ <= TOL["bf16"], f"unit ({b},{h}) dh0: {e_:.3e}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("KV", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("saved", [True, False])
+def test_kda_small_varlen(dtype, KV, saved):
+    """kda_chunk_bwd: every gradient (dg per key channel) against the oracle's reverse mode,
+    ragged lengths, with saved chunk states or recomputing them."""
+    K, V = KV
+    lens = [1, 63, 0, 64, 65, 150]
+    w = synth.varlen("kda-bwd", synth.KDA, dtype, lens, 7, sum(lens) + 20, 2, K, V, backward=True,
+                     seed=13)
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    fw = run_fwd(w, d, h_save=saved)
+    got = run_bwd(w, d, fw["meta"], h_save=fw["h_save"])
+    compare(w, got, oracle_bwd(w, x), TOL[dtype])
+
+
+def test_kda_no_dht_no_h0_strong_gates():
+    """KDA backward without dht and h0, with per-channel log gates down to -40 per token."""
+    w = synth.varlen("kda-bwd0", synth.KDA, "bf16", [130, 7], 2, 200, 2, 128, 128, h0=False,
+                     backward=True, seed=14)
+    x = synth.make_inputs(w)
+    g = x["g"].copy()
+    g[np.random.default_rng(3).random(g.shape) < 0.1] *= 20.0
+    x["g"] = g.astype(np.float32)
+    d = to_device(w, x)
+    meta = Meta(w.t_max, w.n_max)
+    meta.build(d["cu_seqlens"])
+    got = run_bwd(w, d, meta, with_dht=False)
+    compare(w, got, oracle_bwd(w, x, with_dht=False), TOL["bf16"])
