@@ -213,7 +213,7 @@ class Runner:
                     t["off"], t["dq"], t["dk"], t["dv"], t["dg"], t["dbeta"])
             kw = dict(h0=t.get("h0"), dht=t.get("dht"), dh0=t["dh0"], h_save=t["hs"],
                       dev_status=t["status"], scale=w.scale)
-            nb = gcl.bwd_workspace_bytes(*args, **kw)
+            nb = (gcl.kda_bwd_workspace_bytes if w.variant == synth.KDA else gcl.bwd_workspace_bytes)(*args, **kw)
             t["ws"] = torch.empty(nb, dtype=torch.uint8, device=dev)
             self.bwd_args = gcl.bwd_args(*args, workspace=t["ws"], **kw)
 
@@ -231,7 +231,8 @@ class Runner:
             raise RuntimeError(self.gcl.lib().gcl_last_error().decode())
 
     def backward(self, s):
-        st = self.gcl.lib().gdn_chunk_bwd(ctypes.byref(self.bwd_args), s)
+        bwd = self.gcl.lib().kda_chunk_bwd if self.w.variant == synth.KDA else self.gcl.lib().gdn_chunk_bwd
+        st = bwd(ctypes.byref(self.bwd_args), s)
         if st:
             raise RuntimeError(self.gcl.lib().gcl_last_error().decode())
 
@@ -255,10 +256,11 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
 def launches_per_step(w) -> int:
     """Library kernels per step: chunk_meta_build, the forward (prep and chain on the tensor
     cores for GDN and KDA bf16 d_k = d_v = 128, one fused CUDA-core kernel otherwise) and
-    the GDN backward (on the tensor cores: transition records, state-gradient sweep and two
+    the backward (GDN on the tensor cores: transition records, state-gradient sweep and two
     chunk-gradient kernels; otherwise the sweep and one chunk-gradient kernel)."""
     tc = w.dtype == "bf16" and w.K == 128 and w.V == 128
-    return 1 + (2 if tc else 1) + ((4 if tc else 2) if w.backward else 0)
+    tc_bwd = tc and w.variant == synth.GDN
+    return 1 + (2 if tc else 1) + ((4 if tc_bwd else 2) if w.backward else 0)
 
 
 def run_gpu(args, rank, world, dist):

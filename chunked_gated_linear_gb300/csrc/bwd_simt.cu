@@ -721,13 +721,15 @@ cudaError_t launch_k(const BwdParams &p, bool sweep_done, cudaStream_t s) {
 }
 
 template <typename Tin, int K, int VS>
-cudaError_t launch_kda(const BwdParams &p, cudaStream_t s) {
+cudaError_t launch_kda(const BwdParams &p, bool sweep_done, cudaStream_t s) {
     cudaError_t e;
-    auto sweep = dstate_sweep_kernel<kKDA, Tin, K, VS>;
-    const size_t sb = SweepLayout<K, VS, kKDA>::bytes;
-    if ((e = prep(sweep, sb)) != cudaSuccess) return e;
-    sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!sweep_done) {
+        auto sweep = dstate_sweep_kernel<kKDA, Tin, K, VS>;
+        const size_t sb = SweepLayout<K, VS, kKDA>::bytes;
+        if ((e = prep(sweep, sb)) != cudaSuccess) return e;
+        sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     auto grad = chunk_grad_kda_kernel<Tin, K>;
     const size_t gb = GradKdaLayout<K>::bytes;
     if ((e = prep(grad, gb)) != cudaSuccess) return e;
@@ -737,10 +739,11 @@ cudaError_t launch_kda(const BwdParams &p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, cudaStream_t s) {
+cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s) {
     if (dtype == GCL_BF16)
-        return p.K == 64 ? launch_kda<__nv_bfloat16, 64, 64>(p, s) : launch_kda<__nv_bfloat16, 128, 32>(p, s);
-    return p.K == 64 ? launch_kda<float, 64, 64>(p, s) : launch_kda<float, 128, 32>(p, s);
+        return p.K == 64 ? launch_kda<__nv_bfloat16, 64, 64>(p, sweep_done, s)
+                         : launch_kda<__nv_bfloat16, 128, 32>(p, sweep_done, s);
+    return p.K == 64 ? launch_kda<float, 64, 64>(p, sweep_done, s) : launch_kda<float, 128, 32>(p, sweep_done, s);
 }
 
 cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s) {

@@ -31,7 +31,8 @@ struct SweepTParams {
     const int32_t *cu, *chunk_offsets;
     const float *dht;
     const uint8_t *ws;          // transition records + Gamma_c slots
-    uint8_t *dh;                // dS' per chunk: bf16 tiles of 32 KiB (see below)
+    uint8_t *dh;                // dS' per chunk: bf16 tiles of 32 KiB (see below), or
+    float *dh_f32;              // (if not null) fp32 [nt_max, H, K, V] for the CUDA-core gradients
     float *dh0;                 // [n_max, H, K, V]
     int32_t *status;
     int64_t t_max, nt_max;
@@ -57,7 +58,8 @@ constexpr int kSweepThreads = 32 * (kStateWarps + 2);      // + MMA issuer, TMA 
 // Reverse walk: step k handles chunk ic = nch - 1 - k.  Every mbarrier waited on by parity is
 // re-armed only after its waiter has passed; a timed-out wait makes every later wait return
 // at once, so all loops run to their ends.
-template <int VS, int NS>
+// KDA: Gamma_c is a per-key-channel diagonal (dS row m decays by its own entry).
+template <int VS, int NS, bool KDA>
 __global__ void __launch_bounds__(kSweepThreads, 1)
 tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_constant__ CUtensorMap tm_rec64,
                   const __grid_constant__ CUtensorMap tm_do, SweepTParams p) {
@@ -187,8 +189,13 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
             const int64_t rem = eos - bos - (int64_t)ic * C;
             const int len = (int)(rem < C ? rem : C);
             uint8_t *stage = smem + st * Lay::kStage;
-            {   // the gradient w.r.t. the state after chunk ic, as the chunk-gradient kernel's
-                // bf16 operand tile: key rows, two 64-column blocks, 128-byte swizzle
+            if (p.dh_f32) {   // the gradient w.r.t. the state after chunk ic, fp32 rows
+                float *dst = p.dh_f32 + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
+#pragma unroll
+                for (int j = 0; j < HV; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) = make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
+            } else {          // or as the tensor-core chunk-gradient kernel's bf16 operand tile:
+                              // key rows, two 64-column blocks, 128-byte swizzle
                 uint8_t *dst = p.dh + ((row0 + ic) * H + h) * (int64_t)kDsTileBytes;
 #pragma unroll
                 for (int j = 0; j < HV; j += 8)
@@ -205,7 +212,7 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_ops);
-            const float gc = *reinterpret_cast<const float *>(stage + Lay::oG);
+            const float gc = reinterpret_cast<const float *>(stage + Lay::oG)[KDA ? row : 0];
 #pragma unroll
             for (int j = 0; j < HV; ++j) dS[j] *= gc;
             mbar_wait(&bar_g, k & 1, &s_err, 4);
@@ -237,13 +244,13 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
     if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
 }
 
-template <int VS>
+template <int VS, bool KDA>
 cudaError_t launch_sweep(const CUtensorMap &m128, const CUtensorMap &m64, const CUtensorMap &mdo,
                          const SweepTParams &sp, int split, cudaStream_t s) {
     constexpr int NS = 3;
     using Lay = SweepLayout<NS>;
     static_assert(Lay::bytes <= 232448, "sweep shared memory");
-    auto kern = tc_sweep_t_kernel<VS, NS>;
+    auto kern = tc_sweep_t_kernel<VS, NS, KDA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::bytes);
     if (e != cudaSuccess) return e;
     kern<<<dim3(split, sp.H, sp.n_max), kSweepThreads, Lay::bytes, s>>>(m128, m64, mdo, sp);
@@ -252,7 +259,7 @@ cudaError_t launch_sweep(const CUtensorMap &m128, const CUtensorMap &m64, const 
 
 }  // namespace
 
-cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *ws, cudaStream_t s) {
+cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *ws, bool kda, cudaStream_t s) {
     const int H = p.H;
     const int64_t units = p.nt_max * H;
     CUtensorMap m128, m64, mdo;
@@ -272,6 +279,7 @@ cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *ws, cudaStream
     sp.dht = p.dht;
     sp.ws = ws;
     sp.dh = reinterpret_cast<uint8_t *>(p.dh);
+    sp.dh_f32 = kda ? p.dh : nullptr;           // the KDA chunk gradients read fp32 rows
     sp.dh0 = p.dh0;
     sp.status = p.dev_status;
     sp.t_max = p.t_max;
@@ -279,10 +287,17 @@ cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *ws, cudaStream
     sp.n_max = p.n_max;
     sp.H = H;
     const int split = fwd_tc_split(p.n_max, H);
+    if (kda) {
+        switch (VD / split) {
+            case 16: return launch_sweep<16, true>(m128, m64, mdo, sp, split, s);
+            case 32: return launch_sweep<32, true>(m128, m64, mdo, sp, split, s);
+            default: return launch_sweep<64, true>(m128, m64, mdo, sp, split, s);
+        }
+    }
     switch (VD / split) {
-        case 16: return launch_sweep<16>(m128, m64, mdo, sp, split, s);
-        case 32: return launch_sweep<32>(m128, m64, mdo, sp, split, s);
-        default: return launch_sweep<64>(m128, m64, mdo, sp, split, s);
+        case 16: return launch_sweep<16, false>(m128, m64, mdo, sp, split, s);
+        case 32: return launch_sweep<32, false>(m128, m64, mdo, sp, split, s);
+        default: return launch_sweep<64, false>(m128, m64, mdo, sp, split, s);
     }
 }
 

@@ -557,8 +557,7 @@ tc_prep_kda_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 }  // namespace
 
-cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s) {
-    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
+cudaError_t launch_prep_kda(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mrec;
     if (!make_prep_maps(p, ws, &mq, &mk, &mv, &mrec)) return cudaErrorInvalidValue;
     const PrepTParams pp = make_prep_params(p, ws);
@@ -566,7 +565,12 @@ cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int64_t units = p.nt_max * p.H;
     const int grid = (int)(units < (int64_t)num_sms() ? units : (int64_t)num_sms());
-    e = launch_dependent(tc_prep_kda_kernel, dim3(grid), dim3(kThreads), kSmem, s, mq, mk, mv, mrec, pp);
+    return launch_dependent(tc_prep_kda_kernel, dim3(grid), dim3(kThreads), kSmem, s, mq, mk, mv, mrec, pp);
+}
+
+cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s) {
+    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
+    const cudaError_t e = launch_prep_kda(p, ws, s);
     if (e != cudaSuccess) return e;
     return launch_chain_records(p, ws, split, true, s);
 }

@@ -143,8 +143,11 @@ static size_t bwd_ws(const gcl_bwd_args *a, int variant) {
     const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V);
     const bool tc = variant == kGDN && tc_fwd;
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
-    const size_t rec = tc ? align256(transition_record_bytes(ntm, a->H)) + kWsAlign +
-                                align256(bwd_grad_tc_scratch_bytes(ntm, a->H)) : 0;
+    // tensor-core sweep (GDN and KDA bf16 K = V = 128): transition records; GDN's tensor-core
+    // chunk gradients also a scratch record per chunk and head
+    const size_t rec = !tc_fwd ? 0
+                       : align256(transition_record_bytes(ntm, a->H)) + kWsAlign +
+                             (tc ? align256(bwd_grad_tc_scratch_bytes(ntm, a->H)) : 0);
     if (a->h_save) return per + rec;
     const size_t fw = !tc_fwd ? 0
                       : align256(variant == kKDA ? fwd_tc_t_workspace_bytes(ntm, a->H)
@@ -213,25 +216,31 @@ static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int vari
         if (tc_fwd)     // GDN: room for the W form only; KDA: its transition form
             align_ws(ws + 2 * per, fw - 1, &f.workspace, &f.workspace_bytes);
         cudaError_t e = tc_fwd ? launch_fwd_tc(f, variant, s) : launch_fwd_simt(f, variant, a->dtype, s);
-        if ((st = cuda_check(e, "gdn_chunk_bwd (state recompute)")) != GCL_OK) return st;
+        if ((st = cuda_check(e, variant == kKDA ? "kda_chunk_bwd (state recompute)"
+                                                : "gdn_chunk_bwd (state recompute)")) != GCL_OK)
+            return st;
         f.h_save = nullptr;
         p.h = h;
     }
-    if (tc) {   // transition-form records, then the state-gradient sweep on the tensor cores
+    if (tc_fwd) {   // transition-form records, then the state-gradient sweep on the tensor cores
         void *rec = nullptr;
         size_t rec_bytes = 0;
         align_ws(ws + used, a->workspace_bytes - used, &rec, &rec_bytes);
-        if (rec_bytes < align256(transition_record_bytes(ntm, a->H)) + bwd_grad_tc_scratch_bytes(ntm, a->H))
+        if (rec_bytes < align256(transition_record_bytes(ntm, a->H)) + (tc ? bwd_grad_tc_scratch_bytes(ntm, a->H) : 0))
             return fail(GCL_ERR_CAPACITY, "%s: workspace too small for the sweep records", fn);
-        cudaError_t e = launch_prep_t(f, static_cast<uint8_t *>(rec), s);
-        if (e == cudaSuccess) e = launch_bwd_sweep_t(p, static_cast<const uint8_t *>(rec), s);
-        if ((st = cuda_check(e, "gdn_chunk_bwd (state-gradient sweep)")) != GCL_OK) return st;
+        cudaError_t e = variant == kKDA ? launch_prep_kda(f, static_cast<uint8_t *>(rec), s)
+                                        : launch_prep_t(f, static_cast<uint8_t *>(rec), s);
+        if (e == cudaSuccess) e = launch_bwd_sweep_t(p, static_cast<const uint8_t *>(rec), variant == kKDA, s);
+        if ((st = cuda_check(e, variant == kKDA ? "kda_chunk_bwd (state-gradient sweep)"
+                                                : "gdn_chunk_bwd (state-gradient sweep)")) != GCL_OK)
+            return st;
+        if (variant == kKDA) return cuda_check(launch_bwd_simt_kda(p, a->dtype, true, s), fn);
         // chunk gradients on the tensor cores; their scratch follows the records
         float *scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(rec) +
                                                    align256(transition_record_bytes(ntm, a->H)));
         return cuda_check(launch_bwd_grad_tc(p, scratch, s), fn);
     }
-    if (variant == kKDA) return cuda_check(launch_bwd_simt_kda(p, a->dtype, s), fn);
+    if (variant == kKDA) return cuda_check(launch_bwd_simt_kda(p, a->dtype, false, s), fn);
     return cuda_check(launch_bwd_simt(p, a->dtype, false, s), fn);
 }
 

@@ -83,9 +83,13 @@ bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t
 cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s);
 // KDA backward on the CUDA cores: state-gradient sweep with per-channel decay, then the chunk
 // gradients (dg per key channel).
-cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s);
+// KDA transition-form records alone (the backward's sweep reads them).
+cudaError_t launch_prep_kda(const FwdParams &p, uint8_t *ws, cudaStream_t s);
 // Tensor-core state-gradient sweep from transition-form records (GDN, bf16, K = V = 128).
-cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *records, cudaStream_t s);
+// kda: per-key Gamma_c, and dS' as fp32 rows in p.dh (for the CUDA-core KDA chunk gradients)
+// instead of the bf16 tiles of the tensor-core GDN chunk gradients.
+cudaError_t launch_bwd_sweep_t(const BwdParams &p, const uint8_t *records, bool kda, cudaStream_t s);
 // Tensor-core chunk gradients (dq, dk, dv, dg, dbeta) from p.h and p.dh, with a scratch record
 // of bwd_grad_tc_scratch_bytes per launch (GDN, bf16, K = V = 128).
 cudaError_t launch_bwd_grad_tc(const BwdParams &p, float *scratch, cudaStream_t s);

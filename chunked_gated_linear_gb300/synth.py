@@ -95,6 +95,9 @@ def standard_workloads():
                random_lengths(32, 1, 2048, 30), 64, 65536, 16, 128, 128, seed=3),
         dense("gdn_fwdbwd_bf16_B4_T8192_H16_d128", GDN, "bf16", 4, 8192, 16, 128, 128,
               backward=True, seed=4),
+        # beyond the five configurations above: the KDA backward, at the KDA forward's sizes
+        dense("kda_fwdbwd_bf16_T2048_H10_d128", KDA, "bf16", 1, 2048, 10, 128, 128,
+              backward=True, seed=5),
     ]
 
 
