@@ -263,6 +263,59 @@ def launches_per_step(w) -> int:
     return 1 + (2 if tc else 1) + ((4 if tc_bwd else 2) if w.backward else 0)
 
 
+def graph_and_warm_timing(torch, w, sets, stream, step, step_ms, reps):
+    """Medians over `reps` steps (CUDA events on the launching stream) of: the direct launches
+    timed above (L2-cold: input sets rotated), the step captured once per input set in a CUDA
+    graph and replayed (cold, and warm: the same set every replay, so inputs that fit stay in
+    L2), and graph-update-replay (copy the next set's inputs into the captured set's buffers,
+    then replay)."""
+    import ctypes as ct
+    n = len(sets)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    graphs = []
+    for r in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(r, sp=ct.c_void_p(torch.cuda.current_stream().cuda_stream))
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        for i in range(reps):
+            ev[i][0].record(stream)
+            fn(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    inputs = [k for k in ("q", "k", "v", "g", "beta", "cu", "h0", "do", "dht") if k in sets[0].t]
+
+    def update_replay(i):
+        src = sets[1 + i % (n - 1)] if n > 1 else sets[0]
+        for k in inputs:
+            sets[0].t[k].copy_(src.t[k])
+        graphs[0].replay()
+
+    out = {
+        "direct_median_ms": statistics.median(step_ms),
+        "graph_median_ms": timed(lambda i: graphs[i % n].replay()),
+        "graph_warm_median_ms": timed(lambda i: graphs[0].replay()),
+        "graph_update_replay_median_ms": timed(update_replay),
+        "reps": reps,
+        "l2": "direct and graph: input sets rotated (cold); warm: one set replayed",
+    }
+    torch.cuda.synchronize()
+    for r in sets:
+        assert int(r.t["status"].item()) == 0
+    return out
+
+
 def run_gpu(args, rank, world, dist):
     import torch
     import chunked_gated_linear_gb300 as gcl
@@ -279,15 +332,16 @@ def run_gpu(args, rank, world, dist):
     stream = torch.cuda.current_stream()
     s = ctypes.c_void_p(stream.cuda_stream)
 
-    def step(r, ev=None):
-        r.meta(s)
+    def step(r, ev=None, sp=None):
+        sp = s if sp is None else sp
+        r.meta(sp)
         if ev is not None:
             ev[0].record(stream)
-        r.forward(s)
+        r.forward(sp)
         if ev is not None:
             ev[1].record(stream)
         if w.backward:
-            r.backward(s)
+            r.backward(sp)
 
     for i in range(args.warmup):
         step(sets[i % n_sets])
@@ -324,6 +378,9 @@ def run_gpu(args, rank, world, dist):
     ms_kern = tot[1] / K
     value = job_throughput(w.total_tokens, world, ms_step)
 
+    timing = graph_and_warm_timing(torch, w, sets, stream, step, step_ms, max(K, 50))
+    timing["chunk_utilisation"] = int(first.t["off"][-1].item()) / gcl.nt_max(w.t_max, w.n_max, w.bt)
+
     # end-to-end through the C ABI with host buffers: H2D inputs, step, D2H outputs
     e2e = run_e2e(gcl, w, x, first, stream, s, args.e2e_steps, world, dist)
     clk = clocks.summary()
@@ -352,6 +409,7 @@ def run_gpu(args, rank, world, dist):
                      "kernel_ms": ms_kern, "algorithmic_bytes_per_launch": ab,
                      "tensor_flops_per_launch": flops_per_step(w), "peak_source": peak_kind},
         "e2e": e2e,
+        "timing": timing,
         "gpu_launches": K * launches_per_step(w),
         "clocks": clk,
     }
@@ -418,10 +476,17 @@ def cpu_baseline(w, x, budget_s=12.0):
     tokens = int(min(max(64, budget_s * rate / max(heads * len(w.lengths), 1)),
                      max(w.lengths)))
     dt, th = oracle_sample(w, x, heads, tokens)
+    # the whole workload takes less than the budget: run it again until the budget is spent
+    reps = 1
+    while dt < 0.8 * budget_s and reps < 500:
+        d2, t2 = oracle_sample(w, x, heads, tokens)
+        dt += d2
+        th += t2
+        reps += 1
     return {"value": th / w.H / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"fp64 token recurrence, first {tokens} tokens of every sequence, all "
-                      f"{heads} heads ({th} token-heads, {dt:.1f} s)"}
+                      f"{heads} heads, {reps} run(s) ({th} token-heads, {dt:.1f} s)"}
 
 
 def run_reference(args):
