@@ -49,6 +49,9 @@ def parse():
                     choices=[w.name for w in synth.standard_workloads()])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling aid: run a dense workload with this many sequences instead "
+                         "of its own count (a smaller case for ncu); never for a bench line")
     return ap.parse_args()
 
 
@@ -316,6 +319,18 @@ def graph_and_warm_timing(torch, w, sets, stream, step, step_ms, reps):
     return out
 
 
+def resolve_workload(args):
+    """The named workload, or (--batch) the same dense workload with another sequence count."""
+    w = synth.workload_by_name(args.workload)
+    if args.batch:
+        if len(set(w.lengths)) != 1 or w.n_max != len(w.lengths):
+            raise SystemExit("--batch applies to dense workloads only")
+        w = synth.dense(f"{w.name}@batch{args.batch}", w.variant, w.dtype, args.batch,
+                        w.lengths[0], w.H, w.K, w.V, h0=w.h0, backward=w.backward, seed=w.seed,
+                        bt=w.bt)
+    return w
+
+
 def run_gpu(args, rank, world, dist):
     import torch
     import chunked_gated_linear_gb300 as gcl
@@ -323,7 +338,7 @@ def run_gpu(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    w = synth.workload_by_name(args.workload)
+    w = resolve_workload(args)
     x = synth.make_inputs(w, seed=w.seed + 1000 * rank)
     first = Runner(gcl, w, x, dev)
     n_sets = max(2, -(-3 * L2_BYTES // max(first.footprint(), 1)))
@@ -542,7 +557,7 @@ def main():
     line = run_gpu(args, rank, world, dist)
     if rank == 0:
         if not args.no_cpu_baseline:
-            w = synth.workload_by_name(args.workload)
+            w = resolve_workload(args)
             line["cpu_baseline"] = cpu_baseline(w, synth.make_inputs(w))
         print(json.dumps(line), flush=True)
     if dist is not None:
