@@ -11,9 +11,10 @@
 //   M   = beta_r D o dA,   dA = -T^T dT T^T (strictly lower),   D[r][i] = e^{g_r - g_i},
 // and the gate and beta gradients from row sums.  Two launches per chunk and head:
 //   grad1  (tensor cores) the recompute (K K^T, Q K^T, the triangular solve) and five MMA
-//          rounds: [K; Q][S | dS'], [T; L] R and L^T dO, then T^T dE, [E; dO][S | dS']^T,
-//          [E; dO] E^T, [dE; E] R^T, then (T^T dE) S^T.  It writes dv, the partial dq and dk,
-//          and T, D o K K^T, L, dL, dT and four row sums per chunk to a scratch record;
+//          rounds: [K; Q][S | dS'], [T; L] R and L^T dO, then T^T dE, [E; dO] S^T,
+//          [E; dO] E^T, [dE; E] R^T, then (-diag(beta Gamma) T^T dE) S^T and E dS'^T.
+//          It writes dv, the partial dq and dk, and T, D o K K^T, L, dL, dT and four row sums per
+//          chunk to a scratch record;
 //   grad2  dA on the CUDA cores (fp32), the gate and beta gradients, and one MMA round
 //          [M; P] K, M^T K + P^T Q that completes dq and dk.
 #include <cudaTypedefs.h>
@@ -400,19 +401,18 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int q = 0; q < 8; ++q) *kchunk(gT3, 192, r, half * 64 + q * 8) = pack8(x + q * 8);
         }
         to_async();
-        // ---- R4: dVb = T^T dE -> cols 0..127; [E; dO] S^T -> 128..255 (dO S^T in lanes 64..);
-        // [E; dO] dS'^T -> 256..383 (E dS'^T in lanes 0..63); [E; dO] E^T -> 384..447 (dO E^T in
-        // lanes 64..); [dE; E] R^T -> 448..511 (dE R^T in lanes 0..63)
+        // ---- R4: dVb = T^T dE -> cols 256..383; [E; dO] S^T -> 128..255 (dO S^T in lanes 64..);
+        // [E; dO] E^T -> 384..447 (dO E^T in lanes 64..); [dE; E] R^T -> 448..511 (dE R^T in lanes
+        // 0..63).  Columns 0..127 keep K S from R2 (lanes 0..63) for the dbeta and gate sums.
         if (tid == 0) {
             const uint64_t at = smem_desc(sbase + gTL, 8192, 1024, kSwizzle128B);          // T^T
             const uint64_t bde = smem_desc(sbase + gT3, 24576, 1024, kSwizzle128B);        // dE
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem, at + s * 128, bde + s * 128, idesc_bf16(128, 128, 1, 1), s > 0);
+                mma_bf16(tmem + 256, at + s * 128, bde + s * 128, idesc_bf16(128, 128, 1, 1), s > 0);
             const uint64_t aeo = smem_desc(sbase + gT3 + 8192, 16, 1024, kSwizzle128B);    // [E; dO]
             const uint64_t ade = smem_desc(sbase + gT3, 16, 1024, kSwizzle128B);           // [dE; E]
             const uint64_t bs = smem_desc(sbase + gS, 16, 1024, kSwizzle128B);             // S^T
-            const uint64_t bd = smem_desc(sbase + gDS, 16, 1024, kSwizzle128B);            // dS'^T
             const uint64_t be = smem_desc(sbase + gT3 + 8192, 16, 1024, kSwizzle128B);     // E^T
             const uint64_t brr = smem_desc(sbase + gV, 16, 1024, kSwizzle128B);            // R^T
 #pragma unroll
@@ -421,46 +421,59 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint64_t os = (s >> 2) * (16384 >> 4) + (s & 3) * 2;
                 const uint64_t orr = (s >> 2) * (8192 >> 4) + (s & 3) * 2;
                 mma_bf16(tmem + 128, aeo + oa, bs + os, idesc_bf16(128, 128), s > 0);
-                mma_bf16(tmem + 256, aeo + oa, bd + os, idesc_bf16(128, 128), s > 0);
                 mma_bf16(tmem + 384, aeo + oa, be + oa, idesc_bf16(128, 64), s > 0);
                 mma_bf16(tmem + 448, ade + oa, brr + orr, idesc_bf16(128, 64), s > 0);
             }
             mma_commit(&bar_mma);
         }
+        // the v row of this thread (dbeta needs V, whose tile now holds R), while R4 runs
+        uint4 vrow8[8];
+        if (lrow < C && lrow < len) {
+            const uint4 *vrow = reinterpret_cast<const uint4 *>(p.v + ((t0 + lrow) * H + h) * (int64_t)VD + half * 64);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) vrow8[q] = vrow[q];
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) vrow8[q] = make_uint4(0, 0, 0, 0);
+        }
         if (!mma_done(5)) break;
         if (lrow < C) {
+            // dv = beta dVb; RB = sum_v dVb o V; RC = sum_v dVb o (K S); the R5 operand
+            // -beta Gamma dVb (in place of [T; L])
             const int r = lrow;
             const bool live = r < len;
-            float x[64];
-            ld64(half * 64, x);                      // dVb
-            float rb = 0.f;
-            const __nv_bfloat16 *vrow = p.v + ((t0 + r) * H + h) * (int64_t)VD + half * 64;
             float *dvrow = p.dv + ((t0 + r) * H + h) * (int64_t)VD + half * 64;
-            const float br = sB[r];
+            const float br = sB[r], fb = -sB[r] * sEG[r];
+            float rb = 0.f, rc = 0.f;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                *kchunk(gTL, 64, r, half * 64 + q * 8) = pack8(x + q * 8);   // dVb tile
-                if (live) {
-                    float vv[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(vrow + q * 8), vv);
+            for (int q2 = 0; q2 < 4; ++q2) {          // 16 value columns at a time
+                float x[16], ks[16];
+                tmem_ld16(tmem + lane_off + 256 + half * 64 + q2 * 16, x);
+                tmem_ld16(tmem + lane_off + half * 64 + q2 * 16, ks);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) rb = fmaf(x[q * 8 + e], vv[e], rb);
-                    *reinterpret_cast<float4 *>(dvrow + q * 8) =
-                        make_float4(br * x[q * 8], br * x[q * 8 + 1], br * x[q * 8 + 2], br * x[q * 8 + 3]);
-                    *reinterpret_cast<float4 *>(dvrow + q * 8 + 4) =
-                        make_float4(br * x[q * 8 + 4], br * x[q * 8 + 5], br * x[q * 8 + 6], br * x[q * 8 + 7]);
+                for (int hq = 0; hq < 2; ++hq) {
+                    const int q = q2 * 2 + hq, c = half * 64 + q * 8;
+                    const float *xx = x + hq * 8;
+                    float vv[8], sc[8];
+                    unpack8(vrow8[q], vv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        rb = fmaf(xx[e], vv[e], rb);
+                        rc = fmaf(xx[e], ks[hq * 8 + e], rc);
+                        sc[e] = fb * xx[e];
+                    }
+                    *kchunk(gTL, 64, r, c) = pack8(sc);
+                    if (live) {
+                        *reinterpret_cast<float4 *>(dvrow + q * 8) =
+                            make_float4(br * xx[0], br * xx[1], br * xx[2], br * xx[3]);
+                        *reinterpret_cast<float4 *>(dvrow + q * 8 + 4) =
+                            make_float4(br * xx[4], br * xx[5], br * xx[6], br * xx[7]);
+                    }
                 }
             }
             atomicAdd(&sRow[1][r], rb);
-            ld64(256 + half * 64, x);                // E dS'^T
-            if (live) {
-                float *dkrow = p.dk + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
-                const float fr = sFR[r];
-#pragma unroll
-                for (int q = 0; q < 64; q += 4)
-                    *reinterpret_cast<float4 *>(dkrow + q) =
-                        make_float4(fr * x[q], fr * x[q + 1], fr * x[q + 2], fr * x[q + 3]);
-            }
+            atomicAdd(&sRow[2][r], rc);
             {   // dT = dE R^T (32 columns of this half)
                 float t32[32];
                 tmem_ld16(tmem + lane_off + 448 + half * 32, t32);
@@ -493,38 +506,40 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     make_float4(t32[q], t32[q + 1], t32[q + 2], t32[q + 3]);
         }
         to_async();
-        // ---- R5: dVb S^T -> cols 0..127 (lanes 0..63)
+        // ---- R5: (-beta Gamma dVb) S^T -> cols 0..127 and [E; dO] dS'^T -> cols 128..255
+        // (lanes 0..63); dk = the first + exp(g_c - g) the second
         if (tid == 0) {
-            const uint64_t a = smem_desc(sbase + gTL, 16, 1024, kSwizzle128B);
-            const uint64_t b = smem_desc(sbase + gS, 16, 1024, kSwizzle128B);
+            const uint64_t a1 = smem_desc(sbase + gTL, 16, 1024, kSwizzle128B);
+            const uint64_t a2 = smem_desc(sbase + gT3 + 8192, 16, 1024, kSwizzle128B);
+            const uint64_t bs = smem_desc(sbase + gS, 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(sbase + gDS, 16, 1024, kSwizzle128B);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_bf16(tmem, a + (s >> 2) * (8192 >> 4) + (s & 3) * 2, b + (s >> 2) * (16384 >> 4) + (s & 3) * 2,
+                mma_bf16(tmem, a1 + (s >> 2) * (8192 >> 4) + (s & 3) * 2, bs + (s >> 2) * (16384 >> 4) + (s & 3) * 2,
                          idesc_bf16(128, 128), s > 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tmem + 128, a2 + (s >> 2) * (24576 >> 4) + (s & 3) * 2,
+                         bd + (s >> 2) * (16384 >> 4) + (s & 3) * 2, idesc_bf16(128, 128), s > 0);
             mma_commit(&bar_mma);
         }
         if (!mma_done(6)) break;
-        if (lrow < C) {   // dk -= beta Gamma dVb S^T;  RC = sum_c (dVb S^T) o K
+        if (lrow < C) {   // the first part of dk
             const int r = lrow;
-            float x[64];
-            ld64(half * 64, x);
-            float rc = 0.f;
+            const float fr = sFR[r];
+            float *dkrow = p.dk + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float kk[8];
-                unpack8(*kchunk(gKQ, 128, r, half * 64 + q * 8), kk);
+            for (int q = 0; q < 4; ++q) {
+                float x[16], y[16];
+                tmem_ld16(tmem + lane_off + half * 64 + q * 16, x);
+                tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, y);
+                tmem_ld_wait();
+                if (r < len) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) rc = fmaf(x[q * 8 + e], kk[e], rc);
-            }
-            atomicAdd(&sRow[2][r], rc);
-            if (r < len) {
-                float *dkrow = p.dk + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
-                const float f = sB[r] * sEG[r];
-#pragma unroll
-                for (int q = 0; q < 64; q += 4) {
-                    float4 d = *reinterpret_cast<float4 *>(dkrow + q);
-                    d.x -= f * x[q]; d.y -= f * x[q + 1]; d.z -= f * x[q + 2]; d.w -= f * x[q + 3];
-                    *reinterpret_cast<float4 *>(dkrow + q) = d;
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(dkrow + q * 16 + e) =
+                            make_float4(fmaf(fr, y[e], x[e]), fmaf(fr, y[e + 1], x[e + 1]),
+                                        fmaf(fr, y[e + 2], x[e + 2]), fmaf(fr, y[e + 3], x[e + 3]));
                 }
             }
         }
