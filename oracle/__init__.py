@@ -11,6 +11,8 @@ Two independent implementations live here:
   metadata built by plain loops and the reverse-mode backward.
 * ``chunk_form.py``: a separate fp64 evaluator of the chunkwise
   (Map-Reduce-Map) form, used only to cross-check the chunk algebra.
+* ``short_conv.py``: the short causal depthwise convolution that precedes the
+  chunk attention, forward and reverse mode (numpy, fp64).
 
 Every function takes numpy arrays in the token-major layouts of the FLA RFC
 "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths on Ascend
@@ -32,6 +34,8 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 GDN, KDA = 0, 1
+
+from .short_conv import conv_bwd, conv_fwd  # noqa: E402,F401  (the short convolution)
 
 
 def build(force: bool = False) -> str:
