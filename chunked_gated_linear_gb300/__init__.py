@@ -55,6 +55,19 @@ class BwdArgs(ctypes.Structure):
                 ("dtype", ctypes.c_int32)]
 
 
+class ConvArgs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("ht", ctypes.c_void_p), ("dy", ctypes.c_void_p), ("dht", ctypes.c_void_p),
+                ("dx", ctypes.c_void_p), ("dweight", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
+                ("dh0", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+                ("chunk_indices", ctypes.c_void_p), ("dev_status", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("t_max", ctypes.c_int64), ("n_max", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("W", ctypes.c_int32), ("bt", ctypes.c_int32), ("activation", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
 def load_library(path: str = LIB_PATH):
     """Load libgcl.so and declare its C signatures."""
     if not os.path.exists(path):
@@ -84,6 +97,11 @@ def load_library(path: str = LIB_PATH):
     for fn in ("gcl_bwd_workspace_bytes", "gcl_kda_bwd_workspace_bytes"):
         getattr(lib, fn).restype = ctypes.c_size_t
         getattr(lib, fn).argtypes = [ctypes.POINTER(BwdArgs)]
+    for fn in ("causal_conv1d_fwd", "causal_conv1d_bwd"):
+        getattr(lib, fn).restype = ctypes.c_int
+        getattr(lib, fn).argtypes = [ctypes.POINTER(ConvArgs), vp]
+    lib.gcl_causal_conv1d_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.gcl_causal_conv1d_bwd_workspace_bytes.argtypes = [ctypes.POINTER(ConvArgs)]
     return lib
 
 
@@ -233,3 +251,36 @@ def kda_chunk_bwd(*args, stream=None, **kw):
     """The KDA backward; dg has the shape of g, [T, H, K]."""
     a = bwd_args(*args, **kw)
     _check("kda_chunk_bwd", lib().kda_chunk_bwd(ctypes.byref(a), _stream(stream)))
+
+
+# ---------------------------------------------------------------- causal_conv1d
+ACTIVATIONS = {None: 0, "silu": 1}
+
+
+def conv_args(x, weight, cu_seqlens, chunk_indices, bias=None, residual=None, h0=None, y=None,
+              ht=None, dy=None, dht=None, dx=None, dweight=None, dbias=None, dh0=None,
+              workspace=None, dev_status=None, activation=None, bt=CHUNK):
+    """gcl_conv_args for x [T, D], weight [D, W]; see include/gcl.h (causal_conv1d)."""
+    T, D = x.shape
+    return ConvArgs(x=_p(x), weight=_p(weight), bias=_p(bias), residual=_p(residual), h0=_p(h0),
+                    y=_p(y), ht=_p(ht), dy=_p(dy), dht=_p(dht), dx=_p(dx), dweight=_p(dweight),
+                    dbias=_p(dbias), dh0=_p(dh0), cu_seqlens=_p(cu_seqlens),
+                    chunk_indices=_p(chunk_indices), dev_status=_p(dev_status),
+                    workspace=_p(workspace), workspace_bytes=_nbytes(workspace), t_max=T,
+                    n_max=cu_seqlens.shape[0] - 1, D=D, W=weight.shape[1], bt=bt,
+                    activation=ACTIVATIONS[activation], dtype=_dtype_of(x))
+
+
+def causal_conv1d_fwd(*args, stream=None, **kw):
+    a = conv_args(*args, **kw)
+    _check("causal_conv1d_fwd", lib().causal_conv1d_fwd(ctypes.byref(a), _stream(stream)))
+
+
+def causal_conv1d_bwd_workspace_bytes(*args, **kw) -> int:
+    a = conv_args(*args, **kw)
+    return int(lib().gcl_causal_conv1d_bwd_workspace_bytes(ctypes.byref(a)))
+
+
+def causal_conv1d_bwd(*args, stream=None, **kw):
+    a = conv_args(*args, **kw)
+    _check("causal_conv1d_bwd", lib().causal_conv1d_bwd(ctypes.byref(a), _stream(stream)))

@@ -322,4 +322,69 @@ size_t gcl_bwd_workspace_bytes(const gcl_bwd_args *a) {
 gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) { return run_bwd(a, stream, kGDN); }
 gcl_status_t kda_chunk_bwd(const gcl_bwd_args *a, gcl_stream_t stream) { return run_bwd(a, stream, kKDA); }
 
+
+// ---------------------------------------------------------------- causal_conv1d
+static gcl_status_t conv_check(const char *fn, const gcl_conv_args *a, bool backward) {
+    if (!a) return fail(GCL_ERR_INVALID_ARG, "%s: args is NULL", fn);
+    if (!a->x || !a->weight || !a->cu_seqlens || !a->chunk_indices)
+        return fail(GCL_ERR_INVALID_ARG, "%s: x, weight, cu_seqlens and chunk_indices are required", fn);
+    if (!backward && !a->y) return fail(GCL_ERR_INVALID_ARG, "%s: y is required", fn);
+    if (backward && (!a->dy || !a->dx || !a->dweight))
+        return fail(GCL_ERR_INVALID_ARG, "%s: dy, dx and dweight are required", fn);
+    if (a->t_max < 1 || a->t_max >= (int64_t(1) << 31) || a->n_max < 1)
+        return fail(GCL_ERR_INVALID_ARG, "%s: need 1 <= t_max < 2^31 and n_max >= 1", fn);
+    if (a->bt != kChunk)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (this build implements 64)", fn, a->bt);
+    if (a->W < 2 || a->W > 4)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: W=%d taps (supported: 2, 3, 4)", fn, a->W);
+    if (a->D < 8 || a->D % 8 != 0)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: D=%d channels (a positive multiple of 8)", fn, a->D);
+    if (a->dtype != GCL_F32 && a->dtype != GCL_BF16)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: dtype %d (supported: GCL_F32, GCL_BF16)", fn, a->dtype);
+    if (a->activation != GCL_ACT_NONE && a->activation != GCL_ACT_SILU)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: activation %d (supported: none, SiLU)", fn, a->activation);
+    if (!aligned16(a->x) || (a->y && !aligned16(a->y)) || (a->residual && !aligned16(a->residual)) ||
+        (a->dy && !aligned16(a->dy)) || (a->dx && !aligned16(a->dx)) ||
+        (backward && a->workspace && !aligned16(a->workspace)))
+        return fail(GCL_ERR_INVALID_ARG, "%s: x, y, residual, dy, dx and the workspace must be 16-byte aligned", fn);
+    return GCL_OK;
+}
+
+static ConvLaunch conv_launch(const gcl_conv_args *a) {
+    ConvLaunch c{};
+    c.x = a->x; c.w = a->weight; c.bias = a->bias; c.residual = a->residual; c.h0 = a->h0;
+    c.dy = a->dy; c.y = a->y; c.ht = a->ht; c.dht = a->dht;
+    c.dx = a->dx; c.dw = a->dweight; c.dbias = a->dbias; c.dh0 = a->dh0;
+    c.partial = static_cast<float *>(a->workspace);
+    c.cu_seqlens = a->cu_seqlens; c.chunk_indices = a->chunk_indices; c.dev_status = a->dev_status;
+    c.t_max = a->t_max; c.nt_max = gcl_nt_max(a->t_max, a->n_max, a->bt); c.n_max = a->n_max;
+    c.D = a->D; c.W = a->W; c.activation = a->activation; c.dtype = a->dtype;
+    return c;
+}
+
+gcl_status_t causal_conv1d_fwd(const gcl_conv_args *a, gcl_stream_t stream) {
+    g_err[0] = 0;
+    const char *fn = "causal_conv1d_fwd";
+    gcl_status_t st = conv_check(fn, a, false);
+    if (st != GCL_OK) return st;
+    return cuda_check(launch_conv_fwd(conv_launch(a), static_cast<cudaStream_t>(stream)), fn);
+}
+
+size_t gcl_causal_conv1d_bwd_workspace_bytes(const gcl_conv_args *a) {
+    if (!a || a->D <= 0 || a->W < 2 || a->W > 4 || a->n_max < 1 || a->t_max < 1 || a->bt < 1) return 0;
+    return conv_bwd_workspace_bytes(gcl_nt_max(a->t_max, a->n_max, a->bt), a->D, a->W);
+}
+
+gcl_status_t causal_conv1d_bwd(const gcl_conv_args *a, gcl_stream_t stream) {
+    g_err[0] = 0;
+    const char *fn = "causal_conv1d_bwd";
+    gcl_status_t st = conv_check(fn, a, true);
+    if (st != GCL_OK) return st;
+    const size_t need = gcl_causal_conv1d_bwd_workspace_bytes(a);
+    if (!a->workspace || a->workspace_bytes < need)
+        return fail(GCL_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    return cuda_check(launch_conv_bwd(conv_launch(a), static_cast<cudaStream_t>(stream)), fn);
+}
+
 }  // extern "C"

@@ -84,6 +84,20 @@ cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cuda
 // KDA backward on the CUDA cores: state-gradient sweep with per-channel decay, then the chunk
 // gradients (dg per key channel).
 cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s);
+// causal_conv1d (short_conv.cu)
+struct ConvLaunch {
+    const void *x, *w, *bias, *residual, *h0, *dy;
+    void *y, *ht;
+    const float *dht;
+    float *dx, *dw, *dbias, *dh0, *partial;
+    const int32_t *cu_seqlens, *chunk_indices;
+    int32_t *dev_status;
+    int64_t t_max, nt_max;
+    int32_t n_max, D, W, activation, dtype;
+};
+cudaError_t launch_conv_fwd(const ConvLaunch &a, cudaStream_t s);
+cudaError_t launch_conv_bwd(const ConvLaunch &a, cudaStream_t s);
+size_t conv_bwd_workspace_bytes(int64_t nt_max, int D, int W);
 // KDA transition-form records alone (the backward's sweep reads them).
 cudaError_t launch_prep_kda(const FwdParams &p, uint8_t *ws, cudaStream_t s);
 // Tensor-core state-gradient sweep from transition-form records (GDN, bf16, K = V = 128).

@@ -166,3 +166,37 @@ def varlen_layout(w: Workload, layout_seed: int) -> Workload:
     lens = random_lengths(n, 1, hi, layout_seed)
     return varlen(w.name, w.variant, w.dtype, lens, w.n_max, w.t_max, w.H, w.K, w.V, w.h0,
                   w.backward, seed=layout_seed, bt=w.bt)
+
+
+def make_conv_inputs(lengths, n_max: int, t_max: int, D: int, W: int, dtype: str, seed: int,
+                     h0: bool = True, bias: bool = True, residual: bool = False,
+                     pad_value: float = float("nan")):
+    """Inputs of the short convolution over the sequences ``lengths`` (n_max slots, t_max
+    token capacity): x [t_max, D] ~ N(0, 1); weight [D, W] ~ N(0, 1/W); bias [D] ~ N(0, 0.1^2);
+    residual [t_max, D] ~ N(0, 1); h0 [n_max, D, W - 1] ~ N(0, 1) (the inputs before each
+    sequence); dy [t_max, D] ~ N(0, 1); dht [n_max, D, W - 1] ~ N(0, 0.1^2) fp32.  Everything
+    but dht is rounded to bf16 when dtype is bf16; padding rows hold ``pad_value``."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = list(lengths) + [0] * (n_max - len(lengths))
+    cu = np.zeros(n_max + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    T = int(cu[-1])
+    assert T <= t_max
+
+    def rnd(a):
+        return bf16_round(a) if dtype == "bf16" else a.astype(np.float32)
+
+    def pad(a):
+        out = np.full((t_max,) + a.shape[1:], pad_value, dtype=np.float32)
+        out[:T] = a
+        return out
+
+    out = dict(cu_seqlens=cu)
+    out["x"] = pad(rnd(rng.standard_normal((T, D), dtype=np.float32)))
+    out["weight"] = rnd(rng.standard_normal((D, W), dtype=np.float32) / np.sqrt(W))
+    out["bias"] = rnd(0.1 * rng.standard_normal(D, dtype=np.float32)) if bias else None
+    out["residual"] = pad(rnd(rng.standard_normal((T, D), dtype=np.float32))) if residual else None
+    out["h0"] = rnd(rng.standard_normal((n_max, D, W - 1), dtype=np.float32)) if h0 else None
+    out["dy"] = pad(rnd(rng.standard_normal((T, D), dtype=np.float32)))
+    out["dht"] = (0.1 * rng.standard_normal((n_max, D, W - 1), dtype=np.float32)).astype(np.float32)
+    return out

@@ -275,6 +275,61 @@ size_t gcl_kda_bwd_workspace_bytes(const gcl_bwd_args *args);
 gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *args, gcl_stream_t stream);
 gcl_status_t kda_chunk_bwd(const gcl_bwd_args *args, gcl_stream_t stream);
 
+/*
+ * causal_conv1d -- the short causal depthwise convolution that precedes the chunk
+ * attention in the layer (FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and
+ * Training Paths on Ascend NPUs", section "Step 3": dense and varlen inputs, forward and
+ * backward, bias, activation and residual paths, initial and final states, fixed chunk
+ * metadata and state buffers; section "API proposal": the same chunk_indices as the chunk
+ * attention).  The pages print no formula; this library computes, per channel d and for
+ * the inputs xx_n(i) of sequence n (xx_n(i) = x[bos_n + i] for i >= 0, h0[n, d, W - 1 + i]
+ * for -(W - 1) <= i < 0, zeros without h0):
+ *
+ *   y[bos_n + p, d] = act(bias[d] + sum_{j<W} weight[d, j] xx_n(p - (W - 1) + j)) + residual
+ *   ht[n, d, k] = xx_n(len_n - (W - 1) + k),   k = 0 .. W - 2 (oldest first)
+ *
+ * act is the identity or SiLU (z / (1 + exp(-z))).  Zero-length sequences write ht = h0.
+ * The backward returns dx, dweight, dbias, dh0 of <dy, y> + <dht, ht> (the gradient of the
+ * residual is dy itself).  One struct serves both directions; fields of the other direction
+ * are ignored.  All pointers are device pointers.
+ *
+ * Supported: W in {2, 3, 4}; D a multiple of 8; bt = 64; dtype GCL_F32 or GCL_BF16 for x,
+ * weight, bias, residual, h0, y, ht and dy (the gradients are fp32); x, y, residual, dy and
+ * dx 16-byte aligned.  Launch shapes depend only on (nt_max, n_max, D); every call is
+ * graph-capturable.  Errors: INVALID_ARG / UNSUPPORTED on the host before anything is
+ * enqueued, data errors through dev_status as for the chunk attention.
+ */
+typedef enum { GCL_ACT_NONE = 0, GCL_ACT_SILU = 1 } gcl_activation_t;
+
+typedef struct gcl_conv_args {
+    const void *x;                 /* [t_max, D] dtype                                       */
+    const void *weight;            /* [D, W] dtype                                           */
+    const void *bias;              /* [D] dtype or NULL                                      */
+    const void *residual;          /* [t_max, D] dtype or NULL: added after the activation   */
+    const void *h0;                /* [n_max, D, W - 1] dtype or NULL (zeros)                */
+    void *y;                       /* forward: [t_max, D] dtype (out), live rows only        */
+    void *ht;                      /* forward: [n_max, D, W - 1] dtype (out) or NULL         */
+    const void *dy;                /* backward: [t_max, D] dtype, the gradient w.r.t. y      */
+    const float *dht;              /* backward: [n_max, D, W - 1] fp32 or NULL               */
+    float *dx;                     /* backward: [t_max, D] fp32 (out), live rows only        */
+    float *dweight;                /* backward: [D, W] fp32 (out)                            */
+    float *dbias;                  /* backward: [D] fp32 (out) or NULL                       */
+    float *dh0;                    /* backward: [n_max, D, W - 1] fp32 (out) or NULL         */
+    const int32_t *cu_seqlens;     /* [n_max + 1] int32                                      */
+    const int32_t *chunk_indices;  /* [nt_max, 2] from chunk_meta_build (bt = 64)            */
+    int32_t *dev_status;           /* [1] or NULL, as in gcl_fwd_args                        */
+    void *workspace;               /* backward: gcl_causal_conv1d_bwd_workspace_bytes()      */
+    size_t workspace_bytes;        /*   bytes (per-chunk partial sums of dweight, dbias)     */
+    int64_t t_max;                 /* token capacity                                         */
+    int32_t n_max, D, W, bt;       /* sequences, channels, taps, chunk size                  */
+    int32_t activation;            /* gcl_activation_t                                       */
+    int32_t dtype;                 /* gcl_dtype_t                                            */
+} gcl_conv_args;
+
+gcl_status_t causal_conv1d_fwd(const gcl_conv_args *args, gcl_stream_t stream);
+size_t gcl_causal_conv1d_bwd_workspace_bytes(const gcl_conv_args *args);
+gcl_status_t causal_conv1d_bwd(const gcl_conv_args *args, gcl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
