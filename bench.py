@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gcl", choices=["gcl", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[w.name for w in synth.standard_workloads()])
+                    choices=[w.name for w in synth.standard_workloads()] +
+                            [c["name"] for c in synth.conv_workloads()])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
@@ -539,13 +540,218 @@ def run_reference(args):
     }
 
 
+# ----------------------------------------------------------------------------- causal_conv1d
+CONV_METRIC = "causal_conv1d fwd+bwd tokens/s on 1 GB300 and % of HBM roofline"
+
+
+def conv_bytes(c):
+    """Algorithmic HBM bytes of one forward and one backward call: forward reads x and writes
+    y (and h0 -> ht); backward reads x and dy, writes dx (fp32) and dw, db, dh0."""
+    b = 2 if c["dtype"] == "bf16" else 4
+    T, D, W, N = c["B"] * c["T"], c["D"], c["W"], c["B"]
+    state = N * D * (W - 1)
+    fwd = T * D * 2 * b + D * (W + 1) * b + 2 * state * b
+    bwd = T * D * (2 * b + 4) + D * (W + 1) * (b + 4) + state * (b + 4 + 4)
+    return fwd, bwd
+
+
+def run_conv_gpu(args, rank, world, dist):
+    import torch
+    import chunked_gated_linear_gb300 as gcl
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    c = synth.conv_workload_by_name(args.workload)
+    B, T, D, W = c["B"], c["T"], c["D"], c["W"]
+    tm = B * T
+    x = synth.make_conv_inputs([T] * B, B, tm, D, W, c["dtype"], seed=c["seed"] + 1000 * rank)
+    td = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
+    t = {k: torch.from_numpy(v).to(dev).to(td) for k, v in x.items()
+         if v is not None and k not in ("cu_seqlens", "dht")}
+    t["cu"] = torch.from_numpy(x["cu_seqlens"]).to(dev)
+    t["dht"] = torch.from_numpy(x["dht"]).to(dev)
+    ntm = gcl.nt_max(tm, B, 64)
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    t.update(idx=torch.empty((ntm, 2), **i32), off=torch.empty((B + 1,), **i32),
+             status=torch.zeros((1,), **i32), y=torch.empty((tm, D), dtype=td, device=dev),
+             ht=torch.empty((B, D, W - 1), dtype=td, device=dev), dx=torch.empty((tm, D), **f32),
+             dw=torch.empty((D, W), **f32), db=torch.empty((D,), **f32),
+             dh0=torch.empty((B, D, W - 1), **f32))
+    common = (t["x"], t["weight"], t["cu"], t["idx"])
+    kw = dict(bias=t.get("bias"), h0=t.get("h0"), dev_status=t["status"], activation=c["act"])
+    fa = gcl.conv_args(*common, y=t["y"], ht=t["ht"], **kw)
+    bkw = dict(dy=t["dy"], dht=t["dht"], dx=t["dx"], dweight=t["dw"], dbias=t["db"], dh0=t["dh0"], **kw)
+    t["ws"] = torch.empty(gcl.causal_conv1d_bwd_workspace_bytes(*common, **bkw), dtype=torch.uint8,
+                          device=dev)
+    ba = gcl.conv_args(*common, workspace=t["ws"], **bkw)
+    lib = gcl.lib()
+    meta_args = (t["cu"].data_ptr(), B, tm, 64, ntm, t["idx"].data_ptr(), t["off"].data_ptr(),
+                 None, t["status"].data_ptr())
+    stream = torch.cuda.current_stream()
+    s = ctypes.c_void_p(stream.cuda_stream)
+
+    def step(ev=None):
+        if lib.chunk_meta_build(*meta_args, s) != 0:
+            raise RuntimeError(gcl.lib().gcl_last_error().decode())
+        if ev is not None:
+            ev[0].record(stream)
+        if lib.causal_conv1d_fwd(ctypes.byref(fa), s) != 0:
+            raise RuntimeError(gcl.lib().gcl_last_error().decode())
+        if ev is not None:
+            ev[1].record(stream)
+        if lib.causal_conv1d_bwd(ctypes.byref(ba), s) != 0:
+            raise RuntimeError(gcl.lib().gcl_last_error().decode())
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(t["status"].item()) == 0
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(K):
+        ev[i][0].record(stream)
+        step(ev[i][1:])
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    tot = reduce_max([sum(e[0].elapsed_time(e[3]) for e in ev), sum(e[1].elapsed_time(e[2]) for e in ev),
+                      sum(e[2].elapsed_time(e[3]) for e in ev)], dist, dev)
+    ms_step, ms_fwd, ms_bwd = (v / K for v in tot)
+    e2e = conv_e2e(torch, lib, t, x, fa, ba, step, stream, args.e2e_steps, world, dist, tm)
+    clk = clocks.summary()
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    fb, bb = conv_bytes(c)
+    return {
+        "metric": CONV_METRIC, "value": job_throughput(tm, world, ms_step), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"],
+        "data": "synthetic (seeded PCG64; x, dy N(0,1), weight N(0,1/W), bias N(0,0.1^2), "
+                "h0 N(0,1), dht N(0,0.1^2))",
+        "config": {"workload": c["name"], "tokens_per_step": tm, "channels": D, "taps": W,
+                   "activation": c["act"], "parallelism": f"replicas x{world}",
+                   "l2": f"inputs {2 * tm * D * (2 if c['dtype'] == 'bf16' else 4) / 2**20:.0f} MiB "
+                         f"per step (> L2); no flush"},
+        "roofline": {"bound": "hbm", "achieved": bb / (ms_bwd * 1e-3) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": bb / (ms_bwd * 1e-3) / 1e9 / peak,
+                     "traffic": traffic_record(c["name"]), "kernel": "causal_conv1d_bwd",
+                     "kernel_ms": ms_bwd, "algorithmic_bytes_per_launch": bb, "peak_source": peak_kind},
+        "roofline_fwd": {"bound": "hbm", "achieved": fb / (ms_fwd * 1e-3) / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac": fb / (ms_fwd * 1e-3) / 1e9 / peak,
+                         "kernel": "causal_conv1d_fwd", "kernel_ms": ms_fwd,
+                         "algorithmic_bytes_per_launch": fb},
+        "e2e": e2e,
+        "gpu_launches": K * 4,
+        "clocks": clk,
+    }
+
+
+def conv_e2e(torch, lib, t, x, fa, ba, step, stream, steps, world, dist, tm):
+    """The conv step through the C ABI with pinned host buffers: H2D of x, dy (and the small
+    weight, bias, h0, dht, cu_seqlens) each step, D2H of y and dx."""
+    names = [n for n in ("x", "weight", "bias", "h0", "dy", "dht", "cu") if n in t]
+    host = {n: torch.empty_like(t[n], device="cpu").pin_memory() for n in names}
+    for n in names:
+        host[n].copy_(t[n])
+    out_h = {n: torch.empty_like(t[n], device="cpu").pin_memory() for n in ("y", "dx")}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = sum(out_h[n].numel() * out_h[n].element_size() for n in out_h)
+    times = []
+    for i in range(steps + 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for n in names:
+            t[n].copy_(host[n], non_blocking=True)
+        step()
+        for n in out_h:
+            out_h[n].copy_(t[n], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    ms = reduce_max([float(np.mean(times))], dist, t["x"].device)[0]
+    return {"value": job_throughput(tm, world, ms), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def conv_oracle_sample(c, x, tokens):
+    """The conv oracle (forward and backward) on the first `tokens` tokens of every sequence;
+    returns (seconds, tokens processed)."""
+    import oracle
+    cu = x["cu_seqlens"].astype(np.int64)
+    rows, new_cu = [], [0]
+    for n in range(len(cu) - 1):
+        st, en = int(cu[n]), int(min(cu[n + 1], cu[n] + tokens))
+        rows.append(np.arange(st, en))
+        new_cu.append(new_cu[-1] + (en - st))
+    rows = np.concatenate(rows)
+    xs, dys = x["x"][rows], x["dy"][rows]
+    t0 = time.perf_counter()
+    oracle.conv_fwd(xs, x["weight"], x["bias"], None, x["h0"], new_cu, activation=c["act"])
+    oracle.conv_bwd(xs, x["weight"], x["bias"], x["h0"], new_cu, dys, x["dht"], activation=c["act"])
+    return time.perf_counter() - t0, len(rows)
+
+
+def conv_cpu_baseline(c, budget_s=12.0):
+    x = synth.make_conv_inputs([c["T"]] * c["B"], c["B"], c["B"] * c["T"], c["D"], c["W"],
+                               c["dtype"], seed=c["seed"])
+    dt, n = conv_oracle_sample(c, x, 16)                  # calibration
+    tokens = int(min(max(16, budget_s * n / max(dt, 1e-6) / c["B"]), c["T"]))
+    dt, n = conv_oracle_sample(c, x, tokens)
+    return {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy forward + backward, first {tokens} tokens of every sequence, "
+                      f"all {c['D']} channels ({n} tokens, {dt:.1f} s)"}
+
+
+def run_conv_reference(args):
+    c = synth.conv_workload_by_name(args.workload)
+    x = synth.make_conv_inputs([c["T"]] * c["B"], c["B"], c["B"] * c["T"], c["D"], c["W"],
+                               c["dtype"], seed=c["seed"])
+    dt, n = conv_oracle_sample(c, x, 16)
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    tokens = int(min(max(1, budget * n / max(dt, 1e-6) / c["B"]), c["T"]))
+    for _ in range(args.warmup):
+        conv_oracle_sample(c, x, tokens)
+    times = []
+    for _ in range(args.steps):
+        dt, n = conv_oracle_sample(c, x, tokens)
+        times.append(dt)
+    sec = float(np.mean(times))
+    value = n / sec
+    sample = (f"fp64 numpy forward + backward on one host core, per step the first {tokens} "
+              f"tokens of every sequence, all {c['D']} channels")
+    return {
+        "impl": "reference", "metric": CONV_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": c["name"], "tokens_per_step": c["B"] * c["T"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    conv = args.workload in [c["name"] for c in synth.conv_workloads()]
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(run_conv_reference(args) if conv else run_reference(args)), flush=True)
         return
     dist = None
     if world > 1:
@@ -554,11 +760,14 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist_.init_process_group("nccl")
         dist = dist_
-    line = run_gpu(args, rank, world, dist)
+    line = run_conv_gpu(args, rank, world, dist) if conv else run_gpu(args, rank, world, dist)
     if rank == 0:
         if not args.no_cpu_baseline:
-            w = resolve_workload(args)
-            line["cpu_baseline"] = cpu_baseline(w, synth.make_inputs(w))
+            if conv:
+                line["cpu_baseline"] = conv_cpu_baseline(synth.conv_workload_by_name(args.workload))
+            else:
+                w = resolve_workload(args)
+                line["cpu_baseline"] = cpu_baseline(w, synth.make_inputs(w))
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

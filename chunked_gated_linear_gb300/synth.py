@@ -200,3 +200,18 @@ def make_conv_inputs(lengths, n_max: int, t_max: int, D: int, W: int, dtype: str
     out["dy"] = pad(rnd(rng.standard_normal((T, D), dtype=np.float32)))
     out["dht"] = (0.1 * rng.standard_normal((n_max, D, W - 1), dtype=np.float32)).astype(np.float32)
     return out
+
+
+def conv_workloads():
+    """Short-convolution workloads (forward + backward per step): the dense batch of the
+    forward+backward attention workload, D = 2048 channels (16 heads x 128), W = 4 taps, SiLU,
+    bias and initial states."""
+    return [dict(name="conv_fwdbwd_bf16_B4_T8192_D2048_W4", B=4, T=8192, D=2048, W=4,
+                 dtype="bf16", act="silu", seed=40)]
+
+
+def conv_workload_by_name(name: str):
+    for c in conv_workloads():
+        if c["name"] == name:
+            return c
+    raise KeyError(name)
