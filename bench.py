@@ -711,9 +711,13 @@ def conv_cpu_baseline(c, budget_s=12.0):
     dt, n = conv_oracle_sample(c, x, 16)                  # calibration
     tokens = int(min(max(16, budget_s * n / max(dt, 1e-6) / c["B"]), c["T"]))
     dt, n = conv_oracle_sample(c, x, tokens)
+    reps = 1
+    while dt < 0.8 * budget_s and reps < 50:             # the whole workload fits: repeat it
+        d2, n2 = conv_oracle_sample(c, x, tokens)
+        dt, n, reps = dt + d2, n + n2, reps + 1
     return {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"fp64 numpy forward + backward, first {tokens} tokens of every sequence, "
-                      f"all {c['D']} channels ({n} tokens, {dt:.1f} s)"}
+                      f"all {c['D']} channels, {reps} run(s) ({n} tokens, {dt:.1f} s)"}
 
 
 def run_conv_reference(args):

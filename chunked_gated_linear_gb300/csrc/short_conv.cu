@@ -9,15 +9,16 @@
 //   y[bos + p] = act(b + sum_j w[:, j] xx_n(p - (W - 1) + j)) + r[bos + p],
 //   ht[n, :, k] = xx_n(len - (W - 1) + k)   (k = 0 .. W - 2, oldest first).
 // The work list is chunk_indices (64-token chunks), so the grid depends only on the
-// capacities: one CTA per (row, block of 1024 channels); each thread streams 8 channels
-// through its chunk with the W - 1 previous inputs in registers.  Extra blocks after the
-// chunk rows pass the state through for zero-length sequences.  The path is HBM-bound:
-// every input is read once (plus W - 1 halo rows per chunk) and every output written once.
+// capacities: one CTA per (row, block of channels), plus one block per sequence slot that
+// passes the state through for zero-length sequences.  The path is HBM-bound: a CTA stages its
+// chunk's rows and the W - 1 rows before them (the previous chunk, or the initial state) into
+// shared memory with independent 16-byte loads, so every byte of the chunk is in flight at
+// once, then each thread produces whole output rows of 8 channels from shared memory.
 //
-// Backward (reverse mode of <dy, y> + <dht, ht>): per chunk, the same walk recomputes the
-// pre-activation up to W - 1 positions past the chunk, forms dpre = dy act'(pre), and
+// Backward (reverse mode of <dy, y> + <dht, ht>): a CTA also stages dy and the W - 1 rows
+// after the chunk, forms dpre = dy act'(pre) once in shared memory, then
 //   dx[p] = sum_j dpre[p + W - 1 - j] w[:, j] (+ dht for the last W - 1 positions),
-//   dh0 from the first chunk of each sequence, dw and db as per-chunk partial sums that a
+//   dh0 from the first chunk of each sequence, and dw, db as per-chunk partial sums that a
 //   second kernel adds over the chunks in a fixed order (no atomics: reproducible).
 #include "gcl_internal.cuh"
 
@@ -25,9 +26,10 @@ namespace gcl {
 namespace {
 
 constexpr int C = kChunk;
-constexpr int kConvThreads = 128;
-constexpr int kChannelsPerThread = 8;
-constexpr int kChannelsPerBlock = kConvThreads * kChannelsPerThread;
+constexpr int kConvThreads = 256;
+constexpr int kChannelsPerThread = 8;                  // one 16-byte vector of bf16
+constexpr int kFwdChannels = 256;                      // channels per forward CTA
+constexpr int kBwdChannels = 128;                      // channels per backward CTA
 
 struct ConvParams {
     const void *x, *w, *bias, *residual, *h0, *dy;
@@ -82,9 +84,10 @@ __device__ __forceinline__ void st1(T *p, float v) { p[0] = (T)v; }
 template <>
 __device__ __forceinline__ void st1<__nv_bfloat16>(__nv_bfloat16 *p, float v) { p[0] = __float2bfloat16_rn(v); }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+// SiLU and its derivative with the fast reciprocal (a few ulp; the path is bound by memory)
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 __device__ __forceinline__ float silu_grad(float z) {
-    const float s = 1.f / (1.f + __expf(-z));
+    const float s = __fdividef(1.f, 1.f + __expf(-z));
     return s * (1.f + z * (1.f - s));
 }
 
@@ -108,253 +111,329 @@ __device__ __forceinline__ bool conv_row(const ConvParams &p, int j, int &n, int
 }
 
 // A zero-length sequence n (block index past the chunk rows): ht = h0 (or zeros); in the
-// backward dh0 = dht (or zeros).  Returns true if this block was such a block.
+// backward dh0 = dht (or zeros).  Returns true if this block was such a block (or past them).
 template <typename T, int W>
-__device__ __forceinline__ bool conv_empty_sequence(const ConvParams &p, bool backward) {
+__device__ __forceinline__ bool conv_empty_sequence(const ConvParams &p, int channels, bool backward) {
     const int64_t i = (int64_t)blockIdx.x - p.nt_max;
     if (i < 0) return false;
     const int n = (int)i;
     if (n >= p.n_max) return true;
     const int64_t bos = p.cu[n], eos = p.cu[n + 1];
     if (eos != bos) return true;
-    const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * kChannelsPerThread;
-    if (c0 >= p.D) return true;
-    for (int e = 0; e < kChannelsPerThread; ++e)
-        for (int k = 0; k < W - 1; ++k) {
-            const int64_t o = ((int64_t)n * p.D + c0 + e) * (W - 1) + k;
-            if (!backward) {
-                if (p.ht) st1(static_cast<T *>(p.ht) + o, p.h0 ? ld1(static_cast<const T *>(p.h0) + o) : 0.f);
-            } else if (p.dh0) {
-                p.dh0[o] = p.dht ? p.dht[o] : 0.f;
-            }
+    for (int e = threadIdx.x; e < channels * (W - 1); e += kConvThreads) {
+        const int c = blockIdx.y * channels + e / (W - 1), k = e % (W - 1);
+        if (c >= p.D) continue;
+        const int64_t o = ((int64_t)n * p.D + c) * (W - 1) + k;
+        if (!backward) {
+            if (p.ht) st1(static_cast<T *>(p.ht) + o, p.h0 ? ld1(static_cast<const T *>(p.h0) + o) : 0.f);
+        } else if (p.dh0) {
+            p.dh0[o] = p.dht ? p.dht[o] : 0.f;
         }
+    }
     return true;
 }
 
+// Stage rows [r_lo, r_hi) of the chunk (relative to t0; rows < 0 come from the previous chunk,
+// or from the initial state when the chunk is the sequence's first) of `channels` channels
+// starting at c_base into tile[(r - r_lo)][channels] in the input type.  Rows of the initial
+// state without h0 are zeros.  Channels at or past D are not touched.  The rows of the input
+// are asynchronous copies (all in flight at once): conv_stage_wait() before the barrier.
 template <typename T, int W>
-__global__ void __launch_bounds__(kConvThreads)
+__device__ __forceinline__ void conv_stage(const ConvParams &p, const T *src, T *tile, int channels, int c_base,
+                                           int64_t t0, int ic, int n, int r_lo, int r_hi) {
+    const int vec = channels / kChannelsPerThread;          // 16-byte vectors per row (bf16)
+    for (int e = threadIdx.x; e < (r_hi - r_lo) * vec; e += kConvThreads) {
+        const int rr = e / vec, cv = e % vec, r = r_lo + rr, c = c_base + cv * kChannelsPerThread;
+        if (c >= p.D) continue;
+        T *dst = tile + (int64_t)rr * channels + cv * kChannelsPerThread;
+        if (r >= 0 || ic > 0) {                           // asynchronous 16-byte copies
+            const T *s = src + (t0 + r) * p.D + c;
+            constexpr int kPer16 = 16 / (int)sizeof(T);  // elements per 16-byte copy
+#pragma unroll
+            for (int h = 0; h < kChannelsPerThread / kPer16; ++h)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                 (uint32_t)__cvta_generic_to_shared(dst + h * kPer16)),
+                             "l"(s + h * kPer16)
+                             : "memory");
+        } else {
+#pragma unroll
+            for (int q = 0; q < kChannelsPerThread; ++q)
+                st1(dst + q, p.h0 ? ld1(static_cast<const T *>(p.h0) + ((int64_t)n * p.D + c + q) * (W - 1) +
+                                        (W - 1) + r)
+                                  : 0.f);
+        }
+    }
+}
+
+__device__ __forceinline__ void conv_stage_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <typename T, int W>
+__global__ void __launch_bounds__(kConvThreads, 4)
 conv_fwd_kernel(ConvParams p) {
+    constexpr int CB = kFwdChannels * 2 / (int)sizeof(T);   // 34 KB tiles for both types
+    constexpr int G = CB / kChannelsPerThread, RL = kConvThreads / G;
+    __shared__ __align__(16) T tile[(C + W - 1) * CB];
     if (status_blocks(p.status)) return;
-    if (conv_empty_sequence<T, W>(p, false)) return;
+    if (conv_empty_sequence<T, W>(p, CB, false)) return;
     int n, ic;
     int64_t bos, eos;
     if (!conv_row(p, blockIdx.x, n, ic, bos, eos)) return;
-    const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * kChannelsPerThread;
-    if (c0 >= p.D) return;
-    const int D = p.D;
+    const int D = p.D, cb0 = blockIdx.y * CB;
     const int64_t t0 = bos + (int64_t)ic * C;
     const int len = (int)(eos - t0 < C ? eos - t0 : C);
-    const T *x = static_cast<const T *>(p.x);
-    const T *r = static_cast<const T *>(p.residual);
-    T *y = static_cast<T *>(p.y);
-    float w[W][kChannelsPerThread], b[kChannelsPerThread], win[W - 1][kChannelsPerThread];
+    conv_stage<T, W>(p, static_cast<const T *>(p.x), tile, CB, cb0, t0, ic, n, -(W - 1), len);
+    conv_stage_wait();
+    __syncthreads();
+    // thread: 8 channels (vector g) of rows rr, rr + RL, ... (a warp: one row, 512 bytes)
+    const int g = threadIdx.x % G, rr = threadIdx.x / G, c0 = cb0 + g * kChannelsPerThread;
+    if (c0 < D) {
+        float w[W][kChannelsPerThread], b[kChannelsPerThread];
 #pragma unroll
-    for (int e = 0; e < kChannelsPerThread; ++e) {
+        for (int e = 0; e < kChannelsPerThread; ++e) {
 #pragma unroll
-        for (int j = 0; j < W; ++j) w[j][e] = ld1(static_cast<const T *>(p.w) + (int64_t)(c0 + e) * W + j);
-        b[e] = p.bias ? ld1(static_cast<const T *>(p.bias) + c0 + e) : 0.f;
-    }
-    // the W - 1 inputs before the chunk: the previous rows, or the initial state for chunk 0
-#pragma unroll
-    for (int k = 0; k < W - 1; ++k) {
-        if (ic > 0) {
-            load8(x + (t0 - (W - 1) + k) * D + c0, win[k]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e)
-                win[k][e] = p.h0 ? ld1(static_cast<const T *>(p.h0) + ((int64_t)n * D + c0 + e) * (W - 1) + k) : 0.f;
+            for (int j = 0; j < W; ++j) w[j][e] = ld1(static_cast<const T *>(p.w) + (int64_t)(c0 + e) * W + j);
+            b[e] = p.bias ? ld1(static_cast<const T *>(p.bias) + c0 + e) : 0.f;
         }
-    }
-    constexpr int G = 8;                                  // rows loaded ahead
-    for (int g0 = 0; g0 < len; g0 += G) {
-        float xs[G][kChannelsPerThread], rs[G][kChannelsPerThread];
+        const T *r = static_cast<const T *>(p.residual);
+        T *y = static_cast<T *>(p.y);
+        for (int row = rr; row < len; row += RL) {
+            float res[kChannelsPerThread];
+            if (r) load8(r + (t0 + row) * D + c0, res);
+            float a[kChannelsPerThread];
 #pragma unroll
-        for (int q = 0; q < G; ++q) {
-            if (g0 + q < len) {
-                load8(x + (t0 + g0 + q) * D + c0, xs[q]);
-                if (r) load8(r + (t0 + g0 + q) * D + c0, rs[q]);
+            for (int e = 0; e < kChannelsPerThread; ++e) a[e] = b[e];
+#pragma unroll
+            for (int j = 0; j < W; ++j) {               // tile row row + j holds xx(row - (W - 1) + j)
+                float xv[kChannelsPerThread];
+                load8(tile + (int64_t)(row + j) * CB + g * kChannelsPerThread, xv);
+#pragma unroll
+                for (int e = 0; e < kChannelsPerThread; ++e) a[e] = fmaf(w[j][e], xv[e], a[e]);
             }
-        }
 #pragma unroll
-        for (int q = 0; q < G; ++q) {
-            if (g0 + q < len) {
-                float out[kChannelsPerThread];
-#pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e) {
-                    float a = b[e];
-#pragma unroll
-                    for (int j = 0; j < W - 1; ++j) a = fmaf(w[j][e], win[j][e], a);
-                    a = fmaf(w[W - 1][e], xs[q][e], a);
-                    if (p.act == GCL_ACT_SILU) a = silu(a);
-                    out[e] = r ? a + rs[q][e] : a;
-                }
-                store8(y + (t0 + g0 + q) * D + c0, out);
-#pragma unroll
-                for (int j = 0; j < W - 2; ++j)
-#pragma unroll
-                    for (int e = 0; e < kChannelsPerThread; ++e) win[j][e] = win[j + 1][e];
-#pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e) win[W - 2][e] = xs[q][e];
+            for (int e = 0; e < kChannelsPerThread; ++e) {
+                if (p.act == GCL_ACT_SILU) a[e] = silu(a[e]);
+                if (r) a[e] += res[e];
             }
+            store8(y + (t0 + row) * D + c0, a);
         }
     }
     if (t0 + len == eos && p.ht) {                        // the last chunk: the final state
-#pragma unroll
-        for (int k = 0; k < W - 1; ++k)
-#pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e)
-                st1(static_cast<T *>(p.ht) + ((int64_t)n * D + c0 + e) * (W - 1) + k, win[k][e]);
+        for (int e = threadIdx.x; e < CB * (W - 1); e += kConvThreads) {
+            const int c = e / (W - 1), k = e % (W - 1);
+            if (cb0 + c < D)                              // tile row len + k: xx(len - (W - 1) + k)
+                static_cast<T *>(p.ht)[((int64_t)n * D + cb0 + c) * (W - 1) + k] = tile[(int64_t)(len + k) * CB + c];
+        }
     }
 }
+// Column of channel c in a dpre row: each 8-channel vector is split into two float4 halves
+// stored in the two halves of the row.
+__device__ __forceinline__ int dp_col(int c, int cb) { return ((c & 4) ? cb / 2 : 0) + ((c >> 3) << 2) + (c & 3); }
+
+// Backward tiles (dynamic shared memory): x rows [-(W - 1), C + W - 1) and dy rows [0, C + W - 1)
+// in the input type, dpre rows [0, C + W - 1) in fp32, CB channels each.
+template <typename T, int W>
+struct ConvBwdLayout {
+    static constexpr int CB = kBwdChannels * 2 / (int)sizeof(T);
+    static constexpr int RX = C + 2 * (W - 1), RQ = C + W - 1;
+    static constexpr size_t oX = 0, oDY = oX + (size_t)RX * CB * sizeof(T);
+    static constexpr size_t oDP = (oDY + (size_t)RQ * CB * sizeof(T) + 15) / 16 * 16;
+    static constexpr size_t bytes = oDP + (size_t)RQ * CB * sizeof(float);
+    static_assert(kConvThreads % CB == 0 && (size_t)(kConvThreads / CB) * (W + 1) * CB * 4 <= RQ * CB * sizeof(T),
+                  "the dy tile holds the per-group partial sums");
+};
 
 template <typename T, int W>
 __global__ void __launch_bounds__(kConvThreads)
 conv_bwd_kernel(ConvParams p) {
+    using Lay = ConvBwdLayout<T, W>;
+    constexpr int CB = Lay::CB, G = CB / kChannelsPerThread, RL = kConvThreads / G;
+    extern __shared__ __align__(16) uint8_t smem[];
+    T *sx = reinterpret_cast<T *>(smem + Lay::oX);
+    T *sdy = reinterpret_cast<T *>(smem + Lay::oDY);
+    float *sdp = reinterpret_cast<float *>(smem + Lay::oDP);
     if (status_blocks(p.status)) return;
-    if (conv_empty_sequence<T, W>(p, true)) return;
+    if (conv_empty_sequence<T, W>(p, CB, true)) return;
     int n, ic;
     int64_t bos, eos;
     if (!conv_row(p, blockIdx.x, n, ic, bos, eos)) return;
-    const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * kChannelsPerThread;
-    if (c0 >= p.D) return;
-    const int D = p.D;
+    const int D = p.D, cb0 = blockIdx.y * CB;
     const int64_t t0 = bos + (int64_t)ic * C;
-    const int L = (int)(eos - bos);                       // sequence length
-    const int P0 = (int)(t0 - bos);                       // sequence position of the chunk's row 0
+    const int L = (int)(eos - bos), P0 = (int)(t0 - bos);
     const int len = L - P0 < C ? L - P0 : C;
-    const T *x = static_cast<const T *>(p.x);
-    const T *dy = static_cast<const T *>(p.dy);
-    float w[W][kChannelsPerThread], b[kChannelsPerThread], win[W - 1][kChannelsPerThread];
-    float dpre[W][kChannelsPerThread];                    // dpre at positions q - W + 1 .. q
-    float dw[W][kChannelsPerThread], db[kChannelsPerThread];
+    const int nq = (L - P0 < len + W - 1) ? L - P0 : len + W - 1;   // positions with a pre-activation
+    conv_stage<T, W>(p, static_cast<const T *>(p.x), sx, CB, cb0, t0, ic, n, -(W - 1), nq);
+    conv_stage<T, W>(p, static_cast<const T *>(p.dy), sdy, CB, cb0, t0, ic, n, 0, nq);
+    conv_stage_wait();
+    __syncthreads();
+    const int g = threadIdx.x % G, rr = threadIdx.x / G, c0 = cb0 + g * kChannelsPerThread;
+    // dpre rows hold a thread's 8 channels as two float4 in the two halves of the row, so the
+    // 32-byte vectors of neighbouring lanes do not share banks (dp_col maps a channel)
+    auto dp_store = [&](int q, const float *v) {
+        float *row = sdp + (int64_t)q * CB;
+        *reinterpret_cast<float4 *>(row + g * 4) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4 *>(row + CB / 2 + g * 4) = make_float4(v[4], v[5], v[6], v[7]);
+    };
+    auto dp_load = [&](int q, float *v) {
+        const float *row = sdp + (int64_t)q * CB;
+        const float4 lo = *reinterpret_cast<const float4 *>(row + g * 4);
+        const float4 hi = *reinterpret_cast<const float4 *>(row + CB / 2 + g * 4);
+        v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w; v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+    };
+    float w[W][kChannelsPerThread];
+    if (c0 < D) {
 #pragma unroll
-    for (int e = 0; e < kChannelsPerThread; ++e) {
+        for (int e = 0; e < kChannelsPerThread; ++e)
 #pragma unroll
-        for (int j = 0; j < W; ++j) {
-            w[j][e] = ld1(static_cast<const T *>(p.w) + (int64_t)(c0 + e) * W + j);
-            dw[j][e] = 0.f;
-            dpre[j][e] = 0.f;
-        }
-        b[e] = p.bias ? ld1(static_cast<const T *>(p.bias) + c0 + e) : 0.f;
-        db[e] = 0.f;
-    }
+            for (int j = 0; j < W; ++j) w[j][e] = ld1(static_cast<const T *>(p.w) + (int64_t)(c0 + e) * W + j);
+        float b[kChannelsPerThread];
 #pragma unroll
-    for (int k = 0; k < W - 1; ++k) {
-        if (ic > 0) {
-            load8(x + (t0 - (W - 1) + k) * D + c0, win[k]);
-        } else {
+        for (int e = 0; e < kChannelsPerThread; ++e) b[e] = p.bias ? ld1(static_cast<const T *>(p.bias) + c0 + e) : 0.f;
+        // dpre at chunk positions q < len + W - 1 (zero past the sequence)
+        for (int q = rr; q < len + W - 1; q += RL) {
+            float d[kChannelsPerThread];
+            if (q < nq) {
+                float a[kChannelsPerThread], gy[kChannelsPerThread];
 #pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e)
-                win[k][e] = p.h0 ? ld1(static_cast<const T *>(p.h0) + ((int64_t)n * D + c0 + e) * (W - 1) + k) : 0.f;
-        }
-    }
-    // walk q = 0 .. len + W - 2: the pre-activation at chunk row q (if it is in the sequence),
-    // then the input gradient of chunk row p = q - (W - 1) (the initial state for p < 0, chunk 0)
-    for (int q = 0; q < len + W - 1; ++q) {
-        float dp[kChannelsPerThread];
-        const bool in_seq = P0 + q < L;
-        if (in_seq) {
-            float xv[kChannelsPerThread], g[kChannelsPerThread];
-            load8(x + (t0 + q) * D + c0, xv);
-            load8(dy + (t0 + q) * D + c0, g);
+                for (int e = 0; e < kChannelsPerThread; ++e) a[e] = b[e];
 #pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e) {
-                float a = b[e];
+                for (int j = 0; j < W; ++j) {           // x tile row q + j holds xx(q - (W - 1) + j)
+                    float xv[kChannelsPerThread];
+                    load8(sx + (int64_t)(q + j) * CB + g * kChannelsPerThread, xv);
 #pragma unroll
-                for (int j = 0; j < W - 1; ++j) a = fmaf(w[j][e], win[j][e], a);
-                a = fmaf(w[W - 1][e], xv[e], a);
-                dp[e] = p.act == GCL_ACT_SILU ? g[e] * silu_grad(a) : g[e];
-                if (q < len) {                            // this chunk's tokens own dw, db
-                    db[e] += dp[e];
-#pragma unroll
-                    for (int j = 0; j < W - 1; ++j) dw[j][e] = fmaf(dp[e], win[j][e], dw[j][e]);
-                    dw[W - 1][e] = fmaf(dp[e], xv[e], dw[W - 1][e]);
+                    for (int e = 0; e < kChannelsPerThread; ++e) a[e] = fmaf(w[j][e], xv[e], a[e]);
                 }
+                load8(sdy + (int64_t)q * CB + g * kChannelsPerThread, gy);
+#pragma unroll
+                for (int e = 0; e < kChannelsPerThread; ++e)
+                    d[e] = p.act == GCL_ACT_SILU ? gy[e] * silu_grad(a[e]) : gy[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < kChannelsPerThread; ++e) d[e] = 0.f;
             }
-#pragma unroll
-            for (int j = 0; j < W - 2; ++j)
-#pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e) win[j][e] = win[j + 1][e];
-#pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e) win[W - 2][e] = xv[e];
-        } else {
-#pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e) dp[e] = 0.f;
+            dp_store(q, d);
         }
-#pragma unroll
-        for (int j = 0; j < W - 1; ++j)
-#pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e) dpre[j][e] = dpre[j + 1][e];
-#pragma unroll
-        for (int e = 0; e < kChannelsPerThread; ++e) dpre[W - 1][e] = dp[e];
-        // input gradient of row p = q - (W - 1): sum_j dpre(p + W - 1 - j) w_j = sum_j dpre[W-1-j] w_j
-        const int pr = q - (W - 1);
-        const int P = P0 + pr;                            // its sequence position (< 0: initial state)
-        if (pr >= 0 || ic == 0) {
+    }
+    __syncthreads();
+    if (c0 < D) {                                         // dx rows of the chunk
+        for (int pr = rr; pr < len; pr += RL) {
             float gx[kChannelsPerThread];
 #pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e) {
-                float a = 0.f;
+            for (int e = 0; e < kChannelsPerThread; ++e) gx[e] = 0.f;
 #pragma unroll
-                for (int j = 0; j < W; ++j) a = fmaf(dpre[W - 1 - j][e], w[j][e], a);
-                gx[e] = a;
+            for (int j = 0; j < W; ++j) {               // dpre at position pr + W - 1 - j
+                float dv[kChannelsPerThread];
+                dp_load(pr + W - 1 - j, dv);
+#pragma unroll
+                for (int e = 0; e < kChannelsPerThread; ++e) gx[e] = fmaf(dv[e], w[j][e], gx[e]);
             }
-            const int kf = P - (L - (W - 1));             // slot of the final state it lands in
-            if (p.dht && kf >= 0 && kf < W - 1) {
+            const int kf = P0 + pr - (L - (W - 1));       // slot of the final state it lands in
+            if (p.dht && kf >= 0) {
 #pragma unroll
                 for (int e = 0; e < kChannelsPerThread; ++e)
                     gx[e] += p.dht[((int64_t)n * D + c0 + e) * (W - 1) + kf];
             }
-            if (pr >= 0) {
-                float *dst = p.dx + (t0 + pr) * D + c0;
-                *reinterpret_cast<float4 *>(dst) = make_float4(gx[0], gx[1], gx[2], gx[3]);
-                *reinterpret_cast<float4 *>(dst + 4) = make_float4(gx[4], gx[5], gx[6], gx[7]);
-            } else if (p.dh0) {
-#pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e)
-                    p.dh0[((int64_t)n * D + c0 + e) * (W - 1) + (P + (W - 1))] = gx[e];
-            }
+            store8(p.dx + (t0 + pr) * D + c0, gx);
         }
     }
-    // partial sums of this chunk: [row][W + 1][D] (taps, then the bias)
-    float *part = p.partial + (int64_t)blockIdx.x * (W + 1) * D + c0;
+    if (ic == 0 && p.dh0) {                               // the initial state: positions -(W - 1) .. -1
+        for (int e = threadIdx.x; e < CB * (W - 1); e += kConvThreads) {
+            const int c = e / (W - 1), k = e % (W - 1), pos = k - (W - 1);
+            if (cb0 + c >= D) continue;
+            float a = 0.f;
 #pragma unroll
-    for (int j = 0; j < W; ++j) store8(part + (int64_t)j * D, dw[j]);
-    store8(part + (int64_t)W * D, db);
+            for (int j = 0; j < W; ++j) {
+                const int q = pos + W - 1 - j;
+                if (q >= 0 && q < len + W - 1)
+                    a = fmaf(sdp[(int64_t)q * CB + dp_col(c, CB)],
+                             ld1(static_cast<const T *>(p.w) + (int64_t)(cb0 + c) * W + j), a);
+            }
+            const int kf = pos - (L - (W - 1));
+            if (p.dht && kf >= 0) a += p.dht[((int64_t)n * D + cb0 + c) * (W - 1) + kf];
+            p.dh0[((int64_t)n * D + cb0 + c) * (W - 1) + k] = a;
+        }
+    }
+    // dw, db of this chunk's tokens: NG row groups per channel, then added in group order
+    constexpr int NG = kConvThreads / CB;
+    float *red = reinterpret_cast<float *>(sdy);          // dy is consumed
+    __syncthreads();
+    {
+        const int c = threadIdx.x % CB, grp = threadIdx.x / CB;
+        float acc[W + 1];
+#pragma unroll
+        for (int j = 0; j <= W; ++j) acc[j] = 0.f;
+        if (cb0 + c < D) {
+            for (int pr = grp; pr < len; pr += NG) {
+                const float dv = sdp[(int64_t)pr * CB + dp_col(c, CB)];
+#pragma unroll
+                for (int j = 0; j < W; ++j) acc[j] = fmaf(dv, ld1(sx + (int64_t)(pr + j) * CB + c), acc[j]);
+                acc[W] += dv;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j <= W; ++j) red[((int64_t)grp * (W + 1) + j) * CB + c] = acc[j];
+    }
+    __syncthreads();
+    if (threadIdx.x < CB && cb0 + (int)threadIdx.x < D) {
+        const int c = threadIdx.x;
+        float *part = p.partial + (int64_t)blockIdx.x * (W + 1) * D + cb0 + c;
+#pragma unroll
+        for (int j = 0; j <= W; ++j) {
+            float a = 0.f;
+            for (int grp = 0; grp < NG; ++grp) a += red[((int64_t)grp * (W + 1) + j) * CB + c];
+            part[(int64_t)j * D] = a;
+        }
+    }
 }
+// dw[c][j] and db[c]: the chunk rows' partial sums, 32 channels per CTA (one per lane, so every
+// load of a warp is one 128-byte line); warp w takes rows w, w + 16, ..., and the 16 warp sums
+// are added in warp order (sentinel rows end the live rows).
+constexpr int kReduceWarps = 16;
 
-// dw[c][j] and db[c]: the chunk rows' partial sums added in row order (sentinel rows skipped).
 template <int W>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kReduceWarps * 32)
 conv_reduce_kernel(ConvParams p) {
+    __shared__ float red[kReduceWarps][W + 1][32];
     if (status_blocks(p.status)) return;
-    const int c = blockIdx.x * 256 + threadIdx.x;
-    if (c >= p.D) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
     float acc[W + 1];
 #pragma unroll
     for (int j = 0; j <= W; ++j) acc[j] = 0.f;
-    for (int64_t row = 0; row < p.nt_max; ++row) {
-        if (p.chunk_indices[2 * row] < 0) break;          // live rows come first
-        const float *part = p.partial + row * (W + 1) * p.D + c;
+    if (c < p.D) {
+        for (int64_t row = warp; row < p.nt_max; row += kReduceWarps) {
+            if (p.chunk_indices[2 * row] < 0) break;      // live rows come first
+            const float *part = p.partial + row * (W + 1) * p.D + c;
 #pragma unroll
-        for (int j = 0; j <= W; ++j) acc[j] += part[(int64_t)j * p.D];
+            for (int j = 0; j <= W; ++j) acc[j] += part[(int64_t)j * p.D];
+        }
     }
 #pragma unroll
-    for (int j = 0; j < W; ++j) p.dw[(int64_t)c * W + j] = acc[j];
-    if (p.dbias) p.dbias[c] = acc[W];
+    for (int j = 0; j <= W; ++j) red[warp][j][lane] = acc[j];
+    __syncthreads();
+    if (warp <= W && c < p.D) {                           // warp j adds tap j (j = W: the bias)
+        float a = 0.f;
+        for (int w = 0; w < kReduceWarps; ++w) a += red[w][warp][lane];
+        if (warp < W) p.dw[(int64_t)c * W + warp] = a;
+        else if (p.dbias) p.dbias[c] = a;
+    }
 }
 
 template <typename T, int W>
 cudaError_t launch_conv(const ConvParams &p, bool backward, cudaStream_t s) {
-    const dim3 grid((unsigned)(p.nt_max + p.n_max), (unsigned)((p.D + kChannelsPerBlock - 1) / kChannelsPerBlock));
     if (!backward) {
+        constexpr int CB = kFwdChannels * 2 / (int)sizeof(T);
+        const dim3 grid((unsigned)(p.nt_max + p.n_max), (unsigned)((p.D + CB - 1) / CB));
         conv_fwd_kernel<T, W><<<grid, kConvThreads, 0, s>>>(p);
         return cudaGetLastError();
     }
-    conv_bwd_kernel<T, W><<<grid, kConvThreads, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    using Lay = ConvBwdLayout<T, W>;
+    auto kern = conv_bwd_kernel<T, W>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::bytes);
     if (e != cudaSuccess) return e;
-    conv_reduce_kernel<W><<<(p.D + 255) / 256, 256, 0, s>>>(p);
+    const dim3 grid((unsigned)(p.nt_max + p.n_max), (unsigned)((p.D + Lay::CB - 1) / Lay::CB));
+    kern<<<grid, kConvThreads, Lay::bytes, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    conv_reduce_kernel<W><<<(p.D + 31) / 32, kReduceWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 
