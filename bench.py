@@ -259,12 +259,17 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
 
 def launches_per_step(w) -> int:
     """Library kernels per step: chunk_meta_build, the forward (prep and chain on the tensor
-    cores for GDN and KDA bf16 d_k = d_v = 128, one fused CUDA-core kernel otherwise) and
+    cores for GDN and KDA bf16 d_k = d_v = 128 -- prep, segment summaries, scan and segment
+    outputs when the chain is segmented -- one fused CUDA-core kernel otherwise) and
     the backward (GDN on the tensor cores: transition records, state-gradient sweep and two
     chunk-gradient kernels; otherwise the sweep and one chunk-gradient kernel)."""
     tc = w.dtype == "bf16" and w.K == 128 and w.V == 128
     tc_bwd = tc and w.variant == synth.GDN
-    return 1 + (2 if tc else 1) + ((4 if tc_bwd else 2) if w.backward else 0)
+    # a segmented chain (few long sequences): summaries, scan and segment outputs
+    import chunked_gated_linear_gb300 as gcl
+    seg = tc and gcl.fwd_chain_segments(w.t_max, w.n_max, w.H, w.bt) > 0
+    fwd = (4 if seg else 2) if tc else 1
+    return 1 + fwd + ((4 if tc_bwd else 2) if w.backward else 0)
 
 
 def graph_and_warm_timing(torch, w, sets, stream, step, step_ms, reps):

@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH):
     lib.gcl_status_string.argtypes = [i32]
     lib.gcl_nt_max.restype = i64
     lib.gcl_nt_max.argtypes = [i64, i64, i32]
+    lib.gcl_fwd_chain_segments.restype = i32
+    lib.gcl_fwd_chain_segments.argtypes = [i64, i32, i32, i32]
     lib.chunk_meta_build.restype = ctypes.c_int
     lib.chunk_meta_build.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp]
     for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
@@ -147,6 +149,11 @@ def _dtype_of(t):
 
 def nt_max(t_max: int, n_max: int, bt: int = CHUNK) -> int:
     return int(lib().gcl_nt_max(t_max, n_max, bt))
+
+
+def fwd_chain_segments(t_max: int, n_max: int, H: int, bt: int = CHUNK) -> int:
+    """Segments per sequence of the fastest tensor-core forward plan (0: the plain chain)."""
+    return int(lib().gcl_fwd_chain_segments(t_max, n_max, H, bt))
 
 
 def chunk_meta_build(cu_seqlens, t_max, chunk_indices, chunk_offsets, dev_status,

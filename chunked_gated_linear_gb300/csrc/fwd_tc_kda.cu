@@ -572,7 +572,10 @@ cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s) {
     uint8_t *ws = static_cast<uint8_t *>(p.workspace);
     const cudaError_t e = launch_prep_kda(p, ws, s);
     if (e != cudaSuccess) return e;
-    return launch_chain_records(p, ws, split, true, s);
+    int n_seg = 0;
+    float *seg_ws = nullptr;
+    fwd_seg_plan(p, ws, &n_seg, &seg_ws);
+    return launch_chain_records(p, ws, split, true, s, n_seg, seg_ws);
 }
 
 }  // namespace gcl

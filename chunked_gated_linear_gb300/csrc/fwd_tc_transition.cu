@@ -454,6 +454,19 @@ struct ChainTParams {
     int32_t *status;
     int64_t t_max, nt_max;
     int32_t n_max, H;
+    // Segment-parallel Reduce (HA-NPU section 4, third tier): a sequence of nch chunks is cut
+    // into n_seg segments of ceil(nch / n_seg) chunks, blockIdx.z = sequence slot * n_seg + segment.
+    // mode 0: the whole recurrence (n_seg = 1);
+    // mode 1: segment summaries over 256 state columns -- columns 0..127 start at the identity and
+    //         take no B (they become the segment's transition M), columns 128..255 start at zero
+    //         and take B (they become its offset); the end state goes to seg_sum[unit][segment]
+    //         as M transposed [128][128] then B [128][128] (the last segment of a sequence has
+    //         no summary to give);
+    // mode 2: each segment's recurrence from its start state (h0 for segment 0, else
+    //         seg_start[unit][segment] as [128][128]); the last segment writes ht.
+    int32_t mode, n_seg;
+    float *seg_sum;
+    const float *seg_start;
 };
 
 // Shared memory: NS stages of {[Y; N] (two 64-column blocks of 192 rows, 128-byte
@@ -512,14 +525,21 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
+    // a segmented launch waits for the grid before it in full (the records, the start states)
+    // before any exit, so that its own completion implies theirs
+    if (p.mode != 0) grid_dependency_wait();
     if (status_blocks(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int split = blockIdx.x, h = blockIdx.y;
-    const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
+    const int zs = p.mode == 0 ? (int)blockIdx.z : (int)blockIdx.z / p.n_seg;
+    const int seg = p.mode == 0 ? 0 : (int)blockIdx.z % p.n_seg;
+    const int n = p.seq_order ? p.seq_order[zs] : zs;
     const int H = p.H, v0 = split * VS;
+    // the record columns of this slice: in mode 1 the B columns 128.. of the state are the record's
+    const int vr = p.mode == 1 ? (v0 >= VD ? v0 - VD : 0) : v0;
     if (n < 0 || n >= p.n_max) {
         if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
         return;
@@ -529,12 +549,22 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
         if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
         return;
     }
-    const int nch = (int)((eos - bos + C - 1) / C);
+    const int nch_seq = (int)((eos - bos + C - 1) / C);
     const int64_t row0 = p.chunk_offsets[n];
-    if (nch > 0 && (row0 < 0 || row0 + nch > p.nt_max)) {
+    if (nch_seq > 0 && (row0 < 0 || row0 + nch_seq > p.nt_max)) {
         if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
         return;
     }
+    // this CTA's chunks [cb, cb + nch) of the sequence; segments past the end have nothing to do
+    // (segment 0 of an empty sequence still passes h0 through to ht in mode 2)
+    const int seg_len = p.mode == 0 ? nch_seq : (nch_seq + p.n_seg - 1) / p.n_seg;
+    const int cb = seg * seg_len;
+    const int nch = max(0, min(seg_len, nch_seq - cb));
+    const bool last_seg = cb + nch >= nch_seq;
+    if (p.mode == 1 && (nch == 0 || last_seg)) return;
+    if (p.mode == 2 && nch == 0 && !(seg == 0 && nch_seq == 0)) return;
+    const bool add_b = !(p.mode == 1 && v0 < VD);       // mode 1: the M columns take no B
+    const int64_t unit_idx = (int64_t)n * p.H + h;
     const uint32_t sbase = smem_u32(smem);
     const int64_t KV = (int64_t)KD * VD;
     const int64_t state_base = ((int64_t)n * H + h) * KV;
@@ -612,14 +642,14 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
         if (lane == 0) {
             auto issue_tma = [&](int ic) {
                 const int st = ic % NS;
-                const int unit = (int)((row0 + ic) * H + h);
+                const int unit = (int)((row0 + cb + ic) * H + h);
                 uint64_t *bar = &bar_tma[st];
                 uint8_t *b = smem + st * Lay::kStage;
                 mbar_arrive_expect_tx(bar, Lay::kTmaBytes);
                 tma_load_3d(b + Lay::oYN, &tm_yn, 0, 0, unit, bar);
                 tma_load_3d(b + Lay::oYN + 24576, &tm_yn, 64, 0, unit, bar);
-                tma_load_3d(b + Lay::oB, &tm_b, v0, 0, unit, bar);
-                tma_load_3d(b + Lay::oZ, &tm_z, v0, 0, unit, bar);
+                tma_load_3d(b + Lay::oB, &tm_b, vr, 0, unit, bar);
+                tma_load_3d(b + Lay::oZ, &tm_z, vr, 0, unit, bar);
                 bulk_load(b + Lay::oG, p.ws + gc_offset(p.nt_max, H, unit), kGBytes, bar);
             };
             grid_dependency_wait();      // the records are complete (launched as a dependent)
@@ -634,9 +664,9 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
         const uint32_t olane = (uint32_t)((warp - 8) * 32) << 16;
         for (int ic = 0; ic < nch; ++ic) {
             const int st = ic % NS;
-            const int64_t rem = eos - bos - (int64_t)ic * C;
+            const int64_t rem = eos - bos - (int64_t)(cb + ic) * C;
             const int len = (int)(rem < C ? rem : C);
-            const int64_t t0 = bos + (int64_t)ic * C;
+            const int64_t t0 = bos + (int64_t)(cb + ic) * C;
             const uint8_t *stage = smem + st * Lay::kStage;
             mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 5);
             mbar_wait(&bar_g2[ic % 3], (ic / 3) & 1, &s_err, 6);
@@ -687,8 +717,13 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             }
         };
         float S[HV];
-        {
-            const float *src = p.h0 ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
+        if (p.mode == 1) {                                // [I | 0]
+#pragma unroll
+            for (int j = 0; j < HV; ++j) S[j] = row == v0 + c0 + j ? 1.f : 0.f;
+        } else {
+            const float *src = seg > 0 ? p.seg_start + (((unit_idx * p.n_seg + seg) * KD + row) * VD + v0 + c0)
+                               : p.h0  ? p.h0 + state_base + (int64_t)row * VD + v0 + c0
+                                       : nullptr;
 #pragma unroll
             for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
         }
@@ -698,13 +733,17 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             const int st = ic % NS;
             const uint8_t *stage = smem + st * Lay::kStage;
             if (p.h_save) {
-                float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
+                float *dst = p.h_save + ((row0 + cb + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
 #pragma unroll
                 for (int j = 0; j < HV; j += 4)
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
             }
             mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 3);
-            {   // Gamma_c S + B while G1 runs
+            if (!add_b) {   // Gamma_c S (the transition columns of a segment summary)
+                const float gc = reinterpret_cast<const float *>(stage + Lay::oG)[KDA ? row : 0];
+#pragma unroll
+                for (int j = 0; j < HV; ++j) S[j] *= gc;
+            } else {   // Gamma_c S + B while G1 runs
                 const float gc = reinterpret_cast<const float *>(stage + Lay::oG)[KDA ? row : 0];
                 const uint8_t *brow = stage + Lay::oB + row * (VS * 2) + c0 * 2;
 #pragma unroll
@@ -743,7 +782,18 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_free[st]);        // done with B of stage st
         }
-        if (p.ht && *reinterpret_cast<volatile int *>(&s_err) == 0) {
+        if (p.mode == 1 && *reinterpret_cast<volatile int *>(&s_err) == 0) {
+            float *blk = p.seg_sum + (unit_idx * p.n_seg + seg) * (2 * KD * VD);
+            if (v0 < VD) {                                // M, transposed: [k][row]
+#pragma unroll
+                for (int j = 0; j < HV; ++j) blk[(int64_t)(v0 + c0 + j) * KD + row] = S[j];
+            } else {                                      // B: [row][v]
+                float *dst = blk + KD * KD + (int64_t)row * VD + (v0 - VD) + c0;
+#pragma unroll
+                for (int j = 0; j < HV; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            }
+        } else if (p.ht && last_seg && *reinterpret_cast<volatile int *>(&s_err) == 0) {
             float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
 #pragma unroll
             for (int j = 0; j < HV; j += 4)
@@ -754,6 +804,111 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     __syncthreads();
     if (warp == kWarpG1) tmem_dealloc(tmem, kTmemCols);
     if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+// ============================================================================ segment scan
+// The start states of the segments: S(s + 1) = M(s) S(s) + B(s) from S(0) = h0, in fp32, one
+// CTA per (kScanSC value columns, head, sequence slot).  A segment summary is M transposed
+// ([k][i], 64 KiB) then B ([i][v], 64 KiB).  M(s) and the CTA's columns of B(s) are staged in
+// shared memory by asynchronous copies one segment ahead.  Warp w adds the products of key rows
+// 32 w .. 32 w + 31, lane l owning state rows 4 l .. 4 l + 3 and all kScanSC columns (every
+// M value read once, the S row broadcast); the four warps' partial sums are then added in warp
+// order by thread t for state row t.
+struct SegScanParams {
+    const int32_t *cu;
+    const float *h0, *seg_sum;
+    float *seg_start;
+    int32_t *status;
+    int64_t t_max;
+    int32_t n_max, H, n_seg;
+};
+constexpr int kScanSC = 4, kScanWarps = 4, kScanThreads = 32 * kScanWarps;
+struct ScanLayout {
+    static constexpr int oMT = 0, oB = oMT + 2 * KD * KD, oS = oB + 2 * KD * kScanSC;
+    static constexpr int oRed = oS + KD * kScanSC, floats = oRed + kScanWarps * KD * kScanSC;
+    static constexpr int bytes = floats * (int)sizeof(float);
+};
+static_assert(kScanThreads == KD && kScanSC == 4 && KD == 4 * 32 && KD == 32 * kScanWarps,
+              "scan thread mapping: thread t owns state row t; lane l rows 4 l .. 4 l + 3");
+
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(SegScanParams p) {
+    extern __shared__ __align__(16) float sm_scan[];
+    float *sS = sm_scan + ScanLayout::oS;                // [KD][kScanSC]
+    float *sRed = sm_scan + ScanLayout::oRed;            // [kScanWarps][KD][kScanSC]
+    grid_dependency_wait();                              // the segment summaries are complete
+    if (status_blocks(p.status)) return;
+    const int c0 = blockIdx.x * kScanSC, h = blockIdx.y, n = blockIdx.z;
+    const int64_t bos = p.cu[n], eos = p.cu[n + 1];
+    if (bos < 0 || eos < bos || eos > p.t_max) return;  // reported by the chain
+    const int nch = (int)((eos - bos + C - 1) / C);
+    if (nch == 0) return;
+    const int seg_len = (nch + p.n_seg - 1) / p.n_seg, nseg = (nch + seg_len - 1) / seg_len;
+    if (nseg < 2) return;
+    const int64_t unit = (int64_t)n * p.H + h;
+    constexpr int64_t kSum = 2 * KD * VD;                // floats per summary
+    const float *sum0 = p.seg_sum + unit * p.n_seg * kSum;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto prefetch = [&](int sg) {                        // M(sg)^T and B(sg)[tid][c0 ..] into buffer sg & 1
+        const float *src = sum0 + sg * kSum;
+        float *mt = sm_scan + ScanLayout::oMT + (sg & 1) * (KD * KD);
+        for (int e = tid; e < KD * KD / 4; e += kScanThreads) cp_async16(mt + e * 4, src + e * 4);
+        cp_async16(sm_scan + ScanLayout::oB + (sg & 1) * (KD * kScanSC) + tid * kScanSC,
+                   src + KD * KD + (int64_t)tid * VD + c0);
+        cp_async_commit();
+    };
+    prefetch(0);
+    *reinterpret_cast<float4 *>(sS + tid * kScanSC) =
+        p.h0 ? *reinterpret_cast<const float4 *>(p.h0 + (unit * KD + tid) * VD + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sg = 0; sg + 1 < nseg; ++sg) {
+        if (sg + 2 < nseg) {
+            prefetch(sg + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();                                 // M(sg), B(sg) and S(sg) are in shared memory
+        const float *mt = sm_scan + ScanLayout::oMT + (sg & 1) * (KD * KD);
+        float acc[4][kScanSC];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < kScanSC; ++j) acc[i][j] = 0.f;
+#pragma unroll 8
+        for (int kk = 0; kk < 32; ++kk) {
+            const int k = warp * 32 + kk;
+            const float4 a = *reinterpret_cast<const float4 *>(mt + k * KD + 4 * lane);
+            const float4 b = *reinterpret_cast<const float4 *>(sS + k * kScanSC);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < kScanSC; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4 *>(sRed + (warp * KD + 4 * lane + i) * kScanSC) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        __syncthreads();                                 // every partial sum is written; S(sg) is read
+        float4 v = *reinterpret_cast<const float4 *>(sm_scan + ScanLayout::oB + (sg & 1) * (KD * kScanSC) +
+                                                     tid * kScanSC);
+#pragma unroll
+        for (int w = 0; w < kScanWarps; ++w) {
+            const float4 r = *reinterpret_cast<const float4 *>(sRed + (w * KD + tid) * kScanSC);
+            v.x += r.x;
+            v.y += r.y;
+            v.z += r.z;
+            v.w += r.w;
+        }
+        *reinterpret_cast<float4 *>(sS + tid * kScanSC) = v;
+        *reinterpret_cast<float4 *>(p.seg_start + ((unit * p.n_seg + sg + 1) * KD + tid) * VD + c0) = v;
+    }
 }
 
 template <int VS, int NS, bool KDA>
@@ -776,8 +931,8 @@ cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const Chai
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
     // launched as a programmatic dependent of the prep: its prologue overlaps the prep's tail
-    return launch_dependent(kern, dim3(n_split, H, n_max), dim3(kChainThreads), Lay::bytes, s, myn, mb,
-                            mz, cp);
+    return launch_dependent(kern, dim3(n_split, H, n_max * (cp.mode == 0 ? 1 : cp.n_seg)), dim3(kChainThreads),
+                            Lay::bytes, s, myn, mb, mz, cp);
 }
 
 }  // namespace
@@ -837,8 +992,36 @@ cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
                             mrec, pp);
 }
 
+// Segments per sequence: at most one wave of summary CTAs (8 slices of 32 columns per unit),
+// the count that minimises the modelled time of summaries + scan + outputs, and only where
+// that beats the plain chain.  Chunks per sequence are taken from the capacity
+// (nt_max / n_max), so the plan depends on the sizes alone.  Per-chunk and per-step times are
+// GB300 measurements of these kernels (ns): summary + output chain per chunk, scan per
+// segment, the two extra launches, and the plain chain per chunk.
+int fwd_seg_count(int64_t nt_max, int n_max, int H) {
+    constexpr int64_t kChainAC = 1850, kScanStep = 600, kExtra = 5000, kPlain = 700;
+    const int64_t units = (int64_t)n_max * H;
+    const int64_t p_max = num_sms() / (8 * units);
+    if (p_max < 3 || n_max <= 0) return 0;
+    const int64_t nc = nt_max / n_max;
+    int64_t best = 0, best_t = nc * kPlain;
+    for (int64_t P = 3; P <= p_max; ++P) {
+        const int64_t t = (nc + P - 1) / P * kChainAC + (P - 1) * kScanStep + kExtra;
+        if (t < best_t) {
+            best_t = t;
+            best = P;
+        }
+    }
+    return (int)best;
+}
+
+size_t fwd_seg_workspace_bytes(int64_t nt_max, int n_max, int H) {
+    const int P = fwd_seg_count(nt_max, n_max, H);
+    return (size_t)n_max * H * P * (size_t)(KD * 2 * VD + KD * VD) * sizeof(float);
+}
+
 cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int split, bool kda,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, int n_seg, float *seg_ws) {
     const int H = p.H;
     const int64_t units = p.nt_max * H;
     CUtensorMap myn;
@@ -861,6 +1044,40 @@ cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int spli
     cp.nt_max = p.nt_max;
     cp.n_max = p.n_max;
     cp.H = H;
+    cp.n_seg = 1;
+    if (n_seg >= 2) {
+        // segment summaries (8 slices of 32 over [M | B]), the scan, the segments' outputs
+        ChainTParams ca = cp;
+        ca.mode = 1;
+        ca.n_seg = n_seg;
+        ca.o = nullptr;
+        ca.ht = nullptr;
+        ca.h_save = nullptr;
+        ca.seg_sum = seg_ws;
+        cudaError_t e = kda ? launch_chain_t<32, 2, true>(myn, ws, ca, 8, H, p.n_max, s)
+                            : launch_chain_t<32, 2, false>(myn, ws, ca, 8, H, p.n_max, s);
+        if (e != cudaSuccess) return e;
+        SegScanParams sp{};
+        sp.cu = p.cu_seqlens;
+        sp.h0 = p.h0;
+        sp.seg_sum = seg_ws;
+        sp.seg_start = seg_ws + (size_t)p.n_max * H * n_seg * (KD * 2 * VD);
+        sp.status = p.dev_status;
+        sp.t_max = p.t_max;
+        sp.n_max = p.n_max;
+        sp.H = H;
+        sp.n_seg = n_seg;
+        e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ScanLayout::bytes);
+        if (e != cudaSuccess) return e;
+        e = launch_dependent(seg_scan_kernel, dim3(VD / kScanSC, H, p.n_max), dim3(kScanThreads),
+                             ScanLayout::bytes, s, sp);
+        if (e != cudaSuccess) return e;
+        cp.mode = 2;
+        cp.n_seg = n_seg;
+        cp.seg_start = sp.seg_start;
+        return kda ? launch_chain_t<16, 3, true>(myn, ws, cp, 8, H, p.n_max, s)
+                   : launch_chain_t<16, 3, false>(myn, ws, cp, 8, H, p.n_max, s);
+    }
     if (kda) {
         if (split == 8) return launch_chain_t<16, 3, true>(myn, ws, cp, split, H, p.n_max, s);
         if (split == 4) return launch_chain_t<32, 2, true>(myn, ws, cp, split, H, p.n_max, s);
@@ -872,11 +1089,25 @@ cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int spli
     return cudaErrorInvalidValue;                   // GDN takes this plan only at splits 4 and 8
 }
 
+void fwd_seg_plan(const FwdParams &p, uint8_t *ws, int *n_seg, float **seg_ws) {
+    const size_t rec = fwd_tc_t_workspace_bytes(p.nt_max, p.H);
+    const size_t need = fwd_seg_workspace_bytes(p.nt_max, p.n_max, p.H);
+    *n_seg = 0;
+    *seg_ws = nullptr;
+    if (need > 0 && p.workspace_bytes >= rec + need) {
+        *n_seg = fwd_seg_count(p.nt_max, p.n_max, p.H);
+        *seg_ws = reinterpret_cast<float *>(ws + rec);
+    }
+}
+
 cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s) {
     uint8_t *ws = static_cast<uint8_t *>(p.workspace);
     cudaError_t e = launch_prep_t(p, ws, s);
     if (e != cudaSuccess) return e;
-    return launch_chain_records(p, ws, split, false, s);
+    int n_seg = 0;
+    float *seg_ws = nullptr;
+    fwd_seg_plan(p, ws, &n_seg, &seg_ws);
+    return launch_chain_records(p, ws, split, false, s, n_seg, seg_ws);
 }
 
 }  // namespace gcl

@@ -81,9 +81,11 @@ static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
     if (!fwd_tc_supported(variant, a->dtype, a->K, a->V)) return 0;
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->n_max <= 0) return 0;
-    if (variant == kKDA) return fwd_tc_t_workspace_bytes(ntm, a->H) + kWsAlign;   // one plan
+    // the transition form, with the segment buffers when the fastest plan is segmented
+    const size_t seg = fastest ? fwd_seg_workspace_bytes(ntm, a->n_max, a->H) : 0;
+    if (variant == kKDA) return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
     if (fastest && fwd_tc_prefers_transition(a->n_max, a->H))
-        return fwd_tc_t_workspace_bytes(ntm, a->H) + kWsAlign;
+        return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
     return fwd_tc_workspace_bytes(ntm, a->H) + kWsAlign;
 }
 
@@ -297,6 +299,12 @@ size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args) {
 size_t gcl_kda_fwd_workspace_bytes(const gcl_fwd_args *args) {
     if (!args) return 0;
     return fwd_ws(args, kKDA, true);
+}
+
+int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t bt) {
+    const int64_t ntm = gcl_nt_max(t_max, n_max, bt);
+    if (ntm <= 0 || H <= 0 || bt != kChunk) return 0;
+    return fwd_seg_count(ntm, n_max, H);
 }
 
 gcl_status_t gdn_chunk_fwd(const gcl_fwd_args *args, gcl_stream_t stream) {

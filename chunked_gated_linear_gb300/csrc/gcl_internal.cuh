@@ -71,6 +71,10 @@ cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s);
 bool fwd_tc_supported(int variant, int dtype, int K, int V);
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H);     // W form (the minimum)
 size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H);   // transition form
+// Segment-parallel chain (few long sequences): segments per sequence (0: the plain chain) and
+// the buffers it needs after the transition records.
+int fwd_seg_count(int64_t nt_max, int n_max, int H);
+size_t fwd_seg_workspace_bytes(int64_t nt_max, int n_max, int H);
 int fwd_tc_split(int n_max, int H);                        // value-column slices per head
 bool fwd_tc_prefers_transition(int n_max, int H);
 

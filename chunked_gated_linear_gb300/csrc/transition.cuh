@@ -133,8 +133,12 @@ cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s);
 size_t transition_record_bytes(int64_t nt_max, int H);
 // The chain over the records in ws (p.workspace is not used), split value-column slices per
 // head; kda selects the per-key-channel Gamma_c.  Launched as a programmatic dependent.
+// n_seg >= 2: the segment-parallel plan (summaries, scan, segment outputs) with its buffers at
+// seg_ws (fwd_seg_workspace_bytes).
 cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int split, bool kda,
-                                 cudaStream_t s);
+                                 cudaStream_t s, int n_seg = 0, float *seg_ws = nullptr);
+// The segment plan for p when its workspace holds the segment buffers after the records.
+void fwd_seg_plan(const FwdParams &p, uint8_t *ws, int *n_seg, float **seg_ws);
 
 
 }  // namespace gcl

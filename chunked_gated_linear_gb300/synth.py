@@ -98,6 +98,10 @@ def standard_workloads():
         # beyond the five configurations above: the KDA backward, at the KDA forward's sizes
         dense("kda_fwdbwd_bf16_T2048_H10_d128", KDA, "bf16", 1, 2048, 10, 128, 128,
               backward=True, seed=5),
+        # the extreme tail: one long sequence of one head (one unit for 152 SMs), the case
+        # the chunk-head-chunk mapping of the third scheduling tier serves
+        dense("gdn_fwd_bf16_T65536_H1_d128", GDN, "bf16", 1, 65536, 1, 128, 128, seed=6),
+        dense("kda_fwd_bf16_T65536_H1_d128", KDA, "bf16", 1, 65536, 1, 128, 128, seed=7),
     ]
 
 

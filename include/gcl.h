@@ -160,13 +160,37 @@ typedef struct gcl_fwd_args {
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
 size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
 
-/* Bytes of device workspace kda_chunk_fwd needs for these sizes (0 when the fp32
- * CUDA-core kernel serves them).  KDA on the tensor cores has one plan, the
+/* Bytes of device workspace kda_chunk_fwd's fastest plan needs for these sizes (0
+ * when the fp32 CUDA-core kernel serves them).  KDA on the tensor cores runs the
  * transition form (96.5 KiB per chunk and head: the chunk's affine state map and
- * output map, and the per-key-channel state decay of the chunk); a smaller
- * workspace returns GCL_ERR_CAPACITY.  gcl_fwd_workspace_bytes and
+ * output map, and the per-key-channel state decay of the chunk); a workspace
+ * smaller than those records returns GCL_ERR_CAPACITY.  When the fastest plan is
+ * segmented (gcl_fwd_chain_segments) it also holds the segment buffers; without
+ * room for them the forward runs the plain chain.  gcl_fwd_workspace_bytes and
  * gcl_fwd_workspace_min_bytes describe gdn_chunk_fwd only. */
 size_t gcl_kda_fwd_workspace_bytes(const gcl_fwd_args *args);
+
+/*
+ * Segments per sequence of the fastest tensor-core forward plan (GDN and KDA, bf16,
+ * K = V = 128, workspace of the fastest size) for these capacities; 0 when every
+ * (sequence, head, column slice) runs its whole chain in one CTA.
+ *
+ * With few sequence-head units (n_max * H at most SMs / 24) and long sequences
+ * (NT_max at least 4 P n_max chunks), the forward cuts each sequence of nc chunks into
+ * P segments of ceil(nc / P) chunks, following HA-NPU section 4 (third tier: a
+ * long head's chunks spread over cores) and the Map-Reduce-Map split of its
+ * section 2.1, with the transition form's affine chunk maps as the unit of work.
+ * After the chunk records come three launches:
+ *   summaries  each segment but the last: its affine map S_end = M S_start + B over its
+ *              chunks, from the state [I | 0] over 256 columns;
+ *   scan       the start states S(s + 1) = M(s) S(s) + B(s) from S(0) = h0, in fp32;
+ *   outputs    each segment's recurrence from its start state (o, h_save), ht from
+ *              the last segment.
+ * Segment buffers: n_max * H * P * 192 KiB after the records.  The result depends
+ * only on the capacities and the device's SM count, so a captured graph keeps its
+ * plan.  Returns 0 for invalid sizes.
+ */
+int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t bt);
 
 /*
  * gdn_chunk_fwd -- gated delta rule prefill: o and ht from q, k, v, g, beta, h0.

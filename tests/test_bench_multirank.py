@@ -65,3 +65,6 @@ def test_launch_count_per_step():
     assert bench.launches_per_step(ws["kda_fwd_bf16_T2048_H10_d128"]) == 3
     assert bench.launches_per_step(ws["gdn_fwd_fp32_T256_H2_d64"]) == 2
     assert bench.launches_per_step(ws["kda_fwdbwd_bf16_T2048_H10_d128"]) == 5
+    # one 64K-token sequence of one head: the segmented chain (on any GPU of 24 or more SMs)
+    assert bench.launches_per_step(ws["gdn_fwd_bf16_T65536_H1_d128"]) == 5
+    assert bench.launches_per_step(ws["kda_fwd_bf16_T65536_H1_d128"]) == 5
