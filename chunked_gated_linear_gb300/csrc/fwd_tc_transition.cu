@@ -460,8 +460,8 @@ struct ChainTParams {
     // mode 1: segment summaries over 256 state columns -- columns 0..127 start at the identity and
     //         take no B (they become the segment's transition M), columns 128..255 start at zero
     //         and take B (they become its offset); the end state goes to seg_sum[unit][segment]
-    //         as M transposed [128][128] then B [128][128] (the last segment of a sequence has
-    //         no summary to give);
+    //         as M transposed [128][128] then B transposed [128][128] (the last segment of a
+    //         sequence has no summary to give);
     // mode 2: each segment's recurrence from its start state (h0 for segment 0, else
     //         seg_start[unit][segment] as [128][128]); the last segment writes ht.
     int32_t mode, n_seg;
@@ -787,11 +787,9 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             if (v0 < VD) {                                // M, transposed: [k][row]
 #pragma unroll
                 for (int j = 0; j < HV; ++j) blk[(int64_t)(v0 + c0 + j) * KD + row] = S[j];
-            } else {                                      // B: [row][v]
-                float *dst = blk + KD * KD + (int64_t)row * VD + (v0 - VD) + c0;
+            } else {                                      // B, transposed: [v][row]
 #pragma unroll
-                for (int j = 0; j < HV; j += 4)
-                    *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                for (int j = 0; j < HV; ++j) blk[KD * KD + (int64_t)(v0 - VD + c0 + j) * KD + row] = S[j];
             }
         } else if (p.ht && last_seg && *reinterpret_cast<volatile int *>(&s_err) == 0) {
             float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
@@ -809,11 +807,11 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
 // ============================================================================ segment scan
 // The start states of the segments: S(s + 1) = M(s) S(s) + B(s) from S(0) = h0, in fp32, one
 // CTA per (kScanSC value columns, head, sequence slot).  A segment summary is M transposed
-// ([k][i], 64 KiB) then B ([i][v], 64 KiB).  M(s) and the CTA's columns of B(s) are staged in
-// shared memory by asynchronous copies one segment ahead.  Warp w adds the products of key rows
-// 32 w .. 32 w + 31, lane l owning state rows 4 l .. 4 l + 3 and all kScanSC columns (every
-// M value read once, the S row broadcast); the four warps' partial sums are then added in warp
-// order by thread t for state row t.
+// ([k][i], 64 KiB) then B transposed ([v][i], 64 KiB).  M(s) and the CTA's kScanSC rows of B(s)
+// arrive by bulk copies one segment ahead (two buffers, one mbarrier each).  Warp w adds the
+// products of key rows 16 w .. 16 w + 15, lane l owning state rows 4 l .. 4 l + 3 and all
+// kScanSC columns (every M value read once, the S row broadcast); thread t < 128 then adds
+// the eight warps' partial sums for state row t in warp order.
 struct SegScanParams {
     const int32_t *cu;
     const float *h0, *seg_sum;
@@ -822,24 +820,19 @@ struct SegScanParams {
     int64_t t_max;
     int32_t n_max, H, n_seg;
 };
-constexpr int kScanSC = 4, kScanWarps = 4, kScanThreads = 32 * kScanWarps;
+constexpr int kScanSC = 4, kScanWarps = 8, kScanThreads = 32 * kScanWarps, kScanKW = KD / kScanWarps;
 struct ScanLayout {
-    static constexpr int oMT = 0, oB = oMT + 2 * KD * KD, oS = oB + 2 * KD * kScanSC;
+    static constexpr int oMT = 0, oBT = oMT + 2 * KD * KD, oS = oBT + 2 * kScanSC * KD;
     static constexpr int oRed = oS + KD * kScanSC, floats = oRed + kScanWarps * KD * kScanSC;
     static constexpr int bytes = floats * (int)sizeof(float);
+    static constexpr uint32_t kTx = (KD * KD + kScanSC * KD) * sizeof(float);
 };
-static_assert(kScanThreads == KD && kScanSC == 4 && KD == 4 * 32 && KD == 32 * kScanWarps,
-              "scan thread mapping: thread t owns state row t; lane l rows 4 l .. 4 l + 3");
-
-__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+static_assert(kScanSC == 4 && KD == 4 * 32 && KD <= kScanThreads, "scan thread mapping");
 
 __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(SegScanParams p) {
-    extern __shared__ __align__(16) float sm_scan[];
+    extern __shared__ __align__(128) float sm_scan[];
+    __shared__ uint64_t bar[2];
+    __shared__ int s_err;
     float *sS = sm_scan + ScanLayout::oS;                // [KD][kScanSC]
     float *sRed = sm_scan + ScanLayout::oRed;            // [kScanWarps][KD][kScanSC]
     grid_dependency_wait();                              // the segment summaries are complete
@@ -855,34 +848,44 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(SegScanParams
     constexpr int64_t kSum = 2 * KD * VD;                // floats per summary
     const float *sum0 = p.seg_sum + unit * p.n_seg * kSum;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    auto prefetch = [&](int sg) {                        // M(sg)^T and B(sg)[tid][c0 ..] into buffer sg & 1
+    int issued[2] = {0, 0};                              // copies issued per buffer (thread 0)
+    auto issue = [&](int sg) {                           // M(sg)^T and B(sg)^T rows c0 .. into buffer sg & 1
+        const int b = sg & 1;
         const float *src = sum0 + sg * kSum;
-        float *mt = sm_scan + ScanLayout::oMT + (sg & 1) * (KD * KD);
-        for (int e = tid; e < KD * KD / 4; e += kScanThreads) cp_async16(mt + e * 4, src + e * 4);
-        cp_async16(sm_scan + ScanLayout::oB + (sg & 1) * (KD * kScanSC) + tid * kScanSC,
-                   src + KD * KD + (int64_t)tid * VD + c0);
-        cp_async_commit();
+        mbar_arrive_expect_tx(&bar[b], ScanLayout::kTx);
+        bulk_load(sm_scan + ScanLayout::oMT + b * (KD * KD), src, KD * KD * sizeof(float), &bar[b]);
+        bulk_load(sm_scan + ScanLayout::oBT + b * (kScanSC * KD), src + KD * KD + (int64_t)c0 * KD,
+                  kScanSC * KD * sizeof(float), &bar[b]);
+        ++issued[b];
     };
-    prefetch(0);
-    *reinterpret_cast<float4 *>(sS + tid * kScanSC) =
-        p.h0 ? *reinterpret_cast<const float4 *>(p.h0 + (unit * KD + tid) * VD + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        s_err = 0;
+        fence_barrier_init();
+    }
+    if (tid < KD)
+        *reinterpret_cast<float4 *>(sS + tid * kScanSC) =
+            p.h0 ? *reinterpret_cast<const float4 *>(p.h0 + (unit * KD + tid) * VD + c0)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();
+    if (tid == 0) issue(0);
     for (int sg = 0; sg + 1 < nseg; ++sg) {
-        if (sg + 2 < nseg) {
-            prefetch(sg + 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();                                 // M(sg), B(sg) and S(sg) are in shared memory
+        // buffer (sg + 1) & 1 was last read before the previous step's first barrier
+        if (tid == 0 && sg + 2 < nseg) issue(sg + 1);
+        mbar_wait(&bar[sg & 1], (sg >> 1) & 1, &s_err, 1);
         const float *mt = sm_scan + ScanLayout::oMT + (sg & 1) * (KD * KD);
+        const float *bt = sm_scan + ScanLayout::oBT + (sg & 1) * (kScanSC * KD);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (tid < KD) v = make_float4(bt[tid], bt[KD + tid], bt[2 * KD + tid], bt[3 * KD + tid]);
         float acc[4][kScanSC];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < kScanSC; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
-        for (int kk = 0; kk < 32; ++kk) {
-            const int k = warp * 32 + kk;
+#pragma unroll
+        for (int kk = 0; kk < kScanKW; ++kk) {
+            const int k = warp * kScanKW + kk;
             const float4 a = *reinterpret_cast<const float4 *>(mt + k * KD + 4 * lane);
             const float4 b = *reinterpret_cast<const float4 *>(sS + k * kScanSC);
             const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -896,18 +899,29 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(SegScanParams
             *reinterpret_cast<float4 *>(sRed + (warp * KD + 4 * lane + i) * kScanSC) =
                 make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         __syncthreads();                                 // every partial sum is written; S(sg) is read
-        float4 v = *reinterpret_cast<const float4 *>(sm_scan + ScanLayout::oB + (sg & 1) * (KD * kScanSC) +
-                                                     tid * kScanSC);
+        if (tid < KD) {
 #pragma unroll
-        for (int w = 0; w < kScanWarps; ++w) {
-            const float4 r = *reinterpret_cast<const float4 *>(sRed + (w * KD + tid) * kScanSC);
-            v.x += r.x;
-            v.y += r.y;
-            v.z += r.z;
-            v.w += r.w;
+            for (int w = 0; w < kScanWarps; ++w) {
+                const float4 r = *reinterpret_cast<const float4 *>(sRed + (w * KD + tid) * kScanSC);
+                v.x += r.x;
+                v.y += r.y;
+                v.z += r.z;
+                v.w += r.w;
+            }
+            *reinterpret_cast<float4 *>(sS + tid * kScanSC) = v;
+            *reinterpret_cast<float4 *>(p.seg_start + ((unit * p.n_seg + sg + 1) * KD + tid) * VD + c0) = v;
         }
-        *reinterpret_cast<float4 *>(sS + tid * kScanSC) = v;
-        *reinterpret_cast<float4 *>(p.seg_start + ((unit * p.n_seg + sg + 1) * KD + tid) * VD + c0) = v;
+        __syncthreads();                                 // S(sg + 1) is complete; the partial sums are read
+    }
+    if (tid == 0 && *reinterpret_cast<volatile int *>(&s_err) != 0) {
+        // a copy did not arrive in time: wait (bounded) for the last copy into each buffer
+        for (int b = 0; b < 2; ++b) {
+            if (issued[b] == 0) continue;
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(&bar[b], (issued[b] - 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+            }
+        }
+        status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
     }
 }
 
@@ -999,7 +1013,7 @@ cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
 // GB300 measurements of these kernels (ns): summary + output chain per chunk, scan per
 // segment, the two extra launches, and the plain chain per chunk.
 int fwd_seg_count(int64_t nt_max, int n_max, int H) {
-    constexpr int64_t kChainAC = 1850, kScanStep = 600, kExtra = 5000, kPlain = 700;
+    constexpr int64_t kChainAC = 1830, kScanStep = 1200, kExtra = 8000, kPlain = 700;
     const int64_t units = (int64_t)n_max * H;
     const int64_t p_max = num_sms() / (8 * units);
     if (p_max < 3 || n_max <= 0) return 0;

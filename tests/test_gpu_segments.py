@@ -90,9 +90,9 @@ def test_ragged_and_empty_sequences(variant, use_order, lens, H):
 @pytest.mark.parametrize("T", [30, 100, 1221, 4000])
 @pytest.mark.parametrize("h0", [True, False], ids=["h0", "zero-h0"])
 def test_short_sequences_in_a_long_capacity(T, h0):
-    """One sequence of 1, 2, 20 and 63 chunks in an 8192-token capacity cut for 128 chunks
-    (19 segments on 152 SMs) into segments of ceil(chunks / segments) chunks: one segment,
-    two single-chunk segments, ten of two chunks, and so on."""
+    """One sequence of 1, 2, 20 and 63 chunks in an 8192-token capacity, whose plan cuts each
+    sequence into P segments (16 on 152 SMs) of ceil(chunks / P) chunks: one segment, two
+    single-chunk segments, ten of two chunks, and so on."""
     w = synth.varlen("seg-short", synth.GDN, "bf16", [T], 1, 8192, 1, 128, 128, h0=h0, seed=32)
     assert segments(w) >= 3
     x = synth.make_inputs(w)
