@@ -397,11 +397,21 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ld64(384 + half * 64, e64);               // L^T dO
 #pragma unroll
             for (int q = 0; q < 64; ++q) x[q] = fmaf(fr, x[q], e64[q]);
+            // dE as bf16 (hi) and its rounding remainder as bf16 (lo, in the [K; Q] tiles, free
+            // since R2): T^T dE and dE R^T take both, so dE enters them with 16 bits
 #pragma unroll
-            for (int q = 0; q < 8; ++q) *kchunk(gT3, 192, r, half * 64 + q * 8) = pack8(x + q * 8);
+            for (int q = 0; q < 8; ++q) {
+                const uint4 hi = pack8(x + q * 8);
+                float hv[8], lo[8];
+                unpack8(hi, hv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) lo[e] = x[q * 8 + e] - hv[e];
+                *kchunk(gT3, 192, r, half * 64 + q * 8) = hi;
+                *kchunk(gKQ, 64, r, half * 64 + q * 8) = pack8(lo);
+            }
         }
         to_async();
-        // ---- R4: dVb = T^T dE -> cols 256..383; [E; dO] S^T -> 128..255 (dO S^T in lanes 64..);
+        // ---- R4: dVb = T^T (dE_hi + dE_lo) -> cols 256..383; [E; dO] S^T -> 128..255 (dO S^T in lanes 64..);
         // [E; dO] E^T -> 384..447 (dO E^T in lanes 64..); [dE; E] R^T -> 448..511 (dE R^T in lanes
         // 0..63).  Columns 0..127 keep K S from R2 (lanes 0..63) for the dbeta and gate sums.
         if (tid == 0) {
@@ -424,6 +434,16 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_bf16(tmem + 384, aeo + oa, be + oa, idesc_bf16(128, 64), s > 0);
                 mma_bf16(tmem + 448, ade + oa, brr + orr, idesc_bf16(128, 64), s > 0);
             }
+            // the dE remainder: T^T dE_lo, and [dE_lo; -] R^T (lanes 64.. of that product unused)
+            const uint64_t bdl = smem_desc(sbase + gKQ, 8192, 1024, kSwizzle128B);        // dE_lo
+            const uint64_t adl = smem_desc(sbase + gKQ, 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + 256, at + s * 128, bdl + s * 128, idesc_bf16(128, 128, 1, 1), true);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tmem + 448, adl + (s >> 2) * (8192 >> 4) + (s & 3) * 2,
+                         brr + (s >> 2) * (8192 >> 4) + (s & 3) * 2, idesc_bf16(128, 64), true);
             mma_commit(&bar_mma);
         }
         // the v row of this thread (dbeta needs V, whose tile now holds R), while R4 runs
