@@ -83,6 +83,8 @@ def load_library(path: str = LIB_PATH):
     lib.gcl_fwd_chain_segments.argtypes = [i64, i32, i32, i32]
     lib.chunk_meta_build.restype = ctypes.c_int
     lib.chunk_meta_build.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp]
+    lib.chunk_meta_build_i64.restype = ctypes.c_int
+    lib.chunk_meta_build_i64.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp, vp]
     for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
         getattr(lib, fn).restype = ctypes.c_int
         getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs), vp]
@@ -157,8 +159,18 @@ def fwd_chain_segments(t_max: int, n_max: int, H: int, bt: int = CHUNK) -> int:
 
 
 def chunk_meta_build(cu_seqlens, t_max, chunk_indices, chunk_offsets, dev_status,
-                     seq_order=None, bt: int = CHUNK, stream=None):
+                     seq_order=None, bt: int = CHUNK, stream=None, cu_seqlens32=None):
+    """Chunk metadata from cu_seqlens (int32, or int64 with an int32 copy written to
+    cu_seqlens32 for the compute calls)."""
     n_max = cu_seqlens.shape[0] - 1
+    if cu_seqlens.element_size() == 8:
+        if cu_seqlens32 is None:
+            raise ValueError("an int64 cu_seqlens needs cu_seqlens32 (int32 [n_max + 1]) for its copy")
+        _check("chunk_meta_build_i64",
+               lib().chunk_meta_build_i64(_p(cu_seqlens), n_max, t_max, bt, chunk_indices.shape[0],
+                                          _p(cu_seqlens32), _p(chunk_indices), _p(chunk_offsets),
+                                          _p(seq_order), _p(dev_status), _stream(stream)))
+        return
     _check("chunk_meta_build",
            lib().chunk_meta_build(_p(cu_seqlens), n_max, t_max, bt, chunk_indices.shape[0],
                                   _p(chunk_indices), _p(chunk_offsets), _p(seq_order),

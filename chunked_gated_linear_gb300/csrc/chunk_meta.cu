@@ -10,6 +10,10 @@
 // exclusive scan of the per-sequence chunk counts (in tiles of 1024 with a
 // running carry), a fill of the index rows by binary search over the offsets,
 // and an optional longest-first order of the sequences (rank by counting).
+// The RFC's graph infrastructure covers int32 and int64 cu_seqlens ("Improve the
+// common graph infrastructure"): an int64 cu_seqlens is checked in int64 and, once
+// valid (every entry in [0, t_max], t_max < 2^31), narrowed exactly into the int32
+// copy that the compute calls read.
 #include "gcl_internal.cuh"
 
 namespace gcl {
@@ -44,10 +48,11 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *
     return r;
 }
 
+template <typename IdxT>
 __global__ void __launch_bounds__(kThreads)
-chunk_meta_kernel(const int32_t *__restrict__ cu, int32_t n_max, int64_t t_max, int32_t bt,
-                  int64_t nt_max, int32_t *__restrict__ idx, int32_t *__restrict__ off,
-                  int32_t *__restrict__ order, int32_t *__restrict__ status) {
+chunk_meta_kernel(const IdxT *__restrict__ cu, int32_t n_max, int64_t t_max, int32_t bt,
+                  int64_t nt_max, int32_t *__restrict__ cu32, int32_t *__restrict__ idx,
+                  int32_t *__restrict__ off, int32_t *__restrict__ order, int32_t *__restrict__ status) {
     __shared__ int s_flags;
     __shared__ int s_warp[32];
     __shared__ int s_total;
@@ -72,6 +77,8 @@ chunk_meta_kernel(const int32_t *__restrict__ cu, int32_t n_max, int64_t t_max, 
     const int code = (f & 2) ? GCL_DEV_CU_NONZERO_START
                    : (f & 1) ? GCL_DEV_CU_DECREASING
                    : (f & 4) ? GCL_DEV_CU_OVER_CAPACITY : GCL_DEV_OK;
+    if (cu32)                     // the int32 copy: exact once valid, zeros otherwise
+        for (int n = threadIdx.x; n <= n_max; n += kThreads) cu32[n] = code == GCL_DEV_OK ? (int32_t)cu[n] : 0;
     if (code != GCL_DEV_OK) {
         for (int64_t j = threadIdx.x; j < nt_max; j += kThreads) {
             idx[2 * j] = -1;
@@ -86,7 +93,7 @@ chunk_meta_kernel(const int32_t *__restrict__ cu, int32_t n_max, int64_t t_max, 
     // ---- offsets: exclusive scan of ceil(len / bt)
     for (int base = 0; base < n_max; base += kThreads) {
         const int n = base + threadIdx.x;
-        const int cnt = (n < n_max) ? (cu[n + 1] - cu[n] + bt - 1) / bt : 0;
+        const int cnt = (n < n_max) ? (int)(((int64_t)cu[n + 1] - (int64_t)cu[n] + bt - 1) / bt) : 0;
         const int ex = block_exclusive_scan(cnt, s_warp, &s_total);
         if (n < n_max) off[n] = s_carry + ex;
         __syncthreads();
@@ -116,10 +123,10 @@ chunk_meta_kernel(const int32_t *__restrict__ cu, int32_t n_max, int64_t t_max, 
     // ---- longest-first order (stable): rank = #longer + #equal with smaller index
     if (order) {
         for (int n = threadIdx.x; n < n_max; n += kThreads) {
-            const int ln = cu[n + 1] - cu[n];
+            const int ln = (int)(cu[n + 1] - cu[n]);
             int rank = 0;
             for (int m = 0; m < n_max; ++m) {
-                const int lm = cu[m + 1] - cu[m];
+                const int lm = (int)(cu[m + 1] - cu[m]);
                 rank += (lm > ln) || (lm == ln && m < n);
             }
             order[rank] = n;
@@ -133,8 +140,16 @@ chunk_meta_kernel(const int32_t *__restrict__ cu, int32_t n_max, int64_t t_max, 
 cudaError_t launch_chunk_meta(const int32_t *cu, int32_t n_max, int64_t t_max, int32_t bt,
                               int64_t nt_max, int32_t *idx, int32_t *off, int32_t *order,
                               int32_t *status, cudaStream_t s) {
-    chunk_meta_kernel<<<1, kThreads, 0, s>>>(cu, n_max, t_max, bt, nt_max, idx, off, order,
-                                             status);
+    chunk_meta_kernel<int32_t><<<1, kThreads, 0, s>>>(cu, n_max, t_max, bt, nt_max, nullptr, idx, off,
+                                                      order, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_meta_i64(const int64_t *cu, int32_t n_max, int64_t t_max, int32_t bt,
+                                  int64_t nt_max, int32_t *cu32, int32_t *idx, int32_t *off,
+                                  int32_t *order, int32_t *status, cudaStream_t s) {
+    chunk_meta_kernel<int64_t><<<1, kThreads, 0, s>>>(cu, n_max, t_max, bt, nt_max, cu32, idx, off,
+                                                      order, status);
     return cudaGetLastError();
 }
 

@@ -287,6 +287,27 @@ gcl_status_t chunk_meta_build(const int32_t *cu_seqlens, int32_t n_max, int64_t 
                       "chunk_meta_build");
 }
 
+gcl_status_t chunk_meta_build_i64(const int64_t *cu_seqlens, int32_t n_max, int64_t t_max,
+                                  int32_t bt, int64_t nt_max, int32_t *cu_seqlens32,
+                                  int32_t *chunk_indices, int32_t *chunk_offsets, int32_t *seq_order,
+                                  int32_t *dev_status, gcl_stream_t stream) {
+    g_err[0] = 0;
+    if (!cu_seqlens || !cu_seqlens32 || !chunk_indices || !chunk_offsets || !dev_status)
+        return fail(GCL_ERR_INVALID_ARG,
+                    "chunk_meta_build_i64: cu_seqlens, cu_seqlens32, chunk_indices, chunk_offsets, "
+                    "dev_status are required");
+    if (n_max < 1 || t_max < 1 || t_max >= (int64_t(1) << 31) || bt < 1)
+        return fail(GCL_ERR_INVALID_ARG,
+                    "chunk_meta_build_i64: need n_max >= 1, 1 <= t_max < 2^31, bt >= 1");
+    if (nt_max != gcl_nt_max(t_max, n_max, bt))
+        return fail(GCL_ERR_INVALID_ARG, "chunk_meta_build_i64: nt_max=%lld, expected %lld",
+                    (long long)nt_max, (long long)gcl_nt_max(t_max, n_max, bt));
+    return cuda_check(launch_chunk_meta_i64(cu_seqlens, n_max, t_max, bt, nt_max, cu_seqlens32,
+                                            chunk_indices, chunk_offsets, seq_order, dev_status,
+                                            static_cast<cudaStream_t>(stream)),
+                      "chunk_meta_build_i64");
+}
+
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args) {
     if (!args) return 0;
     return fwd_ws(args, kGDN, true);

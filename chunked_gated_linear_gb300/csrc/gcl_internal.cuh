@@ -59,6 +59,9 @@ struct BwdParams {
 cudaError_t launch_chunk_meta(const int32_t *cu, int32_t n_max, int64_t t_max, int32_t bt,
                               int64_t nt_max, int32_t *idx, int32_t *off, int32_t *order,
                               int32_t *status, cudaStream_t s);
+cudaError_t launch_chunk_meta_i64(const int64_t *cu, int32_t n_max, int64_t t_max, int32_t bt,
+                                  int64_t nt_max, int32_t *cu32, int32_t *idx, int32_t *off,
+                                  int32_t *order, int32_t *status, cudaStream_t s);
 cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s);
 // Tensor-core forward (GDN, bf16, K = V = 128).  Two launch plans: the W form
 // (prep + chain, 25 KiB of workspace per chunk and head) and the transition form

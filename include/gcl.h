@@ -117,6 +117,25 @@ gcl_status_t chunk_meta_build(const int32_t *cu_seqlens, int32_t n_max, int64_t 
                               int32_t *dev_status, gcl_stream_t stream);
 
 /*
+ * chunk_meta_build_i64 -- chunk_meta_build for an int64 cu_seqlens (FLA RFC,
+ * "Improve the common graph infrastructure": int32 and int64 cu_seqlens).
+ *
+ *   cu_seqlens     device int64 [n_max + 1], with the contract of chunk_meta_build.
+ *   cu_seqlens32   device int32 [n_max + 1] (out): the same offsets narrowed to
+ *                  int32 (exact: a valid cu_seqlens lies in [0, t_max], t_max < 2^31),
+ *                  or all zeros when a check fails.  Pass it as cu_seqlens to the
+ *                  compute calls, whose arguments are int32.
+ *   the rest       as chunk_meta_build; the checks run on the int64 values.
+ *
+ * One kernel launch; no host synchronisation; graph-capturable.  Host errors as
+ * chunk_meta_build, plus INVALID_ARG for a NULL cu_seqlens32.
+ */
+gcl_status_t chunk_meta_build_i64(const int64_t *cu_seqlens, int32_t n_max, int64_t t_max,
+                                  int32_t bt, int64_t nt_max, int32_t *cu_seqlens32,
+                                  int32_t *chunk_indices, int32_t *chunk_offsets, int32_t *seq_order,
+                                  int32_t *dev_status, gcl_stream_t stream);
+
+/*
  * Forward arguments (GDN and KDA).  All pointers are device pointers.
  */
 typedef struct gcl_fwd_args {

@@ -50,9 +50,10 @@ class Meta:
         self.order = torch.full((n_max,), 77, dtype=torch.int32, device=DEV)
         self.status = torch.full((1,), 77, dtype=torch.int32, device=DEV)
 
-    def build(self, cu_dev, stream=None):
+    def build(self, cu_dev, stream=None, cu_seqlens32=None):
         gcl.chunk_meta_build(cu_dev, self.t_max, self.idx, self.off, self.status,
-                             seq_order=self.order, bt=self.bt, stream=stream)
+                             seq_order=self.order, bt=self.bt, stream=stream,
+                             cu_seqlens32=cu_seqlens32)
 
 
 def run_fwd(w, d, meta=None, h_save=False, o_fill=CANARY, use_order=True, plan="fastest"):

@@ -72,6 +72,10 @@ def test_host_errors_before_any_launch(lib):
     assert lib.chunk_meta_build(fake, 4, 256, 64, 7, fake, fake, None, None, None) == INVALID
     assert lib.chunk_meta_build(fake, 4, 256, 64, 8, fake, fake, None, fake, None) == INVALID
     assert b"nt_max" in lib.gcl_last_error()
+    # the int64 variant also needs the int32 copy
+    assert lib.chunk_meta_build_i64(fake, 4, 256, 64, 8, None, fake, fake, None, fake, None) == INVALID
+    assert b"cu_seqlens32" in lib.gcl_last_error()
+    assert lib.chunk_meta_build_i64(fake, 4, 256, 64, 9, fake, fake, fake, None, fake, None) == INVALID
     # backward: workspace capacity is checked on the host
     b = gcl.BwdArgs(q=fake, k=fake, v=fake, g=fake, beta=fake, d_o=fake, cu_seqlens=fake,
                     chunk_indices=fake, chunk_offsets=fake, dq=fake, dk=fake, dv=fake, dg=fake,
