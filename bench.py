@@ -60,7 +60,7 @@ def parse():
 def bytes_per_step(w) -> int:
     """Algorithmic HBM bytes of one forward launch: every input read once, o written once,
     h0 read and ht written once per (sequence, head)."""
-    b = 2 if w.dtype == "bf16" else 4
+    b = 4 if w.dtype == "f32" else 2
     th = w.total_tokens * w.H
     per_th = (2 * w.K + 2 * w.V + 1) * b + 4 * (w.K if w.variant == synth.KDA else 1)
     units = w.n_max * w.H          # ht is written for every sequence slot (ht = h0 if empty)
@@ -177,7 +177,7 @@ class Runner:
     def __init__(self, gcl, w, x, dev):
         import torch
         self.gcl, self.w = gcl, w
-        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        dt = {"bf16": torch.bfloat16, "f16": torch.float16}.get(w.dtype, torch.float32)
         self.t = {}
         for n in ("q", "k", "v", "beta", "do"):
             if x.get(n) is not None:
@@ -207,7 +207,7 @@ class Runner:
         fargs = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], t["o"])
         fkw = dict(h0=t.get("h0"), ht=t["ht"], h_save=t.get("hs"), chunk_indices=t["idx"],
                    chunk_offsets=t["off"], seq_order=t["order"], dev_status=t["status"],
-                   scale=w.scale)
+                   scale=w.scale, bt=w.bt)
         wsq = gcl.kda_fwd_workspace_bytes if w.variant == synth.KDA else gcl.fwd_workspace_bytes
         t["fws"] = torch.empty(max(wsq(*fargs, **fkw), 16), dtype=torch.uint8, device=dev)
         self.fwd_args = gcl.fwd_args(*fargs, workspace=t["fws"], **fkw)
@@ -216,7 +216,7 @@ class Runner:
             args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], t["cu"], t["idx"],
                     t["off"], t["dq"], t["dk"], t["dv"], t["dg"], t["dbeta"])
             kw = dict(h0=t.get("h0"), dht=t.get("dht"), dh0=t["dh0"], h_save=t["hs"],
-                      dev_status=t["status"], scale=w.scale)
+                      dev_status=t["status"], scale=w.scale, bt=w.bt)
             nb = (gcl.kda_bwd_workspace_bytes if w.variant == synth.KDA else gcl.bwd_workspace_bytes)(*args, **kw)
             t["ws"] = torch.empty(nb, dtype=torch.uint8, device=dev)
             self.bwd_args = gcl.bwd_args(*args, workspace=t["ws"], **kw)
@@ -263,7 +263,7 @@ def launches_per_step(w) -> int:
     outputs when the chain is segmented -- one fused CUDA-core kernel otherwise) and
     the backward (GDN on the tensor cores: transition records, state-gradient sweep and two
     chunk-gradient kernels; otherwise the sweep and one chunk-gradient kernel)."""
-    tc = w.dtype == "bf16" and w.K == 128 and w.V == 128
+    tc = w.dtype == "bf16" and w.K == 128 and w.V == 128 and w.bt == 64
     tc_bwd = tc and w.variant == synth.GDN
     # a segmented chain (few long sequences): summaries, scan and segment outputs
     import chunked_gated_linear_gb300 as gcl

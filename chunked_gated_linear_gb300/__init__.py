@@ -15,7 +15,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgcl.so")
 
-GCL_F32, GCL_BF16 = 0, 1
+GCL_F32, GCL_BF16, GCL_F16 = 0, 1, 2
 DEV_STATUS = {0: "ok", 1: "cu_seqlens decreasing", 2: "cu_seqlens[0] != 0",
               3: "cu_seqlens[N_max] > T_max", 4: "invalid sequence range"}
 CHUNK = 64
@@ -146,6 +146,8 @@ def _dtype_of(t):
         return GCL_F32
     if t.dtype == torch.bfloat16:
         return GCL_BF16
+    if t.dtype == torch.float16:
+        return GCL_F16
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 

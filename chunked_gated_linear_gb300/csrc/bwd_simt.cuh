@@ -1,4 +1,6 @@
-// bwd_simt.cu -- GDN and KDA chunk backward on the CUDA cores (fp32 arithmetic).
+// bwd_simt.cuh -- GDN and KDA chunk backward on the CUDA cores (fp32 arithmetic).
+// The kernel templates (chunk size C = BT, 32 or 64); bwd_simt_{f32,bf16,f16}.cu instantiate
+// them per input type.
 //
 // FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths
 // on Ascend NPUs", section "Step 3": the backward path covers recomputation,
@@ -27,19 +29,19 @@
 //     over it accumulate in registers (dq, dk partials) and shared memory
 //     (dT, dL, row sums), always in a fixed order, so results are bitwise
 //     reproducible (no atomics).
+#pragma once
+
 #include "simt_map.cuh"
 
 namespace gcl {
-namespace {
-
-constexpr int C = kChunk;
+namespace simt_bwd {
 
 // ---------------------------------------------------------------- dstate sweep
 constexpr int kSweepThreads = 256;
 
-template <int K, int VS, int VAR>
+template <int K, int VS, int VAR, int C>
 struct SweepLayout {
-    static constexpr int LK = K + 1, LV = VS + 1;
+    static constexpr int LK = K + 1, LV = VS + 1, kLC = C + 1;
     static constexpr int oQ = 0, oK = oQ + C * LK, oW = oK + C * LK;
     static constexpr int oDO = oW + C * LK, oDE = oDO + C * LV, oDS = oDE + C * LV;
     static constexpr int oA = oDS + K * LV, oT = oA + C * kLC, oL = oT + C * kLC;
@@ -48,10 +50,11 @@ struct SweepLayout {
     static constexpr size_t bytes = sizeof(float) * total;
 };
 
-template <int VAR, typename Tin, int K, int VS>
+template <int VAR, typename Tin, int K, int VS, int C>
 __global__ void __launch_bounds__(kSweepThreads)
 dstate_sweep_kernel(BwdParams p) {
-    using Lay = SweepLayout<K, VS, VAR>;
+    using Lay = SweepLayout<K, VS, VAR, C>;
+    constexpr int kLC = C + 1;
     extern __shared__ float sm[];
     float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sW = sm + Lay::oW;
     float *sDO = sm + Lay::oDO, *sDE = sm + Lay::oDE, *sDS = sm + Lay::oDS;
@@ -96,19 +99,19 @@ dstate_sweep_kernel(BwdParams p) {
                 dst[(int64_t)c * V + v0 + j] = sDS[c * LV + j];
             }
         }
-        simt_load_chunk<VAR, Tin, K, kSweepThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG,
+        simt_load_chunk<VAR, Tin, K, kSweepThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG,
                                                     sB);
         for (int e = tid; e < C * VS; e += kSweepThreads) {
             const int r = e / VS, j = e % VS;
             sDO[r * LV + j] = r < len ? ld_in(d_o, ((t0 + r) * H + h) * (int64_t)V + v0 + j) : 0.f;
         }
         __syncthreads();
-        simt_gate_cumsum<VAR, K, kSweepThreads>(sG);
+        simt_gate_cumsum<VAR, K, kSweepThreads, C>(sG);
         __syncthreads();
-        simt_intra<VAR, K, kSweepThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+        simt_intra<VAR, K, kSweepThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
         __syncthreads();
-        simt_solve<kSweepThreads>(sA, sT);
-        simt_w<VAR, K, kSweepThreads>(sT, sB, sG, sK, sW);
+        simt_solve<kSweepThreads, C>(sA, sT);
+        simt_w<VAR, K, kSweepThreads, C>(sT, sB, sG, sK, sW);
         // dE = L^T dO + Ktil dS'
         for (int e = tid; e < C * VS; e += kSweepThreads) {
             const int i = e / VS, j = e % VS;
@@ -150,9 +153,9 @@ dstate_sweep_kernel(BwdParams p) {
 constexpr int kGradThreads = 512;
 constexpr int kVS = 16;   // value columns per slice
 
-template <int K>
+template <int K, int C>
 struct GradLayout {
-    static constexpr int LK = K + 1, LV = kVS + 1;
+    static constexpr int LK = K + 1, LV = kVS + 1, kLC = C + 1;
     static constexpr int oQ = 0, oK = oQ + C * LK;
     static constexpr int oT = oK + C * LK, oL = oT + C * kLC;
     static constexpr int oDL = oL + C * kLC, oDT = oDL + C * kLC;
@@ -173,13 +176,16 @@ struct GradLayout {
     static constexpr size_t bytes = sizeof(float) * oFreeEnd;
 };
 
-template <typename Tin, int K>
+template <typename Tin, int K, int C>
 __global__ void __launch_bounds__(kGradThreads)
 chunk_grad_kernel(BwdParams p) {
-    using Lay = GradLayout<K>;
+    using Lay = GradLayout<K, C>;
+    constexpr int kLC = C + 1;
     extern __shared__ float sm[];
     constexpr int LK = Lay::LK, LV = Lay::LV;
-    constexpr int CPT = K / 8;   // dq/dk columns owned per thread
+    constexpr int TPR = kGradThreads / C;   // threads per chunk row (8 at C = 64, 16 at C = 32)
+    constexpr int CPT = K / TPR;            // dq/dk columns owned per thread
+    static_assert(TPR * C == kGradThreads && CPT * TPR == K, "one thread group per chunk row");
     float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sT = sm + Lay::oT, *sL = sm + Lay::oL;
     float *sDL = sm + Lay::oDL, *sDT = sm + Lay::oDT, *sB = sm + Lay::oB, *sG = sm + Lay::oG;
     float *sRA = sm + Lay::oRA, *sRB = sm + Lay::oRB, *sRC = sm + Lay::oRC, *sRD = sm + Lay::oRD;
@@ -223,15 +229,15 @@ chunk_grad_kernel(BwdParams p) {
     const float *dSg = p.dh + (row * H + h) * KV;
 
     // ---- Map recompute
-    simt_load_chunk<kGDN, Tin, K, kGradThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    simt_load_chunk<kGDN, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
     __syncthreads();
-    simt_gate_cumsum<kGDN, K, kGradThreads>(sG);
+    simt_gate_cumsum<kGDN, K, kGradThreads, C>(sG);
     __syncthreads();
-    simt_intra<kGDN, K, kGradThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    simt_intra<kGDN, K, kGradThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
     for (int e = tid; e < C * kLC; e += kGradThreads) { sDL[e] = 0.f; sDT[e] = 0.f; }
     for (int r = tid; r < C; r += kGradThreads) { sRA[r] = sRB[r] = sRC[r] = sRD[r] = 0.f; }
     __syncthreads();
-    simt_solve<kGradThreads>(sA, sT);
+    simt_solve<kGradThreads, C>(sA, sT);
 
     const float gC = sG[C - 1];
     // per-row exponentials, once (the loops below only multiply)
@@ -240,7 +246,7 @@ chunk_grad_kernel(BwdParams p) {
         sFR[r] = expf(gC - sG[r]);
     }
     __syncthreads();
-    const int my_r = tid / 8, my_c0 = tid % 8;    // owner of dq/dk partials
+    const int my_r = tid / TPR, my_c0 = tid % TPR;    // owner of dq/dk partials
     float dq_p[CPT], dk_p[CPT];
 #pragma unroll
     for (int m = 0; m < CPT; ++m) { dq_p[m] = 0.f; dk_p[m] = 0.f; }
@@ -315,7 +321,7 @@ chunk_grad_kernel(BwdParams p) {
             const float fb = sB[my_r] * sEG[my_r];
 #pragma unroll
             for (int m = 0; m < CPT; ++m) {
-                const int c = my_c0 + 8 * m;
+                const int c = my_c0 + TPR * m;
                 float aq = dq_p[m], ak = dk_p[m];
                 for (int j = 0; j < kVS; ++j) {
                     aq = fmaf(sDO[my_r * LV + j], sS[c * LV + j], aq);
@@ -361,7 +367,7 @@ chunk_grad_kernel(BwdParams p) {
         sDT[r * kLC + i] = acc;      // sDT now holds dA
     }
     __syncthreads();
-    simt_intra<kGDN, K, kGradThreads>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
+    simt_intra<kGDN, K, kGradThreads, C>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
     __syncthreads();
     const float* sDA = sDT;
     // dgamma and dbeta, one thread per row
@@ -412,7 +418,7 @@ chunk_grad_kernel(BwdParams p) {
         if (r < len) {
 #pragma unroll
             for (int m = 0; m < CPT; ++m) {
-                const int c = my_c0 + 8 * m;
+                const int c = my_c0 + TPR * m;
                 float aq = p.scale * sEG[r] * dq_p[m];
                 for (int i = 0; i <= r; ++i) aq = fmaf(sP[r * kLC + i], sK[i * LK + c], aq);
                 float ak = dk_p[m];
@@ -442,30 +448,35 @@ chunk_grad_kernel(BwdParams p) {
 // and the last row's gamma (gamma_c) adds exp(gamma_c) <dS', S> (per channel) and
 // sum_r k exp(gamma_c - gamma) o Y3 to every row of dg = reverse in-chunk cumsum of dgamma.
 // Exponentials of differences of gammas only, so nothing overflows for gates <= 0.
-template <int K>
+template <int K, int C>
 struct GradKdaLayout {
-    static constexpr int LK = K + 1, LV = kVS + 1;
+    static constexpr int LK = K + 1, LV = kVS + 1, kLC = C + 1;
     static constexpr int oQ = 0, oK = oQ + C * LK, oG = oK + C * LK;
     static constexpr int oT = oG + C * LK, oL = oT + C * kLC, oDL = oL + C * kLC, oDT = oDL + C * kLC;
-    static constexpr int oB = oDT + C * kLC, oGC = oB + C, oSS = oGC + K, oRB = oSS + K, oRC = oRB + C;
+    // T, L, dL, dT are later reused for dgamma and the gamma_c terms (2 C x LK floats)
+    static constexpr int kTiles = 4 * C * kLC > 2 * C * LK ? 4 * C * kLC : 2 * C * LK;
+    static constexpr int oB = oT + kTiles, oGC = oB + C, oSS = oGC + K, oRB = oSS + K, oRC = oRB + C;
     static constexpr int oFree = oRC + C;
     static constexpr int oS = oFree, oDS = oS + K * LV;
     static constexpr int oV = oDS + K * LV, oDO = oV + C * LV, oKS = oDO + C * LV, oR = oKS + C * LV;
     static constexpr int oE = oR + C * LV, oDE = oE + C * LV, oDR = oDE + C * LV, oX2 = oDR + C * LV;
     static constexpr int oFreeEnd = oX2 + C * LV;
     static_assert(oFreeEnd - oFree >= 2 * C * kLC, "slice region reused for X and A'");
-    static_assert(oFree - oT >= 2 * C * LK, "T, L, dL, dT reused for dgamma and the gamma_c terms");
+    static_assert(oB - oT >= 2 * C * LK, "T, L, dL, dT reused for dgamma and the gamma_c terms");
     static constexpr size_t bytes = sizeof(float) * oFreeEnd;
     static_assert(bytes <= 232448, "one CTA per SM");
 };
 
-template <typename Tin, int K>
+template <typename Tin, int K, int C>
 __global__ void __launch_bounds__(kGradThreads)
 chunk_grad_kda_kernel(BwdParams p) {
-    using Lay = GradKdaLayout<K>;
+    using Lay = GradKdaLayout<K, C>;
+    constexpr int kLC = C + 1;
     extern __shared__ float sm[];
     constexpr int LK = Lay::LK, LV = Lay::LV;
-    constexpr int CPT = K / 8;   // (row, channel) pairs owned per thread
+    constexpr int TPR = kGradThreads / C;   // threads per chunk row
+    constexpr int CPT = K / TPR;            // (row, channel) pairs owned per thread
+    static_assert(TPR * C == kGradThreads && CPT * TPR == K, "one thread group per chunk row");
     float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sG = sm + Lay::oG;
     float *sT = sm + Lay::oT, *sL = sm + Lay::oL, *sDL = sm + Lay::oDL, *sDT = sm + Lay::oDT;
     float *sB = sm + Lay::oB, *sGC = sm + Lay::oGC, *sSS = sm + Lay::oSS;
@@ -510,16 +521,16 @@ chunk_grad_kda_kernel(BwdParams p) {
     const float *dSg = p.dh + (row * H + h) * KV;
 
     // ---- Map recompute
-    simt_load_chunk<kKDA, Tin, K, kGradThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    simt_load_chunk<kKDA, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
     __syncthreads();
-    simt_gate_cumsum<kKDA, K, kGradThreads>(sG);
+    simt_gate_cumsum<kKDA, K, kGradThreads, C>(sG);
     __syncthreads();
-    simt_intra<kKDA, K, kGradThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    simt_intra<kKDA, K, kGradThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
     for (int e = tid; e < C * kLC; e += kGradThreads) { sDL[e] = 0.f; sDT[e] = 0.f; }
     for (int r = tid; r < C; r += kGradThreads) { sRB[r] = 0.f; sRC[r] = 0.f; }
     for (int c = tid; c < K; c += kGradThreads) { sSS[c] = 0.f; sGC[c] = sG[(C - 1) * LK + c]; }
     __syncthreads();
-    simt_solve<kGradThreads>(sA, sT);
+    simt_solve<kGradThreads, C>(sA, sT);
     // Kp and Kb in place of Q and gamma (both are reloaded after the slice loop)
     for (int e = tid; e < C * K; e += kGradThreads) {
         const int r = e / K, c = e % K;
@@ -527,7 +538,7 @@ chunk_grad_kda_kernel(BwdParams p) {
         sKp[r * LK + c] = kv * expf(gm);
         sKb[r * LK + c] = kv * expf(sGC[c] - gm);
     }
-    const int my_r = tid / 8, my_c0 = tid % 8;    // owner of (row, channel) partials
+    const int my_r = tid / TPR, my_c0 = tid % TPR;    // owner of (row, channel) partials
     float y1[CPT], y2[CPT], y3[CPT];
 #pragma unroll
     for (int m = 0; m < CPT; ++m) { y1[m] = 0.f; y2[m] = 0.f; y3[m] = 0.f; }
@@ -599,7 +610,7 @@ chunk_grad_kda_kernel(BwdParams p) {
         // (row, channel) partials: Y1 += dR S^T, Y2 += dO S^T, Y3 += E dS'^T
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
-            const int c = my_c0 + 8 * m;
+            const int c = my_c0 + TPR * m;
             float a1 = y1[m], a2 = y2[m], a3 = y3[m];
             for (int j = 0; j < kVS; ++j) {
                 a1 = fmaf(sDR[my_r * LV + j], sS[c * LV + j], a1);
@@ -621,9 +632,9 @@ chunk_grad_kda_kernel(BwdParams p) {
     }
     __syncthreads();
     // q and gamma again (the slice loop held Kp and Kb in their buffers)
-    simt_load_chunk<kKDA, Tin, K, kGradThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    simt_load_chunk<kKDA, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
     __syncthreads();
-    simt_gate_cumsum<kKDA, K, kGradThreads>(sG);
+    simt_gate_cumsum<kKDA, K, kGradThreads, C>(sG);
     // dA = -T^T (dT T^T), strictly lower.  X = dT T^T into sA (dT is lower incl. diag).
     for (int e = tid; e < C * C; e += kGradThreads) {
         const int r = e / C, m = e % C;
@@ -640,7 +651,7 @@ chunk_grad_kda_kernel(BwdParams p) {
         sDT[r * kLC + i] = acc;      // sDT now holds dA
     }
     __syncthreads();
-    simt_intra<kKDA, K, kGradThreads>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
+    simt_intra<kKDA, K, kGradThreads, C>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
     __syncthreads();
     const float *sDA = sDT;
     for (int r = tid; r < C; r += kGradThreads) {   // dbeta, one thread per row
@@ -655,7 +666,7 @@ chunk_grad_kda_kernel(BwdParams p) {
         const float br = sB[r];
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
-            const int c = my_c0 + 8 * m;
+            const int c = my_c0 + TPR * m;
             const float gr = sG[r * LK + c], eg = expf(gr), ec = expf(sGC[c] - gr);
             float pl = 0.f, pa = 0.f, ql = 0.f, qa = 0.f;
             for (int i = 0; i <= r; ++i) {
@@ -682,7 +693,7 @@ chunk_grad_kda_kernel(BwdParams p) {
     __syncthreads();   // every read of T, L, dL, dA is done: reuse them for dgamma
 #pragma unroll
     for (int m = 0; m < CPT; ++m) {
-        const int c = my_c0 + 8 * m;
+        const int c = my_c0 + TPR * m;
         sDGm[my_r * LK + c] = dgv[m];
         sW3[my_r * LK + c] = wv[m];
     }
@@ -703,55 +714,54 @@ cudaError_t prep(Kern kern, size_t bytes) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <typename Tin, int K, int VS>
+template <typename Tin, int K, int VS, int C>
 cudaError_t launch_k(const BwdParams &p, bool sweep_done, cudaStream_t s) {
     cudaError_t e;
     if (!sweep_done) {
-        auto sweep = dstate_sweep_kernel<kGDN, Tin, K, VS>;
-        const size_t sb = SweepLayout<K, VS, kGDN>::bytes;
+        auto sweep = dstate_sweep_kernel<kGDN, Tin, K, VS, C>;
+        const size_t sb = SweepLayout<K, VS, kGDN, C>::bytes;
         if ((e = prep(sweep, sb)) != cudaSuccess) return e;
         sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    auto grad = chunk_grad_kernel<Tin, K>;
-    const size_t gb = GradLayout<K>::bytes;
+    auto grad = chunk_grad_kernel<Tin, K, C>;
+    const size_t gb = GradLayout<K, C>::bytes;
     if ((e = prep(grad, gb)) != cudaSuccess) return e;
     grad<<<dim3((unsigned)p.nt_max, p.H), kGradThreads, gb, s>>>(p);
     return cudaGetLastError();
 }
 
-template <typename Tin, int K, int VS>
+template <typename Tin, int K, int VS, int C>
 cudaError_t launch_kda(const BwdParams &p, bool sweep_done, cudaStream_t s) {
     cudaError_t e;
     if (!sweep_done) {
-        auto sweep = dstate_sweep_kernel<kKDA, Tin, K, VS>;
-        const size_t sb = SweepLayout<K, VS, kKDA>::bytes;
+        auto sweep = dstate_sweep_kernel<kKDA, Tin, K, VS, C>;
+        const size_t sb = SweepLayout<K, VS, kKDA, C>::bytes;
         if ((e = prep(sweep, sb)) != cudaSuccess) return e;
         sweep<<<dim3(p.V / VS, p.H, p.n_max), kSweepThreads, sb, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    auto grad = chunk_grad_kda_kernel<Tin, K>;
-    const size_t gb = GradKdaLayout<K>::bytes;
+    auto grad = chunk_grad_kda_kernel<Tin, K, C>;
+    const size_t gb = GradKdaLayout<K, C>::bytes;
     if ((e = prep(grad, gb)) != cudaSuccess) return e;
     grad<<<dim3((unsigned)p.nt_max, p.H), kGradThreads, gb, s>>>(p);
     return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s) {
-    if (dtype == GCL_BF16)
-        return p.K == 64 ? launch_kda<__nv_bfloat16, 64, 64>(p, sweep_done, s)
-                         : launch_kda<__nv_bfloat16, 128, 32>(p, sweep_done, s);
-    return p.K == 64 ? launch_kda<float, 64, 64>(p, sweep_done, s) : launch_kda<float, 128, 32>(p, sweep_done, s);
+template <typename Tin, int C>
+cudaError_t launch_chunk(const BwdParams &p, bool kda, bool sweep_done, cudaStream_t s) {
+    if (kda)
+        return p.K == 64 ? launch_kda<Tin, 64, 64, C>(p, sweep_done, s) : launch_kda<Tin, 128, 32, C>(p, sweep_done, s);
+    return p.K == 64 ? launch_k<Tin, 64, 64, C>(p, sweep_done, s) : launch_k<Tin, 128, 32, C>(p, sweep_done, s);
 }
 
-cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s) {
-    if (dtype == GCL_BF16)
-        return p.K == 64 ? launch_k<__nv_bfloat16, 64, 64>(p, sweep_done, s)
-                         : launch_k<__nv_bfloat16, 128, 32>(p, sweep_done, s);
-    return p.K == 64 ? launch_k<float, 64, 64>(p, sweep_done, s)
-                     : launch_k<float, 128, 32>(p, sweep_done, s);
+}  // namespace simt_bwd
+
+// The CUDA-core backward for input type Tin (GDN or KDA), chunk size 32 or 64.
+template <typename Tin>
+cudaError_t launch_bwd_simt_t(const BwdParams &p, bool kda, bool sweep_done, cudaStream_t s) {
+    return p.bt == 32 ? simt_bwd::launch_chunk<Tin, 32>(p, kda, sweep_done, s)
+                      : simt_bwd::launch_chunk<Tin, 64>(p, kda, sweep_done, s);
 }
 
 }  // namespace gcl

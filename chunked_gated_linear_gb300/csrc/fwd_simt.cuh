@@ -1,4 +1,5 @@
-// fwd_simt.cu -- fused chunkwise forward on the CUDA cores, all arithmetic in fp32.
+// fwd_simt.cuh -- fused chunkwise forward on the CUDA cores, all arithmetic in fp32.
+// The kernel templates; fwd_simt_{f32,bf16,f16}.cu instantiate them per input type.
 //
 // This kernel serves fp32 inputs (where a 1e-5 relative bound leaves no room
 // for reduced-precision tensor-core operands) and every size the tensor-core
@@ -10,7 +11,7 @@
 // value dimension, which needs no cross-CTA reduction because column j of S
 // depends only on column j of v and h0).
 //
-// Per chunk of c <= 64 tokens (Map phase in simt_map.cuh):
+// Per chunk of c <= C tokens (C = BT, 32 or 64; Map phase in simt_map.cuh):
 //   Map     A, L, T = (I + A)^-1, W = T diag(beta Gamma) K, U = T diag(beta) V
 //   Reduce  E = U - W S                                          (state read)
 //   Map     O = scale diag(Gamma) Q S + L E                      (chunk output)
@@ -19,16 +20,18 @@
 // is computed from the old state before the update overwrites it (HA-NPU
 // section 5, chunk-first order).  Rows past the end of the sequence are loaded
 // as k = q = v = 0, beta = 0, g = 0, which leaves S unchanged.
+#pragma once
+
 #include "simt_map.cuh"
 
 namespace gcl {
-namespace {
+namespace simt_fwd {
 
 constexpr int kThreads = 256;
-constexpr int C = kChunk;
 
-template <int K, int VS, int VAR>
+template <int K, int VS, int VAR, int C>
 struct FwdLayout {
+    static constexpr int kLC = C + 1;
     static constexpr int LK = K + 1;
     static constexpr int LV = VS + 1;
     static constexpr int oQ = 0;                     // Q, later scale*Gamma*Q   [C][LK]
@@ -46,10 +49,11 @@ struct FwdLayout {
     static constexpr size_t bytes = sizeof(float) * total;
 };
 
-template <int VAR, typename Tin, int K, int VS>
+template <int VAR, typename Tin, int K, int VS, int C>
 __global__ void __launch_bounds__(kThreads)
 fwd_simt_kernel(FwdParams p) {
-    using Lay = FwdLayout<K, VS, VAR>;
+    using Lay = FwdLayout<K, VS, VAR, C>;
+    constexpr int kLC = C + 1;
     extern __shared__ float sm[];
     float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sW = sm + Lay::oW;
     float *sV = sm + Lay::oV, *sE = sm + Lay::oE, *sS = sm + Lay::oS;
@@ -97,18 +101,18 @@ fwd_simt_kernel(FwdParams p) {
                 dst[(int64_t)c * V + v0 + j] = sS[c * LV + j];
             }
         }
-        simt_load_chunk<VAR, Tin, K, kThreads>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+        simt_load_chunk<VAR, Tin, K, kThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
         for (int e = tid; e < C * VS; e += kThreads) {
             const int r = e / VS, j = e % VS;
             sV[r * LV + j] = r < len ? ld_in(v, ((t0 + r) * H + h) * (int64_t)V + v0 + j) : 0.f;
         }
         __syncthreads();
-        simt_gate_cumsum<VAR, K, kThreads>(sG);
+        simt_gate_cumsum<VAR, K, kThreads, C>(sG);
         __syncthreads();
-        simt_intra<VAR, K, kThreads>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+        simt_intra<VAR, K, kThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
         __syncthreads();
-        simt_solve<kThreads>(sA, sT);
-        simt_w<VAR, K, kThreads>(sT, sB, sG, sK, sW);
+        simt_solve<kThreads, C>(sA, sT);
+        simt_w<VAR, K, kThreads, C>(sT, sB, sG, sK, sW);
         __syncthreads();
         // E = T diag(beta) V - W S
         for (int e = tid; e < C * VS; e += kThreads) {
@@ -156,10 +160,10 @@ fwd_simt_kernel(FwdParams p) {
     }
 }
 
-template <int VAR, typename Tin, int K, int VS>
+template <int VAR, typename Tin, int K, int VS, int C>
 cudaError_t launch_one(const FwdParams &p, cudaStream_t s) {
-    using Lay = FwdLayout<K, VS, VAR>;
-    auto kern = fwd_simt_kernel<VAR, Tin, K, VS>;
+    using Lay = FwdLayout<K, VS, VAR, C>;
+    auto kern = fwd_simt_kernel<VAR, Tin, K, VS, C>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
@@ -168,20 +172,21 @@ cudaError_t launch_one(const FwdParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int VAR, typename Tin>
-cudaError_t launch_dtype(const FwdParams &p, cudaStream_t s) {
-    if (p.K == 64) return launch_one<VAR, Tin, 64, 64>(p, s);
-    return launch_one<VAR, Tin, 128, 32>(p, s);
+template <int VAR, typename Tin, int C>
+cudaError_t launch_chunk(const FwdParams &p, cudaStream_t s) {
+    if (p.K == 64) return launch_one<VAR, Tin, 64, 64, C>(p, s);
+    return launch_one<VAR, Tin, 128, 32, C>(p, s);
 }
 
-}  // namespace
+}  // namespace simt_fwd
 
-cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s) {
+// The CUDA-core forward for input type Tin: variant, chunk size 32 or 64.
+template <typename Tin>
+cudaError_t launch_fwd_simt_t(const FwdParams &p, int variant, cudaStream_t s) {
+    using namespace simt_fwd;
     if (variant == kGDN)
-        return dtype == GCL_BF16 ? launch_dtype<kGDN, __nv_bfloat16>(p, s)
-                                 : launch_dtype<kGDN, float>(p, s);
-    return dtype == GCL_BF16 ? launch_dtype<kKDA, __nv_bfloat16>(p, s)
-                             : launch_dtype<kKDA, float>(p, s);
+        return p.bt == 32 ? launch_chunk<kGDN, Tin, 32>(p, s) : launch_chunk<kGDN, Tin, 64>(p, s);
+    return p.bt == 32 ? launch_chunk<kKDA, Tin, 32>(p, s) : launch_chunk<kKDA, Tin, 64>(p, s);
 }
 
 }  // namespace gcl

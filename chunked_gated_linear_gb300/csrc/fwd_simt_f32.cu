@@ -1,0 +1,17 @@
+// fwd_simt_f32.cu -- the CUDA-core forward for fp32 inputs, and the dispatch over input types
+// (the bf16 and fp16 instantiations live in their own files so that they compile in parallel).
+#include "fwd_simt.cuh"
+
+namespace gcl {
+
+template cudaError_t launch_fwd_simt_t<float>(const FwdParams &, int, cudaStream_t);
+extern template cudaError_t launch_fwd_simt_t<__nv_bfloat16>(const FwdParams &, int, cudaStream_t);
+extern template cudaError_t launch_fwd_simt_t<__half>(const FwdParams &, int, cudaStream_t);
+
+cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s) {
+    if (dtype == GCL_BF16) return launch_fwd_simt_t<__nv_bfloat16>(p, variant, s);
+    if (dtype == GCL_F16) return launch_fwd_simt_t<__half>(p, variant, s);
+    return launch_fwd_simt_t<float>(p, variant, s);
+}
+
+}  // namespace gcl

@@ -689,8 +689,8 @@ bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool fwd_tc_supported(int variant, int dtype, int K, int V) {
-    return (variant == kGDN || variant == kKDA) && dtype == GCL_BF16 && K == KD && V == VD;
+bool fwd_tc_supported(int variant, int dtype, int K, int V, int bt) {
+    return (variant == kGDN || variant == kKDA) && dtype == GCL_BF16 && K == KD && V == VD && bt == kChunk;
 }
 
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H) {

@@ -53,12 +53,12 @@ static gcl_status_t check_common(const char *fn, const void *q, const void *k, c
         return fail(GCL_ERR_INVALID_ARG, "%s: q, k, v, g, beta and cu_seqlens are required", fn);
     if (t_max < 1 || t_max >= (int64_t(1) << 31) || n_max < 1 || H < 1)
         return fail(GCL_ERR_INVALID_ARG, "%s: need 1 <= t_max < 2^31, n_max >= 1, H >= 1", fn);
-    if (bt != kChunk)
-        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (this build implements 64)", fn, bt);
+    if (bt != kChunk && bt != 32)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (this build implements 32 and 64)", fn, bt);
     if ((K != 64 && K != 128) || (V != 64 && V != 128))
         return fail(GCL_ERR_UNSUPPORTED, "%s: K=%d V=%d (supported: 64 or 128 each)", fn, K, V);
-    if (dtype != GCL_F32 && dtype != GCL_BF16)
-        return fail(GCL_ERR_UNSUPPORTED, "%s: dtype %d (supported: GCL_F32, GCL_BF16)", fn, dtype);
+    if (dtype != GCL_F32 && dtype != GCL_BF16 && dtype != GCL_F16)
+        return fail(GCL_ERR_UNSUPPORTED, "%s: dtype %d (supported: GCL_F32, GCL_BF16, GCL_F16)", fn, dtype);
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
         !aligned16(cu))
         return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
@@ -78,7 +78,7 @@ static void align_ws(void *ws, size_t bytes, void **out, size_t *out_bytes) {
 
 // Forward workspace: the minimum (W form) or what the fastest launch plan uses.
 static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
-    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V)) return 0;
+    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt)) return 0;
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->n_max <= 0) return 0;
     // the transition form, with the segment buffers when the fastest plan is segmented
@@ -97,7 +97,7 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     if (st != GCL_OK) return st;
     if (a->h_save && !a->chunk_offsets)
         return fail(GCL_ERR_INVALID_ARG, "%s: h_save needs chunk_offsets", fn);
-    const bool tc = fwd_tc_supported(variant, a->dtype, a->K, a->V);
+    const bool tc = fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (tc) {
         if (!a->chunk_indices || !a->chunk_offsets)
@@ -124,7 +124,7 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     p.workspace = nullptr;
     p.workspace_bytes = 0;
     if (tc) align_ws(a->workspace, a->workspace_bytes, &p.workspace, &p.workspace_bytes);
-    p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V;
+    p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V; p.bt = a->bt;
     p.nt_max = ntm;
     p.scale = a->scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -142,7 +142,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static size_t bwd_ws(const gcl_bwd_args *a, int variant) {
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
-    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V);
+    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
     const bool tc = variant == kGDN && tc_fwd;
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
     // tensor-core sweep (GDN and KDA bf16 K = V = 128): transition records; GDN's tensor-core
@@ -193,15 +193,15 @@ static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int vari
     p.dq = a->dq; p.dk = a->dk; p.dv = a->dv; p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->dh0;
     p.dev_status = a->dev_status;
     p.t_max = a->t_max; p.nt_max = ntm; p.n_max = a->n_max;
-    p.H = a->H; p.K = a->K; p.V = a->V; p.scale = a->scale;
-    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V);
+    p.H = a->H; p.K = a->K; p.V = a->V; p.bt = a->bt; p.scale = a->scale;
+    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
     const bool tc = variant == kGDN && tc_fwd;        // tensor-core backward: GDN
     FwdParams f{};
     f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
     f.cu_seqlens = a->cu_seqlens; f.chunk_indices = a->chunk_indices;
     f.chunk_offsets = a->chunk_offsets; f.seq_order = nullptr;
     f.o = nullptr; f.ht = nullptr; f.h_save = nullptr; f.dev_status = a->dev_status;
-    f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V;
+    f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V; f.bt = a->bt;
     f.nt_max = ntm;
     f.scale = a->scale;
     const size_t fw = !tc_fwd ? 0

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,7 +14,8 @@
 namespace gcl {
 
 enum Variant { kGDN = 0, kKDA = 1 };
-constexpr int kChunk = 64;   // BT: tokens per chunk
+constexpr int kChunk = 64;   // BT: tokens per chunk of the tensor-core path (the CUDA-core
+                             // path also takes 32)
 
 // Host: record a one-line error for gcl_last_error() and return `st`.
 gcl_status_t fail(gcl_status_t st, const char *fmt, ...);
@@ -33,7 +35,7 @@ struct FwdParams {
     void *workspace;
     size_t workspace_bytes;
     int64_t t_max, nt_max;
-    int32_t n_max, H, K, V;
+    int32_t n_max, H, K, V, bt;
     float scale;
 };
 
@@ -51,7 +53,7 @@ struct BwdParams {
     float *dq, *dk, *dv, *dg, *dbeta, *dh0;
     int32_t *dev_status;
     int64_t t_max, nt_max;
-    int32_t n_max, H, K, V;
+    int32_t n_max, H, K, V, bt;
     float scale;
 };
 
@@ -63,6 +65,8 @@ cudaError_t launch_chunk_meta_i64(const int64_t *cu, int32_t n_max, int64_t t_ma
                                   int64_t nt_max, int32_t *cu32, int32_t *idx, int32_t *off,
                                   int32_t *order, int32_t *status, cudaStream_t s);
 cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s);
+template <typename Tin>
+cudaError_t launch_fwd_simt_t(const FwdParams &p, int variant, cudaStream_t s);
 // Tensor-core forward (GDN, bf16, K = V = 128).  Two launch plans: the W form
 // (prep + chain, 25 KiB of workspace per chunk and head) and the transition form
 // (96 KiB per chunk and head, a shorter serial step), which is taken when the column
@@ -71,7 +75,7 @@ cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s);
 cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s);
 // KDA on the tensor cores: transition-form records with per-channel gates, then the chain.
 cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s);
-bool fwd_tc_supported(int variant, int dtype, int K, int V);
+bool fwd_tc_supported(int variant, int dtype, int K, int V, int bt);
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H);     // W form (the minimum)
 size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H);   // transition form
 // Segment-parallel chain (few long sequences): segments per sequence (0: the plain chain) and
@@ -91,6 +95,8 @@ cudaError_t launch_bwd_simt(const BwdParams &p, int dtype, bool sweep_done, cuda
 // KDA backward on the CUDA cores: state-gradient sweep with per-channel decay, then the chunk
 // gradients (dg per key channel).
 cudaError_t launch_bwd_simt_kda(const BwdParams &p, int dtype, bool sweep_done, cudaStream_t s);
+template <typename Tin>
+cudaError_t launch_bwd_simt_t(const BwdParams &p, bool kda, bool sweep_done, cudaStream_t s);
 // causal_conv1d (short_conv.cu)
 struct ConvLaunch {
     const void *x, *w, *bias, *residual, *h0, *dy;
@@ -121,7 +127,9 @@ __device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i];
 __device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) {
     return __bfloat162float(p[i]);
 }
+__device__ __forceinline__ float ld_in(const __half *p, int64_t i) { return __half2float(p[i]); }
 __device__ __forceinline__ void st_out(float *p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_out(__half *p, int64_t i, float x) { p[i] = __float2half_rn(x); }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, int64_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
 }

@@ -10,14 +10,12 @@
 // ("forward intra": KK^T and QK^T; per key channel for KDA), and
 // T = (I + A)^-1 by row-wise forward substitution ("triangular solve").
 // All decay factors are exp of a non-positive number, so nothing overflows.
+// C is the chunk size (BT, 32 or 64); C x C tiles use the row stride C + 1.
 #pragma once
 
 #include "gcl_internal.cuh"
 
 namespace gcl {
-
-constexpr int kC = kChunk;
-constexpr int kLC = kC + 1;
 
 // Shared-memory row strides: +1 float spreads rows over the banks.
 template <int K>
@@ -25,40 +23,40 @@ struct SimtStrides {
     static constexpr int LK = K + 1;
 };
 
-template <int VAR, typename Tin, int K, int NT>
+template <int VAR, typename Tin, int K, int NT, int C>
 __device__ __forceinline__ void simt_load_chunk(const Tin *q, const Tin *k, const float *g,
                                                 const Tin *beta, int64_t t0, int len, int h,
                                                 int H, float *sQ, float *sK, float *sG,
                                                 float *sB) {
     constexpr int LK = K + 1;
     const int tid = threadIdx.x;
-    for (int e = tid; e < kC * K; e += NT) {
+    for (int e = tid; e < C * K; e += NT) {
         const int r = e / K, c = e % K;
         const int64_t gi = ((t0 + r) * H + h) * (int64_t)K + c;
         sQ[r * LK + c] = r < len ? ld_in(q, gi) : 0.f;
         sK[r * LK + c] = r < len ? ld_in(k, gi) : 0.f;
         if (VAR == kKDA) sG[r * LK + c] = r < len ? g[gi] : 0.f;
     }
-    for (int r = tid; r < kC; r += NT) {
+    for (int r = tid; r < C; r += NT) {
         sB[r] = r < len ? ld_in(beta, (t0 + r) * H + h) : 0.f;
         if (VAR == kGDN) sG[r] = r < len ? g[(t0 + r) * H + h] : 0.f;
     }
 }
 
 // gamma: inclusive cumsum of g down the chunk (per key channel for KDA).
-template <int VAR, int K, int NT>
+template <int VAR, int K, int NT, int C>
 __device__ __forceinline__ void simt_gate_cumsum(float *sG) {
     constexpr int LK = K + 1;
     const int tid = threadIdx.x;
     if (VAR == kGDN) {
         if (tid == 0) {
             float acc = 0.f;
-            for (int r = 0; r < kC; ++r) { acc += sG[r]; sG[r] = acc; }
+            for (int r = 0; r < C; ++r) { acc += sG[r]; sG[r] = acc; }
         }
     } else {
         for (int c = tid; c < K; c += NT) {
             float acc = 0.f;
-            for (int r = 0; r < kC; ++r) { acc += sG[r * LK + c]; sG[r * LK + c] = acc; }
+            for (int r = 0; r < C; ++r) { acc += sG[r * LK + c]; sG[r * LK + c] = acc; }
         }
     }
 }
@@ -70,13 +68,13 @@ __device__ __forceinline__ float gam(const float *sG, int r, int c) {
 
 // A (= beta_r A', strictly lower) into sA and L into sL.  If sAp is not null it
 // also receives A' (without beta).
-template <int VAR, int K, int NT>
+template <int VAR, int K, int NT, int C>
 __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, const float *sG,
                                            const float *sB, float scale, float *sA, float *sL,
                                            float *sAp) {
-    constexpr int LK = K + 1;
-    for (int e = threadIdx.x; e < kC * kC; e += NT) {
-        const int r = e / kC, i = e % kC;
+    constexpr int LK = K + 1, kLC = C + 1;
+    for (int e = threadIdx.x; e < C * C; e += NT) {
+        const int r = e / C, i = e % C;
         float ap = 0.f, l = 0.f;
         if (i <= r) {
             float kk = 0.f, qk = 0.f;
@@ -106,14 +104,15 @@ __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, con
 
 // T = (I + A)^-1 for unit lower-triangular I + A:
 //   T[r,r] = 1,  T[r,i] = -A[r,i] - sum_{i<m<r} A[r,m] T[m,i]  (i < r), row by row.
-template <int NT>
+template <int NT, int C>
 __device__ __forceinline__ void simt_solve(const float *sA, float *sT) {
-    for (int e = threadIdx.x; e < kC * kC; e += NT) {
-        const int r = e / kC, i = e % kC;
+    constexpr int kLC = C + 1;
+    for (int e = threadIdx.x; e < C * C; e += NT) {
+        const int r = e / C, i = e % C;
         sT[r * kLC + i] = (r == i) ? 1.f : 0.f;
     }
     __syncthreads();
-    for (int r = 1; r < kC; ++r) {
+    for (int r = 1; r < C; ++r) {
         for (int i = threadIdx.x; i < r; i += NT) {
             float acc = -sA[r * kLC + i];
             for (int m = i + 1; m < r; ++m) acc = fmaf(-sA[r * kLC + m], sT[m * kLC + i], acc);
@@ -124,11 +123,11 @@ __device__ __forceinline__ void simt_solve(const float *sA, float *sT) {
 }
 
 // W = T diag(beta Gamma) K (GDN) or T diag(beta) (K * Gamma) (KDA).
-template <int VAR, int K, int NT>
+template <int VAR, int K, int NT, int C>
 __device__ __forceinline__ void simt_w(const float *sT, const float *sB, const float *sG,
                                        const float *sK, float *sW) {
-    constexpr int LK = K + 1;
-    for (int e = threadIdx.x; e < kC * K; e += NT) {
+    constexpr int LK = K + 1, kLC = C + 1;
+    for (int e = threadIdx.x; e < C * K; e += NT) {
         const int r = e / K, c = e % K;
         float acc = 0.f;
         for (int i = 0; i <= r; ++i)

@@ -41,6 +41,22 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def f16_round(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest fp16 (numpy's IEEE conversion, ties to even).
+
+    Returns float32 values that are exactly representable in fp16."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Inputs of a workload of element type dtype ("f32", "bf16" or "f16") as float32."""
+    if dtype == "bf16":
+        return bf16_round(x)
+    if dtype == "f16":
+        return f16_round(x)
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
 @dataclass
 class Workload:
     """A named synthetic workload.  Sizes follow the method's own notation."""
@@ -102,6 +118,10 @@ def standard_workloads():
         # the chunk-head-chunk mapping of the third scheduling tier serves
         dense("gdn_fwd_bf16_T65536_H1_d128", GDN, "bf16", 1, 65536, 1, 128, 128, seed=6),
         dense("kda_fwd_bf16_T65536_H1_d128", KDA, "bf16", 1, 65536, 1, 128, 128, seed=7),
+        # the RFC test matrix's variants at the headline sizes: fp16 inputs, chunk size 32
+        dense("gdn_fwd_f16_T4096_H16_d128", GDN, "f16", 1, 4096, 16, 128, 128, seed=8),
+        dense("gdn_fwd_bf16_bt32_T4096_H16_d128", GDN, "bf16", 1, 4096, 16, 128, 128, seed=9,
+              bt=32),
     ]
 
 
@@ -123,8 +143,8 @@ def cu_seqlens_of(w: Workload) -> np.ndarray:
 def make_inputs(w: Workload, seed: int | None = None, pad_value: float = float("nan")):
     """Draw the inputs of workload ``w``.
 
-    Returns a dict of float32 numpy arrays (bf16-representable where w.dtype is
-    bf16) in fixed-capacity layout: q, k [T_max,H,K]; v [T_max,H,V]; beta [T_max,H];
+    Returns a dict of float32 numpy arrays (bf16- or fp16-representable where w.dtype is
+    bf16 or f16) in fixed-capacity layout: q, k [T_max,H,K]; v [T_max,H,V]; beta [T_max,H];
     g [T_max,H] or [T_max,H,K]; h0 [N_max,H,K,V] or None; cu_seqlens int32
     [N_max+1]; and, for backward workloads, do [T_max,H,V] and dht [N_max,H,K,V]."""
     seed = w.seed if seed is None else seed
@@ -138,7 +158,7 @@ def make_inputs(w: Workload, seed: int | None = None, pad_value: float = float("
         return out
 
     def rnd(a):
-        return bf16_round(a) if w.dtype == "bf16" else a.astype(np.float32)
+        return round_to(a, w.dtype)
 
     q = rng.standard_normal((T, H, K), dtype=np.float32)
     q /= np.linalg.norm(q, axis=-1, keepdims=True)

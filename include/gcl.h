@@ -68,7 +68,8 @@ typedef enum gcl_status {
 
 typedef enum gcl_dtype {
     GCL_F32 = 0,   /* q, k, v, beta, do, o in fp32; every internal product in fp32     */
-    GCL_BF16 = 1   /* q, k, v, beta, do, o in bf16; state and accumulation in fp32     */
+    GCL_BF16 = 1,  /* q, k, v, beta, do, o in bf16; state and accumulation in fp32     */
+    GCL_F16 = 2    /* q, k, v, beta, do, o in fp16; every internal product in fp32     */
 } gcl_dtype_t;
 
 typedef void *gcl_stream_t;
@@ -160,7 +161,7 @@ typedef struct gcl_fwd_args {
     int64_t t_max;                 /* token capacity of every [t_max, ...] buffer            */
     int32_t n_max;                 /* sequence capacity (cu_seqlens has n_max + 1 entries)   */
     int32_t H, K, V;               /* heads, key dim, value dim                              */
-    int32_t bt;                    /* chunk size; 64 in this build                           */
+    int32_t bt;                    /* chunk size: 64, or 32 (CUDA-core kernel only)          */
     float scale;                   /* read-out scale, usually K^-1/2                         */
     int32_t dtype;                 /* gcl_dtype_t of q, k, v, beta, o                        */
 } gcl_fwd_args;
@@ -222,8 +223,9 @@ int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t 
  * CTAs (HA-NPU section 4, column-wise split without cross-core reductions).
  * Zero-length sequences write ht = h0 (or zeros).
  *
- * Supported: bt = 64; K, V in {64, 128}; dtype GCL_F32 or GCL_BF16.  GDN and
- * KDA with bf16 inputs and K = V = 128 run on the tensor cores (tcgen05): a
+ * Supported: bt in {32, 64} (the RFC's test matrix, "BT=32 and BT=64"); K, V in
+ * {64, 128}; dtype GCL_F32, GCL_BF16 or GCL_F16.  GDN and KDA with bf16 inputs,
+ * K = V = 128 and bt = 64 run on the tensor cores (tcgen05): a
  * chunk-parallel launch over chunk_indices forms per chunk either T = (I + A)^-1
  * and L (W form, GDN) or the chunk's transition S' = Gamma_c S + N S + B and
  * output O = Y S + Z (transition form; for KDA Gamma_c is a per-key-channel

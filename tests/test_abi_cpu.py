@@ -60,7 +60,7 @@ def test_host_errors_before_any_launch(lib):
     fake = 1 << 20   # a 16-byte aligned non-null value; never dereferenced on these paths
     full = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake, t_max=128,
                 n_max=1, H=1, K=128, V=128, bt=64, scale=1.0, dtype=1)
-    for bad, code in ((dict(bt=32), UNSUPPORTED), (dict(K=96), UNSUPPORTED),
+    for bad, code in ((dict(bt=16), UNSUPPORTED), (dict(K=96), UNSUPPORTED),
                       (dict(V=256), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED),
                       (dict(t_max=0), INVALID), (dict(n_max=0), INVALID),
                       (dict(q=fake + 4), INVALID), (dict(h_save=fake), INVALID)):

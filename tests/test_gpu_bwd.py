@@ -24,7 +24,7 @@ def run_bwd(w, d, meta, h_save=None, with_dht=True):
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["do"], d["cu_seqlens"], meta.idx,
             meta.off, out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"])
     kw = dict(h0=d.get("h0"), dht=d["dht"] if with_dht else None, dh0=out["dh0"],
-              h_save=h_save, dev_status=meta.status, scale=w.scale)
+              h_save=h_save, dev_status=meta.status, scale=w.scale, bt=w.bt)
     nbytes = (gcl.kda_bwd_workspace_bytes if kda else gcl.bwd_workspace_bytes)(*args, **kw)
     ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)      # stale contents
     (gcl.kda_chunk_bwd if kda else gcl.gdn_chunk_bwd)(*args, workspace=ws, **kw)
