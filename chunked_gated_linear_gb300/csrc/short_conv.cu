@@ -8,18 +8,22 @@
 // taps per channel and xx_n(i) the i-th input of sequence n (the initial state for i < 0):
 //   y[bos + p] = act(b + sum_j w[:, j] xx_n(p - (W - 1) + j)) + r[bos + p],
 //   ht[n, :, k] = xx_n(len - (W - 1) + k)   (k = 0 .. W - 2, oldest first).
-// The work list is chunk_indices (64-token chunks), so the grid depends only on the
-// capacities: one CTA per (row, block of channels), plus one block per sequence slot that
-// passes the state through for zero-length sequences.  The path is HBM-bound: a CTA stages its
-// chunk's rows and the W - 1 rows before them (the previous chunk, or the initial state) into
-// shared memory with independent 16-byte loads, so every byte of the chunk is in flight at
-// once, then each thread produces whole output rows of 8 channels from shared memory.
+// The work list is chunk_indices (64-token chunks) x blocks of channels, so the launch depends
+// only on the capacities.  The path is HBM-bound.  Forward: one CTA per (chunk row, block of
+// channels), plus one per sequence slot that passes the state through for zero-length
+// sequences; a CTA stages its chunk's rows and the W - 1 rows before them (the previous chunk,
+// or the initial state) into shared memory with independent 16-byte asynchronous copies, so
+// every byte of the chunk is in flight at once, then each thread produces whole output rows of
+// 8 channels.  Backward: persistent (a fixed grid of two CTAs per SM walks the chunk rows of
+// one block of channels each) and double-buffered: while a CTA computes one chunk from shared
+// memory, the rows of its next chunk are already in flight.
 //
 // Backward (reverse mode of <dy, y> + <dht, ht>): a CTA also stages dy and the W - 1 rows
 // after the chunk, forms dpre = dy act'(pre) once in shared memory, then
 //   dx[p] = sum_j dpre[p + W - 1 - j] w[:, j] (+ dht for the last W - 1 positions),
-//   dh0 from the first chunk of each sequence, and dw, db as per-chunk partial sums that a
-//   second kernel adds over the chunks in a fixed order (no atomics: reproducible).
+//   dh0 from the first chunk of each sequence, and dw, db as partial sums per CTA (each CTA
+//   walks its rows in a fixed order for one block of channels) that a second kernel adds over
+//   the CTAs in a fixed order (no atomics: reproducible on a given GPU).
 #include "gcl_internal.cuh"
 
 namespace gcl {
@@ -40,6 +44,7 @@ struct ConvParams {
     int32_t *status;
     int64_t t_max, nt_max;
     int32_t n_max, D, act;
+    int32_t n_part;                                    // backward: CTAs per block of channels
 };
 
 template <typename T>
@@ -110,18 +115,15 @@ __device__ __forceinline__ bool conv_row(const ConvParams &p, int j, int &n, int
     return true;
 }
 
-// A zero-length sequence n (block index past the chunk rows): ht = h0 (or zeros); in the
-// backward dh0 = dht (or zeros).  Returns true if this block was such a block (or past them).
+// Sequence n, channels [cb * channels, +channels): if the sequence is empty, ht = h0 (or zeros);
+// in the backward dh0 = dht (or zeros).
 template <typename T, int W>
-__device__ __forceinline__ bool conv_empty_sequence(const ConvParams &p, int channels, bool backward) {
-    const int64_t i = (int64_t)blockIdx.x - p.nt_max;
-    if (i < 0) return false;
-    const int n = (int)i;
-    if (n >= p.n_max) return true;
+__device__ __forceinline__ void conv_empty_sequence(const ConvParams &p, int n, int cb, int channels,
+                                                    bool backward) {
     const int64_t bos = p.cu[n], eos = p.cu[n + 1];
-    if (eos != bos) return true;
+    if (eos != bos) return;
     for (int e = threadIdx.x; e < channels * (W - 1); e += kConvThreads) {
-        const int c = blockIdx.y * channels + e / (W - 1), k = e % (W - 1);
+        const int c = cb * channels + e / (W - 1), k = e % (W - 1);
         if (c >= p.D) continue;
         const int64_t o = ((int64_t)n * p.D + c) * (W - 1) + k;
         if (!backward) {
@@ -130,7 +132,6 @@ __device__ __forceinline__ bool conv_empty_sequence(const ConvParams &p, int cha
             p.dh0[o] = p.dht ? p.dht[o] : 0.f;
         }
     }
-    return true;
 }
 
 // Stage rows [r_lo, r_hi) of the chunk (relative to t0; rows < 0 come from the previous chunk,
@@ -165,7 +166,15 @@ __device__ __forceinline__ void conv_stage(const ConvParams &p, const T *src, T 
     }
 }
 
+__device__ __forceinline__ void conv_stage_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// all but the most recent group of copies have landed (this thread's; a barrier follows)
+__device__ __forceinline__ void conv_stage_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void conv_stage_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Row j of chunk_indices is a live chunk (live rows come first, then sentinels).
+__device__ __forceinline__ bool conv_live(const ConvParams &p, int64_t j) {
+    return j < p.nt_max && p.chunk_indices[2 * j] >= 0;
+}
 
 template <typename T, int W>
 __global__ void __launch_bounds__(kConvThreads, 4)
@@ -174,7 +183,11 @@ conv_fwd_kernel(ConvParams p) {
     constexpr int G = CB / kChannelsPerThread, RL = kConvThreads / G;
     __shared__ __align__(16) T tile[(C + W - 1) * CB];
     if (status_blocks(p.status)) return;
-    if (conv_empty_sequence<T, W>(p, CB, false)) return;
+    if ((int64_t)blockIdx.x >= p.nt_max) {                 // the sequence slots: zero-length sequences
+        const int64_t n = (int64_t)blockIdx.x - p.nt_max;
+        if (n < p.n_max) conv_empty_sequence<T, W>(p, (int)n, blockIdx.y, CB, false);
+        return;
+    }
     int n, ic;
     int64_t bos, eos;
     if (!conv_row(p, blockIdx.x, n, ic, bos, eos)) return;
@@ -182,6 +195,7 @@ conv_fwd_kernel(ConvParams p) {
     const int64_t t0 = bos + (int64_t)ic * C;
     const int len = (int)(eos - t0 < C ? eos - t0 : C);
     conv_stage<T, W>(p, static_cast<const T *>(p.x), tile, CB, cb0, t0, ic, n, -(W - 1), len);
+    conv_stage_commit();
     conv_stage_wait();
     __syncthreads();
     // thread: 8 channels (vector g) of rows rr, rr + RL, ... (a warp: one row, 512 bytes)
@@ -229,42 +243,47 @@ conv_fwd_kernel(ConvParams p) {
 // stored in the two halves of the row.
 __device__ __forceinline__ int dp_col(int c, int cb) { return ((c & 4) ? cb / 2 : 0) + ((c >> 3) << 2) + (c & 3); }
 
-// Backward tiles (dynamic shared memory): x rows [-(W - 1), C + W - 1) and dy rows [0, C + W - 1)
-// in the input type, dpre rows [0, C + W - 1) in fp32, CB channels each.
+// Backward tiles (dynamic shared memory): two buffers of {x rows [-(W - 1), C + W - 1) and dy rows
+// [0, C + W - 1) in the input type}, then dpre rows [0, C + W - 1) in fp32, CB channels each.
 template <typename T, int W>
 struct ConvBwdLayout {
     static constexpr int CB = kBwdChannels * 2 / (int)sizeof(T);
     static constexpr int RX = C + 2 * (W - 1), RQ = C + W - 1;
-    static constexpr size_t oX = 0, oDY = oX + (size_t)RX * CB * sizeof(T);
-    static constexpr size_t oDP = (oDY + (size_t)RQ * CB * sizeof(T) + 15) / 16 * 16;
+    static constexpr size_t kX = (size_t)RX * CB * sizeof(T), kDY = (size_t)RQ * CB * sizeof(T);
+    static constexpr size_t kBuf = (kX + kDY + 15) / 16 * 16;
+    static constexpr size_t oDP = 2 * kBuf;
     static constexpr size_t bytes = oDP + (size_t)RQ * CB * sizeof(float);
-    static_assert(kConvThreads % CB == 0 && (size_t)(kConvThreads / CB) * (W + 1) * CB * 4 <= RQ * CB * sizeof(T),
-                  "the dy tile holds the per-group partial sums");
+    static_assert(kConvThreads % CB == 0 && (size_t)(kConvThreads / CB) * (W + 1) * CB <= (size_t)RQ * CB,
+                  "the dpre tile holds the per-group partial sums at the end");
 };
+constexpr int kBwdCtasPerSm = 2;
 
 template <typename T, int W>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, kBwdCtasPerSm)
 conv_bwd_kernel(ConvParams p) {
     using Lay = ConvBwdLayout<T, W>;
     constexpr int CB = Lay::CB, G = CB / kChannelsPerThread, RL = kConvThreads / G;
+    constexpr int NG = kConvThreads / CB;                 // row groups of the dw, db sums
     extern __shared__ __align__(16) uint8_t smem[];
-    T *sx = reinterpret_cast<T *>(smem + Lay::oX);
-    T *sdy = reinterpret_cast<T *>(smem + Lay::oDY);
     float *sdp = reinterpret_cast<float *>(smem + Lay::oDP);
     if (status_blocks(p.status)) return;
-    if (conv_empty_sequence<T, W>(p, CB, true)) return;
-    int n, ic;
-    int64_t bos, eos;
-    if (!conv_row(p, blockIdx.x, n, ic, bos, eos)) return;
-    const int D = p.D, cb0 = blockIdx.y * CB;
-    const int64_t t0 = bos + (int64_t)ic * C;
-    const int L = (int)(eos - bos), P0 = (int)(t0 - bos);
-    const int len = L - P0 < C ? L - P0 : C;
-    const int nq = (L - P0 < len + W - 1) ? L - P0 : len + W - 1;   // positions with a pre-activation
-    conv_stage<T, W>(p, static_cast<const T *>(p.x), sx, CB, cb0, t0, ic, n, -(W - 1), nq);
-    conv_stage<T, W>(p, static_cast<const T *>(p.dy), sdy, CB, cb0, t0, ic, n, 0, nq);
-    conv_stage_wait();
-    __syncthreads();
+    const int D = p.D, cb = blockIdx.y, cb0 = cb * CB, part_idx = blockIdx.x;
+    const int64_t step = gridDim.x;
+    auto tx = [&](int b) { return reinterpret_cast<T *>(smem + b * Lay::kBuf); };
+    auto tdy = [&](int b) { return reinterpret_cast<T *>(smem + b * Lay::kBuf + Lay::kX); };
+    // the rows of chunk j with a pre-activation: positions [0, nq) of the chunk
+    auto stage = [&](int64_t j, int b) -> bool {
+        int n, ic;
+        int64_t bos, eos;
+        if (!conv_row(p, (int)j, n, ic, bos, eos)) return false;
+        const int64_t t0 = bos + (int64_t)ic * C;
+        const int L = (int)(eos - bos), P0 = (int)(t0 - bos);
+        const int len = L - P0 < C ? L - P0 : C;
+        const int nq = (L - P0 < len + W - 1) ? L - P0 : len + W - 1;
+        conv_stage<T, W>(p, static_cast<const T *>(p.x), tx(b), CB, cb0, t0, ic, n, -(W - 1), nq);
+        conv_stage<T, W>(p, static_cast<const T *>(p.dy), tdy(b), CB, cb0, t0, ic, n, 0, nq);
+        return true;
+    };
     const int g = threadIdx.x % G, rr = threadIdx.x / G, c0 = cb0 + g * kChannelsPerThread;
     // dpre rows hold a thread's 8 channels as two float4 in the two halves of the row, so the
     // 32-byte vectors of neighbouring lanes do not share banks (dp_col maps a channel)
@@ -279,114 +298,139 @@ conv_bwd_kernel(ConvParams p) {
         const float4 hi = *reinterpret_cast<const float4 *>(row + CB / 2 + g * 4);
         v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w; v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
     };
-    float w[W][kChannelsPerThread];
+    float w[W][kChannelsPerThread], b[kChannelsPerThread];
     if (c0 < D) {
 #pragma unroll
-        for (int e = 0; e < kChannelsPerThread; ++e)
+        for (int e = 0; e < kChannelsPerThread; ++e) {
 #pragma unroll
             for (int j = 0; j < W; ++j) w[j][e] = ld1(static_cast<const T *>(p.w) + (int64_t)(c0 + e) * W + j);
-        float b[kChannelsPerThread];
+            b[e] = p.bias ? ld1(static_cast<const T *>(p.bias) + c0 + e) : 0.f;
+        }
+    }
+    // dw, db partial sums of this CTA: thread (channel cw, row group grp), rows in item order
+    const int cw = threadIdx.x % CB, grp = threadIdx.x / CB;
+    float acc[W + 1];
 #pragma unroll
-        for (int e = 0; e < kChannelsPerThread; ++e) b[e] = p.bias ? ld1(static_cast<const T *>(p.bias) + c0 + e) : 0.f;
-        // dpre at chunk positions q < len + W - 1 (zero past the sequence)
-        for (int q = rr; q < len + W - 1; q += RL) {
-            float d[kChannelsPerThread];
-            if (q < nq) {
-                float a[kChannelsPerThread], gy[kChannelsPerThread];
+    for (int j = 0; j <= W; ++j) acc[j] = 0.f;
+
+    int64_t cur = part_idx;
+    bool ok_cur = conv_live(p, cur) && stage(cur, 0);
+    conv_stage_commit();
+    int buf = 0;
+    while (conv_live(p, cur)) {
+        const int64_t nxt = cur + step;
+        const bool ok_nxt = conv_live(p, nxt) && stage(nxt, buf ^ 1);
+        conv_stage_commit();
+        conv_stage_wait_prev();
+        __syncthreads();                                  // the current chunk's rows are in the tiles
+        if (ok_cur) {
+            const T *sx = tx(buf), *sdy = tdy(buf);
+            int n, ic;
+            int64_t bos, eos;
+            conv_row(p, (int)cur, n, ic, bos, eos);
+            const int64_t t0 = bos + (int64_t)ic * C;
+            const int L = (int)(eos - bos), P0 = (int)(t0 - bos);
+            const int len = L - P0 < C ? L - P0 : C;
+            const int nq = (L - P0 < len + W - 1) ? L - P0 : len + W - 1;   // positions with a pre-activation
+            if (c0 < D) {
+                // dpre at chunk positions q < len + W - 1 (zero past the sequence)
+                for (int q = rr; q < len + W - 1; q += RL) {
+                    float d[kChannelsPerThread];
+                    if (q < nq) {
+                        float a[kChannelsPerThread], gy[kChannelsPerThread];
 #pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e) a[e] = b[e];
+                        for (int e = 0; e < kChannelsPerThread; ++e) a[e] = b[e];
 #pragma unroll
-                for (int j = 0; j < W; ++j) {           // x tile row q + j holds xx(q - (W - 1) + j)
-                    float xv[kChannelsPerThread];
-                    load8(sx + (int64_t)(q + j) * CB + g * kChannelsPerThread, xv);
+                        for (int j = 0; j < W; ++j) {   // x tile row q + j holds xx(q - (W - 1) + j)
+                            float xv[kChannelsPerThread];
+                            load8(sx + (int64_t)(q + j) * CB + g * kChannelsPerThread, xv);
 #pragma unroll
-                    for (int e = 0; e < kChannelsPerThread; ++e) a[e] = fmaf(w[j][e], xv[e], a[e]);
+                            for (int e = 0; e < kChannelsPerThread; ++e) a[e] = fmaf(w[j][e], xv[e], a[e]);
+                        }
+                        load8(sdy + (int64_t)q * CB + g * kChannelsPerThread, gy);
+#pragma unroll
+                        for (int e = 0; e < kChannelsPerThread; ++e)
+                            d[e] = p.act == GCL_ACT_SILU ? gy[e] * silu_grad(a[e]) : gy[e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < kChannelsPerThread; ++e) d[e] = 0.f;
+                    }
+                    dp_store(q, d);
                 }
-                load8(sdy + (int64_t)q * CB + g * kChannelsPerThread, gy);
-#pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e)
-                    d[e] = p.act == GCL_ACT_SILU ? gy[e] * silu_grad(a[e]) : gy[e];
-            } else {
-#pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e) d[e] = 0.f;
             }
-            dp_store(q, d);
-        }
-    }
-    __syncthreads();
-    if (c0 < D) {                                         // dx rows of the chunk
-        for (int pr = rr; pr < len; pr += RL) {
-            float gx[kChannelsPerThread];
+            __syncthreads();
+            if (c0 < D) {                                 // dx rows of the chunk
+                for (int pr = rr; pr < len; pr += RL) {
+                    float gx[kChannelsPerThread];
 #pragma unroll
-            for (int e = 0; e < kChannelsPerThread; ++e) gx[e] = 0.f;
+                    for (int e = 0; e < kChannelsPerThread; ++e) gx[e] = 0.f;
 #pragma unroll
-            for (int j = 0; j < W; ++j) {               // dpre at position pr + W - 1 - j
-                float dv[kChannelsPerThread];
-                dp_load(pr + W - 1 - j, dv);
+                    for (int j = 0; j < W; ++j) {       // dpre at position pr + W - 1 - j
+                        float dv[kChannelsPerThread];
+                        dp_load(pr + W - 1 - j, dv);
 #pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e) gx[e] = fmaf(dv[e], w[j][e], gx[e]);
+                        for (int e = 0; e < kChannelsPerThread; ++e) gx[e] = fmaf(dv[e], w[j][e], gx[e]);
+                    }
+                    const int kf = P0 + pr - (L - (W - 1));   // slot of the final state it lands in
+                    if (p.dht && kf >= 0) {
+#pragma unroll
+                        for (int e = 0; e < kChannelsPerThread; ++e)
+                            gx[e] += p.dht[((int64_t)n * D + c0 + e) * (W - 1) + kf];
+                    }
+                    store8(p.dx + (t0 + pr) * D + c0, gx);
+                }
             }
-            const int kf = P0 + pr - (L - (W - 1));       // slot of the final state it lands in
-            if (p.dht && kf >= 0) {
+            if (ic == 0 && p.dh0) {                       // the initial state: positions -(W - 1) .. -1
+                for (int e = threadIdx.x; e < CB * (W - 1); e += kConvThreads) {
+                    const int c = e / (W - 1), k = e % (W - 1), pos = k - (W - 1);
+                    if (cb0 + c >= D) continue;
+                    float a = 0.f;
 #pragma unroll
-                for (int e = 0; e < kChannelsPerThread; ++e)
-                    gx[e] += p.dht[((int64_t)n * D + c0 + e) * (W - 1) + kf];
+                    for (int j = 0; j < W; ++j) {
+                        const int q = pos + W - 1 - j;
+                        if (q >= 0 && q < len + W - 1)
+                            a = fmaf(sdp[(int64_t)q * CB + dp_col(c, CB)],
+                                     ld1(static_cast<const T *>(p.w) + (int64_t)(cb0 + c) * W + j), a);
+                    }
+                    const int kf = pos - (L - (W - 1));
+                    if (p.dht && kf >= 0) a += p.dht[((int64_t)n * D + cb0 + c) * (W - 1) + kf];
+                    p.dh0[((int64_t)n * D + cb0 + c) * (W - 1) + k] = a;
+                }
             }
-            store8(p.dx + (t0 + pr) * D + c0, gx);
-        }
-    }
-    if (ic == 0 && p.dh0) {                               // the initial state: positions -(W - 1) .. -1
-        for (int e = threadIdx.x; e < CB * (W - 1); e += kConvThreads) {
-            const int c = e / (W - 1), k = e % (W - 1), pos = k - (W - 1);
-            if (cb0 + c >= D) continue;
-            float a = 0.f;
+            if (cb0 + cw < D) {                           // dw, db of this chunk's tokens
+                for (int pr = grp; pr < len; pr += NG) {
+                    const float dv = sdp[(int64_t)pr * CB + dp_col(cw, CB)];
 #pragma unroll
-            for (int j = 0; j < W; ++j) {
-                const int q = pos + W - 1 - j;
-                if (q >= 0 && q < len + W - 1)
-                    a = fmaf(sdp[(int64_t)q * CB + dp_col(c, CB)],
-                             ld1(static_cast<const T *>(p.w) + (int64_t)(cb0 + c) * W + j), a);
-            }
-            const int kf = pos - (L - (W - 1));
-            if (p.dht && kf >= 0) a += p.dht[((int64_t)n * D + cb0 + c) * (W - 1) + kf];
-            p.dh0[((int64_t)n * D + cb0 + c) * (W - 1) + k] = a;
-        }
-    }
-    // dw, db of this chunk's tokens: NG row groups per channel, then added in group order
-    constexpr int NG = kConvThreads / CB;
-    float *red = reinterpret_cast<float *>(sdy);          // dy is consumed
-    __syncthreads();
-    {
-        const int c = threadIdx.x % CB, grp = threadIdx.x / CB;
-        float acc[W + 1];
-#pragma unroll
-        for (int j = 0; j <= W; ++j) acc[j] = 0.f;
-        if (cb0 + c < D) {
-            for (int pr = grp; pr < len; pr += NG) {
-                const float dv = sdp[(int64_t)pr * CB + dp_col(c, CB)];
-#pragma unroll
-                for (int j = 0; j < W; ++j) acc[j] = fmaf(dv, ld1(sx + (int64_t)(pr + j) * CB + c), acc[j]);
-                acc[W] += dv;
+                    for (int j = 0; j < W; ++j) acc[j] = fmaf(dv, ld1(sx + (int64_t)(pr + j) * CB + cw), acc[j]);
+                    acc[W] += dv;
+                }
             }
         }
-#pragma unroll
-        for (int j = 0; j <= W; ++j) red[((int64_t)grp * (W + 1) + j) * CB + c] = acc[j];
+        __syncthreads();                                  // dpre and the tiles are rewritten next
+        cur = nxt;
+        ok_cur = ok_nxt;
+        buf ^= 1;
     }
+    conv_stage_wait();
+    // this CTA's partial sums: the NG row groups added in group order
+    float *red = sdp;
+#pragma unroll
+    for (int j = 0; j <= W; ++j) red[((int64_t)grp * (W + 1) + j) * CB + cw] = acc[j];
     __syncthreads();
     if (threadIdx.x < CB && cb0 + (int)threadIdx.x < D) {
-        const int c = threadIdx.x;
-        float *part = p.partial + (int64_t)blockIdx.x * (W + 1) * D + cb0 + c;
+        float *part = p.partial + (int64_t)part_idx * (W + 1) * D + cb0 + threadIdx.x;
 #pragma unroll
         for (int j = 0; j <= W; ++j) {
             float a = 0.f;
-            for (int grp = 0; grp < NG; ++grp) a += red[((int64_t)grp * (W + 1) + j) * CB + c];
+            for (int gg = 0; gg < NG; ++gg) a += red[((int64_t)gg * (W + 1) + j) * CB + threadIdx.x];
             part[(int64_t)j * D] = a;
         }
     }
+    for (int64_t e = part_idx; e < p.n_max; e += step) conv_empty_sequence<T, W>(p, (int)e, cb, CB, true);
 }
-// dw[c][j] and db[c]: the chunk rows' partial sums, 32 channels per CTA (one per lane, so every
-// load of a warp is one 128-byte line); warp w takes rows w, w + 16, ..., and the 16 warp sums
-// are added in warp order (sentinel rows end the live rows).
+// dw[c][j] and db[c]: the backward CTAs' partial sums, 32 channels per CTA (one per lane, so
+// every load of a warp is one 128-byte line); warp w takes partials w, w + 16, ..., and the 16
+// warp sums are added in warp order.
 constexpr int kReduceWarps = 16;
 
 template <int W>
@@ -400,8 +444,7 @@ conv_reduce_kernel(ConvParams p) {
 #pragma unroll
     for (int j = 0; j <= W; ++j) acc[j] = 0.f;
     if (c < p.D) {
-        for (int64_t row = warp; row < p.nt_max; row += kReduceWarps) {
-            if (p.chunk_indices[2 * row] < 0) break;      // live rows come first
+        for (int64_t row = warp; row < p.n_part; row += kReduceWarps) {
             const float *part = p.partial + row * (W + 1) * p.D + c;
 #pragma unroll
             for (int j = 0; j <= W; ++j) acc[j] += part[(int64_t)j * p.D];
@@ -418,8 +461,17 @@ conv_reduce_kernel(ConvParams p) {
     }
 }
 
+// Backward CTAs per block of channels: one wave of kBwdCtasPerSm per SM, at most one per chunk
+// row (the partial-sum buffer holds nt_max rows).
+int conv_bwd_parts(int64_t nt_max, int ncb) {
+    const int64_t parts = (int64_t)kBwdCtasPerSm * num_sms() / ncb;
+    return (int)(parts < 1 ? 1 : parts > nt_max ? nt_max : parts);
+}
+
 template <typename T, int W>
-cudaError_t launch_conv(const ConvParams &p, bool backward, cudaStream_t s) {
+cudaError_t launch_conv(const ConvParams &p0, bool backward, cudaStream_t s) {
+    ConvParams p = p0;
+    cudaError_t e;
     if (!backward) {
         constexpr int CB = kFwdChannels * 2 / (int)sizeof(T);
         const dim3 grid((unsigned)(p.nt_max + p.n_max), (unsigned)((p.D + CB - 1) / CB));
@@ -428,10 +480,11 @@ cudaError_t launch_conv(const ConvParams &p, bool backward, cudaStream_t s) {
     }
     using Lay = ConvBwdLayout<T, W>;
     auto kern = conv_bwd_kernel<T, W>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::bytes);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(p.nt_max + p.n_max), (unsigned)((p.D + Lay::CB - 1) / Lay::CB));
-    kern<<<grid, kConvThreads, Lay::bytes, s>>>(p);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::bytes)) != cudaSuccess)
+        return e;
+    const int ncb = (p.D + Lay::CB - 1) / Lay::CB;
+    p.n_part = conv_bwd_parts(p.nt_max, ncb);
+    kern<<<dim3((unsigned)p.n_part, (unsigned)ncb), kConvThreads, Lay::bytes, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     conv_reduce_kernel<W><<<(p.D + 31) / 32, kReduceWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
