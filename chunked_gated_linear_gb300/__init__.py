@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH):
     lib.gcl_nt_max.argtypes = [i64, i64, i32]
     lib.gcl_fwd_chain_segments.restype = i32
     lib.gcl_fwd_chain_segments.argtypes = [i64, i32, i32, i32]
+    lib.gcl_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gcl_selftest_wait_timeout.argtypes = [vp, vp]
     lib.chunk_meta_build.restype = ctypes.c_int
     lib.chunk_meta_build.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp]
     lib.chunk_meta_build_i64.restype = ctypes.c_int
@@ -153,6 +155,12 @@ def _dtype_of(t):
 
 def nt_max(t_max: int, n_max: int, bt: int = CHUNK) -> int:
     return int(lib().gcl_nt_max(t_max, n_max, bt))
+
+
+def selftest_wait_timeout(dev_status, stream=None):
+    """One CTA waits on an mbarrier nothing arrives at; after the time limit dev_status holds
+    GCL_DEV_WAIT_TIMEOUT (the bounded-wait path of every tensor-core kernel)."""
+    _check("gcl_selftest_wait_timeout", lib().gcl_selftest_wait_timeout(_p(dev_status), _stream(stream)))
 
 
 def fwd_chain_segments(t_max: int, n_max: int, H: int, bt: int = CHUNK) -> int:

@@ -268,6 +268,17 @@ gcl_status_t gdn_chunk_fwd_noalloc(const gcl_fwd_args *args, gcl_stream_t stream
 size_t gcl_noalloc_scratch_bytes(void);
 
 /*
+ * gcl_selftest_wait_timeout -- a self-test of the bounded waits.  Every mbarrier
+ * wait of the tensor-core kernels gives up after a time limit (0.2 s), records
+ * GCL_DEV_WAIT_TIMEOUT in the device status word and returns, so that a lost copy
+ * or MMA completion becomes a status the host can read rather than a hung GPU.  This
+ * call launches one CTA that waits on an mbarrier nothing arrives at: after the
+ * limit *dev_status holds GCL_DEV_WAIT_TIMEOUT (if it was 0) and the context stays
+ * usable.  No fault, trap or hang.  Host error: INVALID_ARG for a NULL dev_status.
+ */
+gcl_status_t gcl_selftest_wait_timeout(int32_t *dev_status, gcl_stream_t stream);
+
+/*
  * Backward arguments (GDN and KDA).  All pointers are device pointers.
  */
 typedef struct gcl_bwd_args {
