@@ -216,7 +216,7 @@ class Runner:
             args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], t["cu"], t["idx"],
                     t["off"], t["dq"], t["dk"], t["dv"], t["dg"], t["dbeta"])
             kw = dict(h0=t.get("h0"), dht=t.get("dht"), dh0=t["dh0"], h_save=t["hs"],
-                      dev_status=t["status"], scale=w.scale, bt=w.bt)
+                      dev_status=t["status"], scale=w.scale, bt=w.bt, fwd_workspace=t["fws"])
             nb = (gcl.kda_bwd_workspace_bytes if w.variant == synth.KDA else gcl.bwd_workspace_bytes)(*args, **kw)
             t["ws"] = torch.empty(nb, dtype=torch.uint8, device=dev)
             self.bwd_args = gcl.bwd_args(*args, workspace=t["ws"], **kw)
@@ -261,7 +261,7 @@ def launches_per_step(w) -> int:
     """Library kernels per step: chunk_meta_build, the forward (prep and chain on the tensor
     cores for GDN and KDA bf16 d_k = d_v = 128 -- prep, segment summaries, scan and segment
     outputs when the chain is segmented -- one fused CUDA-core kernel otherwise) and
-    the backward (GDN on the tensor cores: transition records, state-gradient sweep and two
+    the backward (GDN on the tensor cores: state-gradient sweep from the forward's records and two
     chunk-gradient kernels; otherwise the sweep and one chunk-gradient kernel)."""
     tc = w.dtype == "bf16" and w.K == 128 and w.V == 128 and w.bt == 64
     tc_bwd = tc and w.variant == synth.GDN
@@ -269,7 +269,9 @@ def launches_per_step(w) -> int:
     import chunked_gated_linear_gb300 as gcl
     seg = tc and gcl.fwd_chain_segments(w.t_max, w.n_max, w.H, w.bt) > 0
     fwd = (4 if seg else 2) if tc else 1
-    return 1 + fwd + ((4 if tc_bwd else 2) if w.backward else 0)
+    # backward with the forward's saved states and chunk records: the state-gradient sweep and
+    # the chunk gradients (two kernels on the tensor cores for GDN, one otherwise)
+    return 1 + fwd + ((3 if tc_bwd else 2) if w.backward else 0)
 
 
 def graph_and_warm_timing(torch, w, sets, stream, step, step_ms, reps):

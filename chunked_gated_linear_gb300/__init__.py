@@ -52,7 +52,8 @@ class BwdArgs(ctypes.Structure):
                 ("dev_status", ctypes.c_void_p), ("t_max", ctypes.c_int64),
                 ("n_max", ctypes.c_int32), ("H", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("V", ctypes.c_int32), ("bt", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("fwd_workspace", ctypes.c_void_p),
+                ("fwd_workspace_bytes", ctypes.c_size_t)]
 
 
 class ConvArgs(ctypes.Structure):
@@ -248,7 +249,7 @@ def kda_chunk_fwd(*args, stream=None, **kw):
 
 def bwd_args(q, k, v, g, beta, d_o, cu_seqlens, chunk_indices, chunk_offsets, dq, dk, dv, dg,
              dbeta, h0=None, dht=None, dh0=None, h_save=None, workspace=None,
-             dev_status=None, scale=None, bt=CHUNK):
+             dev_status=None, scale=None, bt=CHUNK, fwd_workspace=None):
     T, H, K = q.shape
     V = v.shape[-1]
     return BwdArgs(q=_p(q), k=_p(k), v=_p(v), g=_p(g), beta=_p(beta), h0=_p(h0), d_o=_p(d_o),
@@ -258,7 +259,8 @@ def bwd_args(q, k, v, g, beta, d_o, cu_seqlens, chunk_indices, chunk_offsets, dq
                    workspace=_p(workspace), workspace_bytes=_nbytes(workspace),
                    dev_status=_p(dev_status), t_max=T, n_max=cu_seqlens.shape[0] - 1, H=H, K=K,
                    V=V, bt=bt, scale=float(K ** -0.5 if scale is None else scale),
-                   dtype=_dtype_of(q))
+                   dtype=_dtype_of(q), fwd_workspace=_p(fwd_workspace),
+                   fwd_workspace_bytes=_nbytes(fwd_workspace))
 
 
 def bwd_workspace_bytes(*args, **kw) -> int:

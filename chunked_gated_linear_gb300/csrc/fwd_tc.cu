@@ -709,14 +709,22 @@ int fwd_tc_split(int n_max, int H) {
 
 bool fwd_tc_prefers_transition(int n_max, int H) { return fwd_tc_split(n_max, H) >= 4; }
 
+// The transition plan runs for few units (split 4 or 8: a shorter serial step) and for every
+// training forward (h_save: its records are what the backward's sweep reads, so the backward
+// can take them instead of recomputing them), whenever the workspace holds the records.  KDA
+// has the transition plan only.
+bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max) {
+    if (variant == kKDA) return true;
+    return (fwd_tc_prefers_transition(n_max, H) || h_save) && ws_bytes >= fwd_tc_t_workspace_bytes(nt_max, H);
+}
+
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     const int H = p.H;
     if (variant == kKDA) {   // KDA has the transition form only
         if (p.workspace_bytes < fwd_tc_t_workspace_bytes(p.nt_max, H)) return cudaErrorInvalidValue;
         return launch_fwd_tc_kda(p, fwd_tc_split(p.n_max, H), s);
     }
-    if (fwd_tc_prefers_transition(p.n_max, H) &&
-        p.workspace_bytes >= fwd_tc_t_workspace_bytes(p.nt_max, H))
+    if (fwd_tc_runs_transition(variant, p.n_max, H, p.h_save != nullptr, p.workspace_bytes, p.nt_max))
         return launch_fwd_tc_t(p, fwd_tc_split(p.n_max, H), s);
     const int64_t units = p.nt_max * H;              // chunk-head slots of the workspace
     __nv_bfloat16 *tl = static_cast<__nv_bfloat16 *>(p.workspace);

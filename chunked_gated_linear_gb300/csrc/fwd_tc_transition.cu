@@ -1100,7 +1100,8 @@ cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int spli
     }
     if (split == 8) return launch_chain_t<16, 3, false>(myn, ws, cp, split, H, p.n_max, s);
     if (split == 4) return launch_chain_t<32, 2, false>(myn, ws, cp, split, H, p.n_max, s);
-    return cudaErrorInvalidValue;                   // GDN takes this plan only at splits 4 and 8
+    if (split == 2) return launch_chain_t<64, 2, false>(myn, ws, cp, split, H, p.n_max, s);
+    return cudaErrorInvalidValue;
 }
 
 void fwd_seg_plan(const FwdParams &p, uint8_t *ws, int *n_seg, float **seg_ws) {

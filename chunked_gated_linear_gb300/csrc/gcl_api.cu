@@ -84,7 +84,7 @@ static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
     // the transition form, with the segment buffers when the fastest plan is segmented
     const size_t seg = fastest ? fwd_seg_workspace_bytes(ntm, a->n_max, a->H) : 0;
     if (variant == kKDA) return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
-    if (fastest && fwd_tc_prefers_transition(a->n_max, a->H))
+    if (fastest && (fwd_tc_prefers_transition(a->n_max, a->H) || a->h_save))
         return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
     return fwd_tc_workspace_bytes(ntm, a->H) + kWsAlign;
 }
@@ -139,21 +139,34 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // the recomputed states (same shape) and the forward's own workspace; on the tensor-core
 // path also the transition-form records the state-gradient sweep reads.
 // KDA runs the backward on the CUDA cores (its recompute forward may use the tensor cores).
+// The forward's records, when the caller hands over the workspace of a forward that ran the
+// transition plan (decided from the sizes alone, as the forward decided), else NULL.
+static const uint8_t *fwd_records(const gcl_bwd_args *a, int variant, int64_t ntm) {
+    if (!a->h_save || !a->fwd_workspace || !fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt))
+        return nullptr;
+    void *w = nullptr;
+    size_t wb = 0;
+    align_ws(const_cast<void *>(a->fwd_workspace), a->fwd_workspace_bytes, &w, &wb);
+    if (!fwd_tc_runs_transition(variant, a->n_max, a->H, true, wb, ntm)) return nullptr;
+    return static_cast<const uint8_t *>(w);
+}
+
 static size_t bwd_ws(const gcl_bwd_args *a, int variant) {
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
     const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
     const bool tc = variant == kGDN && tc_fwd;
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
-    // tensor-core sweep (GDN and KDA bf16 K = V = 128): transition records; GDN's tensor-core
-    // chunk gradients also a scratch record per chunk and head
+    // tensor-core sweep (GDN and KDA bf16 K = V = 128): transition records (unless the
+    // forward's, or the state recompute's, are reused); GDN's tensor-core chunk gradients also
+    // a scratch record per chunk and head
+    const bool own_records = tc_fwd && a->h_save && !fwd_records(a, variant, ntm);
     const size_t rec = !tc_fwd ? 0
-                       : align256(transition_record_bytes(ntm, a->H)) + kWsAlign +
+                       : (own_records ? align256(transition_record_bytes(ntm, a->H)) : 0) + kWsAlign +
                              (tc ? align256(bwd_grad_tc_scratch_bytes(ntm, a->H)) : 0);
     if (a->h_save) return per + rec;
-    const size_t fw = !tc_fwd ? 0
-                      : align256(variant == kKDA ? fwd_tc_t_workspace_bytes(ntm, a->H)
-                                                 : fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign;
+    // the state recompute runs the transition plan, whose records the sweep then reads
+    const size_t fw = !tc_fwd ? 0 : align256(fwd_tc_t_workspace_bytes(ntm, a->H)) + kWsAlign;
     return 2 * per + fw + rec;
 }
 
@@ -204,10 +217,9 @@ static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int vari
     f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V; f.bt = a->bt;
     f.nt_max = ntm;
     f.scale = a->scale;
-    const size_t fw = !tc_fwd ? 0
-                      : align256(variant == kKDA ? fwd_tc_t_workspace_bytes(ntm, a->H)
-                                                 : fwd_tc_workspace_bytes(ntm, a->H)) + kWsAlign;
+    const size_t fw = !tc_fwd ? 0 : align256(fwd_tc_t_workspace_bytes(ntm, a->H)) + kWsAlign;
     const size_t used = a->h_save ? per : 2 * per + fw;
+    const uint8_t *records = fwd_records(a, variant, ntm);    // the training forward's
     if (a->h_save) {
         p.h = a->h_save;
     } else {
@@ -215,12 +227,13 @@ static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int vari
         f.h_save = h;
         f.workspace = nullptr;
         f.workspace_bytes = 0;
-        if (tc_fwd)     // GDN: room for the W form only; KDA: its transition form
+        if (tc_fwd)     // the transition plan: its records serve the sweep below
             align_ws(ws + 2 * per, fw - 1, &f.workspace, &f.workspace_bytes);
         cudaError_t e = tc_fwd ? launch_fwd_tc(f, variant, s) : launch_fwd_simt(f, variant, a->dtype, s);
         if ((st = cuda_check(e, variant == kKDA ? "kda_chunk_bwd (state recompute)"
                                                 : "gdn_chunk_bwd (state recompute)")) != GCL_OK)
             return st;
+        if (tc_fwd) records = static_cast<const uint8_t *>(f.workspace);
         f.h_save = nullptr;
         p.h = h;
     }
@@ -228,18 +241,22 @@ static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int vari
         void *rec = nullptr;
         size_t rec_bytes = 0;
         align_ws(ws + used, a->workspace_bytes - used, &rec, &rec_bytes);
-        if (rec_bytes < align256(transition_record_bytes(ntm, a->H)) + (tc ? bwd_grad_tc_scratch_bytes(ntm, a->H) : 0))
+        const size_t own = records ? 0 : align256(transition_record_bytes(ntm, a->H));
+        if (rec_bytes < own + (tc ? bwd_grad_tc_scratch_bytes(ntm, a->H) : 0))
             return fail(GCL_ERR_CAPACITY, "%s: workspace too small for the sweep records", fn);
-        cudaError_t e = variant == kKDA ? launch_prep_kda(f, static_cast<uint8_t *>(rec), s)
-                                        : launch_prep_t(f, static_cast<uint8_t *>(rec), s);
-        if (e == cudaSuccess) e = launch_bwd_sweep_t(p, static_cast<const uint8_t *>(rec), variant == kKDA, s);
+        cudaError_t e = cudaSuccess;
+        if (!records) {
+            e = variant == kKDA ? launch_prep_kda(f, static_cast<uint8_t *>(rec), s)
+                                : launch_prep_t(f, static_cast<uint8_t *>(rec), s);
+            records = static_cast<const uint8_t *>(rec);
+        }
+        if (e == cudaSuccess) e = launch_bwd_sweep_t(p, records, variant == kKDA, s);
         if ((st = cuda_check(e, variant == kKDA ? "kda_chunk_bwd (state-gradient sweep)"
                                                 : "gdn_chunk_bwd (state-gradient sweep)")) != GCL_OK)
             return st;
         if (variant == kKDA) return cuda_check(launch_bwd_simt_kda(p, a->dtype, true, s), fn);
-        // chunk gradients on the tensor cores; their scratch follows the records
-        float *scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(rec) +
-                                                   align256(transition_record_bytes(ntm, a->H)));
+        // chunk gradients on the tensor cores; their scratch follows the records (if any)
+        float *scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(rec) + own);
         return cuda_check(launch_bwd_grad_tc(p, scratch, s), fn);
     }
     if (variant == kKDA) return cuda_check(launch_bwd_simt_kda(p, a->dtype, false, s), fn);

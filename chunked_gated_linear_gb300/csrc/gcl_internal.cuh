@@ -84,6 +84,7 @@ int fwd_seg_count(int64_t nt_max, int n_max, int H);
 size_t fwd_seg_workspace_bytes(int64_t nt_max, int n_max, int H);
 int fwd_tc_split(int n_max, int H);                        // value-column slices per head
 bool fwd_tc_prefers_transition(int n_max, int H);
+bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max);
 
 // Encodes a TMA tensor map (cuTensorMapEncodeTiled, looked up once through the runtime).
 bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,

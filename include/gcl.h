@@ -305,11 +305,25 @@ typedef struct gcl_bwd_args {
     int32_t n_max, H, K, V, bt;
     float scale;
     int32_t dtype;
+    const void *fwd_workspace;     /* the workspace of the forward call that wrote h_save,   */
+    size_t fwd_workspace_bytes;    /* or NULL: its chunk records are then reused (below)     */
 } gcl_bwd_args;
 
 /* Bytes of device workspace gdn_chunk_bwd (gcl_bwd_workspace_bytes) and
  * kda_chunk_bwd (gcl_kda_bwd_workspace_bytes) need for these sizes (depends on
- * whether h_save is NULL).  Returns 0 for unsupported sizes. */
+ * whether h_save and fwd_workspace are NULL).  Returns 0 for unsupported sizes.
+ *
+ * Chunk records.  On the tensor cores (bf16, K = V = 128, bt = 64) the reverse
+ * state-gradient sweep reads each chunk's transition-form records (the affine state
+ * map N, B of the chunk; see gdn_chunk_fwd).  A forward that writes h_save (a
+ * training forward) runs the transition plan whenever its workspace holds it, so
+ * its workspace then holds exactly these records: pass that workspace and its size as
+ * fwd_workspace / fwd_workspace_bytes, with the same inputs and h_save, and the
+ * backward reads them instead of recomputing them (the caller guarantees that the
+ * forward ran on these inputs, as for h_save).  The backward decides from the sizes
+ * alone whether that forward ran the transition plan and ignores fwd_workspace
+ * otherwise.  Without h_save the backward's own recompute of the states runs the
+ * transition plan and reuses its records. */
 size_t gcl_bwd_workspace_bytes(const gcl_bwd_args *args);
 size_t gcl_kda_bwd_workspace_bytes(const gcl_bwd_args *args);
 

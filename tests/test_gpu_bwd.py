@@ -8,12 +8,12 @@ torch = pytest.importorskip("torch")
 import oracle  # noqa: E402
 import chunked_gated_linear_gb300 as gcl  # noqa: E402
 from chunked_gated_linear_gb300 import synth  # noqa: E402
-from gpu_util import DEV, TOL, Meta, relF, run_fwd, to_device  # noqa: E402
+from gpu_util import DEV, TOL, Meta, check_fwd, relF, run_fwd, to_device  # noqa: E402
 
 GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 
 
-def run_bwd(w, d, meta, h_save=None, with_dht=True):
+def run_bwd(w, d, meta, h_save=None, with_dht=True, fwd_ws=None):
     T, H, K, V = w.t_max, w.H, w.K, w.V
     f32 = dict(dtype=torch.float32, device=DEV)
     kda = w.variant == synth.KDA
@@ -24,7 +24,7 @@ def run_bwd(w, d, meta, h_save=None, with_dht=True):
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["do"], d["cu_seqlens"], meta.idx,
             meta.off, out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"])
     kw = dict(h0=d.get("h0"), dht=d["dht"] if with_dht else None, dh0=out["dh0"],
-              h_save=h_save, dev_status=meta.status, scale=w.scale, bt=w.bt)
+              h_save=h_save, dev_status=meta.status, scale=w.scale, bt=w.bt, fwd_workspace=fwd_ws)
     nbytes = (gcl.kda_bwd_workspace_bytes if kda else gcl.bwd_workspace_bytes)(*args, **kw)
     ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)      # stale contents
     (gcl.kda_chunk_bwd if kda else gcl.gdn_chunk_bwd)(*args, workspace=ws, **kw)
@@ -125,3 +125,24 @@ def test_kda_no_dht_no_h0_strong_gates():
     meta.build(d["cu_seqlens"])
     got = run_bwd(w, d, meta, with_dht=False)
     compare(w, got, oracle_bwd(w, x, with_dht=False), TOL["bf16"])
+
+
+@pytest.mark.parametrize("variant", [synth.GDN, synth.KDA], ids=["gdn", "kda"])
+@pytest.mark.parametrize("H", [2, 8], ids=["few-units", "many-units"])
+def test_backward_reuses_forward_records(variant, H):
+    """A training forward (h_save) runs the transition plan; handing its workspace to the
+    backward skips the recompute of the chunk records: gradients bitwise equal to the backward
+    that recomputes them, and within the bar of the oracle.  H = 8 over 8 sequence slots gives
+    64 units (two value slices per head), H = 2 gives 16 (eight slices)."""
+    lens = [1, 63, 0, 64, 65, 200, 130, 77]
+    w = synth.varlen("reuse", variant, "bf16", lens, 8, sum(lens) + 40, H, 128, 128,
+                     backward=True, seed=81)
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    fw = run_fwd(w, d, h_save=True)
+    check_fwd(w, x, fw, label="training forward")
+    a = run_bwd(w, d, fw["meta"], h_save=fw["h_save"], fwd_ws=fw["ws"])
+    b = run_bwd(w, d, fw["meta"], h_save=fw["h_save"])
+    for key in GRADS:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    compare(w, a, oracle_bwd(w, x), TOL["bf16"])
