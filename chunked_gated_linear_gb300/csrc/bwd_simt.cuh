@@ -562,17 +562,24 @@ chunk_grad_kda_kernel(BwdParams p) {
             for (int j = 0; j < kVS; ++j) a = fmaf(sS[c * LV + j], sDS[c * LV + j], a);
             sSS[c] = a;
         }
-        // KS = Kp S, R = diag(beta)(V - KS), X2 = Kb dS'
-        for (int e = tid; e < C * kVS; e += kGradThreads) {
-            const int r = e / kVS, j = e % kVS;
-            float ks = 0.f, kd = 0.f;
+        // KS = Kp S, R = diag(beta)(V - KS), X2 = Kb dS': rows r and r + C/2 per thread, so
+        // each S and dS' value read serves two rows
+        for (int e = tid; e < (C / 2) * kVS; e += kGradThreads) {
+            const int r = e / kVS, j = e % kVS, r2 = r + C / 2;
+            float ks0 = 0.f, kd0 = 0.f, ks1 = 0.f, kd1 = 0.f;
             for (int c = 0; c < K; ++c) {
-                ks = fmaf(sKp[r * LK + c], sS[c * LV + j], ks);
-                kd = fmaf(sKb[r * LK + c], sDS[c * LV + j], kd);
+                const float sv = sS[c * LV + j], dv = sDS[c * LV + j];
+                ks0 = fmaf(sKp[r * LK + c], sv, ks0);
+                kd0 = fmaf(sKb[r * LK + c], dv, kd0);
+                ks1 = fmaf(sKp[r2 * LK + c], sv, ks1);
+                kd1 = fmaf(sKb[r2 * LK + c], dv, kd1);
             }
-            sKS[r * LV + j] = ks;
-            sR[r * LV + j] = sB[r] * (sV[r * LV + j] - ks);
-            sX2[r * LV + j] = kd;
+            sKS[r * LV + j] = ks0;
+            sR[r * LV + j] = sB[r] * (sV[r * LV + j] - ks0);
+            sX2[r * LV + j] = kd0;
+            sKS[r2 * LV + j] = ks1;
+            sR[r2 * LV + j] = sB[r2] * (sV[r2 * LV + j] - ks1);
+            sX2[r2 * LV + j] = kd1;
         }
         __syncthreads();
         // E = T R;  dE = L^T dO + X2
@@ -607,17 +614,18 @@ chunk_grad_kda_kernel(BwdParams p) {
             }
         }
         __syncthreads();
-        // (row, channel) partials: Y1 += dR S^T, Y2 += dO S^T, Y3 += E dS'^T
+        // (row, channel) partials: Y1 += dR S^T, Y2 += dO S^T, Y3 += E dS'^T (the row's three
+        // values read once per column j; each accumulator still adds j in order)
+        for (int j = 0; j < kVS; ++j) {
+            const float dr = sDR[my_r * LV + j], dov = sDO[my_r * LV + j], ev = sE[my_r * LV + j];
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const int c = my_c0 + TPR * m;
-            float a1 = y1[m], a2 = y2[m], a3 = y3[m];
-            for (int j = 0; j < kVS; ++j) {
-                a1 = fmaf(sDR[my_r * LV + j], sS[c * LV + j], a1);
-                a2 = fmaf(sDO[my_r * LV + j], sS[c * LV + j], a2);
-                a3 = fmaf(sE[my_r * LV + j], sDS[c * LV + j], a3);
+            for (int m = 0; m < CPT; ++m) {
+                const int c = my_c0 + TPR * m;
+                const float sv = sS[c * LV + j];
+                y1[m] = fmaf(dr, sv, y1[m]);
+                y2[m] = fmaf(dov, sv, y2[m]);
+                y3[m] = fmaf(ev, sDS[c * LV + j], y3[m]);
             }
-            y1[m] = a1; y2[m] = a2; y3[m] = a3;
         }
         // row sums for dbeta (one thread per row, fixed order)
         for (int r = tid; r < C; r += kGradThreads) {
