@@ -91,3 +91,32 @@ def test_host_errors_before_any_launch(lib):
 def test_status_strings(lib):
     assert lib.gcl_status_string(0) == b"GCL_OK"
     assert lib.gcl_status_string(3) == b"GCL_ERR_CAPACITY"
+
+
+def test_plan_rules_from_sizes_alone(lib):
+    """Host-side plan rules (no device access): a training forward (h_save) asks for the
+    transition records even with many units; handing its workspace to the backward shrinks
+    the backward's; one long sequence of one head is cut into segments, many units are not."""
+    import chunked_gated_linear_gb300 as gcl
+    fake = 1 << 20
+    base = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake,
+                t_max=8192 * 4, n_max=4, H=16, K=128, V=128, bt=64, scale=1.0, dtype=1)
+    infer = gcl.FwdArgs(**base)
+    train = gcl.FwdArgs(**base, h_save=fake, chunk_offsets=fake)
+    w_inf = lib.gcl_fwd_workspace_bytes(ctypes.byref(infer))
+    w_tr = lib.gcl_fwd_workspace_bytes(ctypes.byref(train))
+    assert w_tr > w_inf                                  # transition records (96.5 KiB per chunk-head)
+    assert w_inf == lib.gcl_fwd_workspace_min_bytes(ctypes.byref(infer))   # W form
+    b = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, d_o=fake, cu_seqlens=fake,
+             chunk_indices=fake, chunk_offsets=fake, dq=fake, dk=fake, dv=fake, dg=fake,
+             dbeta=fake, h_save=fake, t_max=8192 * 4, n_max=4, H=16, K=128, V=128, bt=64,
+             scale=1.0, dtype=1)
+    own = lib.gcl_bwd_workspace_bytes(ctypes.byref(gcl.BwdArgs(**b)))
+    reuse = lib.gcl_bwd_workspace_bytes(ctypes.byref(gcl.BwdArgs(**b, fwd_workspace=fake,
+                                                                 fwd_workspace_bytes=w_tr)))
+    small = lib.gcl_bwd_workspace_bytes(ctypes.byref(gcl.BwdArgs(**b, fwd_workspace=fake,
+                                                                 fwd_workspace_bytes=w_inf)))
+    assert reuse < own and small == own                  # a W-form forward has no records to give
+    assert lib.gcl_fwd_chain_segments(65536, 1, 1, 64) >= 3
+    assert lib.gcl_fwd_chain_segments(4096, 1, 16, 64) == 0
+    assert lib.gcl_fwd_chain_segments(65536, 1, 1, 32) == 0

@@ -393,3 +393,22 @@ def test_saved_chunk_states_equal_prefix_runs():
         _, htp = oracle.fwd(GDN, *(x[m][s:e] for m in ("q", "k", "v", "g", "beta")),
                             x["h0"][n:n + 1], [0, e - s], 0.5)
         np.testing.assert_allclose(hc[j], htp[0], rtol=1e-13, atol=1e-15)
+
+
+def test_chunk_states_at_bt32_are_every_other_bt64_state():
+    """The state before 64-token chunk i of a sequence is the state before 32-token chunk 2i:
+    both are the token recurrence's state after the same prefix."""
+    lens = [130, 0, 64, 5, 97]
+    w = synth.varlen("t", GDN, "f32", lens, 5, 300, 2, 8, 6)
+    x = synth.make_inputs(w, seed=98)
+    hc = {}
+    offs = {}
+    for bt in (32, 64):
+        st, idx, off = oracle.chunk_meta(x["cu_seqlens"], 300, bt)
+        _, _, hc[bt] = oracle.fwd(GDN, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                  x["cu_seqlens"], 0.5, bt=bt, chunk_offsets=off,
+                                  nt_rows=idx.shape[0])
+        offs[bt] = off
+    for n in range(len(lens)):
+        for i in range(int(offs[64][n + 1] - offs[64][n])):
+            np.testing.assert_array_equal(hc[32][offs[32][n] + 2 * i], hc[64][offs[64][n] + i])
