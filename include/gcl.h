@@ -174,9 +174,11 @@ typedef struct gcl_fwd_args {
  * the minimum.  The transition form keeps per chunk and head the chunk's affine
  * state map and output map (N, B, Y, Z below, bf16), 96 KiB; it shortens the serial
  * step per chunk and is the fastest plan when each head is split over 4 or more
- * value-column slices (few sequence-head units).  The forward runs the fastest plan
- * whose scratch fits in workspace_bytes, so any workspace of at least the minimum
- * works; a given size always selects the same plan. */
+ * value-column slices (few sequence-head units).  A forward that writes h_save
+ * (training) also takes the transition form, because its records are what the
+ * backward's state-gradient sweep reads (gcl_bwd_args.fwd_workspace).  The forward
+ * runs that plan whenever its scratch fits in workspace_bytes, else the W form, so any
+ * workspace of at least the minimum works; given sizes always select the same plan. */
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
 size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
 
