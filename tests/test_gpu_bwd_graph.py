@@ -1,7 +1,8 @@
 """Forward + backward under CUDA graph capture (the training path of the RFC's graph
 work): chunk_meta_build, the forward with saved chunk states and the backward are captured
 once on static buffers, then replayed for fresh inputs copied in place.  Each replay must
-equal an eager call on the same buffers bit for bit and the oracle within the bf16 bar."""
+equal an eager call on the same buffers bit for bit and the oracle within the bf16 bar; the
+backward either forms its own chunk records or reads the forward's (fwd_workspace)."""
 import numpy as np
 import pytest
 
@@ -17,7 +18,8 @@ GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 
 
 @pytest.mark.parametrize("variant", [synth.GDN, synth.KDA], ids=["gdn", "kda"])
-def test_fwd_bwd_capture_once_replay(variant):
+@pytest.mark.parametrize("reuse", [False, True], ids=["own-records", "forward-records"])
+def test_fwd_bwd_capture_once_replay(variant, reuse):
     lens = [300, 1, 0, 129]
     w = synth.varlen("graph-bwd", variant, "bf16", lens, 4, 512, 4, 128, 128, backward=True,
                      seed=31)
@@ -44,7 +46,7 @@ def test_fwd_bwd_capture_once_replay(variant):
              static["cu_seqlens"], meta.idx, meta.off, out["dq"], out["dk"], out["dv"],
              out["dg"], out["dbeta"])
     bkw = dict(h0=static["h0"], dht=static["dht"], dh0=out["dh0"], h_save=hs,
-               dev_status=meta.status, scale=w.scale)
+               dev_status=meta.status, scale=w.scale, fwd_workspace=fws if reuse else None)
     bws = torch.empty((gcl.kda_bwd_workspace_bytes if kda else gcl.bwd_workspace_bytes)(
         *bargs, **bkw), dtype=torch.uint8, device=DEV)
     fwd = gcl.kda_chunk_fwd if kda else gcl.gdn_chunk_fwd
