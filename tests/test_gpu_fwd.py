@@ -154,3 +154,46 @@ def test_kda_gate_extremes(regime):
         g[:, :, :32] = 0.0                          # and undecayed channels
     x["g"] = g.astype(np.float32)
     check_fwd(w, x, run_fwd(w, to_device(w, x)), label=f"kda gates {regime}")
+
+
+@pytest.mark.parametrize("plan", ["fastest", "min"], ids=["transition", "wform"])
+@pytest.mark.parametrize("regime", ["beta0", "nodecay", "strong", "mixed"])
+def test_gdn_degenerate_gates_and_beta(regime, plan):
+    """GDN on the tensor cores in the method's degenerate regimes: beta = 0 (no delta rule:
+    the state only decays, A = 0 and T = I), g = 0 (no decay), log gates 20x the generator's
+    (decay over a chunk far below fp32's range) and a mix of strong and zero gates."""
+    lens = [300, 77, 0, 130]
+    w = synth.varlen("gdn-gates", synth.GDN, "bf16", lens, 4, 540, 2, 128, 128, seed=25)
+    x = synth.make_inputs(w)
+    T = w.total_tokens
+    rng = np.random.default_rng(26)
+    if regime == "beta0":
+        x["beta"][:T] = 0.0
+    elif regime == "nodecay":
+        x["g"][:T] = 0.0
+    elif regime == "strong":
+        x["g"][:T] *= 20.0
+    else:
+        g = x["g"][:T]
+        g[rng.random(g.shape) < 0.2] *= 40.0
+        g[rng.random(g.shape) < 0.3] = 0.0
+        x["g"][:T] = g
+    check_fwd(w, x, run_fwd(w, to_device(w, x), plan=plan), label=f"gdn {regime} {plan}")
+
+
+def test_many_short_sequences():
+    """1,000 sequence slots of 0..100 tokens (a fifth of them empty), two heads: the longest-
+    first order over many slots, many zero-length sequences passing h0 through."""
+    rng = np.random.default_rng(27)
+    lens = [int(v) for v in rng.integers(0, 101, size=1000)]
+    for i in rng.choice(1000, size=200, replace=False):
+        lens[i] = 0
+    for variant in (synth.GDN, synth.KDA):
+        w = synth.varlen("many", variant, "bf16", lens, 1000, sum(lens) + 64, 2, 128, 128, seed=28)
+        x = synth.make_inputs(w)
+        out = run_fwd(w, to_device(w, x))
+        check_fwd(w, x, out, label=f"many short ({'kda' if variant else 'gdn'})")
+        ht = out["ht"].cpu().numpy()
+        for n, L in enumerate(lens):
+            if L == 0:
+                np.testing.assert_array_equal(ht[n], x["h0"][n])
