@@ -504,8 +504,9 @@ constexpr int kChainThreads = 32 * (kWarpTma + 1);
 //   warp 12      G2(n) = [Y; N_top] S(n) -> D2[n & 1] (the output, off the serial path);
 //   warp 13      the TMA loads of chunk n + NS once chunk n's stage is released.
 // Every mbarrier waited on by parity is re-armed only after its waiter has passed (barriers
-// that a faster party could lap come in pairs indexed by chunk parity), so no waiter can fall
-// two phases behind.  After a failed (timed-out) wait every further wait returns at once, so
+// that a faster party could lap come in sets indexed by chunk: pairs, or four for the hand-off
+// of S to G2, which the state warps may run up to three chunks ahead of), so no waiter can
+// fall two phases behind.  After a failed (timed-out) wait every further wait returns at once, so
 // all loops run to their ends without a uniform break.
 // KDA: Gamma_c is a per-key-channel vector (the state row of thread t decays by its own entry).
 template <int VS, int NS, bool KDA>
@@ -520,7 +521,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb1, bar_sb2[2], bar_g1[kG1Parts], bar_g2[3],
+    __shared__ uint64_t bar_tma[NS], bar_free[NS], bar_sb1, bar_sb2[4], bar_g1[kG1Parts], bar_g2[3],
         bar_d2free[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
@@ -575,10 +576,8 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             mbar_init(&bar_free[i], kComputeThreads / 32 + kOutWarps);
         }
         mbar_init(&bar_sb1, kComputeThreads / 32);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_sb2[i], kComputeThreads / 32);
-            mbar_init(&bar_d2free[i], kOutWarps);
-        }
+        for (int i = 0; i < 4; ++i) mbar_init(&bar_sb2[i], kComputeThreads / 32);
+        for (int i = 0; i < 2; ++i) mbar_init(&bar_d2free[i], kOutWarps);
         for (int i = 0; i < 3; ++i) mbar_init(&bar_g2[i], 1);
         for (int i = 0; i < kG1Parts; ++i) mbar_init(&bar_g1[i], 1);
         s_err = 0;
@@ -625,7 +624,9 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             for (int ic = 0; ic < nch; ++ic) {
                 const int st = ic % NS;
                 if (!mbar_wait(&bar_tma[st], (ic / NS) & 1, &s_err, 9)) break;
-                if (!mbar_wait(&bar_sb2[ic & 1], (ic >> 1) & 1, &s_err, 10)) break;
+                // the state warps may hand over S(ic + 1) and S(ic + 2) before this wait (they
+                // only wait for G2 two chunks back), so the hand-off barriers come in fours
+                if (!mbar_wait(&bar_sb2[ic % 4], (ic / 4) & 1, &s_err, 10)) break;
                 // D2[ic & 1] has been read for chunk ic - 2
                 if (ic >= 2 && !mbar_wait(&bar_d2free[ic & 1], ((ic - 2) >> 1) & 1, &s_err, 12)) break;
                 tc_fence_after();
@@ -713,7 +714,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&bar_sb1);
-                mbar_arrive(&bar_sb2[ic & 1]);
+                mbar_arrive(&bar_sb2[ic % 4]);
             }
         };
         float S[HV];

@@ -54,7 +54,7 @@ static gcl_status_t check_common(const char *fn, const void *q, const void *k, c
     if (t_max < 1 || t_max >= (int64_t(1) << 31) || n_max < 1 || H < 1)
         return fail(GCL_ERR_INVALID_ARG, "%s: need 1 <= t_max < 2^31, n_max >= 1, H >= 1", fn);
     if (bt != kChunk && bt != 32)
-        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (this build implements 32 and 64)", fn, bt);
+        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (implemented: 32 and 64)", fn, bt);
     if ((K != 64 && K != 128) || (V != 64 && V != 128))
         return fail(GCL_ERR_UNSUPPORTED, "%s: K=%d V=%d (supported: 64 or 128 each)", fn, K, V);
     if (dtype != GCL_F32 && dtype != GCL_BF16 && dtype != GCL_F16)
@@ -380,7 +380,7 @@ static gcl_status_t conv_check(const char *fn, const gcl_conv_args *a, bool back
     if (a->t_max < 1 || a->t_max >= (int64_t(1) << 31) || a->n_max < 1)
         return fail(GCL_ERR_INVALID_ARG, "%s: need 1 <= t_max < 2^31 and n_max >= 1", fn);
     if (a->bt != kChunk)
-        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (this build implements 64)", fn, a->bt);
+        return fail(GCL_ERR_UNSUPPORTED, "%s: chunk size bt=%d (implemented: 64)", fn, a->bt);
     if (a->W < 2 || a->W > 4)
         return fail(GCL_ERR_UNSUPPORTED, "%s: W=%d taps (supported: 2, 3, 4)", fn, a->W);
     if (a->D < 8 || a->D % 8 != 0)

@@ -53,7 +53,7 @@ extern "C" {
 typedef enum gcl_status {
     GCL_OK = 0,
     GCL_ERR_INVALID_ARG = 1,   /* NULL pointer, inconsistent or out-of-range size */
-    GCL_ERR_UNSUPPORTED = 2,   /* size, dtype or chunk size this build does not implement */
+    GCL_ERR_UNSUPPORTED = 2,   /* size, dtype or chunk size this library does not implement */
     GCL_ERR_CAPACITY = 3,      /* a fixed capacity (workspace, scratch) is too small */
     GCL_ERR_CUDA = 4           /* a CUDA call failed (message in gcl_last_error) */
 } gcl_status_t;
