@@ -397,7 +397,7 @@ def run_gpu(args, rank, world, dist):
     kern_ms = [a.elapsed_time(b) for a, b in ev_k]
     region_ms = ev_s[0].elapsed_time(ev_e[-1])
     tot = reduce_max([sum(step_ms), sum(kern_ms), region_ms], dist, dev)
-    ms_step = tot[0] / K
+    ms_step = tot[2] / K          # the whole bracketed region, gaps between steps included
     ms_kern = tot[1] / K
     value = job_throughput(w.total_tokens, world, ms_step)
 
@@ -634,9 +634,9 @@ def run_conv_gpu(args, rank, world, dist):
     clocks.stop()
     if dist is not None:
         dist.barrier()
-    tot = reduce_max([sum(e[0].elapsed_time(e[3]) for e in ev), sum(e[1].elapsed_time(e[2]) for e in ev),
+    tot = reduce_max([ev[0][0].elapsed_time(ev[-1][3]), sum(e[1].elapsed_time(e[2]) for e in ev),
                       sum(e[2].elapsed_time(e[3]) for e in ev)], dist, dev)
-    ms_step, ms_fwd, ms_bwd = (v / K for v in tot)
+    ms_step, ms_fwd, ms_bwd = (v / K for v in tot)   # step: the whole bracketed region
     e2e = conv_e2e(torch, lib, t, x, fa, ba, step, stream, args.e2e_steps, world, dist, tm)
     clk = clocks.summary()
     if rank != 0:
