@@ -120,3 +120,51 @@ def test_plan_rules_from_sizes_alone(lib):
     assert lib.gcl_fwd_chain_segments(65536, 1, 1, 64) >= 3
     assert lib.gcl_fwd_chain_segments(4096, 1, 16, 64) == 0
     assert lib.gcl_fwd_chain_segments(65536, 1, 1, 32) == 0
+
+
+def test_host_errors_other_entry_points(lib):
+    """The KDA backward, the short convolution, the no-allocation forward and the wait
+    self-test reject bad arguments on the host, before anything is enqueued."""
+    import chunked_gated_linear_gb300 as gcl
+    INVALID, UNSUPPORTED, CAPACITY = 1, 2, 3
+    fake = 1 << 20
+    # kda_chunk_bwd: same checks as the GDN backward
+    assert lib.kda_chunk_bwd(None, None) == INVALID
+    b = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, d_o=fake, cu_seqlens=fake,
+             chunk_indices=fake, chunk_offsets=fake, dq=fake, dk=fake, dv=fake, dg=fake,
+             dbeta=fake, workspace=fake, workspace_bytes=16, t_max=128, n_max=1, H=1, K=128,
+             V=128, bt=64, scale=1.0, dtype=1)
+    assert lib.kda_chunk_bwd(ctypes.byref(gcl.BwdArgs(**b)), None) == CAPACITY
+    assert b"workspace" in lib.gcl_last_error()
+    assert lib.kda_chunk_bwd(ctypes.byref(gcl.BwdArgs(**{**b, "d_o": None})), None) == INVALID
+    assert lib.kda_chunk_bwd(ctypes.byref(gcl.BwdArgs(**{**b, "K": 96})), None) == UNSUPPORTED
+    need = lib.gcl_kda_bwd_workspace_bytes(ctypes.byref(gcl.BwdArgs(**b)))
+    assert need > 0
+    ok = {**b, "workspace_bytes": need}
+    assert lib.kda_chunk_bwd(ctypes.byref(gcl.BwdArgs(**{**ok, "dq": fake + 4})), None) == INVALID
+    assert b"aligned" in lib.gcl_last_error()
+    # causal_conv1d: forward and backward argument checks
+    assert lib.causal_conv1d_fwd(None, None) == INVALID
+    assert lib.causal_conv1d_bwd(None, None) == INVALID
+    c = dict(x=fake, weight=fake, y=fake, cu_seqlens=fake, chunk_indices=fake, t_max=256,
+             n_max=2, D=64, W=4, bt=64, activation=0, dtype=1)
+    for bad, code in ((dict(W=1), UNSUPPORTED), (dict(W=5), UNSUPPORTED), (dict(D=12), UNSUPPORTED),
+                      (dict(dtype=7), UNSUPPORTED), (dict(bt=32), UNSUPPORTED),
+                      (dict(activation=9), UNSUPPORTED), (dict(t_max=0), INVALID),
+                      (dict(y=None), INVALID), (dict(x=fake + 8), INVALID)):
+        assert lib.causal_conv1d_fwd(ctypes.byref(gcl.ConvArgs(**{**c, **bad})), None) == code, bad
+        assert lib.gcl_last_error() != b""
+    cb = {**c, "y": None, "dy": fake, "dx": fake, "dweight": fake}
+    assert lib.causal_conv1d_bwd(ctypes.byref(gcl.ConvArgs(**{**cb, "dx": None})), None) == INVALID
+    assert lib.causal_conv1d_bwd(ctypes.byref(gcl.ConvArgs(**cb)), None) == CAPACITY
+    assert lib.gcl_causal_conv1d_bwd_workspace_bytes(ctypes.byref(gcl.ConvArgs(**cb))) > 0
+    assert lib.gcl_causal_conv1d_bwd_workspace_bytes(ctypes.byref(gcl.ConvArgs(**{**cb, "W": 7}))) == 0
+    # the no-allocation forward: sizes whose scratch exceeds the static array are rejected
+    assert lib.gdn_chunk_fwd_noalloc(None, None) == INVALID
+    big = gcl.FwdArgs(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake,
+                      t_max=1 << 22, n_max=64, H=64, K=128, V=128, bt=64, scale=1.0, dtype=1)
+    assert lib.gcl_fwd_workspace_min_bytes(ctypes.byref(big)) > lib.gcl_noalloc_scratch_bytes()
+    assert lib.gdn_chunk_fwd_noalloc(ctypes.byref(big), None) == CAPACITY
+    assert b"scratch" in lib.gcl_last_error()
+    # the wait self-test needs a status word
+    assert lib.gcl_selftest_wait_timeout(None, None) == INVALID
