@@ -6,6 +6,7 @@
 // clearly instead of falling back.  Every check here runs on the host before
 // anything is enqueued; launch shapes depend only on the sizes, never on
 // device data, so each call can be captured in a CUDA graph.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -31,16 +32,16 @@ gcl_status_t cuda_check(cudaError_t e, const char *what) {
 }
 
 int num_sms() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];                // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cache[dev] == 0) {
-        int v = 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
             v = 148;
-        cache[dev] = v;
+        cache[dev].store(v, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return v;
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
