@@ -6,10 +6,16 @@ pointers and the current CUDA stream to the C ABI declared in
 library must have been built (``python -m chunked_gated_linear_gb300._build``
 or ``__graft_entry__.build()``); importing this package fails loudly otherwise,
 and there is no other implementation to fall back on.
+
+The library sees raw pointers only, so before each launch the binding checks what a
+pointer cannot carry: every tensor is a contiguous CUDA tensor on the call's device, of the
+dtype and at least the size ``include/gcl.h`` gives it.  A host tensor or a too-small buffer
+would otherwise be read or written out of bounds on the device.
 """
 from __future__ import annotations
 
 import ctypes
+import inspect
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -154,6 +160,126 @@ def _dtype_of(t):
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
+class _Layout:
+    """Checks one call's tensors against their layouts in include/gcl.h: a CUDA tensor on the
+    call's device (when require_cuda), contiguous, of the given dtype(s), with the given
+    trailing dimensions and at least the given number of rows."""
+
+    def __init__(self, fn: str, require_cuda: bool = True):
+        self.fn, self.require_cuda, self.device = fn, require_cuda, None
+
+    def __call__(self, name, t, dtypes=None, shape=None):
+        if t is None:
+            return
+        if self.require_cuda:
+            dev = t.get_device()                         # -1 for a host tensor
+            if dev < 0:
+                raise ValueError(f"{self.fn}: {name} must be a CUDA tensor (got {t.device})")
+            if self.device is None:
+                self.device = dev
+            elif dev != self.device:
+                raise ValueError(f"{self.fn}: {name} is on cuda:{dev}, other tensors on "
+                                 f"cuda:{self.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{self.fn}: {name} must be contiguous")
+        if dtypes is not None:
+            dtypes = dtypes if isinstance(dtypes, tuple) else (dtypes,)
+            if t.dtype not in dtypes:
+                raise ValueError(f"{self.fn}: {name} has dtype {t.dtype}, expected "
+                                 + " or ".join(str(d) for d in dtypes))
+        if shape is not None:
+            got = t.shape
+            if len(got) != len(shape) or tuple(got[1:]) != tuple(shape[1:]) or got[0] < shape[0]:
+                raise ValueError(f"{self.fn}: {name} has shape {tuple(got)}, expected "
+                                 f"{tuple(shape)} (more rows are allowed)")
+
+
+_SIGNATURES = {}
+
+
+def _named(builder, args, kw):
+    """The arguments of a call of `builder` (fwd_args, bwd_args, conv_args) by name."""
+    sig = _SIGNATURES.get(builder)
+    if sig is None:
+        sig = _SIGNATURES[builder] = inspect.signature(builder)
+    b = sig.bind(*args, **kw)
+    b.apply_defaults()
+    return b.arguments
+
+
+def validate_fwd(fn, a, kda, require_cuda=True):
+    """Layouts of a forward call's tensors (a: fwd_args' arguments by name)."""
+    import torch
+    L = _Layout(fn, require_cuda)
+    q, cu = a["q"], a["cu_seqlens"]
+    T, H, K = q.shape
+    V = a["v"].shape[-1]
+    N = cu.shape[0] - 1
+    ntm = nt_max(T, N, a["bt"])
+    dt, f32, i32 = q.dtype, torch.float32, torch.int32
+    for name, shp in (("q", (T, H, K)), ("k", (T, H, K)), ("v", (T, H, V)), ("beta", (T, H)),
+                      ("o", (T, H, V))):
+        L(name, a[name], dt, shp)
+    L("g", a["g"], f32, (T, H, K) if kda else (T, H))
+    L("cu_seqlens", cu, i32, (N + 1,))
+    for name in ("h0", "ht"):
+        L(name, a[name], f32, (N, H, K, V))
+    L("h_save", a["h_save"], f32, (ntm, H, K, V))
+    L("chunk_indices", a["chunk_indices"], i32, (ntm, 2))
+    L("chunk_offsets", a["chunk_offsets"], i32, (N + 1,))
+    L("seq_order", a["seq_order"], i32, (N,))
+    L("dev_status", a["dev_status"], i32, (1,))
+    L("workspace", a["workspace"])
+
+
+def validate_bwd(fn, a, kda, require_cuda=True):
+    """Layouts of a backward call's tensors (a: bwd_args' arguments by name)."""
+    import torch
+    L = _Layout(fn, require_cuda)
+    q, cu = a["q"], a["cu_seqlens"]
+    T, H, K = q.shape
+    V = a["v"].shape[-1]
+    N = cu.shape[0] - 1
+    ntm = nt_max(T, N, a["bt"])
+    dt, f32, i32 = q.dtype, torch.float32, torch.int32
+    gshape = (T, H, K) if kda else (T, H)
+    for name, shp in (("q", (T, H, K)), ("k", (T, H, K)), ("v", (T, H, V)), ("beta", (T, H)),
+                      ("d_o", (T, H, V))):
+        L(name, a[name], dt, shp)
+    for name, shp in (("g", gshape), ("dg", gshape), ("dq", (T, H, K)), ("dk", (T, H, K)),
+                      ("dv", (T, H, V)), ("dbeta", (T, H)), ("h0", (N, H, K, V)),
+                      ("dht", (N, H, K, V)), ("dh0", (N, H, K, V)), ("h_save", (ntm, H, K, V))):
+        L(name, a[name], f32, shp)
+    L("cu_seqlens", cu, i32, (N + 1,))
+    L("chunk_indices", a["chunk_indices"], i32, (ntm, 2))
+    L("chunk_offsets", a["chunk_offsets"], i32, (N + 1,))
+    L("dev_status", a["dev_status"], i32, (1,))
+    L("workspace", a["workspace"])
+    L("fwd_workspace", a["fwd_workspace"])
+
+
+def validate_conv(fn, a, require_cuda=True):
+    """Layouts of a causal_conv1d call's tensors (a: conv_args' arguments by name)."""
+    import torch
+    L = _Layout(fn, require_cuda)
+    x, w, cu = a["x"], a["weight"], a["cu_seqlens"]
+    T, D = x.shape
+    W = w.shape[1]
+    N = cu.shape[0] - 1
+    dt, f32, i32 = x.dtype, torch.float32, torch.int32
+    for name, shp in (("x", (T, D)), ("weight", (D, W)), ("bias", (D,)), ("residual", (T, D)),
+                      ("h0", (N, D, W - 1)), ("y", (T, D)), ("ht", (N, D, W - 1)),
+                      ("dy", (T, D))):
+        L(name, a[name], dt, shp)
+    for name, shp in (("dht", (N, D, W - 1)), ("dx", (T, D)), ("dweight", (D, W)),
+                      ("dbias", (D,)), ("dh0", (N, D, W - 1))):
+        L(name, a[name], f32, shp)
+    L("cu_seqlens", cu, i32, (N + 1,))
+    L("chunk_indices", a["chunk_indices"], i32, (nt_max(T, N, a["bt"]), 2))
+    L("dev_status", a["dev_status"], i32, (1,))
+    L("workspace", a["workspace"])
+
+
 def nt_max(t_max: int, n_max: int, bt: int = CHUNK) -> int:
     return int(lib().gcl_nt_max(t_max, n_max, bt))
 
@@ -161,6 +287,8 @@ def nt_max(t_max: int, n_max: int, bt: int = CHUNK) -> int:
 def selftest_wait_timeout(dev_status, stream=None):
     """One CTA waits on an mbarrier nothing arrives at; after the time limit dev_status holds
     GCL_DEV_WAIT_TIMEOUT (the bounded-wait path of every tensor-core kernel)."""
+    import torch
+    _Layout("gcl_selftest_wait_timeout")("dev_status", dev_status, torch.int32, (1,))
     _check("gcl_selftest_wait_timeout", lib().gcl_selftest_wait_timeout(_p(dev_status), _stream(stream)))
 
 
@@ -173,7 +301,15 @@ def chunk_meta_build(cu_seqlens, t_max, chunk_indices, chunk_offsets, dev_status
                      seq_order=None, bt: int = CHUNK, stream=None, cu_seqlens32=None):
     """Chunk metadata from cu_seqlens (int32, or int64 with an int32 copy written to
     cu_seqlens32 for the compute calls)."""
+    import torch
     n_max = cu_seqlens.shape[0] - 1
+    L = _Layout("chunk_meta_build")
+    L("cu_seqlens", cu_seqlens, (torch.int32, torch.int64), (n_max + 1,))
+    L("chunk_indices", chunk_indices, torch.int32, (chunk_indices.shape[0], 2))
+    L("chunk_offsets", chunk_offsets, torch.int32, (n_max + 1,))
+    L("seq_order", seq_order, torch.int32, (n_max,))
+    L("dev_status", dev_status, torch.int32, (1,))
+    L("cu_seqlens32", cu_seqlens32, torch.int32, (n_max + 1,))
     if cu_seqlens.element_size() == 8:
         if cu_seqlens32 is None:
             raise ValueError("an int64 cu_seqlens needs cu_seqlens32 (int32 [n_max + 1]) for its copy")
@@ -226,6 +362,7 @@ def kda_fwd_workspace_bytes(*args, **kw) -> int:
 
 
 def gdn_chunk_fwd(*args, stream=None, **kw):
+    validate_fwd("gdn_chunk_fwd", _named(fwd_args, args, kw), kda=False)
     a = fwd_args(*args, **kw)
     _check("gdn_chunk_fwd", lib().gdn_chunk_fwd(ctypes.byref(a), _stream(stream)))
 
@@ -234,6 +371,7 @@ def gdn_chunk_fwd_noalloc(*args, stream=None, **kw):
     """gdn_chunk_fwd without a workspace argument: the library's static scratch is used
     (for callers that cannot allocate device memory; see include/gcl.h)."""
     kw.pop("workspace", None)
+    validate_fwd("gdn_chunk_fwd_noalloc", _named(fwd_args, args, kw), kda=False)
     a = fwd_args(*args, **kw)
     _check("gdn_chunk_fwd_noalloc", lib().gdn_chunk_fwd_noalloc(ctypes.byref(a), _stream(stream)))
 
@@ -243,6 +381,7 @@ def noalloc_scratch_bytes() -> int:
 
 
 def kda_chunk_fwd(*args, stream=None, **kw):
+    validate_fwd("kda_chunk_fwd", _named(fwd_args, args, kw), kda=True)
     a = fwd_args(*args, **kw)
     _check("kda_chunk_fwd", lib().kda_chunk_fwd(ctypes.byref(a), _stream(stream)))
 
@@ -269,6 +408,7 @@ def bwd_workspace_bytes(*args, **kw) -> int:
 
 
 def gdn_chunk_bwd(*args, stream=None, **kw):
+    validate_bwd("gdn_chunk_bwd", _named(bwd_args, args, kw), kda=False)
     a = bwd_args(*args, **kw)
     _check("gdn_chunk_bwd", lib().gdn_chunk_bwd(ctypes.byref(a), _stream(stream)))
 
@@ -280,6 +420,7 @@ def kda_bwd_workspace_bytes(*args, **kw) -> int:
 
 def kda_chunk_bwd(*args, stream=None, **kw):
     """The KDA backward; dg has the shape of g, [T, H, K]."""
+    validate_bwd("kda_chunk_bwd", _named(bwd_args, args, kw), kda=True)
     a = bwd_args(*args, **kw)
     _check("kda_chunk_bwd", lib().kda_chunk_bwd(ctypes.byref(a), _stream(stream)))
 
@@ -303,6 +444,7 @@ def conv_args(x, weight, cu_seqlens, chunk_indices, bias=None, residual=None, h0
 
 
 def causal_conv1d_fwd(*args, stream=None, **kw):
+    validate_conv("causal_conv1d_fwd", _named(conv_args, args, kw))
     a = conv_args(*args, **kw)
     _check("causal_conv1d_fwd", lib().causal_conv1d_fwd(ctypes.byref(a), _stream(stream)))
 
@@ -313,5 +455,6 @@ def causal_conv1d_bwd_workspace_bytes(*args, **kw) -> int:
 
 
 def causal_conv1d_bwd(*args, stream=None, **kw):
+    validate_conv("causal_conv1d_bwd", _named(conv_args, args, kw))
     a = conv_args(*args, **kw)
     _check("causal_conv1d_bwd", lib().causal_conv1d_bwd(ctypes.byref(a), _stream(stream)))

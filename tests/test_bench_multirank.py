@@ -41,7 +41,7 @@ def _rank_main(rank, world, port, out):
 
 def test_timings_max_reduced_and_throughput_counts_all_ranks():
     world, port = 2, _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()        # no fork of a process that runs torch threads
     out = mgr.dict()
     mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, start_method="spawn")
     for rank in range(world):
