@@ -168,3 +168,22 @@ def test_host_errors_other_entry_points(lib):
     assert b"scratch" in lib.gcl_last_error()
     # the wait self-test needs a status word
     assert lib.gcl_selftest_wait_timeout(None, None) == INVALID
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """A C99 program that includes include/gcl.h and links libgcl.so builds with gcc and its
+    host-side ABI checks pass (the header is C, not C++; no GPU is touched)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    libdir = os.path.join(ROOT, "chunked_gated_linear_gb300")
+    exe = str(tmp_path / "abi_host_check")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_host_check.c"),
+                    "-L", libdir, "-lgcl", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "c abi ok" in r.stdout
