@@ -1,0 +1,63 @@
+"""bench.py's host arithmetic on CPU: the algorithmic bytes and FLOPs per step behind the
+roofline fraction, the peak lookup, and the traffic record that is reported only while the
+kernel sources it was measured on are unchanged."""
+import hashlib
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from chunked_gated_linear_gb300 import synth  # noqa: E402
+
+
+def test_algorithmic_bytes_per_token_head():
+    """Per token and head: q, k, v read and o written once, beta and the gate read once
+    (GDN bf16 1,030 B; KDA adds the per-channel fp32 gate: 1,538 B; fp32 K = V = 64: 1,032 B),
+    plus h0 read and ht written once per (sequence, head) state of K x V fp32."""
+    for w, per in ((synth.dense("a", synth.GDN, "bf16", 1, 4096, 16, 128, 128, h0=False), 1030),
+                   (synth.dense("b", synth.KDA, "bf16", 1, 2048, 10, 128, 128, h0=False), 1538),
+                   (synth.dense("c", synth.GDN, "f32", 1, 256, 2, 64, 64, h0=False), 1032)):
+        state = w.K * w.V * 4 * w.n_max * w.H                 # ht only (no h0)
+        assert bench.bytes_per_step(w) == w.total_tokens * w.H * per + state
+    w = synth.dense("d", synth.GDN, "bf16", 1, 4096, 16, 128, 128)      # with h0
+    assert bench.bytes_per_step(w) == 4096 * 16 * 1030 + 2 * 128 * 128 * 4 * 16
+    assert bench.bytes_per_step(w) == 69_599_232        # the bench line's figure
+
+
+def test_tensor_flops_per_token_head():
+    """6CK + 4CV + 6KV + 2C^2/3 with C = 64, K = V = 128: about 183 kFLOP per token and head."""
+    w = synth.dense("a", synth.GDN, "bf16", 1, 4096, 16, 128, 128)
+    per = bench.flops_per_step(w) / (4096 * 16)
+    assert per == pytest.approx(6 * 64 * 128 + 4 * 64 * 128 + 6 * 128 * 128 + 2 * 64 * 64 / 3)
+    assert 182_000 < per < 184_000
+
+
+def test_peaks_measured_or_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6681.8}))
+    assert bench.peaks() == (6681.8, "measured")
+
+
+def test_traffic_record_follows_the_source_hash(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("wl") is None                     # no record file
+    src = tmp_path / "k.cu"
+    src.write_bytes(b"__global__ void k() {}\n")
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# comment: ignored\n\n[wl]\nkernel_sources: k.cu\n"
+        f"kernel_sources_sha256_16: {digest}\nprep_dram_bytes: 1\n"
+        "dram_bytes_per_launch_scaled: 12345\n\n[other]\nkernel_sources: missing.cu\n"
+        "kernel_sources_sha256_16: 0\ndram_bytes_per_launch_scaled: 7\n")
+    assert bench.traffic_record("wl") == 12345.0
+    assert bench.traffic_record("other") is None                  # its source is missing
+    assert bench.traffic_record("absent") is None
+    src.write_bytes(b"__global__ void k() { /* changed */ }\n")
+    assert bench.traffic_record("wl") is None                     # stale once the kernel changes
