@@ -472,20 +472,22 @@ def run_e2e(gcl, w, x, r, stream, s, steps, world, dist):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, x, heads, tokens):
-    """The oracle on the first `tokens` tokens of every sequence and the first `heads`
-    heads; returns (seconds, token-heads processed)."""
+def oracle_sample(w, x, heads, tokens, seqs=None):
+    """The oracle on the first `tokens` tokens of every sequence (of the first `seqs`
+    sequences, if given) and the first `heads` heads; returns (seconds, token-heads
+    processed)."""
     import oracle
     cu = x["cu_seqlens"].astype(np.int64)
+    nseq = len(cu) - 1 if seqs is None else min(seqs, len(cu) - 1)
     rows = []
     new_cu = [0]
-    for n in range(len(cu) - 1):
+    for n in range(nseq):
         s, e = int(cu[n]), int(min(cu[n + 1], cu[n] + tokens))
         rows.append(np.arange(s, e))
         new_cu.append(new_cu[-1] + (e - s))
     rows = np.concatenate(rows) if rows else np.zeros(0, dtype=np.int64)
     sl = {n: x[n][rows][:, :heads] for n in ("q", "k", "v", "g", "beta")}
-    h0 = None if x["h0"] is None else x["h0"][:, :heads]
+    h0 = None if x["h0"] is None else x["h0"][:nseq, :heads]
     t0 = time.perf_counter()
     oracle.fwd(w.variant, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], h0, new_cu, w.scale)
     return time.perf_counter() - t0, len(rows) * heads
@@ -506,10 +508,26 @@ def cpu_baseline(w, x, budget_s=12.0):
         dt += d2
         th += t2
         reps += 1
-    return {"value": th / w.H / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
+    line = {"value": th / w.H / dt, "unit": "tokens/s",
+            "cores": min(oracle.num_threads(), heads * len(w.lengths)), "kind": "oracle",
             "sample": f"fp64 token recurrence, first {tokens} tokens of every sequence, all "
                       f"{heads} heads, {reps} run(s) ({th} token-heads, {dt:.1f} s)"}
+    # the same oracle on one (sequence, head) unit: one host thread, about 3 s
+    if w.lengths and w.lengths[0] > 0:
+        d1, t1 = oracle_sample(w, x, 1, 64, seqs=1)
+        tok1 = int(min(max(64, 3.0 * t1 / max(d1, 1e-6)), w.lengths[0]))
+        d1, t1 = oracle_sample(w, x, 1, tok1, seqs=1)
+        reps1 = 1
+        while d1 < 2.4 and reps1 < 500:
+            d2, t2 = oracle_sample(w, x, 1, tok1, seqs=1)
+            d1 += d2
+            t1 += t2
+            reps1 += 1
+        line["single_thread"] = {
+            "value": t1 / w.H / d1, "unit": "tokens/s", "cores": 1,
+            "sample": f"first {tok1} tokens of sequence 0, head 0, {reps1} run(s) "
+                      f"({t1} token-heads, {d1:.1f} s), per token of all {w.H} heads"}
+    return line
 
 
 def run_reference(args):
