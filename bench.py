@@ -792,7 +792,9 @@ def main():
         dist = dist_
     line = run_conv_gpu(args, rank, world, dist) if conv else run_gpu(args, rank, world, dist)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if world > 1:
+            line["cpu_baseline"] = None      # the oracle is timed at one GPU only
+        elif not args.no_cpu_baseline:
             if conv:
                 line["cpu_baseline"] = conv_cpu_baseline(synth.conv_workload_by_name(args.workload))
             else:
