@@ -62,7 +62,7 @@ dstate_sweep_kernel(BwdParams p) {
     float *sB = sm + Lay::oB, *sG = sm + Lay::oG;
     constexpr int LK = Lay::LK, LV = Lay::LV;
 
-    if (status_blocks(p.dev_status)) return;
+    if (status_blocks_cta(p.dev_status)) return;
     const int tid = threadIdx.x;
     const int v0 = blockIdx.x * VS, h = blockIdx.y, n = blockIdx.z;
     const int H = p.H, V = p.V;
@@ -197,7 +197,7 @@ chunk_grad_kernel(BwdParams p) {
     float *sA = sm + Lay::oFree;              // A during the Map; later dT T^T
     float *sAp = sm + Lay::oFree + C * kLC;   // A' at the end
 
-    if (status_blocks(p.dev_status)) return;
+    if (status_blocks_cta(p.dev_status)) return;
     const int n = p.chunk_indices[2 * blockIdx.x];
     if (n < 0) return;                         // sentinel row: nothing to do
     if (n >= p.n_max) {
@@ -489,7 +489,7 @@ chunk_grad_kda_kernel(BwdParams p) {
     float *sKp = sQ, *sKb = sG;               // in place of Q and gamma during the slice loop
     float *sDGm = sT, *sW3 = sT + C * LK;     // dgamma and the gamma_c terms at the end
 
-    if (status_blocks(p.dev_status)) return;
+    if (status_blocks_cta(p.dev_status)) return;
     const int n = p.chunk_indices[2 * blockIdx.x];
     if (n < 0) return;                         // sentinel row: nothing to do
     if (n >= p.n_max) {

@@ -124,7 +124,7 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __shared__ int s_err;
     __shared__ float sG[C], sB[C], sEG[C], sFR[C], sRow[4][C], sRed[kThreads / 32], s_carry;
 
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quarter = warp & 3, half = warp >> 2;
     const int lrow = quarter * 32 + (tid & 31);
@@ -616,7 +616,7 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __shared__ float sG[C], sB[C], sDG[C], sPart[4][C], sRed2[2], s_carry;
     const float *sRA = sRows, *sRB = sRows + C, *sRC = sRows + 2 * C, *sRD = sRows + 3 * C;
 
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int lrow = quarter * 32 + lane;

@@ -72,7 +72,7 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;

@@ -61,12 +61,16 @@ fwd_simt_kernel(FwdParams p) {
     float *sB = sm + Lay::oB, *sG = sm + Lay::oG;
     constexpr int LK = Lay::LK, LV = Lay::LV;
 
-    if (status_blocks(p.dev_status)) return;
+    if (status_blocks_cta(p.dev_status)) return;
     const int tid = threadIdx.x;
     const int split = blockIdx.x, h = blockIdx.y;
     const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
     const int H = p.H, V = p.V;
     const int v0 = split * VS;
+    if (n < 0 || n >= p.n_max) {              // checked before cu[n] and cu[n + 1] are read
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
     const int64_t bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
     if (bos < 0 || eos < bos || eos > p.t_max) {
         if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);

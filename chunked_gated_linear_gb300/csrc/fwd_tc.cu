@@ -114,7 +114,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __shared__ int s_err;
     __shared__ float sG[C], sB[C], sEG[C];
 
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, j = blockIdx.x, h = blockIdx.y;
     const int n = p.chunk_indices[2 * j];
     if (n < 0) return;                              // sentinel: unused chunk slot
@@ -344,7 +344,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool compute = warp < 8;
     const int quarter = warp & 3, half = (warp >> 2) & 1;
@@ -353,8 +353,12 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int split = blockIdx.x, h = blockIdx.y;
     const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
     const int H = p.H, v0 = split * VS;
+    if (n < 0 || n >= p.n_max) {              // checked before cu[n] and cu[n + 1] are read
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
     const int64_t bos = p.cu[n], eos = p.cu[n + 1];
-    if (n < 0 || n >= p.n_max || bos < 0 || eos < bos || eos > p.t_max) {
+    if (bos < 0 || eos < bos || eos > p.t_max) {
         if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
         return;
     }

@@ -110,7 +110,7 @@ tc_prep_kda_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // launched as a dependent of the metadata (or any earlier) kernel
     grid_dependency_wait();
     launch_dependents();
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int lrow = quarter * 32 + lane;                 // TMEM lane read by this thread

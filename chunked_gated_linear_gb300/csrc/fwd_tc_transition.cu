@@ -75,7 +75,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // the chain kernel may be scheduled on SMs this grid leaves; it reads the records only
     // after waiting for this grid's completion
     launch_dependents();
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quarter = warp & 3, half = warp >> 2;
     const int lrow = quarter * 32 + (tid & 31);           // TMEM lane read by this thread
@@ -529,7 +529,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     // a segmented launch waits for the grid before it in full (the records, the start states)
     // before any exit, so that its own completion implies theirs
     if (p.mode != 0) grid_dependency_wait();
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;
@@ -837,7 +837,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(SegScanParams
     float *sS = sm_scan + ScanLayout::oS;                // [KD][kScanSC]
     float *sRed = sm_scan + ScanLayout::oRed;            // [kScanWarps][KD][kScanSC]
     grid_dependency_wait();                              // the segment summaries are complete
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int c0 = blockIdx.x * kScanSC, h = blockIdx.y, n = blockIdx.z;
     const int64_t bos = p.cu[n], eos = p.cu[n + 1];
     if (bos < 0 || eos < bos || eos > p.t_max) return;  // reported by the chain

@@ -170,6 +170,15 @@ inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 bloc
 __device__ __forceinline__ bool status_blocks(const int32_t *st) {
     return st != nullptr && *reinterpret_cast<const volatile int32_t *>(st) != 0;
 }
+// Block-uniform form of status_blocks: thread 0 reads the word once and every thread of the
+// block takes the same answer, so no warp leaves while the others go on to barriers, mbarrier
+// set-up or TMEM allocation.  Every thread of the block must call it (block barrier).
+__device__ __forceinline__ bool status_blocks_cta(const int32_t *st) {
+    __shared__ int s_blocked;
+    if (threadIdx.x == 0) s_blocked = status_blocks(st) ? 1 : 0;
+    __syncthreads();
+    return s_blocked != 0;
+}
 __device__ __forceinline__ void status_set(int32_t *st, int32_t code) {
     if (st != nullptr) atomicCAS(st, 0, code);
 }

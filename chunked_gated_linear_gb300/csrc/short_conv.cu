@@ -182,7 +182,7 @@ conv_fwd_kernel(ConvParams p) {
     constexpr int CB = kFwdChannels * 2 / (int)sizeof(T);   // 34 KB tiles for both types
     constexpr int G = CB / kChannelsPerThread, RL = kConvThreads / G;
     __shared__ __align__(16) T tile[(C + W - 1) * CB];
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     if ((int64_t)blockIdx.x >= p.nt_max) {                 // the sequence slots: zero-length sequences
         const int64_t n = (int64_t)blockIdx.x - p.nt_max;
         if (n < p.n_max) conv_empty_sequence<T, W>(p, (int)n, blockIdx.y, CB, false);
@@ -266,7 +266,7 @@ conv_bwd_kernel(ConvParams p) {
     constexpr int NG = kConvThreads / CB;                 // row groups of the dw, db sums
     extern __shared__ __align__(16) uint8_t smem[];
     float *sdp = reinterpret_cast<float *>(smem + Lay::oDP);
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int D = p.D, cb = blockIdx.y, cb0 = cb * CB, part_idx = blockIdx.x;
     const int64_t step = gridDim.x;
     auto tx = [&](int b) { return reinterpret_cast<T *>(smem + b * Lay::kBuf); };
@@ -437,7 +437,7 @@ template <int W>
 __global__ void __launch_bounds__(kReduceWarps * 32)
 conv_reduce_kernel(ConvParams p) {
     __shared__ float red[kReduceWarps][W + 1][32];
-    if (status_blocks(p.status)) return;
+    if (status_blocks_cta(p.status)) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
     float acc[W + 1];

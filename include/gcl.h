@@ -340,9 +340,12 @@ size_t gcl_kda_bwd_workspace_bytes(const gcl_bwd_args *args);
  * cores (tcgen05), everything else on the CUDA cores in fp32.
  *
  * kda_chunk_bwd -- the same through the KDA chunk forward (per-key-channel gate;
- * dg has the shape of g, [t_max, H, K]).  The sweep and the chunk gradients run on
- * the CUDA cores in fp32 (the recompute of missing states uses the forward's own
- * path, tensor cores for bf16 K = V = 128).  Errors as for gdn_chunk_bwd.
+ * dg has the shape of g, [t_max, H, K]).  For bf16 with K = V = 128 the reverse
+ * state-gradient sweep runs on the tensor cores (tcgen05, from the KDA transition
+ * records: the forward's when handed over, else recomputed) and the chunk gradients
+ * on the CUDA cores in fp32; every other size and dtype runs both on the CUDA cores in
+ * fp32.  The recompute of missing states uses the forward's own path.  Errors as for
+ * gdn_chunk_bwd.
  */
 gcl_status_t gdn_chunk_bwd(const gcl_bwd_args *args, gcl_stream_t stream);
 gcl_status_t kda_chunk_bwd(const gcl_bwd_args *args, gcl_stream_t stream);

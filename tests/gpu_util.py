@@ -17,11 +17,8 @@ CANARY = 1536.0          # exact in bf16; written into output padding, must surv
 TOL = {"f32": 1e-5, "bf16": 5e-3, "f16": 1e-3}
 
 
-def relF(got, want) -> float:
-    got = np.asarray(got, dtype=np.float64)
-    want = np.asarray(want, dtype=np.float64)
-    den = np.linalg.norm(want)
-    return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
+from parity import check as parity_check  # noqa: E402  (global, per-unit and per-row bars)
+from parity import relF  # noqa: E402,F401
 
 
 def tdtype(w):
@@ -93,7 +90,8 @@ def oracle_fwd(w, x):
 
 
 def check_fwd(w, x, out, tol=None, label=""):
-    """Compare device outputs against the oracle; check padding canaries."""
+    """Compare device outputs against the oracle (global, per-unit and per-row bars of
+    tests/parity.py); check padding canaries."""
     tol = TOL[w.dtype] if tol is None else tol
     torch.cuda.synchronize()
     assert int(out["meta"].status.item()) == 0, "device status " + str(out["meta"].status.item())
@@ -102,10 +100,9 @@ def check_fwd(w, x, out, tol=None, label=""):
     o = out["o"].float().cpu().numpy()
     ht = out["ht"].cpu().numpy()
     assert np.isfinite(o[:T]).all(), label + " non-finite o"
-    e_o = relF(o[:T], o_ref[:T])
-    e_h = relF(ht, ht_ref)
-    assert e_o <= tol, f"{label} o rel-Frobenius {e_o:.3e} > {tol}"
-    assert e_h <= tol, f"{label} ht rel-Frobenius {e_h:.3e} > {tol}"
+    cu = np.asarray(x["cu_seqlens"], dtype=np.int64)
+    e_o = parity_check(label + " o", o[:T], o_ref[:T], tol, cu=cu)[0]
+    e_h = parity_check(label + " ht", ht, ht_ref, tol)[0]
     if T < w.t_max:
         pad = o[T:]
         assert (pad == np.float32(CANARY)).all(), label + " output padding was written"

@@ -9,6 +9,7 @@ import oracle  # noqa: E402
 import chunked_gated_linear_gb300 as gcl  # noqa: E402
 from chunked_gated_linear_gb300 import synth  # noqa: E402
 from gpu_util import DEV, TOL, Meta, check_fwd, relF, run_fwd, to_device  # noqa: E402
+from parity import check as parity_check  # noqa: E402
 
 GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 
@@ -39,11 +40,14 @@ def oracle_bwd(w, x, with_dht=True):
 
 
 def compare(w, got, ref, tol):
+    """Every gradient at the global, per-unit and per-row bars (tests/parity.py)."""
     T = w.total_tokens
+    cu = np.asarray(synth.cu_seqlens_of(w), dtype=np.int64)
     for key in GRADS:
-        a, b = (got[key], ref[key]) if key == "dh0" else (got[key][:T], ref[key][:T])
-        e = relF(a, b)
-        assert e <= tol, f"{key}: rel-Frobenius {e:.3e} > {tol}"
+        if key == "dh0":
+            parity_check(key, got[key], ref[key], tol)
+        else:
+            parity_check(key, got[key][:T], ref[key][:T], tol, cu=cu)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -74,25 +78,35 @@ def test_no_dht_no_h0():
 
 def test_fwd_bwd_full_size_sampled_units():
     """B=4, T=8192, H=16, d=128, bf16: forward + backward on the GPU at full size; the oracle
-    recomputes sampled (sequence, head) units one by one and every gradient of those units is
-    compared."""
+    recomputes sampled (sequence, head) units one by one (eight of the 64, including the last
+    sequence and the last head), and o, ht and every gradient of those units are compared at
+    the global, per-unit and per-row bars."""
     w = synth.standard_workloads()[4]
     x = synth.make_inputs(w)
     d = to_device(w, x)
     fw = run_fwd(w, d, h_save=True)
+    torch.cuda.synchronize()
+    assert int(fw["meta"].status.item()) == 0
+    o = fw["o"].float().cpu().numpy()
+    ht = fw["ht"].cpu().numpy()
     got = run_bwd(w, d, fw["meta"], h_save=fw["h_save"])
     T = w.lengths[0]
-    for (b, h) in ((0, 0), (2, 7), (3, 15)):
+    cu1 = np.array([0, T], dtype=np.int64)
+    units = ((0, 0), (0, 15), (1, 3), (1, 9), (2, 7), (2, 12), (3, 0), (3, 15))
+    for (b, h) in units:
         s, e = b * T, (b + 1) * T
         sl = {m: x[m][s:e, h:h + 1] for m in ("q", "k", "v", "g", "beta", "do")}
-        ref = oracle.bwd(synth.GDN, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"],
-                         x["h0"][b:b + 1, h:h + 1], sl["do"], x["dht"][b:b + 1, h:h + 1],
-                         [0, T], w.scale)
+        h0 = x["h0"][b:b + 1, h:h + 1]
+        o_ref, ht_ref = oracle.fwd(synth.GDN, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], h0,
+                                   [0, T], w.scale)
+        parity_check(f"unit ({b},{h}) o", o[s:e, h:h + 1], o_ref, TOL["bf16"], cu=cu1)
+        parity_check(f"unit ({b},{h}) ht", ht[b:b + 1, h:h + 1], ht_ref, TOL["bf16"])
+        ref = oracle.bwd(synth.GDN, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], h0,
+                         sl["do"], x["dht"][b:b + 1, h:h + 1], [0, T], w.scale)
         for key in ("dq", "dk", "dv", "dg", "dbeta"):
-            e_ = relF(got[key][s:e, h:h + 1], ref[key])
-            assert e_ <= TOL["bf16"], f"unit ({b},{h}) {key}: {e_:.3e}"
-        e_ = relF(got["dh0"][b, h], ref["dh0"][0, 0])
-        assert e_ <= TOL["bf16"], f"unit ({b},{h}) dh0: {e_:.3e}"
+            parity_check(f"unit ({b},{h}) {key}", got[key][s:e, h:h + 1], ref[key], TOL["bf16"],
+                         cu=cu1)
+        parity_check(f"unit ({b},{h}) dh0", got["dh0"][b:b + 1, h:h + 1], ref["dh0"], TOL["bf16"])
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
