@@ -104,6 +104,9 @@ def load_library(path: str = LIB_PATH):
     for fn in ("gcl_fwd_workspace_bytes", "gcl_fwd_workspace_min_bytes", "gcl_kda_fwd_workspace_bytes"):
         getattr(lib, fn).restype = ctypes.c_size_t
         getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs)]
+    for fn in ("gcl_fwd_plan", "gcl_kda_fwd_plan"):
+        getattr(lib, fn).restype = i32
+        getattr(lib, fn).argtypes = [ctypes.POINTER(FwdArgs)]
     for fn in ("gdn_chunk_bwd", "kda_chunk_bwd"):
         getattr(lib, fn).restype = ctypes.c_int
         getattr(lib, fn).argtypes = [ctypes.POINTER(BwdArgs), vp]
@@ -350,7 +353,8 @@ def fwd_workspace_bytes(*args, **kw) -> int:
 
 
 def fwd_workspace_min_bytes(*args, **kw) -> int:
-    """Least workspace the forward accepts (it then runs the W-form plan)."""
+    """Least workspace the forward accepts (it then runs the W-form plan; 0 where the fused
+    plan runs)."""
     a = fwd_args(*args, **kw)
     return int(lib().gcl_fwd_workspace_min_bytes(ctypes.byref(a)))
 
@@ -359,6 +363,19 @@ def kda_fwd_workspace_bytes(*args, **kw) -> int:
     """Workspace kda_chunk_fwd needs (its one tensor-core plan; 0 on the CUDA-core path)."""
     a = fwd_args(*args, **kw)
     return int(lib().gcl_kda_fwd_workspace_bytes(ctypes.byref(a)))
+
+
+PLANS = {0: "cuda_cores", 1: "fused", 2: "w_form", 3: "transition", 4: "segmented"}
+
+
+def fwd_plan(*args, kda=False, **kw) -> str:
+    """Name of the launch plan the forward runs with these arguments (workspace included):
+    cuda_cores, fused, w_form, transition or segmented (include/gcl.h, gcl_fwd_plan)."""
+    a = fwd_args(*args, **kw)
+    code = int((lib().gcl_kda_fwd_plan if kda else lib().gcl_fwd_plan)(ctypes.byref(a)))
+    if code < 0:
+        raise GclError("gcl_fwd_plan", code, lib().gcl_last_error().decode())
+    return PLANS[code]
 
 
 def gdn_chunk_fwd(*args, stream=None, **kw):

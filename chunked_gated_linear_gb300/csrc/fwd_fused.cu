@@ -1,0 +1,556 @@
+// fwd_fused.cu -- the fused tensor-core GDN chunk forward: one CTA per (sequence, head)
+// carries the whole Map-Reduce-Map of its chunks on chip (bf16 inputs, d_k = d_v = 128,
+// chunk 64).  Nothing but q, k, v, g, beta, h0 is read and nothing but o, ht (and h_save)
+// is written: no per-chunk records go through HBM.
+//
+// HA-NPU paper "Empowering Hybrid Attention Models on NPUs": section 2.1 (Map-Reduce-Map),
+// section 4 (head-per-core mapping with every intermediate kept on the core, the first
+// scheduling tier when there are at least as many heads as cores), section 5 (GEMM-first
+// grouping: KS and QS before the inverse is applied; chunk-first in-place state update).
+// FLA RFC "[RFC] Add Graph Capture Support for FLA Prefill and Training Paths on Ascend NPUs",
+// "Core design": a fixed grid over the N_max sequence slots; a zero-length slot passes h0 to ht.
+//
+// Per chunk, with gamma the in-chunk cumsum of g, Gamma = exp(gamma), Gamma_c = Gamma at the
+// last row, f = exp(gamma_c - gamma), D[r][i] = exp(gamma_r - gamma_i):
+//   A = beta D o (K K^T) (strict),  T = (I + A)^-1,  L = scale D o (Q K^T) (inclusive)
+//   R = diag(beta) (V - diag(Gamma) K S),  E = T R          (= U - W S, GEMM-first)
+//   O = scale diag(Gamma) Q S + L E,        S' = Gamma_c S + (diag(f) K)^T E.
+// The state is held transposed: thread lane v owns row v of S^T (fp32 registers, the key
+// columns split over two warps); its bf16 copy sits in TMEM as the A operand of S^T K^T and
+// S^T Q^T, so every state-side product has the value index on the 128 MMA rows:
+//   MMA1  [K; Q] K^T          -> D1 [128 x 64]   (A = [K; Q] smem, B = K smem)
+//   MMA2  S^T K^T             -> X  [128 x 64]   (A = S^T TMEM,   B = K smem)
+//   MMA2b S^T (scale Gamma Q)^T -> O^T           (A = S^T TMEM,   B = scaled Q smem)
+//   MMA3  R^T T^T             -> E^T [128 x 64]  (A = R^T TMEM,   B = T smem)
+//   MMA4  (E^T diag f) K      -> dS^T [128x128]  (A TMEM,          B = K MN-major smem)
+//   MMA5  O^T += E^T L^T                         (A = E^T TMEM,   B = L smem)
+// The triangular solve runs in fp32 on the CUDA cores.  Two CTAs share an SM (about 104 KB
+// of shared memory and 256 TMEM columns each), so one CTA's MMAs, copies and waits overlap
+// the other's CUDA-core phases.  Rows past the end of a sequence are selected to zero in every
+// operand the threads build and zeroed in the K tile, so NaN padding never reaches an MMA.
+#include <cudaTypedefs.h>
+
+#include "gcl_internal.cuh"
+#include "tc_ptx.cuh"
+#include "tc_solve.cuh"
+
+namespace gcl {
+namespace {
+
+using namespace tc;
+constexpr int C = 64;
+constexpr int KD = 128;
+constexpr int VD = 128;
+constexpr int kThreads = 256;
+
+struct FusedParams {
+    const int32_t *cu, *chunk_offsets, *seq_order;
+    const float *g;
+    const __nv_bfloat16 *beta;
+    const float *h0;
+    __nv_bfloat16 *o;
+    float *ht, *h_save;
+    int32_t *status;
+    int64_t t_max, nt_max;
+    int32_t n_max, H;
+    float scale;
+};
+
+// Shared memory (offsets from a 1024-byte aligned base).
+struct FusedLayout {
+    static constexpr uint32_t oKQ = 0;                 // [2 key blocks][K rows 0..63 | Q rows 64..127][128 B]
+    static constexpr uint32_t oV = 32768;              // [2 value blocks][64 rows][128 B]
+    static constexpr uint32_t oT = oV + 16384;         // T bf16 [64 x 64], K-major, 128-byte swizzle
+    static constexpr uint32_t oL = oT + 8192;          // L bf16 [64 x 64]
+    static constexpr uint32_t oA = oL + 8192;          // solve: A fp32 [64][kSolveLD]
+    static constexpr uint32_t oTf = oA + 64 * kSolveLD * 4;   // solve: T fp32 (decay table before)
+    static constexpr uint32_t oX = oTf + 64 * kSolveLD * 4;   // solve scratch
+    static constexpr uint32_t oO = oA;                 // O staging [64][kOLD] bf16, after the solve
+    static constexpr uint32_t total = oX + 3 * 16 * kSolveLDX * 4;
+    static constexpr uint32_t bytes = total + 1024;    // + alignment slack
+};
+constexpr int kOLD = 136;                              // O staging row stride (bf16 elements)
+static_assert(64 * kOLD * 2 <= 2 * 64 * kSolveLD * 4, "O staging fits in the solve buffers");
+static_assert(FusedLayout::bytes <= 110 * 1024, "two CTAs per SM");
+
+// TMEM columns (256 per CTA).  Phases of one chunk reuse them:
+//   S^T bf16 [0, 64) until MMA2/2b complete, then D4 (dS^T) [0, 128)
+//   X [64, 128) until R is formed, then E^T (MMA3) [64, 128)
+//   O^T [128, 192): MMA2b, then MMA5 accumulates onto it
+//   D1 [192, 256) until the A / L epilogue; then R^T bf16 [192, 224), then E^T f bf16 [192, 224);
+//   E^T bf16 [224, 256)
+constexpr uint32_t cS = 0, cD4 = 0, cX = 64, cE32 = 64, cO = 128, cD1 = 192, cR = 192, cEF = 192,
+                   cEB = 224;
+constexpr uint32_t kTmemCols = 256;
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
+__device__ __forceinline__ float warp_incl_scan(float x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, FusedParams p) {
+    using Lay = FusedLayout;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t bar_kq, bar_v, bar_m1, bar_m3, bar_m45;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+    __shared__ float sG[C], sB[C], sGam[C], sF[C], s_carry;
+
+    if (status_blocks_cta(p.status)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int m = quarter * 32 + lane;                         // TMEM lane: value row v
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int h = blockIdx.x, z = blockIdx.y, H = p.H;
+    const int n = p.seq_order ? p.seq_order[z] : z;
+    if (n < 0 || n >= p.n_max) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t bos = p.cu[n], eos = p.cu[n + 1];
+    if (bos < 0 || eos < bos || eos > p.t_max) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int nch = (int)((eos - bos + C - 1) / C);
+    const int64_t row0 = p.chunk_offsets ? p.chunk_offsets[n] : 0;
+    if (p.h_save && nch > 0 && (row0 < 0 || row0 + nch > p.nt_max)) {
+        if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t KV = (int64_t)KD * VD;
+    const int64_t state_base = ((int64_t)n * H + h) * KV;
+    const int k0 = half * 64;                                  // this thread's key columns
+
+    // S^T row m, keys k0 .. k0 + 63 (S[k][v] at h0[k * V + v])
+    float S[64];
+    {
+        const float *src = p.h0 ? p.h0 + state_base + (int64_t)k0 * VD + m : nullptr;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) S[j] = src ? src[(int64_t)j * VD] : 0.f;
+    }
+    if (nch == 0) {                                            // zero-length slot: ht = h0
+        if (p.ht) {
+            float *dst = p.ht + state_base + (int64_t)k0 * VD + m;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) dst[(int64_t)j * VD] = S[j];
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        mbar_init(&bar_kq, 1);
+        mbar_init(&bar_v, 1);
+        mbar_init(&bar_m1, 1);
+        mbar_init(&bar_m3, 1);
+        mbar_init(&bar_m45, 1);
+        s_err = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t sbase = smem_u32(smem);
+
+    auto chunk_t0 = [&](int ic) -> int64_t { return bos + (int64_t)ic * C; };
+    auto chunk_len = [&](int ic) -> int {
+        const int64_t t0 = chunk_t0(ic);
+        return (int)(eos - t0 < C ? eos - t0 : C);
+    };
+    auto issue_kq = [&](int ic) {
+        const int t0 = (int)chunk_t0(ic);
+        mbar_arrive_expect_tx(&bar_kq, 32768);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(smem + Lay::oKQ + cb * 16384, &tm_k, cb * 64, h, t0, &bar_kq);
+            tma_load_3d(smem + Lay::oKQ + cb * 16384 + 8192, &tm_q, cb * 64, h, t0, &bar_kq);
+        }
+    };
+    auto issue_v = [&](int ic) {
+        const int t0 = (int)chunk_t0(ic);
+        mbar_arrive_expect_tx(&bar_v, 16384);
+        for (int cb = 0; cb < 2; ++cb)
+            tma_load_3d(smem + Lay::oV + cb * 8192, &tm_v, cb * 64, h, t0, &bar_v);
+    };
+    // S^T (bf16) of this thread's lane and keys into TMEM columns cS + half * 32 ..
+    auto store_state_bf16 = [&]() {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(S[q * 32 + 2 * j], S[q * 32 + 2 * j + 1]);
+            tmem_st16_b32(tmem + lane_off + cS + half * 32 + q * 16, pk);
+        }
+        tmem_st_wait();
+    };
+
+    store_state_bf16();
+    if (tid == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        issue_kq(0);
+        issue_v(0);
+    }
+    // gate and beta of the chunk, one row per thread 0..63, loaded one chunk ahead
+    float g_next = 0.f, b_next = 0.f;
+    if (tid < C) {
+        const int len0 = chunk_len(0);
+        const int64_t t = chunk_t0(0) + tid;
+        g_next = tid < len0 ? p.g[t * H + h] : 0.f;
+        b_next = tid < len0 ? __bfloat162float(p.beta[t * H + h]) : 0.f;
+    }
+
+    float *sAf = reinterpret_cast<float *>(smem + Lay::oA);
+    float *sTf = reinterpret_cast<float *>(smem + Lay::oTf);
+    float *sXf = reinterpret_cast<float *>(smem + Lay::oX);
+    __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + Lay::oO);
+
+    for (int ic = 0; ic < nch; ++ic) {
+        const int len = chunk_len(ic);
+        const int64_t t0 = chunk_t0(ic);
+        const uint32_t ph = ic & 1;
+        // ---- gates: gamma (inclusive cumsum), beta; rows past the end have g = beta = 0
+        {
+            float x = 0.f;
+            if (tid < C) x = warp_incl_scan(g_next);
+            if (tid == 31) s_carry = x;
+            __syncthreads();
+            if (tid >= 32 && tid < 64) x += s_carry;
+            if (tid < C) {
+                sG[tid] = x;
+                sB[tid] = b_next;
+            }
+            if (tid < C && ic + 1 < nch) {                    // next chunk's gates
+                const int len1 = chunk_len(ic + 1);
+                const int64_t t = chunk_t0(ic + 1) + tid;
+                g_next = tid < len1 ? p.g[t * H + h] : 0.f;
+                b_next = tid < len1 ? __bfloat162float(p.beta[t * H + h]) : 0.f;
+            }
+        }
+        // ---- the chunk's K, Q, V tiles; K rows past the end are zeroed (they enter MMA1 and
+        // MMA4 raw and may hold the next sequence or NaN padding)
+        mbar_wait(&bar_kq, ph, &s_err, 1);
+        mbar_wait(&bar_v, ph, &s_err, 2);
+        if (len < C) {
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            for (int e = tid; e < 2 * C * 8; e += kThreads) {
+                const int cb = e >> 9, r = (e >> 3) & 63, j = e & 7;
+                if (r >= len) *reinterpret_cast<uint4 *>(smem + Lay::oKQ + cb * 16384 + r * 128 + j * 16) = zero;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // MMA1: D1 = [K; Q] K^T (M = 128, N = 64, K = 128);  MMA2: X = S^T K^T (N = 64)
+            constexpr uint32_t id1 = idesc_bf16(128, 64);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                const uint64_t dkq = smem_desc(sbase + Lay::oKQ + off, 16, 1024, kSwizzle128B);
+                mma_bf16(tmem + cD1, dkq, dkq, id1, s > 0);
+            }
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                mma_bf16_ta(tmem + cX, tmem + cS + s * 8,
+                            smem_desc(sbase + Lay::oKQ + off, 16, 1024, kSwizzle128B), id1, s > 0);
+            }
+            mma_commit(&bar_m1);
+        }
+        // decay table D[r][c] = exp(gamma_r - gamma_c), c <= r (1 above; the exponent is
+        // selected, so no lane branches around the exponential), in the T buffer of the solve
+        {
+            const float gc = sG[C - 1];
+            if (tid < C) {
+                const float gr = sG[tid];
+                sGam[tid] = tid < len ? __expf(gr) : 0.f;
+                sF[tid] = tid < len ? __expf(gc - gr) : 0.f;
+            }
+            for (int e = tid; e < C * C / 4; e += kThreads) {
+                const int r = e >> 4, c = (e & 15) * 4;
+                const float gr = sG[r];
+                *reinterpret_cast<float4 *>(sTf + r * kSolveLD + c) = make_float4(
+                    __expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
+                    __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
+            }
+        }
+        __syncthreads();
+        mbar_wait(&bar_m1, ph, &s_err, 3);
+        tc_fence_after();
+        // ---- A (fp32, for the solve) and L (bf16) from D1; Q rows -> scale Gamma_r q_r (bf16)
+        {
+            float d[32];
+            tmem_ld16(tmem + lane_off + cD1 + half * 32, d);
+            tmem_ld16(tmem + lane_off + cD1 + half * 32 + 16, d + 16);
+            tmem_ld_wait();
+            const int c0 = half * 32;
+            if (quarter < 2) {                                 // A row r = m
+                const int r = m;
+                const float br = sB[r];
+                const bool live = r < len;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 dd = *reinterpret_cast<const float4 *>(sTf + r * kSolveLD + c0 + j);
+                    const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
+                    float a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) a[e] = (live && c0 + j + e < r) ? br * dv[e] * d[j + e] : 0.f;
+                    *reinterpret_cast<float4 *>(sAf + r * kSolveLD + c0 + j) = make_float4(a[0], a[1], a[2], a[3]);
+                }
+            } else {                                           // L row r = m - 64
+                const int r = m - C;
+                const bool live = r < len;
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 pk;
+                    uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = c0 + j + 2 * e;
+                        const float l0 = (live && c <= r) ? p.scale * sTf[r * kSolveLD + c] * d[j + 2 * e] : 0.f;
+                        const float l1 = (live && c + 1 <= r) ? p.scale * sTf[r * kSolveLD + c + 1] * d[j + 2 * e + 1] : 0.f;
+                        pw[e] = pack_bf16(l0, l1);
+                    }
+                    *reinterpret_cast<uint4 *>(smem + Lay::oL + sw128_offset(C, r, c0 + j)) = pk;
+                }
+            }
+            // Q rows 64..127 of both key blocks, 16 bytes per step, scaled in place
+            for (int e = tid; e < 2 * C * 8; e += kThreads) {
+                const int cb = e >> 9, r = (e >> 3) & 63, j = e & 7;
+                uint4 *ptr = reinterpret_cast<uint4 *>(smem + Lay::oKQ + cb * 16384 + 8192 + r * 128 + j * 16);
+                const float fq = r < len ? p.scale * sGam[r] : 0.f;
+                uint4 v = *ptr;
+                __nv_bfloat162 *pv = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f2 = __bfloat1622float2(pv[q]);
+                    // selected, not multiplied: padding rows may hold NaN
+                    pv[q] = __floats2bfloat162_rn(r < len ? fq * f2.x : 0.f, r < len ? fq * f2.y : 0.f);
+                }
+                *ptr = v;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {   // MMA2b: O^T = S^T (scale Gamma Q)^T (M = 128, N = 64, K = 128)
+            constexpr uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = (s >> 2) * 16384 + 8192 + (s & 3) * 32;
+                mma_bf16_ta(tmem + cO, tmem + cS + s * 8,
+                            smem_desc(sbase + Lay::oKQ + off, 16, 1024, kSwizzle128B), id, s > 0);
+            }
+        }
+        // ---- R^T[v][r] = beta_r (V[r][v] - Gamma_r X[v][r]) -> bf16 A operand in TMEM
+        {
+            float x[32];
+            tmem_ld16(tmem + lane_off + cX + half * 32, x);
+            tmem_ld16(tmem + lane_off + cX + half * 32 + 16, x + 16);
+            tmem_ld_wait();
+            const int v = m, vb = v >> 6, vc = v & 63;
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                float rr[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = half * 32 + j + e;
+                    const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                        smem + Lay::oV + vb * 8192 + sw128_offset(C, r, vc)));
+                    rr[e] = r < len ? sB[r] * (vv - sGam[r] * x[j + e]) : 0.f;
+                }
+                pk[j >> 1] = pack_bf16(rr[0], rr[1]);
+            }
+            tmem_st16_b32(tmem + lane_off + cR + half * 16, pk);
+            tmem_st_wait();
+        }
+        // ---- T = (I + A)^-1 (fp32), then bf16 rows (zeros above the diagonal)
+        solve_unit_lower64<kThreads>(sAf, sTf, sXf);
+        {
+            const int r = tid >> 2, cq = (tid & 3) * 16;
+#pragma unroll
+            for (int j = 0; j < 16; j += 8) {
+                uint4 pk;
+                uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = cq + j + 2 * e;
+                    pw[e] = pack_bf16(c <= r ? sTf[r * kSolveLD + c] : 0.f,
+                                      c + 1 <= r ? sTf[r * kSolveLD + c + 1] : 0.f);
+                }
+                *reinterpret_cast<uint4 *>(smem + Lay::oT + sw128_offset(C, r, cq + j)) = pk;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // MMA3: E^T = R^T T^T (M = 128, N = 64, K = 64)
+            constexpr uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16_ta(tmem + cE32, tmem + cR + s * 8,
+                            smem_desc(sbase + Lay::oT + s * 32, 16, 1024, kSwizzle128B), id, s > 0);
+            mma_commit(&bar_m3);
+            if (ic + 1 < nch) issue_v(ic + 1);              // the V tile is no longer read
+        }
+        mbar_wait(&bar_m3, ph, &s_err, 4);
+        tc_fence_after();
+        // ---- E^T -> bf16 (for O) and E^T diag(f) -> bf16 (for the state), TMEM A operands
+        {
+            float e32[32];
+            tmem_ld16(tmem + lane_off + cE32 + half * 32, e32);
+            tmem_ld16(tmem + lane_off + cE32 + half * 32 + 16, e32 + 16);
+            tmem_ld_wait();
+            uint32_t pe[16], pf[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const int r = half * 32 + j;
+                pe[j >> 1] = pack_bf16(e32[j], e32[j + 1]);
+                pf[j >> 1] = pack_bf16(sF[r] * e32[j], sF[r + 1] * e32[j + 1]);
+            }
+            tmem_st16_b32(tmem + lane_off + cEB + half * 16, pe);
+            tmem_st16_b32(tmem + lane_off + cEF + half * 16, pf);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // MMA4: dS^T = (E^T diag f) K (M = 128, N = 128 keys, K = 64 rows; K MN-major)
+            constexpr uint32_t id4 = idesc_bf16(128, 128, 0, 1);
+            const uint64_t dk = smem_desc(sbase + Lay::oKQ, 16384, 1024, kSwizzle128B);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16_ta(tmem + cD4, tmem + cEF + s * 8, dk + s * 128, id4, s > 0);
+            // MMA5: O^T += E^T L^T (N = 64, K = 64)
+            constexpr uint32_t id5 = idesc_bf16(128, 64);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16_ta(tmem + cO, tmem + cEB + s * 8,
+                            smem_desc(sbase + Lay::oL + s * 32, 16, 1024, kSwizzle128B), id5, 1);
+            mma_commit(&bar_m45);
+        }
+        mbar_wait(&bar_m45, ph, &s_err, 5);
+        tc_fence_after();
+        if (tid == 0 && ic + 1 < nch) issue_kq(ic + 1);       // K and Q are no longer read
+        // ---- state: h_save (the state entering the chunk), S <- Gamma_c S + dS; O staging
+        {
+            if (p.h_save) {
+                float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)k0 * VD + m;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) dst[(int64_t)j * VD] = S[j];
+            }
+            const float GC = __expf(sG[C - 1]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float d4[16];
+                tmem_ld16(tmem + lane_off + cD4 + k0 + q * 16, d4);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) S[q * 16 + j] = fmaf(GC, S[q * 16 + j], d4[j]);
+            }
+            float ov[32];
+            tmem_ld16(tmem + lane_off + cO + half * 32, ov);
+            tmem_ld16(tmem + lane_off + cO + half * 32 + 16, ov + 16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sO[(half * 32 + j) * kOLD + m] = __float2bfloat16_rn(ov[j]);
+        }
+        tc_fence_before();
+        __syncthreads();        // every read of D4 and O^T is done; O staged
+        tc_fence_after();
+        store_state_bf16();     // S^T bf16 for the next chunk's MMA2 (over D4's first columns)
+        if (p.o != nullptr) {   // valid rows of O, 16 threads x 16 bytes per row
+            const int rsub = tid >> 4, cc = (tid & 15) * 8;
+            for (int r = rsub; r < len; r += kThreads / 16) {
+                const uint4 val = *reinterpret_cast<const uint4 *>(sO + r * kOLD + cc);
+                *reinterpret_cast<uint4 *>(p.o + ((t0 + r) * H + h) * (int64_t)VD + cc) = val;
+            }
+        }
+        // a wait that gave up (s_err) ends every thread's loop at the same chunk
+        if (__syncthreads_or(*reinterpret_cast<volatile int *>(&s_err) != 0)) break;
+    }
+    if (s_err == 0 && p.ht) {
+        float *dst = p.ht + state_base + (int64_t)k0 * VD + m;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) dst[(int64_t)j * VD] = S[j];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (tid == 0 && s_err != 0) status_set(p.status, GCL_DEV_WAIT_TIMEOUT);
+}
+
+}  // namespace
+
+// Units (sequence slots x heads) from which the fused plan runs: enough CTAs for two per SM
+// over most of the GPU; fewer units keep the split plans (value-column slices per head).
+int fwd_fused_min_units() { return 64; }
+
+// A training forward (h_save) whose workspace holds the transition records runs the
+// transition plan instead: the backward's state-gradient sweep reads those records.
+bool fwd_tc_runs_fused(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max) {
+    if (variant != kGDN || (int64_t)n_max * H < fwd_fused_min_units() || n_max > 65535)
+        return false;                                           // (grid.y holds the slots)
+    return !(h_save && ws_bytes >= fwd_tc_t_workspace_bytes(nt_max, H));
+}
+
+cudaError_t launch_fwd_fused(const FwdParams &p, cudaStream_t s) {
+    const int H = p.H;
+    CUtensorMap mq, mk, mv;
+    const cuuint64_t dqk[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sqk[2] = {(cuuint64_t)KD * 2, (cuuint64_t)H * KD * 2};
+    const cuuint32_t b64[3] = {64, 1, 64};
+    const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
+    const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
+    if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    FusedParams fp{};
+    fp.cu = p.cu_seqlens;
+    fp.chunk_offsets = p.chunk_offsets;
+    fp.seq_order = p.seq_order;
+    fp.g = p.g;
+    fp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
+    fp.h0 = p.h0;
+    fp.o = static_cast<__nv_bfloat16 *>(p.o);
+    fp.ht = p.ht;
+    fp.h_save = p.h_save;
+    fp.status = p.dev_status;
+    fp.t_max = p.t_max;
+    fp.nt_max = p.nt_max;
+    fp.n_max = p.n_max;
+    fp.H = H;
+    fp.scale = p.scale;
+    cudaError_t e = cudaFuncSetAttribute(tc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)FusedLayout::bytes);
+    if (e != cudaSuccess) return e;
+    tc_fused_kernel<<<dim3(H, p.n_max), kThreads, FusedLayout::bytes, s>>>(mq, mk, mv, fp);
+    return cudaGetLastError();
+}
+
+}  // namespace gcl

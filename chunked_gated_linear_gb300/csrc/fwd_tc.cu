@@ -722,8 +722,20 @@ bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t w
     return (fwd_tc_prefers_transition(n_max, H) || h_save) && ws_bytes >= fwd_tc_t_workspace_bytes(nt_max, H);
 }
 
+int fwd_tc_plan(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max) {
+    if (fwd_tc_runs_fused(variant, n_max, H, h_save, ws_bytes, nt_max)) return GCL_PLAN_FUSED;
+    if (fwd_tc_runs_transition(variant, n_max, H, h_save, ws_bytes, nt_max)) {
+        const size_t rec = fwd_tc_t_workspace_bytes(nt_max, H);
+        const size_t seg = fwd_seg_workspace_bytes(nt_max, n_max, H);
+        return seg > 0 && ws_bytes >= rec + seg ? GCL_PLAN_SEGMENTED : GCL_PLAN_TRANSITION;
+    }
+    return GCL_PLAN_W_FORM;
+}
+
 cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
     const int H = p.H;
+    if (fwd_tc_runs_fused(variant, p.n_max, H, p.h_save != nullptr, p.workspace_bytes, p.nt_max))
+        return launch_fwd_fused(p, s);
     if (variant == kKDA) {   // KDA has the transition form only
         if (p.workspace_bytes < fwd_tc_t_workspace_bytes(p.nt_max, H)) return cudaErrorInvalidValue;
         return launch_fwd_tc_kda(p, fwd_tc_split(p.n_max, H), s);

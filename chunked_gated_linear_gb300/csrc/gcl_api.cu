@@ -82,6 +82,11 @@ static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
     if (!fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt)) return 0;
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->n_max <= 0) return 0;
+    // the fused plan keeps everything on chip; a training forward's fastest plan is the
+    // transition form (its records serve the backward), its least the fused plan
+    if (fwd_tc_runs_fused(variant, a->n_max, a->H, a->h_save != nullptr, 0, ntm) &&
+        (!a->h_save || !fastest))
+        return 0;
     // the transition form, with the segment buffers when the fastest plan is segmented
     const size_t seg = fastest ? fwd_seg_workspace_bytes(ntm, a->n_max, a->H) : 0;
     if (variant == kKDA) return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
@@ -105,13 +110,13 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
             return fail(GCL_ERR_INVALID_ARG,
                         "%s: chunk_indices and chunk_offsets are required for bf16 K=V=128", fn);
         const size_t need = fwd_ws(a, variant, false);
-        if (!a->workspace || a->workspace_bytes < need)
+        if (need > 0 && (!a->workspace || a->workspace_bytes < need))
             return fail(GCL_ERR_CAPACITY,
                         "%s: workspace of at least %zu bytes needed (%zu for the fastest "
                         "plan), %zu given",
                         fn, need, fwd_ws(a, variant, true),
                         a->workspace ? a->workspace_bytes : (size_t)0);
-        if (!aligned16(a->workspace))
+        if (a->workspace && !aligned16(a->workspace))
             return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
     }
     if ((a->o && !aligned16(a->o)) || (a->ht && !aligned16(a->ht)) ||
@@ -124,7 +129,7 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     p.o = a->o; p.ht = a->ht; p.h_save = a->h_save; p.dev_status = a->dev_status;
     p.workspace = nullptr;
     p.workspace_bytes = 0;
-    if (tc) align_ws(a->workspace, a->workspace_bytes, &p.workspace, &p.workspace_bytes);
+    if (tc && a->workspace) align_ws(a->workspace, a->workspace_bytes, &p.workspace, &p.workspace_bytes);
     p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V; p.bt = a->bt;
     p.nt_max = ntm;
     p.scale = a->scale;
@@ -339,6 +344,22 @@ size_t gcl_kda_fwd_workspace_bytes(const gcl_fwd_args *args) {
     if (!args) return 0;
     return fwd_ws(args, kKDA, true);
 }
+
+static int32_t fwd_plan(const gcl_fwd_args *a, int variant) {
+    if (!a) return -1;
+    if (check_common("plan", a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->t_max, a->n_max,
+                     a->H, a->K, a->V, a->bt, a->dtype) != GCL_OK)
+        return -1;
+    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt)) return GCL_PLAN_CUDA_CORES;
+    void *w = nullptr;
+    size_t wb = 0;
+    if (a->workspace) align_ws(a->workspace, a->workspace_bytes, &w, &wb);
+    return fwd_tc_plan(variant, a->n_max, a->H, a->h_save != nullptr, wb,
+                       gcl_nt_max(a->t_max, a->n_max, a->bt));
+}
+
+int32_t gcl_fwd_plan(const gcl_fwd_args *args) { return fwd_plan(args, kGDN); }
+int32_t gcl_kda_fwd_plan(const gcl_fwd_args *args) { return fwd_plan(args, kKDA); }
 
 int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t bt) {
     const int64_t ntm = gcl_nt_max(t_max, n_max, bt);

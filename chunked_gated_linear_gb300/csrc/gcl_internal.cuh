@@ -82,6 +82,14 @@ size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H);   // transition form
 // the buffers it needs after the transition records.
 int fwd_seg_count(int64_t nt_max, int n_max, int H);
 size_t fwd_seg_workspace_bytes(int64_t nt_max, int n_max, int H);
+// Fused plan (fwd_fused.cu): one CTA per (sequence, head) keeps the whole chunk pipeline on
+// chip and needs no workspace; GDN forwards with many units, except a training forward whose
+// workspace holds the transition records.
+int fwd_fused_min_units();
+bool fwd_tc_runs_fused(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max);
+cudaError_t launch_fwd_fused(const FwdParams &p, cudaStream_t s);
+// The plan a tensor-core forward runs for these sizes and this (aligned) workspace size.
+int fwd_tc_plan(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max);
 int fwd_tc_split(int n_max, int H);                        // value-column slices per head
 bool fwd_tc_prefers_transition(int n_max, int H);
 bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max);

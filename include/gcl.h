@@ -181,6 +181,10 @@ typedef struct gcl_fwd_args {
  * workspace of at least the minimum works; given sizes always select the same plan. */
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
 size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
+/* With many sequence-head units (n_max * H >= 64) a GDN forward runs the fused plan,
+ * which needs no workspace: without h_save both queries return 0 and workspace may be
+ * NULL; with h_save (a training forward) the fastest plan stays the transition form
+ * (its records serve the backward) and the fused plan runs with any smaller workspace. */
 
 /* Bytes of device workspace kda_chunk_fwd's fastest plan needs for these sizes (0
  * when the fp32 CUDA-core kernel serves them).  KDA on the tensor cores runs the
@@ -215,6 +219,30 @@ size_t gcl_kda_fwd_workspace_bytes(const gcl_fwd_args *args);
 int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t bt);
 
 /*
+ * The launch plan a forward with these arguments runs (workspace_bytes included), for
+ * callers that size graphs or count launches, and for tests:
+ *   GCL_PLAN_CUDA_CORES  one fp32 CUDA-core kernel (fp32 or fp16 inputs, K or V = 64, bt = 32)
+ *   GCL_PLAN_FUSED       one tensor-core kernel per (sequence, head), everything on chip
+ *                        (GDN, n_max * H >= 64: HA-NPU section 4, first tier)
+ *   GCL_PLAN_W_FORM      chunk prep (T, L records) + chain over value-column slices
+ *   GCL_PLAN_TRANSITION  chunk prep (affine chunk maps) + chain over value-column slices
+ *   GCL_PLAN_SEGMENTED   the transition plan with the segment-parallel chain
+ * Every plan but the last runs chunk_meta_build's output through one or two launches; the
+ * segmented plan adds the segment summaries, the scan and the segment outputs.  Returns -1
+ * for arguments the forward would reject on the host.  gcl_fwd_plan describes
+ * gdn_chunk_fwd, gcl_kda_fwd_plan kda_chunk_fwd.
+ */
+typedef enum {
+    GCL_PLAN_CUDA_CORES = 0,
+    GCL_PLAN_FUSED = 1,
+    GCL_PLAN_W_FORM = 2,
+    GCL_PLAN_TRANSITION = 3,
+    GCL_PLAN_SEGMENTED = 4
+} gcl_fwd_plan_t;
+int32_t gcl_fwd_plan(const gcl_fwd_args *args);
+int32_t gcl_kda_fwd_plan(const gcl_fwd_args *args);
+
+/*
  * gdn_chunk_fwd -- gated delta rule prefill: o and ht from q, k, v, g, beta, h0.
  * kda_chunk_fwd -- the same with the per-key-channel gate of KDA.
  *
@@ -227,7 +255,11 @@ int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t 
  *
  * Supported: bt in {32, 64} (the RFC's test matrix, "BT=32 and BT=64"); K, V in
  * {64, 128}; dtype GCL_F32, GCL_BF16 or GCL_F16.  GDN and KDA with bf16 inputs,
- * K = V = 128 and bt = 64 run on the tensor cores (tcgen05): a
+ * K = V = 128 and bt = 64 run on the tensor cores (tcgen05).  With many sequence-head
+ * units a GDN forward runs the fused plan: one CTA per (sequence, head)
+ * walks its chunks with every intermediate (the gate cumsum, A, T = (I + A)^-1, L, the
+ * GEMM-first R = diag(beta)(V - diag(Gamma) K S), E = T R, the state) on chip, so only
+ * the inputs are read and o, ht written (HA-NPU sections 4 and 5).  Otherwise a
  * chunk-parallel launch over chunk_indices forms per chunk either T = (I + A)^-1
  * and L (W form, GDN) or the chunk's transition S' = Gamma_c S + N S + B and
  * output O = Y S + Z (transition form; for KDA Gamma_c is a per-key-channel

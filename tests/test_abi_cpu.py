@@ -161,9 +161,20 @@ def test_host_errors_other_entry_points(lib):
     assert lib.gcl_causal_conv1d_bwd_workspace_bytes(ctypes.byref(gcl.ConvArgs(**{**cb, "W": 7}))) == 0
     # the no-allocation forward: sizes whose scratch exceeds the static array are rejected
     assert lib.gdn_chunk_fwd_noalloc(None, None) == INVALID
+    # (few sequence-head units: the plans with per-chunk scratch; many units run the fused
+    # plan, which needs none)
     big = gcl.FwdArgs(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake,
-                      t_max=1 << 22, n_max=64, H=64, K=128, V=128, bt=64, scale=1.0, dtype=1)
+                      t_max=1 << 22, n_max=2, H=16, K=128, V=128, bt=64, scale=1.0, dtype=1)
     assert lib.gcl_fwd_workspace_min_bytes(ctypes.byref(big)) > lib.gcl_noalloc_scratch_bytes()
+    assert lib.gcl_fwd_plan(ctypes.byref(big)) == 2                 # GCL_PLAN_W_FORM
+    many = gcl.FwdArgs(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake,
+                       t_max=1 << 16, n_max=64, H=16, K=128, V=128, bt=64, scale=1.0, dtype=1)
+    assert lib.gcl_fwd_plan(ctypes.byref(many)) == 1                # GCL_PLAN_FUSED
+    assert lib.gcl_fwd_workspace_bytes(ctypes.byref(many)) == 0
+    assert lib.gcl_fwd_workspace_min_bytes(ctypes.byref(many)) == 0
+    assert lib.gcl_kda_fwd_plan(ctypes.byref(many)) == 3            # KDA: transition form
+    assert lib.gcl_fwd_plan(ctypes.byref(gcl.FwdArgs(**{**{f: getattr(many, f) for f, _ in gcl.FwdArgs._fields_}, "dtype": 0}))) == 0
+    assert lib.gcl_fwd_plan(None) == -1
     assert lib.gdn_chunk_fwd_noalloc(ctypes.byref(big), None) == CAPACITY
     assert b"scratch" in lib.gcl_last_error()
     # the wait self-test needs a status word

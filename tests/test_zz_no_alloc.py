@@ -69,7 +69,9 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(label, B, T,
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    w = synth.standard_workloads()[3]                # N_max=64, T_max=65536, H=16: ~408 MiB
+    # one 65,536-token sequence of 16 heads: 16 units run the plans with per-chunk scratch,
+    # the least of which (W form) needs 400 MiB
+    w = synth.dense("noalloc-big", synth.GDN, "bf16", 1, 65536, 16, 128, 128, seed=79)
     x = synth.make_inputs(w)
     d = to_device(w, x)
     meta = Meta(w.t_max, w.n_max)
