@@ -67,3 +67,20 @@ def test_non_finite_values_fail():
     got[0, 0, 0] = np.nan
     with pytest.raises(AssertionError):
         check("o", got, ref, TOL, cu=CU)
+
+
+def test_reduction_gradients_take_the_wider_unit_bar():
+    """dg-like tensors: an absolute error at 2e-3 of the tensor's scale on every value passes
+    even where one unit's values are small; a zeroed value of a normal unit still fails."""
+    rng = np.random.default_rng(5)
+    cu = np.array([0, 1, 64, 200], dtype=np.int64)
+    ref = 0.05 * rng.standard_normal((200, 4))
+    ref[0, 2] = 0.01                                  # a one-token unit with a small value
+    got = ref + 1e-4 * rng.standard_normal(ref.shape)
+    got[0, 2] += 1.5e-4
+    check("dg", got, ref, TOL, cu=cu)
+    with pytest.raises(AssertionError):
+        check("o", got, ref, TOL, cu=cu)              # the plain unit bar would reject it
+    got[100, 1] = 0.0
+    with pytest.raises(AssertionError):
+        check("dg", got, ref, TOL, cu=cu)
