@@ -19,14 +19,16 @@
 // columns split over two warps); its bf16 copy sits in TMEM as the A operand of S^T K^T and
 // S^T Q^T, so every state-side product has the value index on the 128 MMA rows:
 //   MMA1  [K; Q] K^T          -> D1 [128 x 64]   (A = [K; Q] smem, B = K smem)
-//   MMA2  S^T K^T             -> X  [128 x 64]   (A = S^T TMEM,   B = K smem)
-//   MMA2b S^T (scale Gamma Q)^T -> O^T           (A = S^T TMEM,   B = scaled Q smem)
+//   MMA2  S^T [K; Q]^T        -> [X | Y] [128 x 128]  (A = S^T TMEM, B = [K; Q] smem)
+//         (Y is then scaled to scale diag(Gamma) Q S in place, giving O^T's first term)
 //   MMA3  R^T T^T             -> E^T [128 x 64]  (A = R^T TMEM,   B = T smem)
 //   MMA4  (E^T diag f) K      -> dS^T [128x128]  (A TMEM,          B = K MN-major smem)
 //   MMA5  O^T += E^T L^T                         (A = E^T TMEM,   B = L smem)
-// The triangular solve runs in fp32 on the CUDA cores.  Two CTAs share an SM (about 104 KB
-// of shared memory and 256 TMEM columns each), so one CTA's MMAs, copies and waits overlap
-// the other's CUDA-core phases.  Rows past the end of a sequence are selected to zero in every
+// The triangular solve runs in fp32 on the CUDA cores of warps 0..3 while warps 4..7 form R;
+// one lane of warp 4 issues every copy and MMA, and warp 5 forms the next chunk's gate vectors
+// (double-buffered) after its share of R.  Two CTAs share an SM (about 104 KB of shared memory
+// and 256 TMEM columns each), so one CTA's MMAs, copies and waits overlap the other's CUDA-core
+// phases.  Rows past the end of a sequence are selected to zero in every
 // operand the threads build and zeroed in the K tile, so NaN padding never reaches an MMA.
 #include <cudaTypedefs.h>
 
@@ -42,6 +44,8 @@ constexpr int C = 64;
 constexpr int KD = 128;
 constexpr int VD = 128;
 constexpr int kThreads = 256;
+constexpr int kIssuer = 128;      // lane 0 of warp 4
+constexpr int kGateWarp = 5;      // forms the gate vectors, one chunk ahead
 
 struct FusedParams {
     const int32_t *cu, *chunk_offsets, *seq_order;
@@ -74,9 +78,10 @@ static_assert(64 * kOLD * 2 <= 2 * 64 * kSolveLD * 4, "O staging fits in the sol
 static_assert(FusedLayout::bytes <= 110 * 1024, "two CTAs per SM");
 
 // TMEM columns (256 per CTA).  Phases of one chunk reuse them:
-//   S^T bf16 [0, 64) until MMA2/2b complete, then D4 (dS^T) [0, 128)
-//   X [64, 128) until R is formed, then E^T (MMA3) [64, 128)
-//   O^T [128, 192): MMA2b, then MMA5 accumulates onto it
+//   S^T bf16 [0, 64) until MMA2 completes; then the fp32 state slice of warps 0..3 while they
+//   run the solve; then D4 (dS^T) [0, 128)
+//   X = (K S)^T [64, 128) until R is formed, then E^T (MMA3) [64, 128)
+//   Y = (Q S)^T [128, 192): MMA2, scaled in place, then MMA5 accumulates onto it (O^T)
 //   D1 [192, 256) until the A / L epilogue; then R^T bf16 [192, 224), then E^T f bf16 [192, 224);
 //   E^T bf16 [224, 256)
 constexpr uint32_t cS = 0, cD4 = 0, cX = 64, cE32 = 64, cO = 128, cD1 = 192, cR = 192, cEF = 192,
@@ -104,10 +109,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     using Lay = FusedLayout;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t bar_kq, bar_v, bar_m1, bar_m3, bar_m45;
+    __shared__ uint64_t bar_kq, bar_v, bar_m1, bar_m2, bar_m3, bar_m45;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
-    __shared__ float sG[C], sB[C], sGam[C], sF[C], s_carry;
+    // per-chunk gate vectors, double-buffered by chunk parity (the next chunk's are formed
+    // while the current chunk's are still read)
+    __shared__ __align__(16) float sGb[2][C], sBb[2][C], sGamb[2][C], sFb[2][C], sF2b[2][4 * C];
 
     if (status_blocks_cta(p.status)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -155,6 +162,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&bar_kq, 1);
         mbar_init(&bar_v, 1);
         mbar_init(&bar_m1, 1);
+        mbar_init(&bar_m2, 1);
         mbar_init(&bar_m3, 1);
         mbar_init(&bar_m45, 1);
         s_err = 0;
@@ -202,20 +210,64 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
 
     store_state_bf16();
-    if (tid == 0) {
+    // one thread issues every copy and MMA: a lane of warp 4, whose warps form R while
+    // warps 0..3 run the triangular solve (the longer of the two)
+    const bool issuer = tid == kIssuer;
+    if (issuer) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         issue_kq(0);
         issue_v(0);
     }
-    // gate and beta of the chunk, one row per thread 0..63, loaded one chunk ahead
-    float g_next = 0.f, b_next = 0.f;
-    if (tid < C) {
-        const int len0 = chunk_len(0);
-        const int64_t t = chunk_t0(0) + tid;
-        g_next = tid < len0 ? p.g[t * H + h] : 0.f;
-        b_next = tid < len0 ? __bfloat162float(p.beta[t * H + h]) : 0.f;
+    // Gates and betas, rows 2l and 2l + 1 in lane l of warp kGateWarp, loaded one chunk ahead;
+    // that warp forms each chunk's gate vectors one chunk ahead too (after its share of R),
+    // so no barrier of the chunk waits for them.
+    float g_next[2] = {0.f, 0.f}, b_next[2] = {0.f, 0.f};
+    auto load_gates = [&](int ic) {
+        const int len1 = chunk_len(ic);
+        const int64_t t = chunk_t0(ic);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * lane + e;
+            g_next[e] = r < len1 ? p.g[(t + r) * H + h] : 0.f;
+            b_next[e] = r < len1 ? __bfloat162float(p.beta[(t + r) * H + h]) : 0.f;
+        }
+    };
+    // gamma (inclusive cumsum; rows past the end have g = 0), beta, Gamma = exp(gamma),
+    // f = exp(gamma_c - gamma), and the cross-block decay factors
+    // F2[b][c] = exp(gamma_{16 b} - gamma_c) for c < 16 b, of chunk ic into buffer ic & 1
+    auto form_gates = [&](int ic) {
+        const int len1 = chunk_len(ic), gb = ic & 1;
+        float *G = sGb[gb];
+        const float a1 = g_next[0] + g_next[1];
+        const float x = warp_incl_scan(a1);                    // through row 2l + 1
+        const float g1 = x, g0 = x - g_next[1];
+        const float gc = __shfl_sync(0xffffffffu, x, 31);
+        const int r0 = 2 * lane;
+        G[r0] = g0;
+        G[r0 + 1] = g1;
+        sBb[gb][r0] = b_next[0];
+        sBb[gb][r0 + 1] = b_next[1];
+        sGamb[gb][r0] = r0 < len1 ? __expf(g0) : 0.f;
+        sGamb[gb][r0 + 1] = r0 + 1 < len1 ? __expf(g1) : 0.f;
+        sFb[gb][r0] = r0 < len1 ? __expf(gc - g0) : 0.f;
+        sFb[gb][r0 + 1] = r0 + 1 < len1 ? __expf(gc - g1) : 0.f;
+        __syncwarp();
+#pragma unroll
+        for (int b = 1; b < 4; ++b) {
+            const float rho = G[16 * b];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = r0 + e;
+                sF2b[gb][b * C + c] = __expf(c < 16 * b ? rho - G[c] : 0.f);
+            }
+        }
+    };
+    if (warp == kGateWarp) {
+        load_gates(0);
+        form_gates(0);
+        if (nch > 1) load_gates(1);
     }
 
     float *sAf = reinterpret_cast<float *>(smem + Lay::oA);
@@ -227,24 +279,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int len = chunk_len(ic);
         const int64_t t0 = chunk_t0(ic);
         const uint32_t ph = ic & 1;
-        // ---- gates: gamma (inclusive cumsum), beta; rows past the end have g = beta = 0
-        {
-            float x = 0.f;
-            if (tid < C) x = warp_incl_scan(g_next);
-            if (tid == 31) s_carry = x;
-            __syncthreads();
-            if (tid >= 32 && tid < 64) x += s_carry;
-            if (tid < C) {
-                sG[tid] = x;
-                sB[tid] = b_next;
-            }
-            if (tid < C && ic + 1 < nch) {                    // next chunk's gates
-                const int len1 = chunk_len(ic + 1);
-                const int64_t t = chunk_t0(ic + 1) + tid;
-                g_next = tid < len1 ? p.g[t * H + h] : 0.f;
-                b_next = tid < len1 ? __bfloat162float(p.beta[t * H + h]) : 0.f;
-            }
-        }
+        const int gb = ic & 1;
+        const float *sG = sGb[gb], *sB = sBb[gb], *sGam = sGamb[gb], *sF = sFb[gb], *sF2 = sF2b[gb];
         // ---- the chunk's K, Q, V tiles; K rows past the end are zeroed (they enter MMA1 and
         // MMA4 raw and may hold the next sequence or NaN padding)
         mbar_wait(&bar_kq, ph, &s_err, 1);
@@ -260,8 +296,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {
-            // MMA1: D1 = [K; Q] K^T (M = 128, N = 64, K = 128);  MMA2: X = S^T K^T (N = 64)
+        if (issuer) {
+            // MMA1: D1 = [K; Q] K^T (M = 128, N = 64, K = 128)
             constexpr uint32_t id1 = idesc_bf16(128, 64);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -269,129 +305,89 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint64_t dkq = smem_desc(sbase + Lay::oKQ + off, 16, 1024, kSwizzle128B);
                 mma_bf16(tmem + cD1, dkq, dkq, id1, s > 0);
             }
+            mma_commit(&bar_m1);
+            // MMA2: [X | Y] = S^T [K; Q]^T (N = 128): X = (K S)^T, Y = (Q S)^T
+            constexpr uint32_t id2 = idesc_bf16(128, 128);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
                 mma_bf16_ta(tmem + cX, tmem + cS + s * 8,
-                            smem_desc(sbase + Lay::oKQ + off, 16, 1024, kSwizzle128B), id1, s > 0);
+                            smem_desc(sbase + Lay::oKQ + off, 16, 1024, kSwizzle128B), id2, s > 0);
             }
-            mma_commit(&bar_m1);
+            mma_commit(&bar_m2);
         }
-        // decay table D[r][c] = exp(gamma_r - gamma_c), c <= r (1 above; the exponent is
-        // selected, so no lane branches around the exponential), in the T buffer of the solve
-        {
-            const float gc = sG[C - 1];
-            if (tid < C) {
-                const float gr = sG[tid];
-                sGam[tid] = tid < len ? __expf(gr) : 0.f;
-                sF[tid] = tid < len ? __expf(gc - gr) : 0.f;
-            }
-            for (int e = tid; e < C * C / 4; e += kThreads) {
-                const int r = e >> 4, c = (e & 15) * 4;
-                const float gr = sG[r];
-                *reinterpret_cast<float4 *>(sTf + r * kSolveLD + c) = make_float4(
-                    __expf(c <= r ? gr - sG[c] : 0.f), __expf(c + 1 <= r ? gr - sG[c + 1] : 0.f),
-                    __expf(c + 2 <= r ? gr - sG[c + 2] : 0.f), __expf(c + 3 <= r ? gr - sG[c + 3] : 0.f));
-            }
-        }
-        __syncthreads();
         mbar_wait(&bar_m1, ph, &s_err, 3);
         tc_fence_after();
-        // ---- A (fp32, for the solve) and L (bf16) from D1; Q rows -> scale Gamma_r q_r (bf16)
+        // ---- A (fp32, for the solve) and L (bf16) from D1, with the decay
+        // D[r][c] = exp(gamma_r - gamma_c): inside a 16-row block one exponential per pair; for
+        // c in an earlier block, exp(gamma_r - gamma_{16 b}) F2[b][c] (both factors <= 1, so
+        // nothing overflows; their product underflows only where the decay itself does).
         {
-            float d[32];
-            tmem_ld16(tmem + lane_off + cD1 + half * 32, d);
-            tmem_ld16(tmem + lane_off + cD1 + half * 32 + 16, d + 16);
-            tmem_ld_wait();
-            const int c0 = half * 32;
-            if (quarter < 2) {                                 // A row r = m
-                const int r = m;
-                const float br = sB[r];
-                const bool live = r < len;
+            const int r = m & 63, br = r >> 4;
+            const bool live = r < len;
+            const float gr = sG[r];
+            const float f1 = __expf(gr - sG[16 * br]);
+            const float rowf = quarter < 2 ? sB[r] : p.scale;      // beta_r (A) or scale (L)
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 dd = *reinterpret_cast<const float4 *>(sTf + r * kSolveLD + c0 + j);
-                    const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
-                    float a[4];
+            for (int cb = 0; cb < 2; ++cb) {          // the thread's two 16-column blocks
+                const int c0 = half * 32 + cb * 16, bc = c0 >> 4;
+                float d[16];
+                tmem_ld16(tmem + lane_off + cD1 + c0, d);
+                tmem_ld_wait();
+                float dec[16];
+                if (bc < br) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) a[e] = (live && c0 + j + e < r) ? br * dv[e] * d[j + e] : 0.f;
-                    *reinterpret_cast<float4 *>(sAf + r * kSolveLD + c0 + j) = make_float4(a[0], a[1], a[2], a[3]);
+                    for (int j = 0; j < 16; ++j) dec[j] = f1 * sF2[br * C + c0 + j];
+                } else if (bc == br) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dec[j] = __expf(c0 + j <= r ? gr - sG[c0 + j] : 0.f);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dec[j] = 0.f;
                 }
-            } else {                                           // L row r = m - 64
-                const int r = m - C;
-                const bool live = r < len;
+                if (quarter < 2) {                             // A row r = m: strictly lower
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 pk;
-                    uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
+                    for (int j = 0; j < 16; j += 4) {
+                        float a[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = c0 + j + 2 * e;
-                        const float l0 = (live && c <= r) ? p.scale * sTf[r * kSolveLD + c] * d[j + 2 * e] : 0.f;
-                        const float l1 = (live && c + 1 <= r) ? p.scale * sTf[r * kSolveLD + c + 1] * d[j + 2 * e + 1] : 0.f;
-                        pw[e] = pack_bf16(l0, l1);
+                        for (int e = 0; e < 4; ++e)
+                            a[e] = (live && c0 + j + e < r) ? rowf * dec[j + e] * d[j + e] : 0.f;
+                        *reinterpret_cast<float4 *>(sAf + r * kSolveLD + c0 + j) = make_float4(a[0], a[1], a[2], a[3]);
                     }
-                    *reinterpret_cast<uint4 *>(smem + Lay::oL + sw128_offset(C, r, c0 + j)) = pk;
-                }
-            }
-            // Q rows 64..127 of both key blocks, 16 bytes per step, scaled in place
-            for (int e = tid; e < 2 * C * 8; e += kThreads) {
-                const int cb = e >> 9, r = (e >> 3) & 63, j = e & 7;
-                uint4 *ptr = reinterpret_cast<uint4 *>(smem + Lay::oKQ + cb * 16384 + 8192 + r * 128 + j * 16);
-                const float fq = r < len ? p.scale * sGam[r] : 0.f;
-                uint4 v = *ptr;
-                __nv_bfloat162 *pv = reinterpret_cast<__nv_bfloat162 *>(&v);
+                } else {                                       // L row r = m - 64: inclusive
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 f2 = __bfloat1622float2(pv[q]);
-                    // selected, not multiplied: padding rows may hold NaN
-                    pv[q] = __floats2bfloat162_rn(r < len ? fq * f2.x : 0.f, r < len ? fq * f2.y : 0.f);
+                    for (int j = 0; j < 16; j += 8) {
+                        uint4 pk;
+                        uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = c0 + j + 2 * e;
+                            const float l0 = (live && c <= r) ? rowf * dec[j + 2 * e] * d[j + 2 * e] : 0.f;
+                            const float l1 = (live && c + 1 <= r) ? rowf * dec[j + 2 * e + 1] * d[j + 2 * e + 1] : 0.f;
+                            pw[e] = pack_bf16(l0, l1);
+                        }
+                        *reinterpret_cast<uint4 *>(smem + Lay::oL + sw128_offset(C, r, c0 + j)) = pk;
+                    }
                 }
-                *ptr = v;
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {   // MMA2b: O^T = S^T (scale Gamma Q)^T (M = 128, N = 64, K = 128)
-            constexpr uint32_t id = idesc_bf16(128, 64);
+        if (warp < 4) {
+            // ---- T = (I + A)^-1 (fp32) on warps 0..3, then bf16 rows (zeros above the diagonal)
+            // the state slice of warps 0..3 waits in TMEM columns [0, 64) (its bf16 copy there
+            // is no longer read once MMA2 completes), so the solve has the registers
+            mbar_wait(&bar_m2, ph, &s_err, 6);
+            tc_fence_after();
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = (s >> 2) * 16384 + 8192 + (s & 3) * 32;
-                mma_bf16_ta(tmem + cO, tmem + cS + s * 8,
-                            smem_desc(sbase + Lay::oKQ + off, 16, 1024, kSwizzle128B), id, s > 0);
-            }
-        }
-        // ---- R^T[v][r] = beta_r (V[r][v] - Gamma_r X[v][r]) -> bf16 A operand in TMEM
-        {
-            float x[32];
-            tmem_ld16(tmem + lane_off + cX + half * 32, x);
-            tmem_ld16(tmem + lane_off + cX + half * 32 + 16, x + 16);
-            tmem_ld_wait();
-            const int v = m, vb = v >> 6, vc = v & 63;
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                float rr[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = half * 32 + j + e;
-                    const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        smem + Lay::oV + vb * 8192 + sw128_offset(C, r, vc)));
-                    rr[e] = r < len ? sB[r] * (vv - sGam[r] * x[j + e]) : 0.f;
-                }
-                pk[j >> 1] = pack_bf16(rr[0], rr[1]);
-            }
-            tmem_st16_b32(tmem + lane_off + cR + half * 16, pk);
+            for (int q = 0; q < 4; ++q) tmem_st16(tmem + lane_off + cS + q * 16, S + q * 16);
             tmem_st_wait();
-        }
-        // ---- T = (I + A)^-1 (fp32), then bf16 rows (zeros above the diagonal)
-        solve_unit_lower64<kThreads>(sAf, sTf, sXf);
-        {
-            const int r = tid >> 2, cq = (tid & 3) * 16;
+            solve_unit_lower64<128, 1>(sAf, sTf, sXf);
+            const int r = tid >> 1, cq = (tid & 1) * 32;
 #pragma unroll
-            for (int j = 0; j < 16; j += 8) {
+            for (int j = 0; j < 32; j += 8) {
                 uint4 pk;
                 uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
 #pragma unroll
@@ -402,12 +398,52 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 *reinterpret_cast<uint4 *>(smem + Lay::oT + sw128_offset(C, r, cq + j)) = pk;
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + cS + q * 16, S + q * 16);
+            tmem_ld_wait();
+        } else {
+            // ---- R^T[v][r] = beta_r (V[r][v] - Gamma_r X[v][r]) -> bf16 A operand in TMEM,
+            // lane v = m, all 64 rows r, on warps 4..7
+            mbar_wait(&bar_m2, ph, &s_err, 6);
+            tc_fence_after();
+            const int v = m, vb = v >> 6, vc = v & 63;
+            const uint8_t *vcol = smem + Lay::oV + vb * 8192 + (vc & 7) * 2;
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                float x[16];
+                tmem_ld16(tmem + lane_off + cX + hh * 16, x);
+                tmem_ld_wait();
+                uint32_t pk[8];
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const int r0 = hh * 16 + j;
+                    const float4 b4 = *reinterpret_cast<const float4 *>(sB + r0);
+                    const float4 g4 = *reinterpret_cast<const float4 *>(sGam + r0);
+                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, gg[4] = {g4.x, g4.y, g4.z, g4.w};
+                    float rr[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = r0 + e;
+                        const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                            vcol + (r >> 3) * 1024 + (r & 7) * 128 + ((((vc >> 3) ^ (r & 7))) << 4)));
+                        rr[e] = r < len ? bb[e] * (vv - gg[e] * x[j + e]) : 0.f;
+                    }
+                    pk[j >> 1] = pack_bf16(rr[0], rr[1]);
+                    pk[(j >> 1) + 1] = pack_bf16(rr[2], rr[3]);
+                }
+                tmem_st8_b32(tmem + lane_off + cR + hh * 8, pk);
+            }
+            tmem_st_wait();
+            if (warp == kGateWarp && ic + 1 < nch) {      // the next chunk's gate vectors
+                form_gates(ic + 1);
+                if (ic + 2 < nch) load_gates(ic + 2);
+            }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {
+        if (issuer) {
             // MMA3: E^T = R^T T^T (M = 128, N = 64, K = 64)
             constexpr uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
@@ -420,26 +456,42 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_wait(&bar_m3, ph, &s_err, 4);
         tc_fence_after();
         // ---- E^T -> bf16 (for O) and E^T diag(f) -> bf16 (for the state), TMEM A operands
-        {
-            float e32[32];
-            tmem_ld16(tmem + lane_off + cE32 + half * 32, e32);
-            tmem_ld16(tmem + lane_off + cE32 + half * 32 + 16, e32 + 16);
-            tmem_ld_wait();
-            uint32_t pe[16], pf[16];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const int r = half * 32 + j;
-                pe[j >> 1] = pack_bf16(e32[j], e32[j + 1]);
-                pf[j >> 1] = pack_bf16(sF[r] * e32[j], sF[r + 1] * e32[j + 1]);
+        for (int hh = 0; hh < 2; ++hh) {
+            const int c0 = half * 32 + hh * 16;
+            float e16[16];
+            tmem_ld16(tmem + lane_off + cE32 + c0, e16);
+            tmem_ld_wait();
+            uint32_t pe[8], pf[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 f4 = *reinterpret_cast<const float4 *>(sF + c0 + j);
+                pe[j >> 1] = pack_bf16(e16[j], e16[j + 1]);
+                pe[(j >> 1) + 1] = pack_bf16(e16[j + 2], e16[j + 3]);
+                pf[j >> 1] = pack_bf16(f4.x * e16[j], f4.y * e16[j + 1]);
+                pf[(j >> 1) + 1] = pack_bf16(f4.z * e16[j + 2], f4.w * e16[j + 3]);
             }
-            tmem_st16_b32(tmem + lane_off + cEB + half * 16, pe);
-            tmem_st16_b32(tmem + lane_off + cEF + half * 16, pf);
-            tmem_st_wait();
+            tmem_st8_b32(tmem + lane_off + cEB + (c0 >> 1), pe);
+            tmem_st8_b32(tmem + lane_off + cEF + (c0 >> 1), pf);
+            // Y -> scale Gamma_r Y (O^T before MMA5 adds E^T L^T); rows past the end selected to 0
+            float y16[16];
+            tmem_ld16(tmem + lane_off + cO + c0, y16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 g4 = *reinterpret_cast<const float4 *>(sGam + c0 + j);
+                const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    y16[j + e] = c0 + j + e < len ? p.scale * gg[e] * y16[j + e] : 0.f;
+            }
+            tmem_st16(tmem + lane_off + cO + c0, y16);
         }
+        tmem_st_wait();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {
+        if (issuer) {
             // MMA4: dS^T = (E^T diag f) K (M = 128, N = 128 keys, K = 64 rows; K MN-major)
             constexpr uint32_t id4 = idesc_bf16(128, 128, 0, 1);
             const uint64_t dk = smem_desc(sbase + Lay::oKQ, 16384, 1024, kSwizzle128B);
@@ -455,7 +507,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mbar_wait(&bar_m45, ph, &s_err, 5);
         tc_fence_after();
-        if (tid == 0 && ic + 1 < nch) issue_kq(ic + 1);       // K and Q are no longer read
+        if (issuer && ic + 1 < nch) issue_kq(ic + 1);       // K and Q are no longer read
         // ---- state: h_save (the state entering the chunk), S <- Gamma_c S + dS; O staging
         {
             if (p.h_save) {
@@ -472,12 +524,15 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 16; ++j) S[q * 16 + j] = fmaf(GC, S[q * 16 + j], d4[j]);
             }
-            float ov[32];
-            tmem_ld16(tmem + lane_off + cO + half * 32, ov);
-            tmem_ld16(tmem + lane_off + cO + half * 32 + 16, ov + 16);
-            tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sO[(half * 32 + j) * kOLD + m] = __float2bfloat16_rn(ov[j]);
+            for (int hh = 0; hh < 2; ++hh) {
+                float ov[16];
+                tmem_ld16(tmem + lane_off + cO + half * 32 + hh * 16, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    sO[(half * 32 + hh * 16 + j) * kOLD + m] = __float2bfloat16_rn(ov[j]);
+            }
         }
         tc_fence_before();
         __syncthreads();        // every read of D4 and O^T is done; O staged

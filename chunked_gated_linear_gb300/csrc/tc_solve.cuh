@@ -22,10 +22,21 @@ constexpr int kSolveLD = 68;
 constexpr int kSolveLDX = 20;
 constexpr int kSolveFloats = 2 * 64 * kSolveLD + 3 * 16 * kSolveLDX;   // A, T, X
 
-// All NT threads of the block must call it (it contains block barriers); NT is 128 or 256.
-template <int NT>
+// Barrier among the solving threads: the whole block (BarId < 0), or threads 0 .. NT-1 on the
+// named barrier BarId (the rest of the block does other work meanwhile).
+template <int NT, int BarId>
+__device__ __forceinline__ void solve_barrier() {
+    if constexpr (BarId < 0) {
+        __syncthreads();
+    } else {
+        asm volatile("bar.sync %0, %1;" ::"n"(BarId), "n"(NT) : "memory");
+    }
+}
+
+// Threads 0 .. NT-1 call it (NT is 128 or 256); with BarId < 0 they are the whole block.
+template <int NT, int BarId = -1>
 __device__ __forceinline__ void solve_unit_lower64(const float *sA, float *sT, float *sX) {
-    static_assert(NT == 128 || NT == 256, "block of 128 or 256 threads");
+    static_assert(NT == 128 || NT == 256, "128 or 256 solving threads");
     const int tid = threadIdx.x;
     if (tid < 64) {   // ---- diagonal blocks: thread (block, column jj), four partial sums
         const int o = (tid >> 4) * 16, jj = tid & 15;
@@ -44,31 +55,36 @@ __device__ __forceinline__ void solve_unit_lower64(const float *sA, float *sT, f
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(o + r) * kSolveLD + o + jj] = x[r];
     }
-    __syncthreads();
+    solve_barrier<NT, BarId>();
     // ---- off-diagonal blocks.  Strip s of level d: block blk (bi = d + blk, bj = blk),
-    // column quad cq, row rr (rows fastest, so 8 consecutive lanes read 8 distinct rows).
+    // column quad cq, row rr (rows fastest, so 8 consecutive lanes read 8 distinct rows).  The
+    // level loop is unrolled, so every dot product has a compile-time length (16 d terms) and
+    // its loads are issued ahead of the FMAs; the summation order is the plain one.
+#pragma unroll
     for (int d = 1; d < 4; ++d) {
         const int nstrip = (4 - d) * 64;
         for (int s = tid; s < nstrip; s += NT) {
             const int blk = s >> 6, cq = (s >> 4) & 3, rr = s & 15;
             const int bi = d + blk, bj = blk;
-            const float *arow = sA + (bi * 16 + rr) * kSolveLD;
+            const float *arow = sA + (bi * 16 + rr) * kSolveLD + bj * 16;
+            const float *tcol = sT + bj * 16 * kSolveLD + bj * 16 + cq * 4;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int m = bj * 16; m < bi * 16; m += 4) {
-                const float4 a = *reinterpret_cast<const float4 *>(arow + m);
+#pragma unroll
+            for (int t = 0; t < 4 * d; ++t) {
+                const float4 a = *reinterpret_cast<const float4 *>(arow + 4 * t);
                 const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float4 t = *reinterpret_cast<const float4 *>(sT + (m + e) * kSolveLD + bj * 16 + cq * 4);
-                    acc.x = fmaf(av[e], t.x, acc.x);
-                    acc.y = fmaf(av[e], t.y, acc.y);
-                    acc.z = fmaf(av[e], t.z, acc.z);
-                    acc.w = fmaf(av[e], t.w, acc.w);
+                    const float4 tv = *reinterpret_cast<const float4 *>(tcol + (4 * t + e) * kSolveLD);
+                    acc.x = fmaf(av[e], tv.x, acc.x);
+                    acc.y = fmaf(av[e], tv.y, acc.y);
+                    acc.z = fmaf(av[e], tv.z, acc.z);
+                    acc.w = fmaf(av[e], tv.w, acc.w);
                 }
             }
             *reinterpret_cast<float4 *>(sX + (blk * 16 + rr) * kSolveLDX + cq * 4) = acc;
         }
-        __syncthreads();
+        solve_barrier<NT, BarId>();
         for (int s = tid; s < nstrip; s += NT) {
             const int blk = s >> 6, cq = (s >> 4) & 3, rr = s & 15;
             const int bi = d + blk, bj = blk;
@@ -90,7 +106,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *sA, float *sT, f
             *reinterpret_cast<float4 *>(sT + (bi * 16 + rr) * kSolveLD + bj * 16 + cq * 4) =
                 make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
-        __syncthreads();
+        solve_barrier<NT, BarId>();
     }
 }
 
