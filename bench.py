@@ -2,11 +2,20 @@
 """GDN/KDA chunk prefill throughput on GB300: tokens/s and fraction of roofline.
 
 One step = the whole hot path over one batch: chunk_meta_build (device
-metadata from cu_seqlens) followed by the fused chunk forward (and, for the
+metadata from cu_seqlens) followed by the chunk forward (and, for the
 forward+backward workload, the backward).  Inputs are seeded synthetic data
 already resident in HBM.  Several input sets are rotated so that the bytes one
 step touches were evicted from L2 by the steps in between (total footprint
 > 3x L2); no explicit flush is needed.
+
+The headline workload is the varlen prefill (32 sequences of 1..2048 tokens in
+a capacity of 64 slots and 65,536 tokens, 16 heads, d = 128): each input set is
+one of the workload's seeded layouts, every set's step is captured once in a
+CUDA graph, and the timed steps replay the graphs in rotation (graph replay,
+fixed grids).  Beside it: the same steps launched directly, and
+graph-update-replay (the next layout's live rows copied into the captured
+buffers, then a replay), each with p50 and p95.  The other standard
+configurations follow under per_config, each with its own roofline.
 
 Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica of the workload (weak scaling: the (sequence, head) units
@@ -34,7 +43,10 @@ sys.path.insert(0, ROOT)
 
 from chunked_gated_linear_gb300 import synth  # noqa: E402
 
-DEFAULT_WORKLOAD = "gdn_fwd_bf16_T4096_H16_d128"
+DEFAULT_WORKLOAD = "gdn_varlen_bf16_N32_Nmax64_Tmax65536_H16_d128"
+# the other standard configurations measured in the same run, one line each under per_config
+PER_CONFIG = ("gdn_fwd_bf16_T4096_H16_d128", "kda_fwd_bf16_T2048_H10_d128",
+              "gdn_fwdbwd_bf16_B4_T8192_H16_d128")
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 
@@ -42,7 +54,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gcl", choices=["gcl", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
@@ -50,6 +62,8 @@ def parse():
                             [c["name"] for c in synth.conv_workloads()])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only the headline workload")
     ap.add_argument("--batch", type=int, default=0,
                     help="profiling aid: run a dense workload with this many sequences instead "
                          "of its own count (a smaller case for ncu); never for a bench line")
@@ -84,6 +98,67 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+# fp32 FMA roof of the CUDA-core kernels: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def bf16_peak():
+    """Dense bf16 tensor-core peak (burst: the forward is timed alone, a fraction of a ms per
+    launch), measured or the fallback."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def tensor_path(w) -> bool:
+    return w.dtype == "bf16" and w.K == 128 and w.V == 128 and w.bt == 64
+
+
+def roofline(w, kernel_ms, traffic=None, kind="forward"):
+    """The slower of the algorithmic bytes at the measured HBM bandwidth and the algorithmic
+    FLOPs at the compute peak of the path (bf16 tensor cores, or the fp32 FMA roof of the
+    CUDA-core kernels) sets the roofline time; frac = that time / the measured kernel time."""
+    hbm, hbm_kind = peaks()
+    ab, fl = bytes_per_step(w), flops_per_step(w)
+    if tensor_path(w):
+        cpeak, ckind, cbound = *bf16_peak(), "tensor"
+    else:
+        cpeak, ckind, cbound = FP32_ALU_TFLOPS, "derived (152 SMs x 128 FP32 lanes x 2 x 2.07 GHz)", "alu"
+    t_hbm = ab / (hbm * 1e9)
+    t_cmp = fl / (cpeak * 1e12)
+    sec = kernel_ms * 1e-3
+    if t_cmp > t_hbm:
+        bound, achieved, peak, unit, pkind = cbound, fl / sec / 1e12, cpeak, "TFLOP/s", ckind
+    else:
+        bound, achieved, peak, unit, pkind = "hbm", ab / sec / 1e9, hbm, "GB/s", hbm_kind
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic, "kernel": kind, "kernel_ms": kernel_ms,
+            "algorithmic_bytes_per_launch": ab, "algorithmic_flops_per_launch": fl,
+            "hbm_time_ms": t_hbm * 1e3, "compute_time_ms": t_cmp * 1e3, "peak_source": pkind}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def traffic_record(workload: str):
@@ -257,74 +332,158 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
     return tokens_per_rank * world / (ms_per_step * 1e-3)
 
 
-def launches_per_step(w) -> int:
-    """Library kernels per step: chunk_meta_build, the forward (prep and chain on the tensor
-    cores for GDN and KDA bf16 d_k = d_v = 128 -- prep, segment summaries, scan and segment
-    outputs when the chain is segmented -- one fused CUDA-core kernel otherwise) and
-    the backward (GDN on the tensor cores: state-gradient sweep from the forward's records and two
-    chunk-gradient kernels; otherwise the sweep and one chunk-gradient kernel)."""
-    tc = w.dtype == "bf16" and w.K == 128 and w.V == 128 and w.bt == 64
-    tc_bwd = tc and w.variant == synth.GDN
-    # a segmented chain (few long sequences): summaries, scan and segment outputs
+def fwd_plan_of(w) -> str:
+    """The forward's launch plan for w's sizes with the workspace the bench gives it (the
+    fastest plan's), from the library's host-side plan query (no GPU needed)."""
+    import ctypes as ct
     import chunked_gated_linear_gb300 as gcl
-    seg = tc and gcl.fwd_chain_segments(w.t_max, w.n_max, w.H, w.bt) > 0
-    fwd = (4 if seg else 2) if tc else 1
-    # backward with the forward's saved states and chunk records: the state-gradient sweep and
-    # the chunk gradients (two kernels on the tensor cores for GDN, one otherwise)
+    fake = 1 << 20                      # an aligned stand-in address: only sizes are read
+    a = gcl.FwdArgs(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake,
+                    ht=fake, h_save=fake if w.backward else None, chunk_indices=fake,
+                    chunk_offsets=fake, t_max=w.t_max, n_max=w.n_max, H=w.H, K=w.K, V=w.V,
+                    bt=w.bt, scale=w.scale, dtype={"bf16": 1, "f16": 2}.get(w.dtype, 0))
+    kda = w.variant == synth.KDA
+    lib = gcl.lib()
+    a.workspace_bytes = (lib.gcl_kda_fwd_workspace_bytes if kda else lib.gcl_fwd_workspace_bytes)(ct.byref(a))
+    if a.workspace_bytes:
+        a.workspace = fake
+    code = (lib.gcl_kda_fwd_plan if kda else lib.gcl_fwd_plan)(ct.byref(a))
+    return gcl.PLANS[int(code)]
+
+
+def launches_per_step(w) -> int:
+    """Library kernels per step: chunk_meta_build, the forward (the fused plan and the CUDA-core
+    kernel: one launch; the W-form and transition plans: the chunk prep and the chain; the
+    segmented plan: prep, segment summaries, scan and segment outputs) and the backward (GDN on
+    the tensor cores: state-gradient sweep from the forward's records and two chunk-gradient
+    kernels; otherwise the sweep and one chunk-gradient kernel)."""
+    plan = fwd_plan_of(w)
+    fwd = {"cuda_cores": 1, "fused": 1, "w_form": 2, "transition": 2, "segmented": 4}[plan]
+    tc_bwd = tensor_path(w) and w.variant == synth.GDN
     return 1 + fwd + ((3 if tc_bwd else 2) if w.backward else 0)
 
 
-def graph_and_warm_timing(torch, w, sets, stream, step, step_ms, reps):
-    """Medians over `reps` steps (CUDA events on the launching stream) of: the direct launches
-    timed above (L2-cold: input sets rotated), the step captured once per input set in a CUDA
-    graph and replayed (cold, and warm: the same set every replay, so inputs that fit stay in
-    L2), and graph-update-replay (copy the next set's inputs into the captured set's buffers,
-    then replay)."""
-    import ctypes as ct
+def pct(values, q):
+    v = sorted(values)
+    return v[min(len(v) - 1, max(0, int(round(q / 100.0 * (len(v) - 1)))))]
+
+
+def input_sets(w, rank, dev, gcl, min_sets=2):
+    """Input sets for the timed steps: the varlen workload's seeded layouts (capture layout and
+    three replay layouts), else fresh seeds of the same shape; as many as keep the rotation
+    above 3x L2."""
+    if len(set(w.lengths)) > 1 or w.n_max > len(w.lengths):
+        layouts = [synth.varlen_layout(w, s) for s in synth.layout_seeds(w)]
+    else:
+        layouts = [w]
+    sets = []
+    i = 0
+    while True:
+        wl = layouts[i % len(layouts)]
+        seed = wl.seed + 1000 * rank + (i // len(layouts)) * 7919
+        sets.append(Runner(gcl, wl, synth.make_inputs(wl, seed=seed), dev))
+        i += 1
+        if i >= max(min_sets, len(layouts)) and i * sets[0].footprint() > 3 * L2_BYTES:
+            return sets
+
+
+def measure(gcl, w, args, rank, world, dist, dev, steps, warmup, graphs=True):
+    """Time one workload: direct launches (per-step and forward-kernel CUDA events, L2-cold by
+    rotation), then, with graphs, the same steps captured once per input set and replayed in
+    rotation (the headline), and graph-update-replay.  Returns the timings and the sets."""
+    import torch
+    sets = input_sets(w, rank, dev, gcl)
     n = len(sets)
-    cap = torch.cuda.Stream()
-    cap.wait_stream(stream)
-    graphs = []
-    for r in sets:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            step(r, sp=ct.c_void_p(torch.cuda.current_stream().cuda_stream))
-        graphs.append(g)
-    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    s = ctypes.c_void_p(stream.cuda_stream)
 
-    def timed(fn):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(reps)]
-        for i in range(3):
-            fn(i)
-        torch.cuda.synchronize()
-        for i in range(reps):
-            ev[i][0].record(stream)
-            fn(i)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        return statistics.median(a.elapsed_time(b) for a, b in ev)
+    def step(r, ev=None, sp=None):
+        sp = s if sp is None else sp
+        r.meta(sp)
+        if ev is not None:
+            ev[0].record(stream)
+        r.forward(sp)
+        if ev is not None:
+            ev[1].record(stream)
+        if r.w.backward:
+            r.backward(sp)
 
-    inputs = [k for k in ("q", "k", "v", "g", "beta", "cu", "h0", "do", "dht") if k in sets[0].t]
-
-    def update_replay(i):
-        src = sets[1 + i % (n - 1)] if n > 1 else sets[0]
-        for k in inputs:
-            sets[0].t[k].copy_(src.t[k])
-        graphs[0].replay()
-
-    out = {
-        "direct_median_ms": statistics.median(step_ms),
-        "graph_median_ms": timed(lambda i: graphs[i % n].replay()),
-        "graph_warm_median_ms": timed(lambda i: graphs[0].replay()),
-        "graph_update_replay_median_ms": timed(update_replay),
-        "reps": reps,
-        "l2": "direct and graph: input sets rotated (cold); warm: one set replayed",
-    }
+    for i in range(warmup):
+        step(sets[i % n])
     torch.cuda.synchronize()
     for r in sets:
         assert int(r.t["status"].item()) == 0
-    return out
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    out = {"sets": n}
+    # ---- direct launches
+    e_s, e_e = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    e_k = [(ev(), ev()) for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        e_s[i].record(stream)
+        step(sets[i % n], e_k[i])
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    direct = [a.elapsed_time(b) for a, b in zip(e_s, e_e)]
+    kern = [a.elapsed_time(b) for a, b in e_k]
+    tok = [sets[i % n].w.total_tokens for i in range(steps)]
+    out["direct"] = {"region_ms": e_s[0].elapsed_time(e_e[-1]), "p50_ms": pct(direct, 50),
+                     "p95_ms": pct(direct, 95), "tokens": sum(tok)}
+    # the forward kernels' time per set (its algorithmic bytes differ by layout)
+    per_set_kern = [float(np.mean(kern[j::n])) for j in range(n)]
+    out["kernel_ms_per_set"] = per_set_kern
+    out["kernel_ms"] = float(np.mean(kern))
+    if not graphs:
+        return out, sets, step
+    # ---- graph replay: one capture per input set, replayed in rotation
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    gs = []
+    for r in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(r, sp=ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        gs.append(g)
+    torch.cuda.synchronize()
+    for i in range(3 * n):
+        gs[i % n].replay()
+    torch.cuda.synchronize()
+    e_s, e_e = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        e_s[i].record(stream)
+        gs[i % n].replay()
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    rep = [a.elapsed_time(b) for a, b in zip(e_s, e_e)]
+    out["graph"] = {"region_ms": e_s[0].elapsed_time(e_e[-1]), "p50_ms": pct(rep, 50),
+                    "p95_ms": pct(rep, 95), "tokens": sum(tok)}
+    # ---- graph-update-replay: the next set's live rows copied into set 0's captured buffers
+    names = [k for k in ("q", "k", "v", "g", "beta", "do") if k in sets[0].t]
+    small = [k for k in ("cu", "h0", "dht") if k in sets[0].t]
+    reps = min(steps, 200)
+    e_s, e_e = [ev() for _ in range(reps)], [ev() for _ in range(reps)]
+    for i in range(reps):
+        src = sets[1 + i % (n - 1)] if n > 1 else sets[0]
+        live = src.w.total_tokens
+        e_s[i].record(stream)
+        for k in names:
+            sets[0].t[k][:live].copy_(src.t[k][:live])
+        for k in small:
+            sets[0].t[k].copy_(src.t[k])
+        gs[0].replay()
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    upd = [a.elapsed_time(b) for a, b in zip(e_s, e_e)]
+    out["graph_update_replay"] = {"p50_ms": pct(upd, 50), "p95_ms": pct(upd, 95), "reps": reps,
+                                  "copies": "live rows of " + ", ".join(names) + "; " + ", ".join(small)}
+    for r in sets:
+        assert int(r.t["status"].item()) == 0
+    return out, sets, step
 
 
 def resolve_workload(args):
@@ -347,128 +506,138 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     w = resolve_workload(args)
-    x = synth.make_inputs(w, seed=w.seed + 1000 * rank)
-    first = Runner(gcl, w, x, dev)
-    n_sets = max(2, -(-3 * L2_BYTES // max(first.footprint(), 1)))
-    sets = [first] + [Runner(gcl, w, synth.make_inputs(w, seed=w.seed + 1000 * rank + i), dev)
-                      for i in range(1, n_sets)]
-    stream = torch.cuda.current_stream()
-    s = ctypes.c_void_p(stream.cuda_stream)
-
-    def step(r, ev=None, sp=None):
-        sp = s if sp is None else sp
-        r.meta(sp)
-        if ev is not None:
-            ev[0].record(stream)
-        r.forward(sp)
-        if ev is not None:
-            ev[1].record(stream)
-        if w.backward:
-            r.backward(sp)
-
-    for i in range(args.warmup):
-        step(sets[i % n_sets])
-    torch.cuda.synchronize()
-    for r in sets:
-        assert int(r.t["status"].item()) == 0
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    K = args.steps
-    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(K)]
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
     clocks.start()
     t_wall = time.perf_counter()
-    for i in range(K):
-        r = sets[i % n_sets]
-        ev_s[i].record(stream)
-        step(r, ev_k[i])
-        ev_e[i].record(stream)
-    torch.cuda.synchronize()
+    m, sets, step = measure(gcl, w, args, rank, world, dist, dev, args.steps, args.warmup)
     wall = time.perf_counter() - t_wall
     clocks.stop()
-    if dist is not None:
-        dist.barrier()
-    step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
-    kern_ms = [a.elapsed_time(b) for a, b in ev_k]
-    region_ms = ev_s[0].elapsed_time(ev_e[-1])
-    tot = reduce_max([sum(step_ms), sum(kern_ms), region_ms], dist, dev)
-    ms_step = tot[2] / K          # the whole bracketed region, gaps between steps included
-    ms_kern = tot[1] / K
-    value = job_throughput(w.total_tokens, world, ms_step)
-
-    timing = graph_and_warm_timing(torch, w, sets, stream, step, step_ms, max(K, 50))
-    timing["chunk_utilisation"] = int(first.t["off"][-1].item()) / gcl.nt_max(w.t_max, w.n_max, w.bt)
-
-    # end-to-end through the C ABI with host buffers: H2D inputs, step, D2H outputs
-    e2e = run_e2e(gcl, w, x, first, stream, s, args.e2e_steps, world, dist)
+    K = args.steps
+    # the headline: graph replay of the captured steps, max over ranks
+    tot = reduce_max([m["graph"]["region_ms"], m["direct"]["region_ms"], m["kernel_ms"]], dist, dev)
+    ms_step, ms_direct, ms_kern = tot[0] / K, tot[1] / K, tot[2]
+    tokens = m["graph"]["tokens"] / K                       # per step, averaged over layouts
+    value = tokens * world / (ms_step * 1e-3)
+    n = m["sets"]
+    # roofline of the forward kernels: each set's algorithmic bytes over its kernel time
+    fw = [r.w for r in sets]
+    rl = [roofline(x, km, kind=fwd_plan_of(x)) for x, km in zip(fw, m["kernel_ms_per_set"])]
+    ab = sum(r["algorithmic_bytes_per_launch"] for r in rl) / n
+    roof = roofline_mean(rl, ms_kern, traffic_record(w.name))
+    util = [int(r.t["off"][-1].item()) / gcl.nt_max(x.t_max, x.n_max, x.bt) for r, x in zip(sets, fw)]
+    e2e = run_e2e(gcl, sets[0].w, sets[0], torch.cuda.current_stream(),
+                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), args.e2e_steps, world,
+                  dist)
     clk = clocks.summary()
+    per = {}
+    if not args.no_per_config and world == 1:
+        for name in PER_CONFIG:
+            if name == w.name:
+                continue
+            wc = synth.workload_by_name(name)
+            mc, sc, _ = measure(gcl, wc, args, rank, world, dist, dev, max(50, min(K, 300)),
+                                max(args.warmup, 3), graphs=False)
+            km = mc["kernel_ms"]
+            per[name] = {"ms_per_step": mc["direct"]["region_ms"] / max(50, min(K, 300)),
+                         "p50_ms": mc["direct"]["p50_ms"], "p95_ms": mc["direct"]["p95_ms"],
+                         "tokens_per_step": wc.total_tokens,
+                         "value": wc.total_tokens / (mc["direct"]["region_ms"] / max(50, min(K, 300)) * 1e-3),
+                         "unit": "tokens/s", "plan": fwd_plan_of(wc),
+                         "roofline": roofline(wc, km, traffic_record(name), kind=fwd_plan_of(wc))}
+            del sc
+            torch.cuda.empty_cache()
     if rank != 0:
         return None
-    peak, peak_kind = peaks()
-    ab = bytes_per_step(w)
-    achieved = ab / (ms_kern * 1e-3) / 1e9
-    traffic = traffic_record(w.name)
     line = {
         "metric": "GDN/KDA chunk prefill tokens/s on 1 GB300 and % of roofline (HBM/TC)",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded PCG64; q,k L2-normalised N(0,1), v N(0,1), "
-                "beta=sigmoid(N), g=-softplus(N), h0 N(0,0.1^2))",
-        "config": {"workload": w.name, "tokens_per_step": w.total_tokens, "heads": w.H,
+                "beta=sigmoid(N), g=-softplus(N), h0 N(0,0.1^2); varlen layouts from seeded "
+                "uniform lengths)",
+        "config": {"workload": w.name, "tokens_per_step": tokens, "heads": w.H,
                    "d_k": w.K, "d_v": w.V, "chunk": w.bt, "n_max": w.n_max,
-                   "t_max": w.t_max, "parallelism": f"replicas x{world}",
-                   "l2": f"rotating {n_sets} input sets, {n_sets * first.footprint() / 2**20:.0f} "
-                         f"MiB total (> 3x L2); no flush",
-                   "timed_region_ms": region_ms, "host_wall_ms": wall * 1e3},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "gdn_chunk_fwd" if w.variant == synth.GDN else "kda_chunk_fwd",
-                     "kernel_ms": ms_kern, "algorithmic_bytes_per_launch": ab,
-                     "tensor_flops_per_launch": flops_per_step(w), "peak_source": peak_kind},
+                   "t_max": w.t_max, "parallelism": f"replicas x{world}", "plan": fwd_plan_of(w),
+                   "timing": "CUDA-graph replay of each input set's captured step, in rotation",
+                   "l2": f"rotating {n} input sets ({n * sets[0].footprint() / 2**20:.0f} MiB, "
+                         f"> 3x L2); no flush",
+                   "host_wall_s": wall},
+        "roofline": roof,
         "e2e": e2e,
-        "timing": timing,
+        "timing": {"graph_replay": m["graph"], "direct": m["direct"],
+                   "graph_update_replay": m["graph_update_replay"],
+                   "direct_ms_per_step": ms_direct,
+                   "chunk_utilisation": float(np.mean(util)),
+                   "chunk_utilisation_per_layout": util,
+                   "tokens_per_layout": [x.total_tokens for x in fw]},
+        "per_config": per,
         "gpu_launches": K * launches_per_step(w),
         "clocks": clk,
     }
     return line
 
 
-def run_e2e(gcl, w, x, r, stream, s, steps, world, dist):
+def roofline_mean(rl, kernel_ms, traffic):
+    """One roofline object for rotating sets: algorithmic bytes and FLOPs averaged over the
+    sets, against the mean forward-kernel time."""
+    n = len(rl)
+    r0 = dict(rl[0])
+    ab = sum(r["algorithmic_bytes_per_launch"] for r in rl) / n
+    fl = sum(r["algorithmic_flops_per_launch"] for r in rl) / n
+    t_hbm = sum(r["hbm_time_ms"] for r in rl) / n
+    t_cmp = sum(r["compute_time_ms"] for r in rl) / n
+    if r0["bound"] == "hbm":
+        achieved = ab / (kernel_ms * 1e-3) / 1e9
+    else:
+        achieved = fl / (kernel_ms * 1e-3) / 1e12
+    r0.update(achieved=achieved, frac=achieved / r0["peak"], traffic=traffic, kernel_ms=kernel_ms,
+              algorithmic_bytes_per_launch=ab, algorithmic_flops_per_launch=fl,
+              hbm_time_ms=t_hbm, compute_time_ms=t_cmp)
+    return r0
+
+
+def run_e2e(gcl, w, r, stream, s, steps, world, dist):
     """Same metric through the public C-ABI calls with pinned host buffers: per step the H2D
-    copy of every input, meta + forward, and the D2H copy of o and ht."""
+    copy of the live rows of every token input (and cu_seqlens, h0), meta + forward (+ backward),
+    and the D2H copy of the live rows of o and of ht."""
     import torch
-    names = [n for n in ("q", "k", "v", "g", "beta", "h0", "cu") if n in r.t]
-    host = {n: torch.empty_like(r.t[n], device="cpu").pin_memory() for n in names}
+    live = w.total_tokens
+    names = [n for n in ("q", "k", "v", "g", "beta", "do") if n in r.t]
+    small = [n for n in ("h0", "dht", "cu") if n in r.t]
+    host = {n: torch.empty_like(r.t[n][:live], device="cpu").pin_memory() for n in names}
+    host.update({n: torch.empty_like(r.t[n], device="cpu").pin_memory() for n in small})
     for n in names:
+        host[n].copy_(r.t[n][:live])
+    for n in small:
         host[n].copy_(r.t[n])
-    out_h = {n: torch.empty_like(r.t[n], device="cpu").pin_memory() for n in ("o", "ht")}
-    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    out_h = {"o": torch.empty_like(r.t["o"][:live], device="cpu").pin_memory(),
+             "ht": torch.empty_like(r.t["ht"], device="cpu").pin_memory()}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in host)
     d2h = sum(out_h[n].numel() * out_h[n].element_size() for n in out_h)
     times = []
     for i in range(steps + 3):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for n in names:
+            r.t[n][:live].copy_(host[n], non_blocking=True)
+        for n in small:
             r.t[n].copy_(host[n], non_blocking=True)
         r.meta(s)
         r.forward(s)
         if w.backward:
             r.backward(s)
-        for n in out_h:
-            out_h[n].copy_(r.t[n], non_blocking=True)
+        out_h["o"].copy_(r.t["o"][:live], non_blocking=True)
+        out_h["ht"].copy_(r.t["ht"], non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
         if i >= 3:
             times.append(e0.elapsed_time(e1))
     ms = reduce_max([float(np.mean(times))], dist, r.t["q"].device)[0]
     return {"value": job_throughput(w.total_tokens, world, ms), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "p50_ms": pct(times, 50), "p95_ms": pct(times, 95)}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -510,6 +679,7 @@ def cpu_baseline(w, x, budget_s=12.0):
         reps += 1
     line = {"value": th / w.H / dt, "unit": "tokens/s",
             "cores": min(oracle.num_threads(), heads * len(w.lengths)), "kind": "oracle",
+            "cpu_model": cpu_model(), "host_threads": os.cpu_count(),
             "sample": f"fp64 token recurrence, first {tokens} tokens of every sequence, all "
                       f"{heads} heads, {reps} run(s) ({th} token-heads, {dt:.1f} s)"}
     # the same oracle on one (sequence, head) unit: one host thread, about 3 s
@@ -560,7 +730,7 @@ def run_reference(args):
         "config": {"workload": w.name, "tokens_per_step": w.total_tokens, "heads": w.H},
         "cpu_baseline": {"value": value, "unit": "tokens/s",
                          "cores": min(oracle.num_threads(), heads * len(w.lengths)),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -61,3 +61,28 @@ def test_traffic_record_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench.traffic_record("absent") is None
     src.write_bytes(b"__global__ void k() { /* changed */ }\n")
     assert bench.traffic_record("wl") is None                     # stale once the kernel changes
+
+
+def test_roofline_takes_the_slower_roof(tmp_path, monkeypatch):
+    """The roofline time is the slower of the algorithmic bytes at the HBM peak and the
+    algorithmic FLOPs at the path's compute peak: the bf16 GDN forward is HBM-bound (about
+    178 FLOP per byte against a ridge near 290), the fp32 CUDA-core K = V = 64 forward is bound
+    by the fp32 FMA roof; frac is achieved over peak of the binding roof either way."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6681.8, "bf16_tflops": 1956.7}))
+    ws = {w.name: w for w in synth.standard_workloads()}
+    w1 = ws["gdn_fwd_bf16_T4096_H16_d128"]
+    r = bench.roofline(w1, 0.1)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6681.8
+    assert r["frac"] == pytest.approx(69_599_232 / 1e-4 / 1e9 / 6681.8)
+    assert r["compute_time_ms"] < r["hbm_time_ms"]
+    w0 = ws["gdn_fwd_fp32_T256_H2_d64"]
+    r0 = bench.roofline(w0, 0.01)
+    assert r0["bound"] == "alu" and r0["unit"] == "TFLOP/s"
+    assert r0["frac"] == pytest.approx(bench.flops_per_step(w0) / 1e-5 / 1e12 / bench.FP32_ALU_TFLOPS)
+    assert r0["compute_time_ms"] > r0["hbm_time_ms"]
+
+
+def test_cpu_model_is_a_name():
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name

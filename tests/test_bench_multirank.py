@@ -61,6 +61,9 @@ def test_launch_count_per_step():
     from chunked_gated_linear_gb300 import synth
     ws = {w.name: w for w in synth.standard_workloads()}
     assert bench.launches_per_step(ws["gdn_fwd_bf16_T4096_H16_d128"]) == 3
+    # the varlen prefill (64 slots x 16 heads): the fused plan, one kernel after the metadata
+    assert bench.launches_per_step(ws["gdn_varlen_bf16_N32_Nmax64_Tmax65536_H16_d128"]) == 2
+    assert bench.fwd_plan_of(ws["gdn_varlen_bf16_N32_Nmax64_Tmax65536_H16_d128"]) == "fused"
     assert bench.launches_per_step(ws["gdn_fwdbwd_bf16_B4_T8192_H16_d128"]) == 6
     assert bench.launches_per_step(ws["kda_fwd_bf16_T2048_H10_d128"]) == 3
     assert bench.launches_per_step(ws["gdn_fwd_fp32_T256_H2_d64"]) == 2
