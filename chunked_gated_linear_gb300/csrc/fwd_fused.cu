@@ -561,9 +561,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 }  // namespace
 
-// Units (sequence slots x heads) from which the fused plan runs: enough CTAs for two per SM
-// over most of the GPU; fewer units keep the split plans (value-column slices per head).
-int fwd_fused_min_units() { return 64; }
+// Units (sequence slots x heads) from which the fused plan runs: at least one CTA per SM.
+// The fused kernel's step per chunk is long (the whole Map-Reduce-Map of a chunk), so it
+// pays only where many units fill the GPU; fewer units keep the split plans, whose serial
+// step is short and whose value-column slices put several CTAs on every head (HA-NPU
+// section 4: head-per-core while heads fill the cores, column-wise split for the rest).
+int fwd_fused_min_units() { return num_sms(); }
 
 // A training forward (h_save) whose workspace holds the transition records runs the
 // transition plan instead: the backward's state-gradient sweep reads those records.

@@ -144,14 +144,18 @@ fwd_simt_kernel(FwdParams p) {
                 }
             }
         }
+        // K <- K * exp(gamma_c - gamma) in place (K is not read again in this chunk): one
+        // exponential per (row, key) instead of one per (row, key, value column) below
+        for (int e = tid; e < C * K; e += kThreads) {
+            const int i = e / K, c = e % K;
+            sK[i * LK + c] = expf(gam<VAR, K>(sG, C - 1, c) - gam<VAR, K>(sG, i, c)) * sK[i * LK + c];
+        }
         __syncthreads();
         // S <- Gamma_c S + (K * exp(gamma_c - gamma))^T E   (in place)
         for (int e = tid; e < K * VS; e += kThreads) {
             const int c = e / VS, j = e % VS;
-            const float gC = gam<VAR, K>(sG, C - 1, c);
-            float acc = expf(gC) * sS[c * LV + j];
-            for (int i = 0; i < C; ++i)
-                acc = fmaf(expf(gC - gam<VAR, K>(sG, i, c)) * sK[i * LK + c], sE[i * LV + j], acc);
+            float acc = expf(gam<VAR, K>(sG, C - 1, c)) * sS[c * LV + j];
+            for (int i = 0; i < C; ++i) acc = fmaf(sK[i * LK + c], sE[i * LV + j], acc);
             sS[c * LV + j] = acc;
         }
     }
@@ -176,9 +180,12 @@ cudaError_t launch_one(const FwdParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Value-column slices: 16 columns per CTA at K = 64 (a 64-wide head in 4 slices, so a few
+// (sequence, head) units still spread over the GPU), 32 at K = 128 (the state slice and the
+// chunk's K, Q, W tiles then fill the shared memory of two CTAs per SM).
 template <int VAR, typename Tin, int C>
 cudaError_t launch_chunk(const FwdParams &p, cudaStream_t s) {
-    if (p.K == 64) return launch_one<VAR, Tin, 64, 64, C>(p, s);
+    if (p.K == 64) return launch_one<VAR, Tin, 64, 16, C>(p, s);
     return launch_one<VAR, Tin, 128, 32, C>(p, s);
 }
 

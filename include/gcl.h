@@ -181,7 +181,8 @@ typedef struct gcl_fwd_args {
  * workspace of at least the minimum works; given sizes always select the same plan. */
 size_t gcl_fwd_workspace_bytes(const gcl_fwd_args *args);
 size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
-/* With many sequence-head units (n_max * H >= 64) a GDN forward runs the fused plan,
+/* With at least as many sequence-head units as SMs (n_max * H >= the device's SM count) a
+ * GDN forward runs the fused plan,
  * which needs no workspace: without h_save both queries return 0 and workspace may be
  * NULL; with h_save (a training forward) the fastest plan stays the transition form
  * (its records serve the backward) and the fused plan runs with any smaller workspace. */
@@ -223,7 +224,7 @@ int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t 
  * callers that size graphs or count launches, and for tests:
  *   GCL_PLAN_CUDA_CORES  one fp32 CUDA-core kernel (fp32 or fp16 inputs, K or V = 64, bt = 32)
  *   GCL_PLAN_FUSED       one tensor-core kernel per (sequence, head), everything on chip
- *                        (GDN, n_max * H >= 64: HA-NPU section 4, first tier)
+ *                        (GDN, n_max * H >= SMs: HA-NPU section 4, first tier)
  *   GCL_PLAN_W_FORM      chunk prep (T, L records) + chain over value-column slices
  *   GCL_PLAN_TRANSITION  chunk prep (affine chunk maps) + chain over value-column slices
  *   GCL_PLAN_SEGMENTED   the transition plan with the segment-parallel chain

@@ -13,7 +13,8 @@ from chunked_gated_linear_gb300 import synth  # noqa: E402
 from gpu_util import CANARY, TOL, Meta, check_fwd, run_fwd, to_device  # noqa: E402
 from parity import check as parity_check  # noqa: E402
 
-LENS = [1, 63, 0, 64, 65, 200, 130, 0]      # 8 slots x 8 heads = 64 units: the fused plan
+LENS = [1, 63, 0, 64, 65, 200, 130, 0]
+HF = 20                                       # 8 slots x 20 heads = 160 units >= SMs: the fused plan
 
 
 def _plan(w, d, meta, h_save=None, workspace=None):
@@ -25,7 +26,7 @@ def _plan(w, d, meta, h_save=None, workspace=None):
 
 @pytest.mark.parametrize("h0", [True, False], ids=["h0", "no-h0"])
 def test_fused_ragged(h0):
-    w = synth.varlen("fused", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, 8, 128, 128, h0=h0,
+    w = synth.varlen("fused", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, HF, 128, 128, h0=h0,
                      seed=31)
     x = synth.make_inputs(w)
     d = to_device(w, x)
@@ -43,7 +44,7 @@ def test_fused_ragged(h0):
 def test_fused_saved_chunk_states():
     """A forward with h_save and less workspace than the transition records runs the fused
     plan; every saved chunk state against the oracle's, unused rows untouched."""
-    w = synth.varlen("fused-hs", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, 8, 128, 128, seed=32)
+    w = synth.varlen("fused-hs", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, HF, 128, 128, seed=32)
     x = synth.make_inputs(w)
     d = to_device(w, x)
     out = run_fwd(w, d, h_save=True, plan="min")
@@ -63,7 +64,7 @@ def test_fused_saved_chunk_states():
 def test_fused_degenerate_gates_and_beta(regime):
     """beta = 0 (A = 0, T = I: the state only decays), g = 0, log gates 20x the generator's
     (chunk decay far below fp32's range) and a mix of strong and zero gates."""
-    w = synth.varlen("fused-gates", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, 8, 128, 128,
+    w = synth.varlen("fused-gates", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, HF, 128, 128,
                      seed=33)
     x = synth.make_inputs(w)
     T = w.total_tokens
@@ -83,10 +84,10 @@ def test_fused_degenerate_gates_and_beta(regime):
 
 
 def test_fused_dense_full_size_sampled_units():
-    """B = 4, T = 8192, H = 16 (64 units of 128 chunks), inference forward: the fused plan;
-    eight sampled units (first and last sequence and head among them) against the oracle at
-    the global, per-unit and per-row bars."""
-    w = synth.dense("fused-dense", synth.GDN, "bf16", 4, 8192, 16, 128, 128, seed=35)
+    """B = 10, T = 8192, H = 16 (160 units of 128 chunks), inference forward: the fused plan;
+    sampled units (first and last sequence and head among them) against the oracle at the
+    global, per-unit and per-row bars."""
+    w = synth.dense("fused-dense", synth.GDN, "bf16", 10, 8192, 16, 128, 128, seed=35)
     x = synth.make_inputs(w)
     d = to_device(w, x)
     out = run_fwd(w, d)
@@ -97,7 +98,7 @@ def test_fused_dense_full_size_sampled_units():
     ht = out["ht"].cpu().numpy()
     T = 8192
     cu1 = np.array([0, T], dtype=np.int64)
-    for (b, h) in ((0, 0), (0, 15), (1, 5), (2, 10), (3, 0), (3, 15)):
+    for (b, h) in ((0, 0), (0, 15), (3, 5), (6, 10), (9, 0), (9, 15)):
         s, e = b * T, (b + 1) * T
         sl = {m: x[m][s:e, h:h + 1] for m in ("q", "k", "v", "g", "beta")}
         o_ref, ht_ref = oracle.fwd(synth.GDN, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"],
@@ -107,17 +108,17 @@ def test_fused_dense_full_size_sampled_units():
 
 
 def test_fused_matches_split_plans_closely():
-    """The same inputs through the fused plan (64 units) and, head by head, through the
+    """The same inputs through the fused plan (160 units) and, head by head, through the
     split plans (one head per call: 8 units): both within the bar of the oracle and of each
     other."""
-    w = synth.varlen("fused-vs", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, 8, 128, 128, seed=36)
+    w = synth.varlen("fused-vs", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, HF, 128, 128, seed=36)
     x = synth.make_inputs(w)
     d = to_device(w, x)
     fused = run_fwd(w, d)
     torch.cuda.synchronize()
     T = w.total_tokens
     o_f = fused["o"].float().cpu().numpy()[:T]
-    for h in (0, 7):
+    for h in (0, HF - 1):
         w1 = synth.varlen("one-head", synth.GDN, "bf16", LENS, 8, sum(LENS) + 40, 1, 128, 128,
                           seed=36)
         x1 = {k: (v[:, h:h + 1] if k in ("q", "k", "v", "g", "beta") else v) for k, v in x.items()}
