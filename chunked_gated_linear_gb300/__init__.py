@@ -20,6 +20,8 @@ import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgcl.so")
+# the bounds-checking debug build (GCL_DEBUG_BOUNDS), for tests: load_library(DEBUG_LIB_PATH)
+DEBUG_LIB_PATH = os.path.join(PKG, "libgcl_debug.so")
 
 GCL_F32, GCL_BF16, GCL_F16 = 0, 1, 2
 DEV_STATUS = {0: "ok", 1: "cu_seqlens decreasing", 2: "cu_seqlens[0] != 0",

@@ -36,8 +36,8 @@ def _headers_mtime() -> float:
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def _compile(src: str, extra: list[str], verbose: bool) -> str:
-    obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], verbose: bool, objdir: str = OBJDIR) -> str:
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
     if (os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(src)
             and os.path.getmtime(obj) >= _headers_mtime()):
         return obj
@@ -52,22 +52,32 @@ def _compile(src: str, extra: list[str], verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra: list[str] | None = None, jobs: int | None = None) -> str:
-    """Compile every csrc/*.cu and link libgcl.so; returns the library path."""
-    os.makedirs(OBJDIR, exist_ok=True)
+DEBUG_LIB = os.path.join(PKG, "libgcl_debug.so")
+DEBUG_FLAGS = ["-DGCL_DEBUG_BOUNDS"]
+
+
+def build(verbose: bool = False, extra: list[str] | None = None, jobs: int | None = None,
+          debug: bool = False) -> str:
+    """Compile every csrc/*.cu and link libgcl.so; returns the library path.  debug=True builds
+    libgcl_debug.so instead, with every checked index tested against its buffer
+    (GCL_DEBUG_BOUNDS: an index outside records GCL_DEV_OUT_OF_BOUNDS and the access is
+    skipped), in objects of its own."""
+    objdir = OBJDIR + ("-debug" if debug else "")
+    lib = DEBUG_LIB if debug else LIB
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    extra = list(extra or [])
+    extra = list(extra or []) + (DEBUG_FLAGS if debug else [])
     with cf.ThreadPoolExecutor(max_workers=jobs or min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra, verbose), srcs))
-    if (not os.path.exists(LIB)
-            or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs)):
-        tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, verbose, objdir), srcs))
+    if (not os.path.exists(lib)
+            or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs)):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -100,7 +100,7 @@ dstate_sweep_kernel(BwdParams p) {
             }
         }
         simt_load_chunk<VAR, Tin, K, kSweepThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG,
-                                                    sB);
+                                                    sB, p.t_max, p.dev_status);
         for (int e = tid; e < C * VS; e += kSweepThreads) {
             const int r = e / VS, j = e % VS;
             sDO[r * LV + j] = r < len ? ld_in(d_o, ((t0 + r) * H + h) * (int64_t)V + v0 + j) : 0.f;
@@ -229,7 +229,7 @@ chunk_grad_kernel(BwdParams p) {
     const float *dSg = p.dh + (row * H + h) * KV;
 
     // ---- Map recompute
-    simt_load_chunk<kGDN, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    simt_load_chunk<kGDN, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB, p.t_max, p.dev_status);
     __syncthreads();
     simt_gate_cumsum<kGDN, K, kGradThreads, C>(sG);
     __syncthreads();
@@ -521,7 +521,7 @@ chunk_grad_kda_kernel(BwdParams p) {
     const float *dSg = p.dh + (row * H + h) * KV;
 
     // ---- Map recompute
-    simt_load_chunk<kKDA, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    simt_load_chunk<kKDA, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB, p.t_max, p.dev_status);
     __syncthreads();
     simt_gate_cumsum<kKDA, K, kGradThreads, C>(sG);
     __syncthreads();
@@ -640,7 +640,7 @@ chunk_grad_kda_kernel(BwdParams p) {
     }
     __syncthreads();
     // q and gamma again (the slice loop held Kp and Kb in their buffers)
-    simt_load_chunk<kKDA, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+    simt_load_chunk<kKDA, Tin, K, kGradThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB, p.t_max, p.dev_status);
     __syncthreads();
     simt_gate_cumsum<kKDA, K, kGradThreads, C>(sG);
     // dA = -T^T (dT T^T), strictly lower.  X = dT T^T into sA (dT is lower incl. diag).

@@ -461,7 +461,10 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // dv = beta dVb; RB = sum_v dVb o V; RC = sum_v dVb o (K S); the R5 operand
             // -beta Gamma dVb (in place of [T; L])
             const int r = lrow;
-            const bool live = r < len;
+            const bool live = r < len &&
+                              GCL_RANGE_IN_BOUNDS(((t0 + r) * H + h) * (int64_t)VD + half * 64,
+                                                  ((t0 + r) * H + h) * (int64_t)VD + half * 64 + 63,
+                                                  p.t_max * H * (int64_t)VD, p.status);
             float *dvrow = p.dv + ((t0 + r) * H + h) * (int64_t)VD + half * 64;
             const float br = sB[r], fb = -sB[r] * sEG[r];
             float rb = 0.f, rc = 0.f;
@@ -508,7 +511,9 @@ tc_grad1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int r = lrow - C;
             float x[64];
             ld64(128 + half * 64, x);                // dO S^T
-            if (r < len) {
+            if (r < len && GCL_RANGE_IN_BOUNDS(((t0 + r) * H + h) * (int64_t)KD + half * 64,
+                                               ((t0 + r) * H + h) * (int64_t)KD + half * 64 + 63,
+                                               p.t_max * H * (int64_t)KD, p.status)) {
                 float *dqrow = p.dq + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
                 const float fq = p.scale * sEG[r];
 #pragma unroll
@@ -739,7 +744,8 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             float frd = fr * sRD[r];
             sDG[r] = p.scale * Gr * sRA[r] + (sPart[0][r] - sPart[1][r]) + sB[r] * da_row - sPart[3][r] -
                      sB[r] * Gr * sRC[r] - frd;
-            if (r < len) p.dbeta[(t0 + r) * H + h] = sRB[r] - Gr * sRC[r] + da_row;
+            if (r < len && GCL_IN_BOUNDS((t0 + r) * H + h, p.t_max * H, p.status))
+                p.dbeta[(t0 + r) * H + h] = sRB[r] - Gr * sRC[r] + da_row;
             // the last row's gamma also carries the Ktil factors of every row: their sum
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) frd += __shfl_xor_sync(0xffffffffu, frd, d);
@@ -776,7 +782,8 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             __syncthreads();
             if (tid >= 32 && tid < C) x += s_carry;
             const int r = C - 1 - tid;
-            if (tid < C && r < len) p.dg[(t0 + r) * H + h] = x;
+            if (tid < C && r < len && GCL_IN_BOUNDS((t0 + r) * H + h, p.t_max * H, p.status))
+                p.dg[(t0 + r) * H + h] = x;
         }
         {
             const bool kq = mbar_wait(&bar_kq, 0, &s_err, 3);

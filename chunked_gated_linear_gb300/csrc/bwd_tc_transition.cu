@@ -179,7 +179,10 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
         };
         float dS[HV];
         {
-            const float *src = p.dht ? p.dht + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
+            const float *src = (p.dht && GCL_RANGE_IN_BOUNDS(state_base + (int64_t)row * VD + v0 + c0,
+                                                             state_base + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                                             (int64_t)p.n_max * H * KV, p.status))
+                                   ? p.dht + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
 #pragma unroll
             for (int j = 0; j < HV; ++j) dS[j] = src ? src[j] : 0.f;
         }
@@ -189,7 +192,9 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
             const int64_t rem = eos - bos - (int64_t)ic * C;
             const int len = (int)(rem < C ? rem : C);
             uint8_t *stage = smem + st * Lay::kStage;
-            if (p.dh_f32) {   // the gradient w.r.t. the state after chunk ic, fp32 rows
+            if (!GCL_IN_BOUNDS((row0 + ic) * H + h, p.nt_max * H, p.status)) {
+                // (debug build: a chunk row outside the state-gradient buffer is skipped)
+            } else if (p.dh_f32) {   // the gradient w.r.t. the state after chunk ic, fp32 rows
                 float *dst = p.dh_f32 + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
 #pragma unroll
                 for (int j = 0; j < HV; j += 4)
@@ -231,7 +236,10 @@ tc_sweep_t_kernel(const __grid_constant__ CUtensorMap tm_rec128, const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_free[st]);
         }
-        if (p.dh0 && *reinterpret_cast<volatile int *>(&s_err) == 0) {
+        if (p.dh0 && *reinterpret_cast<volatile int *>(&s_err) == 0 &&
+            GCL_RANGE_IN_BOUNDS(state_base + (int64_t)row * VD + v0 + c0,
+                                state_base + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                (int64_t)p.n_max * H * KV, p.status)) {
             float *dst = p.dh0 + state_base + (int64_t)row * VD + v0 + c0;
 #pragma unroll
             for (int j = 0; j < HV; j += 4)

@@ -122,11 +122,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int m = quarter * 32 + lane;                         // TMEM lane: value row v
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int h = blockIdx.x, z = blockIdx.y, H = p.H;
-    const int n = p.seq_order ? p.seq_order[z] : z;
+    const int n = (p.seq_order && GCL_IN_BOUNDS(z, p.n_max, p.status)) ? p.seq_order[z] : z;
     if (n < 0 || n >= p.n_max) {
         if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
         return;
     }
+    if (!GCL_RANGE_IN_BOUNDS(n, n + 1, (int64_t)p.n_max + 1, p.status)) return;
     const int64_t bos = p.cu[n], eos = p.cu[n + 1];
     if (bos < 0 || eos < bos || eos > p.t_max) {
         if (tid == 0) status_set(p.status, GCL_DEV_BAD_RANGE);
@@ -141,16 +142,20 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int64_t KV = (int64_t)KD * VD;
     const int64_t state_base = ((int64_t)n * H + h) * KV;
     const int k0 = half * 64;                                  // this thread's key columns
+    // [first, last] element of this thread's strided state column (h0, ht), and the sizes
+    const int64_t st_lo = state_base + (int64_t)k0 * VD + m, st_hi = st_lo + 63 * (int64_t)VD;
+    const int64_t n_state = (int64_t)p.n_max * H * KV;
 
     // S^T row m, keys k0 .. k0 + 63 (S[k][v] at h0[k * V + v])
     float S[64];
     {
-        const float *src = p.h0 ? p.h0 + state_base + (int64_t)k0 * VD + m : nullptr;
+        const float *src = (p.h0 && GCL_RANGE_IN_BOUNDS(st_lo, st_hi, n_state, p.status))
+                               ? p.h0 + state_base + (int64_t)k0 * VD + m : nullptr;
 #pragma unroll
         for (int j = 0; j < 64; ++j) S[j] = src ? src[(int64_t)j * VD] : 0.f;
     }
     if (nch == 0) {                                            // zero-length slot: ht = h0
-        if (p.ht) {
+        if (p.ht && GCL_RANGE_IN_BOUNDS(st_lo, st_hi, n_state, p.status)) {
             float *dst = p.ht + state_base + (int64_t)k0 * VD + m;
 #pragma unroll
             for (int j = 0; j < 64; ++j) dst[(int64_t)j * VD] = S[j];
@@ -185,6 +190,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
     auto issue_kq = [&](int ic) {
         const int t0 = (int)chunk_t0(ic);
+        (void)GCL_IN_BOUNDS(t0, p.t_max, p.status);           // (rows past t_max read zeros)
         mbar_arrive_expect_tx(&bar_kq, 32768);
         for (int cb = 0; cb < 2; ++cb) {
             tma_load_3d(smem + Lay::oKQ + cb * 16384, &tm_k, cb * 64, h, t0, &bar_kq);
@@ -193,6 +199,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
     auto issue_v = [&](int ic) {
         const int t0 = (int)chunk_t0(ic);
+        (void)GCL_IN_BOUNDS(t0, p.t_max, p.status);
         mbar_arrive_expect_tx(&bar_v, 16384);
         for (int cb = 0; cb < 2; ++cb)
             tma_load_3d(smem + Lay::oV + cb * 8192, &tm_v, cb * 64, h, t0, &bar_v);
@@ -230,8 +237,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int r = 2 * lane + e;
-            g_next[e] = r < len1 ? p.g[(t + r) * H + h] : 0.f;
-            b_next[e] = r < len1 ? __bfloat162float(p.beta[(t + r) * H + h]) : 0.f;
+            const bool ok = r < len1 && GCL_IN_BOUNDS((t + r) * H + h, p.t_max * H, p.status);
+            g_next[e] = ok ? p.g[(t + r) * H + h] : 0.f;
+            b_next[e] = ok ? __bfloat162float(p.beta[(t + r) * H + h]) : 0.f;
         }
     };
     // gamma (inclusive cumsum; rows past the end have g = 0), beta, Gamma = exp(gamma),
@@ -337,7 +345,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float dec[16];
                 if (bc < br) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) dec[j] = f1 * sF2[br * C + c0 + j];
+                    for (int j = 0; j < 16; ++j)
+                        dec[j] = GCL_IN_BOUNDS(br * C + c0 + j, 4 * C, p.status) ? f1 * sF2[br * C + c0 + j] : 0.f;
                 } else if (bc == br) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) dec[j] = __expf(c0 + j <= r ? gr - sG[c0 + j] : 0.f);
@@ -352,7 +361,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             a[e] = (live && c0 + j + e < r) ? rowf * dec[j + e] * d[j + e] : 0.f;
-                        *reinterpret_cast<float4 *>(sAf + r * kSolveLD + c0 + j) = make_float4(a[0], a[1], a[2], a[3]);
+                        if (GCL_RANGE_IN_BOUNDS(r * kSolveLD + c0 + j, r * kSolveLD + c0 + j + 3, C * kSolveLD, p.status))
+                            *reinterpret_cast<float4 *>(sAf + r * kSolveLD + c0 + j) = make_float4(a[0], a[1], a[2], a[3]);
                     }
                 } else {                                       // L row r = m - 64: inclusive
 #pragma unroll
@@ -366,7 +376,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             const float l1 = (live && c + 1 <= r) ? rowf * dec[j + 2 * e + 1] * d[j + 2 * e + 1] : 0.f;
                             pw[e] = pack_bf16(l0, l1);
                         }
-                        *reinterpret_cast<uint4 *>(smem + Lay::oL + sw128_offset(C, r, c0 + j)) = pk;
+                        if (GCL_RANGE_IN_BOUNDS(sw128_offset(C, r, c0 + j), sw128_offset(C, r, c0 + j) + 15, 8192, p.status))
+                            *reinterpret_cast<uint4 *>(smem + Lay::oL + sw128_offset(C, r, c0 + j)) = pk;
                     }
                 }
             }
@@ -396,7 +407,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     pw[e] = pack_bf16(c <= r ? sTf[r * kSolveLD + c] : 0.f,
                                       c + 1 <= r ? sTf[r * kSolveLD + c + 1] : 0.f);
                 }
-                *reinterpret_cast<uint4 *>(smem + Lay::oT + sw128_offset(C, r, cq + j)) = pk;
+                if (GCL_RANGE_IN_BOUNDS(sw128_offset(C, r, cq + j), sw128_offset(C, r, cq + j) + 15, 8192, p.status))
+                    *reinterpret_cast<uint4 *>(smem + Lay::oT + sw128_offset(C, r, cq + j)) = pk;
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + cS + q * 16, S + q * 16);
@@ -424,8 +436,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = r0 + e;
-                        const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                            vcol + (r >> 3) * 1024 + (r & 7) * 128 + ((((vc >> 3) ^ (r & 7))) << 4)));
+                        const int voff = vb * 8192 + (vc & 7) * 2 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                         ((((vc >> 3) ^ (r & 7))) << 4);
+                        const float vv = GCL_IN_BOUNDS(voff, 16384, p.status)
+                                             ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                                   vcol + (r >> 3) * 1024 + (r & 7) * 128 + ((((vc >> 3) ^ (r & 7))) << 4)))
+                                             : 0.f;
                         rr[e] = r < len ? bb[e] * (vv - gg[e] * x[j + e]) : 0.f;
                     }
                     pk[j >> 1] = pack_bf16(rr[0], rr[1]);
@@ -510,7 +526,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (issuer && ic + 1 < nch) issue_kq(ic + 1);       // K and Q are no longer read
         // ---- state: h_save (the state entering the chunk), S <- Gamma_c S + dS; O staging
         {
-            if (p.h_save) {
+            const int64_t hs_lo = ((row0 + ic) * H + h) * KV + (int64_t)k0 * VD + m;
+            if (p.h_save && GCL_RANGE_IN_BOUNDS(hs_lo, hs_lo + 63 * (int64_t)VD, p.nt_max * H * KV, p.status)) {
                 float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)k0 * VD + m;
 #pragma unroll
                 for (int j = 0; j < 64; ++j) dst[(int64_t)j * VD] = S[j];
@@ -531,7 +548,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    sO[(half * 32 + hh * 16 + j) * kOLD + m] = __float2bfloat16_rn(ov[j]);
+                    if (GCL_IN_BOUNDS((half * 32 + hh * 16 + j) * kOLD + m, C * kOLD, p.status))
+                        sO[(half * 32 + hh * 16 + j) * kOLD + m] = __float2bfloat16_rn(ov[j]);
             }
         }
         tc_fence_before();
@@ -541,6 +559,10 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (p.o != nullptr) {   // valid rows of O, 16 threads x 16 bytes per row
             const int rsub = tid >> 4, cc = (tid & 15) * 8;
             for (int r = rsub; r < len; r += kThreads / 16) {
+                const int64_t oi = ((t0 + r) * H + h) * (int64_t)VD + cc;
+                if (!GCL_RANGE_IN_BOUNDS(oi, oi + 7, p.t_max * H * VD, p.status) ||
+                    !GCL_RANGE_IN_BOUNDS(r * kOLD + cc, r * kOLD + cc + 7, C * kOLD, p.status))
+                    continue;
                 const uint4 val = *reinterpret_cast<const uint4 *>(sO + r * kOLD + cc);
                 *reinterpret_cast<uint4 *>(p.o + ((t0 + r) * H + h) * (int64_t)VD + cc) = val;
             }
@@ -548,7 +570,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // a wait that gave up (s_err) ends every thread's loop at the same chunk
         if (__syncthreads_or(*reinterpret_cast<volatile int *>(&s_err) != 0)) break;
     }
-    if (s_err == 0 && p.ht) {
+    if (s_err == 0 && p.ht && GCL_RANGE_IN_BOUNDS(st_lo, st_hi, n_state, p.status)) {
         float *dst = p.ht + state_base + (int64_t)k0 * VD + m;
 #pragma unroll
         for (int j = 0; j < 64; ++j) dst[(int64_t)j * VD] = S[j];

@@ -86,7 +86,9 @@ fwd_simt_kernel(FwdParams p) {
 
     for (int e = tid; e < K * VS; e += kThreads) {
         const int c = e / VS, j = e % VS;
-        sS[c * LV + j] = p.h0 ? p.h0[state_base + (int64_t)c * V + v0 + j] : 0.f;
+        sS[c * LV + j] = (p.h0 && GCL_IN_BOUNDS(state_base + (int64_t)c * V + v0 + j,
+                                                (int64_t)p.n_max * H * KV, p.dev_status))
+                             ? p.h0[state_base + (int64_t)c * V + v0 + j] : 0.f;
     }
     const int nchunks = (int)((eos - bos + C - 1) / C);
     for (int ic = 0; ic < nchunks; ++ic) {
@@ -102,13 +104,16 @@ fwd_simt_kernel(FwdParams p) {
             float *dst = p.h_save + (row * H + h) * KV;
             for (int e = tid; e < K * VS; e += kThreads) {
                 const int c = e / VS, j = e % VS;
-                dst[(int64_t)c * V + v0 + j] = sS[c * LV + j];
+                if (GCL_IN_BOUNDS((row * H + h) * KV + (int64_t)c * V + v0 + j, p.nt_max * H * KV, p.dev_status))
+                    dst[(int64_t)c * V + v0 + j] = sS[c * LV + j];
             }
         }
-        simt_load_chunk<VAR, Tin, K, kThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB);
+        simt_load_chunk<VAR, Tin, K, kThreads, C>(q, k, p.g, beta, t0, len, h, H, sQ, sK, sG, sB, p.t_max, p.dev_status);
         for (int e = tid; e < C * VS; e += kThreads) {
             const int r = e / VS, j = e % VS;
-            sV[r * LV + j] = r < len ? ld_in(v, ((t0 + r) * H + h) * (int64_t)V + v0 + j) : 0.f;
+            sV[r * LV + j] = (r < len && GCL_IN_BOUNDS(((t0 + r) * H + h) * (int64_t)V + v0 + j,
+                                                        p.t_max * H * (int64_t)V, p.dev_status))
+                                 ? ld_in(v, ((t0 + r) * H + h) * (int64_t)V + v0 + j) : 0.f;
         }
         __syncthreads();
         simt_gate_cumsum<VAR, K, kThreads, C>(sG);
@@ -140,7 +145,9 @@ fwd_simt_kernel(FwdParams p) {
                     float acc = 0.f;
                     for (int c = 0; c < K; ++c) acc = fmaf(sQ[r * LK + c], sS[c * LV + j], acc);
                     for (int i = 0; i <= r; ++i) acc = fmaf(sL[r * kLC + i], sE[i * LV + j], acc);
-                    st_out(o, ((t0 + r) * H + h) * (int64_t)V + v0 + j, acc);
+                    if (GCL_IN_BOUNDS(((t0 + r) * H + h) * (int64_t)V + v0 + j, p.t_max * H * (int64_t)V,
+                                      p.dev_status))
+                        st_out(o, ((t0 + r) * H + h) * (int64_t)V + v0 + j, acc);
                 }
             }
         }
@@ -163,7 +170,8 @@ fwd_simt_kernel(FwdParams p) {
     if (p.ht) {
         for (int e = tid; e < K * VS; e += kThreads) {
             const int c = e / VS, j = e % VS;
-            p.ht[state_base + (int64_t)c * V + v0 + j] = sS[c * LV + j];
+            if (GCL_IN_BOUNDS(state_base + (int64_t)c * V + v0 + j, (int64_t)p.n_max * H * KV, p.dev_status))
+                p.ht[state_base + (int64_t)c * V + v0 + j] = sS[c * LV + j];
         }
     }
 }

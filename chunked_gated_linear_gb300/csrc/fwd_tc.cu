@@ -143,7 +143,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     __shared__ float s_carry;
     {
-        const float gv = (tid < len) ? p.g[(t0 + tid) * H + h] : 0.f;
+        const float gv = (tid < len && GCL_IN_BOUNDS((t0 + tid) * H + h, p.t_max * H, p.status))
+                             ? p.g[(t0 + tid) * H + h] : 0.f;
         const float gam = chunk_cumsum(gv, &s_carry);
         if (tid < C) {
             sG[tid] = gam;
@@ -548,7 +549,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
         float S[HV];
         {
-            const float *src = p.h0 ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
+            const float *src = (p.h0 && GCL_RANGE_IN_BOUNDS(state_base + (int64_t)row * VD + v0 + c0,
+                                                            state_base + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                                            (int64_t)p.n_max * H * KV, p.status))
+                                   ? p.h0 + state_base + (int64_t)row * VD + v0 + c0 : nullptr;
 #pragma unroll
             for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
 #pragma unroll
@@ -564,7 +568,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int st = ic & 1, len = chunk_len(ic);
             const int64_t t0 = bos + (int64_t)ic * C;
             const float *fac = reinterpret_cast<const float *>(smem + st * Lay::kStage + Lay::oF);
-            if (p.h_save) {
+            if (p.h_save &&
+                GCL_RANGE_IN_BOUNDS(((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0,
+                                    ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                    p.nt_max * H * KV, p.status)) {
                 float *dst = p.h_save + ((row0 + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
 #pragma unroll
                 for (int j = 0; j < HV; j += 4)
@@ -618,7 +625,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int q = 0; q < HV / 8; ++q) tmem_ld8(tmem + lane_off + tD4 + c0 + q * 8, d4 + q * 8);
                     tmem_ld_wait();
-                    if (r < len && p.o != nullptr) {
+                    if (r < len && p.o != nullptr &&
+                        GCL_RANGE_IN_BOUNDS(((t0 + r) * H + h) * (int64_t)VD + v0 + c0,
+                                            ((t0 + r) * H + h) * (int64_t)VD + v0 + c0 + HV - 1,
+                                            p.t_max * H * (int64_t)VD, p.status)) {
                         const float fq = fac[C + r];
                         __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * (int64_t)VD + v0 + c0;
 #pragma unroll
@@ -641,7 +651,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 break;
             }
         }
-        if (!failed && p.ht) {
+        if (!failed && p.ht &&
+            GCL_RANGE_IN_BOUNDS(state_base + (int64_t)row * VD + v0 + c0,
+                                state_base + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                (int64_t)p.n_max * H * KV, p.status)) {
             float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
 #pragma unroll
             for (int j = 0; j < HV; j += 4)

@@ -114,8 +114,10 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         gv = 0.f;
         bv = 0.f;
         if (tid < it.len) {
-            gv = p.g[(it.t0 + tid) * H + it.h];
-            bv = __bfloat162float(p.beta[(it.t0 + tid) * H + it.h]);
+            if (GCL_IN_BOUNDS((it.t0 + tid) * H + it.h, p.t_max * H, p.status)) {
+                gv = p.g[(it.t0 + tid) * H + it.h];
+                bv = __bfloat162float(p.beta[(it.t0 + tid) * H + it.h]);
+            }
         }
     };
     float g_raw, b_raw;
@@ -679,7 +681,10 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_d2free[ic & 1]);
-            if (orow < len && p.o != nullptr) {
+            if (orow < len && p.o != nullptr &&
+                GCL_RANGE_IN_BOUNDS(((t0 + orow) * H + h) * (int64_t)VD + v0,
+                                    ((t0 + orow) * H + h) * (int64_t)VD + v0 + VS - 1,
+                                    p.t_max * H * (int64_t)VD, p.status)) {
                 const uint8_t *zrow = stage + Lay::oZ + orow * (VS * 2);
                 __nv_bfloat16 *dst = p.o + ((t0 + orow) * H + h) * (int64_t)VD + v0;
 #pragma unroll
@@ -723,8 +728,11 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
             for (int j = 0; j < HV; ++j) S[j] = row == v0 + c0 + j ? 1.f : 0.f;
         } else {
             const float *src = seg > 0 ? p.seg_start + (((unit_idx * p.n_seg + seg) * KD + row) * VD + v0 + c0)
-                               : p.h0  ? p.h0 + state_base + (int64_t)row * VD + v0 + c0
-                                       : nullptr;
+                               : (p.h0 && GCL_RANGE_IN_BOUNDS(state_base + (int64_t)row * VD + v0 + c0,
+                                                              state_base + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                                              (int64_t)p.n_max * H * KV, p.status))
+                                   ? p.h0 + state_base + (int64_t)row * VD + v0 + c0
+                                   : nullptr;
 #pragma unroll
             for (int j = 0; j < HV; ++j) S[j] = src ? src[j] : 0.f;
         }
@@ -733,7 +741,10 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
         for (int ic = 0; ic < nch; ++ic) {
             const int st = ic % NS;
             const uint8_t *stage = smem + st * Lay::kStage;
-            if (p.h_save) {
+            if (p.h_save &&
+                GCL_RANGE_IN_BOUNDS(((row0 + cb + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0,
+                                    ((row0 + cb + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                    p.nt_max * H * KV, p.status)) {
                 float *dst = p.h_save + ((row0 + cb + ic) * H + h) * KV + (int64_t)row * VD + v0 + c0;
 #pragma unroll
                 for (int j = 0; j < HV; j += 4)
@@ -792,7 +803,10 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
 #pragma unroll
                 for (int j = 0; j < HV; ++j) blk[KD * KD + (int64_t)(v0 - VD + c0 + j) * KD + row] = S[j];
             }
-        } else if (p.ht && last_seg && *reinterpret_cast<volatile int *>(&s_err) == 0) {
+        } else if (p.ht && last_seg && *reinterpret_cast<volatile int *>(&s_err) == 0 &&
+                   GCL_RANGE_IN_BOUNDS(state_base + (int64_t)row * VD + v0 + c0,
+                                       state_base + (int64_t)row * VD + v0 + c0 + HV - 1,
+                                       (int64_t)p.n_max * H * KV, p.status)) {
             float *dst = p.ht + state_base + (int64_t)row * VD + v0 + c0;
 #pragma unroll
             for (int j = 0; j < HV; j += 4)

@@ -10,6 +10,7 @@
 #include <utility>
 
 #include "gcl.h"
+#include "gcl_bounds.cuh"
 
 namespace gcl {
 

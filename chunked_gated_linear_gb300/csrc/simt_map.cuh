@@ -27,19 +27,21 @@ template <int VAR, typename Tin, int K, int NT, int C>
 __device__ __forceinline__ void simt_load_chunk(const Tin *q, const Tin *k, const float *g,
                                                 const Tin *beta, int64_t t0, int len, int h,
                                                 int H, float *sQ, float *sK, float *sG,
-                                                float *sB) {
+                                                float *sB, int64_t t_max, int32_t *st) {
     constexpr int LK = K + 1;
     const int tid = threadIdx.x;
     for (int e = tid; e < C * K; e += NT) {
         const int r = e / K, c = e % K;
         const int64_t gi = ((t0 + r) * H + h) * (int64_t)K + c;
-        sQ[r * LK + c] = r < len ? ld_in(q, gi) : 0.f;
-        sK[r * LK + c] = r < len ? ld_in(k, gi) : 0.f;
-        if (VAR == kKDA) sG[r * LK + c] = r < len ? g[gi] : 0.f;
+        const bool ok = r < len && GCL_IN_BOUNDS(gi, t_max * H * K, st);
+        sQ[r * LK + c] = ok ? ld_in(q, gi) : 0.f;
+        sK[r * LK + c] = ok ? ld_in(k, gi) : 0.f;
+        if (VAR == kKDA) sG[r * LK + c] = ok ? g[gi] : 0.f;
     }
     for (int r = tid; r < C; r += NT) {
-        sB[r] = r < len ? ld_in(beta, (t0 + r) * H + h) : 0.f;
-        if (VAR == kGDN) sG[r] = r < len ? g[(t0 + r) * H + h] : 0.f;
+        const bool ok = r < len && GCL_IN_BOUNDS((t0 + r) * H + h, t_max * H, st);
+        sB[r] = ok ? ld_in(beta, (t0 + r) * H + h) : 0.f;
+        if (VAR == kGDN) sG[r] = ok ? g[(t0 + r) * H + h] : 0.f;
     }
 }
 

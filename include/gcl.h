@@ -65,6 +65,8 @@ typedef enum gcl_status {
 #define GCL_DEV_CU_OVER_CAPACITY 3 /* cu_seqlens[N_max] > T_max                          */
 #define GCL_DEV_BAD_RANGE 4        /* a compute kernel met an invalid sequence range      */
 #define GCL_DEV_WAIT_TIMEOUT 5     /* a kernel gave up waiting on an async copy or MMA    */
+#define GCL_DEV_OUT_OF_BOUNDS 6    /* debug build (GCL_DEBUG_BOUNDS): an index fell       */
+                                   /* outside its buffer; the access was skipped          */
 
 typedef enum gcl_dtype {
     GCL_F32 = 0,   /* q, k, v, beta, do, o in fp32; every internal product in fp32     */
