@@ -120,7 +120,7 @@ fwd_simt_kernel(FwdParams p) {
         __syncthreads();
         simt_intra<VAR, K, kThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
         __syncthreads();
-        simt_solve<kThreads, C>(sA, sT);
+        simt_solve_blocked<kThreads, C>(sA, sT, sE);    // E is formed only after the solve
         simt_w<VAR, K, kThreads, C>(sT, sB, sG, sK, sW);
         __syncthreads();
         // E = T diag(beta) V - W S

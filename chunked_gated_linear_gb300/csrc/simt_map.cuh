@@ -75,6 +75,48 @@ __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, con
                                            const float *sB, float scale, float *sA, float *sL,
                                            float *sAp) {
     constexpr int LK = K + 1, kLC = C + 1;
+    if constexpr (VAR == kGDN && (C / 4) * (C / 4) <= NT) {
+        // GDN: one 4 x 4 tile of (r, i) pairs per thread, so each loaded key and query
+        // element serves four dot products (tiles above the diagonal are all zero)
+        constexpr int NTILE = C / 4;
+        const int t = threadIdx.x;
+        if (t < NTILE * NTILE) {
+            const int r0 = (t / NTILE) * 4, i0 = (t % NTILE) * 4;
+            float kk[4][4] = {}, qk[4][4] = {};
+            if (i0 <= r0 + 3) {
+                for (int c = 0; c < K; ++c) {
+                    float kr[4], qr[4], ki[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        kr[a] = sK[(r0 + a) * LK + c];
+                        qr[a] = sQ[(r0 + a) * LK + c];
+                        ki[a] = sK[(i0 + a) * LK + c];
+                    }
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            kk[a][b] = fmaf(kr[a], ki[b], kk[a][b]);
+                            qk[a][b] = fmaf(qr[a], ki[b], qk[a][b]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int r = r0 + a, i = i0 + b;
+                    const bool on = i <= r;
+                    const float d = expf(on ? sG[r] - sG[i] : 0.f);
+                    const float ap = (i < r) ? kk[a][b] * d : 0.f;
+                    const float l = on ? scale * (qk[a][b] * d) : 0.f;
+                    if (sA) sA[r * kLC + i] = sB[r] * ap;
+                    if (sAp) sAp[r * kLC + i] = ap;
+                    if (sL) sL[r * kLC + i] = l;
+                }
+        }
+        return;
+    }
     for (int e = threadIdx.x; e < C * C; e += NT) {
         const int r = e / C, i = e % C;
         float ap = 0.f, l = 0.f;
@@ -124,6 +166,65 @@ __device__ __forceinline__ void simt_solve(const float *sA, float *sT) {
     }
 }
 
+// T = (I + A)^-1 by blocked forward substitution over 16-row blocks (the same scheme as the
+// tensor-core path's solve: diagonal blocks column by column, one thread per column, then
+// the off-diagonal blocks level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj), with the
+// row stride of the CUDA-core layouts; 1 + 2 (C / 16 - 1) block barriers instead of C - 1.
+// sX: scratch of at least 3 * 16 * 16 floats.  T is written on and below the diagonal and
+// zero above it.  All NT threads of the block call it.
+template <int NT, int C>
+__device__ __forceinline__ void simt_solve_blocked(const float *sA, float *sT, float *sX) {
+    constexpr int kLC = C + 1, NB = C / 16;
+    static_assert(C % 16 == 0 && NT >= C, "16-row blocks, one thread per column");
+    const int tid = threadIdx.x;
+    for (int e = tid; e < C * C; e += NT) {          // zeros above the diagonal blocks
+        const int r = e / C, i = e % C;
+        if ((i >> 4) > (r >> 4)) sT[r * kLC + i] = 0.f;
+    }
+    if (tid < C) {   // ---- diagonal blocks: thread (block, column jj)
+        const int o = (tid >> 4) * 16, jj = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == jj) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < r; ++m)
+                part[m & 3] = fmaf(sA[(o + r) * kLC + o + m], x[m], part[m & 3]);
+            const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+            if (r > jj) x[r] = -sum;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sT[(o + r) * kLC + o + jj] = x[r];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int d = 1; d < NB; ++d) {
+        const int nel = (NB - d) * 256;               // (block, row, column) of level d
+        for (int s = tid; s < nel; s += NT) {
+            const int blk = s >> 8, rr = (s >> 4) & 15, cc = s & 15;
+            const int bi = d + blk, bj = blk;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16 * d; ++m)
+                acc = fmaf(sA[(bi * 16 + rr) * kLC + bj * 16 + m], sT[(bj * 16 + m) * kLC + bj * 16 + cc], acc);
+            sX[(blk * 16 + rr) * 16 + cc] = acc;
+        }
+        __syncthreads();
+        for (int s = tid; s < nel; s += NT) {
+            const int blk = s >> 8, rr = (s >> 4) & 15, cc = s & 15;
+            const int bi = d + blk, bj = blk;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                acc = fmaf(sT[(bi * 16 + rr) * kLC + bi * 16 + m], sX[(blk * 16 + m) * 16 + cc], acc);
+            sT[(bi * 16 + rr) * kLC + bj * 16 + cc] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
 // W = T diag(beta Gamma) K (GDN) or T diag(beta) (K * Gamma) (KDA).
 template <int VAR, int K, int NT, int C>
 __device__ __forceinline__ void simt_w(const float *sT, const float *sB, const float *sG,
@@ -132,8 +233,13 @@ __device__ __forceinline__ void simt_w(const float *sT, const float *sB, const f
     for (int e = threadIdx.x; e < C * K; e += NT) {
         const int r = e / K, c = e % K;
         float acc = 0.f;
-        for (int i = 0; i <= r; ++i)
-            acc = fmaf(sT[r * kLC + i] * sB[i] * expf(gam<VAR, K>(sG, i, c)), sK[i * LK + c], acc);
+        if (VAR == kGDN) {   // the row factor beta_i Gamma_i does not depend on the key
+            for (int i = 0; i <= r; ++i)
+                acc = fmaf(sT[r * kLC + i] * (sB[i] * expf(sG[i])), sK[i * LK + c], acc);
+        } else {
+            for (int i = 0; i <= r; ++i)
+                acc = fmaf(sT[r * kLC + i] * sB[i] * expf(gam<VAR, K>(sG, i, c)), sK[i * LK + c], acc);
+        }
         sW[r * LK + c] = acc;
     }
 }
