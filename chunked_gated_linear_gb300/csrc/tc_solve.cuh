@@ -1,19 +1,26 @@
 // tc_solve.cuh -- T = (I + A)^-1 for the 64 x 64 strictly lower triangular A of one chunk,
-// in fp32 on the CUDA cores, by blocked forward substitution.
+// in fp32 on the CUDA cores, by blocks of 16 x 16.
 //
 // HA-NPU paper "Empowering Hybrid Attention Models on NPUs", section 5: the matrix
 // inversion of the WY representation is decoupled from the GEMMs and runs on the vector
-// units.  Blocks are 16 x 16:
-//   diagonal      T_bb = (I + A_bb)^-1, column by column (forward substitution), one
-//                 thread per column with four interleaved partial sums (x[m] = 0 for
-//                 m < jj, so the sums need no mask);
-//   off-diagonal  T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, by levels i - j = 1, 2, 3; each
-//                 thread computes a 1 x 4 strip from float4 shared-memory loads.
-// Shared-memory layout: row stride kSolveLD floats (16-byte aligned rows, conflict-free
-// for the strip pattern), X scratch [3][16][kSolveLDX].
-// T is written on and below the block diagonal (zeros above the diagonal inside the
-// diagonal blocks); blocks above the block diagonal are left as they were, so readers
-// take T[r][c] only for c <= r.
+// units.  With blocks 0..3 of 16 rows, T_ii = (I + A_ii)^-1 and C_ij = T_ii A_ij (i > j),
+// expanding T = (I + A)^-1 block by block gives, for every lower block,
+//   T_ij = -P_ij T_jj,  P_ij = sum over the block paths i = p_0 > p_1 > ... > p_m = j of
+//                              (-1)^(m-1) C_{p_0 p_1} C_{p_1 p_2} ... C_{p_(m-1) p_m},
+// which four phases of 16-term products evaluate:
+//   diagonal   T_ii by forward substitution, one thread per column, four partial sums;
+//   1          C_ij = T_ii A_ij for the six lower blocks;
+//   2          P_20 = C_20 - C_21 C_10,  P_31 = C_31 - C_32 C_21,  Q_30 = C_30 - C_31 C_10;
+//   3          P_30 = Q_30 - C_32 P_20;
+//   4          T_ij = -P_ij T_jj (P_ij = C_ij for i - j = 1).
+// Each output strip is 1 x 4 with float4 shared-memory loads; every dot product has 16 terms,
+// so the critical path is five short phases (the level-by-level substitution it replaces
+// had six phases with dot products up to 48 terms long).
+// Shared-memory layout: row stride kSolveLD floats (16-byte aligned rows); X scratch
+// [3][16][kSolveLDX] holds P_20, P_31 and P_30.  The C_ij are kept in the upper blocks of A
+// (block (j, i) holds C_ij), which therefore does not survive the call.  T is written on and
+// below the block diagonal (zeros above the diagonal inside the diagonal blocks); blocks above
+// the block diagonal are left as they were, so readers take T[r][c] only for c <= r.
 #pragma once
 
 namespace gcl {
@@ -22,8 +29,6 @@ constexpr int kSolveLD = 68;
 constexpr int kSolveLDX = 20;
 constexpr int kSolveFloats = 2 * 64 * kSolveLD + 3 * 16 * kSolveLDX;   // A, T, X
 
-// Barrier among the solving threads: the whole block (BarId < 0), or threads 0 .. NT-1 on the
-// named barrier BarId (the rest of the block does other work meanwhile).
 template <int NT, int BarId>
 __device__ __forceinline__ void solve_barrier() {
     if constexpr (BarId < 0) {
@@ -35,7 +40,7 @@ __device__ __forceinline__ void solve_barrier() {
 
 // Threads 0 .. NT-1 call it (NT is 128 or 256); with BarId < 0 they are the whole block.
 template <int NT, int BarId = -1>
-__device__ __forceinline__ void solve_unit_lower64(const float *sA, float *sT, float *sX) {
+__device__ __forceinline__ void solve_unit_lower64(float *sA, float *sT, float *sX) {
     static_assert(NT == 128 || NT == 256, "128 or 256 solving threads");
     const int tid = threadIdx.x;
     if (tid < 64) {   // ---- diagonal blocks: thread (block, column jj), four partial sums
@@ -56,58 +61,79 @@ __device__ __forceinline__ void solve_unit_lower64(const float *sA, float *sT, f
         for (int r = 0; r < 16; ++r) sT[(o + r) * kSolveLD + o + jj] = x[r];
     }
     solve_barrier<NT, BarId>();
-    // ---- off-diagonal blocks.  Strip s of level d: block blk (bi = d + blk, bj = blk),
-    // column quad cq, row rr (rows fastest, so 8 consecutive lanes read 8 distinct rows).  The
-    // level loop is unrolled, so every dot product has a compile-time length (16 d terms) and
-    // its loads are issued ahead of the FMAs; the summation order is the plain one.
+    // ---- off-diagonal blocks by path products.  A strip is row rr, columns 4 cq .. 4 cq + 3
+    // of one 16 x 16 output block; out = sum_m L[rr][m] R[m][4 cq ..] over 16 terms.
+    auto strip = [](const float *L, int ldl, const float *R, int ldr, int rr, int cq) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        const int nstrip = (4 - d) * 64;
-        for (int s = tid; s < nstrip; s += NT) {
-            const int blk = s >> 6, cq = (s >> 4) & 3, rr = s & 15;
-            const int bi = d + blk, bj = blk;
-            const float *arow = sA + (bi * 16 + rr) * kSolveLD + bj * 16;
-            const float *tcol = sT + bj * 16 * kSolveLD + bj * 16 + cq * 4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = 0; m < 16; m += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(L + rr * ldl + m);
+            const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int t = 0; t < 4 * d; ++t) {
-                const float4 a = *reinterpret_cast<const float4 *>(arow + 4 * t);
-                const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 tv = *reinterpret_cast<const float4 *>(tcol + (4 * t + e) * kSolveLD);
-                    acc.x = fmaf(av[e], tv.x, acc.x);
-                    acc.y = fmaf(av[e], tv.y, acc.y);
-                    acc.z = fmaf(av[e], tv.z, acc.z);
-                    acc.w = fmaf(av[e], tv.w, acc.w);
-                }
+            for (int e = 0; e < 4; ++e) {
+                const float4 r = *reinterpret_cast<const float4 *>(R + (m + e) * ldr + cq * 4);
+                acc.x = fmaf(av[e], r.x, acc.x);
+                acc.y = fmaf(av[e], r.y, acc.y);
+                acc.z = fmaf(av[e], r.z, acc.z);
+                acc.w = fmaf(av[e], r.w, acc.w);
             }
-            *reinterpret_cast<float4 *>(sX + (blk * 16 + rr) * kSolveLDX + cq * 4) = acc;
         }
-        solve_barrier<NT, BarId>();
-        for (int s = tid; s < nstrip; s += NT) {
-            const int blk = s >> 6, cq = (s >> 4) & 3, rr = s & 15;
-            const int bi = d + blk, bj = blk;
-            const float *trow = sT + (bi * 16 + rr) * kSolveLD + bi * 16;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < 16; m += 4) {
-                const float4 t = *reinterpret_cast<const float4 *>(trow + m);
-                const float tv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 xv = *reinterpret_cast<const float4 *>(sX + (blk * 16 + m + e) * kSolveLDX + cq * 4);
-                    acc.x = fmaf(tv[e], xv.x, acc.x);
-                    acc.y = fmaf(tv[e], xv.y, acc.y);
-                    acc.z = fmaf(tv[e], xv.z, acc.z);
-                    acc.w = fmaf(tv[e], xv.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4 *>(sT + (bi * 16 + rr) * kSolveLD + bj * 16 + cq * 4) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        solve_barrier<NT, BarId>();
+        return acc;
+    };
+    constexpr int LD = kSolveLD, LX = kSolveLDX;
+    // block (i, j) of A / T, and C_ij kept in A's block (j, i)
+    auto blkA = [&](int i, int j) { return sA + i * 16 * LD + j * 16; };
+    auto blkT = [&](int i, int j) { return sT + i * 16 * LD + j * 16; };
+    auto blkC = [&](int i, int j) { return const_cast<float *>(sA) + j * 16 * LD + i * 16; };
+    float *X20 = sX, *X31 = sX + 16 * LX, *X30 = sX + 32 * LX;
+    // lower block b = 0..5: (1, 0), (2, 0), (3, 0), (2, 1), (3, 1), (3, 2)
+    auto low_i = [](int b) { return b < 3 ? b + 1 : (b < 5 ? b - 1 : 3); };
+    auto low_j = [](int b) { return b < 3 ? 0 : (b < 5 ? 1 : 2); };
+    // phase 1: C_ij = T_ii A_ij
+    for (int s = tid; s < 6 * 64; s += NT) {
+        const int b = s >> 6, rr = s & 15, cq = (s >> 4) & 3;
+        const int i = low_i(b), j = low_j(b);
+        const float4 c = strip(blkT(i, i), LD, blkA(i, j), LD, rr, cq);
+        *reinterpret_cast<float4 *>(blkC(i, j) + rr * LD + cq * 4) = c;
     }
+    solve_barrier<NT, BarId>();
+    // phase 2: P_20 = C_20 - C_21 C_10, P_31 = C_31 - C_32 C_21, Q_30 = C_30 - C_31 C_10
+    for (int s = tid; s < 3 * 64; s += NT) {
+        const int b = s >> 6, rr = s & 15, cq = (s >> 4) & 3;
+        // b = 0: (i, k, j) = (2, 1, 0); b = 1: (3, 2, 1); b = 2: (3, 1, 0)
+        const int i = b == 0 ? 2 : 3, k = b == 1 ? 2 : 1, j = b == 1 ? 1 : 0;
+        const float4 pr = strip(blkC(i, k), LD, blkC(k, j), LD, rr, cq);
+        const float4 c = *reinterpret_cast<const float4 *>(blkC(i, j) + rr * LD + cq * 4);
+        float *dst = (b == 0 ? X20 : b == 1 ? X31 : X30) + rr * LX + cq * 4;
+        *reinterpret_cast<float4 *>(dst) = make_float4(c.x - pr.x, c.y - pr.y, c.z - pr.z, c.w - pr.w);
+    }
+    solve_barrier<NT, BarId>();
+    // phase 3: P_30 = Q_30 - C_32 P_20 (in place)
+    for (int s = tid; s < 64; s += NT) {
+        const int rr = s & 15, cq = (s >> 4) & 3;
+        const float4 pr = strip(blkC(3, 2), LD, X20, LX, rr, cq);
+        float4 *dst = reinterpret_cast<float4 *>(X30 + rr * LX + cq * 4);
+        const float4 q = *dst;
+        *dst = make_float4(q.x - pr.x, q.y - pr.y, q.z - pr.z, q.w - pr.w);
+    }
+    solve_barrier<NT, BarId>();
+    // phase 4: T_ij = -P_ij T_jj
+    for (int s = tid; s < 6 * 64; s += NT) {
+        const int b = s >> 6, rr = s & 15, cq = (s >> 4) & 3;
+        const int i = low_i(b), j = low_j(b);
+        const float *P;
+        int ldp;
+        if (i - j == 1) {
+            P = blkC(i, j);
+            ldp = LD;
+        } else {
+            P = (i == 2 ? X20 : j == 1 ? X31 : X30);
+            ldp = LX;
+        }
+        const float4 t = strip(P, ldp, blkT(j, j), LD, rr, cq);
+        *reinterpret_cast<float4 *>(blkT(i, j) + rr * LD + cq * 4) = make_float4(-t.x, -t.y, -t.z, -t.w);
+    }
+    solve_barrier<NT, BarId>();
 }
 
 }  // namespace gcl
