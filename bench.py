@@ -116,7 +116,10 @@ def bf16_peak():
 
 
 def tensor_path(w) -> bool:
-    return w.dtype == "bf16" and w.K == 128 and w.V == 128 and w.bt == 64
+    """The workload's forward runs on the tensor cores: bf16 inputs (GDN and KDA), or fp16
+    inputs for GDN, at d_k = d_v = 128 and chunk 64 (fp16 and bf16 share one tensor-core rate)."""
+    typed = w.dtype == "bf16" or (w.dtype == "f16" and w.variant == synth.GDN)
+    return typed and w.K == 128 and w.V == 128 and w.bt == 64
 
 
 def roofline(w, kernel_ms, traffic=None, kind="forward"):
@@ -359,7 +362,7 @@ def launches_per_step(w) -> int:
     kernels; otherwise the sweep and one chunk-gradient kernel)."""
     plan = fwd_plan_of(w)
     fwd = {"cuda_cores": 1, "fused": 1, "w_form": 2, "transition": 2, "segmented": 4}[plan]
-    tc_bwd = tensor_path(w) and w.variant == synth.GDN
+    tc_bwd = tensor_path(w) and w.variant == synth.GDN and w.dtype == "bf16"
     return 1 + fwd + ((3 if tc_bwd else 2) if w.backward else 0)
 
 

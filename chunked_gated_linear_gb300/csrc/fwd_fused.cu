@@ -1,6 +1,6 @@
 // fwd_fused.cu -- the fused tensor-core GDN chunk forward: one CTA per (sequence, head)
-// carries the whole Map-Reduce-Map of its chunks on chip (bf16 inputs, d_k = d_v = 128,
-// chunk 64).  Nothing but q, k, v, g, beta, h0 is read and nothing but o, ht (and h_save)
+// carries the whole Map-Reduce-Map of its chunks on chip (bf16 or fp16 inputs, d_k = d_v = 128,
+// chunk 64; every MMA operand in the input type, "bf16" below standing for either).  Nothing but q, k, v, g, beta, h0 is read and nothing but o, ht (and h_save)
 // is written: no per-chunk records go through HBM.
 //
 // HA-NPU paper "Empowering Hybrid Attention Models on NPUs": section 2.1 (Map-Reduce-Map),
@@ -33,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include "gcl_internal.cuh"
+#include "op16.cuh"
 #include "tc_ptx.cuh"
 #include "tc_solve.cuh"
 
@@ -50,9 +51,9 @@ constexpr int kGateWarp = 5;      // forms the gate vectors, one chunk ahead
 struct FusedParams {
     const int32_t *cu, *chunk_offsets, *seq_order;
     const float *g;
-    const __nv_bfloat16 *beta;
+    const void *beta;             // [t_max, H] of the input type
     const float *h0;
-    __nv_bfloat16 *o;
+    void *o;                      // [t_max, H, V] of the input type
     float *ht, *h_save;
     int32_t *status;
     int64_t t_max, nt_max;
@@ -88,10 +89,6 @@ constexpr uint32_t cS = 0, cD4 = 0, cX = 64, cE32 = 64, cO = 128, cD1 = 192, cR 
                    cEB = 224;
 constexpr uint32_t kTmemCols = 256;
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&t);
-}
 
 __device__ __forceinline__ float warp_incl_scan(float x) {
     const int lane = threadIdx.x & 31;
@@ -103,6 +100,9 @@ __device__ __forceinline__ float warp_incl_scan(float x) {
     return x;
 }
 
+// T: the input type (bf16, or fp16), which every MMA operand the kernel forms shares (one
+// kind::f16 instruction takes A and B of the same type).
+template <typename T>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, FusedParams p) {
@@ -210,7 +210,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int q = 0; q < 2; ++q) {
             uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(S[q * 32 + 2 * j], S[q * 32 + 2 * j + 1]);
+            for (int j = 0; j < 16; ++j) pk[j] = Op16<T>::pack2(S[q * 32 + 2 * j], S[q * 32 + 2 * j + 1]);
             tmem_st16_b32(tmem + lane_off + cS + half * 32 + q * 16, pk);
         }
         tmem_st_wait();
@@ -239,7 +239,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int r = 2 * lane + e;
             const bool ok = r < len1 && GCL_IN_BOUNDS((t + r) * H + h, p.t_max * H, p.status);
             g_next[e] = ok ? p.g[(t + r) * H + h] : 0.f;
-            b_next[e] = ok ? __bfloat162float(p.beta[(t + r) * H + h]) : 0.f;
+            b_next[e] = ok ? Op16<T>::to_float(static_cast<const T *>(p.beta)[(t + r) * H + h]) : 0.f;
         }
     };
     // gamma (inclusive cumsum; rows past the end have g = 0), beta, Gamma = exp(gamma),
@@ -281,7 +281,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float *sAf = reinterpret_cast<float *>(smem + Lay::oA);
     float *sTf = reinterpret_cast<float *>(smem + Lay::oTf);
     float *sXf = reinterpret_cast<float *>(smem + Lay::oX);
-    __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + Lay::oO);
+    T *sO = reinterpret_cast<T *>(smem + Lay::oO);
 
     for (int ic = 0; ic < nch; ++ic) {
         const int len = chunk_len(ic);
@@ -306,7 +306,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         if (issuer) {
             // MMA1: D1 = [K; Q] K^T (M = 128, N = 64, K = 128)
-            constexpr uint32_t id1 = idesc_bf16(128, 64);
+            constexpr uint32_t id1 = idesc_f16kind(128, 64, 0, 0, Op16<T>::fmt);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
@@ -315,7 +315,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             mma_commit(&bar_m1);
             // MMA2: [X | Y] = S^T [K; Q]^T (N = 128): X = (K S)^T, Y = (Q S)^T
-            constexpr uint32_t id2 = idesc_bf16(128, 128);
+            constexpr uint32_t id2 = idesc_f16kind(128, 128, 0, 0, Op16<T>::fmt);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
@@ -374,7 +374,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             const int c = c0 + j + 2 * e;
                             const float l0 = (live && c <= r) ? rowf * dec[j + 2 * e] * d[j + 2 * e] : 0.f;
                             const float l1 = (live && c + 1 <= r) ? rowf * dec[j + 2 * e + 1] * d[j + 2 * e + 1] : 0.f;
-                            pw[e] = pack_bf16(l0, l1);
+                            pw[e] = Op16<T>::pack2(l0, l1);
                         }
                         if (GCL_RANGE_IN_BOUNDS(sw128_offset(C, r, c0 + j), sw128_offset(C, r, c0 + j) + 15, 8192, p.status))
                             *reinterpret_cast<uint4 *>(smem + Lay::oL + sw128_offset(C, r, c0 + j)) = pk;
@@ -404,7 +404,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = cq + j + 2 * e;
-                    pw[e] = pack_bf16(c <= r ? sTf[r * kSolveLD + c] : 0.f,
+                    pw[e] = Op16<T>::pack2(c <= r ? sTf[r * kSolveLD + c] : 0.f,
                                       c + 1 <= r ? sTf[r * kSolveLD + c + 1] : 0.f);
                 }
                 if (GCL_RANGE_IN_BOUNDS(sw128_offset(C, r, cq + j), sw128_offset(C, r, cq + j) + 15, 8192, p.status))
@@ -439,13 +439,13 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const int voff = vb * 8192 + (vc & 7) * 2 + (r >> 3) * 1024 + (r & 7) * 128 +
                                          ((((vc >> 3) ^ (r & 7))) << 4);
                         const float vv = GCL_IN_BOUNDS(voff, 16384, p.status)
-                                             ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                             ? Op16<T>::to_float(*reinterpret_cast<const T *>(
                                                    vcol + (r >> 3) * 1024 + (r & 7) * 128 + ((((vc >> 3) ^ (r & 7))) << 4)))
                                              : 0.f;
                         rr[e] = r < len ? bb[e] * (vv - gg[e] * x[j + e]) : 0.f;
                     }
-                    pk[j >> 1] = pack_bf16(rr[0], rr[1]);
-                    pk[(j >> 1) + 1] = pack_bf16(rr[2], rr[3]);
+                    pk[j >> 1] = Op16<T>::pack2(rr[0], rr[1]);
+                    pk[(j >> 1) + 1] = Op16<T>::pack2(rr[2], rr[3]);
                 }
                 tmem_st8_b32(tmem + lane_off + cR + hh * 8, pk);
             }
@@ -461,7 +461,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         if (issuer) {
             // MMA3: E^T = R^T T^T (M = 128, N = 64, K = 64)
-            constexpr uint32_t id = idesc_bf16(128, 64);
+            constexpr uint32_t id = idesc_f16kind(128, 64, 0, 0, Op16<T>::fmt);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16_ta(tmem + cE32, tmem + cR + s * 8,
@@ -482,10 +482,10 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int j = 0; j < 16; j += 4) {
                 const float4 f4 = *reinterpret_cast<const float4 *>(sF + c0 + j);
-                pe[j >> 1] = pack_bf16(e16[j], e16[j + 1]);
-                pe[(j >> 1) + 1] = pack_bf16(e16[j + 2], e16[j + 3]);
-                pf[j >> 1] = pack_bf16(f4.x * e16[j], f4.y * e16[j + 1]);
-                pf[(j >> 1) + 1] = pack_bf16(f4.z * e16[j + 2], f4.w * e16[j + 3]);
+                pe[j >> 1] = Op16<T>::pack2(e16[j], e16[j + 1]);
+                pe[(j >> 1) + 1] = Op16<T>::pack2(e16[j + 2], e16[j + 3]);
+                pf[j >> 1] = Op16<T>::pack2(f4.x * e16[j], f4.y * e16[j + 1]);
+                pf[(j >> 1) + 1] = Op16<T>::pack2(f4.z * e16[j + 2], f4.w * e16[j + 3]);
             }
             tmem_st8_b32(tmem + lane_off + cEB + (c0 >> 1), pe);
             tmem_st8_b32(tmem + lane_off + cEF + (c0 >> 1), pf);
@@ -509,12 +509,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         if (issuer) {
             // MMA4: dS^T = (E^T diag f) K (M = 128, N = 128 keys, K = 64 rows; K MN-major)
-            constexpr uint32_t id4 = idesc_bf16(128, 128, 0, 1);
+            constexpr uint32_t id4 = idesc_f16kind(128, 128, 0, 1, Op16<T>::fmt);
             const uint64_t dk = smem_desc(sbase + Lay::oKQ, 16384, 1024, kSwizzle128B);
 #pragma unroll
             for (int s = 0; s < 4; ++s) mma_bf16_ta(tmem + cD4, tmem + cEF + s * 8, dk + s * 128, id4, s > 0);
             // MMA5: O^T += E^T L^T (N = 64, K = 64)
-            constexpr uint32_t id5 = idesc_bf16(128, 64);
+            constexpr uint32_t id5 = idesc_f16kind(128, 64, 0, 0, Op16<T>::fmt);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16_ta(tmem + cO, tmem + cEB + s * 8,
@@ -549,7 +549,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (GCL_IN_BOUNDS((half * 32 + hh * 16 + j) * kOLD + m, C * kOLD, p.status))
-                        sO[(half * 32 + hh * 16 + j) * kOLD + m] = __float2bfloat16_rn(ov[j]);
+                        sO[(half * 32 + hh * 16 + j) * kOLD + m] = Op16<T>::from_float(ov[j]);
             }
         }
         tc_fence_before();
@@ -564,7 +564,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     !GCL_RANGE_IN_BOUNDS(r * kOLD + cc, r * kOLD + cc + 7, C * kOLD, p.status))
                     continue;
                 const uint4 val = *reinterpret_cast<const uint4 *>(sO + r * kOLD + cc);
-                *reinterpret_cast<uint4 *>(p.o + ((t0 + r) * H + h) * (int64_t)VD + cc) = val;
+                *reinterpret_cast<uint4 *>(static_cast<T *>(p.o) + ((t0 + r) * H + h) * (int64_t)VD + cc) = val;
             }
         }
         // a wait that gave up (s_err) ends every thread's loop at the same chunk
@@ -606,18 +606,20 @@ cudaError_t launch_fwd_fused(const FwdParams &p, cudaStream_t s) {
     const cuuint32_t b64[3] = {64, 1, 64};
     const cuuint64_t dv[3] = {(cuuint64_t)VD, (cuuint64_t)H, (cuuint64_t)p.t_max};
     const cuuint64_t sv[2] = {(cuuint64_t)VD * 2, (cuuint64_t)H * VD * 2};
-    if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B))
+    const CUtensorMapDataType dt = p.dtype == GCL_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_tensor_map(&mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B, dt) ||
+        !make_tensor_map(&mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B, dt) ||
+        !make_tensor_map(&mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B, dt))
         return cudaErrorInvalidValue;
     FusedParams fp{};
     fp.cu = p.cu_seqlens;
     fp.chunk_offsets = p.chunk_offsets;
     fp.seq_order = p.seq_order;
     fp.g = p.g;
-    fp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
+    fp.beta = p.beta;
     fp.h0 = p.h0;
-    fp.o = static_cast<__nv_bfloat16 *>(p.o);
+    fp.o = p.o;
     fp.ht = p.ht;
     fp.h_save = p.h_save;
     fp.status = p.dev_status;
@@ -626,10 +628,11 @@ cudaError_t launch_fwd_fused(const FwdParams &p, cudaStream_t s) {
     fp.n_max = p.n_max;
     fp.H = H;
     fp.scale = p.scale;
-    cudaError_t e = cudaFuncSetAttribute(tc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = p.dtype == GCL_F16 ? tc_fused_kernel<__half> : tc_fused_kernel<__nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)FusedLayout::bytes);
     if (e != cudaSuccess) return e;
-    tc_fused_kernel<<<dim3(H, p.n_max), kThreads, FusedLayout::bytes, s>>>(mq, mk, mv, fp);
+    kern<<<dim3(H, p.n_max), kThreads, FusedLayout::bytes, s>>>(mq, mk, mv, fp);
     return cudaGetLastError();
 }
 

@@ -706,8 +706,15 @@ bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 inputs for GDN and KDA; fp16 inputs for the GDN forward (the transition and fused
+// plans, with every MMA operand and record in fp16).  The backward takes bf16 only
+// (bwd_tc_supported).
 bool fwd_tc_supported(int variant, int dtype, int K, int V, int bt) {
-    return (variant == kGDN || variant == kKDA) && dtype == GCL_BF16 && K == KD && V == VD && bt == kChunk;
+    const bool type_ok = dtype == GCL_BF16 || (dtype == GCL_F16 && variant == kGDN);
+    return (variant == kGDN || variant == kKDA) && type_ok && K == KD && V == VD && bt == kChunk;
+}
+bool bwd_tc_supported(int variant, int dtype, int K, int V, int bt) {
+    return dtype == GCL_BF16 && fwd_tc_supported(variant, dtype, K, V, bt);
 }
 
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H) {
@@ -730,14 +737,15 @@ bool fwd_tc_prefers_transition(int n_max, int H) { return fwd_tc_split(n_max, H)
 // training forward (h_save: its records are what the backward's sweep reads, so the backward
 // can take them instead of recomputing them), whenever the workspace holds the records.  KDA
 // has the transition plan only.
-bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max) {
-    if (variant == kKDA) return true;
+bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max,
+                            int dtype) {
+    if (variant == kKDA || dtype == GCL_F16) return true;    // (the W form is bf16 only)
     return (fwd_tc_prefers_transition(n_max, H) || h_save) && ws_bytes >= fwd_tc_t_workspace_bytes(nt_max, H);
 }
 
-int fwd_tc_plan(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max) {
+int fwd_tc_plan(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max, int dtype) {
     if (fwd_tc_runs_fused(variant, n_max, H, h_save, ws_bytes, nt_max)) return GCL_PLAN_FUSED;
-    if (fwd_tc_runs_transition(variant, n_max, H, h_save, ws_bytes, nt_max)) {
+    if (fwd_tc_runs_transition(variant, n_max, H, h_save, ws_bytes, nt_max, dtype)) {
         const size_t rec = fwd_tc_t_workspace_bytes(nt_max, H);
         const size_t seg = fwd_seg_workspace_bytes(nt_max, n_max, H);
         return seg > 0 && ws_bytes >= rec + seg ? GCL_PLAN_SEGMENTED : GCL_PLAN_TRANSITION;
@@ -753,8 +761,11 @@ cudaError_t launch_fwd_tc(const FwdParams &p, int variant, cudaStream_t s) {
         if (p.workspace_bytes < fwd_tc_t_workspace_bytes(p.nt_max, H)) return cudaErrorInvalidValue;
         return launch_fwd_tc_kda(p, fwd_tc_split(p.n_max, H), s);
     }
-    if (fwd_tc_runs_transition(variant, p.n_max, H, p.h_save != nullptr, p.workspace_bytes, p.nt_max))
+    if (fwd_tc_runs_transition(variant, p.n_max, H, p.h_save != nullptr, p.workspace_bytes, p.nt_max,
+                               p.dtype)) {
+        if (p.workspace_bytes < fwd_tc_t_workspace_bytes(p.nt_max, H)) return cudaErrorInvalidValue;
         return launch_fwd_tc_t(p, fwd_tc_split(p.n_max, H), s);
+    }
     const int64_t units = p.nt_max * H;              // chunk-head slots of the workspace
     __nv_bfloat16 *tl = static_cast<__nv_bfloat16 *>(p.workspace);
     float *fac = reinterpret_cast<float *>(tl + (size_t)units * kTLRows * C);

@@ -154,7 +154,8 @@ tc_prep_kda_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             gq[j] = r < it.len ? *reinterpret_cast<const float4 *>(p.g + ((it.t0 + r) * H + it.h) * (int64_t)KD + lane * 4)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        bv = tid < it.len ? __bfloat162float(p.beta[(it.t0 + tid) * H + it.h]) : 0.f;
+        bv = tid < it.len ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[(it.t0 + tid) * H + it.h])
+                          : 0.f;
     };
     float4 gq[8];
     float b_raw;

@@ -1,6 +1,7 @@
-// fwd_tc_transition.cu -- GDN chunk forward in transition form (bf16, d_k = d_v = 128,
-// chunk 64), for launches whose serial chain dominates: few (sequence, head) units,
-// each split over 4 or 8 value-column slices.
+// fwd_tc_transition.cu -- GDN chunk forward in transition form (bf16 or fp16 inputs, d_k =
+// d_v = 128, chunk 64), for launches whose serial chain dominates: few (sequence, head)
+// units, each split over 4 or 8 value-column slices.  Every MMA operand and record has the
+// input type ("bf16" below stands for either; the KDA records are bf16).
 //
 // HA-NPU paper "Empowering Hybrid Attention Models on NPUs", section 2.1: the Map
 // phases are chunk-parallel, only the Reduce is serial; section 5: the
@@ -55,6 +56,9 @@ static_assert(pEnd - pA >= 4 * 8192, "[W | U] (4 atoms of 8 KiB) reuses the solv
 // Persistent: gridDim.x CTAs (two per SM) walk the items with stride gridDim.x.  The next
 // item's K and Q tiles are requested as soon as MMA3 has consumed the current ones, its V tile
 // once the output stores have read their staging buffers, and its gates during MMA3.
+// T: the input type (bf16, or fp16 for GDN); every MMA operand the kernel forms and every
+// record it writes has the same type.
+template <typename T>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rec,
@@ -116,7 +120,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (tid < it.len) {
             if (GCL_IN_BOUNDS((it.t0 + tid) * H + it.h, p.t_max * H, p.status)) {
                 gv = p.g[(it.t0 + tid) * H + it.h];
-                bv = __bfloat162float(p.beta[(it.t0 + tid) * H + it.h]);
+                bv = Op16<T>::to_float(static_cast<const T *>(p.beta)[(it.t0 + tid) * H + it.h]);
             }
         }
     };
@@ -200,7 +204,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // ---- MMA1: [K; Q] K^T -> lanes 0..63: K K^T, lanes 64..127: Q K^T  (N = 64)
             if (tid == 0) {
                 const uint64_t d = smem_desc(sbase + pKQ, 16, 1024, kSwizzle128B);
-                constexpr uint32_t id = idesc_bf16(128, 64);
+                constexpr uint32_t id = idesc_f16kind(128, 64, 0, 0, Op16<T>::fmt);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint64_t o = (s >> 2) * 1024 + (s & 3) * 2;
@@ -244,7 +248,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             l[e] = (col <= r && r < len) ? p.scale * dec[q * 8 + e] * v[q * 8 + e] : 0.f;
                         }
                         *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, 2 * C + r, half * 32 + q * 8)) =
-                            pack8(l);
+                            pack8_as<T>(l);
                     }
                 }
             }
@@ -273,8 +277,8 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tb[e] = c0 + e <= r ? sT[r * kSolveLD + c0 + e] * sB[c0 + e] : 0.f;
                         tg[e] = tb[e] * sEG[c0 + e];
                     }
-                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, r, c0)) = pack8(tg);
-                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, C + r, c0)) = pack8(tb);
+                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, r, c0)) = pack8_as<T>(tg);
+                    *reinterpret_cast<uint4 *>(smem + pTL + kmaj16(192, C + r, c0)) = pack8_as<T>(tb);
                 }
             }
             to_async();
@@ -285,7 +289,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint64_t a = smem_desc(sbase + pTL, 16, 1024, kSwizzle128B);
                 const uint64_t bk = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
                 const uint64_t bv = smem_desc(sbase + pV, 8192, 1024, kSwizzle128B);
-                constexpr uint32_t id = idesc_bf16(128, 128, 0, 1);
+                constexpr uint32_t id = idesc_f16kind(128, 128, 0, 1, Op16<T>::fmt);
 #pragma unroll
                 for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, bk + s * 128, id, s > 0);
 #pragma unroll
@@ -302,20 +306,17 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<uint4 *>(smem + pA + mnmaj16(8192, tok, n0 + q * 8)) = pack8(wu + q * 8);
+                    *reinterpret_cast<uint4 *>(smem + pA + mnmaj16(8192, tok, n0 + q * 8)) = pack8_as<T>(wu + q * 8);
                 // Ktil = diag(exp(g_c - g)) K, in place (MMA2 has consumed K)
                 for (int t = tid; t < 2 * C * 8; t += kPrepThreads) {
                     const int r = (t >> 3) & 63, cb = t >> 9;
                     uint4 *pk = reinterpret_cast<uint4 *>(smem + pKQ + cb * 16384 + r * 128 + (t & 7) * 16);
-                    uint4 x = *pk;
-                    __nv_bfloat162 *xx = reinterpret_cast<__nv_bfloat162 *>(&x);
+                    float y[8];
+                    unpack8_as<T>(*pk, y);
                     const float f = sF[r];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 y = __bfloat1622float2(xx[e]);
-                        xx[e] = __floats2bfloat162_rn(f * y.x, f * y.y);
-                    }
-                    *pk = x;
+                    for (int e = 0; e < 8; ++e) y[e] *= f;
+                    *pk = pack8_as<T>(y);
                 }
             }
             to_async();
@@ -323,7 +324,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (tid == 0) {
                 const uint64_t a = smem_desc(sbase + pTL + 8192, 16, 1024, kSwizzle128B);
                 const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
-                constexpr uint32_t id = idesc_bf16(128, 256, 0, 1);
+                constexpr uint32_t id = idesc_f16kind(128, 256, 0, 1, Op16<T>::fmt);
 #pragma unroll
                 for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 2, b + s * 128, id, s > 0);
                 mma_commit(&bar_mma);
@@ -342,16 +343,11 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const int c = half * 64 + q * 8;
-                    const uint4 qv = *reinterpret_cast<const uint4 *>(smem + pKQ + kmaj16(128, C + r, c));
-                    const __nv_bfloat162 *qq = reinterpret_cast<const __nv_bfloat162 *>(&qv);
-                    float y[8];
+                    float qf[8], y[8];
+                    unpack8_as<T>(*reinterpret_cast<const uint4 *>(smem + pKQ + kmaj16(128, C + r, c)), qf);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f2 = __bfloat1622float2(qq[e]);
-                        y[2 * e] = live ? fmaf(fq, f2.x, -x[q * 8 + 2 * e]) : 0.f;
-                        y[2 * e + 1] = live ? fmaf(fq, f2.y, -x[q * 8 + 2 * e + 1]) : 0.f;
-                    }
-                    *reinterpret_cast<uint4 *>(box_chunk(pV + half * 8192, r, q)) = pack8(y);
+                    for (int e = 0; e < 8; ++e) y[e] = live ? fmaf(fq, qf[e], -x[q * 8 + e]) : 0.f;
+                    *reinterpret_cast<uint4 *>(box_chunk(pV + half * 8192, r, q)) = pack8_as<T>(y);
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, x + q * 16);
@@ -361,7 +357,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     float z[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) z[e] = live ? x[q * 8 + e] : 0.f;
-                    *reinterpret_cast<uint4 *>(box_chunk(pTL + half * 8192, r, q)) = pack8(z);
+                    *reinterpret_cast<uint4 *>(box_chunk(pTL + half * 8192, r, q)) = pack8_as<T>(z);
                 }
             }
             if (tid == 0) {
@@ -380,7 +376,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (tid == 0) {
                 const uint64_t a = smem_desc(sbase + pKQ, 16384, 1024, kSwizzle128B);
                 const uint64_t b = smem_desc(sbase + pA, 8192, 1024, kSwizzle128B);
-                constexpr uint32_t id = idesc_bf16(128, 256, 1, 1);
+                constexpr uint32_t id = idesc_f16kind(128, 256, 1, 1, Op16<T>::fmt);
 #pragma unroll
                 for (int s = 0; s < 4; ++s) mma_bf16(tmem, a + s * 128, b + s * 128, id, s > 0);
                 mma_commit(&bar_mma);
@@ -412,7 +408,7 @@ tc_prep_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         float y[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) y[e] = sg * x[q * 8 + e];
-                        *reinterpret_cast<uint4 *>(box_chunk(box, m & 63, q)) = pack8(y);
+                        *reinterpret_cast<uint4 *>(box_chunk(box, m & 63, q)) = pack8_as<T>(y);
                     }
                 }
             }
@@ -451,7 +447,7 @@ struct ChainTParams {
     const int32_t *cu, *chunk_offsets, *seq_order;
     const float *h0;
     const uint8_t *ws;
-    __nv_bfloat16 *o;
+    void *o;                     // [t_max, H, V] of the input type
     float *ht, *h_save;
     int32_t *status;
     int64_t t_max, nt_max;
@@ -511,7 +507,8 @@ constexpr int kChainThreads = 32 * (kWarpTma + 1);
 // fall two phases behind.  After a failed (timed-out) wait every further wait returns at once, so
 // all loops run to their ends without a uniform break.
 // KDA: Gamma_c is a per-key-channel vector (the state row of thread t decays by its own entry).
-template <int VS, int NS, bool KDA>
+// T: the records' and the state copies' type (the input type: bf16, or fp16 for GDN).
+template <int VS, int NS, bool KDA, typename T>
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_constant__ CUtensorMap tm_b,
                   const __grid_constant__ CUtensorMap tm_z, ChainTParams p) {
@@ -593,7 +590,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    constexpr uint32_t idm = idesc_bf16(128, VS, 0, 1);
+    constexpr uint32_t idm = idesc_f16kind(128, VS, 0, 1, Op16<T>::fmt);
     auto dS = [&](int ic) {                          // S(ic) as the MN-major B operand
         return smem_desc(sbase + Lay::oSB + (ic % Lay::kSB) * 16384, 8192, 1024, kSwizzle128B);
     };
@@ -686,19 +683,15 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                                     ((t0 + orow) * H + h) * (int64_t)VD + v0 + VS - 1,
                                     p.t_max * H * (int64_t)VD, p.status)) {
                 const uint8_t *zrow = stage + Lay::oZ + orow * (VS * 2);
-                __nv_bfloat16 *dst = p.o + ((t0 + orow) * H + h) * (int64_t)VD + v0;
+                T *dst = static_cast<T *>(p.o) + ((t0 + orow) * H + h) * (int64_t)VD + v0;
 #pragma unroll
                 for (int j = 0; j < VS; j += 8) {
-                    const uint4 zv = *reinterpret_cast<const uint4 *>(zrow + j * 2);
-                    const __nv_bfloat162 *zz = reinterpret_cast<const __nv_bfloat162 *>(&zv);
+                    float zf[8];
+                    unpack8_as<T>(*reinterpret_cast<const uint4 *>(zrow + j * 2), zf);
                     float ov[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 z2 = __bfloat1622float2(zz[e]);
-                        ov[2 * e] = d2[j + 2 * e] + z2.x;
-                        ov[2 * e + 1] = d2[j + 2 * e + 1] + z2.y;
-                    }
-                    *reinterpret_cast<uint4 *>(dst + j) = pack8(ov);
+                    for (int e = 0; e < 8; ++e) ov[e] = d2[j + e] + zf[e];
+                    *reinterpret_cast<uint4 *>(dst + j) = pack8_as<T>(ov);
                 }
             }
             __syncwarp();
@@ -711,7 +704,7 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
 #pragma unroll
             for (int j = 0; j < HV; j += 8)
                 *reinterpret_cast<uint4 *>(smem + Lay::oSB + buf * 16384 + mn_sw128(row, c0 + j)) =
-                    pack8(x + j);
+                    pack8_as<T>(x + j);
         };
         auto handoff = [&](int ic) {                      // this warp's part of S(ic) is in its buffer
             fence_async_smem();
@@ -760,14 +753,10 @@ tc_chain_t_kernel(const __grid_constant__ CUtensorMap tm_yn, const __grid_consta
                 const uint8_t *brow = stage + Lay::oB + row * (VS * 2) + c0 * 2;
 #pragma unroll
                 for (int j = 0; j < HV; j += 8) {
-                    const uint4 bv = *reinterpret_cast<const uint4 *>(brow + j * 2);
-                    const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&bv);
+                    float bf[8];
+                    unpack8_as<T>(*reinterpret_cast<const uint4 *>(brow + j * 2), bf);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 b2 = __bfloat1622float2(bb[e]);
-                        S[j + 2 * e] = fmaf(gc, S[j + 2 * e], b2.x);
-                        S[j + 2 * e + 1] = fmaf(gc, S[j + 2 * e + 1], b2.y);
-                    }
+                    for (int e = 0; e < 8; ++e) S[j + e] = fmaf(gc, S[j + e], bf[e]);
                 }
             }
             {   // + N S(n): the G1 parts
@@ -940,7 +929,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(SegScanParams
     }
 }
 
-template <int VS, int NS, bool KDA>
+template <int VS, int NS, bool KDA, typename T>
 cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const ChainTParams &cp,
                            int n_split, int H, int n_max, cudaStream_t s) {
     using Lay = ChainTLayout<VS, NS>;
@@ -952,10 +941,10 @@ cudaError_t launch_chain_t(const CUtensorMap &myn, const uint8_t *ws, const Chai
     const cuuint32_t bb[3] = {(cuuint32_t)VS, (cuuint32_t)KD, 1};
     const cuuint64_t dz[3] = {(cuuint64_t)VD, (cuuint64_t)C, (cuuint64_t)units};
     const cuuint32_t bz[3] = {(cuuint32_t)VS, (cuuint32_t)C, 1};
-    if (!make_tensor_map(&mb, ws + kYNBytes, 3, db, sb, bb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tensor_map(&mz, ws + kYNBytes + kBBytes, 3, dz, sb, bz, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_tensor_map(&mb, ws + kYNBytes, 3, db, sb, bb, CU_TENSOR_MAP_SWIZZLE_NONE, Op16<T>::tma) ||
+        !make_tensor_map(&mz, ws + kYNBytes + kBBytes, 3, dz, sb, bz, CU_TENSOR_MAP_SWIZZLE_NONE, Op16<T>::tma))
         return cudaErrorInvalidValue;
-    auto kern = tc_chain_t_kernel<VS, NS, KDA>;
+    auto kern = tc_chain_t_kernel<VS, NS, KDA, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
@@ -986,10 +975,12 @@ bool make_prep_maps(const FwdParams &p, uint8_t *ws, CUtensorMap *mq, CUtensorMa
     static_assert(kUnitBytes % (KD * 2) == 0, "a record is whole rows");
     const cuuint64_t srec[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
     const cuuint32_t brec[3] = {64, 64, 1};
-    return make_tensor_map(mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(mrec, ws, 3, drec, srec, brec, CU_TENSOR_MAP_SWIZZLE_128B);
+    const CUtensorMapDataType dt = p.dtype == GCL_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return make_tensor_map(mq, p.q, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B, dt) &&
+           make_tensor_map(mk, p.k, 3, dqk, sqk, b64, CU_TENSOR_MAP_SWIZZLE_128B, dt) &&
+           make_tensor_map(mv, p.v, 3, dv, sv, b64, CU_TENSOR_MAP_SWIZZLE_128B, dt) &&
+           make_tensor_map(mrec, ws, 3, drec, srec, brec, CU_TENSOR_MAP_SWIZZLE_128B, dt);
 }
 
 tr::PrepTParams make_prep_params(const FwdParams &p, uint8_t *ws) {
@@ -997,7 +988,7 @@ tr::PrepTParams make_prep_params(const FwdParams &p, uint8_t *ws) {
     pp.chunk_indices = p.chunk_indices;
     pp.cu = p.cu_seqlens;
     pp.g = p.g;
-    pp.beta = static_cast<const __nv_bfloat16 *>(p.beta);
+    pp.beta = p.beta;
     pp.ws = ws;
     pp.status = p.dev_status;
     pp.t_max = p.t_max;
@@ -1008,17 +999,21 @@ tr::PrepTParams make_prep_params(const FwdParams &p, uint8_t *ws) {
     return pp;
 }
 
-cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
+template <typename T>
+cudaError_t launch_prep_t_as(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mrec;
     if (!make_prep_maps(p, ws, &mq, &mk, &mv, &mrec)) return cudaErrorInvalidValue;
     const PrepTParams pp = make_prep_params(p, ws);
-    cudaError_t e = cudaFuncSetAttribute(tc_prep_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kPrepTSmem);
+    auto kern = tc_prep_t_kernel<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepTSmem);
     if (e != cudaSuccess) return e;
     const int64_t units = p.nt_max * p.H;
     const int grid = (int)(units < 2 * (int64_t)num_sms() ? units : 2 * (int64_t)num_sms());
-    return launch_dependent(tc_prep_t_kernel, dim3(grid), dim3(kPrepThreads), kPrepTSmem, s, mq, mk, mv,
-                            mrec, pp);
+    return launch_dependent(kern, dim3(grid), dim3(kPrepThreads), kPrepTSmem, s, mq, mk, mv, mrec, pp);
+}
+cudaError_t launch_prep_t(const FwdParams &p, uint8_t *ws, cudaStream_t s) {
+    return p.dtype == GCL_F16 ? launch_prep_t_as<__half>(p, ws, s)
+                              : launch_prep_t_as<__nv_bfloat16>(p, ws, s);
 }
 
 // Segments per sequence: at most one wave of summary CTAs (8 slices of 32 columns per unit),
@@ -1049,15 +1044,17 @@ size_t fwd_seg_workspace_bytes(int64_t nt_max, int n_max, int H) {
     return (size_t)n_max * H * P * (size_t)(KD * 2 * VD + KD * VD) * sizeof(float);
 }
 
-cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int split, bool kda,
-                                 cudaStream_t s, int n_seg, float *seg_ws) {
+template <typename T, bool KDA>
+cudaError_t launch_chain_records_as(const FwdParams &p, const uint8_t *ws, int split,
+                                    cudaStream_t s, int n_seg, float *seg_ws) {
     const int H = p.H;
     const int64_t units = p.nt_max * H;
     CUtensorMap myn;
     const cuuint64_t dyn[3] = {(cuuint64_t)KD, (cuuint64_t)kYNRows, (cuuint64_t)units};
     const cuuint64_t syn[2] = {(cuuint64_t)KD * 2, (cuuint64_t)kUnitBytes};
     const cuuint32_t byn[3] = {64, (cuuint32_t)kYNRows, 1};
-    if (!make_tensor_map(&myn, ws, 3, dyn, syn, byn, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!make_tensor_map(&myn, ws, 3, dyn, syn, byn, CU_TENSOR_MAP_SWIZZLE_128B, Op16<T>::tma))
+        return cudaErrorInvalidValue;
 
     ChainTParams cp{};
     cp.cu = p.cu_seqlens;
@@ -1065,7 +1062,7 @@ cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int spli
     cp.seq_order = p.seq_order;
     cp.h0 = p.h0;
     cp.ws = ws;
-    cp.o = static_cast<__nv_bfloat16 *>(p.o);
+    cp.o = p.o;
     cp.ht = p.ht;
     cp.h_save = p.h_save;
     cp.status = p.dev_status;
@@ -1083,8 +1080,7 @@ cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int spli
         ca.ht = nullptr;
         ca.h_save = nullptr;
         ca.seg_sum = seg_ws;
-        cudaError_t e = kda ? launch_chain_t<32, 2, true>(myn, ws, ca, 8, H, p.n_max, s)
-                            : launch_chain_t<32, 2, false>(myn, ws, ca, 8, H, p.n_max, s);
+        cudaError_t e = launch_chain_t<32, 2, KDA, T>(myn, ws, ca, 8, H, p.n_max, s);
         if (e != cudaSuccess) return e;
         SegScanParams sp{};
         sp.cu = p.cu_seqlens;
@@ -1104,19 +1100,19 @@ cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int spli
         cp.mode = 2;
         cp.n_seg = n_seg;
         cp.seg_start = sp.seg_start;
-        return kda ? launch_chain_t<16, 3, true>(myn, ws, cp, 8, H, p.n_max, s)
-                   : launch_chain_t<16, 3, false>(myn, ws, cp, 8, H, p.n_max, s);
+        return launch_chain_t<16, 3, KDA, T>(myn, ws, cp, 8, H, p.n_max, s);
     }
-    if (kda) {
-        if (split == 8) return launch_chain_t<16, 3, true>(myn, ws, cp, split, H, p.n_max, s);
-        if (split == 4) return launch_chain_t<32, 2, true>(myn, ws, cp, split, H, p.n_max, s);
-        if (split == 2) return launch_chain_t<64, 2, true>(myn, ws, cp, split, H, p.n_max, s);
-        return cudaErrorInvalidValue;
-    }
-    if (split == 8) return launch_chain_t<16, 3, false>(myn, ws, cp, split, H, p.n_max, s);
-    if (split == 4) return launch_chain_t<32, 2, false>(myn, ws, cp, split, H, p.n_max, s);
-    if (split == 2) return launch_chain_t<64, 2, false>(myn, ws, cp, split, H, p.n_max, s);
+    if (split == 8) return launch_chain_t<16, 3, KDA, T>(myn, ws, cp, split, H, p.n_max, s);
+    if (split == 4) return launch_chain_t<32, 2, KDA, T>(myn, ws, cp, split, H, p.n_max, s);
+    if (split == 2) return launch_chain_t<64, 2, KDA, T>(myn, ws, cp, split, H, p.n_max, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_chain_records(const FwdParams &p, const uint8_t *ws, int split, bool kda,
+                                 cudaStream_t s, int n_seg, float *seg_ws) {
+    if (kda) return launch_chain_records_as<__nv_bfloat16, true>(p, ws, split, s, n_seg, seg_ws);
+    if (p.dtype == GCL_F16) return launch_chain_records_as<__half, false>(p, ws, split, s, n_seg, seg_ws);
+    return launch_chain_records_as<__nv_bfloat16, false>(p, ws, split, s, n_seg, seg_ws);
 }
 
 void fwd_seg_plan(const FwdParams &p, uint8_t *ws, int *n_seg, float **seg_ws) {

@@ -89,7 +89,8 @@ static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
         return 0;
     // the transition form, with the segment buffers when the fastest plan is segmented
     const size_t seg = fastest ? fwd_seg_workspace_bytes(ntm, a->n_max, a->H) : 0;
-    if (variant == kKDA) return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
+    if (variant == kKDA || a->dtype == GCL_F16)     // the transition form only (no W form)
+        return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
     if (fastest && (fwd_tc_prefers_transition(a->n_max, a->H) || a->h_save))
         return fwd_tc_t_workspace_bytes(ntm, a->H) + seg + kWsAlign;
     return fwd_tc_workspace_bytes(ntm, a->H) + kWsAlign;
@@ -133,6 +134,7 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V; p.bt = a->bt;
     p.nt_max = ntm;
     p.scale = a->scale;
+    p.dtype = a->dtype;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = tc ? launch_fwd_tc(p, variant, s) : launch_fwd_simt(p, variant, a->dtype, s);
     return cuda_check(e, fn);
@@ -148,7 +150,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // The forward's records, when the caller hands over the workspace of a forward that ran the
 // transition plan (decided from the sizes alone, as the forward decided), else NULL.
 static const uint8_t *fwd_records(const gcl_bwd_args *a, int variant, int64_t ntm) {
-    if (!a->h_save || !a->fwd_workspace || !fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt))
+    if (!a->h_save || !a->fwd_workspace || !bwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt))
         return nullptr;
     void *w = nullptr;
     size_t wb = 0;
@@ -160,7 +162,7 @@ static const uint8_t *fwd_records(const gcl_bwd_args *a, int variant, int64_t nt
 static size_t bwd_ws(const gcl_bwd_args *a, int variant) {
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->K <= 0 || a->V <= 0) return 0;
-    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
+    const bool tc_fwd = bwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
     const bool tc = variant == kGDN && tc_fwd;
     const size_t per = align256(sizeof(float) * (size_t)ntm * a->H * a->K * a->V);
     // tensor-core sweep (GDN and KDA bf16 K = V = 128): transition records (unless the
@@ -213,7 +215,7 @@ static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int vari
     p.dev_status = a->dev_status;
     p.t_max = a->t_max; p.nt_max = ntm; p.n_max = a->n_max;
     p.H = a->H; p.K = a->K; p.V = a->V; p.bt = a->bt; p.scale = a->scale;
-    const bool tc_fwd = fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
+    const bool tc_fwd = bwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt);
     const bool tc = variant == kGDN && tc_fwd;        // tensor-core backward: GDN
     FwdParams f{};
     f.q = a->q; f.k = a->k; f.v = a->v; f.g = a->g; f.beta = a->beta; f.h0 = a->h0;
@@ -223,6 +225,7 @@ static gcl_status_t run_bwd(const gcl_bwd_args *a, gcl_stream_t stream, int vari
     f.t_max = a->t_max; f.n_max = a->n_max; f.H = a->H; f.K = a->K; f.V = a->V; f.bt = a->bt;
     f.nt_max = ntm;
     f.scale = a->scale;
+    f.dtype = a->dtype;
     const size_t fw = !tc_fwd ? 0 : align256(fwd_tc_t_workspace_bytes(ntm, a->H)) + kWsAlign;
     const size_t used = a->h_save ? per : 2 * per + fw;
     const uint8_t *records = fwd_records(a, variant, ntm);    // the training forward's
@@ -355,7 +358,7 @@ static int32_t fwd_plan(const gcl_fwd_args *a, int variant) {
     size_t wb = 0;
     if (a->workspace) align_ws(a->workspace, a->workspace_bytes, &w, &wb);
     return fwd_tc_plan(variant, a->n_max, a->H, a->h_save != nullptr, wb,
-                       gcl_nt_max(a->t_max, a->n_max, a->bt));
+                       gcl_nt_max(a->t_max, a->n_max, a->bt), a->dtype);
 }
 
 int32_t gcl_fwd_plan(const gcl_fwd_args *args) { return fwd_plan(args, kGDN); }

@@ -38,6 +38,7 @@ struct FwdParams {
     int64_t t_max, nt_max;
     int32_t n_max, H, K, V, bt;
     float scale;
+    int32_t dtype;        // gcl_dtype_t of q, k, v, beta, o
 };
 
 struct BwdParams {
@@ -77,6 +78,7 @@ cudaError_t launch_fwd_tc_t(const FwdParams &p, int split, cudaStream_t s);
 // KDA on the tensor cores: transition-form records with per-channel gates, then the chain.
 cudaError_t launch_fwd_tc_kda(const FwdParams &p, int split, cudaStream_t s);
 bool fwd_tc_supported(int variant, int dtype, int K, int V, int bt);
+bool bwd_tc_supported(int variant, int dtype, int K, int V, int bt);
 size_t fwd_tc_workspace_bytes(int64_t nt_max, int H);     // W form (the minimum)
 size_t fwd_tc_t_workspace_bytes(int64_t nt_max, int H);   // transition form
 // Segment-parallel chain (few long sequences): segments per sequence (0: the plain chain) and
@@ -90,10 +92,11 @@ int fwd_fused_min_units();
 bool fwd_tc_runs_fused(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max);
 cudaError_t launch_fwd_fused(const FwdParams &p, cudaStream_t s);
 // The plan a tensor-core forward runs for these sizes and this (aligned) workspace size.
-int fwd_tc_plan(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max);
+int fwd_tc_plan(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max, int dtype);
 int fwd_tc_split(int n_max, int H);                        // value-column slices per head
 bool fwd_tc_prefers_transition(int n_max, int H);
-bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max);
+bool fwd_tc_runs_transition(int variant, int n_max, int H, bool h_save, size_t ws_bytes, int64_t nt_max,
+                            int dtype = GCL_BF16);
 
 // Encodes a TMA tensor map (cuTensorMapEncodeTiled, looked up once through the runtime).
 bool make_tensor_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,

@@ -243,15 +243,18 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 constexpr uint32_t kSwizzle128B = 2;
 
-// Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator.
-// a_mn / b_mn: operand is MN-major (1) or K-major (0).
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn = 0, int b_mn = 0) {
+// Instruction descriptor, kind::f16 with A and B of one 16-bit format (fmt 1: bf16, 0: fp16),
+// fp32 accumulator.  a_mn / b_mn: operand is MN-major (1) or K-major (0).
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int a_mn, int b_mn, uint32_t fmt) {
     return (1u << 4)                       // D format: f32
-         | (1u << 7)                       // A format: bf16
-         | (1u << 10)                      // B format: bf16
+         | (fmt << 7)                      // A format
+         | (fmt << 10)                     // B format (the same: one type per instruction)
          | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
          | ((uint32_t)(N >> 3) << 17)
          | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn = 0, int b_mn = 0) {
+    return idesc_f16kind(M, N, a_mn, b_mn, 1);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one instruction (K = 16 for bf16).

@@ -12,6 +12,8 @@
 // first float, KDA's per-key-channel decay exp(gamma_c) as 128 floats.
 #pragma once
 
+#include "op16.cuh"
+
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -82,7 +84,7 @@ __device__ __forceinline__ uint32_t mnmaj16(uint32_t atom_bytes, int k, int n) {
 struct PrepTParams {
     const int32_t *chunk_indices, *cu;
     const float *g;
-    const __nv_bfloat16 *beta;
+    const void *beta;            // [t_max, H] of the input type (bf16 or fp16)
     uint8_t *ws;                 // nt_max * H records of kUnitBytes, then the Gamma_c slots
     int32_t *status;
     int64_t t_max, nt_max;

@@ -71,7 +71,9 @@ typedef enum gcl_status {
 typedef enum gcl_dtype {
     GCL_F32 = 0,   /* q, k, v, beta, do, o in fp32; every internal product in fp32     */
     GCL_BF16 = 1,  /* q, k, v, beta, do, o in bf16; state and accumulation in fp32     */
-    GCL_F16 = 2    /* q, k, v, beta, do, o in fp16; every internal product in fp32     */
+    GCL_F16 = 2    /* q, k, v, beta, do, o in fp16; the GDN forward with K = V = 128,   */
+                   /* bt = 64 on the tensor cores (fp16 MMA operands, fp32 state and   */
+                   /* accumulation), every other product in fp32                      */
 } gcl_dtype_t;
 
 typedef void *gcl_stream_t;
@@ -258,7 +260,8 @@ int32_t gcl_kda_fwd_plan(const gcl_fwd_args *args);
  *
  * Supported: bt in {32, 64} (the RFC's test matrix, "BT=32 and BT=64"); K, V in
  * {64, 128}; dtype GCL_F32, GCL_BF16 or GCL_F16.  GDN and KDA with bf16 inputs,
- * K = V = 128 and bt = 64 run on the tensor cores (tcgen05).  With many sequence-head
+ * and GDN with fp16 inputs (the fused and transition plans, every MMA operand and record
+ * in fp16), K = V = 128 and bt = 64 run on the tensor cores (tcgen05).  With many sequence-head
  * units a GDN forward runs the fused plan: one CTA per (sequence, head)
  * walks its chunks with every intermediate (the gate cumsum, A, T = (I + A)^-1, L, the
  * GEMM-first R = diag(beta)(V - diag(Gamma) K S), E = T R, the state) on chip, so only

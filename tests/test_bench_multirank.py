@@ -71,6 +71,6 @@ def test_launch_count_per_step():
     # one 64K-token sequence of one head: the segmented chain (on any GPU of 24 or more SMs)
     assert bench.launches_per_step(ws["gdn_fwd_bf16_T65536_H1_d128"]) == 5
     assert bench.launches_per_step(ws["kda_fwd_bf16_T65536_H1_d128"]) == 5
-    # fp16 and chunk size 32 run the fused CUDA-core forward
-    assert bench.launches_per_step(ws["gdn_fwd_f16_T4096_H16_d128"]) == 2
+    # chunk size 32 runs the fused CUDA-core forward; fp16 (GDN, d = 128) the transition form
+    assert bench.launches_per_step(ws["gdn_fwd_f16_T4096_H16_d128"]) == 3       # fp16: tensor cores
     assert bench.launches_per_step(ws["gdn_fwd_bf16_bt32_T4096_H16_d128"]) == 2

@@ -1,6 +1,7 @@
-"""The RFC test matrix's variants against the fp64 oracle, through the C ABI: fp16 inputs and
-chunk size BT = 32 (both on the CUDA-core kernels, fp32 arithmetic), forward and backward,
-GDN and KDA, ragged and empty sequences, saved chunk states."""
+"""The RFC test matrix's variants against the fp64 oracle, through the C ABI: fp16 inputs (the
+GDN forward at d = 128 on the tensor cores, everything else on the CUDA cores in fp32) and chunk
+size BT = 32 (CUDA cores), forward and backward, GDN and KDA, ragged and empty sequences, saved
+chunk states."""
 import numpy as np
 import pytest
 
@@ -22,7 +23,7 @@ def _w(variant, dtype, KV, bt, backward=False, seed=60):
                         backward=backward, seed=seed, bt=bt)
 
 
-def _check_states(w, x, out):
+def _check_states(w, x, out, tol=TOL["f32"]):
     meta = out["meta"]
     off = meta.off.cpu().numpy()
     _, _, hc = oracle.fwd(w.variant, x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
@@ -30,7 +31,7 @@ def _check_states(w, x, out):
                           nt_rows=meta.nt_max)
     live = int(off[-1])
     hs = out["h_save"].cpu().numpy()
-    assert relF(hs[:live], hc[:live]) <= TOL["f32"]
+    assert relF(hs[:live], hc[:live]) <= tol
     assert (hs[live:] == np.float32(CANARY)).all()
 
 
@@ -45,18 +46,44 @@ def _compare_grads(w, got, ref, tol):
 @pytest.mark.parametrize("variant,vname", VARIANTS, ids=[v[1] for v in VARIANTS])
 @pytest.mark.parametrize("KV", [(64, 64), (128, 128)], ids=["d64", "d128"])
 def test_fp16_forward_and_backward(variant, vname, KV):
-    """fp16 q, k, v, beta, dO: o within the fp16 output rounding, ht, the saved chunk states
-    and every gradient (fp32 outputs) within the fp32 bar."""
+    """fp16 q, k, v, beta, dO.  On the CUDA cores (fp32 arithmetic): o within the fp16 output
+    rounding, ht, the saved chunk states and every gradient within the fp32 bar.  GDN at
+    d = 128 runs the forward on the tensor cores with every MMA operand in fp16: every output
+    within the fp16 bar (TOL["f16"], about twice fp16's unit roundoff), and the gradients,
+    computed from those saved states, likewise."""
     w = _w(variant, "f16", KV, 64, backward=True)
     x = synth.make_inputs(w)
     d = to_device(w, x)
     assert d["q"].dtype == torch.float16
+    tc = variant == synth.GDN and KV == (128, 128)
+    tol = TOL["f16"] if tc else TOL["f32"]
     out = run_fwd(w, d, h_save=True)
-    e_o, e_h = check_fwd(w, x, out, label=f"{vname} f16")
-    assert e_h <= TOL["f32"], e_h
-    _check_states(w, x, out)
+    e_o, e_h = check_fwd(w, x, out, label=f"{vname} f16", tol=TOL["f16"])
+    assert e_h <= tol, e_h
+    _check_states(w, x, out, tol)
     got = run_bwd(w, d, out["meta"], h_save=out["h_save"])
-    _compare_grads(w, got, oracle_bwd(w, x), TOL["f32"])
+    _compare_grads(w, got, oracle_bwd(w, x), tol)
+
+
+F16_TC = [("transition-split8", 1, 4096, 16), ("segmented", 1, 16384, 1), ("fused", 10, 1024, 16)]
+
+
+@pytest.mark.parametrize("label,B,T,H", F16_TC, ids=[c[0] for c in F16_TC])
+def test_fp16_tensor_core_plans(label, B, T, H):
+    """GDN with fp16 inputs on the tensor cores in each plan it takes: the transition form at
+    the 4,096-token, 16-head size (eight value slices per head), the segmented transition form
+    (one 16,384-token head) and the fused plan (160 units); o and ht within the fp16 bar at the
+    global, per-unit and per-row levels."""
+    import chunked_gated_linear_gb300 as gcl
+    w = synth.dense("f16-tc", synth.GDN, "f16", B, T, H, 128, 128, seed=64)
+    x = synth.make_inputs(w)
+    d = to_device(w, x)
+    out = run_fwd(w, d)
+    plan = gcl.fwd_plan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], out["o"],
+                        h0=d["h0"], chunk_indices=out["meta"].idx, chunk_offsets=out["meta"].off,
+                        workspace=out["ws"], scale=w.scale)
+    assert plan == label.split("-")[0], plan
+    check_fwd(w, x, out, label=f"f16 {label}", tol=TOL["f16"])
 
 
 @pytest.mark.parametrize("variant,vname", VARIANTS, ids=[v[1] for v in VARIANTS])
