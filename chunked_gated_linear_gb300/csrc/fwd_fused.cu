@@ -26,7 +26,7 @@
 //   MMA5  O^T += E^T L^T                         (A = E^T TMEM,   B = L smem)
 // The triangular solve runs in fp32 on the CUDA cores of warps 0..3 while warps 4..7 form R;
 // one lane of warp 4 issues every copy and MMA, and warp 5 forms the next chunk's gate vectors
-// (double-buffered) after its share of R.  Two CTAs share an SM (about 104 KB of shared memory
+// (double-buffered) after its share of R.  Two CTAs share an SM (about 100 KB of shared memory
 // and 256 TMEM columns each), so one CTA's MMAs, copies and waits overlap the other's CUDA-core
 // phases.  Rows past the end of a sequence are selected to zero in every
 // operand the threads build and zeroed in the K tile, so NaN padding never reaches an MMA.
@@ -68,10 +68,9 @@ struct FusedLayout {
     static constexpr uint32_t oT = oV + 16384;         // T bf16 [64 x 64], K-major, 128-byte swizzle
     static constexpr uint32_t oL = oT + 8192;          // L bf16 [64 x 64]
     static constexpr uint32_t oA = oL + 8192;          // solve: A fp32 [64][kSolveLD]
-    static constexpr uint32_t oTf = oA + 64 * kSolveLD * 4;   // solve: T fp32 (decay table before)
-    static constexpr uint32_t oX = oTf + 64 * kSolveLD * 4;   // solve scratch
+    static constexpr uint32_t oTf = oA + 64 * kSolveLD * 4;   // solve: T fp32
     static constexpr uint32_t oO = oA;                 // O staging [64][kOLD] bf16, after the solve
-    static constexpr uint32_t total = oX + 3 * 16 * kSolveLDX * 4;
+    static constexpr uint32_t total = oTf + 64 * kSolveLD * 4;
     static constexpr uint32_t bytes = total + 1024;    // + alignment slack
 };
 constexpr int kOLD = 136;                              // O staging row stride (bf16 elements)
@@ -278,9 +277,13 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (nch > 1) load_gates(1);
     }
 
+    // T and L (bf16) start as zeros: the blocks above their block diagonal are never written
+    // again (T is zero there, L too), so the epilogues and the T write-out skip them
+    for (int e = tid; e < (8192 + 8192) / 16; e += kThreads)
+        *reinterpret_cast<uint4 *>(smem + Lay::oT + e * 16) = make_uint4(0, 0, 0, 0);
+
     float *sAf = reinterpret_cast<float *>(smem + Lay::oA);
     float *sTf = reinterpret_cast<float *>(smem + Lay::oTf);
-    float *sXf = reinterpret_cast<float *>(smem + Lay::oX);
     T *sO = reinterpret_cast<T *>(smem + Lay::oO);
 
     for (int ic = 0; ic < nch; ++ic) {
@@ -330,7 +333,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // D[r][c] = exp(gamma_r - gamma_c): inside a 16-row block one exponential per pair; for
         // c in an earlier block, exp(gamma_r - gamma_{16 b}) F2[b][c] (both factors <= 1, so
         // nothing overflows; their product underflows only where the decay itself does).
-        {
+        // (warps whose rows 0..31 meet columns 32..63 only, all above the diagonal, skip it)
+        if (half == 0 || (quarter & 1) == 1) {
             const int r = m & 63, br = r >> 4;
             const bool live = r < len;
             const float gr = sG[r];
@@ -395,10 +399,11 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_st16(tmem + lane_off + cS + q * 16, S + q * 16);
             tmem_st_wait();
-            solve_unit_lower64<128, 1>(sAf, sTf, sXf);
+            solve_unit_lower64_r32<128, 1>(sAf, sTf);
             const int r = tid >> 1, cq = (tid & 1) * 32;
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
+                if (cq + j > r) continue;                  // all above the diagonal: zeros kept
                 uint4 pk;
                 uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
 #pragma unroll

@@ -136,4 +136,82 @@ __device__ __forceinline__ void solve_unit_lower64(float *sA, float *sT, float *
     solve_barrier<NT, BarId>();
 }
 
+// acc[x][y] += sum over m in [4 mlo, 4 mhi) of L[(r0 + x) ldl + m] R[m ldr + c0 + y]: one TR x 4
+// register tile of a block product (float4 loads; each loaded L row segment serves four
+// columns and each R row segment TR rows).
+template <int TR>
+__device__ __forceinline__ void solve_tile(const float *L, int ldl, const float *R, int ldr, int r0,
+                                           int c0, int mlo, int mhi, float (&acc)[TR][4]) {
+    for (int mb = mlo; mb < mhi; ++mb) {
+        float4 l[TR];
+#pragma unroll
+        for (int x = 0; x < TR; ++x) l[x] = *reinterpret_cast<const float4 *>(L + (r0 + x) * ldl + 4 * mb);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 r = *reinterpret_cast<const float4 *>(R + (4 * mb + e) * ldr + c0);
+#pragma unroll
+            for (int x = 0; x < TR; ++x) {
+                const float lv = e == 0 ? l[x].x : e == 1 ? l[x].y : e == 2 ? l[x].z : l[x].w;
+                acc[x][0] = fmaf(lv, r.x, acc[x][0]);
+                acc[x][1] = fmaf(lv, r.y, acc[x][1]);
+                acc[x][2] = fmaf(lv, r.z, acc[x][2]);
+                acc[x][3] = fmaf(lv, r.w, acc[x][3]);
+            }
+        }
+    }
+}
+
+// T = (I + A)^-1 over two blocks of 32 rows instead (the 2 x 2 block split
+// A = [A_00 0; A_10 A_11]: T_ii = (I + A_ii)^-1, T_10 = -T_11 A_10 T_00), in two phases:
+//   A  forward substitution down the 32 rows of a diagonal block, one column per thread,
+//      four partial sums, for the right-hand sides e_j (the columns of T_00 and T_11) and the
+//      columns of A_10 (which gives X = T_11 A_10 without forming a product): three warps;
+//   B  T_10 = -X T_00: every thread a TR x 4 register tile (TR = 2 with 128 threads, 1 with
+//      256), the sum starting at the tile's first column (T_00 is lower triangular).
+// Two block barriers instead of five.  A is only read; X is left in T's block (0, 1), above
+// the diagonal.  Alone on an SM it takes about two thirds of the latency of the 16-row scheme;
+// inside kernels with several CTAs per SM the 16-row scheme's spread over every thread
+// measured as fast or faster, so only the fused forward (solve on four warps beside other
+// work) takes this one.
+template <int NT, int BarId = -1>
+__device__ __forceinline__ void solve_unit_lower64_r32(const float *sA, float *sT) {
+    static_assert(NT == 128 || NT == 256, "128 or 256 solving threads");
+    constexpr int LD = kSolveLD;
+    const int tid = threadIdx.x;
+    if (tid < 96) {
+        const int grp = tid >> 5, j = tid & 31;       // warp-uniform job
+        const float *Ab = grp == 0 ? sA : sA + 32 * LD + 32;
+        float x[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m4 = 0; m4 < r; m4 += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(Ab + r * LD + m4);
+                part[0] = fmaf(a.x, x[m4], part[0]);
+                if (m4 + 1 < r) part[1] = fmaf(a.y, x[m4 + 1], part[1]);
+                if (m4 + 2 < r) part[2] = fmaf(a.z, x[m4 + 2], part[2]);
+                if (m4 + 3 < r) part[3] = fmaf(a.w, x[m4 + 3], part[3]);
+            }
+            const float rhs = grp == 2 ? sA[(32 + r) * LD + j] : (r == j ? 1.f : 0.f);
+            x[r] = rhs - ((part[0] + part[1]) + (part[2] + part[3]));
+        }
+        float *dst = grp == 0 ? sT + j : grp == 1 ? sT + 32 * LD + 32 + j : sT + 32 + j;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) dst[r * LD] = x[r];
+    }
+    solve_barrier<NT, BarId>();
+    constexpr int TR = NT == 128 ? 2 : 1;
+    for (int s = tid; s < (32 / TR) * 8; s += NT) {
+        const int r0 = (s >> 3) * TR, q = s & 7;
+        float acc[TR][4] = {};
+        solve_tile<TR>(sT + 32, LD, sT, LD, r0, 4 * q, q, 8, acc);
+#pragma unroll
+        for (int x = 0; x < TR; ++x)
+            *reinterpret_cast<float4 *>(sT + (32 + r0 + x) * LD + 4 * q) =
+                make_float4(-acc[x][0], -acc[x][1], -acc[x][2], -acc[x][3]);
+    }
+    solve_barrier<NT, BarId>();
+}
+
 }  // namespace gcl
