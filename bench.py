@@ -45,7 +45,7 @@ from chunked_gated_linear_gb300 import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "gdn_varlen_bf16_N32_Nmax64_Tmax65536_H16_d128"
 # the other standard configurations measured in the same run, one line each under per_config
-PER_CONFIG = ("gdn_fwd_bf16_T4096_H16_d128", "kda_fwd_bf16_T2048_H10_d128",
+PER_CONFIG = ("gdn_fwd_fp32_T256_H2_d64", "gdn_fwd_bf16_T4096_H16_d128", "kda_fwd_bf16_T2048_H10_d128",
               "gdn_fwdbwd_bf16_B4_T8192_H16_d128")
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
@@ -356,12 +356,14 @@ def fwd_plan_of(w) -> str:
 
 def launches_per_step(w) -> int:
     """Library kernels per step: chunk_meta_build, the forward (the fused plan and the CUDA-core
-    kernel: one launch; the W-form and transition plans: the chunk prep and the chain; the
+    kernel: one launch; the W-form, transition and CUDA-core split plans: the chunk prep and the
+    chain; the
     segmented plan: prep, segment summaries, scan and segment outputs) and the backward (GDN on
     the tensor cores: state-gradient sweep from the forward's records and two chunk-gradient
     kernels; otherwise the sweep and one chunk-gradient kernel)."""
     plan = fwd_plan_of(w)
-    fwd = {"cuda_cores": 1, "fused": 1, "w_form": 2, "transition": 2, "segmented": 4}[plan]
+    fwd = {"cuda_cores": 1, "cuda_cores_split": 2, "fused": 1, "w_form": 2, "transition": 2,
+           "segmented": 4}[plan]
     tc_bwd = tensor_path(w) and w.variant == synth.GDN and w.dtype == "bf16"
     return 1 + fwd + ((3 if tc_bwd else 2) if w.backward else 0)
 

@@ -367,7 +367,8 @@ def kda_fwd_workspace_bytes(*args, **kw) -> int:
     return int(lib().gcl_kda_fwd_workspace_bytes(ctypes.byref(a)))
 
 
-PLANS = {0: "cuda_cores", 1: "fused", 2: "w_form", 3: "transition", 4: "segmented"}
+PLANS = {0: "cuda_cores", 1: "fused", 2: "w_form", 3: "transition", 4: "segmented",
+         5: "cuda_cores_split"}
 
 
 def fwd_plan(*args, kda=False, **kw) -> str:

@@ -23,6 +23,7 @@
 #pragma once
 
 #include "simt_map.cuh"
+#include "fwd_simt_split.cuh"
 
 namespace gcl {
 namespace simt_fwd {
@@ -199,10 +200,30 @@ cudaError_t launch_chunk(const FwdParams &p, cudaStream_t s) {
 
 }  // namespace simt_fwd
 
-// The CUDA-core forward for input type Tin: variant, chunk size 32 or 64.
+// The split plan (chunk prep + chain) for K = V, chunk C.
+template <int VAR, typename Tin, int C>
+cudaError_t launch_split(const FwdParams &p, cudaStream_t s) {
+    if (p.K == 64) return simt_split::launch<VAR, Tin, 64, 64, C>(p, s);
+    return simt_split::launch<VAR, Tin, 128, 128, C>(p, s);
+}
+
+// Whether a call runs the split plan: K = V, the chunk metadata given and a workspace that
+// holds the records (the single kernel needs neither).
+inline bool fwd_simt_runs_split(const FwdParams &p) {
+    const size_t need = fwd_simt_split_bytes(p.K, p.V, p.bt, p.nt_max, p.H);
+    return need > 0 && p.workspace && p.workspace_bytes >= need && p.chunk_indices && p.chunk_offsets;
+}
+
+// The CUDA-core forward for input type Tin: variant, chunk size 32 or 64; the split plan
+// where the workspace holds its records, else the single kernel.
 template <typename Tin>
 cudaError_t launch_fwd_simt_t(const FwdParams &p, int variant, cudaStream_t s) {
     using namespace simt_fwd;
+    if (fwd_simt_runs_split(p)) {
+        if (variant == kGDN)
+            return p.bt == 32 ? launch_split<kGDN, Tin, 32>(p, s) : launch_split<kGDN, Tin, 64>(p, s);
+        return p.bt == 32 ? launch_split<kKDA, Tin, 32>(p, s) : launch_split<kKDA, Tin, 64>(p, s);
+    }
     if (variant == kGDN)
         return p.bt == 32 ? launch_chunk<kGDN, Tin, 32>(p, s) : launch_chunk<kGDN, Tin, 64>(p, s);
     return p.bt == 32 ? launch_chunk<kKDA, Tin, 32>(p, s) : launch_chunk<kKDA, Tin, 64>(p, s);

@@ -1,0 +1,492 @@
+// fwd_simt_split.cuh -- the CUDA-core forward as two launches (fp32 arithmetic): a chunk
+// prep over every chunk of every sequence at once, then a chain over (sequence, head,
+// value-column slice) that carries the state through the chunks in order.
+//
+// HA-NPU paper "Empowering Hybrid Attention Models on NPUs", section 2.1: of Map-Reduce-Map
+// only the Reduce is serial; the chunk-local Map runs for all chunks in parallel.  The prep
+// (one CTA per row of chunk_indices and head) forms, from the chunk alone (simt_map.cuh),
+//   W = T diag(beta Gamma) K (GDN) or T diag(beta) (K o Gamma) (KDA),   U = T diag(beta) V,
+//   Q' = scale diag(Gamma) Q (or scale Q o Gamma),   K' = diag(f) K (or K o exp(gamma_c - gamma)),
+//   L,   Gamma_c (per key channel; GDN repeats its scalar),
+// and writes them as one fp32 record per chunk and head.  The chain then needs only
+//   E = U - W S,   O = Q' S + L E,   S <- Gamma_c o S + K'^T E
+// per chunk (section 5's chunk-first order: O from the state before the update), with the
+// next chunk's record copied into shared memory while the current one is used.  Rows past
+// the end of a sequence have zero q, k, beta and g, so their record rows are zero and leave
+// S unchanged.
+#pragma once
+
+#include "simt_map.cuh"
+
+namespace gcl {
+namespace simt_split {
+
+constexpr int kThreads = 256;
+
+// One record per (chunk row, head), fp32, row-major without padding:
+//   W [C][K] | Q' [C][K] | K' [C][K] | L [C][C] | U [C][V] | Gamma_c [K]
+template <int K, int V, int C>
+struct Rec {
+    static constexpr int oW = 0, oQ = C * K, oKt = 2 * C * K, oL = 3 * C * K;
+    static constexpr int oU = oL + C * C, oGC = oU + C * V;
+    static constexpr int floats = oGC + K;
+    static_assert(floats % 4 == 0, "records keep 16-byte alignment");
+};
+
+// ------------------------------------------------------------------------------- prep
+// Four consecutive inputs as fp32 (one 16-byte fp32 load, one 8-byte bf16 or fp16 load).
+__device__ __forceinline__ float4 ld4_in(const float *p, int64_t i) {
+    return *reinterpret_cast<const float4 *>(p + i);
+}
+__device__ __forceinline__ float4 ld4_in(const __nv_bfloat16 *p, int64_t i) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p + i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 ld4_in(const __half *p, int64_t i) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p + i);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// The chunk's [C][W] tile of a [t, H, W] input, four elements per load, held in registers
+// (every load of a batch is in flight before the first store); rows r >= len read as zero.
+template <typename Tin, int W, int C>
+struct Tile4 {
+    static constexpr int N4 = C * W / 4, PER = (N4 + kThreads - 1) / kThreads;
+    float4 b[PER];
+    __device__ __forceinline__ void load(const Tin *x, int64_t t0, int len, int h, int H, int64_t t_max,
+                                         int32_t *st) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int e = threadIdx.x + u * kThreads, r = e / (W / 4), c4 = e % (W / 4);
+            const int64_t gi = ((t0 + r) * H + h) * (int64_t)W + 4 * c4;
+            b[u] = (e < N4 && r < len && GCL_RANGE_IN_BOUNDS(gi, gi + 3, t_max * H * (int64_t)W, st))
+                       ? ld4_in(x, gi) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    __device__ __forceinline__ void store(float *dst, int ld) const {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int e = threadIdx.x + u * kThreads, r = e / (W / 4), c4 = e % (W / 4);
+            if (e < N4) {
+                float *d = dst + r * ld + 4 * c4;
+                d[0] = b[u].x;
+                d[1] = b[u].y;
+                d[2] = b[u].z;
+                d[3] = b[u].w;
+            }
+        }
+    }
+};
+
+template <int K, int V, int VAR, int C>
+struct PrepLayout {
+    static constexpr int LK = K + 1, LV = V + 1, kLC = C + 1;
+    static constexpr int oQ = 0, oK = oQ + C * LK, oV = oK + C * LK;
+    static constexpr int oA = oV + C * LV, oT = oA + C * kLC, oL = oT + C * kLC;
+    static constexpr int oX = oL + C * kLC;                  // solve scratch (3 x 16 x 16)
+    static constexpr int oB = oX + 768, oG = oB + C;
+    static constexpr int total = oG + (VAR == kKDA ? C * LK : C);
+    static constexpr size_t bytes = sizeof(float) * total;
+    static_assert(bytes <= 232448, "one CTA per SM at most");
+};
+
+template <int VAR, typename Tin, int K, int V, int C>
+__global__ void __launch_bounds__(kThreads)
+prep_kernel(FwdParams p) {
+    using Lay = PrepLayout<K, V, VAR, C>;
+    using R = Rec<K, V, C>;
+    constexpr int LK = Lay::LK, LV = Lay::LV, kLC = Lay::kLC;
+    extern __shared__ float sm[];
+    float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sV = sm + Lay::oV;
+    float *sA = sm + Lay::oA, *sT = sm + Lay::oT, *sL = sm + Lay::oL, *sX = sm + Lay::oX;
+    float *sB = sm + Lay::oB, *sG = sm + Lay::oG;
+
+    // launched as a dependent of the metadata kernel: nothing it wrote is read before this
+    grid_dependency_wait();
+    launch_dependents();                 // the chain reads the records after this grid completes
+    if (status_blocks_cta(p.dev_status)) return;
+    const int tid = threadIdx.x, j = blockIdx.x, h = blockIdx.y, H = p.H;
+    const int n = p.chunk_indices[2 * j];
+    if (n < 0) return;                   // sentinel row: nothing to do
+    const int ic = p.chunk_indices[2 * j + 1];
+    if (n >= p.n_max || ic < 0) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+    const int64_t t0 = bos + (int64_t)ic * C;
+    const int64_t row = (int64_t)p.chunk_offsets[n] + ic;
+    if (bos < 0 || eos < bos || eos > p.t_max || t0 >= eos || row < 0 || row >= p.nt_max) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int len = (int)(eos - t0 < C ? eos - t0 : C);
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    const Tin *beta = static_cast<const Tin *>(p.beta);
+    float *rec = static_cast<float *>(p.workspace) + (row * H + h) * (int64_t)R::floats;
+    const int64_t n_rec = p.nt_max * H * (int64_t)R::floats;
+    const int64_t rec0 = (row * H + h) * (int64_t)R::floats;
+
+    {   // q, k (and KDA's gates) in one batch of loads, v in a second
+        Tile4<Tin, K, C> tq, tk;
+        tq.load(q, t0, len, h, H, p.t_max, p.dev_status);
+        tk.load(k, t0, len, h, H, p.t_max, p.dev_status);
+        float gv = 0.f, bv = 0.f;
+        if (tid < C) {
+            const bool ok = tid < len && GCL_IN_BOUNDS((t0 + tid) * H + h, p.t_max * H, p.dev_status);
+            bv = ok ? ld_in(beta, (t0 + tid) * H + h) : 0.f;
+            if (VAR == kGDN) gv = ok ? p.g[(t0 + tid) * H + h] : 0.f;
+        }
+        if constexpr (VAR == kKDA) {
+            Tile4<float, K, C> tg;
+            tg.load(p.g, t0, len, h, H, p.t_max, p.dev_status);
+            tg.store(sG, LK);
+        }
+        tq.store(sQ, LK);
+        tk.store(sK, LK);
+        if (tid < C) {
+            sB[tid] = bv;
+            if (VAR == kGDN) sG[tid] = gv;
+        }
+    }
+    {
+        Tile4<Tin, V, C> tv;
+        tv.load(v, t0, len, h, H, p.t_max, p.dev_status);
+        tv.store(sV, LV);
+    }
+    __syncthreads();
+    if constexpr (VAR == kGDN) {   // inclusive cumsum of g over the rows: warp scans + carry
+        __shared__ float s_carry;
+        float x = tid < C ? sG[tid] : 0.f;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, d);
+            if ((tid & 31) >= d) x += y;
+        }
+        if (tid == 31) s_carry = x;
+        __syncthreads();
+        if (tid >= 32 && tid < C) x += s_carry;
+        if (tid < C) sG[tid] = x;
+    } else {
+        simt_gate_cumsum<VAR, K, kThreads, C>(sG);
+    }
+    __syncthreads();
+    simt_intra<VAR, K, kThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    __syncthreads();
+    simt_solve_blocked<kThreads, C>(sA, sT, sX);    // ends with a block barrier
+    // ---- Q', K', L and Gamma_c straight from shared memory
+    for (int e = tid; e < C * K; e += kThreads) {
+        const int r = e / K, c = e % K;
+        const float gr = gam<VAR, K>(sG, r, c), gc = gam<VAR, K>(sG, C - 1, c);
+        if (GCL_RANGE_IN_BOUNDS(rec0 + R::oQ + e, rec0 + R::oKt + e, n_rec, p.dev_status)) {
+            rec[R::oQ + e] = p.scale * expf(gr) * sQ[r * LK + c];
+            rec[R::oKt + e] = expf(gc - gr) * sK[r * LK + c];
+        }
+    }
+    for (int e = tid; e < C * C; e += kThreads)
+        if (GCL_IN_BOUNDS(rec0 + R::oL + e, n_rec, p.dev_status)) rec[R::oL + e] = sL[(e / C) * kLC + e % C];
+    for (int c = tid; c < K; c += kThreads)
+        if (GCL_IN_BOUNDS(rec0 + R::oGC + c, n_rec, p.dev_status)) rec[R::oGC + c] = expf(gam<VAR, K>(sG, C - 1, c));
+    __syncthreads();     // Q is no longer read: it becomes diag(beta) (K o Gamma)
+    for (int e = tid; e < C * K; e += kThreads) {
+        const int r = e / K, c = e % K;
+        sQ[r * LK + c] = sB[r] * expf(gam<VAR, K>(sG, r, c)) * sK[r * LK + c];
+    }
+    __syncthreads();
+    // ---- W = T (beta Gamma K) and U = T (beta V): 4 x 4 register tiles, i up to the tile's
+    // last row (T lower triangular); V's rows take beta in place first
+    for (int e = tid; e < C * V; e += kThreads) sV[(e / V) * LV + e % V] *= sB[e / V];
+    __syncthreads();
+    auto tile_product = [&](const float *X, int ldx, int W, int oRec) {
+        for (int s = tid; s < (C / 4) * (W / 4); s += kThreads) {
+            const int r0 = (s / (W / 4)) * 4, c0 = (s % (W / 4)) * 4;
+            float acc[4][4] = {};
+            for (int i = 0; i <= r0 + 3; ++i) {
+                float t[4], x[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    t[a] = sT[(r0 + a) * kLC + i];     // zero above the diagonal
+                    x[a] = X[i * ldx + c0 + a];
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(t[a], x[b], acc[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int64_t o = rec0 + oRec + (int64_t)(r0 + a) * W + c0;
+                if (GCL_RANGE_IN_BOUNDS(o, o + 3, n_rec, p.dev_status))
+                    *reinterpret_cast<float4 *>(rec + oRec + (r0 + a) * W + c0) =
+                        make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+            }
+        }
+    };
+    tile_product(sQ, LK, K, R::oW);
+    tile_product(sV, LV, V, R::oU);
+}
+
+// ------------------------------------------------------------------------------ chain
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// N consecutive floats of shared memory (N = 1, 2 or 4, the address aligned to N floats).
+template <int N>
+__device__ __forceinline__ void lds_vec(const float *p, float (&v)[N]) {
+    if constexpr (N == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(p);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else if constexpr (N == 2) {
+        const float2 t = *reinterpret_cast<const float2 *>(p);
+        v[0] = t.x; v[1] = t.y;
+    } else {
+        static_assert(N == 1, "1, 2 or 4 floats");
+        v[0] = p[0];
+    }
+}
+
+// Shared memory of the chain: NB record buffers (two when they fit: the next chunk's record
+// arrives while the current one is used), the state slice S [K][VS] and E [C][VS].  Row
+// strides are the widths + 4 floats: 16-byte aligned rows, consecutive rows 4 banks apart.
+template <int K, int VS, int C>
+struct ChainLayout {
+    static constexpr int LW = K + 4, LL = C + 4, LU = VS + 4;
+    static constexpr int oW = 0, oQ = C * LW, oKt = 2 * C * LW, oL = 3 * C * LW, oU = oL + C * LL;
+    static constexpr int oGC = oU + C * LU, buf = oGC + K;
+    static constexpr int kMaxFloats = 232448 / 4;
+    static constexpr int fixed = K * LU + C * LU;
+    static constexpr int NB = 2 * buf + fixed <= kMaxFloats ? 2 : 1;
+    static constexpr int oS = NB * buf, oE = oS + K * LU, total = oE + C * LU;
+    static constexpr size_t bytes = sizeof(float) * total;
+    static_assert(bytes <= 232448, "chain shared memory");
+};
+
+template <typename Tin, int K, int V, int VS, int C>
+__global__ void __launch_bounds__(kThreads)
+chain_kernel(FwdParams p) {
+    using Lay = ChainLayout<K, VS, C>;
+    using R = Rec<K, V, C>;
+    constexpr int LW = Lay::LW, LL = Lay::LL, LU = Lay::LU;
+    // phase 1 / O tiles: 2 rows x TJ columns; state tiles: TC keys x TS columns
+    constexpr int RP = C / 2, CG = kThreads / RP, TJ = VS / CG;
+    constexpr int TC = K / 32, TS = VS / 8;
+    static_assert(RP * CG == kThreads && TJ * CG == VS && TJ >= 1, "output tiles");
+    static_assert(TC * 32 == K && TS * 8 == VS, "state tiles");
+    extern __shared__ __align__(16) float sm[];
+    float *sS = sm + Lay::oS, *sE = sm + Lay::oE;
+
+    // launched as a dependent of the prep: its records are complete after this wait
+    grid_dependency_wait();
+    if (status_blocks_cta(p.dev_status)) return;
+    const int tid = threadIdx.x, h = blockIdx.y, H = p.H, v0 = blockIdx.x * VS;
+    const int z = blockIdx.z;
+    const int n = (p.seq_order && GCL_IN_BOUNDS(z, p.n_max, p.dev_status)) ? p.seq_order[z] : z;
+    if (n < 0 || n >= p.n_max) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+    if (bos < 0 || eos < bos || eos > p.t_max) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int nch = (int)((eos - bos + C - 1) / C);
+    const int64_t row0 = p.chunk_offsets[n];
+    if (nch > 0 && (row0 < 0 || row0 + nch > p.nt_max)) {
+        if (tid == 0) status_set(p.dev_status, GCL_DEV_BAD_RANGE);
+        return;
+    }
+    const int64_t KV = (int64_t)K * V;
+    const int64_t state_base = ((int64_t)n * H + h) * KV;
+    const int64_t n_state = (int64_t)p.n_max * H * KV;
+    const float *recs = static_cast<const float *>(p.workspace);
+    const int64_t n_rec = p.nt_max * H * (int64_t)R::floats;
+    Tin *o = static_cast<Tin *>(p.o);
+
+    for (int e = tid; e < K * VS; e += kThreads) {
+        const int c = e / VS, jj = e % VS;
+        const int64_t gi = state_base + (int64_t)c * V + v0 + jj;
+        sS[c * LU + jj] = (p.h0 && GCL_IN_BOUNDS(gi, n_state, p.dev_status)) ? p.h0[gi] : 0.f;
+    }
+    // the record of chunk ic into buffer b: 16-byte copies, padded rows
+    auto issue = [&](int ic, int b) {
+        const int64_t r0 = ((row0 + ic) * H + h) * (int64_t)R::floats;
+        if (!GCL_RANGE_IN_BOUNDS(r0, r0 + R::floats - 1, n_rec, p.dev_status)) return;
+        const float *src = recs + r0;
+        float *dst = sm + b * Lay::buf;
+        for (int e = tid; e < 3 * C * K / 4; e += kThreads) {       // W, Q', K'
+            const int m = e / (C * K / 4), w = e % (C * K / 4), r = w / (K / 4), c4 = w % (K / 4);
+            cp_async16(dst + m * C * LW + r * LW + 4 * c4, src + m * C * K + 4 * w);
+        }
+        for (int e = tid; e < C * C / 4; e += kThreads) {           // L
+            const int r = e / (C / 4), c4 = e % (C / 4);
+            cp_async16(dst + Lay::oL + r * LL + 4 * c4, src + R::oL + 4 * e);
+        }
+        for (int e = tid; e < C * VS / 4; e += kThreads) {          // U, this slice's columns
+            const int r = e / (VS / 4), c4 = e % (VS / 4);
+            cp_async16(dst + Lay::oU + r * LU + 4 * c4, src + R::oU + r * V + v0 + 4 * c4);
+        }
+        for (int e = tid; e < K / 4; e += kThreads) cp_async16(dst + Lay::oGC + 4 * e, src + R::oGC + 4 * e);
+        cp_async_commit();
+    };
+    if (nch > 0) issue(0, 0);
+
+    const int rp = tid / CG, r0 = 2 * rp, j0 = (tid % CG) * TJ;      // output tile
+    const int c0 = (tid / 8) * TC, s0 = (tid % 8) * TS;              // state tile
+    for (int ic = 0; ic < nch; ++ic) {
+        const int b = Lay::NB == 2 ? (ic & 1) : 0;
+        const float *sW = sm + b * Lay::buf, *sQp = sW + Lay::oQ, *sKt = sW + Lay::oKt;
+        const float *sL = sW + Lay::oL, *sU = sW + Lay::oU, *sGC = sW + Lay::oGC;
+        const int64_t t0 = bos + (int64_t)ic * C;
+        const int len = (int)(eos - t0 < C ? eos - t0 : C);
+        cp_async_wait_all();
+        __syncthreads();              // chunk ic's record and the state are in place
+        if (Lay::NB == 2 && ic + 1 < nch) issue(ic + 1, b ^ 1);
+        if (p.h_save) {               // the state entering the chunk
+            const int64_t hb = ((row0 + ic) * H + h) * KV;
+            for (int e = tid; e < K * VS; e += kThreads) {
+                const int c = e / VS, jj = e % VS;
+                if (GCL_IN_BOUNDS(hb + (int64_t)c * V + v0 + jj, p.nt_max * H * KV, p.dev_status))
+                    p.h_save[hb + (int64_t)c * V + v0 + jj] = sS[c * LU + jj];
+            }
+        }
+        // ---- phase 1: E = U - W S and Y = Q' S on rows r0, r0 + 1, columns j0 ..
+        float ae[2][TJ], ay[2][TJ];
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int y = 0; y < TJ; ++y) {
+                ae[x][y] = sU[(r0 + x) * LU + j0 + y];
+                ay[x][y] = 0.f;
+            }
+#pragma unroll 2
+        for (int c = 0; c < K; c += 4) {
+            const float4 w0 = *reinterpret_cast<const float4 *>(sW + r0 * LW + c);
+            const float4 w1 = *reinterpret_cast<const float4 *>(sW + (r0 + 1) * LW + c);
+            const float4 q0 = *reinterpret_cast<const float4 *>(sQp + r0 * LW + c);
+            const float4 q1 = *reinterpret_cast<const float4 *>(sQp + (r0 + 1) * LW + c);
+            const float wa[4] = {w0.x, w0.y, w0.z, w0.w}, wb[4] = {w1.x, w1.y, w1.z, w1.w};
+            const float qa[4] = {q0.x, q0.y, q0.z, q0.w}, qb[4] = {q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float sv[TJ];
+                lds_vec<TJ>(sS + (c + e) * LU + j0, sv);
+#pragma unroll
+                for (int y = 0; y < TJ; ++y) {
+                    ae[0][y] = fmaf(-wa[e], sv[y], ae[0][y]);
+                    ae[1][y] = fmaf(-wb[e], sv[y], ae[1][y]);
+                    ay[0][y] = fmaf(qa[e], sv[y], ay[0][y]);
+                    ay[1][y] = fmaf(qb[e], sv[y], ay[1][y]);
+                }
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int y = 0; y < TJ; ++y) sE[(r0 + x) * LU + j0 + y] = ae[x][y];
+        __syncthreads();
+        // ---- phase 2: O = Y + L E (L lower triangular: rows r0, r0 + 1 need i <= r0 + 1)
+        if (o != nullptr) {
+            for (int i = 0; i <= r0 + 1; i += 4) {
+                const float4 l0 = *reinterpret_cast<const float4 *>(sL + r0 * LL + i);
+                const float4 l1 = *reinterpret_cast<const float4 *>(sL + (r0 + 1) * LL + i);
+                const float la[4] = {l0.x, l0.y, l0.z, l0.w}, lb[4] = {l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float ev[TJ];
+                    lds_vec<TJ>(sE + (i + e) * LU + j0, ev);
+#pragma unroll
+                    for (int y = 0; y < TJ; ++y) {
+                        ay[0][y] = fmaf(la[e], ev[y], ay[0][y]);
+                        ay[1][y] = fmaf(lb[e], ev[y], ay[1][y]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                if (r0 + x >= len) continue;
+                const int64_t oi = ((t0 + r0 + x) * H + h) * (int64_t)V + v0 + j0;
+                if (!GCL_RANGE_IN_BOUNDS(oi, oi + TJ - 1, p.t_max * H * (int64_t)V, p.dev_status)) continue;
+#pragma unroll
+                for (int y = 0; y < TJ; ++y) st_out(o, oi + y, ay[x][y]);
+            }
+        }
+        // ---- S <- Gamma_c o S + K'^T E on keys c0 .., columns s0 .. (in place: each thread
+        // reads and writes only its own entries)
+        {
+            float as[TC][TS];
+#pragma unroll
+            for (int x = 0; x < TC; ++x)
+#pragma unroll
+                for (int y = 0; y < TS; ++y) as[x][y] = sGC[c0 + x] * sS[(c0 + x) * LU + s0 + y];
+#pragma unroll 4
+            for (int r = 0; r < C; ++r) {
+                float kt[TC], ev[TS];
+                lds_vec<TC>(sKt + r * LW + c0, kt);
+                lds_vec<TS>(sE + r * LU + s0, ev);
+#pragma unroll
+                for (int x = 0; x < TC; ++x)
+#pragma unroll
+                    for (int y = 0; y < TS; ++y) as[x][y] = fmaf(kt[x], ev[y], as[x][y]);
+            }
+#pragma unroll
+            for (int x = 0; x < TC; ++x)
+#pragma unroll
+                for (int y = 0; y < TS; ++y) sS[(c0 + x) * LU + s0 + y] = as[x][y];
+        }
+        if (Lay::NB == 1 && ic + 1 < nch) {
+            __syncthreads();          // every read of the single record buffer is done
+            issue(ic + 1, 0);
+        }
+    }
+    __syncthreads();
+    if (p.ht) {
+        for (int e = tid; e < K * VS; e += kThreads) {
+            const int c = e / VS, jj = e % VS;
+            const int64_t gi = state_base + (int64_t)c * V + v0 + jj;
+            if (GCL_IN_BOUNDS(gi, n_state, p.dev_status)) p.ht[gi] = sS[c * LU + jj];
+        }
+    }
+}
+
+// Value-column slice of the chain: 16 at K = 64, 32 at K = 128.
+template <int K>
+struct ChainSlice {
+    static constexpr int VS = K == 64 ? 16 : 32;
+};
+
+template <int K, int V, int C>
+size_t record_bytes(int64_t nt_max, int H) {
+    return sizeof(float) * (size_t)nt_max * H * Rec<K, V, C>::floats;
+}
+
+template <int VAR, typename Tin, int K, int V, int C>
+cudaError_t launch(const FwdParams &p, cudaStream_t s) {
+    using PL = PrepLayout<K, V, VAR, C>;
+    constexpr int VS = ChainSlice<K>::VS;
+    using CL = ChainLayout<K, VS, C>;
+    auto prep = prep_kernel<VAR, Tin, K, V, C>;
+    auto chain = chain_kernel<Tin, K, V, VS, C>;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CL::bytes);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(prep, dim3((unsigned)p.nt_max, p.H), dim3(kThreads), PL::bytes, s, p);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(chain, dim3(V / VS, p.H, p.n_max), dim3(kThreads), CL::bytes, s, p);
+}
+
+}  // namespace simt_split
+
+}  // namespace gcl

@@ -79,9 +79,13 @@ static void align_ws(void *ws, size_t bytes, void **out, size_t *out_bytes) {
 
 // Forward workspace: the minimum (W form) or what the fastest launch plan uses.
 static size_t fwd_ws(const gcl_fwd_args *a, int variant, bool fastest) {
-    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt)) return 0;
     const int64_t ntm = gcl_nt_max(a->t_max, a->n_max, a->bt);
     if (ntm <= 0 || a->H <= 0 || a->n_max <= 0) return 0;
+    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt)) {
+        // the CUDA cores: the single kernel needs none; the split plan holds its records
+        const size_t rec = fwd_simt_split_bytes(a->K, a->V, a->bt, ntm, a->H);
+        return fastest && rec > 0 ? rec + kWsAlign : 0;
+    }
     // the fused plan keeps everything on chip; a training forward's fastest plan is the
     // transition form (its records serve the backward), its least the fused plan
     if (fwd_tc_runs_fused(variant, a->n_max, a->H, a->h_save != nullptr, 0, ntm) &&
@@ -130,7 +134,11 @@ static gcl_status_t run_fwd(const gcl_fwd_args *a, gcl_stream_t stream, int vari
     p.o = a->o; p.ht = a->ht; p.h_save = a->h_save; p.dev_status = a->dev_status;
     p.workspace = nullptr;
     p.workspace_bytes = 0;
-    if (tc && a->workspace) align_ws(a->workspace, a->workspace_bytes, &p.workspace, &p.workspace_bytes);
+    if (a->workspace) {
+        if (!aligned16(a->workspace))
+            return fail(GCL_ERR_INVALID_ARG, "%s: every buffer must be 16-byte aligned", fn);
+        align_ws(a->workspace, a->workspace_bytes, &p.workspace, &p.workspace_bytes);
+    }
     p.t_max = a->t_max; p.n_max = a->n_max; p.H = a->H; p.K = a->K; p.V = a->V; p.bt = a->bt;
     p.nt_max = ntm;
     p.scale = a->scale;
@@ -353,10 +361,14 @@ static int32_t fwd_plan(const gcl_fwd_args *a, int variant) {
     if (check_common("plan", a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->t_max, a->n_max,
                      a->H, a->K, a->V, a->bt, a->dtype) != GCL_OK)
         return -1;
-    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt)) return GCL_PLAN_CUDA_CORES;
     void *w = nullptr;
     size_t wb = 0;
     if (a->workspace) align_ws(a->workspace, a->workspace_bytes, &w, &wb);
+    if (!fwd_tc_supported(variant, a->dtype, a->K, a->V, a->bt)) {
+        const size_t rec = fwd_simt_split_bytes(a->K, a->V, a->bt, gcl_nt_max(a->t_max, a->n_max, a->bt), a->H);
+        return rec > 0 && w && wb >= rec && a->chunk_indices && a->chunk_offsets ? GCL_PLAN_CUDA_CORES_SPLIT
+                                                                                  : GCL_PLAN_CUDA_CORES;
+    }
     return fwd_tc_plan(variant, a->n_max, a->H, a->h_save != nullptr, wb,
                        gcl_nt_max(a->t_max, a->n_max, a->bt), a->dtype);
 }

@@ -67,6 +67,8 @@ cudaError_t launch_chunk_meta_i64(const int64_t *cu, int32_t n_max, int64_t t_ma
                                   int64_t nt_max, int32_t *cu32, int32_t *idx, int32_t *off,
                                   int32_t *order, int32_t *status, cudaStream_t s);
 cudaError_t launch_fwd_simt(const FwdParams &p, int variant, int dtype, cudaStream_t s);
+// Workspace of the CUDA-core split plan (chunk prep records + chain), 0 where it does not apply.
+size_t fwd_simt_split_bytes(int K, int V, int bt, int64_t nt_max, int H);
 template <typename Tin>
 cudaError_t launch_fwd_simt_t(const FwdParams &p, int variant, cudaStream_t s);
 // Tensor-core forward (GDN, bf16, K = V = 128).  Two launch plans: the W form

@@ -242,7 +242,8 @@ typedef enum {
     GCL_PLAN_FUSED = 1,
     GCL_PLAN_W_FORM = 2,
     GCL_PLAN_TRANSITION = 3,
-    GCL_PLAN_SEGMENTED = 4
+    GCL_PLAN_SEGMENTED = 4,
+    GCL_PLAN_CUDA_CORES_SPLIT = 5
 } gcl_fwd_plan_t;
 int32_t gcl_fwd_plan(const gcl_fwd_args *args);
 int32_t gcl_kda_fwd_plan(const gcl_fwd_args *args);

@@ -66,11 +66,13 @@ def test_launch_count_per_step():
     assert bench.fwd_plan_of(ws["gdn_varlen_bf16_N32_Nmax64_Tmax65536_H16_d128"]) == "fused"
     assert bench.launches_per_step(ws["gdn_fwdbwd_bf16_B4_T8192_H16_d128"]) == 6
     assert bench.launches_per_step(ws["kda_fwd_bf16_T2048_H10_d128"]) == 3
-    assert bench.launches_per_step(ws["gdn_fwd_fp32_T256_H2_d64"]) == 2
+    # fp32 with the fastest workspace: the CUDA-core split plan (chunk prep + chain)
+    assert bench.fwd_plan_of(ws["gdn_fwd_fp32_T256_H2_d64"]) == "cuda_cores_split"
+    assert bench.launches_per_step(ws["gdn_fwd_fp32_T256_H2_d64"]) == 3
     assert bench.launches_per_step(ws["kda_fwdbwd_bf16_T2048_H10_d128"]) == 5
     # one 64K-token sequence of one head: the segmented chain (on any GPU of 24 or more SMs)
     assert bench.launches_per_step(ws["gdn_fwd_bf16_T65536_H1_d128"]) == 5
     assert bench.launches_per_step(ws["kda_fwd_bf16_T65536_H1_d128"]) == 5
-    # chunk size 32 runs the fused CUDA-core forward; fp16 (GDN, d = 128) the transition form
+    # chunk size 32 runs the CUDA-core split plan; fp16 (GDN, d = 128) the transition form
     assert bench.launches_per_step(ws["gdn_fwd_f16_T4096_H16_d128"]) == 3       # fp16: tensor cores
-    assert bench.launches_per_step(ws["gdn_fwd_bf16_bt32_T4096_H16_d128"]) == 2
+    assert bench.launches_per_step(ws["gdn_fwd_bf16_bt32_T4096_H16_d128"]) == 3
