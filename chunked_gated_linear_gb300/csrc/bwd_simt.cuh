@@ -110,7 +110,7 @@ dstate_sweep_kernel(BwdParams p) {
         __syncthreads();
         simt_intra<VAR, K, kSweepThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
         __syncthreads();
-        simt_solve<kSweepThreads, C>(sA, sT);
+        simt_solve_blocked<kSweepThreads, C>(sA, sT, sW);   // W is formed after the solve
         simt_w<VAR, K, kSweepThreads, C>(sT, sB, sG, sK, sW);
         // dE = L^T dO + Ktil dS'
         for (int e = tid; e < C * VS; e += kSweepThreads) {
@@ -237,7 +237,7 @@ chunk_grad_kernel(BwdParams p) {
     for (int e = tid; e < C * kLC; e += kGradThreads) { sDL[e] = 0.f; sDT[e] = 0.f; }
     for (int r = tid; r < C; r += kGradThreads) { sRA[r] = sRB[r] = sRC[r] = sRD[r] = 0.f; }
     __syncthreads();
-    simt_solve<kGradThreads, C>(sA, sT);
+    simt_solve_blocked<kGradThreads, C>(sA, sT, sAp);   // A' is formed at the end
 
     const float gC = sG[C - 1];
     // per-row exponentials, once (the loops below only multiply)
@@ -525,12 +525,12 @@ chunk_grad_kda_kernel(BwdParams p) {
     __syncthreads();
     simt_gate_cumsum<kKDA, K, kGradThreads, C>(sG);
     __syncthreads();
-    simt_intra<kKDA, K, kGradThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    simt_intra<kKDA, K, kGradThreads, C, true>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
     for (int e = tid; e < C * kLC; e += kGradThreads) { sDL[e] = 0.f; sDT[e] = 0.f; }
     for (int r = tid; r < C; r += kGradThreads) { sRB[r] = 0.f; sRC[r] = 0.f; }
     for (int c = tid; c < K; c += kGradThreads) { sSS[c] = 0.f; sGC[c] = sG[(C - 1) * LK + c]; }
     __syncthreads();
-    simt_solve<kGradThreads, C>(sA, sT);
+    simt_solve_blocked<kGradThreads, C>(sA, sT, sAp);   // A' is formed at the end
     // Kp and Kb in place of Q and gamma (both are reloaded after the slice loop)
     for (int e = tid; e < C * K; e += kGradThreads) {
         const int r = e / K, c = e % K;
@@ -659,7 +659,7 @@ chunk_grad_kda_kernel(BwdParams p) {
         sDT[r * kLC + i] = acc;      // sDT now holds dA
     }
     __syncthreads();
-    simt_intra<kKDA, K, kGradThreads, C>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
+    simt_intra<kKDA, K, kGradThreads, C, true>(sQ, sK, sG, sB, p.scale, nullptr, nullptr, sAp);
     __syncthreads();
     const float *sDA = sDT;
     for (int r = tid; r < C; r += kGradThreads) {   // dbeta, one thread per row
@@ -678,12 +678,12 @@ chunk_grad_kda_kernel(BwdParams p) {
             const float gr = sG[r * LK + c], eg = expf(gr), ec = expf(sGC[c] - gr);
             float pl = 0.f, pa = 0.f, ql = 0.f, qa = 0.f;
             for (int i = 0; i <= r; ++i) {
-                const float kd = sK[i * LK + c] * expf(gr - sG[i * LK + c]);
+                const float kd = sK[i * LK + c] * __expf(gr - sG[i * LK + c]);
                 pl = fmaf(sDL[r * kLC + i], kd, pl);
                 pa = fmaf(sDA[r * kLC + i], kd, pa);
             }
             for (int r2 = r; r2 < C; ++r2) {
-                const float d = expf(sG[r2 * LK + c] - gr);
+                const float d = __expf(sG[r2 * LK + c] - gr);
                 ql = fmaf(sDL[r2 * kLC + r], sQ[r2 * LK + c] * d, ql);
                 qa = fmaf(sDA[r2 * kLC + r] * sB[r2], sK[r2 * LK + c] * d, qa);
             }

@@ -689,36 +689,63 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         __syncthreads();
         // ---- dA = -T^T (dT T^T), strictly lower; dT counts only on and below the diagonal.
-        // X = dT T^T: X[r][m] = sum_{i <= r} dT[r][i] T[m][i]  (T[m][i] = 0 for i > m; 1 x 4 strips)
-        for (int sidx = tid; sidx < C * 16; sidx += kThreads) {
-            const int r = sidx & 63, m0 = (sidx >> 6) * 4;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int i = 0; i <= r; ++i) {
-                const float dt = fDT[r * kSolveLD + i];
+        // Both products in 4 x 4 register tiles with float4 loads (T is zero above its diagonal).
+        // X = dT T^T: X[r][m] = sum_{i <= min(r, m)} dT[r][i] T[m][i]; rows r0 .. r0 + 3, columns
+        // mb + 16 a (interleaved, so the T rows a quarter warp loads sit in distinct banks)
+        {
+            const int r0 = (tid >> 4) * 4, mb = tid & 15;
+            float acc[4][4] = {};
+            for (int i4 = 0; i4 <= r0 / 4; ++i4) {
+                float dt[4][4], tt[4][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = fmaf(dt, fT[(m0 + e) * kSolveLD + i], acc[e]);
+                for (int x = 0; x < 4; ++x) {
+                    const float4 v = *reinterpret_cast<const float4 *>(fDT + (r0 + x) * kSolveLD + 4 * i4);
+                    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dt[x][e] = 4 * i4 + e <= r0 + x ? vv[e] : 0.f;
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float4 v = *reinterpret_cast<const float4 *>(fT + (mb + 16 * a) * kSolveLD + 4 * i4);
+                    tt[a][0] = v.x;
+                    tt[a][1] = v.y;
+                    tt[a][2] = v.z;
+                    tt[a][3] = v.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) acc[x][a] = fmaf(dt[x][e], tt[a][e], acc[x][a]);
             }
-            *reinterpret_cast<float4 *>(fX + r * kSolveLD + m0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int a = 0; a < 4; ++a) fX[(r0 + x) * kSolveLD + mb + 16 * a] = acc[x][a];
         }
         __syncthreads();
-        // dA[r][i] = -sum_{m >= r} T[m][r] X[m][i] for i < r, else 0  (over dT, which is consumed)
-        for (int sidx = tid; sidx < C * 16; sidx += kThreads) {
-            const int r = sidx & 63, i0 = (sidx >> 6) * 4;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (i0 < r) {
-                for (int m = r; m < C; ++m) {
-                    const float t = fT[m * kSolveLD + r];
-                    const float4 x = *reinterpret_cast<const float4 *>(fX + m * kSolveLD + i0);
-                    acc[0] = fmaf(-t, x.x, acc[0]);
-                    acc[1] = fmaf(-t, x.y, acc[1]);
-                    acc[2] = fmaf(-t, x.z, acc[2]);
-                    acc[3] = fmaf(-t, x.w, acc[3]);
+        // dA[r][i] = -sum_{m >= r} T[m][r] X[m][i] for i < r, else 0 (over dT, which is consumed);
+        // rows r0 .. r0 + 3, columns i0 .. i0 + 3
+        {
+            const int r0 = (tid >> 4) * 4, i0 = (tid & 15) * 4;
+            float acc[4][4] = {};
+            if (i0 < r0 + 3) {
+                for (int m = r0; m < C; ++m) {
+                    const float4 t = *reinterpret_cast<const float4 *>(fT + m * kSolveLD + r0);
+                    const float4 xv = *reinterpret_cast<const float4 *>(fX + m * kSolveLD + i0);
+                    const float tv[4] = {t.x, t.y, t.z, t.w}, xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(-tv[x], xx[y], acc[x][y]);
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (i0 + e >= r) acc[e] = 0.f;
-            *reinterpret_cast<float4 *>(fDT + r * kSolveLD + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            for (int x = 0; x < 4; ++x)
+                *reinterpret_cast<float4 *>(fDT + (r0 + x) * kSolveLD + i0) =
+                    make_float4(i0 < r0 + x ? acc[x][0] : 0.f, i0 + 1 < r0 + x ? acc[x][1] : 0.f,
+                                i0 + 2 < r0 + x ? acc[x][2] : 0.f, i0 + 3 < r0 + x ? acc[x][3] : 0.f);
         }
         __syncthreads();
         // ---- gate sums of dA o A' (both strictly lower): row sums, beta-weighted column sums
@@ -820,23 +847,38 @@ tc_grad2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_bf16(tmem + 128, apt + s * 128, bq + s * 128, idesc_bf16(128, 128, 1, 1), 1);
             mma_commit(&bar_mma);
         }
-        const bool ok = mbar_wait(&bar_mma, 0, &s_err, 2);
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) break;
-        // dk += M K + M^T K + P^T Q (lanes 0..63), dq += P K (lanes 64..127), 16 columns at a time
+        // dk += M K + M^T K + P^T Q (lanes 0..63), dq += P K (lanes 64..127), 16 columns at a
+        // time; the first kernel's partial rows are read ahead (two groups of 16 columns in
+        // flight), so their latency overlaps the MMA round and the additions
         const bool isk = lrow < C;
         const int r = isk ? lrow : lrow - C;
         float *grow = (isk ? p.dk : p.dq) + ((t0 + r) * H + h) * (int64_t)KD + half * 64;
-#pragma unroll 1
+        const bool live = r < len;
+        float4 part[2][4];
+        auto fetch = [&](int q, float4 (&dst)[4]) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[e] = live ? *reinterpret_cast<const float4 *>(grow + q * 16 + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        fetch(0, part[0]);
+        fetch(1, part[1]);
+        const bool ok = mbar_wait(&bar_mma, 0, &s_err, 2);
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) break;
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
             float x[16], y[16];
             tmem_ld16(tmem + lane_off + half * 64 + q * 16, x);
             if (isk) tmem_ld16(tmem + lane_off + 128 + half * 64 + q * 16, y);
             tmem_ld_wait();
-            if (r < len) {
+            float4 cur[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cur[e] = part[q & 1][e];
+            if (q + 2 < 4) fetch(q + 2, part[q & 1]);
+            if (live) {
 #pragma unroll
                 for (int e = 0; e < 16; e += 4) {
-                    float4 d = *reinterpret_cast<float4 *>(grow + q * 16 + e);
+                    float4 d = cur[e >> 2];
                     d.x += x[e] + (isk ? y[e] : 0.f);
                     d.y += x[e + 1] + (isk ? y[e + 1] : 0.f);
                     d.z += x[e + 2] + (isk ? y[e + 2] : 0.f);

@@ -69,8 +69,11 @@ __device__ __forceinline__ float gam(const float *sG, int r, int c) {
 }
 
 // A (= beta_r A', strictly lower) into sA and L into sL.  If sAp is not null it
-// also receives A' (without beta).
-template <int VAR, int K, int NT, int C>
+// also receives A' (without beta).  FastExp takes the per-channel decays of KDA with the
+// hardware exponential (__expf: about 2^-21 relative error for the arguments that matter,
+// |gamma_r - gamma_i| of a few units, far inside the fp32 bar; the gradients take it, the
+// forward keeps expf).
+template <int VAR, int K, int NT, int C, bool FastExp = false>
 __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, const float *sG,
                                            const float *sB, float scale, float *sA, float *sL,
                                            float *sAp) {
@@ -132,7 +135,8 @@ __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, con
                 qk *= d;
             } else {
                 for (int c = 0; c < K; ++c) {
-                    const float d = expf(sG[r * LK + c] - sG[i * LK + c]);
+                    const float x = sG[r * LK + c] - sG[i * LK + c];
+                    const float d = FastExp ? __expf(x) : expf(x);
                     kk = fmaf(sK[r * LK + c] * d, sK[i * LK + c], kk);
                     qk = fmaf(sQ[r * LK + c] * d, sK[i * LK + c], qk);
                 }
