@@ -543,19 +543,42 @@ chunk_grad_kda_kernel(BwdParams p) {
 #pragma unroll
     for (int m = 0; m < CPT; ++m) { y1[m] = 0.f; y2[m] = 0.f; y3[m] = 0.f; }
 
+    // the value slice's S, dS', V and dO columns are read into registers one slice ahead, so
+    // their global-memory latency overlaps the previous slice's work
+    constexpr int KI = K * kVS / kGradThreads, CI = C * kVS / kGradThreads;
+    static_assert(KI * kGradThreads == K * kVS && CI * kGradThreads == C * kVS, "whole loads per thread");
+    float pS[KI], pD[KI], pV[CI], pO[CI];
+    auto fetch = [&](int s0) {
+#pragma unroll
+        for (int u = 0; u < KI; ++u) {
+            const int e = tid + u * kGradThreads, c = e / kVS, j = e % kVS;
+            pS[u] = Sg[(int64_t)c * V + s0 + j];
+            pD[u] = dSg[(int64_t)c * V + s0 + j];
+        }
+#pragma unroll
+        for (int u = 0; u < CI; ++u) {
+            const int e = tid + u * kGradThreads, r = e / kVS, j = e % kVS;
+            const int64_t gi = ((t0 + r) * H + h) * (int64_t)V + s0 + j;
+            pV[u] = r < len ? ld_in(v, gi) : 0.f;
+            pO[u] = r < len ? ld_in(d_o, gi) : 0.f;
+        }
+    };
+    fetch(0);
     for (int s0 = 0; s0 < V; s0 += kVS) {
         __syncthreads();
-        for (int e = tid; e < K * kVS; e += kGradThreads) {
-            const int c = e / kVS, j = e % kVS;
-            sS[c * LV + j] = Sg[(int64_t)c * V + s0 + j];
-            sDS[c * LV + j] = dSg[(int64_t)c * V + s0 + j];
+#pragma unroll
+        for (int u = 0; u < KI; ++u) {
+            const int e = tid + u * kGradThreads, c = e / kVS, j = e % kVS;
+            sS[c * LV + j] = pS[u];
+            sDS[c * LV + j] = pD[u];
         }
-        for (int e = tid; e < C * kVS; e += kGradThreads) {
-            const int r = e / kVS, j = e % kVS;
-            const int64_t gi = ((t0 + r) * H + h) * (int64_t)V + s0 + j;
-            sV[r * LV + j] = r < len ? ld_in(v, gi) : 0.f;
-            sDO[r * LV + j] = r < len ? ld_in(d_o, gi) : 0.f;
+#pragma unroll
+        for (int u = 0; u < CI; ++u) {
+            const int e = tid + u * kGradThreads, r = e / kVS, j = e % kVS;
+            sV[r * LV + j] = pV[u];
+            sDO[r * LV + j] = pO[u];
         }
+        if (s0 + kVS < V) fetch(s0 + kVS);
         __syncthreads();
         for (int c = tid; c < K; c += kGradThreads) {   // <dS', S> per key channel
             float a = sSS[c];
@@ -667,34 +690,54 @@ chunk_grad_kda_kernel(BwdParams p) {
         for (int i = 0; i < r; ++i) da_row = fmaf(sDA[r * kLC + i], sAp[r * kLC + i], da_row);
         if (r < len) p.dbeta[(t0 + r) * H + h] = sRB[r] - sRC[r] + da_row;
     }
-    // ---- dq, dk and dgamma of (my_r, channel)
+    // ---- dq, dk and dgamma of (my_r, channel): the row's dL and dA entries are read once
+    // per pair and serve eight channels at a time (eight independent sums per loop)
     float dgv[CPT], wv[CPT];
     {
         const int r = my_r;
         const float br = sB[r];
+        constexpr int HM = CPT >= 8 ? 8 : CPT;
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const int c = my_c0 + TPR * m;
-            const float gr = sG[r * LK + c], eg = expf(gr), ec = expf(sGC[c] - gr);
-            float pl = 0.f, pa = 0.f, ql = 0.f, qa = 0.f;
+        for (int m0 = 0; m0 < CPT; m0 += HM) {
+            float gr[HM], pl[HM], pa[HM], ql[HM], qa[HM];
+#pragma unroll
+            for (int mm = 0; mm < HM; ++mm) {
+                gr[mm] = sG[r * LK + my_c0 + TPR * (m0 + mm)];
+                pl[mm] = pa[mm] = ql[mm] = qa[mm] = 0.f;
+            }
             for (int i = 0; i <= r; ++i) {
-                const float kd = sK[i * LK + c] * __expf(gr - sG[i * LK + c]);
-                pl = fmaf(sDL[r * kLC + i], kd, pl);
-                pa = fmaf(sDA[r * kLC + i], kd, pa);
+                const float dl = sDL[r * kLC + i], da = sDA[r * kLC + i];
+#pragma unroll
+                for (int mm = 0; mm < HM; ++mm) {
+                    const int c = my_c0 + TPR * (m0 + mm);
+                    const float kd = sK[i * LK + c] * __expf(gr[mm] - sG[i * LK + c]);
+                    pl[mm] = fmaf(dl, kd, pl[mm]);
+                    pa[mm] = fmaf(da, kd, pa[mm]);
+                }
             }
             for (int r2 = r; r2 < C; ++r2) {
-                const float d = __expf(sG[r2 * LK + c] - gr);
-                ql = fmaf(sDL[r2 * kLC + r], sQ[r2 * LK + c] * d, ql);
-                qa = fmaf(sDA[r2 * kLC + r] * sB[r2], sK[r2 * LK + c] * d, qa);
+                const float dl = sDL[r2 * kLC + r], dab = sDA[r2 * kLC + r] * sB[r2];
+#pragma unroll
+                for (int mm = 0; mm < HM; ++mm) {
+                    const int c = my_c0 + TPR * (m0 + mm);
+                    const float d = __expf(sG[r2 * LK + c] - gr[mm]);
+                    ql[mm] = fmaf(dl, sQ[r2 * LK + c] * d, ql[mm]);
+                    qa[mm] = fmaf(dab, sK[r2 * LK + c] * d, qa[mm]);
+                }
             }
-            const float qv = sQ[r * LK + c], kv = sK[r * LK + c];
-            const float dq = p.scale * (eg * y2[m] + pl);
-            const float dk = -br * eg * y1[m] + ec * y3[m] + br * pa + p.scale * ql + qa;
-            dgv[m] = qv * dq + kv * (-br * eg * y1[m] - ec * y3[m] + br * pa - p.scale * ql - qa);
-            wv[m] = kv * ec * y3[m];
-            if (r < len) {
-                p.dq[((t0 + r) * H + h) * (int64_t)K + c] = dq;
-                p.dk[((t0 + r) * H + h) * (int64_t)K + c] = dk;
+#pragma unroll
+            for (int mm = 0; mm < HM; ++mm) {
+                const int m = m0 + mm, c = my_c0 + TPR * m;
+                const float eg = expf(gr[mm]), ec = expf(sGC[c] - gr[mm]);
+                const float qv = sQ[r * LK + c], kv = sK[r * LK + c];
+                const float dq = p.scale * (eg * y2[m] + pl[mm]);
+                const float dk = -br * eg * y1[m] + ec * y3[m] + br * pa[mm] + p.scale * ql[mm] + qa[mm];
+                dgv[m] = qv * dq + kv * (-br * eg * y1[m] - ec * y3[m] + br * pa[mm] - p.scale * ql[mm] - qa[mm]);
+                wv[m] = kv * ec * y3[m];
+                if (r < len) {
+                    p.dq[((t0 + r) * H + h) * (int64_t)K + c] = dq;
+                    p.dk[((t0 + r) * H + h) * (int64_t)K + c] = dk;
+                }
             }
         }
     }
