@@ -170,8 +170,15 @@ typedef struct gcl_fwd_args {
     int32_t dtype;                 /* gcl_dtype_t of q, k, v, beta, o                        */
 } gcl_fwd_args;
 
-/* Bytes of device workspace the forward's fastest launch plan uses for these sizes
- * (0 when the fp32 CUDA-core kernel serves them), and the least it accepts.
+/* Bytes of device workspace the forward's fastest launch plan uses for these sizes, and
+ * the least it accepts.
+ *
+ * Sizes the CUDA cores serve (fp32 inputs, K or V = 64, bt = 32, and the KDA forward
+ * with fp16 inputs) have two plans: one fp32 kernel, which needs no workspace (the
+ * minimum, 0), and the split plan, fastest, whose records are per chunk row and head the
+ * fp32 matrices W, Q', K' [BT x K], L [BT x BT], U [BT x V] and Gamma_c [K] (80 KiB at
+ * K = V = 64, BT = 64; 144 KiB at K = V = 128), for K = V only; it runs whenever the
+ * workspace holds them and chunk_indices and chunk_offsets are given.
  *
  * The tensor-core path has two plans.  The W form keeps per chunk and head the
  * inverted intra-chunk matrix T and the masked decayed QK^T, 25 KiB (bf16); it is
@@ -191,8 +198,8 @@ size_t gcl_fwd_workspace_min_bytes(const gcl_fwd_args *args);
  * NULL; with h_save (a training forward) the fastest plan stays the transition form
  * (its records serve the backward) and the fused plan runs with any smaller workspace. */
 
-/* Bytes of device workspace kda_chunk_fwd's fastest plan needs for these sizes (0
- * when the fp32 CUDA-core kernel serves them).  KDA on the tensor cores runs the
+/* Bytes of device workspace kda_chunk_fwd's fastest plan needs for these sizes (on the
+ * CUDA cores: the split plan's records, as above).  KDA on the tensor cores runs the
  * transition form (96.5 KiB per chunk and head: the chunk's affine state map and
  * output map, and the per-key-channel state decay of the chunk); a workspace
  * smaller than those records returns GCL_ERR_CAPACITY.  When the fastest plan is
@@ -226,14 +233,17 @@ int32_t gcl_fwd_chain_segments(int64_t t_max, int32_t n_max, int32_t H, int32_t 
 /*
  * The launch plan a forward with these arguments runs (workspace_bytes included), for
  * callers that size graphs or count launches, and for tests:
- *   GCL_PLAN_CUDA_CORES  one fp32 CUDA-core kernel (fp32 or fp16 inputs, K or V = 64, bt = 32)
+ *   GCL_PLAN_CUDA_CORES  one fp32 CUDA-core kernel (fp32 inputs, K or V = 64, bt = 32, fp16 KDA)
+ *   GCL_PLAN_CUDA_CORES_SPLIT  the same sizes (K = V) as a chunk prep over every chunk and head
+ *                        plus a chain over value-column slices (HA-NPU section 2.1: only the
+ *                        Reduce is serial), when the workspace holds the prep's records
  *   GCL_PLAN_FUSED       one tensor-core kernel per (sequence, head), everything on chip
  *                        (GDN, n_max * H >= SMs: HA-NPU section 4, first tier)
  *   GCL_PLAN_W_FORM      chunk prep (T, L records) + chain over value-column slices
  *   GCL_PLAN_TRANSITION  chunk prep (affine chunk maps) + chain over value-column slices
  *   GCL_PLAN_SEGMENTED   the transition plan with the segment-parallel chain
- * Every plan but the last runs chunk_meta_build's output through one or two launches; the
- * segmented plan adds the segment summaries, the scan and the segment outputs.  Returns -1
+ * Every plan but the segmented one runs chunk_meta_build's output through one or two
+ * launches; the segmented plan adds the segment summaries, the scan and the segment outputs.  Returns -1
  * for arguments the forward would reject on the host.  gcl_fwd_plan describes
  * gdn_chunk_fwd, gcl_kda_fwd_plan kda_chunk_fwd.
  */

@@ -122,6 +122,35 @@ def test_plan_rules_from_sizes_alone(lib):
     assert lib.gcl_fwd_chain_segments(65536, 1, 1, 32) == 0
 
 
+def test_cuda_core_plans_from_sizes_alone(lib):
+    """The CUDA-core sizes: no workspace at the minimum (one kernel); the fastest workspace holds
+    the split plan's records, (3 BT K + BT^2 + BT V + K) fp32 per chunk row and head, for
+    K = V only; the split plan runs only with that workspace and the chunk metadata."""
+    import chunked_gated_linear_gb300 as gcl
+    fake = 1 << 20
+    nt = lambda t, n, bt: lib.gcl_nt_max(t, n, bt)
+    for K, bt, dtype in ((64, 64, 0), (128, 64, 0), (128, 32, 1), (64, 32, 2)):
+        base = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake,
+                    t_max=4096, n_max=3, H=2, K=K, V=K, bt=bt, scale=1.0, dtype=dtype,
+                    chunk_indices=fake, chunk_offsets=fake)
+        a = gcl.FwdArgs(**base)
+        rec = 4 * nt(4096, 3, bt) * 2 * (3 * bt * K + bt * bt + bt * K + K)
+        fastest = lib.gcl_fwd_workspace_bytes(ctypes.byref(a))
+        assert lib.gcl_fwd_workspace_min_bytes(ctypes.byref(a)) == 0
+        assert rec <= fastest <= rec + 1024, (K, bt, dtype)           # + alignment slack
+        assert lib.gcl_fwd_plan(ctypes.byref(a)) == 0                  # no workspace: one kernel
+        w = gcl.FwdArgs(**base, workspace=fake, workspace_bytes=fastest)
+        assert lib.gcl_fwd_plan(ctypes.byref(w)) == 5                  # GCL_PLAN_CUDA_CORES_SPLIT
+        assert lib.gcl_kda_fwd_plan(ctypes.byref(w)) == 5
+        short = gcl.FwdArgs(**base, workspace=fake, workspace_bytes=rec - 16)
+        assert lib.gcl_fwd_plan(ctypes.byref(short)) == 0
+        nometa = gcl.FwdArgs(**{**base, "chunk_indices": None}, workspace=fake, workspace_bytes=fastest)
+        assert lib.gcl_fwd_plan(ctypes.byref(nometa)) == 0
+    mixed = gcl.FwdArgs(q=fake, k=fake, v=fake, g=fake, beta=fake, cu_seqlens=fake, o=fake,
+                        t_max=4096, n_max=3, H=2, K=64, V=128, bt=64, scale=1.0, dtype=0)
+    assert lib.gcl_fwd_workspace_bytes(ctypes.byref(mixed)) == 0       # K != V: one kernel
+
+
 def test_host_errors_other_entry_points(lib):
     """The KDA backward, the short convolution, the no-allocation forward and the wait
     self-test reject bad arguments on the host, before anything is enqueued."""
