@@ -437,7 +437,8 @@ def measure(gcl, w, args, rank, world, dist, dev, steps, warmup, graphs=True):
     out["direct"] = {"region_ms": e_s[0].elapsed_time(e_e[-1]), "p50_ms": pct(direct, 50),
                      "p95_ms": pct(direct, 95), "tokens": sum(tok)}
     # the forward kernels' time per set (its algorithmic bytes differ by layout)
-    per_set_kern = [float(np.mean(kern[j::n])) for j in range(n)]
+    # (a set that no timed step reached, where steps < sets, has no time: None)
+    per_set_kern = [float(np.mean(kern[j::n])) if j < steps else None for j in range(n)]
     out["kernel_ms_per_set"] = per_set_kern
     out["kernel_ms"] = float(np.mean(kern))
     if not graphs:
@@ -527,8 +528,8 @@ def run_gpu(args, rank, world, dist):
     n = m["sets"]
     # roofline of the forward kernels: each set's algorithmic bytes over its kernel time
     fw = [r.w for r in sets]
-    rl = [roofline(x, km, kind=fwd_plan_of(x)) for x, km in zip(fw, m["kernel_ms_per_set"])]
-    ab = sum(r["algorithmic_bytes_per_launch"] for r in rl) / n
+    rl = [roofline(x, km, kind=fwd_plan_of(x)) for x, km in zip(fw, m["kernel_ms_per_set"])
+          if km is not None]
     roof = roofline_mean(rl, ms_kern, traffic_record(w.name))
     util = [int(r.t["off"][-1].item()) / gcl.nt_max(x.t_max, x.n_max, x.bt) for r, x in zip(sets, fw)]
     e2e = run_e2e(gcl, sets[:2], torch.cuda.current_stream(),
