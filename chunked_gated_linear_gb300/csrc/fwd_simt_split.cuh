@@ -17,6 +17,7 @@
 #pragma once
 
 #include "simt_map.cuh"
+#include "tc_solve.cuh"
 
 namespace gcl {
 namespace simt_split {
@@ -85,25 +86,54 @@ struct Tile4 {
 template <int K, int V, int VAR, int C>
 struct PrepLayout {
     static constexpr int LK = K + 1, LV = V + 1, kLC = C + 1;
+    static constexpr int LDA = C + 4;                        // A and T: 16-byte aligned rows
     static constexpr int oQ = 0, oK = oQ + C * LK, oV = oK + C * LK;
-    static constexpr int oA = oV + C * LV, oT = oA + C * kLC, oL = oT + C * kLC;
-    static constexpr int oX = oL + C * kLC;                  // solve scratch (3 x 16 x 16)
-    static constexpr int oB = oX + 768, oG = oB + C;
+    static constexpr int oA = oV + C * LV, oT = oA + C * LDA, oL = oT + C * LDA;
+    static constexpr int oB = oL + C * kLC, oE1 = oB + C, oE2 = oE1 + C, oG = oE2 + C;
     static constexpr int total = oG + (VAR == kKDA ? C * LK : C);
     static constexpr size_t bytes = sizeof(float) * total;
+    static_assert(oA % 4 == 0 && oT % 4 == 0, "float4 rows of A and T");
     static_assert(bytes <= 232448, "one CTA per SM at most");
 };
 
+// T = (I + A)^-1 for a 32 x 32 strictly lower A (row stride LD, 16-byte aligned rows): one
+// warp, lane j forms column j of T by forward substitution down the rows (four partial sums
+// per row).  T is written in full (zeros above the diagonal).
+template <int LD>
+__device__ __forceinline__ void solve_lower32_warp(const float *sA, float *sT) {
+    const int j = threadIdx.x & 31;
+    float x[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m4 = 0; m4 < r; m4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(sA + r * LD + m4);
+            part[0] = fmaf(a.x, x[m4], part[0]);
+            if (m4 + 1 < r) part[1] = fmaf(a.y, x[m4 + 1], part[1]);
+            if (m4 + 2 < r) part[2] = fmaf(a.z, x[m4 + 2], part[2]);
+            if (m4 + 3 < r) part[3] = fmaf(a.w, x[m4 + 3], part[3]);
+        }
+        x[r] = (r == j ? 1.f : 0.f) - ((part[0] + part[1]) + (part[2] + part[3]));
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) sT[r * LD + j] = x[r];
+}
+
+// Warps 0..3 solve for T while warps 4..7 write the records that do not need it (Q', K', L,
+// Gamma_c) and form the operands of W and U in place (HA-NPU section 5: the inversion runs
+// beside the other vector work); then all eight form W and U.
 template <int VAR, typename Tin, int K, int V, int C>
 __global__ void __launch_bounds__(kThreads)
 prep_kernel(FwdParams p) {
     using Lay = PrepLayout<K, V, VAR, C>;
     using R = Rec<K, V, C>;
-    constexpr int LK = Lay::LK, LV = Lay::LV, kLC = Lay::kLC;
+    constexpr int LK = Lay::LK, LV = Lay::LV, kLC = Lay::kLC, LDA = Lay::LDA;
+    static_assert(C == 64 ? LDA == kSolveLD : C == 32, "the 64-row solve's stride");
     extern __shared__ float sm[];
     float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sV = sm + Lay::oV;
-    float *sA = sm + Lay::oA, *sT = sm + Lay::oT, *sL = sm + Lay::oL, *sX = sm + Lay::oX;
-    float *sB = sm + Lay::oB, *sG = sm + Lay::oG;
+    float *sA = sm + Lay::oA, *sT = sm + Lay::oT, *sL = sm + Lay::oL;
+    float *sB = sm + Lay::oB, *sG = sm + Lay::oG, *sE1 = sm + Lay::oE1, *sE2 = sm + Lay::oE2;
 
     // launched as a dependent of the metadata kernel: nothing it wrote is read before this
     grid_dependency_wait();
@@ -177,32 +207,52 @@ prep_kernel(FwdParams p) {
         simt_gate_cumsum<VAR, K, kThreads, C>(sG);
     }
     __syncthreads();
-    simt_intra<VAR, K, kThreads, C>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
-    __syncthreads();
-    simt_solve_blocked<kThreads, C>(sA, sT, sX);    // ends with a block barrier
-    // ---- Q', K', L and Gamma_c straight from shared memory
-    for (int e = tid; e < C * K; e += kThreads) {
-        const int r = e / K, c = e % K;
-        const float gr = gam<VAR, K>(sG, r, c), gc = gam<VAR, K>(sG, C - 1, c);
-        if (GCL_RANGE_IN_BOUNDS(rec0 + R::oQ + e, rec0 + R::oKt + e, n_rec, p.dev_status)) {
-            rec[R::oQ + e] = p.scale * expf(gr) * sQ[r * LK + c];
-            rec[R::oKt + e] = expf(gc - gr) * sK[r * LK + c];
-        }
+    if (VAR == kGDN && tid < C) {      // the row factors Gamma_r and exp(gamma_c - gamma_r)
+        sE1[tid] = expf(sG[tid]);
+        sE2[tid] = expf(sG[C - 1] - sG[tid]);
     }
-    for (int e = tid; e < C * C; e += kThreads)
-        if (GCL_IN_BOUNDS(rec0 + R::oL + e, n_rec, p.dev_status)) rec[R::oL + e] = sL[(e / C) * kLC + e % C];
-    for (int c = tid; c < K; c += kThreads)
-        if (GCL_IN_BOUNDS(rec0 + R::oGC + c, n_rec, p.dev_status)) rec[R::oGC + c] = expf(gam<VAR, K>(sG, C - 1, c));
-    __syncthreads();     // Q is no longer read: it becomes diag(beta) (K o Gamma)
-    for (int e = tid; e < C * K; e += kThreads) {
-        const int r = e / K, c = e % K;
-        sQ[r * LK + c] = sB[r] * expf(gam<VAR, K>(sG, r, c)) * sK[r * LK + c];
+    simt_intra<VAR, K, kThreads, C, false, LDA>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    __syncthreads();
+    if (tid < 128) {
+        // ---- T = (I + A)^-1 on warps 0..3 (named barrier 1 inside the 64-row solve)
+        if constexpr (C == 64) {
+            solve_unit_lower64_r32<128, 1>(sA, sT);
+        } else {
+            if (tid < 32) solve_lower32_warp<LDA>(sA, sT);
+        }
+    } else {
+        // ---- warps 4..7: Q' = scale Gamma o Q and K' = exp(gamma_c - gamma) o K into the
+        // record, then Q's buffer becomes diag(beta) (K o Gamma) (each element read, then
+        // overwritten, by one thread); V's rows take beta; L and Gamma_c into the record
+        const int t = tid - 128;
+        for (int e = t; e < C * K; e += kThreads - 128) {
+            const int r = e / K, c = e % K;
+            float e1, e2;
+            if constexpr (VAR == kGDN) {
+                e1 = sE1[r];
+                e2 = sE2[r];
+            } else {
+                const float gr = gam<VAR, K>(sG, r, c);
+                e1 = expf(gr);
+                e2 = expf(gam<VAR, K>(sG, C - 1, c) - gr);
+            }
+            const float kv = sK[r * LK + c];
+            if (GCL_RANGE_IN_BOUNDS(rec0 + R::oQ + e, rec0 + R::oKt + e, n_rec, p.dev_status)) {
+                rec[R::oQ + e] = p.scale * e1 * sQ[r * LK + c];
+                rec[R::oKt + e] = e2 * kv;
+            }
+            sQ[r * LK + c] = sB[r] * e1 * kv;
+        }
+        for (int e = t; e < C * V; e += kThreads - 128) sV[(e / V) * LV + e % V] *= sB[e / V];
+        for (int e = t; e < C * C; e += kThreads - 128)
+            if (GCL_IN_BOUNDS(rec0 + R::oL + e, n_rec, p.dev_status)) rec[R::oL + e] = sL[(e / C) * kLC + e % C];
+        for (int c = t; c < K; c += kThreads - 128)
+            if (GCL_IN_BOUNDS(rec0 + R::oGC + c, n_rec, p.dev_status)) rec[R::oGC + c] = expf(gam<VAR, K>(sG, C - 1, c));
     }
     __syncthreads();
     // ---- W = T (beta Gamma K) and U = T (beta V): 4 x 4 register tiles, i up to the tile's
-    // last row (T lower triangular); V's rows take beta in place first
-    for (int e = tid; e < C * V; e += kThreads) sV[(e / V) * LV + e % V] *= sB[e / V];
-    __syncthreads();
+    // last row (T is zero above the diagonal inside its 32-row diagonal blocks, and i stays in
+    // the tile's own block)
     auto tile_product = [&](const float *X, int ldx, int W, int oRec) {
         for (int s = tid; s < (C / 4) * (W / 4); s += kThreads) {
             const int r0 = (s / (W / 4)) * 4, c0 = (s % (W / 4)) * 4;
@@ -211,7 +261,7 @@ prep_kernel(FwdParams p) {
                 float t[4], x[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
-                    t[a] = sT[(r0 + a) * kLC + i];     // zero above the diagonal
+                    t[a] = sT[(r0 + a) * LDA + i];
                     x[a] = X[i * ldx + c0 + a];
                 }
 #pragma unroll
@@ -270,6 +320,8 @@ struct ChainLayout {
     static constexpr int oS = NB * buf, oE = oS + K * LU, total = oE + C * LU;
     static constexpr size_t bytes = sizeof(float) * total;
     static_assert(bytes <= 232448, "chain shared memory");
+    static_assert(LW % 4 == 0 && LL % 4 == 0 && LU % 4 == 0 && buf % 4 == 0 && VS % 4 == 0,
+                  "16-byte aligned rows and copies");
 };
 
 template <typename Tin, int K, int V, int VS, int C>
@@ -319,7 +371,8 @@ chain_kernel(FwdParams p) {
         const int64_t gi = state_base + (int64_t)c * V + v0 + jj;
         sS[c * LU + jj] = (p.h0 && GCL_IN_BOUNDS(gi, n_state, p.dev_status)) ? p.h0[gi] : 0.f;
     }
-    // the record of chunk ic into buffer b: 16-byte copies, padded rows
+    // the record of chunk ic into buffer b: 16-byte copies, padded rows (many small bulk
+    // copies, one per row, measured slower: the copy engine takes them one at a time)
     auto issue = [&](int ic, int b) {
         const int64_t r0 = ((row0 + ic) * H + h) * (int64_t)R::floats;
         if (!GCL_RANGE_IN_BOUNDS(r0, r0 + R::floats - 1, n_rec, p.dev_status)) return;
@@ -460,10 +513,14 @@ chain_kernel(FwdParams p) {
     }
 }
 
-// Value-column slice of the chain: 16 at K = 64, 32 at K = 128.
-template <int K>
+// Value-column slice of the chain: 16 at K = 64, 32 at K = 128; half of that (where the tiles
+// allow: VS >= 512 / C for the output tiles) when the grid of (slot, head, slice) CTAs would
+// fill less than the GPU's SMs -- the serial chain then takes half the work per chunk on
+// twice the CTAs (HA-NPU section 4: column-wise split of the residual heads).
+template <int K, int C>
 struct ChainSlice {
     static constexpr int VS = K == 64 ? 16 : 32;
+    static constexpr int VS_small = VS / 2 >= 512 / C ? VS / 2 : VS;
 };
 
 template <int K, int V, int C>
@@ -471,20 +528,27 @@ size_t record_bytes(int64_t nt_max, int H) {
     return sizeof(float) * (size_t)nt_max * H * Rec<K, V, C>::floats;
 }
 
+template <typename Tin, int K, int V, int VS, int C>
+cudaError_t launch_chain(const FwdParams &p, cudaStream_t s) {
+    using CL = ChainLayout<K, VS, C>;
+    auto chain = chain_kernel<Tin, K, V, VS, C>;
+    const cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CL::bytes);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(chain, dim3(V / VS, p.H, p.n_max), dim3(kThreads), CL::bytes, s, p);
+}
+
 template <int VAR, typename Tin, int K, int V, int C>
 cudaError_t launch(const FwdParams &p, cudaStream_t s) {
     using PL = PrepLayout<K, V, VAR, C>;
-    constexpr int VS = ChainSlice<K>::VS;
-    using CL = ChainLayout<K, VS, C>;
+    using CS = ChainSlice<K, C>;
     auto prep = prep_kernel<VAR, Tin, K, V, C>;
-    auto chain = chain_kernel<Tin, K, V, VS, C>;
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::bytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CL::bytes);
     if (e != cudaSuccess) return e;
     e = launch_dependent(prep, dim3((unsigned)p.nt_max, p.H), dim3(kThreads), PL::bytes, s, p);
     if (e != cudaSuccess) return e;
-    return launch_dependent(chain, dim3(V / VS, p.H, p.n_max), dim3(kThreads), CL::bytes, s, p);
+    if (CS::VS_small != CS::VS && (int64_t)p.n_max * p.H * (V / CS::VS) < num_sms())
+        return launch_chain<Tin, K, V, CS::VS_small, C>(p, s);
+    return launch_chain<Tin, K, V, CS::VS, C>(p, s);
 }
 
 }  // namespace simt_split

@@ -72,8 +72,8 @@ __device__ __forceinline__ float gam(const float *sG, int r, int c) {
 // also receives A' (without beta).  FastExp takes the per-channel decays of KDA with the
 // hardware exponential (__expf: about 2^-21 relative error for the arguments that matter,
 // |gamma_r - gamma_i| of a few units, far inside the fp32 bar; the gradients take it, the
-// forward keeps expf).
-template <int VAR, int K, int NT, int C, bool FastExp = false>
+// forward keeps expf).  LDA: the row stride of sA (the others take C + 1).
+template <int VAR, int K, int NT, int C, bool FastExp = false, int LDA = C + 1>
 __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, const float *sG,
                                            const float *sB, float scale, float *sA, float *sL,
                                            float *sAp) {
@@ -113,7 +113,7 @@ __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, con
                     const float d = expf(on ? sG[r] - sG[i] : 0.f);
                     const float ap = (i < r) ? kk[a][b] * d : 0.f;
                     const float l = on ? scale * (qk[a][b] * d) : 0.f;
-                    if (sA) sA[r * kLC + i] = sB[r] * ap;
+                    if (sA) sA[r * LDA + i] = sB[r] * ap;
                     if (sAp) sAp[r * kLC + i] = ap;
                     if (sL) sL[r * kLC + i] = l;
                 }
@@ -144,7 +144,7 @@ __device__ __forceinline__ void simt_intra(const float *sQ, const float *sK, con
             ap = (i < r) ? kk : 0.f;
             l = scale * qk;
         }
-        if (sA) sA[r * kLC + i] = sB[r] * ap;
+        if (sA) sA[r * LDA + i] = sB[r] * ap;
         if (sAp) sAp[r * kLC + i] = ap;
         if (sL) sL[r * kLC + i] = l;
     }

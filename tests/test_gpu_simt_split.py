@@ -1,6 +1,7 @@
 """The CUDA-core forward's two plans against the fp64 oracle: the split plan (chunk prep over
-every chunk at once, then the chain over value-column slices; taken when the workspace holds
-its records) and the single kernel (no workspace).  fp32 inputs at the 1e-5 bar, GDN and KDA,
+every chunk at once, then the chain over value-column slices, half-width slices when the grid
+would not fill the GPU; taken when the workspace holds its records) and the single kernel (no
+workspace).  fp32 inputs at the 1e-5 bar, GDN and KDA,
 d = 64 and 128, chunk 32 and 64, ragged and empty sequences, saved chunk states, and the
 small fp32 configuration (one 256-token sequence, 2 heads, d = 64, h0 = 0)."""
 import numpy as np
@@ -64,6 +65,23 @@ def test_split_plan_fp32(variant, d, bt):
     # the two plans round differently, both far inside the bar of each other
     assert relF(a["o"][:T].cpu().numpy(), b["o"][:T].cpu().numpy()) <= 1e-5
     assert relF(a["ht"].cpu().numpy(), b["ht"].cpu().numpy()) <= 1e-5
+
+
+@pytest.mark.parametrize("d", [64, 128], ids=["d64", "d128"])
+@pytest.mark.parametrize("bt", [64, 32], ids=["bt64", "bt32"])
+def test_split_plan_full_width_slices(d, bt):
+    """Enough (slot, head) units that the chain's CTAs fill the SMs at the full slice width
+    (16 value columns at d = 64, 32 at d = 128); the smaller grids above take half-width
+    slices.  fp32 GDN at the 1e-5 bar, ragged and empty sequences."""
+    lens = [1, 63, 0, 64, 65, 200, 130, 0, 97, 31, 128, 5]
+    w = synth.varlen("simt-split-wide", synth.GDN, "f32", lens, len(lens), sum(lens) + 40, 4, d, d,
+                     seed=74, bt=bt)
+    assert len(lens) * 4 * 4 >= 152      # n_max x H x (V / slice) at the full slice width
+    x = synth.make_inputs(w)
+    dv = to_device(w, x)
+    a = _run(w, dv, split=True)
+    check_fwd(w, x, a, label=f"split wide d{d} bt{bt}")
+    _check_states(w, x, a)
 
 
 def test_split_plan_run_to_run_and_reduced_precision_inputs():
