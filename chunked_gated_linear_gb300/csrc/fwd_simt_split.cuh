@@ -17,6 +17,7 @@
 #pragma once
 
 #include "simt_map.cuh"
+#include "tc_ptx.cuh"
 #include "tc_solve.cuh"
 
 namespace gcl {
@@ -24,14 +25,18 @@ namespace simt_split {
 
 constexpr int kThreads = 256;
 
-// One record per (chunk row, head), fp32, row-major without padding:
-//   W [C][K] | Q' [C][K] | K' [C][K] | L [C][C] | U [C][V] | Gamma_c [K]
+// One record per (chunk row, head), fp32, rows padded to the chain's shared-memory strides
+// (K + 4 and C + 4 floats; the pads are never read):
+//   W [C][K+4] | Q' [C][K+4] | K' [C][K+4] | L [C][C+4] | Gamma_c [K] | U [C][V]
+// so that everything before U reaches a chain buffer as one bulk copy of `head` floats (U is
+// read by value slices, row by row).
 template <int K, int V, int C>
 struct Rec {
-    static constexpr int oW = 0, oQ = C * K, oKt = 2 * C * K, oL = 3 * C * K;
-    static constexpr int oU = oL + C * C, oGC = oU + C * V;
-    static constexpr int floats = oGC + K;
-    static_assert(floats % 4 == 0, "records keep 16-byte alignment");
+    static constexpr int LW = K + 4, LL = C + 4;
+    static constexpr int oW = 0, oQ = C * LW, oKt = 2 * C * LW, oL = 3 * C * LW;
+    static constexpr int oGC = oL + C * LL, oU = oGC + K, head = oU;
+    static constexpr int floats = oU + C * V;
+    static_assert(floats % 4 == 0 && head % 4 == 0, "records keep 16-byte alignment");
 };
 
 // ------------------------------------------------------------------------------- prep
@@ -90,9 +95,14 @@ struct PrepLayout {
     static constexpr int oQ = 0, oK = oQ + C * LK, oV = oK + C * LK;
     static constexpr int oA = oV + C * LV, oT = oA + C * LDA, oL = oT + C * LDA;
     static constexpr int oB = oL + C * kLC, oE1 = oB + C, oE2 = oE1 + C, oG = oE2 + C;
-    static constexpr int total = oG + (VAR == kKDA ? C * LK : C);
+    // GDN, 64-row chunks: Q^T and K^T [K][C + 4] for the intra-chunk products (float4 loads
+    // along rows; at 32 rows the copies would cost a CTA per SM and the plain loads are few)
+    static constexpr bool kTransposed = VAR == kGDN && C == 64;
+    static constexpr int LT = C + 4, oQT = oG + (VAR == kKDA ? C * LK : C);
+    static constexpr int oKT = oQT + (kTransposed ? K * LT : 0);
+    static constexpr int total = oKT + (kTransposed ? K * LT : 0);
     static constexpr size_t bytes = sizeof(float) * total;
-    static_assert(oA % 4 == 0 && oT % 4 == 0, "float4 rows of A and T");
+    static_assert(oA % 4 == 0 && oT % 4 == 0 && oQT % 4 == 0 && oKT % 4 == 0, "float4 rows");
     static_assert(bytes <= 232448, "one CTA per SM at most");
 };
 
@@ -120,6 +130,47 @@ __device__ __forceinline__ void solve_lower32_warp(const float *sA, float *sT) {
     for (int r = 0; r < 32; ++r) sT[r * LD + j] = x[r];
 }
 
+// GDN's A (strictly lower, times beta_r; row stride LDA) and L (inclusive, times scale; row
+// stride C + 1) from transposed copies Q^T, K^T [K][LT]: one 4 x 4 tile of (r, i) pairs per
+// thread, whose four rows and four columns come as one float4 each per key channel (the
+// same sums as simt_intra in the same order; tiles above the diagonal are skipped).
+template <int K, int C, int LDA, int LT>
+__device__ __forceinline__ void simt_intra_t(const float *sQT, const float *sKT, const float *sG,
+                                             const float *sB, float scale, float *sA, float *sL) {
+    constexpr int NTILE = C / 4, kLC = C + 1;
+    const int t = threadIdx.x;
+    if (t >= NTILE * NTILE) return;
+    const int r0 = (t / NTILE) * 4, i0 = (t % NTILE) * 4;
+    float kk[4][4] = {}, qk[4][4] = {};
+    if (i0 <= r0 + 3) {
+#pragma unroll 4
+        for (int c = 0; c < K; ++c) {
+            const float4 kr4 = *reinterpret_cast<const float4 *>(sKT + c * LT + r0);
+            const float4 qr4 = *reinterpret_cast<const float4 *>(sQT + c * LT + r0);
+            const float4 ki4 = *reinterpret_cast<const float4 *>(sKT + c * LT + i0);
+            const float kr[4] = {kr4.x, kr4.y, kr4.z, kr4.w}, qr[4] = {qr4.x, qr4.y, qr4.z, qr4.w};
+            const float ki[4] = {ki4.x, ki4.y, ki4.z, ki4.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    kk[a][b] = fmaf(kr[a], ki[b], kk[a][b]);
+                    qk[a][b] = fmaf(qr[a], ki[b], qk[a][b]);
+                }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int r = r0 + a, i = i0 + b;
+            const bool on = i <= r;
+            const float d = expf(on ? sG[r] - sG[i] : 0.f);
+            sA[r * LDA + i] = sB[r] * ((i < r) ? kk[a][b] * d : 0.f);
+            sL[r * kLC + i] = on ? scale * (qk[a][b] * d) : 0.f;
+        }
+}
+
 // Warps 0..3 solve for T while warps 4..7 write the records that do not need it (Q', K', L,
 // Gamma_c) and form the operands of W and U in place (HA-NPU section 5: the inversion runs
 // beside the other vector work); then all eight form W and U.
@@ -134,6 +185,8 @@ prep_kernel(FwdParams p) {
     float *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sV = sm + Lay::oV;
     float *sA = sm + Lay::oA, *sT = sm + Lay::oT, *sL = sm + Lay::oL;
     float *sB = sm + Lay::oB, *sG = sm + Lay::oG, *sE1 = sm + Lay::oE1, *sE2 = sm + Lay::oE2;
+    float *sQT = sm + Lay::oQT, *sKT = sm + Lay::oKT;
+    constexpr int LW = R::LW, LL = R::LL, LT = Lay::LT;
 
     // launched as a dependent of the metadata kernel: nothing it wrote is read before this
     grid_dependency_wait();
@@ -191,6 +244,13 @@ prep_kernel(FwdParams p) {
         tv.store(sV, LV);
     }
     __syncthreads();
+    if constexpr (Lay::kTransposed) {   // Q^T, K^T (reads down a column, writes along a row)
+        for (int e = tid; e < C * K; e += kThreads) {
+            const int r = e % C, c = e / C;
+            sQT[c * LT + r] = sQ[r * LK + c];
+            sKT[c * LT + r] = sK[r * LK + c];
+        }
+    }
     if constexpr (VAR == kGDN) {   // inclusive cumsum of g over the rows: warp scans + carry
         __shared__ float s_carry;
         float x = tid < C ? sG[tid] : 0.f;
@@ -211,7 +271,10 @@ prep_kernel(FwdParams p) {
         sE1[tid] = expf(sG[tid]);
         sE2[tid] = expf(sG[C - 1] - sG[tid]);
     }
-    simt_intra<VAR, K, kThreads, C, false, LDA>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
+    if constexpr (Lay::kTransposed)
+        simt_intra_t<K, C, LDA, LT>(sQT, sKT, sG, sB, p.scale, sA, sL);
+    else
+        simt_intra<VAR, K, kThreads, C, false, LDA>(sQ, sK, sG, sB, p.scale, sA, sL, nullptr);
     __syncthreads();
     if (tid < 128) {
         // ---- T = (I + A)^-1 on warps 0..3 (named barrier 1 inside the 64-row solve)
@@ -237,15 +300,18 @@ prep_kernel(FwdParams p) {
                 e2 = expf(gam<VAR, K>(sG, C - 1, c) - gr);
             }
             const float kv = sK[r * LK + c];
-            if (GCL_RANGE_IN_BOUNDS(rec0 + R::oQ + e, rec0 + R::oKt + e, n_rec, p.dev_status)) {
-                rec[R::oQ + e] = p.scale * e1 * sQ[r * LK + c];
-                rec[R::oKt + e] = e2 * kv;
+            const int o = r * LW + c;
+            if (GCL_RANGE_IN_BOUNDS(rec0 + R::oQ + o, rec0 + R::oKt + o, n_rec, p.dev_status)) {
+                rec[R::oQ + o] = p.scale * e1 * sQ[r * LK + c];
+                rec[R::oKt + o] = e2 * kv;
             }
             sQ[r * LK + c] = sB[r] * e1 * kv;
         }
         for (int e = t; e < C * V; e += kThreads - 128) sV[(e / V) * LV + e % V] *= sB[e / V];
-        for (int e = t; e < C * C; e += kThreads - 128)
-            if (GCL_IN_BOUNDS(rec0 + R::oL + e, n_rec, p.dev_status)) rec[R::oL + e] = sL[(e / C) * kLC + e % C];
+        for (int e = t; e < C * C; e += kThreads - 128) {
+            const int o = (e / C) * LL + e % C;
+            if (GCL_IN_BOUNDS(rec0 + R::oL + o, n_rec, p.dev_status)) rec[R::oL + o] = sL[(e / C) * kLC + e % C];
+        }
         for (int c = t; c < K; c += kThreads - 128)
             if (GCL_IN_BOUNDS(rec0 + R::oGC + c, n_rec, p.dev_status)) rec[R::oGC + c] = expf(gam<VAR, K>(sG, C - 1, c));
     }
@@ -253,7 +319,7 @@ prep_kernel(FwdParams p) {
     // ---- W = T (beta Gamma K) and U = T (beta V): 4 x 4 register tiles, i up to the tile's
     // last row (T is zero above the diagonal inside its 32-row diagonal blocks, and i stays in
     // the tile's own block)
-    auto tile_product = [&](const float *X, int ldx, int W, int oRec) {
+    auto tile_product = [&](const float *X, int ldx, int W, int ldo, int oRec) {
         for (int s = tid; s < (C / 4) * (W / 4); s += kThreads) {
             const int r0 = (s / (W / 4)) * 4, c0 = (s % (W / 4)) * 4;
             float acc[4][4] = {};
@@ -271,15 +337,15 @@ prep_kernel(FwdParams p) {
             }
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
-                const int64_t o = rec0 + oRec + (int64_t)(r0 + a) * W + c0;
+                const int64_t o = rec0 + oRec + (int64_t)(r0 + a) * ldo + c0;
                 if (GCL_RANGE_IN_BOUNDS(o, o + 3, n_rec, p.dev_status))
-                    *reinterpret_cast<float4 *>(rec + oRec + (r0 + a) * W + c0) =
+                    *reinterpret_cast<float4 *>(rec + oRec + (r0 + a) * ldo + c0) =
                         make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
             }
         }
     };
-    tile_product(sQ, LK, K, R::oW);
-    tile_product(sV, LV, V, R::oU);
+    tile_product(sQ, LK, K, LW, R::oW);
+    tile_product(sV, LV, V, V, R::oU);
 }
 
 // ------------------------------------------------------------------------------ chain
@@ -307,27 +373,37 @@ __device__ __forceinline__ void lds_vec(const float *p, float (&v)[N]) {
 }
 
 // Shared memory of the chain: NB record buffers (two when they fit: the next chunk's record
-// arrives while the current one is used), the state slice S [K][VS] and E [C][VS].  Row
-// strides are the widths + 4 floats: 16-byte aligned rows, consecutive rows 4 banks apart.
-template <int K, int VS, int C>
+// arrives while the current one is used), the state slice S [K][VS] and E [C][VS].  A buffer
+// holds the record's head (W, Q', K', L, Gamma_c in the record's own padded layout: row
+// strides K + 4 and C + 4, consecutive rows 4 banks apart), which a few bulk copies bring in,
+// then this slice's columns of U [C][VS + 4], copied row by row in 16-byte pieces.
+template <int K, int V, int VS, int C>
 struct ChainLayout {
-    static constexpr int LW = K + 4, LL = C + 4, LU = VS + 4;
-    static constexpr int oW = 0, oQ = C * LW, oKt = 2 * C * LW, oL = 3 * C * LW, oU = oL + C * LL;
-    static constexpr int oGC = oU + C * LU, buf = oGC + K;
-    static constexpr int kMaxFloats = 232448 / 4;
+    using R = Rec<K, V, C>;
+    static constexpr int LW = R::LW, LL = R::LL, LU = VS + 4;
+    static constexpr int oW = R::oW, oQ = R::oQ, oKt = R::oKt, oL = R::oL, oGC = R::oGC;
+    static constexpr int oU = R::head, buf = oU + C * LU;
+    static constexpr int kMaxFloats = 232448 / 4 - 64;           // (the static shared memory)
     static constexpr int fixed = K * LU + C * LU;
     static constexpr int NB = 2 * buf + fixed <= kMaxFloats ? 2 : 1;
     static constexpr int oS = NB * buf, oE = oS + K * LU, total = oE + C * LU;
     static constexpr size_t bytes = sizeof(float) * total;
-    static_assert(bytes <= 232448, "chain shared memory");
-    static_assert(LW % 4 == 0 && LL % 4 == 0 && LU % 4 == 0 && buf % 4 == 0 && VS % 4 == 0,
-                  "16-byte aligned rows and copies");
+    static constexpr uint32_t head_bytes = sizeof(float) * R::head;
+    // the head is copied in up to kMaxPieces bulk copies (16-byte multiples; the last takes
+    // the rest)
+    static constexpr int kMaxPieces = 8;
+    static_assert(bytes <= 232448 - 256, "chain shared memory");
+    static_assert(LU % 4 == 0 && buf % 4 == 0 && VS % 4 == 0 && head_bytes < (1u << 20),
+                  "16-byte aligned rows and copies; one bulk copy's byte count");
 };
 
+// pieces: bulk copies per record head, 1 .. kMaxPieces.  With few CTAs each SM's fetch of the
+// next record is what paces the chain, and several copies in flight shorten it (8 measured
+// best on 16 CTAs); with the GPU filled one copy per CTA measured faster.
 template <typename Tin, int K, int V, int VS, int C>
 __global__ void __launch_bounds__(kThreads)
-chain_kernel(FwdParams p) {
-    using Lay = ChainLayout<K, VS, C>;
+chain_kernel(FwdParams p, int pieces) {
+    using Lay = ChainLayout<K, V, VS, C>;
     using R = Rec<K, V, C>;
     constexpr int LW = Lay::LW, LL = Lay::LL, LU = Lay::LU;
     // phase 1 / O tiles: 2 rows x TJ columns; state tiles: TC keys x TS columns
@@ -371,29 +447,45 @@ chain_kernel(FwdParams p) {
         const int64_t gi = state_base + (int64_t)c * V + v0 + jj;
         sS[c * LU + jj] = (p.h0 && GCL_IN_BOUNDS(gi, n_state, p.dev_status)) ? p.h0[gi] : 0.f;
     }
-    // the record of chunk ic into buffer b: 16-byte copies, padded rows (many small bulk
-    // copies, one per row, measured slower: the copy engine takes them one at a time)
+    const int np = pieces < 1 ? 1 : pieces > Lay::kMaxPieces ? Lay::kMaxPieces : pieces;
+    const uint32_t piece_bytes = Lay::head_bytes / np / 16 * 16;
+    __shared__ uint64_t bar_rec[2];
+    __shared__ int s_err;
+    if (tid == 0) {
+        tc::mbar_init(&bar_rec[0], 1);
+        tc::mbar_init(&bar_rec[1], 1);
+        s_err = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    // the record of chunk ic into buffer b: its head in np bulk copies (lanes of warp 0,
+    // counted on the buffer's mbarrier), this slice's U columns in 16-byte cp.async pieces
     auto issue = [&](int ic, int b) {
         const int64_t r0 = ((row0 + ic) * H + h) * (int64_t)R::floats;
         if (!GCL_RANGE_IN_BOUNDS(r0, r0 + R::floats - 1, n_rec, p.dev_status)) return;
         const float *src = recs + r0;
         float *dst = sm + b * Lay::buf;
-        for (int e = tid; e < 3 * C * K / 4; e += kThreads) {       // W, Q', K'
-            const int m = e / (C * K / 4), w = e % (C * K / 4), r = w / (K / 4), c4 = w % (K / 4);
-            cp_async16(dst + m * C * LW + r * LW + 4 * c4, src + m * C * K + 4 * w);
+        if (tid < 32) {
+            if (tid == 0) {
+                tc::fence_async_smem();  // the buffer's last readers are done (block barrier)
+                tc::mbar_arrive_expect_tx(&bar_rec[b], Lay::head_bytes);
+            }
+            __syncwarp();
+            if (tid < np) {              // pieces in flight together
+                const uint32_t off = tid * piece_bytes;
+                const uint32_t nb = tid + 1 < np ? piece_bytes : Lay::head_bytes - off;
+                tc::bulk_load(reinterpret_cast<uint8_t *>(dst) + off,
+                              reinterpret_cast<const uint8_t *>(src) + off, nb, &bar_rec[b]);
+            }
         }
-        for (int e = tid; e < C * C / 4; e += kThreads) {           // L
-            const int r = e / (C / 4), c4 = e % (C / 4);
-            cp_async16(dst + Lay::oL + r * LL + 4 * c4, src + R::oL + 4 * e);
-        }
-        for (int e = tid; e < C * VS / 4; e += kThreads) {          // U, this slice's columns
+        for (int e = tid; e < C * VS / 4; e += kThreads) {
             const int r = e / (VS / 4), c4 = e % (VS / 4);
             cp_async16(dst + Lay::oU + r * LU + 4 * c4, src + R::oU + r * V + v0 + 4 * c4);
         }
-        for (int e = tid; e < K / 4; e += kThreads) cp_async16(dst + Lay::oGC + 4 * e, src + R::oGC + 4 * e);
         cp_async_commit();
     };
     if (nch > 0) issue(0, 0);
+    int issued = nch > 0 ? 1 : 0;        // heads issued so far (one per chunk, in order)
 
     const int rp = tid / CG, r0 = 2 * rp, j0 = (tid % CG) * TJ;      // output tile
     const int c0 = (tid / 8) * TC, s0 = (tid % 8) * TS;              // state tile
@@ -403,9 +495,15 @@ chain_kernel(FwdParams p) {
         const float *sL = sW + Lay::oL, *sU = sW + Lay::oU, *sGC = sW + Lay::oGC;
         const int64_t t0 = bos + (int64_t)ic * C;
         const int len = (int)(eos - t0 < C ? eos - t0 : C);
+        // chunk ic's record: the k = ic / NB-th use of buffer b, parity k & 1 (a wait that
+        // gives up records GCL_DEV_WAIT_TIMEOUT; later waits return at once and the loop runs out)
         cp_async_wait_all();
+        tc::mbar_wait(&bar_rec[b], (uint32_t)(ic / Lay::NB) & 1u, &s_err, 1);
         __syncthreads();              // chunk ic's record and the state are in place
-        if (Lay::NB == 2 && ic + 1 < nch) issue(ic + 1, b ^ 1);
+        if (Lay::NB == 2 && ic + 1 < nch) {
+            issue(ic + 1, b ^ 1);
+            ++issued;
+        }
         if (p.h_save) {               // the state entering the chunk
             const int64_t hb = ((row0 + ic) * H + h) * KV;
             for (int e = tid; e < K * VS; e += kThreads) {
@@ -501,7 +599,18 @@ chain_kernel(FwdParams p) {
         if (Lay::NB == 1 && ic + 1 < nch) {
             __syncthreads();          // every read of the single record buffer is done
             issue(ic + 1, 0);
+            ++issued;
         }
+    }
+    // every issued head has landed before the CTA exits (after a wait that gave up, the last
+    // ones get one more bounded wait each, whose failure is already recorded)
+    __syncthreads();
+    if (s_err != 0 && tid == 0) {
+        for (int k = (issued > Lay::NB ? issued - Lay::NB : 0); k < issued; ++k) {
+            int err2 = 0;
+            tc::mbar_wait(&bar_rec[k % Lay::NB], (uint32_t)(k / Lay::NB) & 1u, &err2, 1);
+        }
+        status_set(p.dev_status, GCL_DEV_WAIT_TIMEOUT);
     }
     __syncthreads();
     if (p.ht) {
@@ -530,11 +639,13 @@ size_t record_bytes(int64_t nt_max, int H) {
 
 template <typename Tin, int K, int V, int VS, int C>
 cudaError_t launch_chain(const FwdParams &p, cudaStream_t s) {
-    using CL = ChainLayout<K, VS, C>;
+    using CL = ChainLayout<K, V, VS, C>;
     auto chain = chain_kernel<Tin, K, V, VS, C>;
     const cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CL::bytes);
     if (e != cudaSuccess) return e;
-    return launch_dependent(chain, dim3(V / VS, p.H, p.n_max), dim3(kThreads), CL::bytes, s, p);
+    const int64_t ctas = (int64_t)(V / VS) * p.H * p.n_max;
+    const int pieces = ctas < num_sms() / 2 ? CL::kMaxPieces : 1;
+    return launch_dependent(chain, dim3(V / VS, p.H, p.n_max), dim3(kThreads), CL::bytes, s, p, pieces);
 }
 
 template <int VAR, typename Tin, int K, int V, int C>

@@ -176,9 +176,10 @@ typedef struct gcl_fwd_args {
  * Sizes the CUDA cores serve (fp32 inputs, K or V = 64, bt = 32, and the KDA forward
  * with fp16 inputs) have two plans: one fp32 kernel, which needs no workspace (the
  * minimum, 0), and the split plan, fastest, whose records are per chunk row and head the
- * fp32 matrices W, Q', K' [BT x K], L [BT x BT], U [BT x V] and Gamma_c [K] (80 KiB at
- * K = V = 64, BT = 64; 144 KiB at K = V = 128), for K = V only; it runs whenever the
- * workspace holds them and chunk_indices and chunk_offsets are given.
+ * fp32 matrices W, Q', K' [BT x K], L [BT x BT] (rows padded by 4 floats), Gamma_c [K]
+ * and U [BT x V] (84.25 KiB at K = V = 64, BT = 64; 148.5 KiB at K = V = 128), for K = V
+ * only; it runs whenever the workspace holds them and chunk_indices and chunk_offsets are
+ * given.
  *
  * The tensor-core path has two plans.  The W form keeps per chunk and head the
  * inverted intra-chunk matrix T and the masked decayed QK^T, 25 KiB (bf16); it is

@@ -124,8 +124,9 @@ def test_plan_rules_from_sizes_alone(lib):
 
 def test_cuda_core_plans_from_sizes_alone(lib):
     """The CUDA-core sizes: no workspace at the minimum (one kernel); the fastest workspace holds
-    the split plan's records, (3 BT K + BT^2 + BT V + K) fp32 per chunk row and head, for
-    K = V only; the split plan runs only with that workspace and the chunk metadata."""
+    the split plan's records, (3 BT (K + 4) + BT (BT + 4) + K + BT V) fp32 per chunk row and
+    head (rows of W, Q', K', L padded by 4 floats), for K = V only; the split plan runs only
+    with that workspace and the chunk metadata."""
     import chunked_gated_linear_gb300 as gcl
     fake = 1 << 20
     nt = lambda t, n, bt: lib.gcl_nt_max(t, n, bt)
@@ -134,7 +135,7 @@ def test_cuda_core_plans_from_sizes_alone(lib):
                     t_max=4096, n_max=3, H=2, K=K, V=K, bt=bt, scale=1.0, dtype=dtype,
                     chunk_indices=fake, chunk_offsets=fake)
         a = gcl.FwdArgs(**base)
-        rec = 4 * nt(4096, 3, bt) * 2 * (3 * bt * K + bt * bt + bt * K + K)
+        rec = 4 * nt(4096, 3, bt) * 2 * (3 * bt * (K + 4) + bt * (bt + 4) + K + bt * K)
         fastest = lib.gcl_fwd_workspace_bytes(ctypes.byref(a))
         assert lib.gcl_fwd_workspace_min_bytes(ctypes.byref(a)) == 0
         assert rec <= fastest <= rec + 1024, (K, bt, dtype)           # + alignment slack
