@@ -375,7 +375,7 @@ __device__ __forceinline__ void lds_vec(const float *p, float (&v)[N]) {
 // Shared memory of the chain: NB record buffers (two when they fit: the next chunk's record
 // arrives while the current one is used), the state slice S [K][VS] and E [C][VS].  A buffer
 // holds the record's head (W, Q', K', L, Gamma_c in the record's own padded layout: row
-// strides K + 4 and C + 4, consecutive rows 4 banks apart), which a few bulk copies bring in,
+// strides K + 4 and C + 4, consecutive rows 4 banks apart), which one bulk copy brings in,
 // then this slice's columns of U [C][VS + 4], copied row by row in 16-byte pieces.
 template <int K, int V, int VS, int C>
 struct ChainLayout {
@@ -389,20 +389,14 @@ struct ChainLayout {
     static constexpr int oS = NB * buf, oE = oS + K * LU, total = oE + C * LU;
     static constexpr size_t bytes = sizeof(float) * total;
     static constexpr uint32_t head_bytes = sizeof(float) * R::head;
-    // the head is copied in up to kMaxPieces bulk copies (16-byte multiples; the last takes
-    // the rest)
-    static constexpr int kMaxPieces = 8;
     static_assert(bytes <= 232448 - 256, "chain shared memory");
     static_assert(LU % 4 == 0 && buf % 4 == 0 && VS % 4 == 0 && head_bytes < (1u << 20),
                   "16-byte aligned rows and copies; one bulk copy's byte count");
 };
 
-// pieces: bulk copies per record head, 1 .. kMaxPieces.  With few CTAs each SM's fetch of the
-// next record is what paces the chain, and several copies in flight shorten it (8 measured
-// best on 16 CTAs); with the GPU filled one copy per CTA measured faster.
 template <typename Tin, int K, int V, int VS, int C>
 __global__ void __launch_bounds__(kThreads)
-chain_kernel(FwdParams p, int pieces) {
+chain_kernel(FwdParams p) {
     using Lay = ChainLayout<K, V, VS, C>;
     using R = Rec<K, V, C>;
     constexpr int LW = Lay::LW, LL = Lay::LL, LU = Lay::LU;
@@ -447,8 +441,6 @@ chain_kernel(FwdParams p, int pieces) {
         const int64_t gi = state_base + (int64_t)c * V + v0 + jj;
         sS[c * LU + jj] = (p.h0 && GCL_IN_BOUNDS(gi, n_state, p.dev_status)) ? p.h0[gi] : 0.f;
     }
-    const int np = pieces < 1 ? 1 : pieces > Lay::kMaxPieces ? Lay::kMaxPieces : pieces;
-    const uint32_t piece_bytes = Lay::head_bytes / np / 16 * 16;
     __shared__ uint64_t bar_rec[2];
     __shared__ int s_err;
     if (tid == 0) {
@@ -458,25 +450,17 @@ chain_kernel(FwdParams p, int pieces) {
         tc::fence_barrier_init();
     }
     __syncthreads();
-    // the record of chunk ic into buffer b: its head in np bulk copies (lanes of warp 0,
-    // counted on the buffer's mbarrier), this slice's U columns in 16-byte cp.async pieces
+    // the record of chunk ic into buffer b: its head in one bulk copy (thread 0, counted on
+    // the buffer's mbarrier), this slice's U columns in 16-byte cp.async pieces
     auto issue = [&](int ic, int b) {
         const int64_t r0 = ((row0 + ic) * H + h) * (int64_t)R::floats;
         if (!GCL_RANGE_IN_BOUNDS(r0, r0 + R::floats - 1, n_rec, p.dev_status)) return;
         const float *src = recs + r0;
         float *dst = sm + b * Lay::buf;
-        if (tid < 32) {
-            if (tid == 0) {
-                tc::fence_async_smem();  // the buffer's last readers are done (block barrier)
-                tc::mbar_arrive_expect_tx(&bar_rec[b], Lay::head_bytes);
-            }
-            __syncwarp();
-            if (tid < np) {              // pieces in flight together
-                const uint32_t off = tid * piece_bytes;
-                const uint32_t nb = tid + 1 < np ? piece_bytes : Lay::head_bytes - off;
-                tc::bulk_load(reinterpret_cast<uint8_t *>(dst) + off,
-                              reinterpret_cast<const uint8_t *>(src) + off, nb, &bar_rec[b]);
-            }
+        if (tid == 0) {
+            tc::fence_async_smem();      // the buffer's last readers are done (block barrier)
+            tc::mbar_arrive_expect_tx(&bar_rec[b], Lay::head_bytes);
+            tc::bulk_load(dst, src, Lay::head_bytes, &bar_rec[b]);
         }
         for (int e = tid; e < C * VS / 4; e += kThreads) {
             const int r = e / (VS / 4), c4 = e % (VS / 4);
@@ -643,9 +627,7 @@ cudaError_t launch_chain(const FwdParams &p, cudaStream_t s) {
     auto chain = chain_kernel<Tin, K, V, VS, C>;
     const cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CL::bytes);
     if (e != cudaSuccess) return e;
-    const int64_t ctas = (int64_t)(V / VS) * p.H * p.n_max;
-    const int pieces = ctas < num_sms() / 2 ? CL::kMaxPieces : 1;
-    return launch_dependent(chain, dim3(V / VS, p.H, p.n_max), dim3(kThreads), CL::bytes, s, p, pieces);
+    return launch_dependent(chain, dim3(V / VS, p.H, p.n_max), dim3(kThreads), CL::bytes, s, p);
 }
 
 template <int VAR, typename Tin, int K, int V, int C>
