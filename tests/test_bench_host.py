@@ -86,3 +86,18 @@ def test_roofline_takes_the_slower_roof(tmp_path, monkeypatch):
 def test_cpu_model_is_a_name():
     name = bench.cpu_model()
     assert isinstance(name, str) and name
+
+
+def test_committed_traffic_records_are_current():
+    """Every section of the committed ncu traffic summary was taken on the kernel sources now in
+    the tree (its hash matches), and the bench line's workloads -- the headline and the
+    per-configuration entries -- each have one; a kernel edited without a new capture fails
+    here instead of silently reporting traffic: null."""
+    import re
+    text = open(os.path.join(ROOT, "profiles", "traffic.txt")).read()
+    names = re.findall(r"^\[([^\]]+)\]$", text, flags=re.M)
+    assert names
+    stale = [n for n in names if bench.traffic_record(n) is None]
+    assert not stale, f"traffic records taken on other kernel sources: {stale}"
+    wanted = {synth.standard_workloads()[3].name, *bench.PER_CONFIG}
+    assert wanted <= set(names), wanted - set(names)
