@@ -285,6 +285,23 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float *sAf = reinterpret_cast<float *>(smem + Lay::oA);
     float *sTf = reinterpret_cast<float *>(smem + Lay::oTf);
     T *sO = reinterpret_cast<T *>(smem + Lay::oO);
+    // the valid rows of a chunk's O from the staging tile, 16 threads x 16 bytes per row; run
+    // during the next chunk's first MMA wait (the tile lives in the solve buffers, which that
+    // chunk's A / L epilogue rewrites only after the wait), or after the last chunk
+    auto store_o = [&](int64_t ot0, int olen) {
+        if (p.o == nullptr) return;
+        const int rsub = tid >> 4, cc = (tid & 15) * 8;
+        for (int r = rsub; r < olen; r += kThreads / 16) {
+            const int64_t oi = ((ot0 + r) * H + h) * (int64_t)VD + cc;
+            if (!GCL_RANGE_IN_BOUNDS(oi, oi + 7, p.t_max * H * VD, p.status) ||
+                !GCL_RANGE_IN_BOUNDS(r * kOLD + cc, r * kOLD + cc + 7, C * kOLD, p.status))
+                continue;
+            const uint4 val = *reinterpret_cast<const uint4 *>(sO + r * kOLD + cc);
+            *reinterpret_cast<uint4 *>(static_cast<T *>(p.o) + ((ot0 + r) * H + h) * (int64_t)VD + cc) = val;
+        }
+    };
+    int64_t prev_t0 = 0;
+    int prev_len = 0;                  // rows of the previous chunk's O still staged
 
     for (int ic = 0; ic < nch; ++ic) {
         const int len = chunk_len(ic);
@@ -327,6 +344,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             mma_commit(&bar_m2);
         }
+        store_o(prev_t0, prev_len);                         // the previous chunk's O
+        __syncthreads();                                    // read before the A / L epilogue
         mbar_wait(&bar_m1, ph, &s_err, 3);
         tc_fence_after();
         // ---- A (fp32, for the solve) and L (bf16) from D1, with the decay
@@ -561,20 +580,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncthreads();        // every read of D4 and O^T is done; O staged
         tc_fence_after();
         store_state_bf16();     // S^T bf16 for the next chunk's MMA2 (over D4's first columns)
-        if (p.o != nullptr) {   // valid rows of O, 16 threads x 16 bytes per row
-            const int rsub = tid >> 4, cc = (tid & 15) * 8;
-            for (int r = rsub; r < len; r += kThreads / 16) {
-                const int64_t oi = ((t0 + r) * H + h) * (int64_t)VD + cc;
-                if (!GCL_RANGE_IN_BOUNDS(oi, oi + 7, p.t_max * H * VD, p.status) ||
-                    !GCL_RANGE_IN_BOUNDS(r * kOLD + cc, r * kOLD + cc + 7, C * kOLD, p.status))
-                    continue;
-                const uint4 val = *reinterpret_cast<const uint4 *>(sO + r * kOLD + cc);
-                *reinterpret_cast<uint4 *>(static_cast<T *>(p.o) + ((t0 + r) * H + h) * (int64_t)VD + cc) = val;
-            }
-        }
+        prev_t0 = t0;
+        prev_len = len;
         // a wait that gave up (s_err) ends every thread's loop at the same chunk
         if (__syncthreads_or(*reinterpret_cast<volatile int *>(&s_err) != 0)) break;
     }
+    if (s_err == 0) store_o(prev_t0, prev_len);             // the last chunk's O
     if (s_err == 0 && p.ht && GCL_RANGE_IN_BOUNDS(st_lo, st_hi, n_state, p.status)) {
         float *dst = p.ht + state_base + (int64_t)k0 * VD + m;
 #pragma unroll
