@@ -442,7 +442,7 @@ chain_kernel(FwdParams p) {
         sS[c * LU + jj] = (p.h0 && GCL_IN_BOUNDS(gi, n_state, p.dev_status)) ? p.h0[gi] : 0.f;
     }
     __shared__ uint64_t bar_rec[2];
-    __shared__ int s_err;
+    __shared__ int s_err, s_err2;        // (s_err2: the error word of the final drain's waits)
     if (tid == 0) {
         tc::mbar_init(&bar_rec[0], 1);
         tc::mbar_init(&bar_rec[1], 1);
@@ -591,8 +591,8 @@ chain_kernel(FwdParams p) {
     __syncthreads();
     if (s_err != 0 && tid == 0) {
         for (int k = (issued > Lay::NB ? issued - Lay::NB : 0); k < issued; ++k) {
-            int err2 = 0;
-            tc::mbar_wait(&bar_rec[k % Lay::NB], (uint32_t)(k / Lay::NB) & 1u, &err2, 1);
+            s_err2 = 0;
+            tc::mbar_wait(&bar_rec[k % Lay::NB], (uint32_t)(k / Lay::NB) & 1u, &s_err2, 1);
         }
         status_set(p.dev_status, GCL_DEV_WAIT_TIMEOUT);
     }
