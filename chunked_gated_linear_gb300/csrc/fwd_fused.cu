@@ -79,7 +79,7 @@ static_assert(FusedLayout::bytes <= 110 * 1024, "two CTAs per SM");
 
 // TMEM columns (256 per CTA).  Phases of one chunk reuse them:
 //   S^T bf16 [0, 64) until MMA2 completes; then the fp32 state slice of warps 0..3 while they
-//   run the solve; then D4 (dS^T) [0, 128)
+//   run the solve (taken back while MMA3 runs); then D4 (dS^T) [0, 128)
 //   X = (K S)^T [64, 128) until R is formed, then E^T (MMA3) [64, 128)
 //   Y = (Q S)^T [128, 192): MMA2, scaled in place, then MMA5 accumulates onto it (O^T)
 //   D1 [192, 256) until the A / L epilogue; then R^T bf16 [192, 224), then E^T f bf16 [192, 224);
@@ -434,9 +434,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (GCL_RANGE_IN_BOUNDS(sw128_offset(C, r, cq + j), sw128_offset(C, r, cq + j) + 15, 8192, p.status))
                     *reinterpret_cast<uint4 *>(smem + Lay::oT + sw128_offset(C, r, cq + j)) = pk;
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + cS + q * 16, S + q * 16);
-            tmem_ld_wait();
+            // (the parked state slice comes back during MMA3, which does not touch its columns)
         } else {
             // ---- R^T[v][r] = beta_r (V[r][v] - Gamma_r X[v][r]) -> bf16 A operand in TMEM,
             // lane v = m, all 64 rows r, on warps 4..7
@@ -492,6 +490,11 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             smem_desc(sbase + Lay::oT + s * 32, 16, 1024, kSwizzle128B), id, s > 0);
             mma_commit(&bar_m3);
             if (ic + 1 < nch) issue_v(ic + 1);              // the V tile is no longer read
+        }
+        if (warp < 4) {                                     // the state slice parked for the solve
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + cS + q * 16, S + q * 16);
+            tmem_ld_wait();
         }
         mbar_wait(&bar_m3, ph, &s_err, 4);
         tc_fence_after();
