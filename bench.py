@@ -392,6 +392,12 @@ def input_sets(w, rank, dev, gcl, min_sets=2):
             return sets
 
 
+def per_set_means(times, n_sets):
+    """Mean of the times of the steps that ran each input set (step i ran set i mod n_sets);
+    None for a set that no step reached (fewer steps than sets)."""
+    return [float(np.mean(times[j::n_sets])) if j < len(times) else None for j in range(n_sets)]
+
+
 def measure(gcl, w, args, rank, world, dist, dev, steps, warmup, graphs=True):
     """Time one workload: direct launches (per-step and forward-kernel CUDA events, L2-cold by
     rotation), then, with graphs, the same steps captured once per input set and replayed in
@@ -437,9 +443,7 @@ def measure(gcl, w, args, rank, world, dist, dev, steps, warmup, graphs=True):
     out["direct"] = {"region_ms": e_s[0].elapsed_time(e_e[-1]), "p50_ms": pct(direct, 50),
                      "p95_ms": pct(direct, 95), "tokens": sum(tok)}
     # the forward kernels' time per set (its algorithmic bytes differ by layout)
-    # (a set that no timed step reached, where steps < sets, has no time: None)
-    per_set_kern = [float(np.mean(kern[j::n])) if j < steps else None for j in range(n)]
-    out["kernel_ms_per_set"] = per_set_kern
+    out["kernel_ms_per_set"] = per_set_means(kern, n)
     out["kernel_ms"] = float(np.mean(kern))
     if not graphs:
         return out, sets, step

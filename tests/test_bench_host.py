@@ -101,3 +101,12 @@ def test_committed_traffic_records_are_current():
     assert not stale, f"traffic records taken on other kernel sources: {stale}"
     wanted = {synth.standard_workloads()[3].name, *bench.PER_CONFIG}
     assert wanted <= set(names), wanted - set(names)
+
+
+def test_per_set_means_rotation_and_unreached_sets():
+    """Step i runs input set i mod n: each set's mean is over its own steps, and a set that no
+    timed step reached (fewer steps than sets, the small workloads' long rotations) has None,
+    so the roofline averages only over sets that were timed."""
+    assert bench.per_set_means([1.0, 2.0, 3.0, 5.0], 2) == [2.0, 3.5]
+    assert bench.per_set_means([1.0, 2.0], 4) == [1.0, 2.0, None, None]
+    assert bench.per_set_means([], 1) == [None]
